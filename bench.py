@@ -1,0 +1,460 @@
+"""Throughput of decode attention over a LeanK-pruned KV cache on one GB300.
+
+One step = one pass of the whole hot path for one decode token of the
+workload: for each layer, lk_append (new K/V into the window ring, eviction
+into K_prun) then lk_decode_attn (split-K decode + in-launch combine).
+Default workload: the Llama-3.1-8B-shaped layer (32 q / 8 kv heads, d 128,
+batch 1, context 32768, sink 16, window 1024, 70 % channel pruning rounded
+down to multiples of 32, K with 4 channel pairs x8).
+
+Timing rules: W untimed warm-up steps; exactly K timed steps bracketed by a
+barrier + synchronize; CUDA events on the launching stream; max over ranks.
+Inputs are larger than L2: the steps rotate over C copies of the cache whose
+resident bytes together exceed 4x L2, and C also bounds the context growth
+of the appends.  The step loop is captured in CUDA graphs (programmatic
+dependent launch between append and decode).
+
+Printed: one JSON line (rank 0).  `value` = decode-attention calls/s of all
+ranks; `roofline` = the decode kernel's algorithmic bytes / its event-timed
+launch duration against the HBM peak; `e2e` = the same metric through
+lk_step_host from pinned host buffers (copies inside the timed region);
+`cpu_baseline` = the fp64 oracle on a bounded sample on the host cores.
+
+--impl reference times the oracle (the only reference this method has) on
+the host cores, on the same workload, one (sequence, kv head) per step.
+"""
+from __future__ import annotations
+
+import os
+
+# the oracle's numpy BLAS runs on exactly one thread (reported as `cores`)
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "decode-attn calls/s & effective HBM GB/s (% of GB300 peak) on pruned KV"
+UNIT = "calls/s"
+FALLBACK_HBM_GBS = 6800.0
+MAX_CONTEXT_GROWTH = 0.01           # appends may lengthen the context by at most 1 %
+COPY_BUDGET_BYTES = 48 << 30        # device memory the rotating copies may take
+
+# DRAM bytes (read + write) per decode launch from an ncu capture, keyed by the
+# sha256 of the decode kernel source it was taken on (null when it changed).
+NCU_TRAFFIC = {}
+
+
+def _rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+                if key in d:
+                    return float(d[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _decode_source_hash():
+    p = os.path.join(ROOT, "decode_attention_pruned_gb300", "csrc", "lk_decode.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+                self.lines = [l for l in out.splitlines() if l.strip()]
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def max_over_ranks(seconds: float, dist, device) -> float:
+    """The slowest rank's time (the job's time for weak-scaled replicas)."""
+    import torch
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(steps: int, layers: int, world: int, seconds: float) -> float:
+    """Calls/s of the whole job: every rank ran `steps` steps of `layers` calls."""
+    return steps * layers * world / seconds
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank, local_rank, world):
+    import torch
+    from decode_attention_pruned_gb300 import binding as lkb
+    from decode_attention_pruned_gb300 import synth as S
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lkb.load()
+    w = S.WORKLOAD_BY_NAME[args.workload]
+    N = w.context
+    pol = S.make_policies(w)
+    masks = S.make_masks(w, pol)
+    spec = S.make_special_table(w)
+    plan = lkb.Plan.for_workload(w, masks, pol, spec if len(spec) else None)
+    L, B = w.num_layers, w.batch
+    W, K = args.warmup, args.steps
+    e2e_steps = min(K, args.e2e_steps)
+    kt_steps = min(K, args.kernel_steps)
+    appends = W + K + 2 * e2e_steps + 8
+
+    # one copy first, to size the rest
+    prop = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(prop, "L2_cache_size", 0) or 126 << 20)
+    max_growth = max(1, int(MAX_CONTEXT_GROWTH * N))
+    cap_probe = N + 64
+    copy_bytes = plan.cache_bytes(B, cap_probe) + plan.workspace_bytes(B)
+
+    # dense history of every layer, generated once on the device
+    hist = {l: S.make_kv(w, l, N, device=dev) for l in range(L)} if L <= 2 else None
+    ids_all = torch.from_numpy(S.make_token_ids(w, N)).to(dev) if len(spec) else None
+
+    first = lkb.Cache(plan, B, cap_probe, device=dev)
+    for l in range(L):
+        k, v = hist[l] if hist else S.make_kv(w, l, N, device=dev)
+        first.prefill(l, k[:, : N - 1].contiguous(), v[:, : N - 1].contiguous(),
+                      None if ids_all is None else ids_all[:, : N - 1].contiguous())
+        first.append(l, k[:, N - 1].contiguous(), v[:, N - 1].contiguous(),
+                     None if ids_all is None else ids_all[:, N - 1].contiguous())
+    torch.cuda.synchronize()
+    resident = [first.resident_bytes(l) for l in range(L)]
+    resident_step = sum(resident)
+    copies = max(1, math.ceil(4 * l2 / max(1, resident_step)), math.ceil(appends / max_growth))
+    copies = int(min(copies, max(1, COPY_BUDGET_BYTES // copy_bytes)))
+    growth = math.ceil(appends / copies) + 2
+    capacity = N + growth
+    del first
+    torch.cuda.empty_cache()
+
+    caches = []
+    for c in range(copies):
+        cache = lkb.Cache(plan, B, capacity, device=dev)
+        for l in range(L):
+            k, v = hist[l] if hist else S.make_kv(w, l, N, device=dev)
+            cache.prefill(l, k[:, : N - 1].contiguous(), v[:, : N - 1].contiguous(),
+                          None if ids_all is None else ids_all[:, : N - 1].contiguous())
+        caches.append(cache)
+    hist = None
+    torch.cuda.synchronize()
+
+    # per-step inputs (a bank cycled through), resident before timing
+    bank = 16
+    gq = [[S.make_q(w, l, N - 1, device=dev, step=s) for l in range(L)] for s in range(bank)]
+    gk, gv = [], []
+    for s in range(bank):
+        kk, vv = S.make_kv(w.scaled(seed=w.seed + 7919 * (s + 1)), 0, 1, device=dev)
+        gk.append(kk[:, 0].contiguous())
+        gv.append(vv[:, 0].contiguous())
+    gid = [torch.zeros(B, dtype=torch.int32, device=dev) + (s * 37) % max(1, w.vocab) for s in range(bank)] \
+        if len(spec) else [None] * bank
+    outs = [torch.empty((B, w.num_q_heads, 128), dtype=torch.float32, device=dev) for _ in range(copies)]
+
+    stream = torch.cuda.Stream(device=dev)
+
+    def enqueue_step(i):
+        c = caches[i % copies]
+        s = i % bank
+        for l in range(L):
+            c.append(l, gk[s], gv[s], gid[s], stream=stream)
+            c.decode(l, gq[s][l], outs[i % copies], stream=stream)
+
+    # graphs of whole rotations (copies steps) plus one of the remainder
+    def capture(n_steps, start):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(n_steps):
+                enqueue_step(start + j)
+        return g
+
+    # warm-up: eager steps (also the first use of every cache copy), then graphs
+    with torch.cuda.stream(stream):
+        for i in range(min(W, copies)):
+            enqueue_step(i)
+    stream.synchronize()
+    for c in caches:
+        c.check(stream)
+    done = min(W, copies)
+    full_graph = capture(copies, 0) if K >= copies or W > copies else None
+    rem = K % copies
+    rem_graph = capture(rem, 0) if rem else None
+    # graph capture records the steps; the host lengths advanced by the capture
+    # are not device lengths -- re-sync by reading them back is unnecessary as
+    # the device-side counts drive the kernels.
+    warm_left = W - done
+    with torch.cuda.stream(stream):
+        while warm_left >= copies and full_graph is not None:
+            full_graph.replay()
+            warm_left -= copies
+        for i in range(warm_left):
+            enqueue_step(done + i)
+    stream.synchronize()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clocks:
+        ev0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(K // copies):
+                full_graph.replay()
+            if rem_graph is not None:
+                rem_graph.replay()
+        ev1.record(stream)
+        ev1.synchronize()
+    torch.cuda.synchronize()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if dist is not None:
+        elapsed = max_over_ranks(elapsed, dist, dev)
+    for c in caches:
+        c.check(stream)
+
+    # decode kernel: event pairs around individual launches (no append between)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(kt_steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(kt_steps)]
+    with torch.cuda.stream(stream):
+        for i in range(kt_steps):
+            c = caches[i % copies]
+            starts[i].record(stream)
+            c.decode(0, gq[i % bank][0], outs[i % copies], stream=stream)
+            ends[i].record(stream)
+    stream.synchronize()
+    kdur = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+
+    # end to end through lk_step_host: pinned host inputs, copies in the region
+    pin = lambda t: t.detach().cpu().contiguous().pin_memory()
+    hq = [pin(gq[s][0]) for s in range(bank)]
+    hk = [pin(gk[s]) for s in range(bank)]
+    hv = [pin(gv[s]) for s in range(bank)]
+    hids = [pin(gid[s]) if gid[s] is not None else None for s in range(bank)]
+    ho = torch.empty((B, w.num_q_heads, 128), dtype=torch.float32).pin_memory()
+    e2e_value = None
+    h2d = (hq[0].numel() * 2 + hk[0].numel() * 2 + hv[0].numel() * 2 + (B * 4 if hids[0] is not None else 0)) * L
+    d2h = ho.numel() * 4 * L
+    if L == 1:
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            s = i % bank
+            caches[i % copies].step_host(0, hq[s], hk[s], hv[s], hids[s], ho, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_elapsed = e0.elapsed_time(e1) / 1e3
+        e2e_value = e2e_steps * world / e2e_elapsed if e2e_steps else None
+        for c in caches:
+            c.check(stream)
+
+    # algorithmic bytes of one decode launch (layer 0 of copy 0 at its length)
+    alg_bytes = resident[0] + B * w.num_q_heads * 128 * (2 + 4)
+    peak, peak_kind = _peaks()
+    achieved = alg_bytes / kdur / 1e9
+    traffic = NCU_TRAFFIC.get(_decode_source_hash())
+
+    line = {
+        "metric": METRIC,
+        "value": job_throughput(K, L, world, elapsed),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": elapsed / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; random K/V/q, seeded LeanK masks)",
+        "config": {
+            "workload": w.name, "layers": L, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+            "head_dim": 128, "context": N, "context_growth_max": growth, "sink": w.sink, "local": w.local,
+            "prune_pct": w.prune_pct, "mask_budget": w.budget,
+            "resident_bytes_per_call": resident[0], "effective_GBps": resident_step * K * world / elapsed / 1e9,
+            "cache_copies": copies, "l2_policy": "inputs larger than L2 (rotating cache copies)",
+            "cuda_graph": True, "pdl": True, "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "peak_source": peak_kind, "kernel": "decode_kernel",
+            "kernel_ms": kdur * 1e3, "alg_bytes_per_launch": alg_bytes, "timed_launches": kt_steps,
+        },
+        "e2e": None if e2e_value is None else {
+            "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": e2e_steps},
+        "gpu_launches": 2 * L * K,
+    }
+    cs = clocks.summary()
+    if cs is not None:
+        line["clocks"] = cs
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the oracle (CPU)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w_name, budget_s, max_units=None):
+    """Time the fp64 oracle on (sequence, kv head) units of the workload's
+    decode call until `budget_s` or `max_units`; returns (calls/s, units, s)."""
+    import torch
+    from decode_attention_pruned_gb300 import synth as S
+    from oracle import attention as OA
+    w = S.WORKLOAD_BY_NAME[w_name]
+    N = w.context
+    pol = S.make_policies(w)
+    masks = S.make_masks(w, pol)
+    spec = S.make_special_table(w)
+    k, v = S.make_kv(w.scaled(batch=1), 0, N)           # one sequence of layer 0
+    q = S.make_q(w.scaled(batch=1), 0, N - 1)
+    K = k[0].float().numpy()
+    V = v[0].float().numpy()
+    Q = q[0].float().numpy()
+    flags = spec[S.make_token_ids(w.scaled(batch=1), N)[0]].astype(bool) if len(spec) else None
+    G = w.group
+    units, t0 = 0, time.perf_counter()
+    while True:
+        h = units % w.num_kv_heads
+        kept = np.nonzero(masks[0, h])[0]
+        OA.decode_head(Q[h * G:(h + 1) * G], K[:, h], V[:, h], int(pol[0, h]), kept, N, w.sink, w.local,
+                       w.local_only_window, flags)
+        units += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_units is not None and units >= max_units):
+            break
+    units_per_call = w.batch * w.num_kv_heads * w.num_layers
+    return units / el / units_per_call, units, el
+
+
+def run_reference(args):
+    W, K = args.warmup, args.steps
+    oracle_sample(args.workload, 0.0, max_units=max(1, min(W, 3)))
+    value, units, el = oracle_sample(args.workload, args.reference_budget, max_units=K)
+    sample = (f"fp64 numpy oracle, one (sequence, kv head) of layer 0 per step; {units} steps in {el:.1f} s "
+              f"(capped at {args.reference_budget:.0f} s); calls/s = steps/s / (batch x kv heads x layers)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": units,
+        "warmup": W, "ms_per_step": el / units * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama31_8b_layer")
+    ap.add_argument("--e2e-steps", type=int, default=4000)
+    ap.add_argument("--kernel-steps", type=int, default=2000)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--reference-budget", type=float, default=60.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local_rank, world = _rank_env()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_gpu(args, rank, local_rank, world)
+    if rank == 0:
+        value, units, el = oracle_sample(args.workload, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 numpy oracle on {units} (sequence, kv head) units of layer 0 in {el:.1f} s, "
+                      f"scaled to calls/s"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,268 @@
+"""Thin Python binding of the C ABI in include/leank.h (ctypes).
+
+Argument marshalling only: torch tensors are passed as raw device pointers
+and the current CUDA stream as a handle.  Every step of prefill, append and
+decode runs in the library's CUDA kernels; there is no CPU path, and a
+missing library raises instead of falling back.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libleank.so")
+
+LK_OK, LK_ERR_ARG, LK_ERR_ALIGN, LK_ERR_CAPACITY, LK_ERR_STATE, LK_ERR_CUDA, LK_ERR_TIMEOUT, \
+    LK_ERR_UNSUPPORTED = range(8)
+STATUS_NAMES = ["LK_OK", "LK_ERR_ARG", "LK_ERR_ALIGN", "LK_ERR_CAPACITY", "LK_ERR_STATE", "LK_ERR_CUDA",
+                "LK_ERR_TIMEOUT", "LK_ERR_UNSUPPORTED"]
+POLICY_FULL, POLICY_LOCAL, POLICY_SPECIAL = 0, 1, 2
+
+# Every symbol include/leank.h declares, with (restype, argtypes).
+_vp, _i32, _sz, _u64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_uint64
+
+
+class PlanDesc(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_layers", "num_q_heads", "num_kv_heads", "head_dim", "sink", "local",
+        "local_only_window", "vocab", "special_capacity")]
+
+
+class RegionInfo(ctypes.Structure):
+    _fields_ = [("policy", ctypes.c_int32), ("n_kept", ctypes.c_int32), ("rows_a", ctypes.c_int32),
+                ("rows_b", ctypes.c_int32), ("k_a_offset", ctypes.c_uint64), ("v_a_offset", ctypes.c_uint64),
+                ("k_b_offset", ctypes.c_uint64), ("v_b_offset", ctypes.c_uint64)]
+
+
+SIGNATURES = {
+    "lk_build_plan": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp, ctypes.POINTER(_vp)]),
+    "lk_plan_destroy": (None, [_vp]),
+    "lk_plan_head": (ctypes.c_int, [_vp, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp]),
+    "lk_cache_bytes": (ctypes.c_int, [_vp, _i32, _i32, ctypes.POINTER(_sz)]),
+    "lk_workspace_bytes": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_sz)]),
+    "lk_cache_init": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, _vp, ctypes.POINTER(_vp)]),
+    "lk_cache_destroy": (None, [_vp]),
+    "lk_workspace_init": (ctypes.c_int, [_vp, _vp, _sz, _vp]),
+    "lk_prefill": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
+    "lk_append": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp]),
+    "lk_decode_attn": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "lk_step_host": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "lk_cache_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i32)]),
+    "lk_cache_region": (ctypes.c_int, [_vp, _i32, _i32, _i32, ctypes.POINTER(RegionInfo)]),
+    "lk_resident_bytes": (ctypes.c_int, [_vp, _i32, _vp, ctypes.POINTER(_u64)]),
+    "lk_set_decode_ctas": (ctypes.c_int, [_vp, _i32]),
+    "lk_check": (ctypes.c_int, [_vp, _vp]),
+    "lk_last_error": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+class LeankError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{name}: {message}")
+
+
+def load(build_if_missing: bool = False):
+    """Load libleank.so (raises if it is missing and not built here)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        if not build_if_missing:
+            raise RuntimeError(f"libleank.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        from . import build as _build
+        _build.build()
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != LK_OK:
+        raise LeankError(status, _lib.lk_last_error().decode())
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, dtype, shape, what, device_kind="cuda"):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{what}: expected contiguous {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+    if t.device.type != device_kind:
+        raise ValueError(f"{what} must be on {device_kind}")
+
+
+class Plan:
+    """lk_build_plan: masks [L, Hkv, 128] uint8, policies [L, Hkv] int32."""
+
+    def __init__(self, num_layers, num_q_heads, num_kv_heads, sink, local, masks, policies=None,
+                 local_only_window=0, is_special=None, special_capacity=0, head_dim=128):
+        lib = load()
+        masks = np.ascontiguousarray(masks, dtype=np.uint8)
+        if policies is None:
+            policies = np.zeros((num_layers, num_kv_heads), dtype=np.int32)
+        policies = np.ascontiguousarray(policies, dtype=np.int32)
+        spec = None if is_special is None else np.ascontiguousarray(is_special, dtype=np.uint8)
+        self.desc = PlanDesc(num_layers, num_q_heads, num_kv_heads, head_dim, sink, local,
+                             local_only_window, 0 if spec is None else len(spec), special_capacity)
+        if masks.shape != (num_layers, num_kv_heads, head_dim):
+            raise ValueError(f"masks shape {masks.shape}")
+        if policies.shape != (num_layers, num_kv_heads):
+            raise ValueError(f"policies shape {policies.shape}")
+        h = ctypes.c_void_p()
+        _check(lib.lk_build_plan(ctypes.byref(self.desc), masks.ctypes.data, policies.ctypes.data,
+                                 None if spec is None else spec.ctypes.data, ctypes.byref(h)))
+        self._h = h
+        self.num_layers, self.num_q_heads, self.num_kv_heads = num_layers, num_q_heads, num_kv_heads
+        self.group = num_q_heads // num_kv_heads
+        self.sink, self.local, self.local_only_window = sink, local, local_only_window
+
+    @classmethod
+    def for_workload(cls, w, masks, policies, is_special=None, special_capacity=0):
+        return cls(w.num_layers, w.num_q_heads, w.num_kv_heads, w.sink, w.local, masks, policies,
+                   local_only_window=w.local_only_window,
+                   is_special=is_special if (is_special is not None and len(is_special)) else None,
+                   special_capacity=special_capacity)
+
+    def head(self, layer, kv_head):
+        pol, nk = ctypes.c_int32(), ctypes.c_int32()
+        kept = np.zeros(128, dtype=np.int16)
+        _check(_lib.lk_plan_head(self._h, layer, kv_head, ctypes.byref(pol), ctypes.byref(nk), kept.ctypes.data))
+        return pol.value, nk.value, kept[: nk.value].copy()
+
+    def cache_bytes(self, batch, capacity):
+        n = ctypes.c_size_t()
+        _check(_lib.lk_cache_bytes(self._h, batch, capacity, ctypes.byref(n)))
+        return n.value
+
+    def workspace_bytes(self, batch):
+        n = ctypes.c_size_t()
+        _check(_lib.lk_workspace_bytes(self._h, batch, ctypes.byref(n)))
+        return n.value
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.lk_plan_destroy(self._h)
+            self._h = None
+
+
+class Cache:
+    """A cache bound to a torch-allocated device buffer, plus its workspace."""
+
+    def __init__(self, plan: Plan, batch: int, capacity: int, device=None, stream=None):
+        import torch
+        self.plan, self.batch, self.capacity = plan, batch, capacity
+        dev = torch.device(device if device is not None else "cuda")
+        self.device = dev
+        nbytes = plan.cache_bytes(batch, capacity)
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.workspace = torch.empty(plan.workspace_bytes(batch), dtype=torch.uint8, device=dev)
+        h = ctypes.c_void_p()
+        s = _stream(stream)
+        _check(_lib.lk_cache_init(plan._h, self.buffer.data_ptr(), nbytes, batch, capacity, s, ctypes.byref(h)))
+        self._h = h
+        _check(_lib.lk_workspace_init(self._h, self.workspace.data_ptr(), self.workspace.numel(), s))
+
+    # -- the hot path
+    def prefill(self, layer, k, v, ids=None, stream=None):
+        import torch
+        B, H = self.batch, self.plan.num_kv_heads
+        n = k.shape[1]
+        _need(k, torch.bfloat16, (B, n, H, 128), "k")
+        _need(v, torch.bfloat16, (B, n, H, 128), "v")
+        if ids is not None:
+            _need(ids, torch.int32, (B, n), "ids")
+        _check(_lib.lk_prefill(self._h, layer, k.data_ptr(), v.data_ptr(), _ptr(ids), n, _stream(stream)))
+
+    def append(self, layer, k, v, ids=None, stream=None):
+        import torch
+        B, H = self.batch, self.plan.num_kv_heads
+        _need(k, torch.bfloat16, (B, H, 128), "k")
+        _need(v, torch.bfloat16, (B, H, 128), "v")
+        if ids is not None:
+            _need(ids, torch.int32, (B,), "ids")
+        _check(_lib.lk_append(self._h, layer, k.data_ptr(), v.data_ptr(), _ptr(ids), _stream(stream)))
+
+    def decode(self, layer, q, o=None, stream=None):
+        import torch
+        B, Hq = self.batch, self.plan.num_q_heads
+        _need(q, torch.bfloat16, (B, Hq, 128), "q")
+        if o is None:
+            o = torch.empty((B, Hq, 128), dtype=torch.float32, device=q.device)
+        _need(o, torch.float32, (B, Hq, 128), "o")
+        _check(_lib.lk_decode_attn(self._h, layer, q.data_ptr(), o.data_ptr(), self.workspace.data_ptr(),
+                                   self.workspace.numel(), _stream(stream)))
+        return o
+
+    def step_host(self, layer, q, k, v, ids, o, stream=None):
+        """q/k/v/ids/o are pinned host tensors; o is valid after the stream syncs."""
+        import torch
+        B, Hq, H = self.batch, self.plan.num_q_heads, self.plan.num_kv_heads
+        _need(q, torch.bfloat16, (B, Hq, 128), "q", "cpu")
+        _need(k, torch.bfloat16, (B, H, 128), "k", "cpu")
+        _need(v, torch.bfloat16, (B, H, 128), "v", "cpu")
+        _need(o, torch.float32, (B, Hq, 128), "o", "cpu")
+        if ids is not None:
+            _need(ids, torch.int32, (B,), "ids", "cpu")
+        _check(_lib.lk_step_host(self._h, layer, q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(ids),
+                                 o.data_ptr(), self.workspace.data_ptr(), self.workspace.numel(),
+                                 _stream(stream)))
+
+    # -- queries
+    def length(self, layer):
+        n = ctypes.c_int32()
+        _check(_lib.lk_cache_length(self._h, layer, ctypes.byref(n)))
+        return n.value
+
+    def region(self, layer, b, kv_head) -> RegionInfo:
+        r = RegionInfo()
+        _check(_lib.lk_cache_region(self._h, layer, b, kv_head, ctypes.byref(r)))
+        return r
+
+    def resident_bytes(self, layer, stream=None):
+        n = ctypes.c_uint64()
+        _check(_lib.lk_resident_bytes(self._h, layer, _stream(stream), ctypes.byref(n)))
+        return n.value
+
+    def set_decode_ctas(self, ctas):
+        _check(_lib.lk_set_decode_ctas(self._h, ctas))
+
+    def check(self, stream=None):
+        _check(_lib.lk_check(self._h, _stream(stream)))
+
+    def rows(self, offset, nrows, width):
+        """View of `nrows` bf16 rows of `width` channels at a byte offset of the buffer."""
+        import torch
+        nb = nrows * width * 2
+        return self.buffer[offset: offset + nb].view(torch.bfloat16).view(nrows, width)
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.lk_cache_destroy(self._h)
+            self._h = None

@@ -1,0 +1,594 @@
+// Host side of the C ABI declared in include/leank.h: validation, the plan
+// (head grouping and kept-channel lists, LeanK article section 3.1), the
+// cache layout inside the caller's buffer, TMA tensor maps and launches.
+// No CPU compute path exists: every step of decode/append/prefill runs in the
+// kernels of lk_decode.cu and lk_kv.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/leank.h"
+#include "lk_internal.h"
+#include "lk_kernels.h"
+
+using namespace lk;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+lk_status fail(lk_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+lk_status cuda_fail(cudaError_t err, const char* what) {
+  return fail(LK_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(err), cudaGetErrorString(err));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s bound on device waits
+constexpr int64_t kMaxPoolRows = (1ll << 31) - 2 * kTmaBoxRows;
+
+}  // namespace
+
+struct lk_plan_s {
+  lk_plan_desc d;
+  std::vector<int32_t> policy;      // [L][Hkv]
+  std::vector<int32_t> n_kept;      // [L][Hkv]
+  std::vector<int16_t> kept;        // [L][Hkv][128] kept channels ascending, then the pruned ones
+  std::vector<uint8_t> is_special;  // [vocab]
+  std::vector<uint8_t> layer_special;
+};
+
+namespace {
+
+struct Layout {
+  size_t off_len, off_cnt, off_heads, off_kept, off_spec;
+  size_t off_pool[kNumPools];
+  int64_t pool_rows[kNumPools];
+  size_t total;
+  int32_t spec_cap;
+  std::vector<HeadDesc> heads;
+};
+
+lk_status compute_layout(const lk_plan_s& p, int B, int cap, Layout* lay) {
+  const lk_plan_desc& d = p.d;
+  const int L = d.num_layers, H = d.num_kv_heads;
+  size_t off = align_up(sizeof(DevHeader), 1024);
+  lay->off_len = off;
+  off = align_up(off + (size_t)L * B * 4, 1024);
+  lay->off_cnt = off;
+  off = align_up(off + (size_t)L * B * 4, 1024);
+  lay->off_heads = off;
+  off = align_up(off + (size_t)L * H * sizeof(HeadDesc), 1024);
+  lay->off_kept = off;
+  off = align_up(off + (size_t)L * H * kHeadDim * 2, 1024);
+  lay->off_spec = off;
+  off = align_up(off + (size_t)std::max(d.vocab, 1), 1024);
+
+  lay->spec_cap = d.special_capacity > 0 ? std::min(d.special_capacity, cap) : cap;
+  lay->heads.assign((size_t)L * H, HeadDesc{});
+  int64_t rows[kNumPools] = {0, 0, 0, 0, 0};
+  int64_t ra = 0;
+  for (int i = 0; i < L * H; ++i) {
+    HeadDesc& hd = lay->heads[i];
+    hd.policy = p.policy[i];
+    hd.n_kept = hd.policy == kFull ? p.n_kept[i] : 0;
+    hd.cap_a = hd.policy == kFull    ? std::min(cap, d.sink + d.local)
+               : hd.policy == kLocal ? std::min(cap, d.local_only_window)
+                                     : lay->spec_cap;
+    hd.row_a = ra;
+    ra += (int64_t)B * hd.cap_a;
+    hd.pool_kb = kPoolK128;
+  }
+  rows[kPoolK128] = ra;
+  rows[kPoolV] = ra;
+  for (int i = 0; i < L * H; ++i) {
+    HeadDesc& hd = lay->heads[i];
+    if (hd.policy == kFull && hd.n_kept > 0) {
+      hd.cap_b = std::max(0, cap - d.sink - d.local);
+      hd.pool_kb = pool_for_width(hd.n_kept);
+      hd.krow_b = rows[hd.pool_kb];
+      rows[hd.pool_kb] += (int64_t)B * hd.cap_b;
+      hd.vrow_b = rows[kPoolV];
+      rows[kPoolV] += (int64_t)B * hd.cap_b;
+    }
+  }
+  for (int pl = 0; pl < kNumPools; ++pl) {
+    const int64_t r = std::max<int64_t>(rows[pl], kTmaBoxRows);
+    if (r > kMaxPoolRows)
+      return fail(LK_ERR_CAPACITY, "pool %d needs %lld rows; at most %lld fit TMA coordinates", pl,
+                  (long long)r, (long long)kMaxPoolRows);
+    lay->pool_rows[pl] = r;
+    lay->off_pool[pl] = off;
+    off = align_up(off + (size_t)r * pool_width(pl) * 2, 1024);
+  }
+  lay->total = off;
+  return LK_OK;
+}
+
+struct WsLayout {
+  size_t off_counters, off_ml, off_part, off_q, off_k, off_v, off_ids, off_o, total;
+};
+
+WsLayout ws_layout(const lk_plan_desc& d, int B) {
+  WsLayout w;
+  const size_t E = (size_t)B * d.num_kv_heads;
+  const size_t G = (size_t)(d.num_q_heads / d.num_kv_heads);
+  const size_t slots = (size_t)kMaxCtas + E;
+  size_t off = 0;
+  w.off_counters = off;
+  off = align_up(off + E * 4, 256);
+  w.off_ml = off;
+  off = align_up(off + slots * G * 8, 256);
+  w.off_part = off;
+  off = align_up(off + slots * G * kHeadDim * 4, 256);
+  w.off_q = off;
+  off = align_up(off + (size_t)B * d.num_q_heads * kHeadDim * 2, 256);
+  w.off_k = off;
+  off = align_up(off + (size_t)B * d.num_kv_heads * kHeadDim * 2, 256);
+  w.off_v = off;
+  off = align_up(off + (size_t)B * d.num_kv_heads * kHeadDim * 2, 256);
+  w.off_ids = off;
+  off = align_up(off + (size_t)B * 4, 256);
+  w.off_o = off;
+  off = align_up(off + (size_t)B * d.num_q_heads * kHeadDim * 4, 256);
+  w.total = off;
+  return w;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+struct lk_cache_s {
+  lk_plan_s plan;
+  Layout lay;
+  CacheView cv;
+  uint8_t* buf = nullptr;
+  size_t bytes = 0;
+  int B = 0, cap = 0;
+  std::vector<int32_t> host_len;
+  CUtensorMap maps[kNumPools];
+  int device = 0, num_sms = 0, decode_ctas = 0;
+  std::vector<uint8_t> upload;     // host image of the tables (kept alive for the async copy)
+};
+
+extern "C" {
+
+const char* lk_last_error(void) { return g_last_error.c_str(); }
+
+lk_status lk_build_plan(const lk_plan_desc* desc, const uint8_t* masks, const int32_t* policies,
+                        const uint8_t* is_special, lk_plan* out) {
+  if (!desc || !masks || !policies || !out) return fail(LK_ERR_ARG, "lk_build_plan: null argument");
+  *out = nullptr;
+  const lk_plan_desc& d = *desc;
+  if (d.num_layers < 1 || d.num_layers > 4096) return fail(LK_ERR_ARG, "num_layers %d out of [1, 4096]", d.num_layers);
+  if (d.num_kv_heads < 1 || d.num_kv_heads > 1024)
+    return fail(LK_ERR_ARG, "num_kv_heads %d out of [1, 1024]", d.num_kv_heads);
+  if (d.num_q_heads < d.num_kv_heads || d.num_q_heads % d.num_kv_heads != 0)
+    return fail(LK_ERR_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", d.num_q_heads, d.num_kv_heads);
+  if (d.num_q_heads / d.num_kv_heads > kMaxGroup)
+    return fail(LK_ERR_UNSUPPORTED, "query heads per kv head %d > %d", d.num_q_heads / d.num_kv_heads, kMaxGroup);
+  if (d.head_dim != kHeadDim) return fail(LK_ERR_UNSUPPORTED, "head_dim %d != 128", d.head_dim);
+  if (d.sink < 0 || d.local < 0 || d.local_only_window < 0 || d.vocab < 0 || d.special_capacity < 0)
+    return fail(LK_ERR_ARG, "negative sink/local/local_only_window/vocab/special_capacity");
+  auto p = new lk_plan_s();
+  p->d = d;
+  const int LH = d.num_layers * d.num_kv_heads;
+  p->policy.assign(policies, policies + LH);
+  p->n_kept.assign(LH, 0);
+  p->kept.assign((size_t)LH * kHeadDim, 0);
+  p->layer_special.assign(d.num_layers, 0);
+  bool any_full = false, any_local = false, any_special = false;
+  for (int i = 0; i < LH; ++i) {
+    const int pol = p->policy[i];
+    if (pol != kFull && pol != kLocal && pol != kSpecial) {
+      delete p;
+      return fail(LK_ERR_ARG, "policy %d of head %d is not FULL/LOCAL/SPECIAL", pol, i);
+    }
+    any_full |= pol == kFull;
+    any_local |= pol == kLocal;
+    any_special |= pol == kSpecial;
+    if (pol == kSpecial) p->layer_special[i / d.num_kv_heads] = 1;
+    const uint8_t* m = masks + (size_t)i * kHeadDim;
+    int cnt = 0;
+    for (int c = 0; c < kHeadDim; ++c) {
+      if (m[c] > 1) {
+        delete p;
+        return fail(LK_ERR_ARG, "mask of head %d channel %d is %d (must be 0 or 1)", i, c, m[c]);
+      }
+      cnt += m[c];
+    }
+    // kept channels ascending, then the pruned ones (the q permutation)
+    int16_t* perm = &p->kept[(size_t)i * kHeadDim];
+    int w = 0;
+    for (int c = 0; c < kHeadDim; ++c)
+      if (m[c]) perm[w++] = (int16_t)c;
+    for (int c = 0; c < kHeadDim; ++c)
+      if (!m[c]) perm[w++] = (int16_t)c;
+    if (pol == kFull) {
+      if (cnt % 32 != 0) {
+        delete p;
+        return fail(LK_ERR_ARG, "FULL head %d keeps %d channels; must be a multiple of 32", i, cnt);
+      }
+      p->n_kept[i] = cnt;
+    }
+  }
+  if (any_full && d.local < 1) {
+    delete p;
+    return fail(LK_ERR_ARG, "FULL heads need local >= 1");
+  }
+  if (any_local && d.local_only_window < 1) {
+    delete p;
+    return fail(LK_ERR_ARG, "LOCAL heads need local_only_window >= 1");
+  }
+  if (any_special) {
+    if (d.vocab < 1 || !is_special) {
+      delete p;
+      return fail(LK_ERR_ARG, "SPECIAL heads need vocab >= 1 and an is_special table");
+    }
+  }
+  if (is_special && d.vocab > 0) {
+    p->is_special.assign(is_special, is_special + d.vocab);
+    for (auto& f : p->is_special) f = f ? 1 : 0;
+  }
+  *out = p;
+  return LK_OK;
+}
+
+void lk_plan_destroy(lk_plan plan) { delete plan; }
+
+lk_status lk_plan_head(lk_plan plan, int32_t layer, int32_t kv_head, int32_t* policy, int32_t* n_kept,
+                       int16_t* kept_channels) {
+  if (!plan) return fail(LK_ERR_ARG, "lk_plan_head: null plan");
+  if (layer < 0 || layer >= plan->d.num_layers || kv_head < 0 || kv_head >= plan->d.num_kv_heads)
+    return fail(LK_ERR_ARG, "lk_plan_head: (layer %d, kv_head %d) out of range", layer, kv_head);
+  const int i = layer * plan->d.num_kv_heads + kv_head;
+  if (policy) *policy = plan->policy[i];
+  if (n_kept) *n_kept = plan->n_kept[i];
+  if (kept_channels) std::memcpy(kept_channels, &plan->kept[(size_t)i * kHeadDim], kHeadDim * 2);
+  return LK_OK;
+}
+
+lk_status lk_cache_bytes(lk_plan plan, int32_t batch, int32_t capacity_tokens, size_t* bytes) {
+  if (!plan || !bytes) return fail(LK_ERR_ARG, "lk_cache_bytes: null argument");
+  if (batch < 1 || (int64_t)batch * plan->d.num_kv_heads > (1 << 20))
+    return fail(LK_ERR_ARG, "batch %d out of range", batch);
+  if (capacity_tokens < 1 || capacity_tokens > (1 << 30))
+    return fail(LK_ERR_ARG, "capacity_tokens %d out of [1, 2^30]", capacity_tokens);
+  Layout lay;
+  lk_status st = compute_layout(*plan, batch, capacity_tokens, &lay);
+  if (st != LK_OK) return st;
+  *bytes = lay.total;
+  return LK_OK;
+}
+
+lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes) {
+  if (!plan || !bytes) return fail(LK_ERR_ARG, "lk_workspace_bytes: null argument");
+  if (batch < 1 || (int64_t)batch * plan->d.num_kv_heads > (1 << 20))
+    return fail(LK_ERR_ARG, "batch %d out of range", batch);
+  *bytes = ws_layout(plan->d, batch).total;
+  return LK_OK;
+}
+
+lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
+                        void* stream, lk_cache* out) {
+  if (!plan || !dev_buf || !out) return fail(LK_ERR_ARG, "lk_cache_init: null argument");
+  *out = nullptr;
+  if (!aligned(dev_buf, 256)) return fail(LK_ERR_ALIGN, "cache buffer must be 256-byte aligned");
+  size_t need = 0;
+  lk_status st = lk_cache_bytes(plan, batch, capacity_tokens, &need);
+  if (st != LK_OK) return st;
+  if (bytes < need) return fail(LK_ERR_CAPACITY, "cache buffer has %zu bytes; %zu needed", bytes, need);
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(LK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+
+  auto c = new lk_cache_s();
+  c->plan = *plan;
+  compute_layout(c->plan, batch, capacity_tokens, &c->lay);
+  c->buf = static_cast<uint8_t*>(dev_buf);
+  c->bytes = bytes;
+  c->B = batch;
+  c->cap = capacity_tokens;
+  c->host_len.assign(plan->d.num_layers, 0);
+  cudaError_t err = cudaGetDevice(&c->device);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (err != cudaSuccess) {
+    delete c;
+    return cuda_fail(err, "lk_cache_init: device query");
+  }
+  const lk_plan_desc& d = plan->d;
+  const Layout& lay = c->lay;
+  CacheView& cv = c->cv;
+  cv.hdr = reinterpret_cast<DevHeader*>(c->buf);
+  cv.len = reinterpret_cast<int32_t*>(c->buf + lay.off_len);
+  cv.cnt = reinterpret_cast<int32_t*>(c->buf + lay.off_cnt);
+  cv.heads = reinterpret_cast<const HeadDesc*>(c->buf + lay.off_heads);
+  cv.kept = reinterpret_cast<const int16_t*>(c->buf + lay.off_kept);
+  cv.is_special = c->buf + lay.off_spec;
+  for (int pl = 0; pl < kNumPools; ++pl) {
+    cv.pool[pl] = reinterpret_cast<uint16_t*>(c->buf + lay.off_pool[pl]);
+    cv.pool_rows[pl] = lay.pool_rows[pl];
+  }
+  cv.L = d.num_layers;
+  cv.B = batch;
+  cv.Hq = d.num_q_heads;
+  cv.Hkv = d.num_kv_heads;
+  cv.G = d.num_q_heads / d.num_kv_heads;
+  cv.S = d.sink;
+  cv.W = d.local;
+  cv.W_loc = d.local_only_window;
+  cv.vocab = d.vocab;
+  cv.capacity = capacity_tokens;
+  cv.spec_cap = lay.spec_cap;
+
+  // host image of the tables region [off_heads, off_pool[0])
+  const size_t tab_lo = lay.off_heads, tab_hi = lay.off_pool[0];
+  c->upload.assign(tab_hi - tab_lo, 0);
+  std::memcpy(c->upload.data(), lay.heads.data(), lay.heads.size() * sizeof(HeadDesc));
+  std::memcpy(c->upload.data() + (lay.off_kept - tab_lo), c->plan.kept.data(), c->plan.kept.size() * 2);
+  if (!c->plan.is_special.empty())
+    std::memcpy(c->upload.data() + (lay.off_spec - tab_lo), c->plan.is_special.data(), c->plan.is_special.size());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  err = cudaMemsetAsync(c->buf, 0, lay.total, s);
+  if (err == cudaSuccess)
+    err = cudaMemcpyAsync(c->buf + tab_lo, c->upload.data(), c->upload.size(), cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) {
+    delete c;
+    return cuda_fail(err, "lk_cache_init: upload");
+  }
+  for (int pl = 0; pl < kNumPools; ++pl) {
+    const cuuint64_t dims[2] = {(cuuint64_t)pool_width(pl), (cuuint64_t)lay.pool_rows[pl]};
+    const cuuint64_t strides[1] = {(cuuint64_t)pool_width(pl) * 2};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kTmaBoxRows};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult r = encode(&c->maps[pl], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cv.pool[pl], dims, strides, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      delete c;
+      return fail(LK_ERR_CUDA, "cuTensorMapEncodeTiled failed for pool %d (CUresult %d)", pl, (int)r);
+    }
+  }
+  *out = c;
+  return LK_OK;
+}
+
+void lk_cache_destroy(lk_cache cache) { delete cache; }
+
+lk_status lk_workspace_init(lk_cache cache, void* workspace, size_t ws_bytes, void* stream) {
+  if (!cache || !workspace) return fail(LK_ERR_ARG, "lk_workspace_init: null argument");
+  if (!aligned(workspace, 256)) return fail(LK_ERR_ALIGN, "workspace must be 256-byte aligned");
+  const WsLayout w = ws_layout(cache->plan.d, cache->B);
+  if (ws_bytes < w.total) return fail(LK_ERR_CAPACITY, "workspace has %zu bytes; %zu needed", ws_bytes, w.total);
+  cudaError_t err = cudaMemsetAsync(workspace, 0, w.total, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_workspace_init");
+  return LK_OK;
+}
+
+lk_status lk_prefill(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids, int32_t n,
+                     void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_prefill: null cache");
+  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_prefill: layer %d out of range", layer);
+  if (n < 0) return fail(LK_ERR_ARG, "lk_prefill: n = %d < 0", n);
+  if (cache->host_len[layer] != 0)
+    return fail(LK_ERR_STATE, "lk_prefill: layer %d already holds %d tokens", layer, cache->host_len[layer]);
+  if (n > cache->cap) return fail(LK_ERR_CAPACITY, "lk_prefill: n = %d exceeds capacity %d", n, cache->cap);
+  if (n == 0) return LK_OK;
+  if (!k || !v) return fail(LK_ERR_ARG, "lk_prefill: null k or v");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(LK_ERR_ALIGN, "lk_prefill: k and v must be 16-byte aligned");
+  if (ids && !aligned(ids, 4)) return fail(LK_ERR_ALIGN, "lk_prefill: ids must be 4-byte aligned");
+  PrefillArgs a;
+  a.cv = cache->cv;
+  a.layer = layer;
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.ids = ids;
+  a.n = n;
+  cudaError_t err = launch_prefill(a, cache->plan.layer_special[layer] != 0, cache->num_sms,
+                                   static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_prefill launch");
+  cache->host_len[layer] = n;
+  return LK_OK;
+}
+
+lk_status lk_append(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
+                    void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_append: null cache");
+  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_append: layer %d out of range", layer);
+  if (!k || !v) return fail(LK_ERR_ARG, "lk_append: null k or v");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(LK_ERR_ALIGN, "lk_append: k and v must be 16-byte aligned");
+  if (ids && !aligned(ids, 4)) return fail(LK_ERR_ALIGN, "lk_append: ids must be 4-byte aligned");
+  if (cache->host_len[layer] >= cache->cap)
+    return fail(LK_ERR_CAPACITY, "lk_append: layer %d is full (%d tokens)", layer, cache->cap);
+  AppendArgs a;
+  a.cv = cache->cv;
+  a.layer = layer;
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.ids = ids;
+  cudaError_t err = launch_append(a, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_append launch");
+  cache->host_len[layer] += 1;
+  return LK_OK;
+}
+
+lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o, void* workspace,
+                         size_t ws_bytes, void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_decode_attn: null cache");
+  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_decode_attn: layer %d out of range", layer);
+  if (!q || !o || !workspace) return fail(LK_ERR_ARG, "lk_decode_attn: null q, o or workspace");
+  if (!aligned(q, 16) || !aligned(o, 16)) return fail(LK_ERR_ALIGN, "lk_decode_attn: q and o must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(LK_ERR_ALIGN, "lk_decode_attn: workspace must be 256-byte aligned");
+  const WsLayout w = ws_layout(cache->plan.d, cache->B);
+  if (ws_bytes < w.total)
+    return fail(LK_ERR_CAPACITY, "lk_decode_attn: workspace has %zu bytes; %zu needed", ws_bytes, w.total);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  DecodeArgs a;
+  a.cv = cache->cv;
+  a.layer = layer;
+  a.q = static_cast<const uint16_t*>(q);
+  a.o = o;
+  a.part = reinterpret_cast<float*>(ws + w.off_part);
+  a.part_ml = reinterpret_cast<float2*>(ws + w.off_ml);
+  a.counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
+  a.wait_limit_ns = kWaitLimitNs;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
+  int ctas = cache->decode_ctas > 0 ? cache->decode_ctas : cache->num_sms;
+  ctas = std::max(1, std::min(ctas, kMaxCtas));
+  cudaError_t err = launch_decode(cache->maps, a, ctas, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn launch");
+  return LK_OK;
+}
+
+lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const void* k_host, const void* v_host,
+                       const int32_t* ids_host, float* o_host, void* workspace, size_t ws_bytes, void* stream) {
+  if (!cache || !q_host || !k_host || !v_host || !o_host || !workspace)
+    return fail(LK_ERR_ARG, "lk_step_host: null argument");
+  const WsLayout w = ws_layout(cache->plan.d, cache->B);
+  if (ws_bytes < w.total)
+    return fail(LK_ERR_CAPACITY, "lk_step_host: workspace has %zu bytes; %zu needed", ws_bytes, w.total);
+  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_step_host: layer %d out of range", layer);
+  if (cache->host_len[layer] >= cache->cap)
+    return fail(LK_ERR_CAPACITY, "lk_step_host: layer %d is full (%d tokens)", layer, cache->cap);
+  const lk_plan_desc& d = cache->plan.d;
+  const size_t B = cache->B;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t qb = B * d.num_q_heads * kHeadDim * 2, kvb = B * d.num_kv_heads * kHeadDim * 2;
+  cudaError_t err = cudaMemcpyAsync(ws + w.off_q, q_host, qb, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_k, k_host, kvb, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_v, v_host, kvb, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess && ids_host)
+    err = cudaMemcpyAsync(ws + w.off_ids, ids_host, B * 4, cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_step_host: host to device copy");
+  lk_status st = lk_append(cache, layer, ws + w.off_k, ws + w.off_v,
+                           ids_host ? reinterpret_cast<const int32_t*>(ws + w.off_ids) : nullptr, stream);
+  if (st != LK_OK) return st;
+  float* o_dev = reinterpret_cast<float*>(ws + w.off_o);
+  st = lk_decode_attn(cache, layer, ws + w.off_q, o_dev, workspace, ws_bytes, stream);
+  if (st != LK_OK) return st;
+  err = cudaMemcpyAsync(o_host, o_dev, B * d.num_q_heads * kHeadDim * 4, cudaMemcpyDeviceToHost, s);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_step_host: device to host copy");
+  return LK_OK;
+}
+
+lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n) {
+  if (!cache || !n) return fail(LK_ERR_ARG, "lk_cache_length: null argument");
+  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_cache_length: layer %d out of range", layer);
+  *n = cache->host_len[layer];
+  return LK_OK;
+}
+
+lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_head, lk_region_info* out) {
+  if (!cache || !out) return fail(LK_ERR_ARG, "lk_cache_region: null argument");
+  if (layer < 0 || layer >= cache->cv.L || b < 0 || b >= cache->B || kv_head < 0 || kv_head >= cache->cv.Hkv)
+    return fail(LK_ERR_ARG, "lk_cache_region: (layer %d, b %d, kv_head %d) out of range", layer, b, kv_head);
+  const HeadDesc& hd = cache->lay.heads[(size_t)layer * cache->cv.Hkv + kv_head];
+  const Layout& lay = cache->lay;
+  const int64_t ra = hd.row_a + (int64_t)b * hd.cap_a;
+  out->policy = hd.policy;
+  out->n_kept = hd.n_kept;
+  out->rows_a = hd.cap_a;
+  out->rows_b = hd.cap_b;
+  out->k_a_offset = lay.off_pool[kPoolK128] + (uint64_t)ra * kHeadDim * 2;
+  out->v_a_offset = lay.off_pool[kPoolV] + (uint64_t)ra * kHeadDim * 2;
+  if (hd.cap_b > 0) {
+    out->k_b_offset = lay.off_pool[hd.pool_kb] + (uint64_t)(hd.krow_b + (int64_t)b * hd.cap_b) * hd.n_kept * 2;
+    out->v_b_offset = lay.off_pool[kPoolV] + (uint64_t)(hd.vrow_b + (int64_t)b * hd.cap_b) * kHeadDim * 2;
+  } else {
+    out->k_b_offset = out->v_b_offset = 0;
+  }
+  return LK_OK;
+}
+
+lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_t* bytes) {
+  if (!cache || !bytes) return fail(LK_ERR_ARG, "lk_resident_bytes: null argument");
+  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_resident_bytes: layer %d out of range", layer);
+  const int B = cache->B, H = cache->cv.Hkv;
+  std::vector<int32_t> len(B), cnt(B);
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err == cudaSuccess)
+    err = cudaMemcpy(len.data(), cache->cv.len + (size_t)layer * B, B * 4, cudaMemcpyDeviceToHost);
+  if (err == cudaSuccess)
+    err = cudaMemcpy(cnt.data(), cache->cv.cnt + (size_t)layer * B, B * 4, cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_resident_bytes");
+  const int S = cache->cv.S, W = cache->cv.W;
+  uint64_t total = 0;
+  for (int b = 0; b < B; ++b) {
+    const int N = len[b];
+    for (int h = 0; h < H; ++h) {
+      const HeadDesc& hd = cache->lay.heads[(size_t)layer * H + h];
+      uint64_t na = 0, nb = 0;
+      if (hd.policy == kFull) {
+        na = std::min(N, S + W);
+        if (hd.n_kept > 0) nb = std::max(0, N - S - W);
+      } else if (hd.policy == kLocal) {
+        na = std::min(N, cache->cv.W_loc);
+      } else {
+        na = std::min(cnt[b], hd.cap_a);
+      }
+      total += na * (2 * kHeadDim * 2) + nb * (uint64_t)(hd.n_kept + kHeadDim) * 2;
+    }
+  }
+  *bytes = total;
+  return LK_OK;
+}
+
+lk_status lk_set_decode_ctas(lk_cache cache, int32_t ctas) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_set_decode_ctas: null cache");
+  if (ctas < 0 || ctas > kMaxCtas) return fail(LK_ERR_ARG, "lk_set_decode_ctas: %d out of [0, %d]", ctas, kMaxCtas);
+  cache->decode_ctas = ctas;
+  return LK_OK;
+}
+
+lk_status lk_check(lk_cache cache, void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_check: null cache");
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_check: stream");
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return cuda_fail(err, "lk_check: pending error");
+  uint32_t status = 0;
+  err = cudaMemcpy(&status, &cache->cv.hdr->status, 4, cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_check: status read");
+  if (status == 0) return LK_OK;
+  err = cudaMemset(&cache->cv.hdr->status, 0, 4);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_check: status clear");
+  if (status & kStatusTimeout) return fail(LK_ERR_TIMEOUT, "a device-side wait ran out (status 0x%x)", status);
+  if (status & kStatusCapacity)
+    return fail(LK_ERR_CAPACITY, "a layer or a SPECIAL head ran out of rows (status 0x%x)", status);
+  return fail(LK_ERR_ARG, "a token id was outside [0, vocab) (status 0x%x)", status);
+}
+
+}  // extern "C"

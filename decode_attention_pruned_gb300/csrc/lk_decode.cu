@@ -1,0 +1,514 @@
+// Decode attention over the split LeanK cache (one launch per layer).
+//
+// What it computes (LeanK article, framerc.cn, section 3.1 "fused
+// computation"; FastGen article, mhpn.cn, section 3.2 stage 2): for every
+// sequence b and kv head h, the G query heads of h score the full-width rows
+// (sinks + window ring, LOCAL ring or SPECIAL rows) on all 128 channels and the
+// middle rows of K_prun on the head's kept channels (q gathered to the kept
+// channel list), s = q.k / sqrt(128); one online softmax runs over both
+// regions and o = sum p V.
+//
+// How:
+//   * The work line.  Each (b, h) "entry" is a sequence of 64-row tiles:
+//     region-A tiles then region-B tiles.  A tile costs its rows x bytes per
+//     row / 32 (K row + V row), so the line is measured in bytes.  CTA i of P
+//     takes the tiles whose start falls in [iC/P, (i+1)C/P).  P is capped so
+//     every CTA range spans at least one full tile; then the CTAs touching an
+//     entry are exactly first..last and each writes one partial.
+//   * Per CTA: warp 4 issues TMA loads (64-byte swizzled 32-channel boxes) of
+//     a K tile and a V tile per stage into a 6-deep mbarrier ring; warps 0-3
+//     each take 16 rows of the tile.
+//   * Tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate) with tokens on M:
+//     S^T[16 tok x 8] = K[16 x w] Q^T[w x 8] and O^T[128 x 8] += V^T P^T, so
+//     the G <= 8 query heads only pad N.  P goes from the S^T accumulator to
+//     the B operand of P.V with one movmatrix transpose per 8x8 block; it is
+//     split into bf16 hi + lo halves (two mmas) so P.V keeps ~16 bits of P.
+//   * Segment end: warps merge through shared memory; a CTA that owns the
+//     whole entry writes o, otherwise it writes (o, m, l) to its partial slot
+//     and the last of the entry's CTAs (atomic counter) merges them.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "lk_device.cuh"
+#include "lk_internal.h"
+#include "lk_kernels.h"
+
+namespace lk {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kTileRows = 16 * kConsumerWarps;          // 64 tokens per stage
+static_assert(kTileRows == kTmaBoxRows, "tensor-map box rows");
+constexpr int kStages = 6;
+constexpr int kBoxBytes = kTileRows * 64;               // 64 rows x 32 bf16 channels
+constexpr int kStageBytes = 8 * kBoxBytes;              // K (<= 4 boxes) + V (4 boxes)
+constexpr int kUnitsA = 16;                             // cost per full-width row (512 B / 32)
+constexpr int kFirst = 1, kLast = 2;
+
+struct StageDesc {
+  int32_t e;           // entry = b * Hkv + h; < 0 ends the stream
+  int32_t region;      // 0: full width, 1: kept channels
+  int32_t nrows;       // valid rows of the tile
+  int32_t width;       // K channels of the tile
+  int32_t flags;       // kFirst / kLast of this CTA's segment of the entry
+  int32_t first_cta;   // CTAs first..last hold partials of the entry
+  int32_t last_cta;
+  int32_t pad;
+};
+
+struct SmemLayout {
+  static constexpr int kStagesOff = 0;
+  static constexpr int kMergeOOff = kStagesOff + kStages * kStageBytes;
+  static constexpr int kMergeMOff = kMergeOOff + kConsumerWarps * kMaxGroup * kHeadDim * 4;
+  static constexpr int kMergeLOff = kMergeMOff + kConsumerWarps * kMaxGroup * 4;
+  static constexpr int kDescOff = kMergeLOff + kConsumerWarps * kMaxGroup * 4;
+  static constexpr int kBarOff = kDescOff + kStages * (int)sizeof(StageDesc);
+  static constexpr int kScanOff = kBarOff + 2 * kStages * 8;
+  static constexpr int kMiscOff = kScanOff + (kThreads / 32) * 8;
+  static constexpr int kBytes = kMiscOff + 64;
+};
+constexpr int kSmemBytes = SmemLayout::kBytes + 1024;   // + alignment slack
+
+struct Entry {
+  int n_a, n_b, kb;
+};
+
+__device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) {
+  const CacheView& cv = a.cv;
+  const int b = e / cv.Hkv, h = e - b * cv.Hkv;
+  const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
+  const int N = cv.len[a.layer * cv.B + b];
+  Entry r{0, 0, 0};
+  if (hd.policy == kFull) {
+    r.n_a = min(N, cv.S + cv.W);
+    if (hd.n_kept > 0) {
+      r.n_b = max(0, N - cv.S - cv.W);
+      r.kb = hd.n_kept;
+    }
+  } else if (hd.policy == kLocal) {
+    r.n_a = min(N, cv.W_loc);
+  } else {
+    r.n_a = min(cv.cnt[a.layer * cv.B + b], hd.cap_a);
+  }
+  r.n_a = min(r.n_a, hd.cap_a);
+  r.n_b = min(r.n_b, hd.cap_b);
+  return r;
+}
+
+__device__ __forceinline__ uint64_t entry_cost(const Entry& g) {
+  return (uint64_t)kUnitsA * g.n_a + (uint64_t)(g.kb / 16 + 8) * g.n_b;
+}
+
+// Largest CTA index i < P with floor(i*C/P) <= x.
+__device__ __forceinline__ int range_owner(uint64_t x, uint64_t C, int P) {
+  uint64_t i = C ? (x * (uint64_t)P) / C : 0;
+  if (i > (uint64_t)P - 1) i = P - 1;
+  while (i + 1 < (uint64_t)P && ((i + 1) * C) / P <= x) ++i;
+  while (i > 0 && (i * C) / P > x) --i;
+  return (int)i;
+}
+
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ void record_status(const DecodeArgs& a, uint32_t bits) {
+  atomicOr(&a.cv.hdr->status, bits);
+}
+
+__device__ __forceinline__ uint32_t ld_q_pair(const uint16_t* row, int c) {
+  return *reinterpret_cast<const uint32_t*>(row + c);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_k32, const __grid_constant__ CUtensorMap tm_k64,
+                  const __grid_constant__ CUtensorMap tm_k96, const DecodeArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sm = smem_raw + (base - raw);
+  float* merge_o = reinterpret_cast<float*>(sm + SmemLayout::kMergeOOff);
+  float* merge_m = reinterpret_cast<float*>(sm + SmemLayout::kMergeMOff);
+  float* merge_l = reinterpret_cast<float*>(sm + SmemLayout::kMergeLOff);
+  StageDesc* desc = reinterpret_cast<StageDesc*>(sm + SmemLayout::kDescOff);
+  const uint32_t bar_full = base + SmemLayout::kBarOff;
+  const uint32_t bar_empty = bar_full + kStages * 8;
+  uint64_t* scan = reinterpret_cast<uint64_t*>(sm + SmemLayout::kScanOff);
+  volatile int64_t* misc = reinterpret_cast<volatile int64_t*>(sm + SmemLayout::kMiscOff);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const CacheView& cv = a.cv;
+  const int E = cv.B * cv.Hkv;
+  const int G = cv.G;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, kConsumerWarps);
+    }
+    fence_barrier_init();
+    misc[0] = E;       // first entry of this CTA
+    misc[1] = 0;       // its line offset
+    misc[2] = 0;       // last-CTA flag of a segment
+  }
+  if (warp == kConsumerWarps && lane == 0) {
+    tma_prefetch_map(&tm_k128);
+    tma_prefetch_map(&tm_v);
+  }
+  // lengths and special counts are written by the preceding append
+  grid_dependency_wait();
+
+  // ---- the line: per-thread chunks of entries, block exclusive scan
+  const int per = (E + kThreads - 1) / kThreads;
+  const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
+  uint64_t local = 0;
+  for (int e = e_lo; e < e_hi; ++e) local += entry_cost(entry_geometry(a, e));
+  uint64_t incl = local;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) scan[warp] = incl;
+  __syncthreads();
+  uint64_t warp_base = 0, C = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w < warp) warp_base += scan[w];
+    C += scan[w];
+  }
+  const uint64_t excl = warp_base + incl - local;
+  // each CTA range must cover at least one full tile (see header comment)
+  const uint64_t full_tile = (uint64_t)kUnitsA * kTileRows;
+  const int P = (int)max((uint64_t)1, min((uint64_t)gridDim.x, C / full_tile));
+  const int cta = blockIdx.x;
+  const uint64_t start = cta < P ? ((uint64_t)cta * C) / P : C;
+  const uint64_t end = cta < P ? ((uint64_t)(cta + 1) * C) / P : C;
+  if (local > 0 && excl <= start && start < excl + local) {
+    uint64_t acc = excl;
+    for (int e = e_lo; e < e_hi; ++e) {
+      const uint64_t c = entry_cost(entry_geometry(a, e));
+      if (acc + c > start) {
+        misc[0] = e;
+        misc[1] = (int64_t)acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ================================================================ producer
+    if (lane == 0) {
+      const uint64_t policy = l2_policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int e = (int)misc[0];
+      uint64_t off = (uint64_t)misc[1];
+      for (; ok && e < E && off < end; ++e) {
+        const Entry g = entry_geometry(a, e);
+        const uint64_t cost = entry_cost(g);
+        const int ta = (g.n_a + kTileRows - 1) / kTileRows;
+        const int tb = (g.n_b + kTileRows - 1) / kTileRows;
+        const uint64_t cb = (uint64_t)(g.kb / 16 + 8);
+        auto tile_off = [&](int j) -> uint64_t {
+          return j < ta ? off + full_tile * j : off + (uint64_t)kUnitsA * g.n_a + cb * kTileRows * (j - ta);
+        };
+        if (ta + tb > 0) {
+          const int b = e / cv.Hkv, h = e - b * cv.Hkv;
+          const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
+          const int fc = range_owner(tile_off(0), C, P);
+          const int lc = range_owner(tile_off(ta + tb - 1), C, P);
+          const CUtensorMap* kmap_b = hd.pool_kb == kPoolK32   ? &tm_k32
+                                      : hd.pool_kb == kPoolK64 ? &tm_k64
+                                      : hd.pool_kb == kPoolK96 ? &tm_k96
+                                                               : &tm_k128;
+          bool first = true;
+          for (int j = 0; j < ta + tb; ++j) {
+            const uint64_t to = tile_off(j);
+            if (to < start) continue;
+            if (to >= end) break;
+            const bool last = (j + 1 == ta + tb) || (tile_off(j + 1) >= end);
+            if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, a.wait_limit_ns)) {
+              ok = false;
+              break;
+            }
+            const bool in_a = j < ta;
+            const int jr = in_a ? j : j - ta;
+            StageDesc d;
+            d.e = e;
+            d.region = in_a ? 0 : 1;
+            d.nrows = min(kTileRows, (in_a ? g.n_a : g.n_b) - jr * kTileRows);
+            d.width = in_a ? kHeadDim : g.kb;
+            d.flags = (first ? kFirst : 0) | (last ? kLast : 0);
+            d.first_cta = fc;
+            d.last_cta = lc;
+            d.pad = 0;
+            desc[stage] = d;
+            const int64_t krow = in_a ? hd.row_a + (int64_t)b * hd.cap_a + (int64_t)jr * kTileRows
+                                      : hd.krow_b + (int64_t)b * hd.cap_b + (int64_t)jr * kTileRows;
+            const int64_t vrow = in_a ? krow : hd.vrow_b + (int64_t)b * hd.cap_b + (int64_t)jr * kTileRows;
+            const int kboxes = d.width / 32;
+            const uint32_t fb = bar_full + 8 * stage;
+            mbar_arrive_expect_tx(fb, (uint32_t)(kboxes + 4) * kBoxBytes);
+            const uint32_t sbase = base + SmemLayout::kStagesOff + stage * kStageBytes;
+            const CUtensorMap* kmap = in_a ? &tm_k128 : kmap_b;
+            for (int c = 0; c < kboxes; ++c)
+              tma_load_2d(sbase + c * kBoxBytes, kmap, 32 * c, (int32_t)krow, fb, policy);
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d(sbase + (4 + c) * kBoxBytes, &tm_v, 32 * c, (int32_t)vrow, fb, policy);
+            first = false;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        off += cost;
+      }
+      if (ok && mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, a.wait_limit_ns)) {
+        desc[stage].e = -1;
+        mbar_arrive(bar_full + 8 * stage);
+      } else {
+        record_status(a, kStatusTimeout);
+      }
+    }
+    return;
+  }
+
+  // ================================================================ consumers
+  const int ct = tid;                       // 0 .. 127
+  const int gid = lane >> 2, tig = lane & 3;
+  const int r0 = warp * 16;
+  const int rowK = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int chK = lane >> 4;
+  const int rowV = r0 + (lane & 7) + (lane >> 4) * 8;
+  const int chV = (lane >> 3) & 1;
+  const float NEG_INF = -INFINITY;
+
+  // entries with no resident token: o = 0, written by CTA (e mod grid)
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    if (entry_cost(entry_geometry(a, e)) != 0) continue;
+    const int b = e / cv.Hkv, h = e - b * cv.Hkv;
+    float* dst = a.o + ((size_t)b * cv.Hq + (size_t)h * G) * kHeadDim;
+    for (int i = ct; i < G * kHeadDim; i += kConsumerWarps * 32) dst[i] = 0.f;
+  }
+
+  float o[8][4];
+  float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+  uint32_t qa[8][2], qb[8][2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    qa[i][0] = qa[i][1] = qb[i][0] = qb[i][1] = 0u;
+  }
+
+  int stage = 0;
+  uint32_t phase = 0;
+  while (true) {
+    if (!mbar_wait_bounded(bar_full + 8 * stage, phase, a.wait_limit_ns)) {
+      if (lane == 0) record_status(a, kStatusTimeout);
+      break;
+    }
+    const StageDesc d = desc[stage];
+    if (d.e < 0) break;
+    if (d.flags & kFirst) {
+      // (re)load q fragments of the entry: B operand of S^T = K Q^T
+      const int b = d.e / cv.Hkv, h = d.e - b * cv.Hkv;
+      const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
+      const int16_t* kept = cv.kept + ((size_t)a.layer * cv.Hkv + h) * kHeadDim;
+      const bool live = gid < G;
+      const uint16_t* qrow = a.q + ((size_t)b * cv.Hq + (size_t)h * G + (live ? gid : 0)) * kHeadDim;
+      const int kk = hd.policy == kFull ? hd.n_kept : 0;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int c = ks * 16 + 2 * tig;
+        qa[ks][0] = live ? ld_q_pair(qrow, c) : 0u;
+        qa[ks][1] = live ? ld_q_pair(qrow, c + 8) : 0u;
+        if (live && c < kk) {
+          qb[ks][0] = (uint32_t)qrow[kept[c]] | ((uint32_t)qrow[kept[c + 1]] << 16);
+          qb[ks][1] = (uint32_t)qrow[kept[c + 8]] | ((uint32_t)qrow[kept[c + 9]] << 16);
+        } else {
+          qb[ks][0] = qb[ks][1] = 0u;
+        }
+      }
+      m0 = m1 = NEG_INF;
+      l0 = l1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    }
+
+    const int nv = d.nrows - r0;
+    if (nv > 0) {
+      const uint32_t kbase = base + SmemLayout::kStagesOff + stage * kStageBytes;
+      const uint32_t vbase = kbase + 4 * kBoxBytes;
+      const bool in_a = d.region == 0;
+      const int nks = d.width >> 4;
+      float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        if (ks < nks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(swz64(kbase + (ks >> 1) * kBoxBytes, rowK, ((ks & 1) << 1) + chK), a0, a1, a2, a3);
+          const uint32_t b0 = in_a ? qa[ks][0] : qb[ks][0];
+          const uint32_t b1 = in_a ? qa[ks][1] : qb[ks][1];
+          mma_bf16_16816(s, a0, a1, a2, a3, b0, b1);
+        }
+      }
+      const bool v0 = gid < nv, v1 = gid + 8 < nv;
+      const float x0 = v0 ? s[0] * a.scale_log2 : NEG_INF;
+      const float x1 = v0 ? s[1] * a.scale_log2 : NEG_INF;
+      const float x2 = v1 ? s[2] * a.scale_log2 : NEG_INF;
+      const float x3 = v1 ? s[3] * a.scale_log2 : NEG_INF;
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int sh = 4; sh < 32; sh <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      // P as a bf16 pair hi + lo (two mmas below): P.V keeps ~16 mantissa bits
+      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);     // token gid
+      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);     // token gid + 8
+      const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+      const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+      const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+      l0 = l0 * al0 + (p0 + p2);
+      l1 = l1 * al1 + (p1 + p3);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        o[i][0] *= al0;
+        o[i][1] *= al1;
+        o[i][2] *= al0;
+        o[i][3] *= al1;
+      }
+      // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
+      const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+      const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(swz64(vbase + (i >> 1) * kBoxBytes, rowV, ((i & 1) << 1) + chV), a0, a1, a2, a3);
+        mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
+        mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
+
+    if (d.flags & kLast) {
+      // ---- merge the 4 warps' (o, m, l) of this segment
+      float lr0 = l0, lr1 = l1;
+#pragma unroll
+      for (int sh = 4; sh < 32; sh <<= 1) {
+        lr0 += __shfl_xor_sync(0xffffffffu, lr0, sh);
+        lr1 += __shfl_xor_sync(0xffffffffu, lr1, sh);
+      }
+      float* ob = merge_o + warp * kMaxGroup * kHeadDim;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ob[(2 * tig) * kHeadDim + 16 * i + gid] = o[i][0];
+        ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] = o[i][1];
+        ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] = o[i][2];
+        ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] = o[i][3];
+      }
+      if (gid == 0) {
+        merge_m[warp * kMaxGroup + 2 * tig] = m0;
+        merge_m[warp * kMaxGroup + 2 * tig + 1] = m1;
+        merge_l[warp * kMaxGroup + 2 * tig] = lr0;
+        merge_l[warp * kMaxGroup + 2 * tig + 1] = lr1;
+      }
+      consumer_bar();
+      const int b = d.e / cv.Hkv, h = d.e - b * cv.Hkv;
+      float* dst = a.o + ((size_t)b * cv.Hq + (size_t)h * G) * kHeadDim;
+      const bool single = d.first_cta == d.last_cta;
+      const size_t slot = (size_t)blockIdx.x + d.e;
+      for (int idx = ct; idx < G * kHeadDim; idx += kConsumerWarps * 32) {
+        const int g = idx >> 7, dd = idx & 127;
+        float M = NEG_INF;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * kMaxGroup + g]);
+        float acc = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float mw = merge_m[w * kMaxGroup + g];
+          const float f = mw == NEG_INF ? 0.f : exp2f(mw - M);
+          acc += f * merge_o[(w * kMaxGroup + g) * kHeadDim + dd];
+          L += f * merge_l[w * kMaxGroup + g];
+        }
+        if (single) {
+          dst[idx] = L > 0.f ? acc / L : 0.f;
+        } else {
+          a.part[(slot * G + g) * kHeadDim + dd] = acc;
+          if (dd == 0) a.part_ml[slot * G + g] = make_float2(M, L);
+        }
+      }
+      if (!single) {
+        __threadfence();
+        consumer_bar();
+        if (ct == 0) {
+          const int prev = atomicAdd(&a.counters[d.e], 1);
+          misc[2] = (prev == d.last_cta - d.first_cta) ? 1 : 0;
+        }
+        consumer_bar();
+        if (misc[2]) {
+          __threadfence();
+          for (int idx = ct; idx < G * kHeadDim; idx += kConsumerWarps * 32) {
+            const int g = idx >> 7, dd = idx & 127;
+            float M = NEG_INF;
+            for (int c = d.first_cta; c <= d.last_cta; ++c)
+              M = fmaxf(M, __ldcg(&a.part_ml[((size_t)c + d.e) * G + g]).x);
+            float acc = 0.f, L = 0.f;
+            for (int c = d.first_cta; c <= d.last_cta; ++c) {
+              const float2 ml = __ldcg(&a.part_ml[((size_t)c + d.e) * G + g]);
+              const float f = ml.x == NEG_INF ? 0.f : exp2f(ml.x - M);
+              acc += f * __ldcg(&a.part[(((size_t)c + d.e) * G + g) * kHeadDim + dd]);
+              L += f * ml.y;
+            }
+            dst[idx] = L > 0.f ? acc / L : 0.f;
+          }
+          if (ct == 0) a.counters[d.e] = 0;
+        }
+      }
+      consumer_bar();
+    }
+    if (++stage == kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+}  // namespace
+
+size_t decode_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int ctas, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err != cudaSuccess) return err;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel, maps[kPoolK128], maps[kPoolV], maps[kPoolK32],
+                            maps[kPoolK64], maps[kPoolK96], args);
+}
+
+}  // namespace lk

@@ -1,0 +1,83 @@
+// Internal data structures shared by the host API and the device kernels.
+//
+// Device layout of a cache buffer (every block 1024-byte aligned):
+//   DevHeader | len[L][B] | cnt[L][B] | HeadDesc[L][Hkv] | kept[L][Hkv][128] i16
+//   | is_special[vocab] u8 | pool K128 | pool V | pool K32 | pool K64 | pool K96
+//
+// Pools are 2-D row arrays (rows x width bf16) so that one TMA tensor map
+// covers each; heads of equal kept width share a pool (the head grouping of
+// LeanK section 3.1).  Region A (full width: sinks + window ring, LOCAL ring,
+// SPECIAL rows) of every head sits at the same row index in pools K128 and V.
+// Region B (middle tokens of FULL heads with k > 0) has its K rows in the
+// pool of width k and its V rows after all region-A rows of pool V.
+#pragma once
+#include <stdint.h>
+
+namespace lk {
+
+constexpr int kHeadDim = 128;
+constexpr int kMaxGroup = 8;        // query heads per kv head handled by one mma n8 tile
+constexpr int kMaxCtas = 1024;      // decode grid cap (sizes the partial workspace)
+constexpr int kTmaBoxRows = 64;     // token rows per TMA box = decode tile rows
+
+enum Policy : int32_t { kFull = 0, kLocal = 1, kSpecial = 2 };
+enum Pool : int32_t { kPoolK128 = 0, kPoolV = 1, kPoolK32 = 2, kPoolK64 = 3, kPoolK96 = 4, kNumPools = 5 };
+
+// Sticky device status bits (cache header).
+enum StatusBits : uint32_t {
+  kStatusTimeout = 1u << 0,     // a bounded wait ran out
+  kStatusCapacity = 1u << 1,    // a SPECIAL head overflowed its rows or a layer was full
+  kStatusBadId = 1u << 2,       // token id outside [0, vocab)
+};
+
+struct HeadDesc {                 // one (layer, kv head)
+  int32_t policy;
+  int32_t n_kept;                 // k for FULL heads, 0 otherwise
+  int32_t cap_a;                  // region-A rows per sequence
+  int32_t cap_b;                  // region-B rows per sequence (0 if none)
+  int32_t pool_kb;                // pool of region-B K rows
+  int32_t pad;
+  int64_t row_a;                  // first region-A row (sequence 0) in K128 and V
+  int64_t krow_b;                 // first region-B row (sequence 0) in pool_kb
+  int64_t vrow_b;                 // first region-B row (sequence 0) in V
+};
+static_assert(sizeof(HeadDesc) == 48, "HeadDesc layout");
+
+struct DevHeader {
+  uint32_t status;
+  uint32_t pad[63];
+};
+
+// Pointers into one cache buffer, filled at cache init.
+struct CacheView {
+  DevHeader* hdr;
+  int32_t* len;                   // [L][B] tokens per layer and sequence
+  int32_t* cnt;                   // [L][B] special-token rows per layer and sequence
+  const HeadDesc* heads;          // [L][Hkv]
+  const int16_t* kept;            // [L][Hkv][128] kept channels ascending
+  const uint8_t* is_special;      // [vocab]
+  uint16_t* pool[kNumPools];      // bf16 rows
+  int64_t pool_rows[kNumPools];
+  int32_t L, B, Hq, Hkv, G, S, W, W_loc, vocab, capacity;
+  int32_t spec_cap;               // rows of a SPECIAL head per sequence
+};
+
+inline int pool_width(int pool) {
+  switch (pool) {
+    case kPoolK32: return 32;
+    case kPoolK64: return 64;
+    case kPoolK96: return 96;
+    default: return 128;
+  }
+}
+
+inline int pool_for_width(int k) {
+  switch (k) {
+    case 32: return kPoolK32;
+    case 64: return kPoolK64;
+    case 96: return kPoolK96;
+    default: return kPoolK128;
+  }
+}
+
+}  // namespace lk

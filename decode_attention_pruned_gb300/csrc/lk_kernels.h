@@ -1,0 +1,44 @@
+// Kernel argument blocks and launchers (internal).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "lk_internal.h"
+
+namespace lk {
+
+struct DecodeArgs {
+  CacheView cv;
+  int32_t layer;
+  const uint16_t* q;        // bf16 [B][Hq][128]
+  float* o;                 // fp32 [B][Hq][128]
+  float* part;              // fp32 [slots][G][128] split partials (unnormalised o)
+  float2* part_ml;          // [slots][G] (running max in log2 units, sum of p)
+  int32_t* counters;        // [B*Hkv] CTAs done per entry; self-resetting
+  uint64_t wait_limit_ns;   // bound of every mbarrier wait
+  float scale_log2;         // log2(e) / sqrt(128)
+};
+
+struct AppendArgs {
+  CacheView cv;
+  int32_t layer;
+  const uint16_t* k;        // bf16 [B][Hkv][128]
+  const uint16_t* v;
+  const int32_t* ids;       // [B] or null
+};
+
+struct PrefillArgs {
+  CacheView cv;
+  int32_t layer;
+  const uint16_t* k;        // bf16 [B][n][Hkv][128]
+  const uint16_t* v;
+  const int32_t* ids;       // [B][n] or null
+  int32_t n;
+};
+
+size_t decode_smem_bytes();
+cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int ctas, cudaStream_t stream);
+cudaError_t launch_append(const AppendArgs& args, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& args, bool has_special, int num_sms, cudaStream_t stream);
+
+}  // namespace lk

@@ -1,0 +1,198 @@
+/*
+ * leank.h -- C ABI of a decode-attention library for a LeanK-pruned KV cache
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * The method (the passages each call follows):
+ *   - "KV cache optimisation for LLMs and LeanK pruning" (framerc.cn),
+ *     section 2.2 stage 2: a static binary mask beta per (layer, kv head) keeps
+ *     a multiple of 32 K channels; section 3.1: heads are grouped by kept count,
+ *     the K cache is split into a full-width part for the attention sinks and
+ *     the local window and a pruned part K_prun for the middle tokens, and a
+ *     fused FlashAttention reads both; section 3.2: a head with no kept channel
+ *     drops its middle V as well.
+ *   - "FastGen: profile-based adaptive KV compression" (mhpn.cn), section 2.1:
+ *     each decode step appends K_t, V_t and then attends with Q_t over the
+ *     whole cache; sections 3.1-3.2: per-head policies (local window only,
+ *     special tokens only, full); section 5.1: the three integration points
+ *     (per-head allocation, policy-aware append, a kernel reading per-head
+ *     ranges).
+ *
+ * Conventions (all calls):
+ *   - Every call returns lk_status.  On a non-OK status nothing was enqueued
+ *     and lk_last_error() holds a message (per calling thread).
+ *   - Device memory (cache buffer, workspace, q/k/v/o/ids) is owned by the
+ *     caller and passed as raw device pointers.  The library never calls
+ *     cudaMalloc or cudaFree; its handles are host objects.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Hot calls only enqueue work; they never synchronise.
+ *   - Tensors are dense row-major: bf16 = 16-bit bfloat16 stored as uint16.
+ *   - Errors found on the device (capacity overflow of a special-token head,
+ *     an out-of-range token id, a bounded wait that ran out) set a sticky
+ *     status word inside the cache; lk_check() reads and clears it.
+ */
+#ifndef LEANK_H
+#define LEANK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lk_status {
+  LK_OK = 0,
+  LK_ERR_ARG = 1,         /* bad argument (null pointer, range, mask count, ...) */
+  LK_ERR_ALIGN = 2,       /* a pointer is not aligned as required */
+  LK_ERR_CAPACITY = 3,    /* token capacity or buffer size exceeded */
+  LK_ERR_STATE = 4,       /* call not valid in the cache's current state */
+  LK_ERR_CUDA = 5,        /* a CUDA runtime call failed (message has the CUDA error) */
+  LK_ERR_TIMEOUT = 6,     /* a device-side bounded wait ran out (lk_check) */
+  LK_ERR_UNSUPPORTED = 7  /* shape outside what the kernels implement */
+} lk_status;
+
+/* Per-(layer, kv head) cache policy (FastGen section 3.1). */
+typedef enum lk_policy {
+  LK_POLICY_FULL = 0,     /* LeanK layout: sinks + window at full width, middle on kept channels */
+  LK_POLICY_LOCAL = 1,    /* last local_only_window tokens only, full width, no sinks */
+  LK_POLICY_SPECIAL = 2   /* tokens whose id is special only, full width, in arrival order */
+} lk_policy;
+
+/* Model geometry and cache parameters. */
+typedef struct lk_plan_desc {
+  int32_t num_layers;         /* L >= 1 */
+  int32_t num_q_heads;        /* Hq, a multiple of num_kv_heads */
+  int32_t num_kv_heads;       /* Hkv >= 1; query head j reads kv head j / (Hq/Hkv) */
+  int32_t head_dim;           /* d; must be 128 */
+  int32_t sink;               /* S >= 0: attention-sink tokens of FULL heads */
+  int32_t local;              /* W >= 1: local window of FULL heads */
+  int32_t local_only_window;  /* W_loc >= 1 if any head is LOCAL */
+  int32_t vocab;              /* entries of is_special (>= 1 if any head is SPECIAL) */
+  int32_t special_capacity;   /* max rows of a SPECIAL head per sequence; 0 = token capacity */
+} lk_plan_desc;
+
+typedef struct lk_plan_s* lk_plan;    /* host object owned by the library */
+typedef struct lk_cache_s* lk_cache;  /* host object; its device buffer is the caller's */
+
+/* Where one (layer, sequence, kv head) lives inside the cache buffer (byte
+ * offsets from the buffer start).  Region A is full width (sinks + window
+ * ring, LOCAL ring, or SPECIAL rows); region B holds middle tokens on the
+ * kept channels (FULL heads with n_kept > 0). */
+typedef struct lk_region_info {
+  int32_t policy;
+  int32_t n_kept;             /* kept K channels (FULL), else 0 */
+  int32_t rows_a;             /* row capacity of region A */
+  int32_t rows_b;             /* row capacity of region B */
+  uint64_t k_a_offset;        /* bf16 [rows_a][128] */
+  uint64_t v_a_offset;        /* bf16 [rows_a][128] */
+  uint64_t k_b_offset;        /* bf16 [rows_b][n_kept], kept channels ascending */
+  uint64_t v_b_offset;        /* bf16 [rows_b][128] */
+} lk_region_info;
+
+/* Build a plan (host only; touches no GPU).
+ *   masks      host uint8 [L][Hkv][128], 0/1: the static mask beta (LeanK 2.2).
+ *              For FULL heads the kept count must be 0, 32, 64, 96 or 128;
+ *              rows of other policies are ignored.
+ *   policies   host int32 [L][Hkv] of lk_policy.
+ *   is_special host uint8 [vocab] (1 = special id) or NULL if no SPECIAL head.
+ * Heads are grouped by (policy, kept count) and each FULL head gets its kept
+ * channel list (ascending), used to permute q.  Errors: LK_ERR_ARG,
+ * LK_ERR_UNSUPPORTED (head_dim != 128 or Hq/Hkv > 8). */
+lk_status lk_build_plan(const lk_plan_desc* desc, const uint8_t* masks, const int32_t* policies,
+                        const uint8_t* is_special, lk_plan* out);
+void lk_plan_destroy(lk_plan plan);
+
+/* Host-side query of one head's policy, kept count and kept channels
+ * (kept_channels: host int16 [128] or NULL; first n_kept entries valid). */
+lk_status lk_plan_head(lk_plan plan, int32_t layer, int32_t kv_head, int32_t* policy,
+                       int32_t* n_kept, int16_t* kept_channels);
+
+/* Bytes of the cache buffer for `batch` sequences of up to `capacity_tokens`
+ * tokens each (LeanK 3.1 split cache, FastGen 5.1 per-head allocation). */
+lk_status lk_cache_bytes(lk_plan plan, int32_t batch, int32_t capacity_tokens, size_t* bytes);
+
+/* Bytes of the decode workspace (split partials, counters, staging of
+ * lk_step_host) for `batch` sequences. */
+lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes);
+
+/* Bind a cache to a caller-owned device buffer of at least lk_cache_bytes
+ * bytes, 256-byte aligned.  Enqueues a zero fill of the buffer and the upload
+ * of the plan's tables on `stream`; all layers start empty.  The plan must
+ * outlive nothing: the cache copies what it needs.  Needs a CUDA device. */
+lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch,
+                        int32_t capacity_tokens, void* stream, lk_cache* out);
+void lk_cache_destroy(lk_cache cache);
+
+/* Zero a caller-owned workspace of at least lk_workspace_bytes bytes
+ * (256-byte aligned).  Needed once before the first lk_decode_attn with it,
+ * and again after lk_check reported LK_ERR_TIMEOUT. */
+lk_status lk_workspace_init(lk_cache cache, void* workspace, size_t ws_bytes, void* stream);
+
+/* Build one empty layer from a dense history of n tokens (prefill, "white
+ * paper" 2.3): equal, byte for byte, to n successive lk_append calls.
+ *   k, v  device bf16 [B][n][Hkv][128];  ids device int32 [B][n] or NULL.
+ * Errors: LK_ERR_STATE if the layer is not empty, LK_ERR_CAPACITY if n
+ * exceeds the token capacity. */
+lk_status lk_prefill(lk_cache cache, int32_t layer, const void* k, const void* v,
+                     const int32_t* ids, int32_t n, void* stream);
+
+/* Append one token per sequence to a layer (FastGen 2.1, 3.2 stage 2).
+ *   k, v  device bf16 [B][Hkv][128];  ids device int32 [B] or NULL.
+ * FULL heads: token n < S goes to sink row n; later tokens go to window ring
+ * row S + (n-S) mod W, and once the window is full the token n-W it replaces
+ * first moves to the middle (K gathered to the kept channels into K_prun row
+ * n-W-S, V copied; dropped when n_kept = 0).  LOCAL: ring row n mod W_loc.
+ * SPECIAL: appended (row = count) only if is_special[id].  Bit-exact copies.
+ * Errors: LK_ERR_CAPACITY when the layer already holds capacity_tokens. */
+lk_status lk_append(lk_cache cache, int32_t layer, const void* k, const void* v,
+                    const int32_t* ids, void* stream);
+
+/* Decode attention of one layer (LeanK 3.1 fused FlashAttention over the
+ * split cache; FastGen 3.2 per-policy ranges).
+ *   q  device bf16 [B][Hq][128];  o  device fp32 [B][Hq][128].
+ * For query head j of sequence b (kv head h = j / G): scores q.k / sqrt(128)
+ * over sinks + window at all channels and over the middle tokens at the kept
+ * channels (q gathered to the kept channel list), one softmax over both,
+ * o = sum p V.  Split over tokens across CTAs; partials are merged inside the
+ * same launch.  A head with no resident token gives o = 0.
+ * workspace: >= lk_workspace_bytes bytes, zeroed once by lk_workspace_init;
+ * calls sharing one workspace must not overlap on the GPU. */
+lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* One decode step end to end from host memory: copies q [B][Hq][128] bf16,
+ * k, v [B][Hkv][128] bf16 and ids [B] int32 (NULL allowed) from host to the
+ * workspace, runs lk_append then lk_decode_attn, and copies o [B][Hq][128]
+ * fp32 back to host.  Host buffers should be pinned for the copies to be
+ * asynchronous; read o only after synchronising `stream`. */
+lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const void* k_host,
+                       const void* v_host, const int32_t* ids_host, float* o_host,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* Host-tracked token count of a layer (tokens appended or prefilled). */
+lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n);
+
+/* Location of one (layer, sequence, kv head) in the cache buffer. */
+lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_head,
+                          lk_region_info* out);
+
+/* K+V bytes one lk_decode_attn of `layer` reads from the resident cache
+ * (synchronises `stream` to read the special-token counts). */
+lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_t* bytes);
+
+/* Override the number of CTAs of lk_decode_attn (0 = one per SM); for
+ * split-invariance tests.  Must be <= 1024. */
+lk_status lk_set_decode_ctas(lk_cache cache, int32_t ctas);
+
+/* Synchronise `stream`, read and clear the device status word.  Returns
+ * LK_ERR_TIMEOUT, LK_ERR_CAPACITY or LK_ERR_ARG (bad token id) for a set
+ * bit, LK_ERR_CUDA for a pending CUDA error, else LK_OK. */
+lk_status lk_check(lk_cache cache, void* stream);
+
+/* Message of the last non-OK status on the calling thread ("" if none). */
+const char* lk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LEANK_H */

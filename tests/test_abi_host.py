@@ -1,0 +1,139 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and the host-only calls validate their arguments."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from decode_attention_pruned_gb300 import binding as lkb
+from decode_attention_pruned_gb300 import synth as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "leank.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lk_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_symbols()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(lkb.SIGNATURES), set(names) ^ set(lkb.SIGNATURES)
+
+
+def _plan(masks, policies=None, **kw):
+    L, H, _ = masks.shape
+    args = dict(num_layers=L, num_q_heads=4 * H, num_kv_heads=H, sink=4, local=16)
+    args.update(kw)
+    return lkb.Plan(args.pop("num_layers"), args.pop("num_q_heads"), args.pop("num_kv_heads"),
+                    args.pop("sink"), args.pop("local"), masks, policies, **args)
+
+
+def test_plan_rejects_unaligned_mask_count(lib):
+    m = np.zeros((1, 2, 128), dtype=np.uint8)
+    m[0, 0, :33] = 1
+    with pytest.raises(lkb.LeankError) as e:
+        _plan(m)
+    assert e.value.status == lkb.LK_ERR_ARG
+    assert "multiple of 32" in str(e.value)
+
+
+def test_plan_rejects_bad_values(lib):
+    m = np.ones((1, 2, 128), dtype=np.uint8)
+    m2 = m.copy(); m2[0, 1, 5] = 2
+    with pytest.raises(lkb.LeankError) as e:
+        _plan(m2)
+    assert e.value.status == lkb.LK_ERR_ARG
+    with pytest.raises(lkb.LeankError) as e:
+        _plan(m, policies=np.array([[0, 7]], dtype=np.int32))
+    assert e.value.status == lkb.LK_ERR_ARG
+    with pytest.raises(lkb.LeankError) as e:                 # SPECIAL without a table
+        _plan(m, policies=np.array([[0, 2]], dtype=np.int32))
+    assert e.value.status == lkb.LK_ERR_ARG
+    with pytest.raises(lkb.LeankError) as e:                 # LOCAL without a window
+        _plan(m, policies=np.array([[1, 0]], dtype=np.int32))
+    assert e.value.status == lkb.LK_ERR_ARG
+    with pytest.raises(lkb.LeankError) as e:
+        _plan(m, num_q_heads=5)
+    assert e.value.status == lkb.LK_ERR_ARG
+
+
+def test_plan_rejects_unsupported_shapes(lib):
+    m = np.ones((1, 2, 128), dtype=np.uint8)
+    with pytest.raises(lkb.LeankError) as e:
+        _plan(m, num_q_heads=18)                              # G = 9 > 8
+    assert e.value.status == lkb.LK_ERR_UNSUPPORTED
+    desc = lkb.PlanDesc(1, 2, 2, 64, 4, 16, 0, 0, 0)
+    h = ctypes.c_void_p()
+    pol = np.zeros((1, 2), np.int32)
+    st = lib.lk_build_plan(ctypes.byref(desc), np.ones((1, 2, 64), np.uint8).ctypes.data, pol.ctypes.data,
+                           None, ctypes.byref(h))
+    assert st == lkb.LK_ERR_UNSUPPORTED
+    st = lib.lk_build_plan(None, None, None, None, ctypes.byref(h))
+    assert st == lkb.LK_ERR_ARG
+    assert b"null" in lib.lk_last_error()
+
+
+def test_plan_groups_heads_and_orders_kept_channels(lib):
+    w = S.WORKLOADS[2]
+    pol = S.make_policies(w)
+    masks = S.make_masks(w, pol)
+    plan = lkb.Plan.for_workload(w, masks, pol)
+    for l, h in [(0, 0), (3, 5), (31, 7)]:
+        p, k, kept = plan.head(l, h)
+        assert p == S.POLICY_FULL
+        assert k == int(masks[l, h].sum())
+        assert np.array_equal(kept, np.nonzero(masks[l, h])[0])
+
+
+def test_cache_bytes_grow_with_capacity_and_width(lib):
+    w = S.WORKLOADS[1]
+    m32 = S.masks_with_counts(w, [32] * 8)
+    m128 = S.masks_with_counts(w, [128] * 8)
+    m0 = S.masks_with_counts(w, [0] * 8)
+    sizes = {}
+    for name, m in [("k0", m0), ("k32", m32), ("k128", m128)]:
+        plan = lkb.Plan.for_workload(w, m, S.make_policies(w))
+        sizes[name] = plan.cache_bytes(1, 32768)
+        assert plan.cache_bytes(1, 40000) > sizes[name] or name == "k0"
+    # dense K+V of 8 heads x 32768 tokens is 128 MiB; the k=128 layout holds it
+    dense = 2 * 8 * 32768 * 128 * 2
+    assert dense <= sizes["k128"] < dense + (4 << 20)
+    mid = 32768 - 16 - 1024
+    # (less the 64-row minimum every pool keeps for its tensor map)
+    assert sizes["k32"] - sizes["k0"] >= 8 * mid * (32 + 128) * 2 - 64 * 32 * 2
+    assert sizes["k0"] < 8 * (16 + 1024) * 512 + (8 << 20)
+    with pytest.raises(lkb.LeankError):
+        plan.cache_bytes(0, 10)
+    with pytest.raises(lkb.LeankError):
+        plan.cache_bytes(1, 0)
+
+
+def test_workspace_bytes(lib):
+    w = S.WORKLOADS[3]
+    plan = lkb.Plan.for_workload(w, S.make_masks(w), S.make_policies(w))
+    n = plan.workspace_bytes(w.batch)
+    E, G = w.batch * w.num_kv_heads, w.group
+    assert n >= (1024 + E) * G * 128 * 4
+
+
+def test_cache_init_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    w = S.WORKLOADS[0]
+    plan = lkb.Plan.for_workload(w, S.make_masks(w), S.make_policies(w))
+    buf = np.zeros(plan.cache_bytes(1, 64) + 256, dtype=np.uint8)
+    addr = (buf.ctypes.data + 255) // 256 * 256
+    h = ctypes.c_void_p()
+    st = lib.lk_cache_init(plan._h, addr, plan.cache_bytes(1, 64), 1, 64, None, ctypes.byref(h))
+    assert st in (lkb.LK_ERR_CUDA,)
+    assert h.value is None
+    st = lib.lk_cache_init(plan._h, addr + 8, 1 << 20, 1, 64, None, ctypes.byref(h))
+    assert st == lkb.LK_ERR_ALIGN

@@ -1,0 +1,206 @@
+"""GPU decode attention vs the fp64 oracle, element by element, at sizes the
+oracle finishes in seconds (several 64-row tiles and ragged tails).  Every
+call goes through the C ABI (libleank.so)."""
+import numpy as np
+import pytest
+import torch
+
+from decode_attention_pruned_gb300 import binding as lkb
+from decode_attention_pruned_gb300 import synth as S
+from helpers import DECODE_TOL, Case
+
+pytestmark = pytest.mark.gpu
+
+TINY = S.WORKLOADS[0]
+LLAMA = S.WORKLOADS[1]
+SERVING = S.WORKLOADS[2]
+QWEN = S.WORKLOADS[3]
+FASTGEN = S.WORKLOADS[4]
+
+
+def _max_err(o, ref):
+    return float(np.abs(o.double().cpu().numpy() - ref).max())
+
+
+def _decode_steps(case, layer, n0, n_steps, layout=False):
+    case.prefill(layer, n0)
+    if layout:
+        case.check_layout(layer, n0)
+    worst = 0.0
+    for t in range(n0, n0 + n_steps):
+        case.append(layer, t)
+        N = t + 1
+        q = case.q(layer, N, step=t)
+        o = case.cache.decode(layer, q)
+        case.cache.check()
+        err = _max_err(o, case.expected(layer, q, N))
+        assert err <= DECODE_TOL, (layer, N, err)
+        worst = max(worst, err)
+        if layout:
+            case.check_layout(layer, N)
+    return worst
+
+
+@pytest.mark.parametrize("counts", [(0, 0), (0, 64), (64, 0), (64, 64), None],
+                         ids=["k0-0", "k0-64", "k64-0", "k64-64", "seeded"])
+def test_tiny_prefill_then_16_appends(cuda, counts):
+    masks = None if counts is None else S.masks_with_counts(TINY, counts)
+    case = Case(TINY, total=528, masks=masks)
+    _decode_steps(case, 0, 512, 16, layout=True)
+
+
+def test_llama_layer_shape_all_widths(cuda):
+    w = LLAMA.scaled(context=3000)
+    masks = S.masks_with_counts(w, [0, 32, 64, 96, 128, 32, 0, 64])
+    case = Case(w, total=3003, masks=masks)
+    _decode_steps(case, 0, 3000, 3, layout=True)
+
+
+def test_llama_layer_seeded_masks_outliers(cuda):
+    w = LLAMA.scaled(context=2600)
+    case = Case(w, total=2601)
+    _decode_steps(case, 0, 2600, 1, layout=True)
+
+
+def test_serving_shape_two_layers(cuda):
+    w = SERVING.scaled(num_layers=2, batch=3, context=700)
+    case = Case(w, total=702)
+    for layer in range(2):
+        _decode_steps(case, layer, 700, 2, layout=True)
+
+
+def test_qwen_shape_group7_rope(cuda):
+    w = QWEN.scaled(batch=2, context=2500)
+    masks = S.masks_with_counts(w, [32, 0, 96, 64])
+    case = Case(w, total=2501, masks=masks)
+    _decode_steps(case, 0, 2500, 1, layout=True)
+
+
+def test_fastgen_policy_mix(cuda):
+    w = FASTGEN.scaled(num_layers=2, batch=3, context=900, policy_counts=(6, 4, 6))
+    case = Case(w, total=903)
+    for layer in range(2):
+        _decode_steps(case, layer, 880, 23, layout=(layer == 0))
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 7, 0])
+def test_split_invariance(cuda, ctas):
+    w = LLAMA.scaled(context=2300, batch=2)
+    masks = S.masks_with_counts(w, [32, 64, 0, 96, 128, 32, 32, 64])
+    case = Case(w, total=2300, masks=masks)
+    case.prefill(0, 2300)
+    case.cache.set_decode_ctas(ctas)
+    q = case.q(0, 2300)
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    assert _max_err(o, case.expected(0, q, 2300)) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("N", [1, 3, 16, 17, 1039, 1040, 1041, 1105])
+def test_region_boundaries(cuda, N):
+    # S = 16, W = 1024: below the sinks, inside the window fill, at the first
+    # eviction, and one ragged tile past it
+    w = LLAMA.scaled(context=N)
+    masks = S.masks_with_counts(w, [0, 32, 64, 96, 128, 32, 0, 64])
+    case = Case(w, total=N, masks=masks)
+    case.prefill(0, N - 1)
+    case.append(0, N - 1)
+    q = case.q(0, N)
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    assert _max_err(o, case.expected(0, q, N)) <= DECODE_TOL
+    case.check_layout(0, N)
+
+
+def test_all_heads_dropped(cuda):
+    w = SERVING.scaled(num_layers=1, batch=2, context=1500)
+    masks = np.zeros((1, 8, 128), dtype=np.uint8)
+    case = Case(w, total=1500, masks=masks)
+    case.prefill(0, 1500)
+    q = case.q(0, 1500)
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    assert _max_err(o, case.expected(0, q, 1500)) <= DECODE_TOL
+
+
+def test_special_head_without_special_tokens_gives_zero(cuda):
+    w = FASTGEN.scaled(num_layers=1, batch=2, context=300, policy_counts=(2, 4, 2))
+    case = Case(w, total=300)
+    case.flags[:] = False
+    case.is_special[:] = 0
+    case.plan = lkb.Plan.for_workload(w, case.masks, case.policies, case.is_special)
+    case.cache = lkb.Cache(case.plan, w.batch, 300)
+    case.prefill(0, 300)
+    q = case.q(0, 300)
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    ref = case.expected(0, q, 300)
+    assert _max_err(o, ref) <= DECODE_TOL
+    G = w.group
+    for h in range(8):
+        if case.policies[0, h] == S.POLICY_SPECIAL:
+            assert torch.all(o[:, h * G:(h + 1) * G] == 0)
+
+
+def test_empty_layer_decodes_to_zero(cuda):
+    w = TINY
+    case = Case(w, total=4)
+    q = case.q(0, 1)
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    assert torch.all(o == 0)
+
+
+def test_prefill_equals_appends_byte_for_byte(cuda):
+    w = FASTGEN.scaled(num_layers=1, batch=2, context=700, policy_counts=(3, 2, 3))
+    a = Case(w, total=716)
+    b = Case(w, total=716)
+    a.prefill(0, 716)
+    b.prefill(0, 700)
+    for t in range(700, 716):
+        b.append(0, t)
+    a.cache.check()
+    b.cache.check()
+    torch.cuda.synchronize()
+    assert torch.equal(a.cache.buffer, b.cache.buffer)
+    a.check_layout(0, 716)
+
+
+def test_step_host_matches_device_path(cuda):
+    w = SERVING.scaled(num_layers=1, batch=2, context=600)
+    a = Case(w, total=601)
+    b = Case(w, total=601)
+    a.prefill(0, 600)
+    b.prefill(0, 600)
+    k, v = a.history(0)
+    q = a.q(0, 601)
+    a.append(0, 600)
+    o_dev = a.cache.decode(0, q)
+    pin = lambda t: t.cpu().pin_memory()
+    o_host = torch.empty(o_dev.shape, dtype=torch.float32).pin_memory()
+    b.cache.step_host(0, pin(q), pin(k[:, 600].contiguous()), pin(v[:, 600].contiguous()), None, o_host)
+    torch.cuda.synchronize()
+    b.cache.check()
+    assert torch.equal(o_host, o_dev.cpu())
+
+
+def test_capacity_is_enforced(cuda):
+    w = TINY
+    case = Case(w, total=10, capacity=10)
+    case.prefill(0, 10)
+    with pytest.raises(lkb.LeankError) as e:
+        case.append(0, 9)
+    assert e.value.status == lkb.LK_ERR_CAPACITY
+    with pytest.raises(lkb.LeankError) as e:
+        case.prefill(0, 5)
+    assert e.value.status == lkb.LK_ERR_STATE
+
+
+def test_special_overflow_is_reported_on_device(cuda):
+    w = FASTGEN.scaled(num_layers=1, batch=1, context=400, policy_counts=(2, 4, 2))
+    case = Case(w, total=400, special_capacity=4)
+    case.prefill(0, 400)
+    with pytest.raises(lkb.LeankError) as e:
+        case.cache.check()
+    assert e.value.status == lkb.LK_ERR_CAPACITY
+    case.cache.check()   # cleared
