@@ -368,13 +368,24 @@ lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch
     delete c;
     return cuda_fail(err, "lk_cache_init: upload");
   }
+  // One TMA operation per tile and operand (bandwidth grows with the size of
+  // each operation): 128-byte-row pools load as 64-channel halves with
+  // 128-byte swizzle, 64-byte-row pools as 32-channel stripes with 64-byte
+  // swizzle; 3-D maps fold the halves / stripes of a row into one box.
   for (int pl = 0; pl < kNumPools; ++pl) {
-    const cuuint64_t dims[2] = {(cuuint64_t)pool_width(pl), (cuuint64_t)lay.pool_rows[pl]};
-    const cuuint64_t strides[1] = {(cuuint64_t)pool_width(pl) * 2};
-    const cuuint32_t box[2] = {32, (cuuint32_t)kTmaBoxRows};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult r = encode(&c->maps[pl], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cv.pool[pl], dims, strides, box,
-                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+    const int width = pool_width(pl);
+    const bool fam128 = (width % 64) == 0;
+    const int inner = fam128 ? 64 : 32;              // channels per half / stripe
+    const int parts = width / inner;
+    const cuuint64_t row_bytes = (cuuint64_t)width * 2;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)lay.pool_rows[pl], (cuuint64_t)parts};
+    cuuint64_t strides[2] = {row_bytes, (cuuint64_t)inner * 2};
+    cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)kTmaBoxRows, (cuuint32_t)parts};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    const cuuint32_t rank = parts > 1 ? 3 : 2;
+    CUresult r = encode(&c->maps[pl], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, cv.pool[pl], dims, strides, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        fam128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
       delete c;

@@ -39,11 +39,12 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kTileRows = 16 * kConsumerWarps;          // 64 tokens per stage
-static_assert(kTileRows == kTmaBoxRows, "tensor-map box rows");
-constexpr int kStages = 6;
-constexpr int kBoxBytes = kTileRows * 64;               // 64 rows x 32 bf16 channels
-constexpr int kStageBytes = 8 * kBoxBytes;              // K (<= 4 boxes) + V (4 boxes)
+constexpr int kTileRows = kTmaBoxRows;                  // 128 tokens per stage
+constexpr int kSubPerWarp = kTileRows / 16 / kConsumerWarps;   // m16 row blocks per warp
+static_assert(kSubPerWarp == 2, "two 16-row blocks per consumer warp");
+constexpr int kStages = 3;
+constexpr int kSlotBytes = kTileRows * 256;             // one full-width tile (32 KB)
+constexpr int kStageBytes = 2 * kSlotBytes;             // K slot + V slot
 constexpr int kUnitsA = 16;                             // cost per full-width row (512 B / 32)
 constexpr int kFirst = 1, kLast = 2;
 
@@ -97,8 +98,18 @@ __device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) {
   return r;
 }
 
+__device__ __forceinline__ uint64_t row_cost_b(int kb) { return (uint64_t)(kb / 16 + 8); }
+
 __device__ __forceinline__ uint64_t entry_cost(const Entry& g) {
-  return (uint64_t)kUnitsA * g.n_a + (uint64_t)(g.kb / 16 + 8) * g.n_b;
+  return (uint64_t)kUnitsA * g.n_a + row_cost_b(g.kb) * g.n_b;
+}
+
+// Rows r in [0, n) of a region whose row r sits at line offset o0 + c*r and
+// starts inside [start, end): r in [r0, r1).
+__device__ __forceinline__ void rows_in_range(uint64_t o0, uint64_t c, int n, uint64_t start, uint64_t end,
+                                              int& r0, int& r1) {
+  r0 = start > o0 ? (int)min((uint64_t)n, (start - o0 + c - 1) / c) : 0;
+  r1 = end > o0 ? (int)min((uint64_t)n, (end - o0 + c - 1) / c) : 0;
 }
 
 // Largest CTA index i < P with floor(i*C/P) <= x.
@@ -120,6 +131,19 @@ __device__ __forceinline__ void record_status(const DecodeArgs& a, uint32_t bits
 
 __device__ __forceinline__ uint32_t ld_q_pair(const uint16_t* row, int c) {
   return *reinterpret_cast<const uint32_t*>(row + c);
+}
+
+// Shared-memory address of 16-byte chunk `c` (channels 8c..8c+7) of tile row
+// `r`.  128-byte family (K128, V, K64): 64-channel halves of T rows x 128 B,
+// 128-byte swizzle (chunk ^= row mod 8).  64-byte family (K32, K96):
+// 32-channel stripes of T rows x 64 B, 64-byte swizzle (chunk ^= (row/2) mod 4).
+__device__ __forceinline__ uint32_t tile_addr128(uint32_t base, int r, int c) {
+  return base + (uint32_t)(c >> 3) * (kTileRows * 128) + (uint32_t)r * 128u +
+         ((uint32_t)((c & 7) ^ (r & 7)) << 4);
+}
+__device__ __forceinline__ uint32_t tile_addr64(uint32_t base, int r, int c) {
+  return base + (uint32_t)(c >> 2) * (kTileRows * 64) + (uint32_t)r * 64u +
+         ((uint32_t)((c & 3) ^ ((r >> 1) & 3)) << 4);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -157,9 +181,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps && lane == 0) {
     tma_prefetch_map(&tm_k128);
     tma_prefetch_map(&tm_v);
+    tma_prefetch_map(&tm_k32);
   }
   // lengths and special counts are written by the preceding append
   grid_dependency_wait();
+  grid_launch_dependents();
 
   // ---- the line: per-thread chunks of entries, block exclusive scan
   const int per = (E + kThreads - 1) / kThreads;
@@ -180,9 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     C += scan[w];
   }
   const uint64_t excl = warp_base + incl - local;
-  // each CTA range must cover at least one full tile (see header comment)
-  const uint64_t full_tile = (uint64_t)kUnitsA * kTileRows;
-  const int P = (int)max((uint64_t)1, min((uint64_t)gridDim.x, C / full_tile));
+  // every CTA range must hold at least one row start (a row costs <= 16)
+  const int P = (int)max((uint64_t)1, min((uint64_t)gridDim.x, C / kUnitsA));
   const int cta = blockIdx.x;
   const uint64_t start = cta < P ? ((uint64_t)cta * C) / P : C;
   const uint64_t end = cta < P ? ((uint64_t)(cta + 1) * C) / P : C;
@@ -212,56 +237,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; ok && e < E && off < end; ++e) {
         const Entry g = entry_geometry(a, e);
         const uint64_t cost = entry_cost(g);
-        const int ta = (g.n_a + kTileRows - 1) / kTileRows;
-        const int tb = (g.n_b + kTileRows - 1) / kTileRows;
-        const uint64_t cb = (uint64_t)(g.kb / 16 + 8);
-        auto tile_off = [&](int j) -> uint64_t {
-          return j < ta ? off + full_tile * j : off + (uint64_t)kUnitsA * g.n_a + cb * kTileRows * (j - ta);
-        };
-        if (ta + tb > 0) {
+        const uint64_t cb = row_cost_b(g.kb);
+        const uint64_t off_b = off + (uint64_t)kUnitsA * g.n_a;
+        int a0, a1, b0, b1;
+        rows_in_range(off, kUnitsA, g.n_a, start, end, a0, a1);
+        rows_in_range(off_b, cb, g.n_b, start, end, b0, b1);
+        const int nta = (a1 - a0 + kTileRows - 1) / kTileRows;
+        const int ntb = (b1 - b0 + kTileRows - 1) / kTileRows;
+        if (nta + ntb > 0) {
           const int b = e / cv.Hkv, h = e - b * cv.Hkv;
           const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
-          const int fc = range_owner(tile_off(0), C, P);
-          const int lc = range_owner(tile_off(ta + tb - 1), C, P);
-          const CUtensorMap* kmap_b = hd.pool_kb == kPoolK32   ? &tm_k32
-                                      : hd.pool_kb == kPoolK64 ? &tm_k64
-                                      : hd.pool_kb == kPoolK96 ? &tm_k96
-                                                               : &tm_k128;
-          bool first = true;
-          for (int j = 0; j < ta + tb; ++j) {
-            const uint64_t to = tile_off(j);
-            if (to < start) continue;
-            if (to >= end) break;
-            const bool last = (j + 1 == ta + tb) || (tile_off(j + 1) >= end);
+          const uint64_t last_row_off = g.n_b > 0 ? off_b + cb * (g.n_b - 1) : off + (uint64_t)kUnitsA * (g.n_a - 1);
+          const int fc = range_owner(off, C, P);
+          const int lc = range_owner(last_row_off, C, P);
+          for (int j = 0; j < nta + ntb; ++j) {
             if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, a.wait_limit_ns)) {
               ok = false;
               break;
             }
-            const bool in_a = j < ta;
-            const int jr = in_a ? j : j - ta;
+            const bool in_a = j < nta;
+            const int r = in_a ? a0 + j * kTileRows : b0 + (j - nta) * kTileRows;
             StageDesc d;
             d.e = e;
             d.region = in_a ? 0 : 1;
-            d.nrows = min(kTileRows, (in_a ? g.n_a : g.n_b) - jr * kTileRows);
+            d.nrows = min(kTileRows, (in_a ? a1 : b1) - r);
             d.width = in_a ? kHeadDim : g.kb;
-            d.flags = (first ? kFirst : 0) | (last ? kLast : 0);
+            d.flags = (j == 0 ? kFirst : 0) | (j + 1 == nta + ntb ? kLast : 0);
             d.first_cta = fc;
             d.last_cta = lc;
             d.pad = 0;
             desc[stage] = d;
-            const int64_t krow = in_a ? hd.row_a + (int64_t)b * hd.cap_a + (int64_t)jr * kTileRows
-                                      : hd.krow_b + (int64_t)b * hd.cap_b + (int64_t)jr * kTileRows;
-            const int64_t vrow = in_a ? krow : hd.vrow_b + (int64_t)b * hd.cap_b + (int64_t)jr * kTileRows;
-            const int kboxes = d.width / 32;
             const uint32_t fb = bar_full + 8 * stage;
-            mbar_arrive_expect_tx(fb, (uint32_t)(kboxes + 4) * kBoxBytes);
-            const uint32_t sbase = base + SmemLayout::kStagesOff + stage * kStageBytes;
-            const CUtensorMap* kmap = in_a ? &tm_k128 : kmap_b;
-            for (int c = 0; c < kboxes; ++c)
-              tma_load_2d(sbase + c * kBoxBytes, kmap, 32 * c, (int32_t)krow, fb, policy);
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d(sbase + (4 + c) * kBoxBytes, &tm_v, 32 * c, (int32_t)vrow, fb, policy);
-            first = false;
+            mbar_arrive_expect_tx(fb, (uint32_t)kTileRows * (2 * d.width + 256));
+            const uint32_t kdst = base + SmemLayout::kStagesOff + stage * kStageBytes;
+            const uint32_t vdst = kdst + kSlotBytes;
+            if (in_a) {
+              const int32_t row = (int32_t)(hd.row_a + (int64_t)b * hd.cap_a + r);
+              tma_load_3d(kdst, &tm_k128, 0, row, 0, fb, policy);
+              tma_load_3d(vdst, &tm_v, 0, row, 0, fb, policy);
+            } else {
+              const int32_t krow = (int32_t)(hd.krow_b + (int64_t)b * hd.cap_b + r);
+              const int32_t vrow = (int32_t)(hd.vrow_b + (int64_t)b * hd.cap_b + r);
+              switch (hd.pool_kb) {
+                case kPoolK32: tma_load_2d(kdst, &tm_k32, 0, krow, fb, policy); break;
+                case kPoolK64: tma_load_2d(kdst, &tm_k64, 0, krow, fb, policy); break;
+                case kPoolK96: tma_load_3d(kdst, &tm_k96, 0, krow, 0, fb, policy); break;
+                default: tma_load_3d(kdst, &tm_k128, 0, krow, 0, fb, policy); break;
+              }
+              tma_load_3d(vdst, &tm_v, 0, vrow, 0, fb, policy);
+            }
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -283,11 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ================================================================ consumers
   const int ct = tid;                       // 0 .. 127
   const int gid = lane >> 2, tig = lane & 3;
-  const int r0 = warp * 16;
-  const int rowK = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int chK = lane >> 4;
-  const int rowV = r0 + (lane & 7) + (lane >> 4) * 8;
-  const int chV = (lane >> 3) & 1;
+  const int rk = (lane & 7) + ((lane >> 3) & 1) * 8;    // ldmatrix row of the K (A) operand
+  const int ck = lane >> 4;                              // +0 / +1 chunk
+  const int rv = (lane & 7) + (lane >> 4) * 8;          // ldmatrix.trans row of the V^T operand
+  const int cvh = (lane >> 3) & 1;
   const float NEG_INF = -INFINITY;
 
   // entries with no resident token: o = 0, written by CTA (e mod grid)
@@ -342,29 +365,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
 
-    const int nv = d.nrows - r0;
-    if (nv > 0) {
+    // this warp's two 16-row blocks of the tile: rows 16*(warp + 4j)
+    const int nv0 = d.nrows - 16 * warp;
+    if (nv0 > 0) {
       const uint32_t kbase = base + SmemLayout::kStagesOff + stage * kStageBytes;
-      const uint32_t vbase = kbase + 4 * kBoxBytes;
+      const uint32_t vbase = kbase + kSlotBytes;
       const bool in_a = d.region == 0;
+      const bool fam128 = (d.width & 63) == 0;          // widths 64 / 128 use 128-byte rows
       const int nks = d.width >> 4;
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
+      float x[kSubPerWarp][4];
+      bool live[kSubPerWarp];
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (ks < nks) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(swz64(kbase + (ks >> 1) * kBoxBytes, rowK, ((ks & 1) << 1) + chK), a0, a1, a2, a3);
-          const uint32_t b0 = in_a ? qa[ks][0] : qb[ks][0];
-          const uint32_t b1 = in_a ? qa[ks][1] : qb[ks][1];
-          mma_bf16_16816(s, a0, a1, a2, a3, b0, b1);
+      for (int j = 0; j < kSubPerWarp; ++j) {
+        const int r0 = 16 * (warp + kConsumerWarps * j);
+        const int nv = d.nrows - r0;
+        live[j] = nv > 0;
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        if (live[j]) {
+          const int row = r0 + rk;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            if (ks < nks) {
+              const int c = 2 * ks + ck;
+              const uint32_t addr = fam128 ? tile_addr128(kbase, row, c) : tile_addr64(kbase, row, c);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(addr, a0, a1, a2, a3);
+              const uint32_t b0 = in_a ? qa[ks][0] : qb[ks][0];
+              const uint32_t b1 = in_a ? qa[ks][1] : qb[ks][1];
+              mma_bf16_16816(s, a0, a1, a2, a3, b0, b1);
+            }
+          }
         }
+        const bool v0 = gid < nv, v1 = gid + 8 < nv;
+        x[j][0] = v0 ? s[0] * a.scale_log2 : NEG_INF;
+        x[j][1] = v0 ? s[1] * a.scale_log2 : NEG_INF;
+        x[j][2] = v1 ? s[2] * a.scale_log2 : NEG_INF;
+        x[j][3] = v1 ? s[3] * a.scale_log2 : NEG_INF;
       }
-      const bool v0 = gid < nv, v1 = gid + 8 < nv;
-      const float x0 = v0 ? s[0] * a.scale_log2 : NEG_INF;
-      const float x1 = v0 ? s[1] * a.scale_log2 : NEG_INF;
-      const float x2 = v1 ? s[2] * a.scale_log2 : NEG_INF;
-      const float x3 = v1 ? s[3] * a.scale_log2 : NEG_INF;
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+      float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
+      float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
 #pragma unroll
       for (int sh = 4; sh < 32; sh <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
@@ -374,14 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
       m0 = mn0;
       m1 = mn1;
-      // P as a bf16 pair hi + lo (two mmas below): P.V keeps ~16 mantissa bits
-      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);     // token gid
-      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);     // token gid + 8
-      const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-      const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-      const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-      l0 = l0 * al0 + (p0 + p2);
-      l1 = l1 * al1 + (p1 + p3);
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         o[i][0] *= al0;
@@ -389,15 +422,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         o[i][2] *= al0;
         o[i][3] *= al1;
       }
-      // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
-      const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
-      const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_trans(swz64(vbase + (i >> 1) * kBoxBytes, rowV, ((i & 1) << 1) + chV), a0, a1, a2, a3);
-        mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
-        mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
+      for (int j = 0; j < kSubPerWarp; ++j) {
+        if (!live[j]) continue;
+        // P as a bf16 pair hi + lo (two mmas): P.V keeps ~16 mantissa bits
+        const float p0 = exp2f(x[j][0] - mn0), p1 = exp2f(x[j][1] - mn1);   // token gid
+        const float p2 = exp2f(x[j][2] - mn0), p3 = exp2f(x[j][3] - mn1);   // token gid + 8
+        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+        const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+        const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
+        const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+        const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
+        const int row = 16 * (warp + kConsumerWarps * j) + rv;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(tile_addr128(vbase, row, 2 * i + cvh), a0, a1, a2, a3);
+          mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
+          mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
+        }
       }
     }
     __syncwarp();
@@ -430,23 +476,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* dst = a.o + ((size_t)b * cv.Hq + (size_t)h * G) * kHeadDim;
       const bool single = d.first_cta == d.last_cta;
       const size_t slot = (size_t)blockIdx.x + d.e;
-      for (int idx = ct; idx < G * kHeadDim; idx += kConsumerWarps * 32) {
-        const int g = idx >> 7, dd = idx & 127;
+      // CTA-level merge, 4 channels per thread
+      for (int q4 = ct; q4 < G * 32; q4 += kConsumerWarps * 32) {
+        const int g = q4 >> 5, dd = (q4 & 31) * 4;
         float M = NEG_INF;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * kMaxGroup + g]);
-        float acc = 0.f, L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
           const float mw = merge_m[w * kMaxGroup + g];
           const float f = mw == NEG_INF ? 0.f : exp2f(mw - M);
-          acc += f * merge_o[(w * kMaxGroup + g) * kHeadDim + dd];
+          const float4 v = *reinterpret_cast<const float4*>(&merge_o[(w * kMaxGroup + g) * kHeadDim + dd]);
+          acc.x += f * v.x;
+          acc.y += f * v.y;
+          acc.z += f * v.z;
+          acc.w += f * v.w;
           L += f * merge_l[w * kMaxGroup + g];
         }
         if (single) {
-          dst[idx] = L > 0.f ? acc / L : 0.f;
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          *reinterpret_cast<float4*>(&dst[g * kHeadDim + dd]) =
+              make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         } else {
-          a.part[(slot * G + g) * kHeadDim + dd] = acc;
+          *reinterpret_cast<float4*>(&a.part[(slot * G + g) * kHeadDim + dd]) = acc;
           if (dd == 0) a.part_ml[slot * G + g] = make_float2(M, L);
         }
       }
@@ -459,20 +513,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         consumer_bar();
         if (misc[2]) {
+          // last CTA of the entry: LSE-merge the partials of CTAs first..last
+          // (slots first+e .. last+e, consecutive).  The (m, l) pairs go to
+          // shared memory in one parallel pass, a warp per query head turns
+          // them into weights, then each thread sums 4 channels with 8 loads
+          // in flight.
           __threadfence();
-          for (int idx = ct; idx < G * kHeadDim; idx += kConsumerWarps * 32) {
-            const int g = idx >> 7, dd = idx & 127;
+          const int np = d.last_cta - d.first_cta + 1;
+          const size_t slot0 = (size_t)d.first_cta + d.e;
+          float2* mlb = reinterpret_cast<float2*>(merge_o);      // [np][G], np * G <= 2048
+          for (int i = ct; i < np * G; i += kConsumerWarps * 32) mlb[i] = __ldcg(&a.part_ml[slot0 * G + i]);
+          consumer_bar();
+          for (int g = warp; g < G; g += kConsumerWarps) {
             float M = NEG_INF;
-            for (int c = d.first_cta; c <= d.last_cta; ++c)
-              M = fmaxf(M, __ldcg(&a.part_ml[((size_t)c + d.e) * G + g]).x);
-            float acc = 0.f, L = 0.f;
-            for (int c = d.first_cta; c <= d.last_cta; ++c) {
-              const float2 ml = __ldcg(&a.part_ml[((size_t)c + d.e) * G + g]);
-              const float f = ml.x == NEG_INF ? 0.f : exp2f(ml.x - M);
-              acc += f * __ldcg(&a.part[(((size_t)c + d.e) * G + g) * kHeadDim + dd]);
-              L += f * ml.y;
+            for (int c = lane; c < np; c += 32) M = fmaxf(M, mlb[c * G + g].x);
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+            float L = 0.f;
+            for (int c = lane; c < np; c += 32) {
+              const float2 ml = mlb[c * G + g];
+              L += ml.x == NEG_INF ? 0.f : exp2f(ml.x - M) * ml.y;
             }
-            dst[idx] = L > 0.f ? acc / L : 0.f;
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(0xffffffffu, L, sh);
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            for (int c = lane; c < np; c += 32) {
+              const float mc = mlb[c * G + g].x;
+              mlb[c * G + g].x = mc == NEG_INF ? 0.f : exp2f(mc - M) * inv;
+            }
+          }
+          consumer_bar();
+          const float4* src = reinterpret_cast<const float4*>(a.part) + slot0 * G * 32;
+          for (int q4 = ct; q4 < G * 32; q4 += kConsumerWarps * 32) {
+            const int g = q4 >> 5;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int c = 0; c < np; ++c) {
+              const float wgt = mlb[c * G + g].x;
+              const float4 v = __ldcg(src + (size_t)c * G * 32 + q4);
+              acc.x += wgt * v.x;
+              acc.y += wgt * v.y;
+              acc.z += wgt * v.z;
+              acc.w += wgt * v.w;
+            }
+            *reinterpret_cast<float4*>(&dst[q4 * 4]) = acc;
           }
           if (ct == 0) a.counters[d.e] = 0;
         }

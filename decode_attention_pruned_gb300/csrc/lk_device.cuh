@@ -77,6 +77,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            int32_t z, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // ----------------------------------------------------- programmatic launch
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -122,13 +131,5 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
-
-// Address of 16-byte chunk `chunk` of row `row` inside a box of 64-byte rows
-// written by TMA with 64-byte swizzling (box base 512-byte aligned): the
-// chunk index is XORed with address bits 7..8, i.e. (row / 2) mod 4.
-__device__ __forceinline__ uint32_t swz64(uint32_t box_base, int row, int chunk) {
-  return box_base + static_cast<uint32_t>(row) * 64u +
-         (static_cast<uint32_t>(chunk ^ ((row >> 1) & 3)) << 4);
-}
 
 }  // namespace lk

@@ -17,8 +17,8 @@ namespace lk {
 
 constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 8;        // query heads per kv head handled by one mma n8 tile
-constexpr int kMaxCtas = 1024;      // decode grid cap (sizes the partial workspace)
-constexpr int kTmaBoxRows = 64;     // token rows per TMA box = decode tile rows
+constexpr int kMaxCtas = 256;       // decode grid cap (partial workspace; combine staging np*G <= 2048)
+constexpr int kTmaBoxRows = 128;    // token rows per TMA box = decode tile rows
 
 enum Policy : int32_t { kFull = 0, kLocal = 1, kSpecial = 2 };
 enum Pool : int32_t { kPoolK128 = 0, kPoolV = 1, kPoolK32 = 2, kPoolK64 = 3, kPoolK96 = 4, kNumPools = 5 };

@@ -181,7 +181,7 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
 lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_t* bytes);
 
 /* Override the number of CTAs of lk_decode_attn (0 = one per SM); for
- * split-invariance tests.  Must be <= 1024. */
+ * split-invariance tests.  Must be <= 256. */
 lk_status lk_set_decode_ctas(lk_cache cache, int32_t ctas);
 
 /* Synchronise `stream`, read and clear the device status word.  Returns
