@@ -295,12 +295,27 @@ def run_gpu(args, rank, local_rank, world):
     stream.synchronize()
     kdur = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
 
-    # end to end through lk_step_host: pinned host inputs, copies in the region
-    pin = lambda t: t.detach().cpu().contiguous().pin_memory()
-    hq = [pin(gq[s][0]) for s in range(bank)]
-    hk = [pin(gk[s]) for s in range(bank)]
-    hv = [pin(gv[s]) for s in range(bank)]
-    hids = [pin(gid[s]) if gid[s] is not None else None for s in range(bank)]
+    # end to end through lk_step_host: each step's inputs sit in one pinned
+    # host block (q | k | v | ids, the staging order, so one copy moves them)
+    def packed_inputs(s):
+        parts = [gq[s][0].view(torch.uint8).reshape(-1), gk[s].view(torch.uint8).reshape(-1),
+                 gv[s].view(torch.uint8).reshape(-1)]
+        if gid[s] is not None:
+            parts.append(gid[s].view(torch.uint8).reshape(-1))
+        blk = torch.cat([p.cpu() for p in parts]).pin_memory()
+        sizes = [p.numel() for p in parts]
+        offs = [sum(sizes[:i]) for i in range(len(sizes))]
+        view = lambda i, dt, shape: blk[offs[i]:offs[i] + sizes[i]].view(dt).view(shape)
+        q_h = view(0, torch.bfloat16, (B, w.num_q_heads, 128))
+        k_h = view(1, torch.bfloat16, (B, w.num_kv_heads, 128))
+        v_h = view(2, torch.bfloat16, (B, w.num_kv_heads, 128))
+        i_h = view(3, torch.int32, (B,)) if gid[s] is not None else None
+        return blk, q_h, k_h, v_h, i_h
+    packed = [packed_inputs(s) for s in range(bank)]
+    hq = [p[1] for p in packed]
+    hk = [p[2] for p in packed]
+    hv = [p[3] for p in packed]
+    hids = [p[4] for p in packed]
     ho = torch.empty((B, w.num_q_heads, 128), dtype=torch.float32).pin_memory()
     e2e_value = None
     h2d = (hq[0].numel() * 2 + hk[0].numel() * 2 + hv[0].numel() * 2 + (B * 4 if hids[0] is not None else 0)) * L

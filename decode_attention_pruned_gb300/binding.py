@@ -109,13 +109,13 @@ def _stream(stream=None):
 
 
 def _need(t, dtype, shape, what, device_kind="cuda"):
-    import torch
-    if not isinstance(t, torch.Tensor):
-        raise TypeError(f"{what} must be a torch tensor")
-    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
-        raise ValueError(f"{what}: expected contiguous {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
-    if t.device.type != device_kind:
-        raise ValueError(f"{what} must be on {device_kind}")
+    try:
+        if t.dtype is dtype and t.shape == shape and t.device.type == device_kind and t.is_contiguous():
+            return
+    except AttributeError:
+        raise TypeError(f"{what} must be a torch tensor") from None
+    raise ValueError(f"{what}: expected contiguous {dtype} {tuple(shape)} on {device_kind}, got "
+                     f"{t.dtype} {tuple(t.shape)} on {t.device.type}")
 
 
 class Plan:

@@ -17,6 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libleank.so")
 SOURCES = ["lk_api.cu", "lk_decode.cu", "lk_kv.cu"]
+# the decode kernel's exp2f / reciprocals use the hardware approximations
+PER_SOURCE = {"lk_decode.cu": ["--use_fast_math"]}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]
@@ -53,7 +55,8 @@ def build(force: bool = False, verbose: bool = False, extra: list | None = None)
     for src in SOURCES:
         obj = os.path.join(OUT, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [exe, *ARCH, *FLAGS, *(extra or []), "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [exe, *ARCH, *FLAGS, *PER_SOURCE.get(src, []), *(extra or []), "-c", os.path.join(CSRC, src),
+               "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))

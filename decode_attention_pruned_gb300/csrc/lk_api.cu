@@ -498,11 +498,23 @@ lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t qb = B * d.num_q_heads * kHeadDim * 2, kvb = B * d.num_kv_heads * kHeadDim * 2;
-  cudaError_t err = cudaMemcpyAsync(ws + w.off_q, q_host, qb, cudaMemcpyHostToDevice, s);
-  if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_k, k_host, kvb, cudaMemcpyHostToDevice, s);
-  if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_v, v_host, kvb, cudaMemcpyHostToDevice, s);
-  if (err == cudaSuccess && ids_host)
-    err = cudaMemcpyAsync(ws + w.off_ids, ids_host, B * 4, cudaMemcpyHostToDevice, s);
+  // inputs laid out back to back on the host exactly as in the workspace
+  // staging (q | k | v | ids) go over in one copy
+  const char* qh = static_cast<const char*>(q_host);
+  const bool packed = w.off_k == w.off_q + qb && w.off_v == w.off_k + kvb && w.off_ids == w.off_v + kvb &&
+                      static_cast<const char*>(k_host) == qh + qb &&
+                      static_cast<const char*>(v_host) == qh + qb + kvb &&
+                      (!ids_host || reinterpret_cast<const char*>(ids_host) == qh + qb + 2 * kvb);
+  cudaError_t err;
+  if (packed) {
+    err = cudaMemcpyAsync(ws + w.off_q, q_host, qb + 2 * kvb + (ids_host ? B * 4 : 0), cudaMemcpyHostToDevice, s);
+  } else {
+    err = cudaMemcpyAsync(ws + w.off_q, q_host, qb, cudaMemcpyHostToDevice, s);
+    if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_k, k_host, kvb, cudaMemcpyHostToDevice, s);
+    if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_v, v_host, kvb, cudaMemcpyHostToDevice, s);
+    if (err == cudaSuccess && ids_host)
+      err = cudaMemcpyAsync(ws + w.off_ids, ids_host, B * 4, cudaMemcpyHostToDevice, s);
+  }
   if (err != cudaSuccess) return cuda_fail(err, "lk_step_host: host to device copy");
   lk_status st = lk_append(cache, layer, ws + w.off_k, ws + w.off_v,
                            ids_host ? reinterpret_cast<const int32_t*>(ws + w.off_ids) : nullptr, stream);

@@ -104,21 +104,25 @@ __device__ __forceinline__ uint64_t entry_cost(const Entry& g) {
   return (uint64_t)kUnitsA * g.n_a + row_cost_b(g.kb) * g.n_b;
 }
 
+// a / b for 64-bit a with a 32-bit path when it fits
+__device__ __forceinline__ uint64_t udiv(uint64_t a, uint64_t b) {
+  if ((a >> 32) == 0 && (b >> 32) == 0) return (uint32_t)a / (uint32_t)b;
+  return a / b;
+}
+
 // Rows r in [0, n) of a region whose row r sits at line offset o0 + c*r and
 // starts inside [start, end): r in [r0, r1).
 __device__ __forceinline__ void rows_in_range(uint64_t o0, uint64_t c, int n, uint64_t start, uint64_t end,
                                               int& r0, int& r1) {
-  r0 = start > o0 ? (int)min((uint64_t)n, (start - o0 + c - 1) / c) : 0;
-  r1 = end > o0 ? (int)min((uint64_t)n, (end - o0 + c - 1) / c) : 0;
+  r0 = start > o0 ? (int)min((uint64_t)n, udiv(start - o0 + c - 1, c)) : 0;
+  r1 = end > o0 ? (int)min((uint64_t)n, udiv(end - o0 + c - 1, c)) : 0;
 }
 
-// Largest CTA index i < P with floor(i*C/P) <= x.
+// The CTA whose range [floor(iC/P), floor((i+1)C/P)) holds offset x < C:
+// floor(iC/P) <= x  <=>  iC < (x+1)P, so i = ceil((x+1)P/C) - 1.
 __device__ __forceinline__ int range_owner(uint64_t x, uint64_t C, int P) {
-  uint64_t i = C ? (x * (uint64_t)P) / C : 0;
-  if (i > (uint64_t)P - 1) i = P - 1;
-  while (i + 1 < (uint64_t)P && ((i + 1) * C) / P <= x) ++i;
-  while (i > 0 && (i * C) / P > x) --i;
-  return (int)i;
+  const uint64_t i = udiv((x + 1) * (uint64_t)P - 1, C);
+  return (int)min(i, (uint64_t)P - 1);
 }
 
 __device__ __forceinline__ void consumer_bar() {
@@ -248,8 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = e / cv.Hkv, h = e - b * cv.Hkv;
           const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
           const uint64_t last_row_off = g.n_b > 0 ? off_b + cb * (g.n_b - 1) : off + (uint64_t)kUnitsA * (g.n_a - 1);
-          const int fc = range_owner(off, C, P);
-          const int lc = range_owner(last_row_off, C, P);
+          // the entry's first / last owning CTA is read only from the segment's
+          // last descriptor: work it out after the first load is in flight
+          int fc = -1, lc = -1;
+          if (nta + ntb == 1) {
+            fc = range_owner(off, C, P);
+            lc = range_owner(last_row_off, C, P);
+          }
           for (int j = 0; j < nta + ntb; ++j) {
             if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, a.wait_limit_ns)) {
               ok = false;
@@ -285,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 default: tma_load_3d(kdst, &tm_k128, 0, krow, 0, fb, policy); break;
               }
               tma_load_3d(vdst, &tm_v, 0, vrow, 0, fb, policy);
+            }
+            if (fc < 0) {
+              fc = range_owner(off, C, P);
+              lc = range_owner(last_row_off, C, P);
             }
             if (++stage == kStages) {
               stage = 0;
@@ -514,49 +527,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         consumer_bar();
         if (misc[2]) {
           // last CTA of the entry: LSE-merge the partials of CTAs first..last
-          // (slots first+e .. last+e, consecutive).  The (m, l) pairs go to
-          // shared memory in one parallel pass, a warp per query head turns
-          // them into weights, then each thread sums 4 channels with 8 loads
-          // in flight.
+          // (slots first+e .. last+e, consecutive), one running (M, L, acc)
+          // per 4 output channels; each chunk of 16 partials issues all its
+          // (m, l) and o loads before using any.
           __threadfence();
           const int np = d.last_cta - d.first_cta + 1;
           const size_t slot0 = (size_t)d.first_cta + d.e;
-          float2* mlb = reinterpret_cast<float2*>(merge_o);      // [np][G], np * G <= 2048
-          for (int i = ct; i < np * G; i += kConsumerWarps * 32) mlb[i] = __ldcg(&a.part_ml[slot0 * G + i]);
-          consumer_bar();
-          for (int g = warp; g < G; g += kConsumerWarps) {
-            float M = NEG_INF;
-            for (int c = lane; c < np; c += 32) M = fmaxf(M, mlb[c * G + g].x);
-#pragma unroll
-            for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
-            float L = 0.f;
-            for (int c = lane; c < np; c += 32) {
-              const float2 ml = mlb[c * G + g];
-              L += ml.x == NEG_INF ? 0.f : exp2f(ml.x - M) * ml.y;
-            }
-#pragma unroll
-            for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(0xffffffffu, L, sh);
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            for (int c = lane; c < np; c += 32) {
-              const float mc = mlb[c * G + g].x;
-              mlb[c * G + g].x = mc == NEG_INF ? 0.f : exp2f(mc - M) * inv;
-            }
-          }
-          consumer_bar();
           const float4* src = reinterpret_cast<const float4*>(a.part) + slot0 * G * 32;
           for (int q4 = ct; q4 < G * 32; q4 += kConsumerWarps * 32) {
             const int g = q4 >> 5;
+            float M = NEG_INF, L = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int c = 0; c < np; ++c) {
-              const float wgt = mlb[c * G + g].x;
-              const float4 v = __ldcg(src + (size_t)c * G * 32 + q4);
-              acc.x += wgt * v.x;
-              acc.y += wgt * v.y;
-              acc.z += wgt * v.z;
-              acc.w += wgt * v.w;
+            for (int c0 = 0; c0 < np; c0 += 16) {
+              float2 ml[16];
+              float4 v[16];
+#pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const int c = min(c0 + u, np - 1);
+                ml[u] = __ldcg(&a.part_ml[(slot0 + c) * G + g]);
+                v[u] = __ldcg(src + (size_t)c * G * 32 + q4);
+              }
+              float Mn = M;
+#pragma unroll
+              for (int u = 0; u < 16; ++u)
+                if (c0 + u < np) Mn = fmaxf(Mn, ml[u].x);
+              const float sc = M == NEG_INF ? 0.f : exp2f(M - Mn);
+              L *= sc;
+              acc.x *= sc;
+              acc.y *= sc;
+              acc.z *= sc;
+              acc.w *= sc;
+#pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const float f = (c0 + u < np && ml[u].x != NEG_INF) ? exp2f(ml[u].x - Mn) : 0.f;
+                L += f * ml[u].y;
+                acc.x += f * v[u].x;
+                acc.y += f * v[u].y;
+                acc.z += f * v[u].z;
+                acc.w += f * v[u].w;
+              }
+              M = Mn;
             }
-            *reinterpret_cast<float4*>(&dst[q4 * 4]) = acc;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            *reinterpret_cast<float4*>(&dst[q4 * 4]) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
           }
           if (ct == 0) a.counters[d.e] = 0;
         }

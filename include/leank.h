@@ -164,7 +164,8 @@ lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
  * k, v [B][Hkv][128] bf16 and ids [B] int32 (NULL allowed) from host to the
  * workspace, runs lk_append then lk_decode_attn, and copies o [B][Hq][128]
  * fp32 back to host.  Host buffers should be pinned for the copies to be
- * asynchronous; read o only after synchronising `stream`. */
+ * asynchronous; read o only after synchronising `stream`.  When q, k, v
+ * (and ids) are adjacent in host memory in that order, one copy moves them. */
 lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const void* k_host,
                        const void* v_host, const int32_t* ids_host, float* o_host,
                        void* workspace, size_t ws_bytes, void* stream);
