@@ -50,6 +50,7 @@ SIGNATURES = {
     "lk_prefill": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
     "lk_append": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp]),
     "lk_decode_attn": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "lk_decode_attn_static": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp]),
     "lk_step_host": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lk_cache_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i32)]),
     "lk_cache_region": (ctypes.c_int, [_vp, _i32, _i32, _i32, ctypes.POINTER(RegionInfo)]),
@@ -218,6 +219,17 @@ class Cache:
         _need(o, torch.float32, (B, Hq, 128), "o")
         _check(_lib.lk_decode_attn(self._h, layer, q.data_ptr(), o.data_ptr(), self.workspace.data_ptr(),
                                    self.workspace.numel(), _stream(stream)))
+        return o
+
+    def decode_static(self, layer, q, o, stream=None):
+        """lk_decode_attn_static: decode with the library's built-in split
+        scratch instead of this cache's workspace (no allocation in the call;
+        `o` must be given).  Calls must not overlap on the GPU."""
+        import torch
+        B, Hq = self.batch, self.plan.num_q_heads
+        _need(q, torch.bfloat16, (B, Hq, 128), "q")
+        _need(o, torch.float32, (B, Hq, 128), "o")
+        _check(_lib.lk_decode_attn_static(self._h, layer, q.data_ptr(), o.data_ptr(), _stream(stream)))
         return o
 
     def step_host(self, layer, q, k, v, ids, o, stream=None):

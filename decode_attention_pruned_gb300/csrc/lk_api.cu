@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <mutex>
 #include <vector>
 
 #include "../../include/leank.h"
@@ -169,6 +170,41 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Scratch of lk_decode_attn_static: the split counters and partials live in
+// this fixed device array instead of a caller workspace, for callers that may
+// not allocate device memory.  Every GPU that loads the library holds it
+// until the process exits; all calls share it.
+namespace {
+constexpr size_t kStaticScratchBytes = 8u << 20;
+constexpr int kStaticMaxDevices = 64;
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kStaticMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device, looked up (and
+// zeroed) once per device.  Host code must not use the symbol itself: on the
+// host it names a stand-in, not device memory.
+lk_status static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static: cudaGetDevice");
+  if (dev < 0 || dev >= kStaticMaxDevices)
+    return fail(LK_ERR_UNSUPPORTED, "lk_decode_attn_static: device %d >= %d", dev, kStaticMaxDevices);
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    err = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static: cudaGetSymbolAddress");
+    err = cudaMemset(ptr, 0, kStaticScratchBytes);
+    if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static: scratch clear");
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return LK_OK;
+}
 }  // namespace
 
 struct lk_cache_s {
@@ -612,6 +648,46 @@ lk_status lk_check(lk_cache cache, void* stream) {
   if (status & kStatusCapacity)
     return fail(LK_ERR_CAPACITY, "a layer or a SPECIAL head ran out of rows (status 0x%x)", status);
   return fail(LK_ERR_ARG, "a token id was outside [0, vocab) (status 0x%x)", status);
+}
+
+lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, float* o, void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_decode_attn_static: null cache");
+  if (layer < 0 || layer >= cache->cv.L)
+    return fail(LK_ERR_ARG, "lk_decode_attn_static: layer %d out of range", layer);
+  if (!q || !o) return fail(LK_ERR_ARG, "lk_decode_attn_static: null q or o");
+  if (!aligned(q, 16) || !aligned(o, 16))
+    return fail(LK_ERR_ALIGN, "lk_decode_attn_static: q and o must be 16-byte aligned");
+  // counters + partial (m, l) + partial o; the host staging of lk_step_host is not needed
+  const WsLayout w = ws_layout(cache->plan.d, cache->B);
+  const size_t need = w.off_q;
+  if (need > kStaticScratchBytes)
+    return fail(LK_ERR_CAPACITY,
+                "lk_decode_attn_static: this cache needs %zu bytes of split scratch; the built-in array has %zu "
+                "(batch x kv heads too large; use lk_decode_attn with a workspace)",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  lk_status st = static_scratch(&scratch);
+  if (st != LK_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the counters must start at zero whatever an earlier call left behind
+  cudaError_t err = cudaMemsetAsync(ws + w.off_counters, 0, (size_t)cache->B * cache->cv.Hkv * 4, s);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static: counter clear");
+  DecodeArgs a;
+  a.cv = cache->cv;
+  a.layer = layer;
+  a.q = static_cast<const uint16_t*>(q);
+  a.o = o;
+  a.part = reinterpret_cast<float*>(ws + w.off_part);
+  a.part_ml = reinterpret_cast<float2*>(ws + w.off_ml);
+  a.counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
+  a.wait_limit_ns = kWaitLimitNs;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
+  int ctas = cache->decode_ctas > 0 ? cache->decode_ctas : cache->num_sms;
+  ctas = std::max(1, std::min(ctas, kMaxCtas));
+  err = launch_decode(cache->maps, a, ctas, s);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static launch");
+  return LK_OK;
 }
 
 }  // extern "C"

@@ -160,6 +160,26 @@ lk_status lk_append(lk_cache cache, int32_t layer, const void* k, const void* v,
 lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
                          void* workspace, size_t ws_bytes, void* stream);
 
+/* lk_decode_attn without a caller workspace.  The pages have no counterpart:
+ * this is a library convenience.  Some callers cannot call cudaMalloc at all
+ * -- a plugin running inside a host runtime that owns the device allocator
+ * and its memory accounting, or a latency-critical loop where an allocation
+ * would synchronise the device -- and so cannot provide the split workspace.
+ * This entry point keeps the split counters and partials in a fixed 8 MiB
+ * device array built into the library (a file-scope __device__ array that
+ * every GPU loading the library holds until the process exits); it
+ * allocates nothing.
+ *   q, o  as for lk_decode_attn.
+ * Limit: the split scratch of the cache (about (256 + B*Hkv) * G * 520
+ * bytes) must fit in 8 MiB, else LK_ERR_CAPACITY and nothing is enqueued.
+ * The first call on a device looks up the array's device address and zeroes
+ * it (synchronously); make that first call before any stream capture.  Each
+ * call then clears the split counters on `stream` before its launch.  All
+ * calls share the one array and it keeps the last call's contents: calls
+ * that overlap on the GPU (other streams, other threads) race and give wrong
+ * results. */
+lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, float* o, void* stream);
+
 /* One decode step end to end from host memory: copies q [B][Hq][128] bf16,
  * k, v [B][Hkv][128] bf16 and ids [B] int32 (NULL allowed) from host to the
  * workspace, runs lk_append then lk_decode_attn, and copies o [B][Hq][128]
