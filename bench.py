@@ -17,7 +17,7 @@ dependent launch between append and decode).
 Printed: one JSON line (rank 0).  `value` = decode-attention calls/s of all
 ranks; `roofline` = the decode kernel's algorithmic bytes / its event-timed
 launch duration against the HBM peak; `e2e` = the same metric through
-lk_step_host from pinned host buffers (copies inside the timed region);
+lk_step_host_packed from pinned host memory (copies inside the timed region);
 `cpu_baseline` = the fp64 oracle on a bounded sample on the host cores.
 
 --impl reference times the oracle (the only reference this method has) on
@@ -295,8 +295,8 @@ def run_gpu(args, rank, local_rank, world):
     stream.synchronize()
     kdur = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
 
-    # end to end through lk_step_host: each step's inputs sit in one pinned
-    # host block (q | k | v | ids, the staging order, so one copy moves them)
+    # end to end through lk_step_host_packed: each step's inputs sit in one
+    # pinned host block (q | k | v | ids) moved by one copy
     def packed_inputs(s):
         parts = [gq[s][0].view(torch.uint8).reshape(-1), gk[s].view(torch.uint8).reshape(-1),
                  gv[s].view(torch.uint8).reshape(-1)]
@@ -323,10 +323,10 @@ def run_gpu(args, rank, local_rank, world):
     if L == 1:
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with_ids = hids[0] is not None
         e0.record(stream)
         for i in range(e2e_steps):
-            s = i % bank
-            caches[i % copies].step_host(0, hq[s], hk[s], hv[s], hids[s], ho, stream=stream)
+            caches[i % copies].step_host_packed(0, packed[i % bank][0], with_ids, ho, stream=stream)
         e1.record(stream)
         e1.synchronize()
         e2e_elapsed = e0.elapsed_time(e1) / 1e3

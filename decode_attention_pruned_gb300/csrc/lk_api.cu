@@ -519,6 +519,23 @@ lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
   return LK_OK;
 }
 
+// Append + decode from the inputs staged in the workspace, then copy o back.
+static lk_status step_from_staging(lk_cache cache, int32_t layer, bool has_ids, float* o_host, void* workspace,
+                            size_t ws_bytes, void* stream) {
+  const WsLayout w = ws_layout(cache->plan.d, cache->B);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  lk_status st = lk_append(cache, layer, ws + w.off_k, ws + w.off_v,
+                           has_ids ? reinterpret_cast<const int32_t*>(ws + w.off_ids) : nullptr, stream);
+  if (st != LK_OK) return st;
+  float* o_dev = reinterpret_cast<float*>(ws + w.off_o);
+  st = lk_decode_attn(cache, layer, ws + w.off_q, o_dev, workspace, ws_bytes, stream);
+  if (st != LK_OK) return st;
+  const size_t ob = (size_t)cache->B * cache->plan.d.num_q_heads * kHeadDim * 4;
+  cudaError_t err = cudaMemcpyAsync(o_host, o_dev, ob, cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_step_host: device to host copy");
+  return LK_OK;
+}
+
 lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const void* k_host, const void* v_host,
                        const int32_t* ids_host, float* o_host, void* workspace, size_t ws_bytes, void* stream) {
   if (!cache || !q_host || !k_host || !v_host || !o_host || !workspace)
@@ -534,33 +551,35 @@ lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t qb = B * d.num_q_heads * kHeadDim * 2, kvb = B * d.num_kv_heads * kHeadDim * 2;
-  // inputs laid out back to back on the host exactly as in the workspace
-  // staging (q | k | v | ids) go over in one copy
-  const char* qh = static_cast<const char*>(q_host);
-  const bool packed = w.off_k == w.off_q + qb && w.off_v == w.off_k + kvb && w.off_ids == w.off_v + kvb &&
-                      static_cast<const char*>(k_host) == qh + qb &&
-                      static_cast<const char*>(v_host) == qh + qb + kvb &&
-                      (!ids_host || reinterpret_cast<const char*>(ids_host) == qh + qb + 2 * kvb);
-  cudaError_t err;
-  if (packed) {
-    err = cudaMemcpyAsync(ws + w.off_q, q_host, qb + 2 * kvb + (ids_host ? B * 4 : 0), cudaMemcpyHostToDevice, s);
-  } else {
-    err = cudaMemcpyAsync(ws + w.off_q, q_host, qb, cudaMemcpyHostToDevice, s);
-    if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_k, k_host, kvb, cudaMemcpyHostToDevice, s);
-    if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_v, v_host, kvb, cudaMemcpyHostToDevice, s);
-    if (err == cudaSuccess && ids_host)
-      err = cudaMemcpyAsync(ws + w.off_ids, ids_host, B * 4, cudaMemcpyHostToDevice, s);
-  }
+  cudaError_t err = cudaMemcpyAsync(ws + w.off_q, q_host, qb, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_k, k_host, kvb, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(ws + w.off_v, v_host, kvb, cudaMemcpyHostToDevice, s);
+  if (err == cudaSuccess && ids_host)
+    err = cudaMemcpyAsync(ws + w.off_ids, ids_host, B * 4, cudaMemcpyHostToDevice, s);
   if (err != cudaSuccess) return cuda_fail(err, "lk_step_host: host to device copy");
-  lk_status st = lk_append(cache, layer, ws + w.off_k, ws + w.off_v,
-                           ids_host ? reinterpret_cast<const int32_t*>(ws + w.off_ids) : nullptr, stream);
-  if (st != LK_OK) return st;
-  float* o_dev = reinterpret_cast<float*>(ws + w.off_o);
-  st = lk_decode_attn(cache, layer, ws + w.off_q, o_dev, workspace, ws_bytes, stream);
-  if (st != LK_OK) return st;
-  err = cudaMemcpyAsync(o_host, o_dev, B * d.num_q_heads * kHeadDim * 4, cudaMemcpyDeviceToHost, s);
-  if (err != cudaSuccess) return cuda_fail(err, "lk_step_host: device to host copy");
-  return LK_OK;
+  return step_from_staging(cache, layer, ids_host != nullptr, o_host, workspace, ws_bytes, stream);
+}
+
+lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in, int32_t has_ids, float* o_host,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  if (!cache || !host_in || !o_host || !workspace) return fail(LK_ERR_ARG, "lk_step_host_packed: null argument");
+  const WsLayout w = ws_layout(cache->plan.d, cache->B);
+  if (ws_bytes < w.total)
+    return fail(LK_ERR_CAPACITY, "lk_step_host_packed: workspace has %zu bytes; %zu needed", ws_bytes, w.total);
+  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_step_host_packed: layer %d out of range", layer);
+  if (cache->host_len[layer] >= cache->cap)
+    return fail(LK_ERR_CAPACITY, "lk_step_host_packed: layer %d is full (%d tokens)", layer, cache->cap);
+  const lk_plan_desc& d = cache->plan.d;
+  const size_t B = cache->B;
+  const size_t qb = B * d.num_q_heads * kHeadDim * 2, kvb = B * d.num_kv_heads * kHeadDim * 2;
+  const size_t bytes = qb + 2 * kvb + (has_ids ? B * 4 : 0);
+  // the staging areas q | k | v | ids are adjacent in the workspace
+  if (w.off_k != w.off_q + qb || w.off_v != w.off_k + kvb || w.off_ids != w.off_v + kvb)
+    return fail(LK_ERR_UNSUPPORTED, "lk_step_host_packed: staging areas are not adjacent");
+  cudaError_t err = cudaMemcpyAsync(static_cast<uint8_t*>(workspace) + w.off_q, host_in, bytes, cudaMemcpyHostToDevice,
+                                    static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_step_host_packed: host to device copy");
+  return step_from_staging(cache, layer, has_ids != 0, o_host, workspace, ws_bytes, stream);
 }
 
 lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n) {

@@ -42,9 +42,11 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileRows = kTmaBoxRows;                  // 128 tokens per stage
 constexpr int kSubPerWarp = kTileRows / 16 / kConsumerWarps;   // m16 row blocks per warp
 static_assert(kSubPerWarp == 2, "two 16-row blocks per consumer warp");
-constexpr int kStages = 3;
-constexpr int kSlotBytes = kTileRows * 256;             // one full-width tile (32 KB)
-constexpr int kStageBytes = 2 * kSlotBytes;             // K slot + V slot
+// Stages live in a byte ring: a stage holds a K tile (128 rows x width) and a
+// V tile (128 rows x 128), so narrow-K tiles (40 KB at k = 32) keep five
+// stages in flight where full-width ones (64 KB) keep three.
+constexpr int kSlots = 6;                               // barrier pairs = stages in flight at most
+constexpr int kRingBytes = 208 * 1024;
 constexpr int kUnitsA = 16;                             // cost per full-width row (512 B / 32)
 constexpr int kFirst = 1, kLast = 2;
 
@@ -56,21 +58,24 @@ struct StageDesc {
   int32_t flags;       // kFirst / kLast of this CTA's segment of the entry
   int32_t first_cta;   // CTAs first..last hold partials of the entry
   int32_t last_cta;
-  int32_t pad;
+  uint32_t koff;       // ring offset of the K tile; the V tile follows it
 };
 
 struct SmemLayout {
-  static constexpr int kStagesOff = 0;
-  static constexpr int kMergeOOff = kStagesOff + kStages * kStageBytes;
+  static constexpr int kRingOff = 0;
+  static constexpr int kMergeOOff = kRingOff + kRingBytes;
   static constexpr int kMergeMOff = kMergeOOff + kConsumerWarps * kMaxGroup * kHeadDim * 4;
   static constexpr int kMergeLOff = kMergeMOff + kConsumerWarps * kMaxGroup * 4;
   static constexpr int kDescOff = kMergeLOff + kConsumerWarps * kMaxGroup * 4;
-  static constexpr int kBarOff = kDescOff + kStages * (int)sizeof(StageDesc);
-  static constexpr int kScanOff = kBarOff + 2 * kStages * 8;
+  static constexpr int kBarOff = kDescOff + kSlots * (int)sizeof(StageDesc);
+  static constexpr int kScanOff = kBarOff + 2 * kSlots * 8;
   static constexpr int kMiscOff = kScanOff + (kThreads / 32) * 8;
   static constexpr int kBytes = kMiscOff + 64;
 };
 constexpr int kSmemBytes = SmemLayout::kBytes + 1024;   // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
+
+__device__ __forceinline__ uint32_t stage_bytes(int width) { return (uint32_t)kTileRows * (2 * width + 256); }
 
 struct Entry {
   int n_a, n_b, kb;
@@ -163,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* merge_l = reinterpret_cast<float*>(sm + SmemLayout::kMergeLOff);
   StageDesc* desc = reinterpret_cast<StageDesc*>(sm + SmemLayout::kDescOff);
   const uint32_t bar_full = base + SmemLayout::kBarOff;
-  const uint32_t bar_empty = bar_full + kStages * 8;
+  const uint32_t bar_empty = bar_full + kSlots * 8;
   uint64_t* scan = reinterpret_cast<uint64_t*>(sm + SmemLayout::kScanOff);
   volatile int64_t* misc = reinterpret_cast<volatile int64_t*>(sm + SmemLayout::kMiscOff);
 
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = cv.G;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, kConsumerWarps);
     }
@@ -187,7 +192,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tm_v);
     tma_prefetch_map(&tm_k32);
   }
-  // lengths and special counts are written by the preceding append
+  // the layer's head table is static: pull it towards L1 while the preceding
+  // kernel finishes (lengths and special counts are written by that append,
+  // so they are read only after the dependency wait)
+  for (int h = tid; h < cv.Hkv; h += kThreads)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(&cv.heads[a.layer * cv.Hkv + h]));
+  const uint64_t policy = l2_policy_evict_first();
   grid_dependency_wait();
   grid_launch_dependents();
 
@@ -232,10 +242,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     // ================================================================ producer
     if (lane == 0) {
-      const uint64_t policy = l2_policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
+      uint32_t issued = 0, freed = 0;     // stages issued / known released
+      uint32_t head = 0;                   // next free ring byte
       bool ok = true;
+      // Wait (bounded) until the oldest in-flight stage is released.
+      auto free_oldest = [&]() -> bool {
+        const uint32_t slot = freed % kSlots;
+        if (!mbar_wait_bounded(bar_empty + 8 * slot, (freed / kSlots) & 1u, a.wait_limit_ns)) return false;
+        ++freed;
+        return true;
+      };
+      // Ring offset for a stage of `bytes`, once a slot is free and no
+      // in-flight stage overlaps it.
+      auto reserve = [&](uint32_t bytes, uint32_t& at) -> bool {
+        at = head + bytes <= (uint32_t)kRingBytes ? head : 0u;
+        while (issued != freed) {
+          bool clash = issued - freed == (uint32_t)kSlots;
+          for (uint32_t m = freed; !clash && m != issued; ++m) {
+            const StageDesc& o = desc[m % kSlots];
+            const uint32_t ob = stage_bytes(o.width);
+            clash = at < o.koff + ob && o.koff < at + bytes;
+          }
+          if (!clash) break;
+          if (!free_oldest()) return false;
+        }
+        head = at + bytes;
+        return true;
+      };
       int e = (int)misc[0];
       uint64_t off = (uint64_t)misc[1];
       for (; ok && e < E && off < end; ++e) {
@@ -260,11 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             lc = range_owner(last_row_off, C, P);
           }
           for (int j = 0; j < nta + ntb; ++j) {
-            if (!mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, a.wait_limit_ns)) {
+            const bool in_a = j < nta;
+            const int width = in_a ? kHeadDim : g.kb;
+            uint32_t at = 0;
+            if (!reserve(stage_bytes(width), at)) {
               ok = false;
               break;
             }
-            const bool in_a = j < nta;
+            const uint32_t stage = issued % kSlots;
             const int r = in_a ? a0 + j * kTileRows : b0 + (j - nta) * kTileRows;
             StageDesc d;
             d.e = e;
@@ -274,12 +310,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             d.flags = (j == 0 ? kFirst : 0) | (j + 1 == nta + ntb ? kLast : 0);
             d.first_cta = fc;
             d.last_cta = lc;
-            d.pad = 0;
+            d.koff = at;
             desc[stage] = d;
             const uint32_t fb = bar_full + 8 * stage;
-            mbar_arrive_expect_tx(fb, (uint32_t)kTileRows * (2 * d.width + 256));
-            const uint32_t kdst = base + SmemLayout::kStagesOff + stage * kStageBytes;
-            const uint32_t vdst = kdst + kSlotBytes;
+            mbar_arrive_expect_tx(fb, stage_bytes(width));
+            const uint32_t kdst = base + SmemLayout::kRingOff + at;
+            const uint32_t vdst = kdst + (uint32_t)kTileRows * 2 * width;
             if (in_a) {
               const int32_t row = (int32_t)(hd.row_a + (int64_t)b * hd.cap_a + r);
               tma_load_3d(kdst, &tm_k128, 0, row, 0, fb, policy);
@@ -295,19 +331,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               tma_load_3d(vdst, &tm_v, 0, vrow, 0, fb, policy);
             }
+            ++issued;
             if (fc < 0) {
               fc = range_owner(off, C, P);
               lc = range_owner(last_row_off, C, P);
-            }
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1u;
             }
           }
         }
         off += cost;
       }
-      if (ok && mbar_wait_bounded(bar_empty + 8 * stage, phase ^ 1u, a.wait_limit_ns)) {
+      // end of stream: a descriptor with e < 0 in the next slot
+      if (ok && issued - freed == (uint32_t)kSlots) ok = free_oldest();
+      if (ok) {
+        const uint32_t stage = issued % kSlots;
         desc[stage].e = -1;
         mbar_arrive(bar_full + 8 * stage);
       } else {
@@ -381,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this warp's two 16-row blocks of the tile: rows 16*(warp + 4j)
     const int nv0 = d.nrows - 16 * warp;
     if (nv0 > 0) {
-      const uint32_t kbase = base + SmemLayout::kStagesOff + stage * kStageBytes;
-      const uint32_t vbase = kbase + kSlotBytes;
+      const uint32_t kbase = base + SmemLayout::kRingOff + d.koff;
+      const uint32_t vbase = kbase + (uint32_t)kTileRows * 2 * d.width;
       const bool in_a = d.region == 0;
       const bool fam128 = (d.width & 63) == 0;          // widths 64 / 128 use 128-byte rows
       const int nks = d.width >> 4;
@@ -527,56 +563,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         consumer_bar();
         if (misc[2]) {
           // last CTA of the entry: LSE-merge the partials of CTAs first..last
-          // (slots first+e .. last+e, consecutive), one running (M, L, acc)
-          // per 4 output channels; each chunk of 16 partials issues all its
-          // (m, l) and o loads before using any.
+          // (slots first+e .. last+e, consecutive).  Each thread owns 4 output
+          // channels: it issues the o loads of its first chunk of partials
+          // while the (m, l) pairs are staged into shared memory, so a chunk
+          // costs one round trip; a warp per query head turns the pairs into
+          // weights w_c = 2^(m_c - M) / L.
           __threadfence();
           const int np = d.last_cta - d.first_cta + 1;
           const size_t slot0 = (size_t)d.first_cta + d.e;
           const float4* src = reinterpret_cast<const float4*>(a.part) + slot0 * G * 32;
-          for (int q4 = ct; q4 < G * 32; q4 += kConsumerWarps * 32) {
-            const int g = q4 >> 5;
-            float M = NEG_INF, L = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int c0 = 0; c0 < np; c0 += 16) {
-              float2 ml[16];
-              float4 v[16];
+          float2* mlb = reinterpret_cast<float2*>(merge_o);      // [np][G], np * G <= 2048
+          constexpr int kChunk = 20;
+          const int q4a = ct, q4b = ct + kConsumerWarps * 32;  // G * 32 <= 256 outputs
+          float4 v[kChunk];
 #pragma unroll
-              for (int u = 0; u < 16; ++u) {
-                const int c = min(c0 + u, np - 1);
-                ml[u] = __ldcg(&a.part_ml[(slot0 + c) * G + g]);
-                v[u] = __ldcg(src + (size_t)c * G * 32 + q4);
-              }
-              float Mn = M;
+          for (int u = 0; u < kChunk; ++u) {
+            const int c = min(u, np - 1);
+            v[u] = q4a < G * 32 ? __ldcg(src + (size_t)c * G * 32 + q4a) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          for (int i = ct; i < np * G; i += kConsumerWarps * 32) mlb[i] = __ldcg(&a.part_ml[slot0 * G + i]);
+          consumer_bar();
+          for (int g = warp; g < G; g += kConsumerWarps) {
+            float M = NEG_INF;
+            for (int c = lane; c < np; c += 32) M = fmaxf(M, mlb[c * G + g].x);
 #pragma unroll
-              for (int u = 0; u < 16; ++u)
-                if (c0 + u < np) Mn = fmaxf(Mn, ml[u].x);
-              const float sc = M == NEG_INF ? 0.f : exp2f(M - Mn);
-              L *= sc;
-              acc.x *= sc;
-              acc.y *= sc;
-              acc.z *= sc;
-              acc.w *= sc;
-#pragma unroll
-              for (int u = 0; u < 16; ++u) {
-                const float f = (c0 + u < np && ml[u].x != NEG_INF) ? exp2f(ml[u].x - Mn) : 0.f;
-                L += f * ml[u].y;
-                acc.x += f * v[u].x;
-                acc.y += f * v[u].y;
-                acc.z += f * v[u].z;
-                acc.w += f * v[u].w;
-              }
-              M = Mn;
+            for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
+            float L = 0.f;
+            for (int c = lane; c < np; c += 32) {
+              const float2 ml = mlb[c * G + g];
+              L += ml.x == NEG_INF ? 0.f : exp2f(ml.x - M) * ml.y;
             }
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(0xffffffffu, L, sh);
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            *reinterpret_cast<float4*>(&dst[q4 * 4]) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            __syncwarp();
+            for (int c = lane; c < np; c += 32) {
+              const float mc = mlb[c * G + g].x;
+              mlb[c * G + g].x = mc == NEG_INF ? 0.f : exp2f(mc - M) * inv;
+            }
+          }
+          consumer_bar();
+          for (int pass = 0; pass < 2; ++pass) {
+            const int q4 = pass == 0 ? q4a : q4b;
+            if (q4 >= G * 32) continue;
+            const int g = q4 >> 5;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int c0 = 0; c0 < np; c0 += kChunk) {
+              if (pass == 1 || c0 > 0) {
+#pragma unroll
+                for (int u = 0; u < kChunk; ++u)
+                  v[u] = __ldcg(src + (size_t)min(c0 + u, np - 1) * G * 32 + q4);
+              }
+#pragma unroll
+              for (int u = 0; u < kChunk; ++u) {
+                const float wgt = c0 + u < np ? mlb[(c0 + u) * G + g].x : 0.f;
+                acc.x += wgt * v[u].x;
+                acc.y += wgt * v[u].y;
+                acc.z += wgt * v[u].z;
+                acc.w += wgt * v[u].w;
+              }
+            }
+            *reinterpret_cast<float4*>(&dst[q4 * 4]) = acc;
           }
           if (ct == 0) a.counters[d.e] = 0;
         }
       }
       consumer_bar();
     }
-    if (++stage == kStages) {
+    if (++stage == kSlots) {
       stage = 0;
       phase ^= 1u;
     }

@@ -184,11 +184,17 @@ lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, fl
  * k, v [B][Hkv][128] bf16 and ids [B] int32 (NULL allowed) from host to the
  * workspace, runs lk_append then lk_decode_attn, and copies o [B][Hq][128]
  * fp32 back to host.  Host buffers should be pinned for the copies to be
- * asynchronous; read o only after synchronising `stream`.  When q, k, v
- * (and ids) are adjacent in host memory in that order, one copy moves them. */
+ * asynchronous; read o only after synchronising `stream`. */
 lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const void* k_host,
                        const void* v_host, const int32_t* ids_host, float* o_host,
                        void* workspace, size_t ws_bytes, void* stream);
+
+/* lk_step_host with the step's inputs in one host block, moved by a single
+ * copy: host_in = q bf16 [B][Hq][128] | k bf16 [B][Hkv][128] | v bf16
+ * [B][Hkv][128] | ids int32 [B] (present iff has_ids != 0), back to back.
+ * The block should be one pinned allocation. */
+lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in, int32_t has_ids,
+                              float* o_host, void* workspace, size_t ws_bytes, void* stream);
 
 /* Host-tracked token count of a layer (tokens appended or prefilled). */
 lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n);
