@@ -208,26 +208,30 @@ def run_gpu(args, rank, local_rank, world):
     hist = None
     torch.cuda.synchronize()
 
-    # per-step inputs (a bank cycled through), resident before timing
+    # per-step inputs (a bank cycled through), resident before timing:
+    # q [L, B, Hq, 128]; the new token's k, v [L, B, Hkv, 128]
     bank = 16
-    gq = [[S.make_q(w, l, N - 1, device=dev, step=s) for l in range(L)] for s in range(bank)]
+    gq = [torch.stack([S.make_q(w, l, N - 1, device=dev, step=s) for l in range(L)]).contiguous()
+          for s in range(bank)]
     gk, gv = [], []
     for s in range(bank):
-        kk, vv = S.make_kv(w.scaled(seed=w.seed + 7919 * (s + 1)), 0, 1, device=dev)
-        gk.append(kk[:, 0].contiguous())
-        gv.append(vv[:, 0].contiguous())
+        kk, vv = S.make_kv(w.scaled(seed=w.seed + 7919 * (s + 1), num_layers=1, batch=L * B), 0, 1, device=dev)
+        gk.append(kk[:, 0].reshape(L, B, w.num_kv_heads, 128).contiguous())
+        gv.append(vv[:, 0].reshape(L, B, w.num_kv_heads, 128).contiguous())
     gid = [torch.zeros(B, dtype=torch.int32, device=dev) + (s * 37) % max(1, w.vocab) for s in range(bank)] \
         if len(spec) else [None] * bank
-    outs = [torch.empty((B, w.num_q_heads, 128), dtype=torch.float32, device=dev) for _ in range(copies)]
+    outs = [torch.empty((L, B, w.num_q_heads, 128), dtype=torch.float32, device=dev) for _ in range(copies)]
 
     stream = torch.cuda.Stream(device=dev)
 
+    # one step: the new token into every layer (one launch), then decode
+    # attention of every layer (one launch; for one layer these are the plain
+    # per-layer calls)
     def enqueue_step(i):
         c = caches[i % copies]
         s = i % bank
-        for l in range(L):
-            c.append(l, gk[s], gv[s], gid[s], stream=stream)
-            c.decode(l, gq[s][l], outs[i % copies], stream=stream)
+        c.append_layers(0, gk[s], gv[s], gid[s], stream=stream)
+        c.decode_layers(0, gq[s], outs[i % copies], stream=stream)
 
     # graphs of whole rotations (copies steps) plus one of the remainder
     def capture(n_steps, start):
@@ -290,16 +294,16 @@ def run_gpu(args, rank, local_rank, world):
         for i in range(kt_steps):
             c = caches[i % copies]
             starts[i].record(stream)
-            c.decode(0, gq[i % bank][0], outs[i % copies], stream=stream)
+            c.decode_layers(0, gq[i % bank], outs[i % copies], stream=stream)
             ends[i].record(stream)
     stream.synchronize()
     kdur = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
 
     # end to end through lk_step_host_packed: each step's inputs sit in one
     # pinned host block (q | k | v | ids) moved by one copy
-    def packed_inputs(s):
-        parts = [gq[s][0].view(torch.uint8).reshape(-1), gk[s].view(torch.uint8).reshape(-1),
-                 gv[s].view(torch.uint8).reshape(-1)]
+    def packed_inputs(s, l):
+        parts = [gq[s][l].view(torch.uint8).reshape(-1), gk[s][l].view(torch.uint8).reshape(-1),
+                 gv[s][l].view(torch.uint8).reshape(-1)]
         if gid[s] is not None:
             parts.append(gid[s].view(torch.uint8).reshape(-1))
         blk = torch.cat([p.cpu() for p in parts]).pin_memory()
@@ -311,31 +315,27 @@ def run_gpu(args, rank, local_rank, world):
         v_h = view(2, torch.bfloat16, (B, w.num_kv_heads, 128))
         i_h = view(3, torch.int32, (B,)) if gid[s] is not None else None
         return blk, q_h, k_h, v_h, i_h
-    packed = [packed_inputs(s) for s in range(bank)]
-    hq = [p[1] for p in packed]
-    hk = [p[2] for p in packed]
-    hv = [p[3] for p in packed]
-    hids = [p[4] for p in packed]
+    packed = [[packed_inputs(s, l) for l in range(L)] for s in range(bank)]
+    with_ids = gid[0] is not None
     ho = torch.empty((B, w.num_q_heads, 128), dtype=torch.float32).pin_memory()
-    e2e_value = None
-    h2d = (hq[0].numel() * 2 + hk[0].numel() * 2 + hv[0].numel() * 2 + (B * 4 if hids[0] is not None else 0)) * L
+    h2d = packed[0][0][0].numel() * L
     d2h = ho.numel() * 4 * L
-    if L == 1:
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with_ids = hids[0] is not None
-        e0.record(stream)
-        for i in range(e2e_steps):
-            caches[i % copies].step_host_packed(0, packed[i % bank][0], with_ids, ho, stream=stream)
-        e1.record(stream)
-        e1.synchronize()
-        e2e_elapsed = e0.elapsed_time(e1) / 1e3
-        e2e_value = e2e_steps * world / e2e_elapsed if e2e_steps else None
-        for c in caches:
-            c.check(stream)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        c = caches[i % copies]
+        for l in range(L):
+            c.step_host_packed(l, packed[i % bank][l][0], with_ids, ho, stream=stream)
+    e1.record(stream)
+    e1.synchronize()
+    e2e_elapsed = e0.elapsed_time(e1) / 1e3
+    e2e_value = e2e_steps * L * world / e2e_elapsed if e2e_steps else None
+    for c in caches:
+        c.check(stream)
 
-    # algorithmic bytes of one decode launch (layer 0 of copy 0 at its length)
-    alg_bytes = resident[0] + B * w.num_q_heads * 128 * (2 + 4)
+    # algorithmic bytes of one decode launch (every layer of copy 0 at its length)
+    alg_bytes = resident_step + L * B * w.num_q_heads * 128 * (2 + 4)
     peak, peak_kind = _peaks()
     achieved = alg_bytes / kdur / 1e9
     traffic = NCU_TRAFFIC.get(_decode_source_hash())
@@ -357,7 +357,8 @@ def run_gpu(args, rank, local_rank, world):
             "workload": w.name, "layers": L, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
             "head_dim": 128, "context": N, "context_growth_max": growth, "sink": w.sink, "local": w.local,
             "prune_pct": w.prune_pct, "mask_budget": w.budget,
-            "resident_bytes_per_call": resident[0], "effective_GBps": resident_step * K * world / elapsed / 1e9,
+            "resident_bytes_per_call": resident_step // L, "effective_GBps": resident_step * K * world / elapsed / 1e9,
+            "launches_per_step": "append (all layers) + decode (all layers)",
             "cache_copies": copies, "l2_policy": "inputs larger than L2 (rotating cache copies)",
             "cuda_graph": True, "pdl": True, "parallelism": f"replicas x{world}",
         },
@@ -369,7 +370,7 @@ def run_gpu(args, rank, local_rank, world):
         "e2e": None if e2e_value is None else {
             "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": e2e_steps},
-        "gpu_launches": 2 * L * K,
+        "gpu_launches": 2 * K,
     }
     cs = clocks.summary()
     if cs is not None:

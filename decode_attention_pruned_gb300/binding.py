@@ -48,12 +48,16 @@ SIGNATURES = {
     "lk_cache_destroy": (None, [_vp]),
     "lk_workspace_init": (ctypes.c_int, [_vp, _vp, _sz, _vp]),
     "lk_prefill": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
+    "lk_prefill_ragged": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp]),
     "lk_append": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp]),
+    "lk_append_layers": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp]),
     "lk_decode_attn": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "lk_decode_attn_layers": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "lk_decode_attn_static": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp]),
     "lk_step_host": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lk_step_host_packed": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
     "lk_cache_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i32)]),
+    "lk_cache_lengths": (ctypes.c_int, [_vp, _i32, _vp]),
     "lk_cache_region": (ctypes.c_int, [_vp, _i32, _i32, _i32, ctypes.POINTER(RegionInfo)]),
     "lk_resident_bytes": (ctypes.c_int, [_vp, _i32, _vp, ctypes.POINTER(_u64)]),
     "lk_set_decode_ctas": (ctypes.c_int, [_vp, _i32]),
@@ -201,6 +205,50 @@ class Cache:
         if ids is not None:
             _need(ids, torch.int32, (B, n), "ids")
         _check(_lib.lk_prefill(self._h, layer, k.data_ptr(), v.data_ptr(), _ptr(ids), n, _stream(stream)))
+
+    def prefill_ragged(self, layer, k, v, lens, ids=None, stream=None):
+        """lk_prefill_ragged: k, v [B, n_max, Hkv, 128]; lens: B host ints."""
+        import torch
+        B, H = self.batch, self.plan.num_kv_heads
+        n = k.shape[1]
+        _need(k, torch.bfloat16, (B, n, H, 128), "k")
+        _need(v, torch.bfloat16, (B, n, H, 128), "v")
+        if ids is not None:
+            _need(ids, torch.int32, (B, n), "ids")
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        if lens.shape != (B,):
+            raise ValueError(f"lens shape {lens.shape}")
+        _check(_lib.lk_prefill_ragged(self._h, layer, k.data_ptr(), v.data_ptr(), _ptr(ids), lens.ctypes.data, n,
+                                      _stream(stream)))
+
+    def lengths(self, layer):
+        out = np.zeros(self.batch, dtype=np.int32)
+        _check(_lib.lk_cache_lengths(self._h, layer, out.ctypes.data))
+        return out
+
+    def append_layers(self, layer0, k, v, ids=None, stream=None):
+        """lk_append_layers: k, v [nlayers, B, Hkv, 128] bf16 (one token, every layer)."""
+        import torch
+        nl = k.shape[0]
+        B, H = self.batch, self.plan.num_kv_heads
+        _need(k, torch.bfloat16, (nl, B, H, 128), "k")
+        _need(v, torch.bfloat16, (nl, B, H, 128), "v")
+        if ids is not None:
+            _need(ids, torch.int32, (B,), "ids")
+        _check(_lib.lk_append_layers(self._h, layer0, nl, k.data_ptr(), v.data_ptr(), _ptr(ids), _stream(stream)))
+
+    def decode_layers(self, layer0, q, o=None, stream=None):
+        """lk_decode_attn_layers: q [nlayers, B, Hq, 128] bf16 -> o fp32."""
+        import torch
+        nl = q.shape[0]
+        B, Hq = self.batch, self.plan.num_q_heads
+        _need(q, torch.bfloat16, (nl, B, Hq, 128), "q")
+        if o is None:
+            o = torch.empty((nl, B, Hq, 128), dtype=torch.float32, device=q.device)
+        _need(o, torch.float32, (nl, B, Hq, 128), "o")
+        _check(_lib.lk_decode_attn_layers(self._h, layer0, nl, q.data_ptr(), o.data_ptr(), self.workspace.data_ptr(),
+                                          self.workspace.numel(), _stream(stream)))
+        return o
 
     def append(self, layer, k, v, ids=None, stream=None):
         import torch

@@ -129,9 +129,11 @@ struct WsLayout {
   size_t off_counters, off_ml, off_part, off_q, off_k, off_v, off_ids, off_o, total;
 };
 
+// Workspace: split counters and partials for every (layer, sequence, kv head)
+// entry (a launch may cover all layers), then the staging of lk_step_host.
 WsLayout ws_layout(const lk_plan_desc& d, int B) {
   WsLayout w;
-  const size_t E = (size_t)B * d.num_kv_heads;
+  const size_t E = (size_t)d.num_layers * B * d.num_kv_heads;
   const size_t G = (size_t)(d.num_q_heads / d.num_kv_heads);
   const size_t slots = (size_t)kMaxCtas + E;
   size_t off = 0;
@@ -214,7 +216,13 @@ struct lk_cache_s {
   uint8_t* buf = nullptr;
   size_t bytes = 0;
   int B = 0, cap = 0;
-  std::vector<int32_t> host_len;
+  std::vector<int32_t> host_len;   // [L][B] tokens per layer and sequence (host mirror)
+  std::vector<int32_t> len_upload; // [L][B] source of the prefill length copies
+  int32_t max_len(int layer) const {
+    int32_t m = 0;
+    for (int b = 0; b < B; ++b) m = std::max(m, host_len[(size_t)layer * B + b]);
+    return m;
+  }
   CUtensorMap maps[kNumPools];
   int device = 0, num_sms = 0, decode_ctas = 0;
   std::vector<uint8_t> upload;     // host image of the tables (kept alive for the async copy)
@@ -357,7 +365,8 @@ lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch
   c->bytes = bytes;
   c->B = batch;
   c->cap = capacity_tokens;
-  c->host_len.assign(plan->d.num_layers, 0);
+  c->host_len.assign((size_t)plan->d.num_layers * batch, 0);
+  c->len_upload.assign((size_t)plan->d.num_layers * batch, 0);
   cudaError_t err = cudaGetDevice(&c->device);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   if (err != cudaSuccess) {
@@ -444,57 +453,89 @@ lk_status lk_workspace_init(lk_cache cache, void* workspace, size_t ws_bytes, vo
   return LK_OK;
 }
 
-lk_status lk_prefill(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids, int32_t n,
-                     void* stream) {
+// Shared by the uniform and ragged prefill: lengths go to the device length
+// row first, then the copy kernels read each sequence's length there.
+static lk_status prefill_impl(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
+                              const int32_t* lens, int32_t n_max, void* stream) {
   if (!cache) return fail(LK_ERR_ARG, "lk_prefill: null cache");
   if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_prefill: layer %d out of range", layer);
-  if (n < 0) return fail(LK_ERR_ARG, "lk_prefill: n = %d < 0", n);
-  if (cache->host_len[layer] != 0)
-    return fail(LK_ERR_STATE, "lk_prefill: layer %d already holds %d tokens", layer, cache->host_len[layer]);
-  if (n > cache->cap) return fail(LK_ERR_CAPACITY, "lk_prefill: n = %d exceeds capacity %d", n, cache->cap);
-  if (n == 0) return LK_OK;
+  if (n_max < 0) return fail(LK_ERR_ARG, "lk_prefill: n = %d < 0", n_max);
+  if (cache->max_len(layer) != 0) return fail(LK_ERR_STATE, "lk_prefill: layer %d already holds tokens", layer);
+  if (n_max > cache->cap) return fail(LK_ERR_CAPACITY, "lk_prefill: n = %d exceeds capacity %d", n_max, cache->cap);
+  const int B = cache->B;
+  int32_t* up = &cache->len_upload[(size_t)layer * B];
+  for (int b = 0; b < B; ++b) {
+    const int32_t nb = lens ? lens[b] : n_max;
+    if (nb < 0 || nb > n_max)
+      return fail(LK_ERR_ARG, "lk_prefill: length %d of sequence %d outside [0, %d]", nb, b, n_max);
+    up[b] = nb;
+  }
+  if (n_max == 0) return LK_OK;
   if (!k || !v) return fail(LK_ERR_ARG, "lk_prefill: null k or v");
   if (!aligned(k, 16) || !aligned(v, 16)) return fail(LK_ERR_ALIGN, "lk_prefill: k and v must be 16-byte aligned");
   if (ids && !aligned(ids, 4)) return fail(LK_ERR_ALIGN, "lk_prefill: ids must be 4-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemcpyAsync(cache->cv.len + (size_t)layer * B, up, (size_t)B * 4, cudaMemcpyHostToDevice, s);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_prefill: length upload");
   PrefillArgs a;
   a.cv = cache->cv;
   a.layer = layer;
   a.k = static_cast<const uint16_t*>(k);
   a.v = static_cast<const uint16_t*>(v);
   a.ids = ids;
-  a.n = n;
-  cudaError_t err = launch_prefill(a, cache->plan.layer_special[layer] != 0, cache->num_sms,
-                                   static_cast<cudaStream_t>(stream));
+  a.n = n_max;
+  err = launch_prefill(a, cache->plan.layer_special[layer] != 0, cache->num_sms, s);
   if (err != cudaSuccess) return cuda_fail(err, "lk_prefill launch");
-  cache->host_len[layer] = n;
+  for (int b = 0; b < B; ++b) cache->host_len[(size_t)layer * B + b] = up[b];
   return LK_OK;
 }
 
-lk_status lk_append(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
-                    void* stream) {
+lk_status lk_prefill(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids, int32_t n,
+                     void* stream) {
+  return prefill_impl(cache, layer, k, v, ids, nullptr, n, stream);
+}
+
+lk_status lk_prefill_ragged(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
+                            const int32_t* lens, int32_t n_max, void* stream) {
+  if (!lens) return fail(LK_ERR_ARG, "lk_prefill_ragged: null lens");
+  return prefill_impl(cache, layer, k, v, ids, lens, n_max, stream);
+}
+
+lk_status lk_append_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* k, const void* v,
+                           const int32_t* ids, void* stream) {
   if (!cache) return fail(LK_ERR_ARG, "lk_append: null cache");
-  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_append: layer %d out of range", layer);
+  if (nlayers < 1 || layer0 < 0 || layer0 + nlayers > cache->cv.L)
+    return fail(LK_ERR_ARG, "lk_append: layers [%d, %d) out of range", layer0, layer0 + nlayers);
   if (!k || !v) return fail(LK_ERR_ARG, "lk_append: null k or v");
   if (!aligned(k, 16) || !aligned(v, 16)) return fail(LK_ERR_ALIGN, "lk_append: k and v must be 16-byte aligned");
   if (ids && !aligned(ids, 4)) return fail(LK_ERR_ALIGN, "lk_append: ids must be 4-byte aligned");
-  if (cache->host_len[layer] >= cache->cap)
-    return fail(LK_ERR_CAPACITY, "lk_append: layer %d is full (%d tokens)", layer, cache->cap);
+  for (int l = layer0; l < layer0 + nlayers; ++l)
+    if (cache->max_len(l) >= cache->cap)
+      return fail(LK_ERR_CAPACITY, "lk_append: a sequence of layer %d is full (%d tokens)", l, cache->cap);
   AppendArgs a;
   a.cv = cache->cv;
-  a.layer = layer;
+  a.layer = layer0;
+  a.nlayers = nlayers;
   a.k = static_cast<const uint16_t*>(k);
   a.v = static_cast<const uint16_t*>(v);
   a.ids = ids;
   cudaError_t err = launch_append(a, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "lk_append launch");
-  cache->host_len[layer] += 1;
+  for (int l = layer0; l < layer0 + nlayers; ++l)
+    for (int b = 0; b < cache->B; ++b) cache->host_len[(size_t)l * cache->B + b] += 1;
   return LK_OK;
 }
 
-lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o, void* workspace,
-                         size_t ws_bytes, void* stream) {
+lk_status lk_append(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
+                    void* stream) {
+  return lk_append_layers(cache, layer, 1, k, v, ids, stream);
+}
+
+lk_status lk_decode_attn_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, float* o,
+                                void* workspace, size_t ws_bytes, void* stream) {
   if (!cache) return fail(LK_ERR_ARG, "lk_decode_attn: null cache");
-  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_decode_attn: layer %d out of range", layer);
+  if (nlayers < 1 || layer0 < 0 || layer0 + nlayers > cache->cv.L)
+    return fail(LK_ERR_ARG, "lk_decode_attn: layers [%d, %d) out of range", layer0, layer0 + nlayers);
   if (!q || !o || !workspace) return fail(LK_ERR_ARG, "lk_decode_attn: null q, o or workspace");
   if (!aligned(q, 16) || !aligned(o, 16)) return fail(LK_ERR_ALIGN, "lk_decode_attn: q and o must be 16-byte aligned");
   if (!aligned(workspace, 256)) return fail(LK_ERR_ALIGN, "lk_decode_attn: workspace must be 256-byte aligned");
@@ -504,7 +545,8 @@ lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeArgs a;
   a.cv = cache->cv;
-  a.layer = layer;
+  a.layer = layer0;
+  a.nlayers = nlayers;
   a.q = static_cast<const uint16_t*>(q);
   a.o = o;
   a.part = reinterpret_cast<float*>(ws + w.off_part);
@@ -517,6 +559,11 @@ lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
   cudaError_t err = launch_decode(cache->maps, a, ctas, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn launch");
   return LK_OK;
+}
+
+lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o, void* workspace,
+                         size_t ws_bytes, void* stream) {
+  return lk_decode_attn_layers(cache, layer, 1, q, o, workspace, ws_bytes, stream);
 }
 
 // Append + decode from the inputs staged in the workspace, then copy o back.
@@ -544,8 +591,8 @@ lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const 
   if (ws_bytes < w.total)
     return fail(LK_ERR_CAPACITY, "lk_step_host: workspace has %zu bytes; %zu needed", ws_bytes, w.total);
   if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_step_host: layer %d out of range", layer);
-  if (cache->host_len[layer] >= cache->cap)
-    return fail(LK_ERR_CAPACITY, "lk_step_host: layer %d is full (%d tokens)", layer, cache->cap);
+  if (cache->max_len(layer) >= cache->cap)
+    return fail(LK_ERR_CAPACITY, "lk_step_host: a sequence of layer %d is full (%d tokens)", layer, cache->cap);
   const lk_plan_desc& d = cache->plan.d;
   const size_t B = cache->B;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -567,8 +614,9 @@ lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in
   if (ws_bytes < w.total)
     return fail(LK_ERR_CAPACITY, "lk_step_host_packed: workspace has %zu bytes; %zu needed", ws_bytes, w.total);
   if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_step_host_packed: layer %d out of range", layer);
-  if (cache->host_len[layer] >= cache->cap)
-    return fail(LK_ERR_CAPACITY, "lk_step_host_packed: layer %d is full (%d tokens)", layer, cache->cap);
+  if (cache->max_len(layer) >= cache->cap)
+    return fail(LK_ERR_CAPACITY, "lk_step_host_packed: a sequence of layer %d is full (%d tokens)", layer,
+                cache->cap);
   const lk_plan_desc& d = cache->plan.d;
   const size_t B = cache->B;
   const size_t qb = B * d.num_q_heads * kHeadDim * 2, kvb = B * d.num_kv_heads * kHeadDim * 2;
@@ -585,7 +633,14 @@ lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in
 lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n) {
   if (!cache || !n) return fail(LK_ERR_ARG, "lk_cache_length: null argument");
   if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_cache_length: layer %d out of range", layer);
-  *n = cache->host_len[layer];
+  *n = cache->max_len(layer);
+  return LK_OK;
+}
+
+lk_status lk_cache_lengths(lk_cache cache, int32_t layer, int32_t* lens) {
+  if (!cache || !lens) return fail(LK_ERR_ARG, "lk_cache_lengths: null argument");
+  if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_cache_lengths: layer %d out of range", layer);
+  std::memcpy(lens, &cache->host_len[(size_t)layer * cache->B], (size_t)cache->B * 4);
   return LK_OK;
 }
 
@@ -676,8 +731,10 @@ lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, fl
   if (!q || !o) return fail(LK_ERR_ARG, "lk_decode_attn_static: null q or o");
   if (!aligned(q, 16) || !aligned(o, 16))
     return fail(LK_ERR_ALIGN, "lk_decode_attn_static: q and o must be 16-byte aligned");
-  // counters + partial (m, l) + partial o; the host staging of lk_step_host is not needed
-  const WsLayout w = ws_layout(cache->plan.d, cache->B);
+  // counters + partial (m, l) + partial o of one layer's entries
+  lk_plan_desc one = cache->plan.d;
+  one.num_layers = 1;
+  const WsLayout w = ws_layout(one, cache->B);
   const size_t need = w.off_q;
   if (need > kStaticScratchBytes)
     return fail(LK_ERR_CAPACITY,
@@ -695,6 +752,7 @@ lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, fl
   DecodeArgs a;
   a.cv = cache->cv;
   a.layer = layer;
+  a.nlayers = 1;
   a.q = static_cast<const uint16_t*>(q);
   a.o = o;
   a.part = reinterpret_cast<float*>(ws + w.off_part);

@@ -81,11 +81,31 @@ struct Entry {
   int n_a, n_b, kb;
 };
 
+// Entry e of a launch = (layer offset lr, sequence b, kv head h), layers
+// outermost.
+struct EntryId {
+  int lr, l, b, h;
+};
+__device__ __forceinline__ EntryId entry_id(const DecodeArgs& a, int e) {
+  const CacheView& cv = a.cv;
+  const int per_layer = cv.B * cv.Hkv;
+  EntryId r;
+  r.lr = e / per_layer;
+  const int rem = e - r.lr * per_layer;
+  r.b = rem / cv.Hkv;
+  r.h = rem - r.b * cv.Hkv;
+  r.l = a.layer + r.lr;
+  return r;
+}
+
+// Lengths and special counts are read through L2 (they are written by the
+// preceding append kernel).
 __device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) {
   const CacheView& cv = a.cv;
-  const int b = e / cv.Hkv, h = e - b * cv.Hkv;
-  const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
-  const int N = cv.len[a.layer * cv.B + b];
+  const EntryId id = entry_id(a, e);
+  const int b = id.b;
+  const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+  const int N = __ldcg(&cv.len[id.l * cv.B + b]);
   Entry r{0, 0, 0};
   if (hd.policy == kFull) {
     r.n_a = min(N, cv.S + cv.W);
@@ -96,7 +116,7 @@ __device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) {
   } else if (hd.policy == kLocal) {
     r.n_a = min(N, cv.W_loc);
   } else {
-    r.n_a = min(cv.cnt[a.layer * cv.B + b], hd.cap_a);
+    r.n_a = min(__ldcg(&cv.cnt[id.l * cv.B + b]), hd.cap_a);
   }
   r.n_a = min(r.n_a, hd.cap_a);
   r.n_b = min(r.n_b, hd.cap_b);
@@ -174,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const CacheView& cv = a.cv;
-  const int E = cv.B * cv.Hkv;
+  const int E = a.nlayers * cv.B * cv.Hkv;
   const int G = cv.G;
 
   if (tid == 0) {
@@ -195,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the layer's head table is static: pull it towards L1 while the preceding
   // kernel finishes (lengths and special counts are written by that append,
   // so they are read only after the dependency wait)
-  for (int h = tid; h < cv.Hkv; h += kThreads)
+  for (int h = tid; h < a.nlayers * cv.Hkv; h += kThreads)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(&cv.heads[a.layer * cv.Hkv + h]));
   const uint64_t policy = l2_policy_evict_first();
   grid_dependency_wait();
@@ -282,8 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nta = (a1 - a0 + kTileRows - 1) / kTileRows;
         const int ntb = (b1 - b0 + kTileRows - 1) / kTileRows;
         if (nta + ntb > 0) {
-          const int b = e / cv.Hkv, h = e - b * cv.Hkv;
-          const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
+          const EntryId id = entry_id(a, e);
+          const int b = id.b;
+          const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
           const uint64_t last_row_off = g.n_b > 0 ? off_b + cb * (g.n_b - 1) : off + (uint64_t)kUnitsA * (g.n_a - 1);
           // the entry's first / last owning CTA is read only from the segment's
           // last descriptor: work it out after the first load is in flight
@@ -365,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // entries with no resident token: o = 0, written by CTA (e mod grid)
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
     if (entry_cost(entry_geometry(a, e)) != 0) continue;
-    const int b = e / cv.Hkv, h = e - b * cv.Hkv;
-    float* dst = a.o + ((size_t)b * cv.Hq + (size_t)h * G) * kHeadDim;
+    const EntryId id = entry_id(a, e);
+    float* dst = a.o + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
     for (int i = ct; i < G * kHeadDim; i += kConsumerWarps * 32) dst[i] = 0.f;
   }
 
@@ -390,11 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (d.e < 0) break;
     if (d.flags & kFirst) {
       // (re)load q fragments of the entry: B operand of S^T = K Q^T
-      const int b = d.e / cv.Hkv, h = d.e - b * cv.Hkv;
-      const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
-      const int16_t* kept = cv.kept + ((size_t)a.layer * cv.Hkv + h) * kHeadDim;
+      const EntryId id = entry_id(a, d.e);
+      const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+      const int16_t* kept = cv.kept + ((size_t)id.l * cv.Hkv + id.h) * kHeadDim;
       const bool live = gid < G;
-      const uint16_t* qrow = a.q + ((size_t)b * cv.Hq + (size_t)h * G + (live ? gid : 0)) * kHeadDim;
+      const uint16_t* qrow =
+          a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G + (live ? gid : 0)) * kHeadDim;
       const int kk = hd.policy == kFull ? hd.n_kept : 0;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -451,26 +473,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         x[j][2] = v1 ? s[2] * a.scale_log2 : NEG_INF;
         x[j][3] = v1 ? s[3] * a.scale_log2 : NEG_INF;
       }
+      // Lazy rescaling: the running max m of a column moves only when some
+      // score of the tile exceeds it by more than kRescaleGap (log2 units);
+      // otherwise p = 2^(s - m) <= 2^kRescaleGap, exact in the fp32
+      // accumulators and in the bf16 hi/lo split.  One warp vote replaces the
+      // column-max shuffles in the common case.
       float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
       float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+      constexpr float kRescaleGap = 8.f;
+      if (__any_sync(0xffffffffu, mx0 > m0 + kRescaleGap || mx1 > m1 + kRescaleGap)) {
 #pragma unroll
-      for (int sh = 4; sh < 32; sh <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
-      }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      l0 *= al0;
-      l1 *= al1;
+        for (int sh = 4; sh < 32; sh <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 *= al0;
+        l1 *= al1;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        o[i][0] *= al0;
-        o[i][1] *= al1;
-        o[i][2] *= al0;
-        o[i][3] *= al1;
+        for (int i = 0; i < 8; ++i) {
+          o[i][0] *= al0;
+          o[i][1] *= al1;
+          o[i][2] *= al0;
+          o[i][3] *= al1;
+        }
       }
+      const float mn0 = m0, mn1 = m1;
 #pragma unroll
       for (int j = 0; j < kSubPerWarp; ++j) {
         if (!live[j]) continue;
@@ -521,8 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         merge_l[warp * kMaxGroup + 2 * tig + 1] = lr1;
       }
       consumer_bar();
-      const int b = d.e / cv.Hkv, h = d.e - b * cv.Hkv;
-      float* dst = a.o + ((size_t)b * cv.Hq + (size_t)h * G) * kHeadDim;
+      const EntryId id = entry_id(a, d.e);
+      float* dst = a.o + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
       const bool single = d.first_cta == d.last_cta;
       const size_t slot = (size_t)blockIdx.x + d.e;
       // CTA-level merge, 4 channels per thread

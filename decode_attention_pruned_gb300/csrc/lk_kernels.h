@@ -9,22 +9,24 @@ namespace lk {
 
 struct DecodeArgs {
   CacheView cv;
-  int32_t layer;
-  const uint16_t* q;        // bf16 [B][Hq][128]
-  float* o;                 // fp32 [B][Hq][128]
+  int32_t layer;            // first layer
+  int32_t nlayers;          // layers layer .. layer + nlayers - 1 in one launch
+  const uint16_t* q;        // bf16 [nlayers][B][Hq][128]
+  float* o;                 // fp32 [nlayers][B][Hq][128]
   float* part;              // fp32 [slots][G][128] split partials (unnormalised o)
   float2* part_ml;          // [slots][G] (running max in log2 units, sum of p)
-  int32_t* counters;        // [B*Hkv] CTAs done per entry; self-resetting
+  int32_t* counters;        // [nlayers*B*Hkv] CTAs done per entry; self-resetting
   uint64_t wait_limit_ns;   // bound of every mbarrier wait
   float scale_log2;         // log2(e) / sqrt(128)
 };
 
 struct AppendArgs {
   CacheView cv;
-  int32_t layer;
-  const uint16_t* k;        // bf16 [B][Hkv][128]
+  int32_t layer;            // first layer
+  int32_t nlayers;          // layers layer .. layer + nlayers - 1 (grid.y)
+  const uint16_t* k;        // bf16 [nlayers][B][Hkv][128]
   const uint16_t* v;
-  const int32_t* ids;       // [B] or null
+  const int32_t* ids;       // [B] or null (the same token for every layer)
 };
 
 struct PrefillArgs {

@@ -47,10 +47,13 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   grid_launch_dependents();
   const CacheView& cv = a.cv;
   const int b = blockIdx.x;
-  const int lb = a.layer * cv.B + b;
+  const int layer = a.layer + (int)blockIdx.y;
+  const int lb = layer * cv.B + b;
+  const uint16_t* k_in = a.k + (size_t)blockIdx.y * cv.B * cv.Hkv * kHeadDim;
+  const uint16_t* v_in = a.v + (size_t)blockIdx.y * cv.B * cv.Hkv * kHeadDim;
   __shared__ int s_n, s_cnt, s_special, s_ok;
   if (threadIdx.x == 0) {
-    const int n = cv.len[lb];
+    const int n = __ldcg(&cv.len[lb]);
     int special = 0;
     if (a.ids != nullptr) {
       const int id = a.ids[b];
@@ -61,7 +64,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
       }
     }
     s_n = n;
-    s_cnt = cv.cnt[lb];
+    s_cnt = __ldcg(&cv.cnt[lb]);
     s_special = special;
     s_ok = n < cv.capacity;
     if (!s_ok) set_status(cv, kStatusCapacity);
@@ -73,10 +76,10 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   uint16_t* ka_pool = cv.pool[kPoolK128];
   uint16_t* va_pool = cv.pool[kPoolV];
   for (int h = warp; h < cv.Hkv; h += nw) {
-    const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
+    const HeadDesc& hd = cv.heads[layer * cv.Hkv + h];
     const size_t src = ((size_t)b * cv.Hkv + h) * kHeadDim;
-    const uint2 kx = reinterpret_cast<const uint2*>(a.k + src)[lane];
-    const uint2 vx = reinterpret_cast<const uint2*>(a.v + src)[lane];
+    const uint2 kx = reinterpret_cast<const uint2*>(k_in + src)[lane];
+    const uint2 vx = reinterpret_cast<const uint2*>(v_in + src)[lane];
     const int64_t abase = hd.row_a + (int64_t)b * hd.cap_a;
     int64_t row = -1;
     if (hd.policy == kFull) {
@@ -87,7 +90,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
           const int mid = n - cv.W - cv.S;               // K_prun row of token n - W
           const uint16_t* k_old = ka_pool + (abase + slot) * kHeadDim;
           const uint2 v_old = row8(va_pool, abase + slot)[lane];
-          write_middle(cv, hd, cv.kept + ((size_t)a.layer * cv.Hkv + h) * kHeadDim,
+          write_middle(cv, hd, cv.kept + ((size_t)layer * cv.Hkv + h) * kHeadDim,
                        hd.krow_b + (int64_t)b * hd.cap_b + mid, hd.vrow_b + (int64_t)b * hd.cap_b + mid,
                        k_old, v_old, lane);
           __syncwarp();
@@ -115,20 +118,24 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   }
 }
 
+// The layer's per-sequence lengths are already in len[layer][b] (the host
+// enqueues them first); inputs are padded to n_max tokens per sequence.
 __global__ void __launch_bounds__(256) prefill_kernel(const PrefillArgs a) {
   grid_dependency_wait();
   const CacheView& cv = a.cv;
-  const int n = a.n;
+  const int nmax = a.n;
   const int lane = threadIdx.x & 31;
-  const int64_t items = (int64_t)cv.B * n * cv.Hkv;
+  const int64_t items = (int64_t)cv.B * nmax * cv.Hkv;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   uint16_t* ka_pool = cv.pool[kPoolK128];
   uint16_t* va_pool = cv.pool[kPoolV];
   for (int64_t it = (((int64_t)blockIdx.x * blockDim.x) + threadIdx.x) >> 5; it < items; it += nwarps) {
     const int h = (int)(it % cv.Hkv);
-    const int64_t bt = it / cv.Hkv;              // b * n + t
-    const int t = (int)(bt % n);
-    const int b = (int)(bt / n);
+    const int64_t bt = it / cv.Hkv;              // b * n_max + t
+    const int t = (int)(bt % nmax);
+    const int b = (int)(bt / nmax);
+    const int n = __ldcg(&cv.len[a.layer * cv.B + b]);
+    if (t >= n) continue;
     const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
     const uint16_t* k_src = a.k + (size_t)it * kHeadDim;
     const uint16_t* v_src = a.v + (size_t)it * kHeadDim;
@@ -150,8 +157,6 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillArgs a) {
                    k_src, reinterpret_cast<const uint2*>(v_src)[lane], lane);
     }
   }
-  if (blockIdx.x == 0)
-    for (int b = threadIdx.x; b < cv.B; b += blockDim.x) cv.len[a.layer * cv.B + b] = n;
 }
 
 // SPECIAL heads: one block per sequence ranks the special tokens in position
@@ -161,7 +166,8 @@ __global__ void __launch_bounds__(1024) prefill_special_kernel(const PrefillArgs
   grid_dependency_wait();
   const CacheView& cv = a.cv;
   const int b = blockIdx.x;
-  const int n = a.n;
+  const int nmax = a.n;
+  const int n = __ldcg(&cv.len[a.layer * cv.B + b]);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ int s_warp[32];
   __shared__ int s_total;
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(1024) prefill_special_kernel(const PrefillArgs
     const int t = c0 + tid;
     bool flag = false;
     if (t < n && a.ids != nullptr) {
-      const int id = a.ids[(size_t)b * n + t];
+      const int id = a.ids[(size_t)b * nmax + t];
       if (id >= 0 && id < cv.vocab) flag = cv.is_special[id] != 0;
       else set_status(cv, kStatusBadId);
     }
@@ -203,7 +209,7 @@ __global__ void __launch_bounds__(1024) prefill_special_kernel(const PrefillArgs
         if (lane == 0) set_status(cv, kStatusCapacity);
         continue;
       }
-      const size_t src = (((size_t)b * n + s_tok[j]) * cv.Hkv + h) * kHeadDim;
+      const size_t src = (((size_t)b * nmax + s_tok[j]) * cv.Hkv + h) * kHeadDim;
       const int64_t row = hd.row_a + (int64_t)b * hd.cap_a + r;
       row8(cv.pool[kPoolK128], row)[lane] = reinterpret_cast<const uint2*>(a.k + src)[lane];
       row8(cv.pool[kPoolV], row)[lane] = reinterpret_cast<const uint2*>(a.v + src)[lane];
@@ -218,7 +224,7 @@ __global__ void __launch_bounds__(1024) prefill_special_kernel(const PrefillArgs
 
 cudaError_t launch_append(const AppendArgs& args, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(args.cv.B);
+  cfg.gridDim = dim3(args.cv.B, args.nlayers);
   cfg.blockDim = dim3(256);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

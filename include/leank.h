@@ -111,8 +111,8 @@ lk_status lk_plan_head(lk_plan plan, int32_t layer, int32_t kv_head, int32_t* po
  * tokens each (LeanK 3.1 split cache, FastGen 5.1 per-head allocation). */
 lk_status lk_cache_bytes(lk_plan plan, int32_t batch, int32_t capacity_tokens, size_t* bytes);
 
-/* Bytes of the decode workspace (split partials, counters, staging of
- * lk_step_host) for `batch` sequences. */
+/* Bytes of the decode workspace (split partials and counters for every
+ * layer's entries, staging of lk_step_host) for `batch` sequences. */
 lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes);
 
 /* Bind a cache to a caller-owned device buffer of at least lk_cache_bytes
@@ -135,6 +135,14 @@ lk_status lk_workspace_init(lk_cache cache, void* workspace, size_t ws_bytes, vo
  * exceeds the token capacity. */
 lk_status lk_prefill(lk_cache cache, int32_t layer, const void* k, const void* v,
                      const int32_t* ids, int32_t n, void* stream);
+
+/* lk_prefill with a length per sequence: sequence b gets the first lens[b]
+ * tokens of its row of the padded inputs.
+ *   k, v  device bf16 [B][n_max][Hkv][128];  ids device int32 [B][n_max] or NULL;
+ *   lens  host int32 [B], each in [0, n_max].
+ * Decode then handles each sequence at its own length (continuous batching). */
+lk_status lk_prefill_ragged(lk_cache cache, int32_t layer, const void* k, const void* v,
+                            const int32_t* ids, const int32_t* lens, int32_t n_max, void* stream);
 
 /* Append one token per sequence to a layer (FastGen 2.1, 3.2 stage 2).
  *   k, v  device bf16 [B][Hkv][128];  ids device int32 [B] or NULL.
@@ -180,6 +188,19 @@ lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
  * results. */
 lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, float* o, void* stream);
 
+/* lk_append over layers layer0 .. layer0+nlayers-1 in one launch:
+ *   k, v  device bf16 [nlayers][B][Hkv][128];  ids device int32 [B] or NULL
+ *   (the same token enters every layer). */
+lk_status lk_append_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* k, const void* v,
+                           const int32_t* ids, void* stream);
+
+/* lk_decode_attn over layers layer0 .. layer0+nlayers-1 in one launch (the
+ * work of all layers is split across the CTAs together):
+ *   q  device bf16 [nlayers][B][Hq][128];  o  device fp32 [nlayers][B][Hq][128].
+ * Useful when every layer's query is known up front (benchmarks, drafts). */
+lk_status lk_decode_attn_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, float* o,
+                                void* workspace, size_t ws_bytes, void* stream);
+
 /* One decode step end to end from host memory: copies q [B][Hq][128] bf16,
  * k, v [B][Hkv][128] bf16 and ids [B] int32 (NULL allowed) from host to the
  * workspace, runs lk_append then lk_decode_attn, and copies o [B][Hq][128]
@@ -196,8 +217,11 @@ lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const 
 lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in, int32_t has_ids,
                               float* o_host, void* workspace, size_t ws_bytes, void* stream);
 
-/* Host-tracked token count of a layer (tokens appended or prefilled). */
+/* Host-tracked token count of a layer: the longest sequence's length. */
 lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n);
+
+/* Host-tracked token count of every sequence of a layer (lens: host int32 [B]). */
+lk_status lk_cache_lengths(lk_cache cache, int32_t layer, int32_t* lens);
 
 /* Location of one (layer, sequence, kv head) in the cache buffer. */
 lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_head,

@@ -68,20 +68,29 @@ class Case:
         return S.make_q(self.w, layer, N - 1, device=self.gen_device, step=step).to(self.device)
 
     def expected(self, layer, q, N, heads=None):
-        """fp64 oracle output for the first N tokens of the history."""
+        """fp64 oracle output for the first N tokens of the history (N an int,
+        or one length per sequence)."""
         k, v = self.history(layer)
         w = self.w
-        if heads is None:
+        ragged = not np.isscalar(N)
+        if heads is None and not ragged:
             K, V = f64(k[:, :N]), f64(v[:, :N])
             return OA.decode_layer(f64(q), K, V, self.masks[layer], self.policies[layer], N, w.sink,
                                    w.local, w.local_only_window, self.flags)
+        pairs = heads if heads is not None else [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
         out = {}
         G = w.group
-        for b, h in heads:
-            K, V = f64(k[b, :N, h]), f64(v[b, :N, h])
+        for b, h in pairs:
+            Nb = int(N[b]) if ragged else N
+            K, V = f64(k[b, :Nb, h]), f64(v[b, :Nb, h])
             kept = np.nonzero(self.masks[layer, h])[0]
             out[(b, h)] = OA.decode_head(f64(q[b, h * G:(h + 1) * G]), K, V, int(self.policies[layer, h]),
-                                         kept, N, w.sink, w.local, w.local_only_window, self.flags[b])
+                                         kept, Nb, w.sink, w.local, w.local_only_window, self.flags[b])
+        if heads is None:
+            full = np.zeros((w.batch, w.num_q_heads, 128))
+            for (b, h), r in out.items():
+                full[b, h * G:(h + 1) * G] = r
+            return full
         return out
 
     def check_layout(self, layer, N, heads=None):
@@ -91,10 +100,11 @@ class Case:
         B, H = w.batch, w.num_kv_heads
         pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(H)]
         for b, h in pairs:
+            Nb = N if np.isscalar(N) else int(N[b])
             r = self.cache.region(layer, b, h)
             pol = int(self.policies[layer, h])
             kept = np.nonzero(self.masks[layer, h])[0] if pol == S.POLICY_FULL else np.arange(0)
-            rows, toks = OL.region_a(pol, N, w.sink, w.local, w.local_only_window, self.flags[b],
+            rows, toks = OL.region_a(pol, Nb, w.sink, w.local, w.local_only_window, self.flags[b],
                                      special_capacity=r.rows_a)
             if len(rows):
                 ka = self.cache.rows(r.k_a_offset, r.rows_a, 128)
@@ -103,7 +113,7 @@ class Case:
                 ti = torch.from_numpy(toks).to(self.device)
                 assert torch.equal(ka[ri], k[b, ti, h]), (layer, b, h, "K region A")
                 assert torch.equal(va[ri], v[b, ti, h]), (layer, b, h, "V region A")
-            rows, toks = OL.region_b(pol, len(kept), N, w.sink, w.local)
+            rows, toks = OL.region_b(pol, len(kept), Nb, w.sink, w.local)
             if len(rows):
                 kb = self.cache.rows(r.k_b_offset, r.rows_b, r.n_kept)
                 vb = self.cache.rows(r.v_b_offset, r.rows_b, 128)

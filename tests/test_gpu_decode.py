@@ -204,3 +204,66 @@ def test_special_overflow_is_reported_on_device(cuda):
         case.cache.check()
     assert e.value.status == lkb.LK_ERR_CAPACITY
     case.cache.check()   # cleared
+
+
+def test_all_layers_in_one_append_and_one_decode(cuda):
+    w = FASTGEN.scaled(num_layers=4, batch=3, context=700, policy_counts=(10, 6, 16))
+    case = Case(w, total=702)
+    L = w.num_layers
+    for layer in range(L):
+        case.prefill(layer, 700)
+    for t in (700, 701):
+        ks = torch.stack([case.history(l)[0][:, t] for l in range(L)]).contiguous()
+        vs = torch.stack([case.history(l)[1][:, t] for l in range(L)]).contiguous()
+        case.cache.append_layers(0, ks, vs, case.ids[:, t].contiguous())
+        qs = torch.stack([case.q(l, t + 1, step=t) for l in range(L)]).contiguous()
+        o = case.cache.decode_layers(0, qs)
+        case.cache.check()
+        for layer in range(L):
+            assert case.cache.length(layer) == t + 1
+            assert _max_err(o[layer], case.expected(layer, qs[layer], t + 1)) <= DECODE_TOL, (layer, t)
+    for layer in range(L):
+        case.check_layout(layer, 702)
+    # a sub-range of layers
+    q2 = torch.stack([case.q(l, 702, step=9) for l in (1, 2)]).contiguous()
+    o2 = case.cache.decode_layers(1, q2)
+    for i, layer in enumerate((1, 2)):
+        assert _max_err(o2[i], case.expected(layer, q2[i], 702)) <= DECODE_TOL
+
+
+def test_ragged_lengths(cuda):
+    # four sequences at different lengths: past the window, inside the window
+    # fill, and below the sinks; then appends advance each at its own position
+    w = FASTGEN.scaled(num_layers=1, batch=4, context=1300, policy_counts=(3, 2, 3))
+    case = Case(w, total=1304)
+    k, v = case.history(0)
+    lens = np.array([1300, 1163, 700, 9], dtype=np.int32)
+    n_max = int(lens.max())
+    case.cache.prefill_ragged(0, k[:, :n_max].contiguous(), v[:, :n_max].contiguous(), lens,
+                              case.ids[:, :n_max].contiguous())
+    assert list(case.cache.lengths(0)) == list(lens)
+    case.check_layout(0, lens)
+    B = w.batch
+    for step in range(3):
+        pos = torch.from_numpy(lens.astype(np.int64)).to(k.device)
+        bi = torch.arange(B, device=k.device)
+        case.cache.append(0, k[bi, pos].contiguous(), v[bi, pos].contiguous(), case.ids[bi, pos].contiguous())
+        lens = lens + 1
+        q = case.q(0, int(lens.max()), step=step)
+        o = case.cache.decode(0, q)
+        case.cache.check()
+        assert _max_err(o, case.expected(0, q, lens)) <= DECODE_TOL, step
+        case.check_layout(0, lens)
+
+
+def test_alignment_64_masks(cuda):
+    # per-head kept counts rounded to multiples of 64 (the H100 setting of the
+    # LeanK article's troubleshooting notes): widths 0, 64 and 128 only
+    w = SERVING.scaled(num_layers=2, batch=2, context=900, tau=0.5)
+    alpha = S.draw_alpha(w)
+    masks = S.aligned_prune_masks(alpha, 60.0, align=64, budget="exact")
+    counts = masks.sum(-1)
+    assert set(np.unique(counts)) <= {0, 64, 128} and len(set(np.unique(counts))) >= 2
+    case = Case(w, total=901, masks=masks)
+    for layer in range(2):
+        _decode_steps(case, layer, 900, 1, layout=True)
