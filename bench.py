@@ -49,7 +49,7 @@ METRIC = "decode-attn calls/s & effective HBM GB/s (% of GB300 peak) on pruned K
 UNIT = "calls/s"
 FALLBACK_HBM_GBS = 6800.0
 MAX_CONTEXT_GROWTH = 0.01           # appends may lengthen the context by at most 1 %
-COPY_BUDGET_BYTES = 48 << 30        # device memory the rotating copies may take
+COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 
 # DRAM bytes (read + write) per decode launch from an ncu capture, keyed by the
 # sha256 of the decode kernel source it was taken on (null when it changed).

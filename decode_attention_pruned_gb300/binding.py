@@ -41,6 +41,7 @@ class RegionInfo(ctypes.Structure):
 SIGNATURES = {
     "lk_build_plan": (ctypes.c_int, [ctypes.POINTER(PlanDesc), _vp, _vp, _vp, ctypes.POINTER(_vp)]),
     "lk_plan_destroy": (None, [_vp]),
+    "lk_build_masks": (ctypes.c_int, [_vp, _vp, _i32, _i32, ctypes.c_double, _i32, _i32, _vp, _vp]),
     "lk_plan_head": (ctypes.c_int, [_vp, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp]),
     "lk_cache_bytes": (ctypes.c_int, [_vp, _i32, _i32, ctypes.POINTER(_sz)]),
     "lk_workspace_bytes": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_sz)]),
@@ -122,6 +123,20 @@ def _need(t, dtype, shape, what, device_kind="cuda"):
         raise TypeError(f"{what} must be a torch tensor") from None
     raise ValueError(f"{what}: expected contiguous {dtype} {tuple(shape)} on {device_kind}, got "
                      f"{t.dtype} {tuple(t.shape)} on {t.device.type}")
+
+
+def build_masks(alpha, prune_pct, align=32, exact=False, eligible=None, stream=None):
+    """lk_build_masks: alpha device fp32 [L, Hkv, 128] -> device uint8 masks."""
+    import torch
+    load()
+    L, H = alpha.shape[0], alpha.shape[1]
+    _need(alpha, torch.float32, (L, H, 128), "alpha")
+    if eligible is not None:
+        _need(eligible, torch.uint8, (L, H), "eligible")
+    out = torch.empty((L, H, 128), dtype=torch.uint8, device=alpha.device)
+    _check(_lib.lk_build_masks(alpha.data_ptr(), _ptr(eligible), L, H, float(prune_pct), align, 1 if exact else 0,
+                               out.data_ptr(), _stream(stream)))
+    return out
 
 
 class Plan:

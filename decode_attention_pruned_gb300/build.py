@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libleank.so")
-SOURCES = ["lk_api.cu", "lk_decode.cu", "lk_kv.cu"]
+SOURCES = ["lk_api.cu", "lk_decode.cu", "lk_kv.cu", "lk_masks.cu"]
 # the decode kernel's exp2f / reciprocals use the hardware approximations
 PER_SOURCE = {"lk_decode.cu": ["--use_fast_math"]}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

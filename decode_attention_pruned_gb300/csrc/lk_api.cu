@@ -313,6 +313,23 @@ lk_status lk_build_plan(const lk_plan_desc* desc, const uint8_t* masks, const in
 
 void lk_plan_destroy(lk_plan plan) { delete plan; }
 
+lk_status lk_build_masks(const float* alpha, const uint8_t* eligible, int32_t num_layers, int32_t num_kv_heads,
+                         double prune_pct, int32_t align, int32_t exact, uint8_t* masks, void* stream) {
+  if (!alpha || !masks) return fail(LK_ERR_ARG, "lk_build_masks: null alpha or masks");
+  if (!aligned(alpha, 4)) return fail(LK_ERR_ALIGN, "lk_build_masks: alpha must be 4-byte aligned");
+  if (num_layers < 1 || num_kv_heads < 1 || (int64_t)num_layers * num_kv_heads > 8192)
+    return fail(LK_ERR_ARG, "lk_build_masks: layers x kv heads must be in [1, 8192]");
+  if (align != 32 && align != 64 && align != 128)
+    return fail(LK_ERR_ARG, "lk_build_masks: align %d is not 32, 64 or 128", align);
+  if (!(prune_pct >= 0.0 && prune_pct <= 100.0))
+    return fail(LK_ERR_ARG, "lk_build_masks: prune_pct %g outside [0, 100]", prune_pct);
+  if (exact != 0 && exact != 1) return fail(LK_ERR_ARG, "lk_build_masks: exact must be 0 or 1");
+  cudaError_t err = launch_build_masks(alpha, eligible, num_layers * num_kv_heads, prune_pct, align, exact, masks,
+                                       static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_build_masks launch");
+  return LK_OK;
+}
+
 lk_status lk_plan_head(lk_plan plan, int32_t layer, int32_t kv_head, int32_t* policy, int32_t* n_kept,
                        int16_t* kept_channels) {
   if (!plan) return fail(LK_ERR_ARG, "lk_plan_head: null plan");

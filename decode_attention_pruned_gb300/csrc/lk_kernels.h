@@ -42,5 +42,7 @@ size_t decode_smem_bytes();
 cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int ctas, cudaStream_t stream);
 cudaError_t launch_append(const AppendArgs& args, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& args, bool has_special, int num_sms, cudaStream_t stream);
+cudaError_t launch_build_masks(const float* alpha, const uint8_t* eligible, int nh, double pct, int align,
+                               int exact, uint8_t* masks, cudaStream_t stream);
 
 }  // namespace lk

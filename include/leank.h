@@ -102,6 +102,25 @@ lk_status lk_build_plan(const lk_plan_desc* desc, const uint8_t* masks, const in
                         const uint8_t* is_special, lk_plan* out);
 void lk_plan_destroy(lk_plan plan);
 
+/* Build the static mask beta on the device from learned channel importances
+ * (LeanK 2.2 stage 2):
+ *   alpha     device fp32 [L][Hkv][128] importances
+ *   eligible  device uint8 [L][Hkv], 1 for heads that take a mask (FULL
+ *             policy), or NULL for all; other heads get all ones
+ *   prune_pct s in [0, 100]: share of eligible channels pruned; a channel
+ *             stays when alpha >= the s-th percentile of the eligible alphas
+ *             (linear interpolation, computed in fp32)
+ *   align     32, 64 or 128: per-head kept counts become multiples of it
+ *   exact     0: counts rounded down; 1: then topped up by +align on the heads
+ *             with the largest remainders (ties: lower head index) until the
+ *             total is align * floor((1 - s/100) * heads * 128 / align + 1/2)
+ *   masks     device uint8 [L][Hkv][128] out; a head keeps its channels of
+ *             largest alpha, equal alphas to the lower channel index.
+ * L * Hkv <= 8192.  Enqueued on `stream`; copy the masks to the host for
+ * lk_build_plan. */
+lk_status lk_build_masks(const float* alpha, const uint8_t* eligible, int32_t num_layers, int32_t num_kv_heads,
+                         double prune_pct, int32_t align, int32_t exact, uint8_t* masks, void* stream);
+
 /* Host-side query of one head's policy, kept count and kept channels
  * (kept_channels: host int16 [128] or NULL; first n_kept entries valid). */
 lk_status lk_plan_head(lk_plan plan, int32_t layer, int32_t kv_head, int32_t* policy,

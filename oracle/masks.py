@@ -48,6 +48,8 @@ def aligned_counts(alpha, prune_pct: float, align: int, budget: str, eligible=No
     a = np.asarray(alpha, dtype=np.float32)
     L, H, D = a.shape
     elig = np.ones((L, H), dtype=bool) if eligible is None else np.asarray(eligible, dtype=bool)
+    if not elig.any():                      # nothing to prune: every head keeps all channels
+        return np.full((L, H), D, dtype=np.int64)
     thr = percentile_fp32(a[elig], prune_pct)
     above = (a >= thr).sum(axis=-1)
     keep = (above // align) * align
