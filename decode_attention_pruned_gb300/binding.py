@@ -35,7 +35,9 @@ class PlanDesc(ctypes.Structure):
 class RegionInfo(ctypes.Structure):
     _fields_ = [("policy", ctypes.c_int32), ("n_kept", ctypes.c_int32), ("rows_a", ctypes.c_int32),
                 ("rows_b", ctypes.c_int32), ("k_a_offset", ctypes.c_uint64), ("v_a_offset", ctypes.c_uint64),
-                ("k_b_offset", ctypes.c_uint64), ("v_b_offset", ctypes.c_uint64)]
+                ("k_b_offset", ctypes.c_uint64), ("v_b_offset", ctypes.c_uint64),
+                ("page_rows", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("page_table_offset", ctypes.c_uint64)]
 
 
 SIGNATURES = {
@@ -44,12 +46,17 @@ SIGNATURES = {
     "lk_build_masks": (ctypes.c_int, [_vp, _vp, _i32, _i32, ctypes.c_double, _i32, _i32, _vp, _vp]),
     "lk_plan_head": (ctypes.c_int, [_vp, _i32, _i32, ctypes.POINTER(_i32), ctypes.POINTER(_i32), _vp]),
     "lk_cache_bytes": (ctypes.c_int, [_vp, _i32, _i32, ctypes.POINTER(_sz)]),
+    "lk_cache_bytes_paged": (ctypes.c_int, [_vp, _i32, _i32, ctypes.c_int64, ctypes.POINTER(_sz)]),
     "lk_workspace_bytes": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_sz)]),
     "lk_cache_init": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, _vp, ctypes.POINTER(_vp)]),
+    "lk_cache_init_paged": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, ctypes.c_int64, _vp, ctypes.POINTER(_vp)]),
     "lk_cache_destroy": (None, [_vp]),
     "lk_workspace_init": (ctypes.c_int, [_vp, _vp, _sz, _vp]),
     "lk_prefill": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
     "lk_prefill_ragged": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp]),
+    "lk_prefill_sequence": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp]),
+    "lk_release_sequence": (ctypes.c_int, [_vp, _i32, _vp]),
+    "lk_cache_pages": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     "lk_append": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp]),
     "lk_append_layers": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp]),
     "lk_decode_attn": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _sz, _vp]),
@@ -177,9 +184,13 @@ class Plan:
         _check(_lib.lk_plan_head(self._h, layer, kv_head, ctypes.byref(pol), ctypes.byref(nk), kept.ctypes.data))
         return pol.value, nk.value, kept[: nk.value].copy()
 
-    def cache_bytes(self, batch, capacity):
+    def cache_bytes(self, batch, capacity, middle_tokens=None):
+        """Cache buffer bytes; paged layout when middle_tokens is given."""
         n = ctypes.c_size_t()
-        _check(_lib.lk_cache_bytes(self._h, batch, capacity, ctypes.byref(n)))
+        if middle_tokens is None:
+            _check(_lib.lk_cache_bytes(self._h, batch, capacity, ctypes.byref(n)))
+        else:
+            _check(_lib.lk_cache_bytes_paged(self._h, batch, capacity, int(middle_tokens), ctypes.byref(n)))
         return n.value
 
     def workspace_bytes(self, batch):
@@ -194,19 +205,29 @@ class Plan:
 
 
 class Cache:
-    """A cache bound to a torch-allocated device buffer, plus its workspace."""
+    """A cache bound to a torch-allocated device buffer, plus its workspace.
 
-    def __init__(self, plan: Plan, batch: int, capacity: int, device=None, stream=None):
+    With ``middle_tokens`` the cache is paged (lk_cache_init_paged): the
+    middle rows of all sequences share page pools sized for that many middle
+    tokens in total."""
+
+    def __init__(self, plan: Plan, batch: int, capacity: int, device=None, stream=None, middle_tokens=None):
         import torch
         self.plan, self.batch, self.capacity = plan, batch, capacity
+        self.paged = middle_tokens is not None
         dev = torch.device(device if device is not None else "cuda")
         self.device = dev
-        nbytes = plan.cache_bytes(batch, capacity)
+        nbytes = plan.cache_bytes(batch, capacity, middle_tokens)
         self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.workspace = torch.empty(plan.workspace_bytes(batch), dtype=torch.uint8, device=dev)
         h = ctypes.c_void_p()
         s = _stream(stream)
-        _check(_lib.lk_cache_init(plan._h, self.buffer.data_ptr(), nbytes, batch, capacity, s, ctypes.byref(h)))
+        if self.paged:
+            _check(_lib.lk_cache_init_paged(plan._h, self.buffer.data_ptr(), nbytes, batch, capacity,
+                                            int(middle_tokens), s, ctypes.byref(h)))
+        else:
+            _check(_lib.lk_cache_init(plan._h, self.buffer.data_ptr(), nbytes, batch, capacity, s,
+                                      ctypes.byref(h)))
         self._h = h
         _check(_lib.lk_workspace_init(self._h, self.workspace.data_ptr(), self.workspace.numel(), s))
 
@@ -235,6 +256,44 @@ class Cache:
             raise ValueError(f"lens shape {lens.shape}")
         _check(_lib.lk_prefill_ragged(self._h, layer, k.data_ptr(), v.data_ptr(), _ptr(ids), lens.ctypes.data, n,
                                       _stream(stream)))
+
+    def prefill_sequence(self, layer, b, k, v, ids=None, stream=None):
+        """lk_prefill_sequence: k, v [n, Hkv, 128] bf16 into empty slot b."""
+        import torch
+        H = self.plan.num_kv_heads
+        n = k.shape[0]
+        _need(k, torch.bfloat16, (n, H, 128), "k")
+        _need(v, torch.bfloat16, (n, H, 128), "v")
+        if ids is not None:
+            _need(ids, torch.int32, (n,), "ids")
+        _check(_lib.lk_prefill_sequence(self._h, layer, b, k.data_ptr() if n else None, v.data_ptr() if n else None,
+                                        _ptr(ids) if n else None, n, _stream(stream)))
+
+    def release(self, b, stream=None):
+        """lk_release_sequence: empty slot b in every layer."""
+        _check(_lib.lk_release_sequence(self._h, b, _stream(stream)))
+
+    def pages(self, width):
+        """(total, free) pages of a width class of a paged cache."""
+        total, free = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.lk_cache_pages(self._h, width, ctypes.byref(total), ctypes.byref(free)))
+        return total.value, free.value
+
+    def page_table(self, r: RegionInfo):
+        """The int32 page-table row of a paged head (a view of the buffer)."""
+        import torch
+        o = r.page_table_offset
+        return self.buffer[o: o + 4 * r.max_pages].view(torch.int32)
+
+    def middle_rows(self, r: RegionInfo, width_offset, width, m):
+        """Rows of middle positions m (int64 tensor) of region B: K (width_offset
+        = r.k_b_offset, width = n_kept) or V (r.v_b_offset, 128)."""
+        import torch
+        if r.page_rows == 0:
+            return self.rows(width_offset, r.rows_b, width)[m]
+        pt = self.page_table(r).to(torch.int64)
+        rows = pt[m // r.page_rows] * r.page_rows + m % r.page_rows
+        return self.rows(width_offset, r.rows_b, width)[rows]
 
     def lengths(self, layer):
         out = np.zeros(self.batch, dtype=np.int32)

@@ -61,33 +61,48 @@ struct lk_plan_s {
 namespace {
 
 struct Layout {
-  size_t off_len, off_cnt, off_heads, off_kept, off_spec;
+  size_t off_len, off_cnt, off_active, off_pt, off_free, off_heads, off_kept, off_spec;
   size_t off_pool[kNumPools];
   int64_t pool_rows[kNumPools];
   size_t total;
   int32_t spec_cap;
+  int32_t max_pages = 0;                 // 0: contiguous region B
+  int32_t num_pages[kNumPools] = {};     // paged: pages of each width class
+  int32_t free_off[kNumPools] = {};
   std::vector<HeadDesc> heads;
 };
 
-lk_status compute_layout(const lk_plan_s& p, int B, int cap, Layout* lay) {
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Region-B pages one (FULL, k > 0) head holds for a sequence of n tokens.
+inline int32_t pages_at(int n, int S, int W) { return (int32_t)ceil_div(std::max(0, n - S - W), kPageRows); }
+
+// middle_tokens < 0: region B contiguous per (layer, sequence, head), sized
+// for `cap` tokens.  Otherwise paged: each FULL head with k > 0 gets pages for
+// middle_tokens middle tokens summed over the batch, plus one partly filled
+// page per sequence (and never more than batch x max_pages).
+lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_tokens, Layout* lay) {
   const lk_plan_desc& d = p.d;
   const int L = d.num_layers, H = d.num_kv_heads;
+  const bool paged = middle_tokens >= 0;
+  lay->max_pages = paged ? std::max<int32_t>(1, pages_at(cap, d.sink, d.local)) : 0;
+  int64_t pages_per_head = 0;
+  if (paged) pages_per_head = std::min<int64_t>(ceil_div(middle_tokens, kPageRows) + B, (int64_t)B * lay->max_pages);
   size_t off = align_up(sizeof(DevHeader), 1024);
   lay->off_len = off;
   off = align_up(off + (size_t)L * B * 4, 1024);
   lay->off_cnt = off;
   off = align_up(off + (size_t)L * B * 4, 1024);
-  lay->off_heads = off;
-  off = align_up(off + (size_t)L * H * sizeof(HeadDesc), 1024);
-  lay->off_kept = off;
-  off = align_up(off + (size_t)L * H * kHeadDim * 2, 1024);
-  lay->off_spec = off;
-  off = align_up(off + (size_t)std::max(d.vocab, 1), 1024);
+  lay->off_active = off;
+  off = align_up(off + (size_t)B * 4, 1024);
+  lay->off_pt = off;
+  off = align_up(off + (size_t)L * B * H * lay->max_pages * 4, 1024);
 
   lay->spec_cap = d.special_capacity > 0 ? std::min(d.special_capacity, cap) : cap;
   lay->heads.assign((size_t)L * H, HeadDesc{});
   int64_t rows[kNumPools] = {0, 0, 0, 0, 0};
   int64_t ra = 0;
+  int64_t class_heads[kNumPools] = {0, 0, 0, 0, 0};
   for (int i = 0; i < L * H; ++i) {
     HeadDesc& hd = lay->heads[i];
     hd.policy = p.policy[i];
@@ -98,18 +113,55 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, Layout* lay) {
     hd.row_a = ra;
     ra += (int64_t)B * hd.cap_a;
     hd.pool_kb = kPoolK128;
+    if (hd.policy == kFull && hd.n_kept > 0) class_heads[pool_for_width(hd.n_kept)] += 1;
   }
   rows[kPoolK128] = ra;
   rows[kPoolV] = ra;
+  int64_t page_k[kNumPools] = {0, 0, 0, 0, 0}, page_v[kNumPools] = {0, 0, 0, 0, 0};
+  if (paged) {
+    int64_t free_total = 0;
+    for (int pl = 0; pl < kNumPools; ++pl) {
+      const int64_t np = class_heads[pl] * pages_per_head;
+      if (np > (int64_t)1 << 30)
+        return fail(LK_ERR_CAPACITY, "width class %d needs %lld pages", pool_width(pl), (long long)np);
+      lay->num_pages[pl] = (int32_t)np;
+      lay->free_off[pl] = (int32_t)free_total;
+      free_total += np;
+      page_k[pl] = rows[pl];
+      rows[pl] += np * kPageRows;
+      page_v[pl] = rows[kPoolV];
+      rows[kPoolV] += np * kPageRows;
+    }
+    if (free_total > ((int64_t)1 << 31) - 1) return fail(LK_ERR_CAPACITY, "%lld pages in all", (long long)free_total);
+  }
+  lay->off_free = off;
+  {
+    int64_t nfree = 0;
+    for (int pl = 0; pl < kNumPools; ++pl) nfree += lay->num_pages[pl];
+    off = align_up(off + (size_t)nfree * 4, 1024);
+  }
+  lay->off_heads = off;
+  off = align_up(off + (size_t)L * H * sizeof(HeadDesc), 1024);
+  lay->off_kept = off;
+  off = align_up(off + (size_t)L * H * kHeadDim * 2, 1024);
+  lay->off_spec = off;
+  off = align_up(off + (size_t)std::max(d.vocab, 1), 1024);
   for (int i = 0; i < L * H; ++i) {
     HeadDesc& hd = lay->heads[i];
     if (hd.policy == kFull && hd.n_kept > 0) {
-      hd.cap_b = std::max(0, cap - d.sink - d.local);
       hd.pool_kb = pool_for_width(hd.n_kept);
-      hd.krow_b = rows[hd.pool_kb];
-      rows[hd.pool_kb] += (int64_t)B * hd.cap_b;
-      hd.vrow_b = rows[kPoolV];
-      rows[kPoolV] += (int64_t)B * hd.cap_b;
+      if (paged) {
+        hd.cap_b = lay->max_pages * kPageRows;
+        hd.krow_b = page_k[hd.pool_kb];
+        hd.vrow_b = page_v[hd.pool_kb];
+        hd.free_off = lay->free_off[hd.pool_kb];
+      } else {
+        hd.cap_b = std::max(0, cap - d.sink - d.local);
+        hd.krow_b = rows[hd.pool_kb];
+        rows[hd.pool_kb] += (int64_t)B * hd.cap_b;
+        hd.vrow_b = rows[kPoolV];
+        rows[kPoolV] += (int64_t)B * hd.cap_b;
+      }
     }
   }
   for (int pl = 0; pl < kNumPools; ++pl) {
@@ -218,10 +270,30 @@ struct lk_cache_s {
   int B = 0, cap = 0;
   std::vector<int32_t> host_len;   // [L][B] tokens per layer and sequence (host mirror)
   std::vector<int32_t> len_upload; // [L][B] source of the prefill length copies
+  std::vector<int32_t> active;     // [B] host mirror of the slot flags
+  std::vector<int32_t> class_heads;  // [L][kNumPools] paged FULL heads of each width class
+  int64_t host_free[kNumPools] = {}; // paged: free pages per class (host mirror)
+  int32_t one = 1;                 // source of the slot-activation copy
   int32_t max_len(int layer) const {
     int32_t m = 0;
     for (int b = 0; b < B; ++b) m = std::max(m, host_len[(size_t)layer * B + b]);
     return m;
+  }
+  bool paged() const { return lay.max_pages > 0; }
+  // pages per class that taking sequence b of `layer` from n0 to n1 tokens needs
+  void pages_needed(int layer, int n0, int n1, int64_t* need) const {
+    if (!paged()) return;
+    const int d = pages_at(n1, cv.S, cv.W) - pages_at(n0, cv.S, cv.W);
+    if (d == 0) return;
+    for (int pl = 0; pl < kNumPools; ++pl) need[pl] += (int64_t)d * class_heads[(size_t)layer * kNumPools + pl];
+  }
+  lk_status take_pages(const int64_t* need, const char* who) {
+    for (int pl = 0; pl < kNumPools; ++pl)
+      if (need[pl] > host_free[pl])
+        return fail(LK_ERR_CAPACITY, "%s: width class %d needs %lld pages; %lld are free", who, pool_width(pl),
+                    (long long)need[pl], (long long)host_free[pl]);
+    for (int pl = 0; pl < kNumPools; ++pl) host_free[pl] -= need[pl];
+    return LK_OK;
   }
   CUtensorMap maps[kNumPools];
   int device = 0, num_sms = 0, decode_ctas = 0;
@@ -342,17 +414,28 @@ lk_status lk_plan_head(lk_plan plan, int32_t layer, int32_t kv_head, int32_t* po
   return LK_OK;
 }
 
-lk_status lk_cache_bytes(lk_plan plan, int32_t batch, int32_t capacity_tokens, size_t* bytes) {
+static lk_status cache_bytes_impl(lk_plan plan, int32_t batch, int32_t capacity_tokens, int64_t middle_tokens,
+                                  size_t* bytes) {
   if (!plan || !bytes) return fail(LK_ERR_ARG, "lk_cache_bytes: null argument");
   if (batch < 1 || (int64_t)batch * plan->d.num_kv_heads > (1 << 20))
     return fail(LK_ERR_ARG, "batch %d out of range", batch);
   if (capacity_tokens < 1 || capacity_tokens > (1 << 30))
     return fail(LK_ERR_ARG, "capacity_tokens %d out of [1, 2^30]", capacity_tokens);
   Layout lay;
-  lk_status st = compute_layout(*plan, batch, capacity_tokens, &lay);
+  lk_status st = compute_layout(*plan, batch, capacity_tokens, middle_tokens, &lay);
   if (st != LK_OK) return st;
   *bytes = lay.total;
   return LK_OK;
+}
+
+lk_status lk_cache_bytes(lk_plan plan, int32_t batch, int32_t capacity_tokens, size_t* bytes) {
+  return cache_bytes_impl(plan, batch, capacity_tokens, -1, bytes);
+}
+
+lk_status lk_cache_bytes_paged(lk_plan plan, int32_t batch, int32_t capacity_tokens, int64_t middle_tokens,
+                               size_t* bytes) {
+  if (middle_tokens < 0) return fail(LK_ERR_ARG, "lk_cache_bytes_paged: middle_tokens %lld < 0", (long long)middle_tokens);
+  return cache_bytes_impl(plan, batch, capacity_tokens, middle_tokens, bytes);
 }
 
 lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes) {
@@ -363,13 +446,13 @@ lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes) {
   return LK_OK;
 }
 
-lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
-                        void* stream, lk_cache* out) {
+static lk_status cache_init_impl(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
+                                 int64_t middle_tokens, void* stream, lk_cache* out) {
   if (!plan || !dev_buf || !out) return fail(LK_ERR_ARG, "lk_cache_init: null argument");
   *out = nullptr;
   if (!aligned(dev_buf, 256)) return fail(LK_ERR_ALIGN, "cache buffer must be 256-byte aligned");
   size_t need = 0;
-  lk_status st = lk_cache_bytes(plan, batch, capacity_tokens, &need);
+  lk_status st = cache_bytes_impl(plan, batch, capacity_tokens, middle_tokens, &need);
   if (st != LK_OK) return st;
   if (bytes < need) return fail(LK_ERR_CAPACITY, "cache buffer has %zu bytes; %zu needed", bytes, need);
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -377,25 +460,38 @@ lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch
 
   auto c = new lk_cache_s();
   c->plan = *plan;
-  compute_layout(c->plan, batch, capacity_tokens, &c->lay);
+  compute_layout(c->plan, batch, capacity_tokens, middle_tokens, &c->lay);
   c->buf = static_cast<uint8_t*>(dev_buf);
   c->bytes = bytes;
   c->B = batch;
   c->cap = capacity_tokens;
-  c->host_len.assign((size_t)plan->d.num_layers * batch, 0);
-  c->len_upload.assign((size_t)plan->d.num_layers * batch, 0);
+  const lk_plan_desc& d = plan->d;
+  const int L = d.num_layers, H = d.num_kv_heads;
+  c->host_len.assign((size_t)L * batch, 0);
+  c->len_upload.assign((size_t)L * batch, 0);
+  c->active.assign(batch, 1);
+  c->class_heads.assign((size_t)L * kNumPools, 0);
+  const Layout& lay = c->lay;
+  if (c->paged()) {
+    for (int i = 0; i < L * H; ++i) {
+      const HeadDesc& hd = lay.heads[i];
+      if (hd.policy == kFull && hd.n_kept > 0) c->class_heads[(size_t)(i / H) * kNumPools + hd.pool_kb] += 1;
+    }
+    for (int pl = 0; pl < kNumPools; ++pl) c->host_free[pl] = lay.num_pages[pl];
+  }
   cudaError_t err = cudaGetDevice(&c->device);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   if (err != cudaSuccess) {
     delete c;
     return cuda_fail(err, "lk_cache_init: device query");
   }
-  const lk_plan_desc& d = plan->d;
-  const Layout& lay = c->lay;
   CacheView& cv = c->cv;
   cv.hdr = reinterpret_cast<DevHeader*>(c->buf);
   cv.len = reinterpret_cast<int32_t*>(c->buf + lay.off_len);
   cv.cnt = reinterpret_cast<int32_t*>(c->buf + lay.off_cnt);
+  cv.active = reinterpret_cast<int32_t*>(c->buf + lay.off_active);
+  cv.page_table = c->paged() ? reinterpret_cast<int32_t*>(c->buf + lay.off_pt) : nullptr;
+  cv.free_list = reinterpret_cast<int32_t*>(c->buf + lay.off_free);
   cv.heads = reinterpret_cast<const HeadDesc*>(c->buf + lay.off_heads);
   cv.kept = reinterpret_cast<const int16_t*>(c->buf + lay.off_kept);
   cv.is_special = c->buf + lay.off_spec;
@@ -403,10 +499,10 @@ lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch
     cv.pool[pl] = reinterpret_cast<uint16_t*>(c->buf + lay.off_pool[pl]);
     cv.pool_rows[pl] = lay.pool_rows[pl];
   }
-  cv.L = d.num_layers;
+  cv.L = L;
   cv.B = batch;
   cv.Hq = d.num_q_heads;
-  cv.Hkv = d.num_kv_heads;
+  cv.Hkv = H;
   cv.G = d.num_q_heads / d.num_kv_heads;
   cv.S = d.sink;
   cv.W = d.local;
@@ -414,18 +510,29 @@ lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch
   cv.vocab = d.vocab;
   cv.capacity = capacity_tokens;
   cv.spec_cap = lay.spec_cap;
+  cv.max_pages = lay.max_pages;
 
-  // host image of the tables region [off_heads, off_pool[0])
-  const size_t tab_lo = lay.off_heads, tab_hi = lay.off_pool[0];
-  c->upload.assign(tab_hi - tab_lo, 0);
-  std::memcpy(c->upload.data(), lay.heads.data(), lay.heads.size() * sizeof(HeadDesc));
-  std::memcpy(c->upload.data() + (lay.off_kept - tab_lo), c->plan.kept.data(), c->plan.kept.size() * 2);
-  if (!c->plan.is_special.empty())
-    std::memcpy(c->upload.data() + (lay.off_spec - tab_lo), c->plan.is_special.data(), c->plan.is_special.size());
+  // host image of everything before the pools: header (free stack tops),
+  // lengths 0, slots active, page table -1, free stacks (pops hand out page
+  // 0, 1, 2, ... of each class), head table, kept channels, special table
+  const size_t tab_hi = lay.off_pool[0];
+  c->upload.assign(tab_hi, 0);
+  uint8_t* img = c->upload.data();
+  DevHeader* hdr = reinterpret_cast<DevHeader*>(img);
+  for (int pl = 0; pl < kNumPools; ++pl) hdr->free_top[pl] = lay.num_pages[pl];
+  int32_t* act = reinterpret_cast<int32_t*>(img + lay.off_active);
+  for (int b = 0; b < batch; ++b) act[b] = 1;
+  int32_t* pt = reinterpret_cast<int32_t*>(img + lay.off_pt);
+  std::fill(pt, pt + (size_t)L * batch * H * lay.max_pages, -1);
+  int32_t* fl = reinterpret_cast<int32_t*>(img + lay.off_free);
+  for (int pl = 0; pl < kNumPools; ++pl)
+    for (int32_t i = 0; i < lay.num_pages[pl]; ++i) fl[lay.free_off[pl] + i] = lay.num_pages[pl] - 1 - i;
+  std::memcpy(img + lay.off_heads, lay.heads.data(), lay.heads.size() * sizeof(HeadDesc));
+  std::memcpy(img + lay.off_kept, c->plan.kept.data(), c->plan.kept.size() * 2);
+  if (!c->plan.is_special.empty()) std::memcpy(img + lay.off_spec, c->plan.is_special.data(), c->plan.is_special.size());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  err = cudaMemsetAsync(c->buf, 0, lay.total, s);
-  if (err == cudaSuccess)
-    err = cudaMemcpyAsync(c->buf + tab_lo, c->upload.data(), c->upload.size(), cudaMemcpyHostToDevice, s);
+  err = cudaMemsetAsync(c->buf + tab_hi, 0, lay.total - tab_hi, s);
+  if (err == cudaSuccess) err = cudaMemcpyAsync(c->buf, img, tab_hi, cudaMemcpyHostToDevice, s);
   if (err != cudaSuccess) {
     delete c;
     return cuda_fail(err, "lk_cache_init: upload");
@@ -458,6 +565,18 @@ lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch
   return LK_OK;
 }
 
+lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
+                        void* stream, lk_cache* out) {
+  return cache_init_impl(plan, dev_buf, bytes, batch, capacity_tokens, -1, stream, out);
+}
+
+lk_status lk_cache_init_paged(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
+                              int64_t middle_tokens, void* stream, lk_cache* out) {
+  if (out) *out = nullptr;
+  if (middle_tokens < 0) return fail(LK_ERR_ARG, "lk_cache_init_paged: middle_tokens %lld < 0", (long long)middle_tokens);
+  return cache_init_impl(plan, dev_buf, bytes, batch, capacity_tokens, middle_tokens, stream, out);
+}
+
 void lk_cache_destroy(lk_cache cache) { delete cache; }
 
 lk_status lk_workspace_init(lk_cache cache, void* workspace, size_t ws_bytes, void* stream) {
@@ -470,52 +589,106 @@ lk_status lk_workspace_init(lk_cache cache, void* workspace, size_t ws_bytes, vo
   return LK_OK;
 }
 
-// Shared by the uniform and ragged prefill: lengths go to the device length
-// row first, then the copy kernels read each sequence's length there.
-static lk_status prefill_impl(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
-                              const int32_t* lens, int32_t n_max, void* stream) {
+// Shared by the uniform, ragged and single-sequence prefill of sequences
+// b0 .. b0 + nb - 1: lengths go to the device length row first, then the copy
+// kernels read each sequence's length there.
+static lk_status prefill_impl(lk_cache cache, int32_t layer, int32_t b0, int32_t nb, const void* k, const void* v,
+                              const int32_t* ids, const int32_t* lens, int32_t n_max, void* stream) {
   if (!cache) return fail(LK_ERR_ARG, "lk_prefill: null cache");
   if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_prefill: layer %d out of range", layer);
   if (n_max < 0) return fail(LK_ERR_ARG, "lk_prefill: n = %d < 0", n_max);
-  if (cache->max_len(layer) != 0) return fail(LK_ERR_STATE, "lk_prefill: layer %d already holds tokens", layer);
-  if (n_max > cache->cap) return fail(LK_ERR_CAPACITY, "lk_prefill: n = %d exceeds capacity %d", n_max, cache->cap);
   const int B = cache->B;
-  int32_t* up = &cache->len_upload[(size_t)layer * B];
-  for (int b = 0; b < B; ++b) {
-    const int32_t nb = lens ? lens[b] : n_max;
-    if (nb < 0 || nb > n_max)
-      return fail(LK_ERR_ARG, "lk_prefill: length %d of sequence %d outside [0, %d]", nb, b, n_max);
-    up[b] = nb;
+  for (int b = b0; b < b0 + nb; ++b)
+    if (cache->host_len[(size_t)layer * B + b] != 0)
+      return fail(LK_ERR_STATE, "lk_prefill: sequence %d of layer %d already holds tokens", b, layer);
+  if (n_max > cache->cap) return fail(LK_ERR_CAPACITY, "lk_prefill: n = %d exceeds capacity %d", n_max, cache->cap);
+  int32_t* up = &cache->len_upload[(size_t)layer * B + b0];
+  int64_t need[kNumPools] = {0, 0, 0, 0, 0};
+  for (int i = 0; i < nb; ++i) {
+    const int32_t n = lens ? lens[i] : n_max;
+    if (n < 0 || n > n_max)
+      return fail(LK_ERR_ARG, "lk_prefill: length %d of sequence %d outside [0, %d]", n, b0 + i, n_max);
+    up[i] = n;
+    cache->pages_needed(layer, 0, n, need);
   }
   if (n_max == 0) return LK_OK;
   if (!k || !v) return fail(LK_ERR_ARG, "lk_prefill: null k or v");
   if (!aligned(k, 16) || !aligned(v, 16)) return fail(LK_ERR_ALIGN, "lk_prefill: k and v must be 16-byte aligned");
   if (ids && !aligned(ids, 4)) return fail(LK_ERR_ALIGN, "lk_prefill: ids must be 4-byte aligned");
+  lk_status st = cache->take_pages(need, "lk_prefill");
+  if (st != LK_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t err = cudaMemcpyAsync(cache->cv.len + (size_t)layer * B, up, (size_t)B * 4, cudaMemcpyHostToDevice, s);
+  cudaError_t err =
+      cudaMemcpyAsync(cache->cv.len + (size_t)layer * B + b0, up, (size_t)nb * 4, cudaMemcpyHostToDevice, s);
   if (err != cudaSuccess) return cuda_fail(err, "lk_prefill: length upload");
   PrefillArgs a;
   a.cv = cache->cv;
   a.layer = layer;
+  a.b0 = b0;
+  a.nb = nb;
   a.k = static_cast<const uint16_t*>(k);
   a.v = static_cast<const uint16_t*>(v);
   a.ids = ids;
   a.n = n_max;
   err = launch_prefill(a, cache->plan.layer_special[layer] != 0, cache->num_sms, s);
-  if (err != cudaSuccess) return cuda_fail(err, "lk_prefill launch");
-  for (int b = 0; b < B; ++b) cache->host_len[(size_t)layer * B + b] = up[b];
+  if (err != cudaSuccess) {
+    for (int pl = 0; pl < kNumPools; ++pl) cache->host_free[pl] += need[pl];
+    return cuda_fail(err, "lk_prefill launch");
+  }
+  for (int i = 0; i < nb; ++i) cache->host_len[(size_t)layer * B + b0 + i] = up[i];
   return LK_OK;
 }
 
 lk_status lk_prefill(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids, int32_t n,
                      void* stream) {
-  return prefill_impl(cache, layer, k, v, ids, nullptr, n, stream);
+  if (!cache) return fail(LK_ERR_ARG, "lk_prefill: null cache");
+  return prefill_impl(cache, layer, 0, cache->B, k, v, ids, nullptr, n, stream);
 }
 
 lk_status lk_prefill_ragged(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
                             const int32_t* lens, int32_t n_max, void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_prefill_ragged: null cache");
   if (!lens) return fail(LK_ERR_ARG, "lk_prefill_ragged: null lens");
-  return prefill_impl(cache, layer, k, v, ids, lens, n_max, stream);
+  return prefill_impl(cache, layer, 0, cache->B, k, v, ids, lens, n_max, stream);
+}
+
+lk_status lk_prefill_sequence(lk_cache cache, int32_t layer, int32_t b, const void* k, const void* v,
+                              const int32_t* ids, int32_t n, void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_prefill_sequence: null cache");
+  if (b < 0 || b >= cache->B) return fail(LK_ERR_ARG, "lk_prefill_sequence: sequence %d out of range", b);
+  lk_status st = prefill_impl(cache, layer, b, 1, k, v, ids, nullptr, n, stream);
+  if (st != LK_OK || cache->active[b]) return st;
+  cudaError_t err = cudaMemcpyAsync(cache->cv.active + b, &cache->one, 4, cudaMemcpyHostToDevice,
+                                    static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_prefill_sequence: slot activation");
+  cache->active[b] = 1;
+  return LK_OK;
+}
+
+lk_status lk_release_sequence(lk_cache cache, int32_t b, void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_release_sequence: null cache");
+  if (b < 0 || b >= cache->B) return fail(LK_ERR_ARG, "lk_release_sequence: sequence %d out of range", b);
+  cudaError_t err = launch_release(cache->cv, b, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_release_sequence launch");
+  for (int l = 0; l < cache->cv.L; ++l) {
+    int32_t& n = cache->host_len[(size_t)l * cache->B + b];
+    int64_t back[kNumPools] = {0, 0, 0, 0, 0};
+    cache->pages_needed(l, 0, n, back);
+    for (int pl = 0; pl < kNumPools; ++pl) cache->host_free[pl] += back[pl];
+    n = 0;
+  }
+  cache->active[b] = 0;
+  return LK_OK;
+}
+
+lk_status lk_cache_pages(lk_cache cache, int32_t width, int64_t* total, int64_t* free_pages) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_cache_pages: null cache");
+  if (width != 32 && width != 64 && width != 96 && width != 128)
+    return fail(LK_ERR_ARG, "lk_cache_pages: width %d is not 32, 64, 96 or 128", width);
+  const int pl = pool_for_width(width);
+  if (total) *total = cache->lay.num_pages[pl];
+  if (free_pages) *free_pages = cache->host_free[pl];
+  return LK_OK;
 }
 
 lk_status lk_append_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* k, const void* v,
@@ -526,9 +699,18 @@ lk_status lk_append_layers(lk_cache cache, int32_t layer0, int32_t nlayers, cons
   if (!k || !v) return fail(LK_ERR_ARG, "lk_append: null k or v");
   if (!aligned(k, 16) || !aligned(v, 16)) return fail(LK_ERR_ALIGN, "lk_append: k and v must be 16-byte aligned");
   if (ids && !aligned(ids, 4)) return fail(LK_ERR_ALIGN, "lk_append: ids must be 4-byte aligned");
+  const int B = cache->B;
+  int64_t need[kNumPools] = {0, 0, 0, 0, 0};
   for (int l = layer0; l < layer0 + nlayers; ++l)
-    if (cache->max_len(l) >= cache->cap)
-      return fail(LK_ERR_CAPACITY, "lk_append: a sequence of layer %d is full (%d tokens)", l, cache->cap);
+    for (int b = 0; b < B; ++b) {
+      if (!cache->active[b]) continue;
+      const int n = cache->host_len[(size_t)l * B + b];
+      if (n >= cache->cap)
+        return fail(LK_ERR_CAPACITY, "lk_append: sequence %d of layer %d is full (%d tokens)", b, l, cache->cap);
+      cache->pages_needed(l, n, n + 1, need);
+    }
+  lk_status st = cache->take_pages(need, "lk_append");
+  if (st != LK_OK) return st;
   AppendArgs a;
   a.cv = cache->cv;
   a.layer = layer0;
@@ -537,9 +719,13 @@ lk_status lk_append_layers(lk_cache cache, int32_t layer0, int32_t nlayers, cons
   a.v = static_cast<const uint16_t*>(v);
   a.ids = ids;
   cudaError_t err = launch_append(a, static_cast<cudaStream_t>(stream));
-  if (err != cudaSuccess) return cuda_fail(err, "lk_append launch");
+  if (err != cudaSuccess) {
+    for (int pl = 0; pl < kNumPools; ++pl) cache->host_free[pl] += need[pl];
+    return cuda_fail(err, "lk_append launch");
+  }
   for (int l = layer0; l < layer0 + nlayers; ++l)
-    for (int b = 0; b < cache->B; ++b) cache->host_len[(size_t)l * cache->B + b] += 1;
+    for (int b = 0; b < B; ++b)
+      if (cache->active[b]) cache->host_len[(size_t)l * B + b] += 1;
   return LK_OK;
 }
 
@@ -674,7 +860,18 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
   out->rows_b = hd.cap_b;
   out->k_a_offset = lay.off_pool[kPoolK128] + (uint64_t)ra * kHeadDim * 2;
   out->v_a_offset = lay.off_pool[kPoolV] + (uint64_t)ra * kHeadDim * 2;
-  if (hd.cap_b > 0) {
+  out->page_rows = 0;
+  out->max_pages = 0;
+  out->page_table_offset = 0;
+  if (hd.cap_b > 0 && cache->paged()) {
+    out->rows_b = (int32_t)std::min<int64_t>((int64_t)lay.num_pages[hd.pool_kb] * kPageRows, INT32_MAX);
+    out->k_b_offset = lay.off_pool[hd.pool_kb] + (uint64_t)hd.krow_b * hd.n_kept * 2;
+    out->v_b_offset = lay.off_pool[kPoolV] + (uint64_t)hd.vrow_b * kHeadDim * 2;
+    out->page_rows = kPageRows;
+    out->max_pages = lay.max_pages;
+    out->page_table_offset =
+        lay.off_pt + ((((uint64_t)layer * cache->B + b) * cache->cv.Hkv + kv_head) * lay.max_pages) * 4;
+  } else if (hd.cap_b > 0) {
     out->k_b_offset = lay.off_pool[hd.pool_kb] + (uint64_t)(hd.krow_b + (int64_t)b * hd.cap_b) * hd.n_kept * 2;
     out->v_b_offset = lay.off_pool[kPoolV] + (uint64_t)(hd.vrow_b + (int64_t)b * hd.cap_b) * kHeadDim * 2;
   } else {

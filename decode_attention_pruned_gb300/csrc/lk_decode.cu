@@ -99,13 +99,27 @@ __device__ __forceinline__ EntryId entry_id(const DecodeArgs& a, int e) {
 }
 
 // Lengths and special counts are read through L2 (they are written by the
-// preceding append kernel).
-__device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) {
+// preceding append kernel).  The loads are split from the arithmetic so the
+// producer can issue the next entry's loads one entry ahead.
+struct EntryLen {
+  int n;      // tokens of the sequence in this layer
+  int cnt;    // special rows (SPECIAL heads), else 0
+};
+__device__ __forceinline__ EntryLen entry_len(const DecodeArgs& a, int e) {
   const CacheView& cv = a.cv;
   const EntryId id = entry_id(a, e);
-  const int b = id.b;
   const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
-  const int N = __ldcg(&cv.len[id.l * cv.B + b]);
+  EntryLen r;
+  r.n = __ldcg(&cv.len[id.l * cv.B + id.b]);
+  r.cnt = hd.policy == kSpecial ? __ldcg(&cv.cnt[id.l * cv.B + id.b]) : 0;
+  return r;
+}
+
+__device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen len) {
+  const CacheView& cv = a.cv;
+  const EntryId id = entry_id(a, e);
+  const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+  const int N = len.n;
   Entry r{0, 0, 0};
   if (hd.policy == kFull) {
     r.n_a = min(N, cv.S + cv.W);
@@ -116,12 +130,14 @@ __device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) {
   } else if (hd.policy == kLocal) {
     r.n_a = min(N, cv.W_loc);
   } else {
-    r.n_a = min(__ldcg(&cv.cnt[id.l * cv.B + b]), hd.cap_a);
+    r.n_a = min(len.cnt, hd.cap_a);
   }
   r.n_a = min(r.n_a, hd.cap_a);
   r.n_b = min(r.n_b, hd.cap_b);
   return r;
 }
+
+__device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) { return entry_from(a, e, entry_len(a, e)); }
 
 __device__ __forceinline__ uint64_t row_cost_b(int kb) { return (uint64_t)(kb / 16 + 8); }
 
@@ -206,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[0] = E;       // first entry of this CTA
     misc[1] = 0;       // its line offset
     misc[2] = 0;       // last-CTA flag of a segment
+    misc[3] = misc[4] = misc[5] = 0;   // geometry of the first entry
   }
   if (warp == kConsumerWarps && lane == 0) {
     tma_prefetch_map(&tm_k128);
@@ -221,11 +238,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();
   grid_launch_dependents();
 
-  // ---- the line: per-thread chunks of entries, block exclusive scan
+  // ---- the line: per-thread chunks of entries, block exclusive scan.  The
+  // lengths of a chunk's first kKeep entries stay in registers for the
+  // second pass; the rest load kKeep at a time.
+  constexpr int kKeep = 4;
   const int per = (E + kThreads - 1) / kThreads;
   const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
+  EntryLen keep[kKeep];
+#pragma unroll
+  for (int i = 0; i < kKeep; ++i) keep[i] = e_lo + i < e_hi ? entry_len(a, e_lo + i) : EntryLen{0, 0};
   uint64_t local = 0;
-  for (int e = e_lo; e < e_hi; ++e) local += entry_cost(entry_geometry(a, e));
+#pragma unroll
+  for (int i = 0; i < kKeep; ++i)
+    if (e_lo + i < e_hi) local += entry_cost(entry_from(a, e_lo + i, keep[i]));
+  for (int e = e_lo + kKeep; e < e_hi; e += kKeep) {
+    EntryLen t[kKeep];
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) t[i] = e + i < e_hi ? entry_len(a, e + i) : EntryLen{0, 0};
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i)
+      if (e + i < e_hi) local += entry_cost(entry_from(a, e + i, t[i]));
+  }
   uint64_t incl = local;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -246,16 +279,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t start = cta < P ? ((uint64_t)cta * C) / P : C;
   const uint64_t end = cta < P ? ((uint64_t)(cta + 1) * C) / P : C;
   if (local > 0 && excl <= start && start < excl + local) {
+    // this chunk holds the CTA's first row: its entry, line offset and
+    // geometry go to the producer through shared memory
     uint64_t acc = excl;
-    for (int e = e_lo; e < e_hi; ++e) {
-      const uint64_t c = entry_cost(entry_geometry(a, e));
-      if (acc + c > start) {
-        misc[0] = e;
-        misc[1] = (int64_t)acc;
-        break;
+    int found = -1;
+    Entry fg{0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) {
+      if (found < 0 && e_lo + i < e_hi) {
+        const Entry g = entry_from(a, e_lo + i, keep[i]);
+        const uint64_t c = entry_cost(g);
+        if (acc + c > start) {
+          found = e_lo + i;
+          fg = g;
+        } else {
+          acc += c;
+        }
       }
-      acc += c;
     }
+    for (int e = e_lo + kKeep; found < 0 && e < e_hi; ++e) {
+      const Entry g = entry_geometry(a, e);
+      const uint64_t c = entry_cost(g);
+      if (acc + c > start) {
+        found = e;
+        fg = g;
+      } else {
+        acc += c;
+      }
+    }
+    misc[0] = found;
+    misc[1] = (int64_t)acc;
+    misc[3] = fg.n_a;
+    misc[4] = fg.n_b;
+    misc[5] = fg.kb;
   }
   __syncthreads();
 
@@ -289,22 +345,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         head = at + bytes;
         return true;
       };
-      int e = (int)misc[0];
+      const int e0 = (int)misc[0];
+      int e = e0;
       uint64_t off = (uint64_t)misc[1];
+      // entry geometry: the first from the scan, later ones from lengths
+      // loaded one entry ahead
+      Entry g{(int)misc[3], (int)misc[4], (int)misc[5]};
+      EntryLen ahead{0, 0};
+      if (e + 1 < E) ahead = entry_len(a, e + 1);
       for (; ok && e < E && off < end; ++e) {
-        const Entry g = entry_geometry(a, e);
+        if (e != e0) {
+          g = entry_from(a, e, ahead);
+          if (e + 1 < E) ahead = entry_len(a, e + 1);
+        }
         const uint64_t cost = entry_cost(g);
         const uint64_t cb = row_cost_b(g.kb);
         const uint64_t off_b = off + (uint64_t)kUnitsA * g.n_a;
         int a0, a1, b0, b1;
         rows_in_range(off, kUnitsA, g.n_a, start, end, a0, a1);
         rows_in_range(off_b, cb, g.n_b, start, end, b0, b1);
+        // paged region B: tiles end at page boundaries (the box may read
+        // past a page end; those rows are beyond nrows and ignored)
+        const bool paged = cv.max_pages > 0;
         const int nta = (a1 - a0 + kTileRows - 1) / kTileRows;
-        const int ntb = (b1 - b0 + kTileRows - 1) / kTileRows;
+        const int ntb = b1 <= b0  ? 0
+                        : paged ? (b1 - 1) / kPageRows - b0 / kPageRows + 1
+                                : (b1 - b0 + kTileRows - 1) / kTileRows;
         if (nta + ntb > 0) {
           const EntryId id = entry_id(a, e);
           const int b = id.b;
           const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+          const int32_t* pt =
+              cv.page_table + (((int64_t)id.l * cv.B + b) * cv.Hkv + id.h) * cv.max_pages;
           const uint64_t last_row_off = g.n_b > 0 ? off_b + cb * (g.n_b - 1) : off + (uint64_t)kUnitsA * (g.n_a - 1);
           // the entry's first / last owning CTA is read only from the segment's
           // last descriptor: work it out after the first load is in flight
@@ -313,20 +385,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             fc = range_owner(off, C, P);
             lc = range_owner(last_row_off, C, P);
           }
+          int32_t page_ahead = 0;
           for (int j = 0; j < nta + ntb; ++j) {
             const bool in_a = j < nta;
             const int width = in_a ? kHeadDim : g.kb;
+            int r, rend;
+            int32_t page = 0;
+            if (in_a) {
+              r = a0 + j * kTileRows;
+              rend = min(a1, r + kTileRows);
+            } else if (paged) {
+              const int pg = b0 / kPageRows + (j - nta);
+              r = max(b0, pg * kPageRows);
+              rend = min(b1, (pg + 1) * kPageRows);
+              // page ids load one tile ahead (and before the slot wait); a
+              // missing page (status already recorded) reads page 0
+              page = j == nta ? __ldcg(pt + pg) : page_ahead;
+              if (j + 1 < nta + ntb) page_ahead = __ldcg(pt + pg + 1);
+              page = max(0, page);
+            } else {
+              r = b0 + (j - nta) * kTileRows;
+              rend = min(b1, r + kTileRows);
+            }
             uint32_t at = 0;
             if (!reserve(stage_bytes(width), at)) {
               ok = false;
               break;
             }
             const uint32_t stage = issued % kSlots;
-            const int r = in_a ? a0 + j * kTileRows : b0 + (j - nta) * kTileRows;
             StageDesc d;
             d.e = e;
             d.region = in_a ? 0 : 1;
-            d.nrows = min(kTileRows, (in_a ? a1 : b1) - r);
+            d.nrows = rend - r;
             d.width = in_a ? kHeadDim : g.kb;
             d.flags = (j == 0 ? kFirst : 0) | (j + 1 == nta + ntb ? kLast : 0);
             d.first_cta = fc;
@@ -342,8 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(kdst, &tm_k128, 0, row, 0, fb, policy);
               tma_load_3d(vdst, &tm_v, 0, row, 0, fb, policy);
             } else {
-              const int32_t krow = (int32_t)(hd.krow_b + (int64_t)b * hd.cap_b + r);
-              const int32_t vrow = (int32_t)(hd.vrow_b + (int64_t)b * hd.cap_b + r);
+              const int64_t rb = paged ? (int64_t)page * kPageRows + r % kPageRows : (int64_t)b * hd.cap_b + r;
+              const int32_t krow = (int32_t)(hd.krow_b + rb);
+              const int32_t vrow = (int32_t)(hd.vrow_b + rb);
               switch (hd.pool_kb) {
                 case kPoolK32: tma_load_2d(kdst, &tm_k32, 0, krow, fb, policy); break;
                 case kPoolK64: tma_load_2d(kdst, &tm_k64, 0, krow, fb, policy); break;

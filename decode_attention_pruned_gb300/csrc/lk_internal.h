@@ -1,15 +1,21 @@
 // Internal data structures shared by the host API and the device kernels.
 //
 // Device layout of a cache buffer (every block 1024-byte aligned):
-//   DevHeader | len[L][B] | cnt[L][B] | HeadDesc[L][Hkv] | kept[L][Hkv][128] i16
-//   | is_special[vocab] u8 | pool K128 | pool V | pool K32 | pool K64 | pool K96
+//   DevHeader | len[L][B] | cnt[L][B] | active[B] | page table | free lists
+//   | HeadDesc[L][Hkv] | kept[L][Hkv][128] i16 | is_special[vocab] u8
+//   | pool K128 | pool V | pool K32 | pool K64 | pool K96
 //
 // Pools are 2-D row arrays (rows x width bf16) so that one TMA tensor map
 // covers each; heads of equal kept width share a pool (the head grouping of
 // LeanK section 3.1).  Region A (full width: sinks + window ring, LOCAL ring,
 // SPECIAL rows) of every head sits at the same row index in pools K128 and V.
 // Region B (middle tokens of FULL heads with k > 0) has its K rows in the
-// pool of width k and its V rows after all region-A rows of pool V.
+// pool of width k and its V rows after all region-A rows of pool V: either
+// contiguous per (layer, sequence, head), or in 128-row pages drawn from a
+// page area per width class (page p of class c: K rows krow_b + 128p.. of
+// pool c, V rows vrow_b + 128p.. of pool V), located through the page table
+// [L][B][Hkv][max_pages].  Free pages of each class sit on a device stack, so
+// appends allocate pages inside the kernel (graph replays included).
 #pragma once
 #include <stdint.h>
 
@@ -19,6 +25,7 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 8;        // query heads per kv head handled by one mma n8 tile
 constexpr int kMaxCtas = 256;       // decode grid cap (partial workspace; combine staging np*G <= 2048)
 constexpr int kTmaBoxRows = 128;    // token rows per TMA box = decode tile rows
+constexpr int kPageRows = 128;      // middle rows per page (paged caches)
 
 enum Policy : int32_t { kFull = 0, kLocal = 1, kSpecial = 2 };
 enum Pool : int32_t { kPoolK128 = 0, kPoolV = 1, kPoolK32 = 2, kPoolK64 = 3, kPoolK96 = 4, kNumPools = 5 };
@@ -26,7 +33,7 @@ enum Pool : int32_t { kPoolK128 = 0, kPoolV = 1, kPoolK32 = 2, kPoolK64 = 3, kPo
 // Sticky device status bits (cache header).
 enum StatusBits : uint32_t {
   kStatusTimeout = 1u << 0,     // a bounded wait ran out
-  kStatusCapacity = 1u << 1,    // a SPECIAL head overflowed its rows or a layer was full
+  kStatusCapacity = 1u << 1,    // a SPECIAL head overflowed its rows, a layer was full or no page was free
   kStatusBadId = 1u << 2,       // token id outside [0, vocab)
 };
 
@@ -35,24 +42,29 @@ struct HeadDesc {                 // one (layer, kv head)
   int32_t n_kept;                 // k for FULL heads, 0 otherwise
   int32_t cap_a;                  // region-A rows per sequence
   int32_t cap_b;                  // region-B rows per sequence (0 if none)
-  int32_t pool_kb;                // pool of region-B K rows
-  int32_t pad;
+  int32_t pool_kb;                // pool of region-B K rows (= its page class)
+  int32_t free_off;               // paged: first entry of the class's free stack
   int64_t row_a;                  // first region-A row (sequence 0) in K128 and V
-  int64_t krow_b;                 // first region-B row (sequence 0) in pool_kb
-  int64_t vrow_b;                 // first region-B row (sequence 0) in V
+  int64_t krow_b;                 // first region-B row (sequence 0) in pool_kb; paged: page area
+  int64_t vrow_b;                 // first region-B row (sequence 0) in V; paged: page area
 };
 static_assert(sizeof(HeadDesc) == 48, "HeadDesc layout");
 
 struct DevHeader {
   uint32_t status;
-  uint32_t pad[63];
+  int32_t free_top[kNumPools];    // paged: free pages on each class's stack
+  uint32_t pad[58];
 };
+static_assert(sizeof(DevHeader) == 256, "DevHeader layout");
 
 // Pointers into one cache buffer, filled at cache init.
 struct CacheView {
   DevHeader* hdr;
   int32_t* len;                   // [L][B] tokens per layer and sequence
   int32_t* cnt;                   // [L][B] special-token rows per layer and sequence
+  int32_t* active;                // [B] 0: released slot, appends skip it
+  int32_t* page_table;            // [L][B][Hkv][max_pages] or null (contiguous region B)
+  int32_t* free_list;             // free page ids, class stacks at HeadDesc::free_off
   const HeadDesc* heads;          // [L][Hkv]
   const int16_t* kept;            // [L][Hkv][128] kept channels ascending
   const uint8_t* is_special;      // [vocab]
@@ -60,6 +72,7 @@ struct CacheView {
   int64_t pool_rows[kNumPools];
   int32_t L, B, Hq, Hkv, G, S, W, W_loc, vocab, capacity;
   int32_t spec_cap;               // rows of a SPECIAL head per sequence
+  int32_t max_pages;              // pages per (layer, sequence, head); 0: not paged
 };
 
 inline int pool_width(int pool) {

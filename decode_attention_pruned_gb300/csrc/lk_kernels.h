@@ -32,16 +32,18 @@ struct AppendArgs {
 struct PrefillArgs {
   CacheView cv;
   int32_t layer;
-  const uint16_t* k;        // bf16 [B][n][Hkv][128]
+  int32_t b0, nb;           // sequences b0 .. b0 + nb - 1
+  const uint16_t* k;        // bf16 [nb][n][Hkv][128]
   const uint16_t* v;
-  const int32_t* ids;       // [B][n] or null
-  int32_t n;
+  const int32_t* ids;       // [nb][n] or null
+  int32_t n;                // tokens per sequence in k / v / ids (the longest length)
 };
 
 size_t decode_smem_bytes();
 cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int ctas, cudaStream_t stream);
 cudaError_t launch_append(const AppendArgs& args, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& args, bool has_special, int num_sms, cudaStream_t stream);
+cudaError_t launch_release(const CacheView& cv, int b, cudaStream_t stream);
 cudaError_t launch_build_masks(const float* alpha, const uint8_t* eligible, int nh, double pct, int align,
                                int exact, uint8_t* masks, cudaStream_t stream);
 

@@ -13,6 +13,13 @@
 //   SPECIAL appended at row `count` only if its id is special.
 // Prefill of n tokens writes each position where n successive appends leave
 // it: sinks, the last W positions in their ring rows, the middle in K_prun.
+//
+// Paged caches hold the middle of each (layer, sequence, head) in 128-row
+// pages of its width class: an append whose eviction starts a new page pops
+// one from the class's free stack (an atomic on the stack top), prefill pops
+// all the pages a sequence needs at once, and release pushes them back.  The
+// host checks that enough pages are free before it launches, so a pop that
+// finds the stack empty only records kStatusCapacity.
 #include <cuda_runtime.h>
 
 #include "lk_device.cuh"
@@ -42,6 +49,43 @@ __device__ __forceinline__ void write_middle(const CacheView& cv, const HeadDesc
   row8(cv.pool[kPoolV], brow_v)[lane] = v_word;
 }
 
+__device__ __forceinline__ int32_t* page_row(const CacheView& cv, int layer, int b, int h) {
+  return cv.page_table + (((int64_t)layer * cv.B + b) * cv.Hkv + h) * cv.max_pages;
+}
+
+// Pops `k` pages of the head's class into dst[0..k) (page ids in the order the
+// stack hands them out); on an empty stack restores the top, fills -1 and
+// records kStatusCapacity.
+__device__ void pop_pages(const CacheView& cv, const HeadDesc& hd, int k, int32_t* dst) {
+  if (k <= 0) return;
+  int* top = &cv.hdr->free_top[hd.pool_kb];
+  const int t = atomicSub(top, k);
+  if (t < k) {
+    atomicAdd(top, k);
+    set_status(cv, kStatusCapacity);
+    for (int i = 0; i < k; ++i) dst[i] = -1;
+    return;
+  }
+  for (int i = 0; i < k; ++i) dst[i] = __ldcg(&cv.free_list[hd.free_off + t - 1 - i]);
+}
+
+// K_prun / V rows of middle row `mid` of sequence b of a head; `page` is the
+// page holding it (paged caches).  False if that page is missing (a pop found
+// no free page).
+__device__ __forceinline__ bool middle_rows(const CacheView& cv, const HeadDesc& hd, int b, int mid, int32_t page,
+                                            int64_t& krow, int64_t& vrow) {
+  if (cv.max_pages == 0) {
+    krow = hd.krow_b + (int64_t)b * hd.cap_b + mid;
+    vrow = hd.vrow_b + (int64_t)b * hd.cap_b + mid;
+    return true;
+  }
+  if (page < 0) return false;
+  const int64_t r = (int64_t)page * kPageRows + mid % kPageRows;
+  krow = hd.krow_b + r;
+  vrow = hd.vrow_b + r;
+  return true;
+}
+
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
   grid_dependency_wait();
   grid_launch_dependents();
@@ -66,8 +110,12 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     s_n = n;
     s_cnt = __ldcg(&cv.cnt[lb]);
     s_special = special;
-    s_ok = n < cv.capacity;
-    if (!s_ok) set_status(cv, kStatusCapacity);
+    // a released slot takes no tokens until it is prefilled again
+    s_ok = __ldcg(&cv.active[b]) != 0;
+    if (s_ok && n >= cv.capacity) {
+      s_ok = 0;
+      set_status(cv, kStatusCapacity);
+    }
   }
   __syncthreads();
   if (!s_ok) return;
@@ -88,11 +136,26 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
         slot = cv.S + (n - cv.S) % cv.W;
         if (n - cv.S >= cv.W && hd.n_kept > 0) {
           const int mid = n - cv.W - cv.S;               // K_prun row of token n - W
-          const uint16_t* k_old = ka_pool + (abase + slot) * kHeadDim;
-          const uint2 v_old = row8(va_pool, abase + slot)[lane];
-          write_middle(cv, hd, cv.kept + ((size_t)layer * cv.Hkv + h) * kHeadDim,
-                       hd.krow_b + (int64_t)b * hd.cap_b + mid, hd.vrow_b + (int64_t)b * hd.cap_b + mid,
-                       k_old, v_old, lane);
+          int32_t page = -1;
+          if (cv.max_pages > 0) {
+            int32_t* pt = page_row(cv, layer, b, h) + mid / kPageRows;
+            if (mid % kPageRows == 0) {         // first row of a new page
+              if (lane == 0) {
+                pop_pages(cv, hd, 1, &page);
+                *pt = page;
+              }
+              page = __shfl_sync(0xffffffffu, page, 0);
+            } else {
+              page = __ldcg(pt);
+            }
+          }
+          int64_t krow, vrow;
+          if (middle_rows(cv, hd, b, mid, page, krow, vrow)) {
+            const uint16_t* k_old = ka_pool + (abase + slot) * kHeadDim;
+            const uint2 v_old = row8(va_pool, abase + slot)[lane];
+            write_middle(cv, hd, cv.kept + ((size_t)layer * cv.Hkv + h) * kHeadDim, krow, vrow, k_old, v_old,
+                         lane);
+          }
           __syncwarp();
         }
       }
@@ -120,27 +183,28 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
 
 // The layer's per-sequence lengths are already in len[layer][b] (the host
 // enqueues them first); inputs are padded to n_max tokens per sequence.
+// Sequences b0 .. b0 + nb - 1 are filled; input sequence i is sequence b0 + i.
 __global__ void __launch_bounds__(256) prefill_kernel(const PrefillArgs a) {
   grid_dependency_wait();
   const CacheView& cv = a.cv;
   const int nmax = a.n;
   const int lane = threadIdx.x & 31;
-  const int64_t items = (int64_t)cv.B * nmax * cv.Hkv;
+  const int64_t items = (int64_t)a.nb * nmax * cv.Hkv;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   uint16_t* ka_pool = cv.pool[kPoolK128];
   uint16_t* va_pool = cv.pool[kPoolV];
   for (int64_t it = (((int64_t)blockIdx.x * blockDim.x) + threadIdx.x) >> 5; it < items; it += nwarps) {
     const int h = (int)(it % cv.Hkv);
-    const int64_t bt = it / cv.Hkv;              // b * n_max + t
+    const int64_t bt = it / cv.Hkv;              // i * n_max + t
     const int t = (int)(bt % nmax);
-    const int b = (int)(bt / nmax);
+    const int b = a.b0 + (int)(bt / nmax);
     const int n = __ldcg(&cv.len[a.layer * cv.B + b]);
     if (t >= n) continue;
     const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
     const uint16_t* k_src = a.k + (size_t)it * kHeadDim;
     const uint16_t* v_src = a.v + (size_t)it * kHeadDim;
     const int64_t abase = hd.row_a + (int64_t)b * hd.cap_a;
-    int64_t arow = -1, mid = -1;
+    int arow = -1, mid = -1;
     if (hd.policy == kFull) {
       if (t < cv.S) arow = t;
       else if (t >= n - cv.W) arow = cv.S + (t - cv.S) % cv.W;
@@ -152,10 +216,56 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillArgs a) {
       row8(ka_pool, abase + arow)[lane] = reinterpret_cast<const uint2*>(k_src)[lane];
       row8(va_pool, abase + arow)[lane] = reinterpret_cast<const uint2*>(v_src)[lane];
     } else if (mid >= 0) {
-      write_middle(cv, hd, cv.kept + ((size_t)a.layer * cv.Hkv + h) * kHeadDim,
-                   hd.krow_b + (int64_t)b * hd.cap_b + mid, hd.vrow_b + (int64_t)b * hd.cap_b + mid,
-                   k_src, reinterpret_cast<const uint2*>(v_src)[lane], lane);
+      const int32_t page = cv.max_pages > 0 ? __ldcg(&page_row(cv, a.layer, b, h)[mid / kPageRows]) : -1;
+      int64_t krow, vrow;
+      if (middle_rows(cv, hd, b, mid, page, krow, vrow))
+        write_middle(cv, hd, cv.kept + ((size_t)a.layer * cv.Hkv + h) * kHeadDim, krow, vrow, k_src,
+                     reinterpret_cast<const uint2*>(v_src)[lane], lane);
     }
+  }
+}
+
+// Paged caches: before the copy, each (sequence, FULL head with k > 0) of the
+// range pops the pages its middle rows need (the slots are empty).
+__global__ void __launch_bounds__(256) prefill_pages_kernel(const PrefillArgs a) {
+  grid_dependency_wait();
+  const CacheView& cv = a.cv;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.nb * cv.Hkv) return;
+  const int b = a.b0 + i / cv.Hkv, h = i % cv.Hkv;
+  const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
+  if (hd.policy != kFull || hd.n_kept == 0) return;
+  const int n = __ldcg(&cv.len[a.layer * cv.B + b]);
+  const int k = (max(0, n - cv.S - cv.W) + kPageRows - 1) / kPageRows;
+  pop_pages(cv, hd, min(k, cv.max_pages), page_row(cv, a.layer, b, h));
+}
+
+// Empties slot b in every layer (block = layer): pushes its pages back on
+// their class stacks, clears the page table, lengths and special counts, and
+// marks the slot released.
+__global__ void __launch_bounds__(128) release_kernel(const CacheView cv, int b) {
+  const int layer = blockIdx.x;
+  const int lb = layer * cv.B + b;
+  const int n = __ldcg(&cv.len[lb]);
+  if (cv.max_pages > 0) {
+    for (int h = threadIdx.x; h < cv.Hkv; h += blockDim.x) {
+      const HeadDesc& hd = cv.heads[layer * cv.Hkv + h];
+      if (hd.policy != kFull || hd.n_kept == 0) continue;
+      const int k = min(cv.max_pages, (max(0, n - cv.S - cv.W) + kPageRows - 1) / kPageRows);
+      int32_t* pt = page_row(cv, layer, b, h);
+      if (k > 0) {
+        const int t = atomicAdd(&cv.hdr->free_top[hd.pool_kb], k);
+        // reversed, so the next pops hand the pages out in table order
+        for (int i = 0; i < k; ++i) cv.free_list[hd.free_off + t + i] = pt[k - 1 - i];
+      }
+      for (int i = 0; i < k; ++i) pt[i] = -1;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    cv.len[lb] = 0;
+    cv.cnt[lb] = 0;
+    if (layer == 0) cv.active[b] = 0;
   }
 }
 
@@ -165,7 +275,8 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillArgs a) {
 __global__ void __launch_bounds__(1024) prefill_special_kernel(const PrefillArgs a) {
   grid_dependency_wait();
   const CacheView& cv = a.cv;
-  const int b = blockIdx.x;
+  const int i = blockIdx.x;               // input sequence
+  const int b = a.b0 + i;
   const int nmax = a.n;
   const int n = __ldcg(&cv.len[a.layer * cv.B + b]);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -177,7 +288,7 @@ __global__ void __launch_bounds__(1024) prefill_special_kernel(const PrefillArgs
     const int t = c0 + tid;
     bool flag = false;
     if (t < n && a.ids != nullptr) {
-      const int id = a.ids[(size_t)b * nmax + t];
+      const int id = a.ids[(size_t)i * nmax + t];
       if (id >= 0 && id < cv.vocab) flag = cv.is_special[id] != 0;
       else set_status(cv, kStatusBadId);
     }
@@ -209,7 +320,7 @@ __global__ void __launch_bounds__(1024) prefill_special_kernel(const PrefillArgs
         if (lane == 0) set_status(cv, kStatusCapacity);
         continue;
       }
-      const size_t src = (((size_t)b * nmax + s_tok[j]) * cv.Hkv + h) * kHeadDim;
+      const size_t src = (((size_t)i * nmax + s_tok[j]) * cv.Hkv + h) * kHeadDim;
       const int64_t row = hd.row_a + (int64_t)b * hd.cap_a + r;
       row8(cv.pool[kPoolK128], row)[lane] = reinterpret_cast<const uint2*>(a.k + src)[lane];
       row8(cv.pool[kPoolV], row)[lane] = reinterpret_cast<const uint2*>(a.v + src)[lane];
@@ -236,14 +347,25 @@ cudaError_t launch_append(const AppendArgs& args, cudaStream_t stream) {
 }
 
 cudaError_t launch_prefill(const PrefillArgs& args, bool has_special, int num_sms, cudaStream_t stream) {
-  const int64_t items = (int64_t)args.cv.B * args.n * args.cv.Hkv;
+  if (args.cv.max_pages > 0) {
+    const int threads = args.nb * args.cv.Hkv;
+    prefill_pages_kernel<<<(threads + 255) / 256, 256, 0, stream>>>(args);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  const int64_t items = (int64_t)args.nb * args.n * args.cv.Hkv;
   int64_t blocks = (items + 7) / 8;
   if (blocks > (int64_t)num_sms * 16) blocks = (int64_t)num_sms * 16;
   if (blocks < 1) blocks = 1;
   prefill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(args);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || !has_special) return err;
-  prefill_special_kernel<<<args.cv.B, 1024, 0, stream>>>(args);
+  prefill_special_kernel<<<args.nb, 1024, 0, stream>>>(args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_release(const CacheView& cv, int b, cudaStream_t stream) {
+  release_kernel<<<cv.L, 128, 0, stream>>>(cv, b);
   return cudaGetLastError();
 }
 

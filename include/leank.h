@@ -77,16 +77,24 @@ typedef struct lk_cache_s* lk_cache;  /* host object; its device buffer is the c
 /* Where one (layer, sequence, kv head) lives inside the cache buffer (byte
  * offsets from the buffer start).  Region A is full width (sinks + window
  * ring, LOCAL ring, or SPECIAL rows); region B holds middle tokens on the
- * kept channels (FULL heads with n_kept > 0). */
+ * kept channels (FULL heads with n_kept > 0).
+ *   Contiguous cache (page_rows = 0): middle row m is row m of region B.
+ *   Paged cache (page_rows = 128): region B is the page area of the head's
+ *   width class, shared by every head of that class; middle row m is row
+ *   page_table[m / 128] * 128 + m % 128 of it, page_table being the head's
+ *   int32 [max_pages] row at page_table_offset (-1: no page). */
 typedef struct lk_region_info {
   int32_t policy;
   int32_t n_kept;             /* kept K channels (FULL), else 0 */
   int32_t rows_a;             /* row capacity of region A */
-  int32_t rows_b;             /* row capacity of region B */
+  int32_t rows_b;             /* rows of region B (paged: of the class's page area) */
   uint64_t k_a_offset;        /* bf16 [rows_a][128] */
   uint64_t v_a_offset;        /* bf16 [rows_a][128] */
   uint64_t k_b_offset;        /* bf16 [rows_b][n_kept], kept channels ascending */
   uint64_t v_b_offset;        /* bf16 [rows_b][128] */
+  int32_t page_rows;          /* 0: contiguous region B; else rows per page */
+  int32_t max_pages;          /* entries of the head's page-table row */
+  uint64_t page_table_offset; /* int32 [max_pages] */
 } lk_region_info;
 
 /* Build a plan (host only; touches no GPU).
@@ -130,6 +138,19 @@ lk_status lk_plan_head(lk_plan plan, int32_t layer, int32_t kv_head, int32_t* po
  * tokens each (LeanK 3.1 split cache, FastGen 5.1 per-head allocation). */
 lk_status lk_cache_bytes(lk_plan plan, int32_t batch, int32_t capacity_tokens, size_t* bytes);
 
+/* Paged variant (continuous batching; paged KV blocks as in the pruning
+ * white paper, yyx235 blog, section 3.2 "granularity", with FastGen 5.1's
+ * per-head variable allocation): region B of every FULL head with k > 0 is
+ * held in 128-row pages of its width class instead of a contiguous
+ * capacity-sized run.  Each class gets enough pages for `middle_tokens`
+ * middle tokens (positions past the sinks and the window) summed over the
+ * batch, plus one partly filled page per sequence; a sequence still holds at
+ * most `capacity_tokens` tokens.  Pages are taken by appends and prefills on
+ * the device and given back by lk_release_sequence.  Errors as
+ * lk_cache_bytes; LK_ERR_ARG for middle_tokens < 0. */
+lk_status lk_cache_bytes_paged(lk_plan plan, int32_t batch, int32_t capacity_tokens, int64_t middle_tokens,
+                               size_t* bytes);
+
 /* Bytes of the decode workspace (split partials and counters for every
  * layer's entries, staging of lk_step_host) for `batch` sequences. */
 lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes);
@@ -140,6 +161,9 @@ lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes);
  * outlive nothing: the cache copies what it needs.  Needs a CUDA device. */
 lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch,
                         int32_t capacity_tokens, void* stream, lk_cache* out);
+/* As lk_cache_init, for a paged cache of lk_cache_bytes_paged bytes. */
+lk_status lk_cache_init_paged(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch,
+                              int32_t capacity_tokens, int64_t middle_tokens, void* stream, lk_cache* out);
 void lk_cache_destroy(lk_cache cache);
 
 /* Zero a caller-owned workspace of at least lk_workspace_bytes bytes
@@ -163,6 +187,28 @@ lk_status lk_prefill(lk_cache cache, int32_t layer, const void* k, const void* v
 lk_status lk_prefill_ragged(lk_cache cache, int32_t layer, const void* k, const void* v,
                             const int32_t* ids, const int32_t* lens, int32_t n_max, void* stream);
 
+/* Prefill one slot b of one layer while the other slots keep their tokens
+ * (continuous batching: a new request takes a released slot).
+ *   k, v  device bf16 [n][Hkv][128];  ids device int32 [n] or NULL.
+ * Sequence b of `layer` must be empty (fresh or released); n = 0 is allowed.
+ * The slot becomes active: lk_append writes to it again.  Paged caches take
+ * the pages of its middle rows here.  Errors: LK_ERR_STATE (slot not empty),
+ * LK_ERR_CAPACITY (n > capacity, or not enough free pages: nothing is
+ * launched then). */
+lk_status lk_prefill_sequence(lk_cache cache, int32_t layer, int32_t b, const void* k, const void* v,
+                              const int32_t* ids, int32_t n, void* stream);
+
+/* Release slot b in every layer: its pages (paged caches) go back to the
+ * free stacks, its lengths and special counts become 0, and the slot turns
+ * inactive: lk_append skips it (decode gives o = 0 for it) until
+ * lk_prefill_sequence fills it again.  Enqueued on `stream`. */
+lk_status lk_release_sequence(lk_cache cache, int32_t b, void* stream);
+
+/* Pages of one width class (32, 64, 96 or 128 kept channels) of a paged
+ * cache: total and currently free (host mirror, exact at every call
+ * boundary).  A contiguous cache reports 0 and 0. */
+lk_status lk_cache_pages(lk_cache cache, int32_t width, int64_t* total, int64_t* free_pages);
+
 /* Append one token per sequence to a layer (FastGen 2.1, 3.2 stage 2).
  *   k, v  device bf16 [B][Hkv][128];  ids device int32 [B] or NULL.
  * FULL heads: token n < S goes to sink row n; later tokens go to window ring
@@ -170,7 +216,11 @@ lk_status lk_prefill_ragged(lk_cache cache, int32_t layer, const void* k, const 
  * first moves to the middle (K gathered to the kept channels into K_prun row
  * n-W-S, V copied; dropped when n_kept = 0).  LOCAL: ring row n mod W_loc.
  * SPECIAL: appended (row = count) only if is_special[id].  Bit-exact copies.
- * Errors: LK_ERR_CAPACITY when the layer already holds capacity_tokens. */
+ * Released slots (lk_release_sequence) are skipped.  Paged caches take a
+ * page from the class's free stack when a middle row starts a new page.
+ * Errors: LK_ERR_CAPACITY when an active sequence of the layer already holds
+ * capacity_tokens, or a paged cache has too few free pages (nothing is
+ * launched then). */
 lk_status lk_append(lk_cache cache, int32_t layer, const void* k, const void* v,
                     const int32_t* ids, void* stream);
 

@@ -27,7 +27,7 @@ class Case:
     """
 
     def __init__(self, w: S.Workload, total: int, masks=None, policies=None, capacity=None,
-                 special_capacity=0, device="cuda", layers=None, gen_device=None):
+                 special_capacity=0, device="cuda", layers=None, gen_device=None, middle_tokens=None):
         self.w = w
         self.total = total
         self.policies = S.make_policies(w) if policies is None else np.asarray(policies, np.int32)
@@ -36,7 +36,7 @@ class Case:
         self.plan = lkb.Plan.for_workload(w, self.masks, self.policies, self.is_special,
                                           special_capacity=special_capacity)
         self.capacity = capacity or total
-        self.cache = lkb.Cache(self.plan, w.batch, self.capacity, device=device)
+        self.cache = lkb.Cache(self.plan, w.batch, self.capacity, device=device, middle_tokens=middle_tokens)
         self.device = device
         self.layers = list(range(w.num_layers)) if layers is None else layers
         self.ids = torch.from_numpy(S.make_token_ids(w, total)).to(device)
@@ -115,10 +115,10 @@ class Case:
                 assert torch.equal(va[ri], v[b, ti, h]), (layer, b, h, "V region A")
             rows, toks = OL.region_b(pol, len(kept), Nb, w.sink, w.local)
             if len(rows):
-                kb = self.cache.rows(r.k_b_offset, r.rows_b, r.n_kept)
-                vb = self.cache.rows(r.v_b_offset, r.rows_b, 128)
                 ri = torch.from_numpy(rows).to(self.device)
                 ti = torch.from_numpy(toks).to(self.device)
                 ki = torch.from_numpy(kept).to(self.device)
-                assert torch.equal(kb[ri], k[b, ti, h][:, ki]), (layer, b, h, "K_prun")
-                assert torch.equal(vb[ri], v[b, ti, h]), (layer, b, h, "V middle")
+                kb = self.cache.middle_rows(r, r.k_b_offset, r.n_kept, ri)
+                vb = self.cache.middle_rows(r, r.v_b_offset, 128, ri)
+                assert torch.equal(kb, k[b, ti, h][:, ki]), (layer, b, h, "K_prun")
+                assert torch.equal(vb, v[b, ti, h]), (layer, b, h, "V middle")

@@ -137,3 +137,23 @@ def test_cache_init_without_gpu_fails_cleanly(lib):
     assert h.value is None
     st = lib.lk_cache_init(plan._h, addr + 8, 1 << 20, 1, 64, None, ctypes.byref(h))
     assert st == lkb.LK_ERR_ALIGN
+
+
+def test_paged_cache_bytes(lib):
+    w = S.WORKLOADS[1]
+    plan = lkb.Plan.for_workload(w, S.masks_with_counts(w, [32] * 8), S.make_policies(w))
+    B, cap = 4, 32768
+    mid = cap - w.sink - w.local
+    contiguous = plan.cache_bytes(B, cap)
+    # room for every sequence's whole middle: the contiguous size plus the
+    # rounding of each sequence's last page and the page tables
+    full = plan.cache_bytes(B, cap, middle_tokens=B * mid)
+    assert contiguous <= full <= contiguous + (1 << 20)
+    # a quarter of that: about a quarter of the middle bytes
+    small = plan.cache_bytes(B, cap, middle_tokens=mid)
+    middle_bytes = 8 * B * mid * (32 + 128) * 2
+    assert abs((contiguous - small) - 0.75 * middle_bytes) < 0.01 * middle_bytes
+    assert plan.cache_bytes(B, cap, middle_tokens=0) < contiguous - middle_bytes + (8 << 20)
+    with pytest.raises(lkb.LeankError) as e:
+        plan.cache_bytes(B, cap, middle_tokens=-1)
+    assert e.value.status == lkb.LK_ERR_ARG
