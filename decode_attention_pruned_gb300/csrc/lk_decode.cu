@@ -234,31 +234,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   // so they are read only after the dependency wait)
   for (int h = tid; h < a.nlayers * cv.Hkv; h += kThreads)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(&cv.heads[a.layer * cv.Hkv + h]));
+  {
+    // warm L2 and the TLB for this thread's first length word (the line may
+    // be rewritten by the preceding append: only L2 is touched, which stays
+    // coherent)
+    const int per0 = (E + kThreads - 1) / kThreads;
+    const int e0 = min(E, tid * per0);
+    if (e0 < E) {
+      const EntryId id0 = entry_id(a, e0);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(&cv.len[id0.l * cv.B + id0.b]));
+    }
+  }
   const uint64_t policy = l2_policy_evict_first();
   grid_dependency_wait();
   grid_launch_dependents();
 
-  // ---- the line: per-thread chunks of entries, block exclusive scan.  The
-  // lengths of a chunk's first kKeep entries stay in registers for the
-  // second pass; the rest load kKeep at a time.
-  constexpr int kKeep = 4;
+  // ---- the line: per-thread chunks of entries, block exclusive scan
   const int per = (E + kThreads - 1) / kThreads;
   const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
-  EntryLen keep[kKeep];
-#pragma unroll
-  for (int i = 0; i < kKeep; ++i) keep[i] = e_lo + i < e_hi ? entry_len(a, e_lo + i) : EntryLen{0, 0};
   uint64_t local = 0;
-#pragma unroll
-  for (int i = 0; i < kKeep; ++i)
-    if (e_lo + i < e_hi) local += entry_cost(entry_from(a, e_lo + i, keep[i]));
-  for (int e = e_lo + kKeep; e < e_hi; e += kKeep) {
-    EntryLen t[kKeep];
-#pragma unroll
-    for (int i = 0; i < kKeep; ++i) t[i] = e + i < e_hi ? entry_len(a, e + i) : EntryLen{0, 0};
-#pragma unroll
-    for (int i = 0; i < kKeep; ++i)
-      if (e + i < e_hi) local += entry_cost(entry_from(a, e + i, t[i]));
-  }
+  for (int e = e_lo; e < e_hi; ++e) local += entry_cost(entry_geometry(a, e));
   uint64_t incl = local;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -284,20 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t acc = excl;
     int found = -1;
     Entry fg{0, 0, 0};
-#pragma unroll
-    for (int i = 0; i < kKeep; ++i) {
-      if (found < 0 && e_lo + i < e_hi) {
-        const Entry g = entry_from(a, e_lo + i, keep[i]);
-        const uint64_t c = entry_cost(g);
-        if (acc + c > start) {
-          found = e_lo + i;
-          fg = g;
-        } else {
-          acc += c;
-        }
-      }
-    }
-    for (int e = e_lo + kKeep; found < 0 && e < e_hi; ++e) {
+    for (int e = e_lo; found < 0 && e < e_hi; ++e) {
       const Entry g = entry_geometry(a, e);
       const uint64_t c = entry_cost(g);
       if (acc + c > start) {
