@@ -175,15 +175,16 @@ def run_gpu(args, rank, local_rank, world):
     max_growth = max(1, int(MAX_CONTEXT_GROWTH * N))
     cap_probe = N + 64
     paged = args.layout == "paged"
+    kvf = lkb.KV_INT8 if args.kv == "int8" else lkb.KV_BF16
     # paged: page pools sized for every sequence's middle at the capacity
     middle = (lambda cap: B * max(0, cap - w.sink - w.local)) if paged else (lambda cap: None)
-    copy_bytes = plan.cache_bytes(B, cap_probe, middle(cap_probe)) + plan.workspace_bytes(B)
+    copy_bytes = plan.cache_bytes(B, cap_probe, middle(cap_probe), kvf) + plan.workspace_bytes(B)
 
     # dense history of every layer, generated once on the device
     hist = {l: S.make_kv(w, l, N, device=dev) for l in range(L)} if L <= 2 else None
     ids_all = torch.from_numpy(S.make_token_ids(w, N)).to(dev) if len(spec) else None
 
-    first = lkb.Cache(plan, B, cap_probe, device=dev, middle_tokens=middle(cap_probe))
+    first = lkb.Cache(plan, B, cap_probe, device=dev, middle_tokens=middle(cap_probe), kv_format=kvf)
     for l in range(L):
         k, v = hist[l] if hist else S.make_kv(w, l, N, device=dev)
         first.prefill(l, k[:, : N - 1].contiguous(), v[:, : N - 1].contiguous(),
@@ -202,7 +203,7 @@ def run_gpu(args, rank, local_rank, world):
 
     caches = []
     for c in range(copies):
-        cache = lkb.Cache(plan, B, capacity, device=dev, middle_tokens=middle(capacity))
+        cache = lkb.Cache(plan, B, capacity, device=dev, middle_tokens=middle(capacity), kv_format=kvf)
         for l in range(L):
             k, v = hist[l] if hist else S.make_kv(w, l, N, device=dev)
             cache.prefill(l, k[:, : N - 1].contiguous(), v[:, : N - 1].contiguous(),
@@ -375,7 +376,7 @@ def run_gpu(args, rank, local_rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if kvf == lkb.KV_BF16 else "bf16 + int8 (middle blocks)",
         "data": "synthetic (seeded; random K/V/q, seeded LeanK masks)",
         "config": {
             "workload": w.name, "layers": L, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
@@ -386,6 +387,8 @@ def run_gpu(args, rank, local_rank, world):
             "cache_copies": copies, "l2_policy": "inputs larger than L2 (rotating cache copies)",
             "cuda_graph": True, "pdl": True, "parallelism": f"replicas x{world}",
             "cache_layout": "paged (128-row pages per width class)" if paged else "contiguous",
+            "middle_format": "int8 (complete 128-row blocks; per-channel K / per-token V scales)"
+            if kvf == lkb.KV_INT8 else "bf16",
         },
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -409,12 +412,15 @@ def run_gpu(args, rank, local_rank, world):
 # the oracle (CPU)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w_name, budget_s, max_units=None):
+def oracle_sample(w_name, budget_s, max_units=None, kv="bf16"):
     """Time the fp64 oracle on (sequence, kv head) units of the workload's
-    decode call until `budget_s` or `max_units`; returns (calls/s, units, s)."""
+    decode call until `budget_s` or `max_units`; returns (calls/s, units, s).
+    kv="int8": the oracle over the quantised middle (quantisation included)."""
     import torch
     from decode_attention_pruned_gb300 import synth as S
     from oracle import attention as OA
+    from oracle import quant as OQ
+    head_fn = OQ.decode_head_quantized if kv == "int8" else OA.decode_head
     w = S.WORKLOAD_BY_NAME[w_name]
     N = w.context
     pol = S.make_policies(w)
@@ -431,8 +437,8 @@ def oracle_sample(w_name, budget_s, max_units=None):
     while True:
         h = units % w.num_kv_heads
         kept = np.nonzero(masks[0, h])[0]
-        OA.decode_head(Q[h * G:(h + 1) * G], K[:, h], V[:, h], int(pol[0, h]), kept, N, w.sink, w.local,
-                       w.local_only_window, flags)
+        head_fn(Q[h * G:(h + 1) * G], K[:, h], V[:, h], int(pol[0, h]), kept, N, w.sink, w.local,
+                w.local_only_window, flags)
         units += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_units is not None and units >= max_units):
@@ -443,8 +449,8 @@ def oracle_sample(w_name, budget_s, max_units=None):
 
 def run_reference(args):
     W, K = args.warmup, args.steps
-    oracle_sample(args.workload, 0.0, max_units=max(1, min(W, 3)))
-    value, units, el = oracle_sample(args.workload, args.reference_budget, max_units=K)
+    oracle_sample(args.workload, 0.0, max_units=max(1, min(W, 3)), kv=args.kv)
+    value, units, el = oracle_sample(args.workload, args.reference_budget, max_units=K, kv=args.kv)
     sample = (f"fp64 numpy oracle, one (sequence, kv head) of layer 0 per step; {units} steps in {el:.1f} s "
               f"(capped at {args.reference_budget:.0f} s); calls/s = steps/s / (batch x kv heads x layers)")
     line = {
@@ -466,6 +472,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama31_8b_layer")
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"])
     ap.add_argument("--e2e-steps", type=int, default=4000)
     ap.add_argument("--kernel-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
@@ -487,7 +494,7 @@ def main(argv=None):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = run_gpu(args, rank, local_rank, world)
     if rank == 0:
-        value, units, el = oracle_sample(args.workload, args.cpu_budget)
+        value, units, el = oracle_sample(args.workload, args.cpu_budget, kv=args.kv)
         line["cpu_baseline"] = {
             "value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"fp64 numpy oracle on {units} (sequence, kv head) units of layer 0 in {el:.1f} s, "

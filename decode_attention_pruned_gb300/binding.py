@@ -37,7 +37,15 @@ class RegionInfo(ctypes.Structure):
                 ("rows_b", ctypes.c_int32), ("k_a_offset", ctypes.c_uint64), ("v_a_offset", ctypes.c_uint64),
                 ("k_b_offset", ctypes.c_uint64), ("v_b_offset", ctypes.c_uint64),
                 ("page_rows", ctypes.c_int32), ("max_pages", ctypes.c_int32),
-                ("page_table_offset", ctypes.c_uint64)]
+                ("page_table_offset", ctypes.c_uint64), ("kv_format", ctypes.c_int32),
+                ("sealed_blocks", ctypes.c_int32)]
+
+
+KV_BF16, KV_INT8 = 0, 1
+
+
+class CacheOptions(ctypes.Structure):
+    _fields_ = [("middle_tokens", ctypes.c_int64), ("kv_format", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 SIGNATURES = {
@@ -50,6 +58,10 @@ SIGNATURES = {
     "lk_workspace_bytes": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_sz)]),
     "lk_cache_init": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, _vp, ctypes.POINTER(_vp)]),
     "lk_cache_init_paged": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, ctypes.c_int64, _vp, ctypes.POINTER(_vp)]),
+    "lk_cache_bytes_ex": (ctypes.c_int, [_vp, _i32, _i32, ctypes.POINTER(CacheOptions), ctypes.POINTER(_sz)]),
+    "lk_cache_init_ex": (ctypes.c_int, [_vp, _vp, _sz, _i32, _i32, ctypes.POINTER(CacheOptions), _vp,
+                                        ctypes.POINTER(_vp)]),
+    "lk_cache_block": (ctypes.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "lk_cache_destroy": (None, [_vp]),
     "lk_workspace_init": (ctypes.c_int, [_vp, _vp, _sz, _vp]),
     "lk_prefill": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _i32, _vp]),
@@ -184,10 +196,13 @@ class Plan:
         _check(_lib.lk_plan_head(self._h, layer, kv_head, ctypes.byref(pol), ctypes.byref(nk), kept.ctypes.data))
         return pol.value, nk.value, kept[: nk.value].copy()
 
-    def cache_bytes(self, batch, capacity, middle_tokens=None):
+    def cache_bytes(self, batch, capacity, middle_tokens=None, kv_format=KV_BF16):
         """Cache buffer bytes; paged layout when middle_tokens is given."""
         n = ctypes.c_size_t()
-        if middle_tokens is None:
+        if kv_format != KV_BF16:
+            opt = CacheOptions(-1 if middle_tokens is None else int(middle_tokens), kv_format, 0)
+            _check(_lib.lk_cache_bytes_ex(self._h, batch, capacity, ctypes.byref(opt), ctypes.byref(n)))
+        elif middle_tokens is None:
             _check(_lib.lk_cache_bytes(self._h, batch, capacity, ctypes.byref(n)))
         else:
             _check(_lib.lk_cache_bytes_paged(self._h, batch, capacity, int(middle_tokens), ctypes.byref(n)))
@@ -209,20 +224,27 @@ class Cache:
 
     With ``middle_tokens`` the cache is paged (lk_cache_init_paged): the
     middle rows of all sequences share page pools sized for that many middle
-    tokens in total."""
+    tokens in total.  ``kv_format=KV_INT8`` quantises complete 128-row
+    blocks of the middle (lk_cache_init_ex)."""
 
-    def __init__(self, plan: Plan, batch: int, capacity: int, device=None, stream=None, middle_tokens=None):
+    def __init__(self, plan: Plan, batch: int, capacity: int, device=None, stream=None, middle_tokens=None,
+                 kv_format=KV_BF16):
         import torch
         self.plan, self.batch, self.capacity = plan, batch, capacity
         self.paged = middle_tokens is not None
+        self.kv_format = kv_format
         dev = torch.device(device if device is not None else "cuda")
         self.device = dev
-        nbytes = plan.cache_bytes(batch, capacity, middle_tokens)
+        nbytes = plan.cache_bytes(batch, capacity, middle_tokens, kv_format)
         self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.workspace = torch.empty(plan.workspace_bytes(batch), dtype=torch.uint8, device=dev)
         h = ctypes.c_void_p()
         s = _stream(stream)
-        if self.paged:
+        if kv_format != KV_BF16:
+            opt = CacheOptions(-1 if middle_tokens is None else int(middle_tokens), kv_format, 0)
+            _check(_lib.lk_cache_init_ex(plan._h, self.buffer.data_ptr(), nbytes, batch, capacity,
+                                         ctypes.byref(opt), s, ctypes.byref(h)))
+        elif self.paged:
             _check(_lib.lk_cache_init_paged(plan._h, self.buffer.data_ptr(), nbytes, batch, capacity,
                                             int(middle_tokens), s, ctypes.byref(h)))
         else:
@@ -294,6 +316,18 @@ class Cache:
         pt = self.page_table(r).to(torch.int64)
         rows = pt[m // r.page_rows] * r.page_rows + m % r.page_rows
         return self.rows(width_offset, r.rows_b, width)[rows]
+
+    def block(self, layer, b, kv_head, j, stream=None):
+        """lk_cache_block: (k_codes [128, k], k_scales [k], v_codes [128, 128],
+        v_scales [128]) of sealed block j, logical order."""
+        k = self.plan.head(layer, kv_head)[1]
+        kc = np.zeros((128, k), np.int8)
+        ks = np.zeros(k, np.float32)
+        vc = np.zeros((128, 128), np.int8)
+        vs = np.zeros(128, np.float32)
+        _check(_lib.lk_cache_block(self._h, layer, b, kv_head, j, kc.ctypes.data, ks.ctypes.data, vc.ctypes.data,
+                                   vs.ctypes.data, _stream(stream)))
+        return kc, ks, vc, vs
 
     def lengths(self, layer):
         out = np.zeros(self.batch, dtype=np.int32)

@@ -61,7 +61,9 @@ struct lk_plan_s {
 namespace {
 
 struct Layout {
-  size_t off_len, off_cnt, off_active, off_pt, off_free, off_heads, off_kept, off_spec;
+  size_t off_len, off_cnt, off_active, off_pt, off_free, off_heads, off_kept, off_spec, off_q;
+  size_t q_bytes = 0;                    // INT8: Q pool bytes
+  int32_t kv_format = kKvBf16;
   size_t off_pool[kNumPools];
   int64_t pool_rows[kNumPools];
   size_t total;
@@ -74,20 +76,29 @@ struct Layout {
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Region-B pages one (FULL, k > 0) head holds for a sequence of n tokens.
-inline int32_t pages_at(int n, int S, int W) { return (int32_t)ceil_div(std::max(0, n - S - W), kPageRows); }
+// Region-B pages one (FULL, k > 0) head holds for a sequence of n tokens:
+// every started page (bf16), or the sealed blocks only (INT8; the open block
+// is the head's bf16 tail).
+inline int32_t pages_at(int n, int S, int W, int fmt) {
+  const int m = std::max(0, n - S - W);
+  return fmt == kKvInt8 ? m / kQBlockRows : (int32_t)ceil_div(m, kPageRows);
+}
 
 // middle_tokens < 0: region B contiguous per (layer, sequence, head), sized
 // for `cap` tokens.  Otherwise paged: each FULL head with k > 0 gets pages for
 // middle_tokens middle tokens summed over the batch, plus one partly filled
 // page per sequence (and never more than batch x max_pages).
-lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_tokens, Layout* lay) {
+lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_tokens, int fmt, Layout* lay) {
   const lk_plan_desc& d = p.d;
   const int L = d.num_layers, H = d.num_kv_heads;
   const bool paged = middle_tokens >= 0;
-  lay->max_pages = paged ? std::max<int32_t>(1, pages_at(cap, d.sink, d.local)) : 0;
+  const bool q8 = fmt == kKvInt8;
+  lay->kv_format = fmt;
+  lay->max_pages = paged ? std::max<int32_t>(1, pages_at(cap, d.sink, d.local, fmt)) : 0;
   int64_t pages_per_head = 0;
-  if (paged) pages_per_head = std::min<int64_t>(ceil_div(middle_tokens, kPageRows) + B, (int64_t)B * lay->max_pages);
+  if (paged)
+    pages_per_head = std::min<int64_t>(q8 ? middle_tokens / kQBlockRows : ceil_div(middle_tokens, kPageRows) + B,
+                                       (int64_t)B * lay->max_pages);
   size_t off = align_up(sizeof(DevHeader), 1024);
   lay->off_len = off;
   off = align_up(off + (size_t)L * B * 4, 1024);
@@ -118,6 +129,8 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_toke
   rows[kPoolK128] = ra;
   rows[kPoolV] = ra;
   int64_t page_k[kNumPools] = {0, 0, 0, 0, 0}, page_v[kNumPools] = {0, 0, 0, 0, 0};
+  int64_t page_q[kNumPools] = {0, 0, 0, 0, 0};
+  int64_t qbytes = 0;
   if (paged) {
     int64_t free_total = 0;
     for (int pl = 0; pl < kNumPools; ++pl) {
@@ -127,10 +140,16 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_toke
       lay->num_pages[pl] = (int32_t)np;
       lay->free_off[pl] = (int32_t)free_total;
       free_total += np;
-      page_k[pl] = rows[pl];
-      rows[pl] += np * kPageRows;
-      page_v[pl] = rows[kPoolV];
-      rows[kPoolV] += np * kPageRows;
+      if (q8) {
+        // sealed blocks are the pages; bf16 rows hold only the tails
+        page_q[pl] = qbytes;
+        qbytes += np * qblock_bytes(pool_width(pl));
+      } else {
+        page_k[pl] = rows[pl];
+        rows[pl] += np * kPageRows;
+        page_v[pl] = rows[kPoolV];
+        rows[kPoolV] += np * kPageRows;
+      }
     }
     if (free_total > ((int64_t)1 << 31) - 1) return fail(LK_ERR_CAPACITY, "%lld pages in all", (long long)free_total);
   }
@@ -146,11 +165,28 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_toke
   off = align_up(off + (size_t)L * H * kHeadDim * 2, 1024);
   lay->off_spec = off;
   off = align_up(off + (size_t)std::max(d.vocab, 1), 1024);
+  const int64_t mid_cap = std::max(0, cap - d.sink - d.local);
   for (int i = 0; i < L * H; ++i) {
     HeadDesc& hd = lay->heads[i];
     if (hd.policy == kFull && hd.n_kept > 0) {
       hd.pool_kb = pool_for_width(hd.n_kept);
-      if (paged) {
+      if (q8) {
+        // bf16 tail of 128 rows per sequence; sealed blocks in the Q pool
+        hd.cap_b = (int32_t)std::min<int64_t>(mid_cap, kQBlockRows);
+        hd.krow_b = rows[hd.pool_kb];
+        rows[hd.pool_kb] += (int64_t)B * hd.cap_b;
+        hd.vrow_b = rows[kPoolV];
+        rows[kPoolV] += (int64_t)B * hd.cap_b;
+        if (paged) {
+          hd.qoff = page_q[hd.pool_kb];
+          hd.free_off = lay->free_off[hd.pool_kb];
+          hd.qblocks = lay->max_pages;
+        } else {
+          hd.qblocks = (int32_t)(mid_cap / kQBlockRows);
+          hd.qoff = qbytes;
+          qbytes += (int64_t)B * hd.qblocks * qblock_bytes(hd.n_kept);
+        }
+      } else if (paged) {
         hd.cap_b = lay->max_pages * kPageRows;
         hd.krow_b = page_k[hd.pool_kb];
         hd.vrow_b = page_v[hd.pool_kb];
@@ -173,6 +209,9 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_toke
     lay->off_pool[pl] = off;
     off = align_up(off + (size_t)r * pool_width(pl) * 2, 1024);
   }
+  lay->off_q = off;
+  lay->q_bytes = (size_t)qbytes;
+  off = align_up(off + (size_t)qbytes, 1024);
   lay->total = off;
   return LK_OK;
 }
@@ -283,7 +322,7 @@ struct lk_cache_s {
   // pages per class that taking sequence b of `layer` from n0 to n1 tokens needs
   void pages_needed(int layer, int n0, int n1, int64_t* need) const {
     if (!paged()) return;
-    const int d = pages_at(n1, cv.S, cv.W) - pages_at(n0, cv.S, cv.W);
+    const int d = pages_at(n1, cv.S, cv.W, lay.kv_format) - pages_at(n0, cv.S, cv.W, lay.kv_format);
     if (d == 0) return;
     for (int pl = 0; pl < kNumPools; ++pl) need[pl] += (int64_t)d * class_heads[(size_t)layer * kNumPools + pl];
   }
@@ -415,27 +454,35 @@ lk_status lk_plan_head(lk_plan plan, int32_t layer, int32_t kv_head, int32_t* po
 }
 
 static lk_status cache_bytes_impl(lk_plan plan, int32_t batch, int32_t capacity_tokens, int64_t middle_tokens,
-                                  size_t* bytes) {
+                                  int32_t fmt, size_t* bytes) {
   if (!plan || !bytes) return fail(LK_ERR_ARG, "lk_cache_bytes: null argument");
   if (batch < 1 || (int64_t)batch * plan->d.num_kv_heads > (1 << 20))
     return fail(LK_ERR_ARG, "batch %d out of range", batch);
   if (capacity_tokens < 1 || capacity_tokens > (1 << 30))
     return fail(LK_ERR_ARG, "capacity_tokens %d out of [1, 2^30]", capacity_tokens);
+  if (fmt != kKvBf16 && fmt != kKvInt8) return fail(LK_ERR_ARG, "kv_format %d is not LK_KV_BF16 or LK_KV_INT8", fmt);
   Layout lay;
-  lk_status st = compute_layout(*plan, batch, capacity_tokens, middle_tokens, &lay);
+  lk_status st = compute_layout(*plan, batch, capacity_tokens, middle_tokens, fmt, &lay);
   if (st != LK_OK) return st;
   *bytes = lay.total;
   return LK_OK;
 }
 
 lk_status lk_cache_bytes(lk_plan plan, int32_t batch, int32_t capacity_tokens, size_t* bytes) {
-  return cache_bytes_impl(plan, batch, capacity_tokens, -1, bytes);
+  return cache_bytes_impl(plan, batch, capacity_tokens, -1, kKvBf16, bytes);
 }
 
 lk_status lk_cache_bytes_paged(lk_plan plan, int32_t batch, int32_t capacity_tokens, int64_t middle_tokens,
                                size_t* bytes) {
   if (middle_tokens < 0) return fail(LK_ERR_ARG, "lk_cache_bytes_paged: middle_tokens %lld < 0", (long long)middle_tokens);
-  return cache_bytes_impl(plan, batch, capacity_tokens, middle_tokens, bytes);
+  return cache_bytes_impl(plan, batch, capacity_tokens, middle_tokens, kKvBf16, bytes);
+}
+
+lk_status lk_cache_bytes_ex(lk_plan plan, int32_t batch, int32_t capacity_tokens, const lk_cache_options* opt,
+                            size_t* bytes) {
+  if (!opt) return fail(LK_ERR_ARG, "lk_cache_bytes_ex: null options");
+  return cache_bytes_impl(plan, batch, capacity_tokens, opt->middle_tokens < 0 ? -1 : opt->middle_tokens,
+                          opt->kv_format, bytes);
 }
 
 lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes) {
@@ -447,12 +494,12 @@ lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes) {
 }
 
 static lk_status cache_init_impl(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
-                                 int64_t middle_tokens, void* stream, lk_cache* out) {
+                                 int64_t middle_tokens, int32_t fmt, void* stream, lk_cache* out) {
   if (!plan || !dev_buf || !out) return fail(LK_ERR_ARG, "lk_cache_init: null argument");
   *out = nullptr;
   if (!aligned(dev_buf, 256)) return fail(LK_ERR_ALIGN, "cache buffer must be 256-byte aligned");
   size_t need = 0;
-  lk_status st = cache_bytes_impl(plan, batch, capacity_tokens, middle_tokens, &need);
+  lk_status st = cache_bytes_impl(plan, batch, capacity_tokens, middle_tokens, fmt, &need);
   if (st != LK_OK) return st;
   if (bytes < need) return fail(LK_ERR_CAPACITY, "cache buffer has %zu bytes; %zu needed", bytes, need);
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -460,7 +507,7 @@ static lk_status cache_init_impl(lk_plan plan, void* dev_buf, size_t bytes, int3
 
   auto c = new lk_cache_s();
   c->plan = *plan;
-  compute_layout(c->plan, batch, capacity_tokens, middle_tokens, &c->lay);
+  compute_layout(c->plan, batch, capacity_tokens, middle_tokens, fmt, &c->lay);
   c->buf = static_cast<uint8_t*>(dev_buf);
   c->bytes = bytes;
   c->B = batch;
@@ -511,6 +558,8 @@ static lk_status cache_init_impl(lk_plan plan, void* dev_buf, size_t bytes, int3
   cv.capacity = capacity_tokens;
   cv.spec_cap = lay.spec_cap;
   cv.max_pages = lay.max_pages;
+  cv.kv_format = lay.kv_format;
+  cv.qpool = c->buf + lay.off_q;
 
   // host image of everything before the pools: header (free stack tops),
   // lengths 0, slots active, page table -1, free stacks (pops hand out page
@@ -567,14 +616,22 @@ static lk_status cache_init_impl(lk_plan plan, void* dev_buf, size_t bytes, int3
 
 lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
                         void* stream, lk_cache* out) {
-  return cache_init_impl(plan, dev_buf, bytes, batch, capacity_tokens, -1, stream, out);
+  return cache_init_impl(plan, dev_buf, bytes, batch, capacity_tokens, -1, kKvBf16, stream, out);
 }
 
 lk_status lk_cache_init_paged(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
                               int64_t middle_tokens, void* stream, lk_cache* out) {
   if (out) *out = nullptr;
   if (middle_tokens < 0) return fail(LK_ERR_ARG, "lk_cache_init_paged: middle_tokens %lld < 0", (long long)middle_tokens);
-  return cache_init_impl(plan, dev_buf, bytes, batch, capacity_tokens, middle_tokens, stream, out);
+  return cache_init_impl(plan, dev_buf, bytes, batch, capacity_tokens, middle_tokens, kKvBf16, stream, out);
+}
+
+lk_status lk_cache_init_ex(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch, int32_t capacity_tokens,
+                           const lk_cache_options* opt, void* stream, lk_cache* out) {
+  if (out) *out = nullptr;
+  if (!opt) return fail(LK_ERR_ARG, "lk_cache_init_ex: null options");
+  return cache_init_impl(plan, dev_buf, bytes, batch, capacity_tokens, opt->middle_tokens < 0 ? -1 : opt->middle_tokens,
+                         opt->kv_format, stream, out);
 }
 
 void lk_cache_destroy(lk_cache cache) { delete cache; }
@@ -863,7 +920,12 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
   out->page_rows = 0;
   out->max_pages = 0;
   out->page_table_offset = 0;
-  if (hd.cap_b > 0 && cache->paged()) {
+  out->kv_format = lay.kv_format;
+  out->sealed_blocks = 0;
+  const bool q8 = lay.kv_format == kKvInt8;
+  if (q8 && hd.cap_b > 0)
+    out->sealed_blocks = pages_at(cache->host_len[(size_t)layer * cache->B + b], cache->cv.S, cache->cv.W, kKvInt8);
+  if (hd.cap_b > 0 && cache->paged() && !q8) {
     out->rows_b = (int32_t)std::min<int64_t>((int64_t)lay.num_pages[hd.pool_kb] * kPageRows, INT32_MAX);
     out->k_b_offset = lay.off_pool[hd.pool_kb] + (uint64_t)hd.krow_b * hd.n_kept * 2;
     out->v_b_offset = lay.off_pool[kPoolV] + (uint64_t)hd.vrow_b * kHeadDim * 2;
@@ -877,6 +939,47 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
   } else {
     out->k_b_offset = out->v_b_offset = 0;
   }
+  return LK_OK;
+}
+
+lk_status lk_cache_block(lk_cache cache, int32_t layer, int32_t b, int32_t kv_head, int32_t block, int8_t* k_codes,
+                         float* k_scales, int8_t* v_codes, float* v_scales, void* stream) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_cache_block: null cache");
+  if (cache->lay.kv_format != kKvInt8) return fail(LK_ERR_STATE, "lk_cache_block: the cache is not INT8");
+  if (layer < 0 || layer >= cache->cv.L || b < 0 || b >= cache->B || kv_head < 0 || kv_head >= cache->cv.Hkv)
+    return fail(LK_ERR_ARG, "lk_cache_block: (layer %d, b %d, kv_head %d) out of range", layer, b, kv_head);
+  const HeadDesc& hd = cache->lay.heads[(size_t)layer * cache->cv.Hkv + kv_head];
+  const int sealed = hd.cap_b > 0 ? pages_at(cache->host_len[(size_t)layer * cache->B + b], cache->cv.S,
+                                             cache->cv.W, kKvInt8)
+                                  : 0;
+  if (block < 0 || block >= sealed)
+    return fail(LK_ERR_ARG, "lk_cache_block: block %d not in [0, %d) sealed blocks", block, sealed);
+  const int k = hd.n_kept;
+  const int qb = qblock_bytes(k);
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  int64_t at = 0;
+  if (cache->paged()) {
+    int32_t page = -1;
+    const int32_t* pt = cache->cv.page_table +
+                        (((int64_t)layer * cache->B + b) * cache->cv.Hkv + kv_head) * cache->lay.max_pages + block;
+    if (err == cudaSuccess) err = cudaMemcpy(&page, pt, 4, cudaMemcpyDeviceToHost);
+    if (err == cudaSuccess && page < 0) return fail(LK_ERR_STATE, "lk_cache_block: block %d has no page", block);
+    at = hd.qoff + (int64_t)page * qb;
+  } else {
+    at = hd.qoff + ((int64_t)b * hd.qblocks + block) * qb;
+  }
+  std::vector<uint8_t> img(qb);
+  if (err == cudaSuccess) err = cudaMemcpy(img.data(), cache->cv.qpool + at, qb, cudaMemcpyDeviceToHost);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_cache_block");
+  for (int r = 0; r < kQBlockRows; ++r) {
+    if (k_codes)
+      for (int c = 0; c < k; ++c) k_codes[r * k + c] = (int8_t)img[(size_t)r * k + qbyte(k, r, c)];
+    if (v_codes)
+      for (int c = 0; c < kHeadDim; ++c)
+        v_codes[r * kHeadDim + c] = (int8_t)img[qblock_voff(k) + (size_t)r * kHeadDim + qbyte(kHeadDim, r, c)];
+  }
+  if (k_scales) std::memcpy(k_scales, img.data() + qblock_ksoff(k), (size_t)k * 4);
+  if (v_scales) std::memcpy(v_scales, img.data() + qblock_vsoff(k), (size_t)kQBlockRows * 4);
   return LK_OK;
 }
 
@@ -906,7 +1009,13 @@ lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_
       } else {
         na = std::min(cnt[b], hd.cap_a);
       }
-      total += na * (2 * kHeadDim * 2) + nb * (uint64_t)(hd.n_kept + kHeadDim) * 2;
+      if (cache->lay.kv_format == kKvInt8 && nb > 0) {
+        const uint64_t sealed = nb / kQBlockRows, tail = nb % kQBlockRows;
+        total += na * (2 * kHeadDim * 2) + sealed * (uint64_t)qblock_bytes(hd.n_kept) +
+                 tail * (uint64_t)(hd.n_kept + kHeadDim) * 2;
+      } else {
+        total += na * (2 * kHeadDim * 2) + nb * (uint64_t)(hd.n_kept + kHeadDim) * 2;
+      }
     }
   }
   *bytes = total;

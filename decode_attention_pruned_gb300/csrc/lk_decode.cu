@@ -45,15 +45,16 @@ static_assert(kSubPerWarp == 2, "two 16-row blocks per consumer warp");
 // Stages live in a byte ring: a stage holds a K tile (128 rows x width) and a
 // V tile (128 rows x 128), so narrow-K tiles (40 KB at k = 32) keep five
 // stages in flight where full-width ones (64 KB) keep three.
-constexpr int kSlots = 6;                               // barrier pairs = stages in flight at most
+constexpr int kSlots = 10;                              // barrier pairs = stages in flight at most
 constexpr int kRingBytes = 208 * 1024;
-constexpr int kUnitsA = 16;                             // cost per full-width row (512 B / 32)
+constexpr int kUnitsA = 2 * kHeadDim * 2;               // line cost of a full-width row: its bytes
 constexpr int kFirst = 1, kLast = 2;
 
 struct StageDesc {
   int32_t e;           // entry = b * Hkv + h; < 0 ends the stream
-  int32_t region;      // 0: full width, 1: kept channels
-  int32_t nrows;       // valid rows of the tile
+  int32_t region;      // 0: full width, 1: kept channels (bf16), 2: sealed INT8 block
+  int32_t rlo;         // first valid row of the tile (sealed blocks; else 0)
+  int32_t nrows;       // valid rows of the tile: rlo .. rlo + nrows - 1
   int32_t width;       // K channels of the tile
   int32_t flags;       // kFirst / kLast of this CTA's segment of the entry
   int32_t first_cta;   // CTAs first..last hold partials of the entry
@@ -75,10 +76,19 @@ struct SmemLayout {
 constexpr int kSmemBytes = SmemLayout::kBytes + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
 
-__device__ __forceinline__ uint32_t stage_bytes(int width) { return (uint32_t)kTileRows * (2 * width + 256); }
+__device__ __forceinline__ uint32_t stage_bytes(int region, int width) {
+  return region == 2 ? (uint32_t)qblock_bytes(width) : (uint32_t)kTileRows * (2 * width + 256);
+}
+// ring footprint of a stage: 1024-byte granules (swizzled TMA boxes need
+// 1024-byte aligned destinations)
+__device__ __forceinline__ uint32_t ring_bytes(int region, int width) {
+  return (stage_bytes(region, width) + 1023u) & ~1023u;
+}
 
+// Rows of an entry in line order: n_a full width, n_q in sealed INT8 blocks,
+// n_b bf16 kept-channel rows (INT8 caches: the open tail block).
 struct Entry {
-  int n_a, n_b, kb;
+  int n_a, n_q, n_b, kb;
 };
 
 // Entry e of a launch = (layer offset lr, sequence b, kv head h), layers
@@ -120,11 +130,18 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
   const EntryId id = entry_id(a, e);
   const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
   const int N = len.n;
-  Entry r{0, 0, 0};
+  Entry r{0, 0, 0, 0};
   if (hd.policy == kFull) {
     r.n_a = min(N, cv.S + cv.W);
     if (hd.n_kept > 0) {
-      r.n_b = max(0, N - cv.S - cv.W);
+      const int m = max(0, N - cv.S - cv.W);
+      if (cv.kv_format == kKvInt8) {
+        const int nblk = min(m / kQBlockRows, cv.max_pages > 0 ? cv.max_pages : hd.qblocks);
+        r.n_q = nblk * kQBlockRows;
+        r.n_b = m - m / kQBlockRows * kQBlockRows;
+      } else {
+        r.n_b = m;
+      }
       r.kb = hd.n_kept;
     }
   } else if (hd.policy == kLocal) {
@@ -139,10 +156,12 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
 
 __device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) { return entry_from(a, e, entry_len(a, e)); }
 
-__device__ __forceinline__ uint64_t row_cost_b(int kb) { return (uint64_t)(kb / 16 + 8); }
+// line costs per row = bytes streamed per row
+__device__ __forceinline__ uint64_t row_cost_b(int kb) { return (uint64_t)(2 * kb + 256); }
+__device__ __forceinline__ uint64_t row_cost_q(int kb) { return (uint64_t)(qblock_bytes(kb) / kQBlockRows); }
 
 __device__ __forceinline__ uint64_t entry_cost(const Entry& g) {
-  return (uint64_t)kUnitsA * g.n_a + row_cost_b(g.kb) * g.n_b;
+  return (uint64_t)kUnitsA * g.n_a + row_cost_q(g.kb) * g.n_q + row_cost_b(g.kb) * g.n_b;
 }
 
 // a / b for 64-bit a with a 32-bit path when it fits
@@ -222,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[0] = E;       // first entry of this CTA
     misc[1] = 0;       // its line offset
     misc[2] = 0;       // last-CTA flag of a segment
-    misc[3] = misc[4] = misc[5] = 0;   // geometry of the first entry
+    misc[3] = misc[4] = misc[5] = misc[6] = 0;   // geometry of the first entry
   }
   if (warp == kConsumerWarps && lane == 0) {
     tma_prefetch_map(&tm_k128);
@@ -278,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // geometry go to the producer through shared memory
     uint64_t acc = excl;
     int found = -1;
-    Entry fg{0, 0, 0};
+    Entry fg{0, 0, 0, 0};
     for (int e = e_lo; found < 0 && e < e_hi; ++e) {
       const Entry g = entry_geometry(a, e);
       const uint64_t c = entry_cost(g);
@@ -294,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[3] = fg.n_a;
     misc[4] = fg.n_b;
     misc[5] = fg.kb;
+    misc[6] = fg.n_q;
   }
   __syncthreads();
 
@@ -318,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool clash = issued - freed == (uint32_t)kSlots;
           for (uint32_t m = freed; !clash && m != issued; ++m) {
             const StageDesc& o = desc[m % kSlots];
-            const uint32_t ob = stage_bytes(o.width);
+            const uint32_t ob = ring_bytes(o.region, o.width);
             clash = at < o.koff + ob && o.koff < at + bytes;
           }
           if (!clash) break;
@@ -332,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t off = (uint64_t)misc[1];
       // entry geometry: the first from the scan, later ones from lengths
       // loaded one entry ahead
-      Entry g{(int)misc[3], (int)misc[4], (int)misc[5]};
+      Entry g{(int)misc[3], (int)misc[6], (int)misc[4], (int)misc[5]};
       EntryLen ahead{0, 0};
       if (e + 1 < E) ahead = entry_len(a, e + 1);
       for (; ok && e < E && off < end; ++e) {
@@ -341,80 +361,104 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (e + 1 < E) ahead = entry_len(a, e + 1);
         }
         const uint64_t cost = entry_cost(g);
-        const uint64_t cb = row_cost_b(g.kb);
-        const uint64_t off_b = off + (uint64_t)kUnitsA * g.n_a;
-        int a0, a1, b0, b1;
+        const uint64_t cq = row_cost_q(g.kb), cb = row_cost_b(g.kb);
+        const uint64_t off_q = off + (uint64_t)kUnitsA * g.n_a;
+        const uint64_t off_b = off_q + cq * g.n_q;
+        int a0, a1, q0, q1, b0, b1;
         rows_in_range(off, kUnitsA, g.n_a, start, end, a0, a1);
+        rows_in_range(off_q, cq, g.n_q, start, end, q0, q1);
         rows_in_range(off_b, cb, g.n_b, start, end, b0, b1);
-        // paged region B: tiles end at page boundaries (the box may read
-        // past a page end; those rows are beyond nrows and ignored)
+        // paged bf16 region B: tiles end at page boundaries (the box may read
+        // past a page end; those rows are beyond nrows and ignored).  Sealed
+        // INT8 blocks: one tile per block, whole block loaded, rows masked.
         const bool paged = cv.max_pages > 0;
+        const bool bpaged = paged && cv.kv_format == kKvBf16;
         const int nta = (a1 - a0 + kTileRows - 1) / kTileRows;
-        const int ntb = b1 <= b0  ? 0
-                        : paged ? (b1 - 1) / kPageRows - b0 / kPageRows + 1
-                                : (b1 - b0 + kTileRows - 1) / kTileRows;
-        if (nta + ntb > 0) {
+        const int ntq = q1 <= q0 ? 0 : (q1 - 1) / kQBlockRows - q0 / kQBlockRows + 1;
+        const int ntb = b1 <= b0   ? 0
+                        : bpaged ? (b1 - 1) / kPageRows - b0 / kPageRows + 1
+                                 : (b1 - b0 + kTileRows - 1) / kTileRows;
+        const int nt = nta + ntq + ntb;
+        if (nt > 0) {
           const EntryId id = entry_id(a, e);
           const int b = id.b;
           const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
           const int32_t* pt =
               cv.page_table + (((int64_t)id.l * cv.B + b) * cv.Hkv + id.h) * cv.max_pages;
-          const uint64_t last_row_off = g.n_b > 0 ? off_b + cb * (g.n_b - 1) : off + (uint64_t)kUnitsA * (g.n_a - 1);
+          const uint64_t last_row_off = g.n_b > 0   ? off_b + cb * (g.n_b - 1)
+                                        : g.n_q > 0 ? off_q + cq * (g.n_q - 1)
+                                                    : off + (uint64_t)kUnitsA * (g.n_a - 1);
           // the entry's first / last owning CTA is read only from the segment's
           // last descriptor: work it out after the first load is in flight
           int fc = -1, lc = -1;
-          if (nta + ntb == 1) {
+          if (nt == 1) {
             fc = range_owner(off, C, P);
             lc = range_owner(last_row_off, C, P);
           }
           int32_t page_ahead = 0;
-          for (int j = 0; j < nta + ntb; ++j) {
-            const bool in_a = j < nta;
-            const int width = in_a ? kHeadDim : g.kb;
-            int r, rend;
+          for (int j = 0; j < nt; ++j) {
+            const int region = j < nta ? 0 : j < nta + ntq ? 2 : 1;
+            const int width = region == 0 ? kHeadDim : g.kb;
+            int r, rend, rlo = 0;
             int32_t page = 0;
-            if (in_a) {
+            if (region == 0) {
               r = a0 + j * kTileRows;
               rend = min(a1, r + kTileRows);
-            } else if (paged) {
-              const int pg = b0 / kPageRows + (j - nta);
+            } else if (region == 2) {
+              const int blk = q0 / kQBlockRows + (j - nta);
+              r = max(q0, blk * kQBlockRows);
+              rend = min(q1, (blk + 1) * kQBlockRows);
+              rlo = r - blk * kQBlockRows;
+              if (paged) {
+                page = j == nta ? __ldcg(pt + blk) : page_ahead;
+                if (j + 1 < nta + ntq) page_ahead = __ldcg(pt + blk + 1);
+                page = max(0, page);
+              } else {
+                page = b * hd.qblocks + blk;
+              }
+            } else if (bpaged) {
+              const int pg = b0 / kPageRows + (j - nta - ntq);
               r = max(b0, pg * kPageRows);
               rend = min(b1, (pg + 1) * kPageRows);
               // page ids load one tile ahead (and before the slot wait); a
               // missing page (status already recorded) reads page 0
-              page = j == nta ? __ldcg(pt + pg) : page_ahead;
-              if (j + 1 < nta + ntb) page_ahead = __ldcg(pt + pg + 1);
+              page = j == nta + ntq ? __ldcg(pt + pg) : page_ahead;
+              if (j + 1 < nt) page_ahead = __ldcg(pt + pg + 1);
               page = max(0, page);
             } else {
-              r = b0 + (j - nta) * kTileRows;
+              r = b0 + (j - nta - ntq) * kTileRows;
               rend = min(b1, r + kTileRows);
             }
+            const uint32_t bytes = stage_bytes(region, width);
             uint32_t at = 0;
-            if (!reserve(stage_bytes(width), at)) {
+            if (!reserve(ring_bytes(region, width), at)) {
               ok = false;
               break;
             }
             const uint32_t stage = issued % kSlots;
             StageDesc d;
             d.e = e;
-            d.region = in_a ? 0 : 1;
+            d.region = region;
+            d.rlo = rlo;
             d.nrows = rend - r;
-            d.width = in_a ? kHeadDim : g.kb;
-            d.flags = (j == 0 ? kFirst : 0) | (j + 1 == nta + ntb ? kLast : 0);
+            d.width = width;
+            d.flags = (j == 0 ? kFirst : 0) | (j + 1 == nt ? kLast : 0);
             d.first_cta = fc;
             d.last_cta = lc;
             d.koff = at;
             desc[stage] = d;
             const uint32_t fb = bar_full + 8 * stage;
-            mbar_arrive_expect_tx(fb, stage_bytes(width));
+            mbar_arrive_expect_tx(fb, bytes);
             const uint32_t kdst = base + SmemLayout::kRingOff + at;
             const uint32_t vdst = kdst + (uint32_t)kTileRows * 2 * width;
-            if (in_a) {
+            if (region == 0) {
               const int32_t row = (int32_t)(hd.row_a + (int64_t)b * hd.cap_a + r);
               tma_load_3d(kdst, &tm_k128, 0, row, 0, fb, policy);
               tma_load_3d(vdst, &tm_v, 0, row, 0, fb, policy);
+            } else if (region == 2) {
+              bulk_load(kdst, cv.qpool + hd.qoff + (int64_t)page * bytes, bytes, fb, policy);
             } else {
-              const int64_t rb = paged ? (int64_t)page * kPageRows + r % kPageRows : (int64_t)b * hd.cap_b + r;
+              const int64_t rb = bpaged ? (int64_t)page * kPageRows + r % kPageRows : (int64_t)b * hd.cap_b + r;
               const int32_t krow = (int32_t)(hd.krow_b + rb);
               const int32_t vrow = (int32_t)(hd.vrow_b + rb);
               switch (hd.pool_kb) {
@@ -509,24 +553,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
 
-    // this warp's two 16-row blocks of the tile: rows 16*(warp + 4j)
-    const int nv0 = d.nrows - 16 * warp;
-    if (nv0 > 0) {
-      const uint32_t kbase = base + SmemLayout::kRingOff + d.koff;
-      const uint32_t vbase = kbase + (uint32_t)kTileRows * 2 * d.width;
-      const bool in_a = d.region == 0;
-      const bool fam128 = (d.width & 63) == 0;          // widths 64 / 128 use 128-byte rows
-      const int nks = d.width >> 4;
-      float x[kSubPerWarp][4];
-      bool live[kSubPerWarp];
+    // this warp's two 16-row blocks of the tile: rows 16*(warp + 4j); valid
+    // rows rlo .. rhi - 1 (sealed blocks may be shared with another CTA)
+    const int rlo = d.rlo, rhi = d.rlo + d.nrows;
+    const uint32_t kbase = base + SmemLayout::kRingOff + d.koff;
+    float x[kSubPerWarp][4];
+    bool live[kSubPerWarp];
 #pragma unroll
-      for (int j = 0; j < kSubPerWarp; ++j) {
-        const int r0 = 16 * (warp + kConsumerWarps * j);
-        const int nv = d.nrows - r0;
-        live[j] = nv > 0;
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-        if (live[j]) {
-          const int row = r0 + rk;
+    for (int j = 0; j < kSubPerWarp; ++j) {
+      const int r0 = 16 * (warp + kConsumerWarps * j);
+      live[j] = r0 < rhi && r0 + 16 > rlo;
+    }
+    if (live[0] || live[1]) {
+      float s[kSubPerWarp][4];
+#pragma unroll
+      for (int j = 0; j < kSubPerWarp; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+      if (d.region == 2) {
+        // ---- sealed INT8 block: S^T = K_codes (f16, exact) . Q'^T with
+        // Q' = q[kept] * (K scale of the channel), split into f16 hi + lo
+        const int kb = d.width;
+        const float* ksc = reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + d.koff + qblock_ksoff(kb));
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          if (2 * kp < (kb >> 4)) {
+            uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int ks = 2 * kp + u;
+              const int c = 16 * ks + 2 * tig;
+              const float2 s01 = *reinterpret_cast<const float2*>(&ksc[c]);
+              const float2 s89 = *reinterpret_cast<const float2*>(&ksc[c + 8]);
+              const float q0 = bf16_lo(qb[ks][0]) * s01.x, q1 = bf16_hi(qb[ks][0]) * s01.y;
+              const float q8 = bf16_lo(qb[ks][1]) * s89.x, q9 = bf16_hi(qb[ks][1]) * s89.y;
+              bh[u][0] = pack_f16x2(q0, q1);
+              bh[u][1] = pack_f16x2(q8, q9);
+              bl[u][0] = pack_f16x2(q0 - f16_lo(bh[u][0]), q1 - f16_hi(bh[u][0]));
+              bl[u][1] = pack_f16x2(q8 - f16_lo(bh[u][1]), q9 - f16_hi(bh[u][1]));
+            }
+#pragma unroll
+            for (int j = 0; j < kSubPerWarp; ++j) {
+              if (!live[j]) continue;
+              const int row = 16 * (warp + kConsumerWarps * j) + rk;
+              const int grp = 2 * kp + ck;
+              uint32_t w0, w1, w2, w3;
+              ldsm_x4(kbase + (uint32_t)(row * kb + 16 * (grp ^ qswz(kb, row))), w0, w1, w2, w3);
+              uint32_t f0, f1, f2, f3;
+              i8x4_to_f16x2(w0, f0, f2);       // rows gid: k 2tig.. / 2tig+8..
+              i8x4_to_f16x2(w1, f1, f3);       // rows gid + 8
+              mma_f16_16816(s[j], f0, f1, f2, f3, bh[0][0], bh[0][1]);
+              mma_f16_16816(s[j], f0, f1, f2, f3, bl[0][0], bl[0][1]);
+              i8x4_to_f16x2(w2, f0, f2);
+              i8x4_to_f16x2(w3, f1, f3);
+              mma_f16_16816(s[j], f0, f1, f2, f3, bh[1][0], bh[1][1]);
+              mma_f16_16816(s[j], f0, f1, f2, f3, bl[1][0], bl[1][1]);
+            }
+          }
+        }
+      } else {
+        const bool in_a = d.region == 0;
+        const bool fam128 = (d.width & 63) == 0;          // widths 64 / 128 use 128-byte rows
+        const int nks = d.width >> 4;
+#pragma unroll
+        for (int j = 0; j < kSubPerWarp; ++j) {
+          if (!live[j]) continue;
+          const int row = 16 * (warp + kConsumerWarps * j) + rk;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             if (ks < nks) {
@@ -536,21 +626,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               ldsm_x4(addr, a0, a1, a2, a3);
               const uint32_t b0 = in_a ? qa[ks][0] : qb[ks][0];
               const uint32_t b1 = in_a ? qa[ks][1] : qb[ks][1];
-              mma_bf16_16816(s, a0, a1, a2, a3, b0, b1);
+              mma_bf16_16816(s[j], a0, a1, a2, a3, b0, b1);
             }
           }
         }
-        const bool v0 = gid < nv, v1 = gid + 8 < nv;
-        x[j][0] = v0 ? s[0] * a.scale_log2 : NEG_INF;
-        x[j][1] = v0 ? s[1] * a.scale_log2 : NEG_INF;
-        x[j][2] = v1 ? s[2] * a.scale_log2 : NEG_INF;
-        x[j][3] = v1 ? s[3] * a.scale_log2 : NEG_INF;
+      }
+#pragma unroll
+      for (int j = 0; j < kSubPerWarp; ++j) {
+        const int t0 = 16 * (warp + kConsumerWarps * j) + gid;
+        const bool v0 = live[j] && t0 >= rlo && t0 < rhi, v1 = live[j] && t0 + 8 >= rlo && t0 + 8 < rhi;
+        x[j][0] = v0 ? s[j][0] * a.scale_log2 : NEG_INF;
+        x[j][1] = v0 ? s[j][1] * a.scale_log2 : NEG_INF;
+        x[j][2] = v1 ? s[j][2] * a.scale_log2 : NEG_INF;
+        x[j][3] = v1 ? s[j][3] * a.scale_log2 : NEG_INF;
       }
       // Lazy rescaling: the running max m of a column moves only when some
       // score of the tile exceeds it by more than kRescaleGap (log2 units);
       // otherwise p = 2^(s - m) <= 2^kRescaleGap, exact in the fp32
-      // accumulators and in the bf16 hi/lo split.  One warp vote replaces the
-      // column-max shuffles in the common case.
+      // accumulators and in the hi/lo splits of P.  One warp vote replaces
+      // the column-max shuffles in the common case.
       float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
       float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
       constexpr float kRescaleGap = 8.f;
@@ -575,27 +669,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float mn0 = m0, mn1 = m1;
+      const uint32_t vbase = kbase + (d.region == 2 ? (uint32_t)qblock_voff(d.width) : (uint32_t)kTileRows * 2 * d.width);
 #pragma unroll
       for (int j = 0; j < kSubPerWarp; ++j) {
         if (!live[j]) continue;
-        // P as a bf16 pair hi + lo (two mmas): P.V keeps ~16 mantissa bits
         const float p0 = exp2f(x[j][0] - mn0), p1 = exp2f(x[j][1] - mn1);   // token gid
         const float p2 = exp2f(x[j][2] - mn0), p3 = exp2f(x[j][3] - mn1);   // token gid + 8
-        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-        const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-        const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
         l0 += p0 + p2;
         l1 += p1 + p3;
-        // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
-        const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
-        const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
-        const int row = 16 * (warp + kConsumerWarps * j) + rv;
+        const int r0 = 16 * (warp + kConsumerWarps * j);
+        if (d.region == 2) {
+          // ---- O^T += V_codes^T (f16, exact) . P'^T, P' = p * (V scale of
+          // the token), split into f16 hi + lo
+          const float* vsc =
+              reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + d.koff + qblock_vsoff(d.width));
+          const float sv0 = vsc[r0 + gid], sv1 = vsc[r0 + gid + 8];
+          const float q0 = p0 * sv0, q1 = p1 * sv0, q2 = p2 * sv1, q3 = p3 * sv1;
+          const uint32_t h01 = pack_f16x2(q0, q1), h23 = pack_f16x2(q2, q3);
+          const uint32_t r01 = pack_f16x2(q0 - f16_lo(h01), q1 - f16_hi(h01));
+          const uint32_t r23 = pack_f16x2(q2 - f16_lo(h23), q3 - f16_hi(h23));
+          const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+          const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
+          const int row = r0 + rk;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(tile_addr128(vbase, row, 2 * i + cvh), a0, a1, a2, a3);
-          mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
-          mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
+          for (int i2 = 0; i2 < 4; ++i2) {
+            const int grp = 2 * i2 + ck;
+            uint32_t w0, w1, w2, w3;
+            ldsm_x4_trans(vbase + (uint32_t)(row * kHeadDim + 16 * (grp ^ (row & 7))), w0, w1, w2, w3);
+            uint32_t f0, f1, f2, f3;
+            i8x4_to_f16x2(w0, f0, f1);         // tokens 2tig.. of rows 0-7: channels gid / gid + 8
+            i8x4_to_f16x2(w1, f2, f3);         // tokens 2tig + 8..
+            mma_f16_16816(o[2 * i2], f0, f1, f2, f3, ph0, ph1);
+            mma_f16_16816(o[2 * i2], f0, f1, f2, f3, pr0, pr1);
+            i8x4_to_f16x2(w2, f0, f1);
+            i8x4_to_f16x2(w3, f2, f3);
+            mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, ph0, ph1);
+            mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, pr0, pr1);
+          }
+        } else {
+          // P as a bf16 pair hi + lo (two mmas): P.V keeps ~16 mantissa bits
+          const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+          const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+          const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+          // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
+          const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+          const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
+          const int row = r0 + rv;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(tile_addr128(vbase, row, 2 * i + cvh), a0, a1, a2, a3);
+            mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
+            mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
+          }
         }
       }
     }

@@ -16,6 +16,16 @@
 // pool c, V rows vrow_b + 128p.. of pool V), located through the page table
 // [L][B][Hkv][max_pages].  Free pages of each class sit on a device stack, so
 // appends allocate pages inside the kernel (graph replays included).
+//
+// INT8 caches (KIVI-style quantisation after pruning): region B keeps only
+// its last, incomplete 128-row block in bf16 (the "tail", 128 rows per
+// (layer, sequence, head) in pools K_k and V); every complete block is sealed
+// into a byte block of the Q pool (contiguous per head and sequence, or a
+// page of its width class):
+//   [K codes 128 x k][V codes 128 x 128][K scales k x f32][V scales 128 x f32]
+// Codes are row-major; within each 16-channel group a row stores channels
+// (0, 8, 1, 9, ..., 7, 15) and its 16-byte groups are XOR-swizzled by row
+// (qswz), so ldmatrix reads mma fragments without bank conflicts.
 #pragma once
 #include <stdint.h>
 
@@ -26,6 +36,23 @@ constexpr int kMaxGroup = 8;        // query heads per kv head handled by one mm
 constexpr int kMaxCtas = 256;       // decode grid cap (partial workspace; combine staging np*G <= 2048)
 constexpr int kTmaBoxRows = 128;    // token rows per TMA box = decode tile rows
 constexpr int kPageRows = 128;      // middle rows per page (paged caches)
+constexpr int kQBlockRows = 128;    // rows per sealed INT8 block (= one page, one tile)
+
+enum KvFormat : int32_t { kKvBf16 = 0, kKvInt8 = 1 };
+
+// Bytes of a sealed INT8 block of width k and the offsets of its parts.
+__host__ __device__ constexpr int qblock_bytes(int k) { return 132 * (k + 128); }
+__host__ __device__ constexpr int qblock_voff(int k) { return 128 * k; }
+__host__ __device__ constexpr int qblock_ksoff(int k) { return 128 * k + 128 * 128; }
+__host__ __device__ constexpr int qblock_vsoff(int k) { return 128 * k + 128 * 128 + 4 * k; }
+// 16-byte group swizzle of row r in a block row of `width` bytes
+__host__ __device__ constexpr int qswz(int width, int r) {
+  return width == 128 ? (r & 7) : width == 64 ? ((r >> 1) & 3) : ((r >> 2) & 1);
+}
+// byte of channel c (< width) in row r of a sealed block part of that width
+__host__ __device__ constexpr int qbyte(int width, int r, int c) {
+  return 16 * ((c >> 4) ^ qswz(width, r)) + ((c & 15) < 8 ? 2 * (c & 7) : 2 * (c & 7) + 1);
+}
 
 enum Policy : int32_t { kFull = 0, kLocal = 1, kSpecial = 2 };
 enum Pool : int32_t { kPoolK128 = 0, kPoolV = 1, kPoolK32 = 2, kPoolK64 = 3, kPoolK96 = 4, kNumPools = 5 };
@@ -47,8 +74,12 @@ struct HeadDesc {                 // one (layer, kv head)
   int64_t row_a;                  // first region-A row (sequence 0) in K128 and V
   int64_t krow_b;                 // first region-B row (sequence 0) in pool_kb; paged: page area
   int64_t vrow_b;                 // first region-B row (sequence 0) in V; paged: page area
+  int64_t qoff;                   // INT8: byte offset in the Q pool of sequence 0's blocks
+                                  //       (paged: of the class's page area)
+  int32_t qblocks;                // INT8, contiguous: sealed blocks per sequence
+  int32_t pad;
 };
-static_assert(sizeof(HeadDesc) == 48, "HeadDesc layout");
+static_assert(sizeof(HeadDesc) == 64, "HeadDesc layout");
 
 struct DevHeader {
   uint32_t status;
@@ -69,10 +100,12 @@ struct CacheView {
   const int16_t* kept;            // [L][Hkv][128] kept channels ascending
   const uint8_t* is_special;      // [vocab]
   uint16_t* pool[kNumPools];      // bf16 rows
+  uint8_t* qpool;                 // INT8: sealed blocks
   int64_t pool_rows[kNumPools];
   int32_t L, B, Hq, Hkv, G, S, W, W_loc, vocab, capacity;
   int32_t spec_cap;               // rows of a SPECIAL head per sequence
   int32_t max_pages;              // pages per (layer, sequence, head); 0: not paged
+  int32_t kv_format;              // KvFormat of region B
 };
 
 inline int pool_width(int pool) {

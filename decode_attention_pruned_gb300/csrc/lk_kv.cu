@@ -74,6 +74,11 @@ __device__ void pop_pages(const CacheView& cv, const HeadDesc& hd, int k, int32_
 // no free page).
 __device__ __forceinline__ bool middle_rows(const CacheView& cv, const HeadDesc& hd, int b, int mid, int32_t page,
                                             int64_t& krow, int64_t& vrow) {
+  if (cv.kv_format == kKvInt8) {           // the open block: bf16 tail row mid mod 128
+    krow = hd.krow_b + (int64_t)b * hd.cap_b + mid % kQBlockRows;
+    vrow = hd.vrow_b + (int64_t)b * hd.cap_b + mid % kQBlockRows;
+    return true;
+  }
   if (cv.max_pages == 0) {
     krow = hd.krow_b + (int64_t)b * hd.cap_b + mid;
     vrow = hd.vrow_b + (int64_t)b * hd.cap_b + mid;
@@ -84,6 +89,66 @@ __device__ __forceinline__ bool middle_rows(const CacheView& cv, const HeadDesc&
   krow = hd.krow_b + r;
   vrow = hd.vrow_b + r;
   return true;
+}
+
+// Region-B pages a (FULL, k > 0) head holds at n tokens: started pages
+// (bf16) or sealed blocks (INT8).
+__device__ __forceinline__ int pages_at(const CacheView& cv, int n) {
+  const int m = max(0, n - cv.S - cv.W);
+  return cv.kv_format == kKvInt8 ? m / kQBlockRows : (m + kPageRows - 1) / kPageRows;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// Symmetric INT8 code of x for scale s (s = max|x| / 127 in fp32): x / s in
+// fp32 rounded half to even, clipped to [-127, 127]; s = 0 gives 0.
+__device__ __forceinline__ int8_t quant8(float x, float s) {
+  if (!(s > 0.f)) return 0;
+  const int q = __float2int_rn(__fdiv_rn(x, s));
+  return (int8_t)max(-127, min(127, q));
+}
+
+// Device address of sealed block j of (layer, b, h); null if its page is
+// missing.
+__device__ __forceinline__ uint8_t* qblock_addr(const CacheView& cv, const HeadDesc& hd, int layer, int b, int h,
+                                                int j) {
+  const int qb = qblock_bytes(hd.n_kept);
+  if (cv.max_pages == 0) return cv.qpool + hd.qoff + ((int64_t)b * hd.qblocks + j) * qb;
+  const int32_t page = __ldcg(&page_row(cv, layer, b, h)[j]);
+  return page < 0 ? nullptr : cv.qpool + hd.qoff + (int64_t)page * qb;
+}
+
+// One warp seals a 128-row block: kv(r, c) / vv(r, c) give the bf16 bits of
+// K row r at kept channel c (c < k) and of V row r at channel c.  K: one
+// scale per channel (lane per channel); V: one scale per row (lane per four
+// channels, warp max).  Codes go to their swizzled byte (qbyte).
+template <class KF, class VF>
+__device__ void seal_block(uint8_t* dst, int k, KF kv, VF vv, int lane) {
+  float* ks = reinterpret_cast<float*>(dst + qblock_ksoff(k));
+  float* vs = reinterpret_cast<float*>(dst + qblock_vsoff(k));
+  for (int c = lane; c < k; c += 32) {
+    float m = 0.f;
+    for (int r = 0; r < kQBlockRows; ++r) m = fmaxf(m, fabsf(bf16_to_f32(kv(r, c))));
+    const float sc = __fdiv_rn(m, 127.f);
+    ks[c] = sc;
+    for (int r = 0; r < kQBlockRows; ++r) dst[r * k + qbyte(k, r, c)] = (uint8_t)quant8(bf16_to_f32(kv(r, c)), sc);
+  }
+  uint8_t* vc = dst + qblock_voff(k);
+  for (int r = 0; r < kQBlockRows; ++r) {
+    float x[4];
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[i] = bf16_to_f32(vv(r, 4 * lane + i));
+      m = fmaxf(m, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
+    const float sc = __fdiv_rn(m, 127.f);
+    if (lane == 0) vs[r] = sc;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vc[r * kHeadDim + qbyte(kHeadDim, r, 4 * lane + i)] = (uint8_t)quant8(x[i], sc);
+  }
 }
 
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
@@ -137,7 +202,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
         if (n - cv.S >= cv.W && hd.n_kept > 0) {
           const int mid = n - cv.W - cv.S;               // K_prun row of token n - W
           int32_t page = -1;
-          if (cv.max_pages > 0) {
+          if (cv.max_pages > 0 && cv.kv_format == kKvBf16) {
             int32_t* pt = page_row(cv, layer, b, h) + mid / kPageRows;
             if (mid % kPageRows == 0) {         // first row of a new page
               if (lane == 0) {
@@ -157,6 +222,38 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
                          lane);
           }
           __syncwarp();
+          if (cv.kv_format == kKvInt8 && mid % kQBlockRows == kQBlockRows - 1) {
+            // the tail block is complete: seal it into block mid / 128
+            const int j = mid / kQBlockRows;
+            uint8_t* dst;
+            if (cv.max_pages > 0) {
+              int32_t pg = -1;
+              if (lane == 0) {
+                pop_pages(cv, hd, 1, &pg);
+                page_row(cv, layer, b, h)[j] = pg;
+              }
+              pg = __shfl_sync(0xffffffffu, pg, 0);
+              dst = pg < 0 ? nullptr : cv.qpool + hd.qoff + (int64_t)pg * qblock_bytes(hd.n_kept);
+            } else {
+              dst = qblock_addr(cv, hd, layer, b, h, j);
+            }
+            if (dst != nullptr) {
+              const int k = hd.n_kept;
+              const uint16_t* kt = cv.pool[hd.pool_kb] + (hd.krow_b + (int64_t)b * hd.cap_b) * k;
+              const uint16_t* vt = va_pool + (hd.vrow_b + (int64_t)b * hd.cap_b) * kHeadDim;
+              seal_block(
+                  dst, k, [&](int r, int c) { return kt[(size_t)r * k + c]; },
+                  [&](int r, int c) { return vt[(size_t)r * kHeadDim + c]; }, lane);
+              __syncwarp();
+              // the open block restarts empty (zeros), as a prefill leaves it
+              uint4* kz = reinterpret_cast<uint4*>(cv.pool[hd.pool_kb] + (hd.krow_b + (int64_t)b * hd.cap_b) * k);
+              uint4* vz = reinterpret_cast<uint4*>(va_pool + (hd.vrow_b + (int64_t)b * hd.cap_b) * kHeadDim);
+              const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+              for (int i = lane; i < kQBlockRows * k / 8; i += 32) kz[i] = zero;
+              for (int i = lane; i < kQBlockRows * kHeadDim / 8; i += 32) vz[i] = zero;
+            }
+            __syncwarp();
+          }
         }
       }
       row = abase + slot;
@@ -216,7 +313,12 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillArgs a) {
       row8(ka_pool, abase + arow)[lane] = reinterpret_cast<const uint2*>(k_src)[lane];
       row8(va_pool, abase + arow)[lane] = reinterpret_cast<const uint2*>(v_src)[lane];
     } else if (mid >= 0) {
-      const int32_t page = cv.max_pages > 0 ? __ldcg(&page_row(cv, a.layer, b, h)[mid / kPageRows]) : -1;
+      // INT8: rows of complete blocks are sealed from the inputs by
+      // prefill_seal_kernel; only the open block's rows go to the bf16 tail
+      if (cv.kv_format == kKvInt8 && mid < (n - cv.S - cv.W) / kQBlockRows * kQBlockRows) continue;
+      const int32_t page = cv.max_pages > 0 && cv.kv_format == kKvBf16
+                               ? __ldcg(&page_row(cv, a.layer, b, h)[mid / kPageRows])
+                               : -1;
       int64_t krow, vrow;
       if (middle_rows(cv, hd, b, mid, page, krow, vrow))
         write_middle(cv, hd, cv.kept + ((size_t)a.layer * cv.Hkv + h) * kHeadDim, krow, vrow, k_src,
@@ -236,8 +338,36 @@ __global__ void __launch_bounds__(256) prefill_pages_kernel(const PrefillArgs a)
   const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
   if (hd.policy != kFull || hd.n_kept == 0) return;
   const int n = __ldcg(&cv.len[a.layer * cv.B + b]);
-  const int k = (max(0, n - cv.S - cv.W) + kPageRows - 1) / kPageRows;
-  pop_pages(cv, hd, min(k, cv.max_pages), page_row(cv, a.layer, b, h));
+  pop_pages(cv, hd, min(pages_at(cv, n), cv.max_pages), page_row(cv, a.layer, b, h));
+}
+
+// INT8 caches: a warp per (sequence, head, complete block) quantises the
+// block straight from the prefill inputs (K gathered to the kept channels),
+// exactly as appends seal it from the bf16 tail.
+__global__ void __launch_bounds__(256) prefill_seal_kernel(const PrefillArgs a, int max_blocks) {
+  grid_dependency_wait();
+  const CacheView& cv = a.cv;
+  const int lane = threadIdx.x & 31;
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (w >= (int64_t)a.nb * cv.Hkv * max_blocks) return;
+  const int j = (int)(w % max_blocks);
+  const int h = (int)((w / max_blocks) % cv.Hkv);
+  const int i = (int)(w / ((int64_t)max_blocks * cv.Hkv));
+  const int b = a.b0 + i;
+  const HeadDesc& hd = cv.heads[a.layer * cv.Hkv + h];
+  if (hd.policy != kFull || hd.n_kept == 0) return;
+  const int n = __ldcg(&cv.len[a.layer * cv.B + b]);
+  if (j >= pages_at(cv, n)) return;
+  uint8_t* dst = qblock_addr(cv, hd, a.layer, b, h, j);
+  if (dst == nullptr) return;
+  const int16_t* kept = cv.kept + ((size_t)a.layer * cv.Hkv + h) * kHeadDim;
+  const int t0 = cv.S + j * kQBlockRows;
+  const uint16_t* kin = a.k + (((size_t)i * a.n + t0) * cv.Hkv + h) * kHeadDim;
+  const uint16_t* vin = a.v + (((size_t)i * a.n + t0) * cv.Hkv + h) * kHeadDim;
+  const size_t rs = (size_t)cv.Hkv * kHeadDim;
+  seal_block(
+      dst, hd.n_kept, [&](int r, int c) { return kin[r * rs + kept[c]]; },
+      [&](int r, int c) { return vin[r * rs + c]; }, lane);
 }
 
 // Empties slot b in every layer (block = layer): pushes its pages back on
@@ -251,7 +381,7 @@ __global__ void __launch_bounds__(128) release_kernel(const CacheView cv, int b)
     for (int h = threadIdx.x; h < cv.Hkv; h += blockDim.x) {
       const HeadDesc& hd = cv.heads[layer * cv.Hkv + h];
       if (hd.policy != kFull || hd.n_kept == 0) continue;
-      const int k = min(cv.max_pages, (max(0, n - cv.S - cv.W) + kPageRows - 1) / kPageRows);
+      const int k = min(cv.max_pages, pages_at(cv, n));
       int32_t* pt = page_row(cv, layer, b, h);
       if (k > 0) {
         const int t = atomicAdd(&cv.hdr->free_top[hd.pool_kb], k);
@@ -359,7 +489,17 @@ cudaError_t launch_prefill(const PrefillArgs& args, bool has_special, int num_sm
   if (blocks < 1) blocks = 1;
   prefill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(args);
   cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess || !has_special) return err;
+  if (err != cudaSuccess) return err;
+  if (args.cv.kv_format == kKvInt8) {
+    const int max_blocks = max(0, args.n - args.cv.S - args.cv.W) / kQBlockRows;
+    const int64_t warps = (int64_t)args.nb * args.cv.Hkv * max_blocks;
+    if (warps > 0) {
+      prefill_seal_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(args, max_blocks);
+      err = cudaGetLastError();
+      if (err != cudaSuccess) return err;
+    }
+  }
+  if (!has_special) return cudaSuccess;
   prefill_special_kernel<<<args.nb, 1024, 0, stream>>>(args);
   return cudaGetLastError();
 }

@@ -95,7 +95,34 @@ typedef struct lk_region_info {
   int32_t page_rows;          /* 0: contiguous region B; else rows per page */
   int32_t max_pages;          /* entries of the head's page-table row */
   uint64_t page_table_offset; /* int32 [max_pages] */
+  int32_t kv_format;          /* lk_kv_format of region B */
+  int32_t sealed_blocks;      /* INT8: complete 128-row blocks (read them with
+                                 lk_cache_block); region B's offsets then give
+                                 the bf16 tail: middle row m >= 128 * sealed_blocks
+                                 is tail row m - 128 * sealed_blocks */
 } lk_region_info;
+
+/* Storage format of region B (the middle tokens).
+ *   LK_KV_BF16  K_prun and V rows in bf16.
+ *   LK_KV_INT8  KIVI-style quantisation applied after pruning and
+ *               reorganisation (LeanK 4.2 and 5.2 problem 3; KIVI's
+ *               per-channel K / per-token V, pruning white paper 5.2.1):
+ *               every complete 128-row block of a head's middle is stored as
+ *               INT8 codes with one fp32 scale per kept K channel and one per
+ *               V token, scale = max|x| / 127 (fp32), code = x / scale
+ *               rounded half to even, clipped to +-127; the last,
+ *               incomplete block stays bf16. */
+typedef enum { LK_KV_BF16 = 0, LK_KV_INT8 = 1 } lk_kv_format;
+
+/* Cache options for lk_cache_bytes_ex / lk_cache_init_ex. */
+typedef struct lk_cache_options {
+  int64_t middle_tokens;      /* < 0: contiguous region B; >= 0: paged, pools
+                                 sized as in lk_cache_bytes_paged (INT8: sealed
+                                 blocks are the pages, floor(middle_tokens/128)
+                                 per head of a class) */
+  int32_t kv_format;          /* lk_kv_format */
+  int32_t reserved;           /* 0 */
+} lk_cache_options;
 
 /* Build a plan (host only; touches no GPU).
  *   masks      host uint8 [L][Hkv][128], 0/1: the static mask beta (LeanK 2.2).
@@ -161,6 +188,23 @@ lk_status lk_workspace_bytes(lk_plan plan, int32_t batch, size_t* bytes);
  * outlive nothing: the cache copies what it needs.  Needs a CUDA device. */
 lk_status lk_cache_init(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch,
                         int32_t capacity_tokens, void* stream, lk_cache* out);
+/* lk_cache_bytes / lk_cache_init with explicit options (paging and the
+ * storage format of region B).  Errors as lk_cache_bytes; LK_ERR_ARG for a
+ * null opt or an unknown kv_format. */
+lk_status lk_cache_bytes_ex(lk_plan plan, int32_t batch, int32_t capacity_tokens,
+                            const lk_cache_options* opt, size_t* bytes);
+lk_status lk_cache_init_ex(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch,
+                           int32_t capacity_tokens, const lk_cache_options* opt, void* stream,
+                           lk_cache* out);
+
+/* Host copy of sealed block `block` of an INT8 cache's (layer, b, kv_head),
+ * in logical order: k_codes [128][n_kept] (kept channels ascending), k_scales
+ * [n_kept], v_codes [128][128], v_scales [128]; any pointer may be NULL.
+ * Synchronises `stream`.  Errors: LK_ERR_STATE (not an INT8 cache),
+ * LK_ERR_ARG (no such sealed block). */
+lk_status lk_cache_block(lk_cache cache, int32_t layer, int32_t b, int32_t kv_head, int32_t block,
+                         int8_t* k_codes, float* k_scales, int8_t* v_codes, float* v_scales, void* stream);
+
 /* As lk_cache_init, for a paged cache of lk_cache_bytes_paged bytes. */
 lk_status lk_cache_init_paged(lk_plan plan, void* dev_buf, size_t bytes, int32_t batch,
                               int32_t capacity_tokens, int64_t middle_tokens, void* stream, lk_cache* out);

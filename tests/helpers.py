@@ -9,6 +9,7 @@ from decode_attention_pruned_gb300 import binding as lkb
 from decode_attention_pruned_gb300 import synth as S
 from oracle import attention as OA
 from oracle import layout as OL
+from oracle import quant as OQ
 
 # max |err| bound of the decode output against the fp64 oracle (bf16 inputs,
 # fp32 accumulation), as stated for this method's GPU path
@@ -27,7 +28,8 @@ class Case:
     """
 
     def __init__(self, w: S.Workload, total: int, masks=None, policies=None, capacity=None,
-                 special_capacity=0, device="cuda", layers=None, gen_device=None, middle_tokens=None):
+                 special_capacity=0, device="cuda", layers=None, gen_device=None, middle_tokens=None,
+                 kv_format=lkb.KV_BF16):
         self.w = w
         self.total = total
         self.policies = S.make_policies(w) if policies is None else np.asarray(policies, np.int32)
@@ -36,7 +38,9 @@ class Case:
         self.plan = lkb.Plan.for_workload(w, self.masks, self.policies, self.is_special,
                                           special_capacity=special_capacity)
         self.capacity = capacity or total
-        self.cache = lkb.Cache(self.plan, w.batch, self.capacity, device=device, middle_tokens=middle_tokens)
+        self.kv_format = kv_format
+        self.cache = lkb.Cache(self.plan, w.batch, self.capacity, device=device, middle_tokens=middle_tokens,
+                               kv_format=kv_format)
         self.device = device
         self.layers = list(range(w.num_layers)) if layers is None else layers
         self.ids = torch.from_numpy(S.make_token_ids(w, total)).to(device)
@@ -73,7 +77,8 @@ class Case:
         k, v = self.history(layer)
         w = self.w
         ragged = not np.isscalar(N)
-        if heads is None and not ragged:
+        quant = self.kv_format == lkb.KV_INT8
+        if heads is None and not ragged and not quant:
             K, V = f64(k[:, :N]), f64(v[:, :N])
             return OA.decode_layer(f64(q), K, V, self.masks[layer], self.policies[layer], N, w.sink,
                                    w.local, w.local_only_window, self.flags)
@@ -84,8 +89,9 @@ class Case:
             Nb = int(N[b]) if ragged else N
             K, V = f64(k[b, :Nb, h]), f64(v[b, :Nb, h])
             kept = np.nonzero(self.masks[layer, h])[0]
-            out[(b, h)] = OA.decode_head(f64(q[b, h * G:(h + 1) * G]), K, V, int(self.policies[layer, h]),
-                                         kept, Nb, w.sink, w.local, w.local_only_window, self.flags[b])
+            head = OQ.decode_head_quantized if quant else OA.decode_head
+            out[(b, h)] = head(f64(q[b, h * G:(h + 1) * G]), K, V, int(self.policies[layer, h]),
+                               kept, Nb, w.sink, w.local, w.local_only_window, self.flags[b])
         if heads is None:
             full = np.zeros((w.batch, w.num_q_heads, 128))
             for (b, h), r in out.items():
@@ -114,6 +120,20 @@ class Case:
                 assert torch.equal(ka[ri], k[b, ti, h]), (layer, b, h, "K region A")
                 assert torch.equal(va[ri], v[b, ti, h]), (layer, b, h, "V region A")
             rows, toks = OL.region_b(pol, len(kept), Nb, w.sink, w.local)
+            if len(rows) and self.kv_format == lkb.KV_INT8:
+                # complete blocks: codes and scales exactly as the oracle
+                # quantises them; the open block: bf16 tail rows
+                blocks = OQ.middle_blocks(f64(k[b, :, h]).astype(np.float32), f64(v[b, :, h]).astype(np.float32),
+                                          kept, Nb, w.sink, w.local)
+                assert r.sealed_blocks == len(blocks), (layer, b, h, r.sealed_blocks, len(blocks))
+                for j, (kc, ks, vc, vs) in enumerate(blocks):
+                    gk, gks, gv, gvs = self.cache.block(layer, b, h, j)
+                    assert np.array_equal(gk, kc) and np.array_equal(gks.view(np.uint32), ks.view(np.uint32)), \
+                        (layer, b, h, j, "K block")
+                    assert np.array_equal(gv, vc) and np.array_equal(gvs.view(np.uint32), vs.view(np.uint32)), \
+                        (layer, b, h, j, "V block")
+                keep = rows >= 128 * len(blocks)
+                rows, toks = rows[keep] - 128 * len(blocks), toks[keep]
             if len(rows):
                 ri = torch.from_numpy(rows).to(self.device)
                 ti = torch.from_numpy(toks).to(self.device)

@@ -157,3 +157,21 @@ def test_paged_cache_bytes(lib):
     with pytest.raises(lkb.LeankError) as e:
         plan.cache_bytes(B, cap, middle_tokens=-1)
     assert e.value.status == lkb.LK_ERR_ARG
+
+
+def test_int8_cache_bytes(lib):
+    w = S.WORKLOADS[1]
+    plan = lkb.Plan.for_workload(w, S.masks_with_counts(w, [32] * 8), S.make_policies(w))
+    B, cap = 2, 32768
+    mid = cap - w.sink - w.local
+    bf16 = plan.cache_bytes(B, cap)
+    q8 = plan.cache_bytes(B, cap, kv_format=lkb.KV_INT8)
+    # middle rows: 320 B in bf16, 165 B per row in sealed blocks (+ a 128-row bf16 tail)
+    blocks = mid // 128
+    expect = bf16 - 8 * B * mid * 320 + 8 * B * (blocks * 132 * 160 + 128 * 320)
+    assert abs(q8 - expect) < (1 << 20)
+    paged = plan.cache_bytes(B, cap, middle_tokens=B * mid, kv_format=lkb.KV_INT8)
+    assert abs(paged - q8) < (1 << 20)
+    with pytest.raises(lkb.LeankError) as e:
+        plan.cache_bytes(B, cap, kv_format=7)
+    assert e.value.status == lkb.LK_ERR_ARG

@@ -71,3 +71,19 @@ def test_full_fastgen_mix_all_layers(cuda):
                 pairs.add((int(rng.integers(w.batch)), int(hs[0])))
         pairs = sorted(pairs)
         _check_layer(case, layer, w.context, pairs, pairs[:2])
+
+
+def test_full_qwen25_7b_long_int8(cuda):
+    from decode_attention_pruned_gb300 import binding as lkb
+    w = S.WORKLOADS[3]
+    case = Case(w, total=w.context, gen_device=cuda, kv_format=lkb.KV_INT8)
+    pairs = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    _check_layer(case, 0, w.context, pairs, [(1, h) for h in range(w.num_kv_heads)])
+
+
+def test_full_llama31_8b_layer_int8_paged(cuda):
+    from decode_attention_pruned_gb300 import binding as lkb
+    w = S.WORKLOADS[1]
+    case = Case(w, total=w.context, gen_device=cuda, kv_format=lkb.KV_INT8, middle_tokens=w.context)
+    pairs = [(0, h) for h in range(w.num_kv_heads)]
+    _check_layer(case, 0, w.context, pairs, pairs)
