@@ -210,6 +210,9 @@ __device__ __forceinline__ uint32_t tile_addr64(uint32_t base, int r, int c) {
          ((uint32_t)((c & 3) ^ ((r >> 1) & 3)) << 4);
 }
 
+// kQ8: the cache's middle is INT8 (sealed blocks may occur); the bf16
+// instantiation carries no INT8 code.
+template <bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_k32, const __grid_constant__ CUtensorMap tm_k64,
@@ -568,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float s[kSubPerWarp][4];
 #pragma unroll
       for (int j = 0; j < kSubPerWarp; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-      if (d.region == 2) {
+      if (kQ8 && d.region == 2) {
         // ---- sealed INT8 block: S^T = K_codes (f16, exact) . Q'^T with
         // Q' = q[kept] * (K scale of the channel), split into f16 hi + lo
         const int kb = d.width;
@@ -669,7 +672,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float mn0 = m0, mn1 = m1;
-      const uint32_t vbase = kbase + (d.region == 2 ? (uint32_t)qblock_voff(d.width) : (uint32_t)kTileRows * 2 * d.width);
+      const uint32_t vbase =
+          kbase + (kQ8 && d.region == 2 ? (uint32_t)qblock_voff(d.width) : (uint32_t)kTileRows * 2 * d.width);
 #pragma unroll
       for (int j = 0; j < kSubPerWarp; ++j) {
         if (!live[j]) continue;
@@ -678,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l0 += p0 + p2;
         l1 += p1 + p3;
         const int r0 = 16 * (warp + kConsumerWarps * j);
-        if (d.region == 2) {
+        if (kQ8 && d.region == 2) {
           // ---- O^T += V_codes^T (f16, exact) . P'^T, P' = p * (V scale of
           // the token), split into f16 hi + lo
           const float* vsc =
@@ -874,7 +878,9 @@ size_t decode_smem_bytes() { return kSmemBytes; }
 cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int ctas, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t err = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_done = true;
   }
@@ -888,7 +894,10 @@ cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel, maps[kPoolK128], maps[kPoolV], maps[kPoolK32],
+  if (args.cv.kv_format == kKvInt8)
+    return cudaLaunchKernelEx(&cfg, decode_kernel<true>, maps[kPoolK128], maps[kPoolV], maps[kPoolK32],
+                              maps[kPoolK64], maps[kPoolK96], args);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<false>, maps[kPoolK128], maps[kPoolV], maps[kPoolK32],
                             maps[kPoolK64], maps[kPoolK96], args);
 }
 
