@@ -976,7 +976,7 @@ lk_status lk_cache_block(lk_cache cache, int32_t layer, int32_t b, int32_t kv_he
       for (int c = 0; c < k; ++c) k_codes[r * k + c] = (int8_t)img[(size_t)r * k + qbyte(k, r, c)];
     if (v_codes)
       for (int c = 0; c < kHeadDim; ++c)
-        v_codes[r * kHeadDim + c] = (int8_t)img[qblock_voff(k) + (size_t)r * kHeadDim + qbyte(kHeadDim, r, c)];
+        v_codes[r * kHeadDim + c] = (int8_t)((int)img[qblock_voff(k) + (size_t)r * kHeadDim + qbyte(kHeadDim, r, c)] - 128);
   }
   if (k_scales) std::memcpy(k_scales, img.data() + qblock_ksoff(k), (size_t)k * 4);
   if (v_scales) std::memcpy(v_scales, img.data() + qblock_vsoff(k), (size_t)kQBlockRows * 4);

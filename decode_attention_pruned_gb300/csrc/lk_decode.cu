@@ -37,16 +37,18 @@
 namespace lk {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 8;                       // two per SM sub-partition
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileRows = kTmaBoxRows;                  // 128 tokens per stage
-constexpr int kSubPerWarp = kTileRows / 16 / kConsumerWarps;   // m16 row blocks per warp
-static_assert(kSubPerWarp == 2, "two 16-row blocks per consumer warp");
+static_assert(kTileRows == 16 * kConsumerWarps, "one 16-row block per consumer warp");
+constexpr int kMergeSlots = 4;                          // (o, m, l) slots of the segment merge
+constexpr int kQStride = kHeadDim + 8;                  // padded q row (bf16): conflict-free ldmatrix
 // Stages live in a byte ring: a stage holds a K tile (128 rows x width) and a
 // V tile (128 rows x 128), so narrow-K tiles (40 KB at k = 32) keep five
-// stages in flight where full-width ones (64 KB) keep three.
-constexpr int kSlots = 10;                              // barrier pairs = stages in flight at most
-constexpr int kRingBytes = 208 * 1024;
+// stages in flight where full-width ones (64 KB) keep three; sealed INT8
+// blocks (21-33 KB) keep up to nine.
+constexpr int kSlots = 16;                              // barrier pairs = stages in flight at most (power of 2)
+constexpr int kRingBytes = 204 * 1024;
 constexpr int kUnitsA = 2 * kHeadDim * 2;               // line cost of a full-width row: its bytes
 constexpr int kFirst = 1, kLast = 2;
 
@@ -65,9 +67,11 @@ struct StageDesc {
 struct SmemLayout {
   static constexpr int kRingOff = 0;
   static constexpr int kMergeOOff = kRingOff + kRingBytes;
-  static constexpr int kMergeMOff = kMergeOOff + kConsumerWarps * kMaxGroup * kHeadDim * 4;
-  static constexpr int kMergeLOff = kMergeMOff + kConsumerWarps * kMaxGroup * 4;
-  static constexpr int kDescOff = kMergeLOff + kConsumerWarps * kMaxGroup * 4;
+  static constexpr int kMergeMOff = kMergeOOff + kMergeSlots * kMaxGroup * kHeadDim * 4;
+  static constexpr int kMergeLOff = kMergeMOff + kMergeSlots * kMaxGroup * 4;
+  static constexpr int kQOff = kMergeLOff + kMergeSlots * kMaxGroup * 4;     // q of the segment: all channels
+  static constexpr int kQKOff = kQOff + kMaxGroup * kQStride * 2;             //   and kept channels first
+  static constexpr int kDescOff = kQKOff + kMaxGroup * kQStride * 2;
   static constexpr int kBarOff = kDescOff + kSlots * (int)sizeof(StageDesc);
   static constexpr int kScanOff = kBarOff + 2 * kSlots * 8;
   static constexpr int kMiscOff = kScanOff + (kThreads / 32) * 8;
@@ -191,10 +195,6 @@ __device__ __forceinline__ void consumer_bar() {
 
 __device__ __forceinline__ void record_status(const DecodeArgs& a, uint32_t bits) {
   atomicOr(&a.cv.hdr->status, bits);
-}
-
-__device__ __forceinline__ uint32_t ld_q_pair(const uint16_t* row, int c) {
-  return *reinterpret_cast<const uint32_t*>(row + c);
 }
 
 // Shared-memory address of 16-byte chunk `c` (channels 8c..8c+7) of tile row
@@ -323,28 +323,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     // ================================================================ producer
     if (lane == 0) {
+      // The ring is a FIFO of variable-size stages: the oldest in-flight
+      // stage starts at `tail`, the next one goes at `head` (or at 0 when it
+      // does not fit before the end).  `wrapped`: the in-flight bytes run
+      // from tail to the end and on from 0 to head.  O(1) per stage.
       uint32_t issued = 0, freed = 0;     // stages issued / known released
-      uint32_t head = 0;                   // next free ring byte
+      uint32_t head = 0, tail = 0;
+      bool wrapped = false;
       bool ok = true;
       // Wait (bounded) until the oldest in-flight stage is released.
       auto free_oldest = [&]() -> bool {
-        const uint32_t slot = freed % kSlots;
+        const uint32_t slot = freed & (kSlots - 1);
         if (!mbar_wait_bounded(bar_empty + 8 * slot, (freed / kSlots) & 1u, a.wait_limit_ns)) return false;
         ++freed;
+        if (freed == issued) {
+          head = tail = 0;
+          wrapped = false;
+        } else {
+          const uint32_t t = desc[freed & (kSlots - 1)].koff;
+          if (t < tail) wrapped = false;            // the oldest stage is now past the wrap
+          tail = t;
+        }
         return true;
       };
-      // Ring offset for a stage of `bytes`, once a slot is free and no
-      // in-flight stage overlaps it.
+      // Ring offset for a stage of `bytes`, once a slot and the bytes are free.
       auto reserve = [&](uint32_t bytes, uint32_t& at) -> bool {
-        at = head + bytes <= (uint32_t)kRingBytes ? head : 0u;
-        while (issued != freed) {
-          bool clash = issued - freed == (uint32_t)kSlots;
-          for (uint32_t m = freed; !clash && m != issued; ++m) {
-            const StageDesc& o = desc[m % kSlots];
-            const uint32_t ob = ring_bytes(o.region, o.width);
-            clash = at < o.koff + ob && o.koff < at + bytes;
+        while (true) {
+          if (issued == freed) {
+            at = 0;
+            break;
           }
-          if (!clash) break;
+          if (issued - freed < (uint32_t)kSlots) {
+            if (!wrapped) {
+              if (head + bytes <= (uint32_t)kRingBytes) {
+                at = head;
+                break;
+              }
+              if (bytes <= tail) {
+                at = 0;
+                wrapped = true;
+                break;
+              }
+            } else if (head + bytes <= tail) {
+              at = head;
+              break;
+            }
+          }
           if (!free_oldest()) return false;
         }
         head = at + bytes;
@@ -438,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            const uint32_t stage = issued % kSlots;
+            const uint32_t stage = issued & (kSlots - 1);
             StageDesc d;
             d.e = e;
             d.region = region;
@@ -484,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // end of stream: a descriptor with e < 0 in the next slot
       if (ok && issued - freed == (uint32_t)kSlots) ok = free_oldest();
       if (ok) {
-        const uint32_t stage = issued % kSlots;
+        const uint32_t stage = issued & (kSlots - 1);
         desc[stage].e = -1;
         mbar_arrive(bar_full + 8 * stage);
       } else {
@@ -495,13 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ================================================================ consumers
-  const int ct = tid;                       // 0 .. 127
+  const int ct = tid;                       // 0 .. 255
   const int gid = lane >> 2, tig = lane & 3;
   const int rk = (lane & 7) + ((lane >> 3) & 1) * 8;    // ldmatrix row of the K (A) operand
   const int ck = lane >> 4;                              // +0 / +1 chunk
   const int rv = (lane & 7) + (lane >> 4) * 8;          // ldmatrix.trans row of the V^T operand
   const int cvh = (lane >> 3) & 1;
   const float NEG_INF = -INFINITY;
+  uint16_t* qa_s = reinterpret_cast<uint16_t*>(sm + SmemLayout::kQOff);
+  uint16_t* qb_s = reinterpret_cast<uint16_t*>(sm + SmemLayout::kQKOff);
+  // ldmatrix address of the q B-fragments: heads (lane & 7), 8-channel
+  // column (lane >> 3) of a 32-channel group
+  const uint32_t qa_lane = base + SmemLayout::kQOff + (uint32_t)((lane & 7) * kQStride + 8 * (lane >> 3)) * 2;
+  const uint32_t qb_lane = base + SmemLayout::kQKOff + (uint32_t)((lane & 7) * kQStride + 8 * (lane >> 3)) * 2;
 
   // entries with no resident token: o = 0, written by CTA (e mod grid)
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
@@ -513,13 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   float o[8][4];
   float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
-  uint32_t qa[8][2], qb[8][2];
+  // INT8 tiles accumulate V codes as 1152 + code: o carries 1152 * sum(P')
+  // per head column, removed at the segment end (c0, c1: this lane's share)
+  float c0 = 0.f, c1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    qa[i][0] = qa[i][1] = qb[i][0] = qb[i][1] = 0u;
-  }
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
+  // this warp's 16 rows of every tile
+  const int r0 = 16 * warp;
   int stage = 0;
   uint32_t phase = 0;
   while (true) {
@@ -530,47 +561,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const StageDesc d = desc[stage];
     if (d.e < 0) break;
     if (d.flags & kFirst) {
-      // (re)load q fragments of the entry: B operand of S^T = K Q^T
+      // q of the entry into shared memory: all channels (full-width rows)
+      // and the kept channels in kept order (middle rows); the B operand of
+      // S^T = K Q^T is read from there with ldmatrix.  Every consumer warp
+      // passed the previous segment's merge barrier, so the old q is dead.
       const EntryId id = entry_id(a, d.e);
       const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
       const int16_t* kept = cv.kept + ((size_t)id.l * cv.Hkv + id.h) * kHeadDim;
-      const bool live = gid < G;
-      const uint16_t* qrow =
-          a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G + (live ? gid : 0)) * kHeadDim;
       const int kk = hd.policy == kFull ? hd.n_kept : 0;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int c = ks * 16 + 2 * tig;
-        qa[ks][0] = live ? ld_q_pair(qrow, c) : 0u;
-        qa[ks][1] = live ? ld_q_pair(qrow, c + 8) : 0u;
-        if (live && c < kk) {
-          qb[ks][0] = (uint32_t)qrow[kept[c]] | ((uint32_t)qrow[kept[c + 1]] << 16);
-          qb[ks][1] = (uint32_t)qrow[kept[c + 8]] | ((uint32_t)qrow[kept[c + 9]] << 16);
-        } else {
-          qb[ks][0] = qb[ks][1] = 0u;
+      const uint16_t* qg = a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
+      for (int i = ct; i < kMaxGroup * kHeadDim; i += kConsumerWarps * 32) {
+        const int g = i >> 7, c = i & (kHeadDim - 1);
+        uint16_t va = 0, vb = 0;
+        if (g < G) {
+          va = qg[g * kHeadDim + c];
+          if (c < kk) vb = qg[g * kHeadDim + kept[c]];
         }
+        qa_s[g * kQStride + c] = va;
+        qb_s[g * kQStride + c] = vb;
       }
+      consumer_bar();
       m0 = m1 = NEG_INF;
-      l0 = l1 = 0.f;
+      l0 = l1 = c0 = c1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
 
-    // this warp's two 16-row blocks of the tile: rows 16*(warp + 4j); valid
-    // rows rlo .. rhi - 1 (sealed blocks may be shared with another CTA)
+    // valid rows rlo .. rhi - 1 of the tile (sealed blocks may be shared with
+    // another CTA)
     const int rlo = d.rlo, rhi = d.rlo + d.nrows;
     const uint32_t kbase = base + SmemLayout::kRingOff + d.koff;
-    float x[kSubPerWarp][4];
-    bool live[kSubPerWarp];
-#pragma unroll
-    for (int j = 0; j < kSubPerWarp; ++j) {
-      const int r0 = 16 * (warp + kConsumerWarps * j);
-      live[j] = r0 < rhi && r0 + 16 > rlo;
-    }
-    if (live[0] || live[1]) {
-      float s[kSubPerWarp][4];
-#pragma unroll
-      for (int j = 0; j < kSubPerWarp; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+    if (r0 < rhi && r0 + 16 > rlo) {
+      // two independent accumulators halve the mma dependency chain
+      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
       if (kQ8 && d.region == 2) {
         // ---- sealed INT8 block: S^T = K_codes (f16, exact) . Q'^T with
         // Q' = q[kept] * (K scale of the channel), split into f16 hi + lo
@@ -579,77 +602,74 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
           if (2 * kp < (kb >> 4)) {
+            uint32_t qv[4];
+            ldsm_x4(qb_lane + 64u * kp, qv[0], qv[1], qv[2], qv[3]);
             uint32_t bh[2][2], bl[2][2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int ks = 2 * kp + u;
-              const int c = 16 * ks + 2 * tig;
+              const int c = 16 * (2 * kp + u) + 2 * tig;
               const float2 s01 = *reinterpret_cast<const float2*>(&ksc[c]);
               const float2 s89 = *reinterpret_cast<const float2*>(&ksc[c + 8]);
-              const float q0 = bf16_lo(qb[ks][0]) * s01.x, q1 = bf16_hi(qb[ks][0]) * s01.y;
-              const float q8 = bf16_lo(qb[ks][1]) * s89.x, q9 = bf16_hi(qb[ks][1]) * s89.y;
+              const float q0 = bf16_lo(qv[2 * u]) * s01.x, q1 = bf16_hi(qv[2 * u]) * s01.y;
+              const float q8 = bf16_lo(qv[2 * u + 1]) * s89.x, q9 = bf16_hi(qv[2 * u + 1]) * s89.y;
               bh[u][0] = pack_f16x2(q0, q1);
               bh[u][1] = pack_f16x2(q8, q9);
               bl[u][0] = pack_f16x2(q0 - f16_lo(bh[u][0]), q1 - f16_hi(bh[u][0]));
               bl[u][1] = pack_f16x2(q8 - f16_lo(bh[u][1]), q9 - f16_hi(bh[u][1]));
             }
-#pragma unroll
-            for (int j = 0; j < kSubPerWarp; ++j) {
-              if (!live[j]) continue;
-              const int row = 16 * (warp + kConsumerWarps * j) + rk;
-              const int grp = 2 * kp + ck;
-              uint32_t w0, w1, w2, w3;
-              ldsm_x4(kbase + (uint32_t)(row * kb + 16 * (grp ^ qswz(kb, row))), w0, w1, w2, w3);
-              uint32_t f0, f1, f2, f3;
-              i8x4_to_f16x2(w0, f0, f2);       // rows gid: k 2tig.. / 2tig+8..
-              i8x4_to_f16x2(w1, f1, f3);       // rows gid + 8
-              mma_f16_16816(s[j], f0, f1, f2, f3, bh[0][0], bh[0][1]);
-              mma_f16_16816(s[j], f0, f1, f2, f3, bl[0][0], bl[0][1]);
-              i8x4_to_f16x2(w2, f0, f2);
-              i8x4_to_f16x2(w3, f1, f3);
-              mma_f16_16816(s[j], f0, f1, f2, f3, bh[1][0], bh[1][1]);
-              mma_f16_16816(s[j], f0, f1, f2, f3, bl[1][0], bl[1][1]);
-            }
+            const int row = r0 + rk;
+            const int grp = 2 * kp + ck;
+            uint32_t w0, w1, w2, w3;
+            ldsm_x4(kbase + (uint32_t)(row * kb + 16 * (grp ^ qswz(kb, row))), w0, w1, w2, w3);
+            uint32_t f0, f1, f2, f3;
+            i8x4_to_f16x2(w0, f0, f2);       // rows gid: k 2tig.. / 2tig+8..
+            i8x4_to_f16x2(w1, f1, f3);       // rows gid + 8
+            mma_f16_16816(sc, f0, f1, f2, f3, bh[0][0], bh[0][1]);
+            mma_f16_16816(sd, f0, f1, f2, f3, bl[0][0], bl[0][1]);
+            i8x4_to_f16x2(w2, f0, f2);
+            i8x4_to_f16x2(w3, f1, f3);
+            mma_f16_16816(sc, f0, f1, f2, f3, bh[1][0], bh[1][1]);
+            mma_f16_16816(sd, f0, f1, f2, f3, bl[1][0], bl[1][1]);
           }
         }
       } else {
-        const bool in_a = d.region == 0;
         const bool fam128 = (d.width & 63) == 0;          // widths 64 / 128 use 128-byte rows
         const int nks = d.width >> 4;
+        const uint32_t q_lane = d.region == 0 ? qa_lane : qb_lane;
+        const int row = r0 + rk;
 #pragma unroll
-        for (int j = 0; j < kSubPerWarp; ++j) {
-          if (!live[j]) continue;
-          const int row = 16 * (warp + kConsumerWarps * j) + rk;
+        for (int kp = 0; kp < 4; ++kp) {
+          if (2 * kp < nks) {
+            uint32_t qv[4];
+            ldsm_x4(q_lane + 64u * kp, qv[0], qv[1], qv[2], qv[3]);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            if (ks < nks) {
-              const int c = 2 * ks + ck;
+            for (int u = 0; u < 2; ++u) {
+              const int c = 2 * (2 * kp + u) + ck;
               const uint32_t addr = fam128 ? tile_addr128(kbase, row, c) : tile_addr64(kbase, row, c);
               uint32_t a0, a1, a2, a3;
               ldsm_x4(addr, a0, a1, a2, a3);
-              const uint32_t b0 = in_a ? qa[ks][0] : qb[ks][0];
-              const uint32_t b1 = in_a ? qa[ks][1] : qb[ks][1];
-              mma_bf16_16816(s[j], a0, a1, a2, a3, b0, b1);
+              if (u == 0)
+                mma_bf16_16816(sc, a0, a1, a2, a3, qv[0], qv[1]);
+              else
+                mma_bf16_16816(sd, a0, a1, a2, a3, qv[2], qv[3]);
             }
           }
         }
       }
 #pragma unroll
-      for (int j = 0; j < kSubPerWarp; ++j) {
-        const int t0 = 16 * (warp + kConsumerWarps * j) + gid;
-        const bool v0 = live[j] && t0 >= rlo && t0 < rhi, v1 = live[j] && t0 + 8 >= rlo && t0 + 8 < rhi;
-        x[j][0] = v0 ? s[j][0] * a.scale_log2 : NEG_INF;
-        x[j][1] = v0 ? s[j][1] * a.scale_log2 : NEG_INF;
-        x[j][2] = v1 ? s[j][2] * a.scale_log2 : NEG_INF;
-        x[j][3] = v1 ? s[j][3] * a.scale_log2 : NEG_INF;
-      }
+      for (int i = 0; i < 4; ++i) sc[i] += sd[i];
+      const int t0 = r0 + gid;
+      const bool v0 = t0 >= rlo && t0 < rhi, v1 = t0 + 8 >= rlo && t0 + 8 < rhi;
+      const float x0 = v0 ? sc[0] * a.scale_log2 : NEG_INF;
+      const float x1 = v0 ? sc[1] * a.scale_log2 : NEG_INF;
+      const float x2 = v1 ? sc[2] * a.scale_log2 : NEG_INF;
+      const float x3 = v1 ? sc[3] * a.scale_log2 : NEG_INF;
       // Lazy rescaling: the running max m of a column moves only when some
       // score of the tile exceeds it by more than kRescaleGap (log2 units);
       // otherwise p = 2^(s - m) <= 2^kRescaleGap, exact in the fp32
       // accumulators and in the hi/lo splits of P.  One warp vote replaces
       // the column-max shuffles in the common case.
-      float mx0 = fmaxf(fmaxf(x[0][0], x[0][2]), fmaxf(x[1][0], x[1][2]));
-      float mx1 = fmaxf(fmaxf(x[0][1], x[0][3]), fmaxf(x[1][1], x[1][3]));
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
       constexpr float kRescaleGap = 8.f;
       if (__any_sync(0xffffffffu, mx0 > m0 + kRescaleGap || mx1 > m1 + kRescaleGap)) {
 #pragma unroll
@@ -663,6 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         m1 = mn1;
         l0 *= al0;
         l1 *= al1;
+        c0 *= al0;
+        c1 *= al1;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           o[i][0] *= al0;
@@ -671,61 +693,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           o[i][3] *= al1;
         }
       }
-      const float mn0 = m0, mn1 = m1;
-      const uint32_t vbase =
-          kbase + (kQ8 && d.region == 2 ? (uint32_t)qblock_voff(d.width) : (uint32_t)kTileRows * 2 * d.width);
+      const float p0 = exp2f(x0 - m0), p1 = exp2f(x1 - m1);   // token gid
+      const float p2 = exp2f(x2 - m0), p3 = exp2f(x3 - m1);   // token gid + 8
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      if (kQ8 && d.region == 2) {
+        // ---- O^T += V_codes^T (f16, exact) . P'^T, P' = p * (V scale of
+        // the token), split into f16 hi + lo
+        const uint32_t vbase = kbase + (uint32_t)qblock_voff(d.width);
+        const float* vsc =
+            reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + d.koff + qblock_vsoff(d.width));
+        const float sv0 = vsc[r0 + gid], sv1 = vsc[r0 + gid + 8];
+        const float q0 = p0 * sv0, q1 = p1 * sv0, q2 = p2 * sv1, q3 = p3 * sv1;
+        c0 += q0 + q2;
+        c1 += q1 + q3;
+        const uint32_t h01 = pack_f16x2(q0, q1), h23 = pack_f16x2(q2, q3);
+        const uint32_t r01 = pack_f16x2(q0 - f16_lo(h01), q1 - f16_hi(h01));
+        const uint32_t r23 = pack_f16x2(q2 - f16_lo(h23), q3 - f16_hi(h23));
+        const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+        const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
+        const int row = r0 + rk;
 #pragma unroll
-      for (int j = 0; j < kSubPerWarp; ++j) {
-        if (!live[j]) continue;
-        const float p0 = exp2f(x[j][0] - mn0), p1 = exp2f(x[j][1] - mn1);   // token gid
-        const float p2 = exp2f(x[j][2] - mn0), p3 = exp2f(x[j][3] - mn1);   // token gid + 8
-        l0 += p0 + p2;
-        l1 += p1 + p3;
-        const int r0 = 16 * (warp + kConsumerWarps * j);
-        if (kQ8 && d.region == 2) {
-          // ---- O^T += V_codes^T (f16, exact) . P'^T, P' = p * (V scale of
-          // the token), split into f16 hi + lo
-          const float* vsc =
-              reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + d.koff + qblock_vsoff(d.width));
-          const float sv0 = vsc[r0 + gid], sv1 = vsc[r0 + gid + 8];
-          const float q0 = p0 * sv0, q1 = p1 * sv0, q2 = p2 * sv1, q3 = p3 * sv1;
-          const uint32_t h01 = pack_f16x2(q0, q1), h23 = pack_f16x2(q2, q3);
-          const uint32_t r01 = pack_f16x2(q0 - f16_lo(h01), q1 - f16_hi(h01));
-          const uint32_t r23 = pack_f16x2(q2 - f16_lo(h23), q3 - f16_hi(h23));
-          const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
-          const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
-          const int row = r0 + rk;
+        for (int i2 = 0; i2 < 4; ++i2) {
+          const int grp = 2 * i2 + ck;
+          uint32_t w0, w1, w2, w3;
+          ldsm_x4_trans(vbase + (uint32_t)(row * kHeadDim + 16 * (grp ^ (row & 7))), w0, w1, w2, w3);
+          uint32_t f0, f1, f2, f3;
+          u8x4_to_f16x2_biased(w0, f0, f1);  // tokens 2tig.. of rows 0-7: channels gid / gid + 8
+          u8x4_to_f16x2_biased(w1, f2, f3);  // tokens 2tig + 8..
+          mma_f16_16816(o[2 * i2], f0, f1, f2, f3, ph0, ph1);
+          mma_f16_16816(o[2 * i2], f0, f1, f2, f3, pr0, pr1);
+          u8x4_to_f16x2_biased(w2, f0, f1);
+          u8x4_to_f16x2_biased(w3, f2, f3);
+          mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, ph0, ph1);
+          mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, pr0, pr1);
+        }
+      } else {
+        // P as a bf16 pair hi + lo (two mmas): P.V keeps ~16 mantissa bits
+        const uint32_t vbase = kbase + (uint32_t)kTileRows * 2 * d.width;
+        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
+        const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+        const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+        // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
+        const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+        const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
+        const int row = r0 + rv;
 #pragma unroll
-          for (int i2 = 0; i2 < 4; ++i2) {
-            const int grp = 2 * i2 + ck;
-            uint32_t w0, w1, w2, w3;
-            ldsm_x4_trans(vbase + (uint32_t)(row * kHeadDim + 16 * (grp ^ (row & 7))), w0, w1, w2, w3);
-            uint32_t f0, f1, f2, f3;
-            i8x4_to_f16x2(w0, f0, f1);         // tokens 2tig.. of rows 0-7: channels gid / gid + 8
-            i8x4_to_f16x2(w1, f2, f3);         // tokens 2tig + 8..
-            mma_f16_16816(o[2 * i2], f0, f1, f2, f3, ph0, ph1);
-            mma_f16_16816(o[2 * i2], f0, f1, f2, f3, pr0, pr1);
-            i8x4_to_f16x2(w2, f0, f1);
-            i8x4_to_f16x2(w3, f2, f3);
-            mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, ph0, ph1);
-            mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, pr0, pr1);
-          }
-        } else {
-          // P as a bf16 pair hi + lo (two mmas): P.V keeps ~16 mantissa bits
-          const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-          const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-          const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-          // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
-          const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
-          const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
-          const int row = r0 + rv;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(tile_addr128(vbase, row, 2 * i + cvh), a0, a1, a2, a3);
-            mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
-            mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
-          }
+        for (int i = 0; i < 8; ++i) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(tile_addr128(vbase, row, 2 * i + cvh), a0, a1, a2, a3);
+          mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
+          mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
         }
       }
     }
@@ -733,27 +751,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
 
     if (d.flags & kLast) {
-      // ---- merge the 4 warps' (o, m, l) of this segment
+      if (kQ8) {
+        // remove the 1152 bias of the INT8 V codes: o -= 1152 * sum(P')
+        float s0 = c0, s1 = c1;
+#pragma unroll
+        for (int sh = 4; sh < 32; sh <<= 1) {
+          s0 += __shfl_xor_sync(0xffffffffu, s0, sh);
+          s1 += __shfl_xor_sync(0xffffffffu, s1, sh);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i][0] = fmaf(-1152.f, s0, o[i][0]);
+          o[i][1] = fmaf(-1152.f, s1, o[i][1]);
+          o[i][2] = fmaf(-1152.f, s0, o[i][2]);
+          o[i][3] = fmaf(-1152.f, s1, o[i][3]);
+        }
+      }
+      // ---- merge the warps' (o, m, l) of this segment: warps 4..7 hand
+      // theirs to warps 0..3 through the merge slots, then 0..3 publish
       float lr0 = l0, lr1 = l1;
 #pragma unroll
       for (int sh = 4; sh < 32; sh <<= 1) {
         lr0 += __shfl_xor_sync(0xffffffffu, lr0, sh);
         lr1 += __shfl_xor_sync(0xffffffffu, lr1, sh);
       }
-      float* ob = merge_o + warp * kMaxGroup * kHeadDim;
+      const int slotw = warp & (kMergeSlots - 1);
+      float* ob = merge_o + slotw * kMaxGroup * kHeadDim;
+      if (warp >= kMergeSlots) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        ob[(2 * tig) * kHeadDim + 16 * i + gid] = o[i][0];
-        ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] = o[i][1];
-        ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] = o[i][2];
-        ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] = o[i][3];
+        for (int i = 0; i < 8; ++i) {
+          ob[(2 * tig) * kHeadDim + 16 * i + gid] = o[i][0];
+          ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] = o[i][1];
+          ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] = o[i][2];
+          ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] = o[i][3];
+        }
+        if (gid == 0) {
+          merge_m[slotw * kMaxGroup + 2 * tig] = m0;
+          merge_m[slotw * kMaxGroup + 2 * tig + 1] = m1;
+          merge_l[slotw * kMaxGroup + 2 * tig] = lr0;
+          merge_l[slotw * kMaxGroup + 2 * tig + 1] = lr1;
+        }
       }
-      if (gid == 0) {
-        merge_m[warp * kMaxGroup + 2 * tig] = m0;
-        merge_m[warp * kMaxGroup + 2 * tig + 1] = m1;
-        merge_l[warp * kMaxGroup + 2 * tig] = lr0;
-        merge_l[warp * kMaxGroup + 2 * tig + 1] = lr1;
+      consumer_bar();
+      if (warp < kMergeSlots) {
+        const float mo0 = merge_m[slotw * kMaxGroup + 2 * tig], mo1 = merge_m[slotw * kMaxGroup + 2 * tig + 1];
+        const float lo0 = merge_l[slotw * kMaxGroup + 2 * tig], lo1 = merge_l[slotw * kMaxGroup + 2 * tig + 1];
+        const float mn0 = fmaxf(m0, mo0), mn1 = fmaxf(m1, mo1);
+        const float fa0 = m0 == NEG_INF ? 0.f : exp2f(m0 - mn0), fb0 = mo0 == NEG_INF ? 0.f : exp2f(mo0 - mn0);
+        const float fa1 = m1 == NEG_INF ? 0.f : exp2f(m1 - mn1), fb1 = mo1 == NEG_INF ? 0.f : exp2f(mo1 - mn1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i][0] = o[i][0] * fa0 + ob[(2 * tig) * kHeadDim + 16 * i + gid] * fb0;
+          o[i][1] = o[i][1] * fa1 + ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] * fb1;
+          o[i][2] = o[i][2] * fa0 + ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] * fb0;
+          o[i][3] = o[i][3] * fa1 + ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] * fb1;
+        }
+        lr0 = lr0 * fa0 + lo0 * fb0;
+        lr1 = lr1 * fa1 + lo1 * fb1;
+        m0 = mn0;
+        m1 = mn1;
       }
+      consumer_bar();
+      if (warp < kMergeSlots) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          ob[(2 * tig) * kHeadDim + 16 * i + gid] = o[i][0];
+          ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] = o[i][1];
+          ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] = o[i][2];
+          ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] = o[i][3];
+        }
+        if (gid == 0) {
+          merge_m[slotw * kMaxGroup + 2 * tig] = m0;
+          merge_m[slotw * kMaxGroup + 2 * tig + 1] = m1;
+          merge_l[slotw * kMaxGroup + 2 * tig] = lr0;
+          merge_l[slotw * kMaxGroup + 2 * tig + 1] = lr1;
+        }
+      }
+      // the segment's state now lives in the merge slots (the next tile
+      // starts a segment); free its registers for the combine below
+      m0 = m1 = NEG_INF;
+      l0 = l1 = c0 = c1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
       consumer_bar();
       const EntryId id = entry_id(a, d.e);
       float* dst = a.o + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
@@ -764,11 +843,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = q4 >> 5, dd = (q4 & 31) * 4;
         float M = NEG_INF;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, merge_m[w * kMaxGroup + g]);
+        for (int w = 0; w < kMergeSlots; ++w) M = fmaxf(M, merge_m[w * kMaxGroup + g]);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float L = 0.f;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < kMergeSlots; ++w) {
           const float mw = merge_m[w * kMaxGroup + g];
           const float f = mw == NEG_INF ? 0.f : exp2f(mw - M);
           const float4 v = *reinterpret_cast<const float4*>(&merge_o[(w * kMaxGroup + g) * kHeadDim + dd]);

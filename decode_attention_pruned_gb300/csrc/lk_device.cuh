@@ -172,6 +172,14 @@ __device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& even, uint32
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(odd) : "r"(o), "r"(0x64806480u));
 }
 
+// Four offset-binary codes u (bytes 0..3 of w) as the exact f16 values
+// 1024 + u: (byte 0, byte 2) and (byte 1, byte 3).  The caller removes the
+// 1152 = 1024 + 128 bias afterwards.
+__device__ __forceinline__ void u8x4_to_f16x2_biased(uint32_t w, uint32_t& even, uint32_t& odd) {
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(even) : "r"(w), "r"(0x64646464u), "r"(0x4240u));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(odd) : "r"(w), "r"(0x64646464u), "r"(0x4341u));
+}
+
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;

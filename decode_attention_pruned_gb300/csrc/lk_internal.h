@@ -25,7 +25,8 @@
 //   [K codes 128 x k][V codes 128 x 128][K scales k x f32][V scales 128 x f32]
 // Codes are row-major; within each 16-channel group a row stores channels
 // (0, 8, 1, 9, ..., 7, 15) and its 16-byte groups are XOR-swizzled by row
-// (qswz), so ldmatrix reads mma fragments without bank conflicts.
+// (qswz), so ldmatrix reads mma fragments without bank conflicts.  K codes
+// are two's complement, V codes offset binary (code + 128).
 #pragma once
 #include <stdint.h>
 

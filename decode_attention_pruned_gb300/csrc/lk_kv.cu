@@ -147,7 +147,8 @@ __device__ void seal_block(uint8_t* dst, int k, KF kv, VF vv, int lane) {
     const float sc = __fdiv_rn(m, 127.f);
     if (lane == 0) vs[r] = sc;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) vc[r * kHeadDim + qbyte(kHeadDim, r, 4 * lane + i)] = (uint8_t)quant8(x[i], sc);
+    for (int i = 0; i < 4; ++i)
+      vc[r * kHeadDim + qbyte(kHeadDim, r, 4 * lane + i)] = (uint8_t)(quant8(x[i], sc) + 128);   // offset binary
   }
 }
 
