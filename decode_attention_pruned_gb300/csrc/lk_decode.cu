@@ -235,12 +235,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int E = a.nlayers * cv.B * cv.Hkv;
   const int G = cv.G;
 
-  if (tid == 0) {
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, kConsumerWarps);
-    }
+  static_assert(kSlots <= 32, "one barrier pair per lane of warp 0");
+  if (tid < kSlots) {
+    mbar_init(bar_full + 8 * tid, 1);
+    mbar_init(bar_empty + 8 * tid, kConsumerWarps);
     fence_barrier_init();
+  }
+  if (tid == 0) {
     misc[0] = E;       // first entry of this CTA
     misc[1] = 0;       // its line offset
     misc[2] = 0;       // last-CTA flag of a segment
@@ -549,6 +550,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
+  // q of entry e into shared memory: all channels (full-width rows) and the
+  // kept channels in kept order (middle rows); the B operand of S^T = K Q^T
+  // is read from there with ldmatrix.  Callers separate it from readers of
+  // the previous q with a consumer barrier.
+  auto stage_q = [&](int e) {
+    const EntryId id = entry_id(a, e);
+    const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+    const int16_t* kept = cv.kept + ((size_t)id.l * cv.Hkv + id.h) * kHeadDim;
+    const int kk = hd.policy == kFull ? hd.n_kept : 0;
+    const uint16_t* qg = a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
+    for (int i = ct; i < kMaxGroup * kHeadDim; i += kConsumerWarps * 32) {
+      const int g = i >> 7, c = i & (kHeadDim - 1);
+      uint16_t va = 0, vb = 0;
+      if (g < G) {
+        va = qg[g * kHeadDim + c];
+        if (c < kk) vb = qg[g * kHeadDim + kept[c]];
+      }
+      qa_s[g * kQStride + c] = va;
+      qb_s[g * kQStride + c] = vb;
+    }
+  };
+  auto prefetch_q = [&](int e) {
+    const EntryId id = entry_id(a, e);
+    if (ct < G * 2) {       // G rows of 256 B: two 128-byte lines each
+      const uint16_t* qg = a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(qg + ct * 64));
+    } else if (ct < G * 2 + 2) {
+      const int16_t* kept = cv.kept + ((size_t)id.l * cv.Hkv + id.h) * kHeadDim;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(kept + (ct - G * 2) * 64));
+    }
+  };
+  // the first entry's q loads while the first tile is in flight
+  int q_entry = (int)misc[0];
+  if (q_entry < E) stage_q(q_entry);
+
   // this warp's 16 rows of every tile
   const int r0 = 16 * warp;
   int stage = 0;
@@ -561,25 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const StageDesc d = desc[stage];
     if (d.e < 0) break;
     if (d.flags & kFirst) {
-      // q of the entry into shared memory: all channels (full-width rows)
-      // and the kept channels in kept order (middle rows); the B operand of
-      // S^T = K Q^T is read from there with ldmatrix.  Every consumer warp
-      // passed the previous segment's merge barrier, so the old q is dead.
-      const EntryId id = entry_id(a, d.e);
-      const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
-      const int16_t* kept = cv.kept + ((size_t)id.l * cv.Hkv + id.h) * kHeadDim;
-      const int kk = hd.policy == kFull ? hd.n_kept : 0;
-      const uint16_t* qg = a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
-      for (int i = ct; i < kMaxGroup * kHeadDim; i += kConsumerWarps * 32) {
-        const int g = i >> 7, c = i & (kHeadDim - 1);
-        uint16_t va = 0, vb = 0;
-        if (g < G) {
-          va = qg[g * kHeadDim + c];
-          if (c < kk) vb = qg[g * kHeadDim + kept[c]];
-        }
-        qa_s[g * kQStride + c] = va;
-        qb_s[g * kQStride + c] = vb;
-      }
+      // q of the entry into shared memory (staged ahead for the CTA's first
+      // entry); the next entry's q and kept list head for L2 meanwhile
+      if (d.e != q_entry) stage_q(d.e);
+      if (d.e + 1 < E) prefetch_q(d.e + 1);
+      q_entry = -1;
       consumer_bar();
       m0 = m1 = NEG_INF;
       l0 = l1 = c0 = c1 = 0.f;
