@@ -51,9 +51,13 @@ FALLBACK_HBM_GBS = 6800.0
 MAX_CONTEXT_GROWTH = 0.01           # appends may lengthen the context by at most 1 %
 COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 
-# DRAM bytes (read + write) per decode launch from an ncu capture, keyed by the
-# sha256 of the decode kernel source it was taken on (null when it changed).
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per decode launch from one ncu capture, keyed by
+# "<sha256[:16] of the decode kernel source>:<workload>:<kv format>" (the
+# bench reports null when the kernel changed since the capture).
+NCU_TRAFFIC = {
+    "c5dd6fa6b3dabdee:llama31_8b_layer:bf16": 85905664 + 2395904,
+    "c5dd6fa6b3dabdee:qwen25_7b_long:int8": 276224000 + 3402752,
+}
 
 
 def _rank_env():
@@ -363,7 +367,7 @@ def run_gpu(args, rank, local_rank, world):
     alg_bytes = resident_step + L * B * w.num_q_heads * 128 * (2 + 4)
     peak, peak_kind = _peaks()
     achieved = alg_bytes / kdur / 1e9
-    traffic = NCU_TRAFFIC.get(_decode_source_hash())
+    traffic = NCU_TRAFFIC.get(f"{_decode_source_hash()}:{w.name}:{args.kv}")
 
     line = {
         "metric": METRIC,

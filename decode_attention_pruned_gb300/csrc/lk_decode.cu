@@ -252,11 +252,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tm_v);
     tma_prefetch_map(&tm_k32);
   }
-  // the layer's head table is static: pull it towards L1 while the preceding
-  // kernel finishes (lengths and special counts are written by that append,
-  // so they are read only after the dependency wait)
-  for (int h = tid; h < a.nlayers * cv.Hkv; h += kThreads)
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(&cv.heads[a.layer * cv.Hkv + h]));
+  // the head table is static (written once at cache init): load it while
+  // the preceding kernel finishes, which also walks the page table for the
+  // cache header (a prefetch may be dropped on a TLB miss; a load is not).
+  // Lengths and special counts are written by that kernel, so they are read
+  // only after the dependency wait.
+  {
+    int64_t touch = 0;
+    for (int h = tid; h < a.nlayers * cv.Hkv; h += kThreads) touch += cv.heads[a.layer * cv.Hkv + h].row_a;
+    asm volatile("" ::"l"(touch));
+  }
   {
     // warm L2 and the TLB for this thread's first length word (the line may
     // be rewritten by the preceding append: only L2 is touched, which stays
