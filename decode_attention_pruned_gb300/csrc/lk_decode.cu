@@ -51,6 +51,7 @@ constexpr int kSlots = 16;                              // barrier pairs = stage
 constexpr int kRingBytes = 204 * 1024;
 constexpr int kUnitsA = 2 * kHeadDim * 2;               // line cost of a full-width row: its bytes
 constexpr int kFirst = 1, kLast = 2;
+constexpr uint64_t kDrainLimitNs = 1000000000ull;      // bound of the producer's final wait for its copies
 
 struct StageDesc {
   int32_t e;           // entry = b * Hkv + h; < 0 ends the stream
@@ -251,6 +252,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_map(&tm_k128);
     tma_prefetch_map(&tm_v);
     tma_prefetch_map(&tm_k32);
+    tma_prefetch_map(&tm_k64);
+    tma_prefetch_map(&tm_k96);
+    // read every launch parameter the producer uses once, so their constant
+    // cache lines arrive while the preceding kernel finishes
+    uint64_t touch = (uint64_t)cv.hdr ^ (uint64_t)cv.len ^ (uint64_t)cv.cnt ^ (uint64_t)cv.page_table ^
+                     (uint64_t)cv.heads ^ (uint64_t)cv.qpool ^ (uint64_t)cv.kept ^ (uint64_t)a.q ^ (uint64_t)a.o ^
+                     (uint64_t)a.part ^ (uint64_t)a.part_ml ^ (uint64_t)a.counters ^ a.wait_limit_ns;
+    touch ^= (uint64_t)(cv.B ^ cv.Hkv ^ cv.S ^ cv.W ^ cv.W_loc ^ cv.max_pages ^ cv.kv_format ^ a.layer ^ a.nlayers ^
+                        cv.G ^ cv.Hq);
+    asm volatile("" ::"l"(touch));
   }
   // the head table is static (written once at cache init): load it while
   // the preceding kernel finishes, which also walks the page table for the
@@ -280,8 +291,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- the line: per-thread chunks of entries, block exclusive scan
   const int per = (E + kThreads - 1) / kThreads;
   const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
-  uint64_t local = 0;
-  for (int e = e_lo; e < e_hi; ++e) local += entry_cost(entry_geometry(a, e));
+  // the first two entries of the chunk keep their geometry for the second
+  // pass (a whole single-layer launch fits that)
+  Entry g0{0, 0, 0, 0}, g1{0, 0, 0, 0};
+  if (e_lo < e_hi) g0 = entry_geometry(a, e_lo);
+  if (e_lo + 1 < e_hi) g1 = entry_geometry(a, e_lo + 1);
+  uint64_t local = entry_cost(g0) + entry_cost(g1);
+  for (int e = e_lo + 2; e < e_hi; ++e) local += entry_cost(entry_geometry(a, e));
   uint64_t incl = local;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -308,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int found = -1;
     Entry fg{0, 0, 0, 0};
     for (int e = e_lo; found < 0 && e < e_hi; ++e) {
-      const Entry g = entry_geometry(a, e);
+      const Entry g = e == e_lo ? g0 : e == e_lo + 1 ? g1 : entry_geometry(a, e);
       const uint64_t c = entry_cost(g);
       if (acc + c > start) {
         found = e;
@@ -520,6 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         record_status(a, kStatusTimeout);
       }
+      // Keep the CTA alive until every copy this thread issued has landed
+      // (its full barrier completed), so no copy can write shared memory
+      // after the consumers left on a timed-out wait.  Normally these waits
+      // return at once or overlap the consumers' last tiles.
+      for (uint32_t m = freed; m != issued; ++m)
+        if (!mbar_wait_bounded(bar_full + 8 * (m & (kSlots - 1)), (m / kSlots) & 1u, kDrainLimitNs)) {
+          record_status(a, kStatusTimeout);
+          break;
+        }
     }
     return;
   }

@@ -267,3 +267,22 @@ def test_alignment_64_masks(cuda):
     case = Case(w, total=901, masks=masks)
     for layer in range(2):
         _decode_steps(case, layer, 900, 1, layout=True)
+
+
+def test_device_status_bits_reach_the_host(cuda):
+    # the kernels report a timed-out wait, a full layer and a bad token id
+    # through sticky bits in the cache header; lk_check maps and clears them
+    # (set here directly: no kernel is made to time out)
+    case = Case(TINY, total=8)
+    for bit, status in ((1, lkb.LK_ERR_TIMEOUT), (2, lkb.LK_ERR_CAPACITY), (4, lkb.LK_ERR_ARG)):
+        case.cache.buffer[0:4].copy_(torch.tensor([bit], dtype=torch.int32).view(torch.uint8))
+        with pytest.raises(lkb.LeankError) as e:
+            case.cache.check()
+        assert e.value.status == status
+        case.cache.check()                   # cleared
+    # the cache keeps working afterwards
+    case.prefill(0, 8)
+    q = case.q(0, 8)
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    assert _max_err(o, case.expected(0, q, 8)) <= DECODE_TOL
