@@ -208,6 +208,8 @@ def run_gpu(args, rank, local_rank, world):
     caches = []
     for c in range(copies):
         cache = lkb.Cache(plan, B, capacity, device=dev, middle_tokens=middle(capacity), kv_format=kvf)
+        if args.decode_ctas:
+            cache.set_decode_ctas(args.decode_ctas)
         for l in range(L):
             k, v = hist[l] if hist else S.make_kv(w, l, N, device=dev)
             cache.prefill(l, k[:, : N - 1].contiguous(), v[:, : N - 1].contiguous(),
@@ -391,6 +393,7 @@ def run_gpu(args, rank, local_rank, world):
             "cache_copies": copies, "l2_policy": "inputs larger than L2 (rotating cache copies)",
             "cuda_graph": True, "pdl": True, "parallelism": f"replicas x{world}",
             "cache_layout": "paged (128-row pages per width class)" if paged else "contiguous",
+            "decode_ctas": args.decode_ctas or "library default",
             "middle_format": "int8 (complete 128-row blocks; per-channel K / per-token V scales)"
             if kvf == lkb.KV_INT8 else "bf16",
         },
@@ -477,6 +480,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama31_8b_layer")
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"])
+    ap.add_argument("--decode-ctas", type=int, default=0, help="CTAs of a decode launch (0: the library's choice)")
     ap.add_argument("--e2e-steps", type=int, default=4000)
     ap.add_argument("--kernel-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=10.0)

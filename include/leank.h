@@ -344,8 +344,10 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
  * (synchronises `stream` to read the special-token counts). */
 lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_t* bytes);
 
-/* Override the number of CTAs of lk_decode_attn (0 = one per SM); for
- * split-invariance tests.  Must be <= 256. */
+/* Override the number of CTAs of lk_decode_attn (0 = the library's choice:
+ * one per SM, or 27/32 of the SMs for a bf16 launch over at most 64
+ * (sequence, kv head) entries, where fewer, longer streams reach a higher
+ * HBM rate); for tuning and split-invariance tests.  Must be <= 256. */
 lk_status lk_set_decode_ctas(lk_cache cache, int32_t ctas);
 
 /* Synchronise `stream`, read and clear the device status word.  Returns
