@@ -55,8 +55,9 @@ COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 # "<sha256[:16] of the decode kernel source>:<workload>:<kv format>" (the
 # bench reports null when the kernel changed since the capture).
 NCU_TRAFFIC = {
-    "c5dd6fa6b3dabdee:llama31_8b_layer:bf16": 85905664 + 2395904,
-    "c5dd6fa6b3dabdee:qwen25_7b_long:int8": 276224000 + 3402752,
+    "f47b0c3eea6a36c7:llama31_8b_layer:bf16": 86093312 + 2300672,
+    "f47b0c3eea6a36c7:qwen25_7b_long:bf16": 515159040 + 2912768,
+    "f47b0c3eea6a36c7:qwen25_7b_long:int8": 276249600 + 3323136,
 }
 
 

@@ -1,4 +1,5 @@
-// Decode attention over the split LeanK cache (one launch per layer).
+// Decode attention over the split LeanK cache (one launch covers one or
+// more layers).
 //
 // What it computes (LeanK article, framerc.cn, section 3.1 "fused
 // computation"; FastGen article, mhpn.cn, section 3.2 stage 2): for every
@@ -6,23 +7,26 @@
 // (sinks + window ring, LOCAL ring or SPECIAL rows) on all 128 channels and the
 // middle rows of K_prun on the head's kept channels (q gathered to the kept
 // channel list), s = q.k / sqrt(128); one online softmax runs over both
-// regions and o = sum p V.
+// regions and o = sum p V.  INT8 caches hold complete 128-row middle blocks
+// as codes with per-channel K / per-token V scales (KIVI-style, after the
+// pruning); those blocks are scored on the dequantised values.
 //
 // How:
-//   * The work line.  Each (b, h) "entry" is a sequence of 64-row tiles:
-//     region-A tiles then region-B tiles.  A tile costs its rows x bytes per
-//     row / 32 (K row + V row), so the line is measured in bytes.  CTA i of P
-//     takes the tiles whose start falls in [iC/P, (i+1)C/P).  P is capped so
-//     every CTA range spans at least one full tile; then the CTAs touching an
-//     entry are exactly first..last and each writes one partial.
-//   * Per CTA: warp 4 issues TMA loads (64-byte swizzled 32-channel boxes) of
-//     a K tile and a V tile per stage into a 6-deep mbarrier ring; warps 0-3
-//     each take 16 rows of the tile.
-//   * Tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate) with tokens on M:
+//   * The work line.  Each (layer, b, h) "entry" is a run of rows: full-width
+//     rows, then sealed INT8 rows, then bf16 kept-channel rows.  A row costs
+//     the bytes it streams, so the line is measured in bytes.  CTA i of P
+//     takes the rows whose line offset falls in [iC/P, (i+1)C/P); the CTAs
+//     touching an entry are exactly first..last and each writes one partial.
+//   * Per CTA: warp 8 (one lane) issues one TMA load per K tile and one per V
+//     tile (swizzled boxes), or one bulk copy per sealed INT8 block, into a
+//     FIFO ring of variable-size stages with sixteen mbarrier slots; warps
+//     0-7 each take 16 rows of every 128-row tile.
+//   * Tensor cores (mma.sync m16n8k16, fp32 accumulate) with tokens on M:
 //     S^T[16 tok x 8] = K[16 x w] Q^T[w x 8] and O^T[128 x 8] += V^T P^T, so
 //     the G <= 8 query heads only pad N.  P goes from the S^T accumulator to
 //     the B operand of P.V with one movmatrix transpose per 8x8 block; it is
-//     split into bf16 hi + lo halves (two mmas) so P.V keeps ~16 bits of P.
+//     split into hi + lo halves (two mmas) so P.V keeps ~16 bits of P.  INT8
+//     codes enter the f16 mmas exactly; the scales fold into q and p.
 //   * Segment end: warps merge through shared memory; a CTA that owns the
 //     whole entry writes o, otherwise it writes (o, m, l) to its partial slot
 //     and the last of the entry's CTAs (atomic counter) merges them.

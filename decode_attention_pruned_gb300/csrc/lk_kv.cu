@@ -1,5 +1,6 @@
 // Cache editing: append one token per sequence, and prefill a layer from a
-// dense history.  Pure data movement; every copy is bit-exact.
+// dense history.  Pure data movement (every bf16 copy is bit-exact) plus the
+// INT8 sealing of complete middle blocks.
 //
 // Rules (LeanK article, framerc.cn, section 3.1 "cache partition" and 3.2;
 // StreamingLLM sinks + sliding window as in the "intelligent pruning white
@@ -20,6 +21,14 @@
 // all the pages a sequence needs at once, and release pushes them back.  The
 // host checks that enough pages are free before it launches, so a pop that
 // finds the stack empty only records kStatusCapacity.
+//
+// INT8 caches (KIVI-style quantisation after the pruning; LeanK article
+// sections 4.2 and 5.2, the white paper's section 5.2.1): middle rows go to a
+// 128-row bf16 tail; the append that fills its last row seals it into a byte
+// block of the Q pool (per-channel K and per-token V scales, absmax / 127 in
+// fp32, codes x / scale rounded half to even) and clears the tail.  Prefill
+// seals complete blocks straight from its inputs, so both give the same
+// bytes; with paging the sealed blocks are the pages.
 #include <cuda_runtime.h>
 
 #include "lk_device.cuh"
