@@ -386,17 +386,12 @@ def run_gpu(args, rank, local_rank, world):
         "dtype": "bf16" if kvf == lkb.KV_BF16 else "bf16 + int8 (middle blocks)",
         "data": "synthetic (seeded; random K/V/q, seeded LeanK masks)",
         "config": {
-            "workload": w.name, "layers": L, "batch": B, "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
-            "head_dim": 128, "context": N, "context_growth_max": growth, "sink": w.sink, "local": w.local,
-            "prune_pct": w.prune_pct, "mask_budget": w.budget,
+            **workload_config(w, args), "context_growth_max": growth,
             "resident_bytes_per_call": resident_step // L, "effective_GBps": resident_step * K * world / elapsed / 1e9,
             "launches_per_step": "append (all layers) + decode (all layers)",
             "cache_copies": copies, "l2_policy": "inputs larger than L2 (rotating cache copies)",
             "cuda_graph": True, "pdl": True, "parallelism": f"replicas x{world}",
-            "cache_layout": "paged (128-row pages per width class)" if paged else "contiguous",
             "decode_ctas": args.decode_ctas or "library default",
-            "middle_format": "int8 (complete 128-row blocks; per-channel K / per-token V scales)"
-            if kvf == lkb.KV_INT8 else "bf16",
         },
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -455,7 +450,20 @@ def oracle_sample(w_name, budget_s, max_units=None, kv="bf16"):
     return units / el / units_per_call, units, el
 
 
+def workload_config(w, args):
+    """The keys of `config` that define the workload (shared by both arms)."""
+    return {
+        "workload": w.name, "layers": w.num_layers, "batch": w.batch, "q_heads": w.num_q_heads,
+        "kv_heads": w.num_kv_heads, "head_dim": 128, "context": w.context, "sink": w.sink, "local": w.local,
+        "prune_pct": w.prune_pct, "mask_budget": w.budget,
+        "cache_layout": "paged (128-row pages per width class)" if args.layout == "paged" else "contiguous",
+        "middle_format": "int8 (complete 128-row blocks; per-channel K / per-token V scales)"
+        if args.kv == "int8" else "bf16",
+    }
+
+
 def run_reference(args):
+    from decode_attention_pruned_gb300 import synth as S
     W, K = args.warmup, args.steps
     oracle_sample(args.workload, 0.0, max_units=max(1, min(W, 3)), kv=args.kv)
     value, units, el = oracle_sample(args.workload, args.reference_budget, max_units=K, kv=args.kv)
@@ -465,7 +473,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": units,
         "warmup": W, "ms_per_step": el / units * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": args.workload},
+        "config": workload_config(S.WORKLOAD_BY_NAME[args.workload], args),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -286,3 +286,19 @@ def test_device_status_bits_reach_the_host(cuda):
     o = case.cache.decode(0, q)
     case.cache.check()
     assert _max_err(o, case.expected(0, q, 8)) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (32, 4), (12, 4)], ids=["G1", "G8", "G3"])
+@pytest.mark.parametrize("kv", [lkb.KV_BF16, lkb.KV_INT8], ids=["bf16", "int8"])
+def test_query_group_sizes(cuda, hq, hkv, kv):
+    # G = 1 (one query head per kv head), G = 8 (the largest group, all of the
+    # mma's N) and an odd G = 3
+    w = LLAMA.scaled(num_q_heads=hq, num_kv_heads=hkv, context=1700, batch=2)
+    masks = S.masks_with_counts(w, [32, 0, 96, 128])
+    case = Case(w, total=1701, masks=masks, kv_format=kv)
+    case.prefill(0, 1700)
+    case.append(0, 1700)
+    q = case.q(0, 1701)
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    assert _max_err(o, case.expected(0, q, 1701)) <= DECODE_TOL
