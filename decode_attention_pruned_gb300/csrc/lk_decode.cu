@@ -78,7 +78,8 @@ struct SmemLayout {
   static constexpr int kQKOff = kQOff + kMaxGroup * kQStride * 2;             //   and kept channels first
   static constexpr int kDescOff = kQKOff + kMaxGroup * kQStride * 2;
   static constexpr int kBarOff = kDescOff + kSlots * (int)sizeof(StageDesc);
-  static constexpr int kScanOff = kBarOff + 2 * kSlots * 8;
+  static constexpr int kCBarOff = kBarOff + 2 * kSlots * 8;                  // consumer barrier
+  static constexpr int kScanOff = kCBarOff + 8;
   static constexpr int kMiscOff = kScanOff + (kThreads / 32) * 8;
   static constexpr int kBytes = kMiscOff + 64;
 };
@@ -194,12 +195,19 @@ __device__ __forceinline__ int range_owner(uint64_t x, uint64_t C, int P) {
   return (int)min(i, (uint64_t)P - 1);
 }
 
-__device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-}
 
 __device__ __forceinline__ void record_status(const DecodeArgs& a, uint32_t bits) {
   atomicOr(&a.cv.hdr->status, bits);
+}
+
+// Barrier of the consumer warps, on an mbarrier (one arrival per warp) so it
+// is bounded like every other wait: on time-out the warp records the status
+// bit and goes on (its results are then garbage, and lk_check reports it).
+__device__ __forceinline__ void consumer_sync(uint32_t cbar, uint32_t& phase, const DecodeArgs& a) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(cbar);
+  if (!mbar_wait_bounded(cbar, phase, a.wait_limit_ns) && (threadIdx.x & 31) == 0) record_status(a, kStatusTimeout);
+  phase ^= 1u;
 }
 
 // Shared-memory address of 16-byte chunk `c` (channels 8c..8c+7) of tile row
@@ -240,10 +248,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int E = a.nlayers * cv.B * cv.Hkv;
   const int G = cv.G;
 
-  static_assert(kSlots <= 32, "one barrier pair per lane of warp 0");
+  static_assert(kSlots < 32, "one barrier pair per lane of warp 0, plus the consumer barrier");
   if (tid < kSlots) {
     mbar_init(bar_full + 8 * tid, 1);
     mbar_init(bar_empty + 8 * tid, kConsumerWarps);
+    fence_barrier_init();
+  } else if (tid == kSlots) {
+    mbar_init(base + SmemLayout::kCBarOff, kConsumerWarps);
     fence_barrier_init();
   }
   if (tid == 0) {
@@ -555,6 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ================================================================ consumers
   const int ct = tid;                       // 0 .. 255
+  const uint32_t cbar = base + SmemLayout::kCBarOff;
+  uint32_t cphase = 0;
   const int gid = lane >> 2, tig = lane & 3;
   const int rk = (lane & 7) + ((lane >> 3) & 1) * 8;    // ldmatrix row of the K (A) operand
   const int ck = lane >> 4;                              // +0 / +1 chunk
@@ -636,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (d.e != q_entry) stage_q(d.e);
       if (d.e + 1 < E) prefetch_q(d.e + 1);
       q_entry = -1;
-      consumer_bar();
+      consumer_sync(cbar, cphase, a);
       m0 = m1 = NEG_INF;
       l0 = l1 = c0 = c1 = 0.f;
 #pragma unroll
@@ -848,7 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           merge_l[slotw * kMaxGroup + 2 * tig + 1] = lr1;
         }
       }
-      consumer_bar();
+      consumer_sync(cbar, cphase, a);
       if (warp < kMergeSlots) {
         const float mo0 = merge_m[slotw * kMaxGroup + 2 * tig], mo1 = merge_m[slotw * kMaxGroup + 2 * tig + 1];
         const float lo0 = merge_l[slotw * kMaxGroup + 2 * tig], lo1 = merge_l[slotw * kMaxGroup + 2 * tig + 1];
@@ -867,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m0 = mn0;
         m1 = mn1;
       }
-      consumer_bar();
+      consumer_sync(cbar, cphase, a);
       if (warp < kMergeSlots) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -889,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       l0 = l1 = c0 = c1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-      consumer_bar();
+      consumer_sync(cbar, cphase, a);
       const EntryId id = entry_id(a, d.e);
       float* dst = a.o + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
       const bool single = d.first_cta == d.last_cta;
@@ -924,12 +937,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!single) {
         __threadfence();
-        consumer_bar();
+        consumer_sync(cbar, cphase, a);
         if (ct == 0) {
           const int prev = atomicAdd(&a.counters[d.e], 1);
           misc[2] = (prev == d.last_cta - d.first_cta) ? 1 : 0;
         }
-        consumer_bar();
+        consumer_sync(cbar, cphase, a);
         if (misc[2]) {
           // last CTA of the entry: LSE-merge the partials of CTAs first..last
           // (slots first+e .. last+e, consecutive).  Each thread owns 4 output
@@ -951,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[u] = q4a < G * 32 ? __ldcg(src + (size_t)c * G * 32 + q4a) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
           for (int i = ct; i < np * G; i += kConsumerWarps * 32) mlb[i] = __ldcg(&a.part_ml[slot0 * G + i]);
-          consumer_bar();
+          consumer_sync(cbar, cphase, a);
           for (int g = warp; g < G; g += kConsumerWarps) {
             float M = NEG_INF;
             for (int c = lane; c < np; c += 32) M = fmaxf(M, mlb[c * G + g].x);
@@ -971,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mlb[c * G + g].x = mc == NEG_INF ? 0.f : exp2f(mc - M) * inv;
             }
           }
-          consumer_bar();
+          consumer_sync(cbar, cphase, a);
           for (int pass = 0; pass < 2; ++pass) {
             const int q4 = pass == 0 ? q4a : q4b;
             if (q4 >= G * 32) continue;
@@ -997,7 +1010,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ct == 0) a.counters[d.e] = 0;
         }
       }
-      consumer_bar();
+      consumer_sync(cbar, cphase, a);
     }
     if (++stage == kSlots) {
       stage = 0;
