@@ -1,8 +1,10 @@
 """Throughput of decode attention over a LeanK-pruned KV cache on one GB300.
 
 One step = one pass of the whole hot path for one decode token of the
-workload: for each layer, lk_append (new K/V into the window ring, eviction
-into K_prun) then lk_decode_attn (split-K decode + in-launch combine).
+workload: for each layer, the append (new K/V into the window ring, eviction
+into K_prun) then the split-K decode with its in-launch combine.  With a bf16
+middle both run in one launch per step (lk_step_layers); --step split (and
+every INT8 cache) runs lk_append_layers then lk_decode_attn_layers.
 Default workload: the Llama-3.1-8B-shaped layer (32 q / 8 kv heads, d 128,
 batch 1, context 32768, sink 16, window 1024, 70 % channel pruning rounded
 down to multiples of 32, K with 4 channel pairs x8).
@@ -12,11 +14,12 @@ barrier + synchronize; CUDA events on the launching stream; max over ranks.
 Inputs are larger than L2: the steps rotate over C copies of the cache whose
 resident bytes together exceed 4x L2, and C also bounds the context growth
 of the appends.  The step loop is captured in CUDA graphs (programmatic
-dependent launch between append and decode).
+dependent launch between consecutive kernels).
 
 Printed: one JSON line (rank 0).  `value` = decode-attention calls/s of all
-ranks; `roofline` = the decode kernel's algorithmic bytes / its event-timed
-launch duration against the HBM peak; `e2e` = the same metric through
+ranks; `roofline` = the step's decode kernel (the fused one when the step is one
+launch): algorithmic bytes / event-timed launch duration, against the HBM
+peak; `e2e` = the same metric through
 lk_step_host_packed from pinned host memory (copies inside the timed region);
 `cpu_baseline` = the fp64 oracle on a bounded sample on the host cores.
 
@@ -52,12 +55,9 @@ MAX_CONTEXT_GROWTH = 0.01           # appends may lengthen the context by at mos
 COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 
 # DRAM bytes (read + write) per decode launch from one ncu capture, keyed by
-# "<sha256[:16] of the decode kernel source>:<workload>:<kv format>" (the
-# bench reports null when the kernel changed since the capture).
+# "<sha256[:16] of the decode kernel sources>:<workload>:<kv format>:<fused |
+# decode>" (the bench reports null when the kernel changed since the capture).
 NCU_TRAFFIC = {
-    "f47b0c3eea6a36c7:llama31_8b_layer:bf16": 86093312 + 2300672,
-    "f47b0c3eea6a36c7:qwen25_7b_long:bf16": 515159040 + 2912768,
-    "f47b0c3eea6a36c7:qwen25_7b_long:int8": 276249600 + 3323136,
 }
 
 
@@ -80,8 +80,12 @@ def _peaks():
 
 
 def _decode_source_hash():
-    p = os.path.join(ROOT, "decode_attention_pruned_gb300", "csrc", "lk_decode.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """sha256[:16] of the decode kernel's sources (the kernel file and the
+    device headers it includes)."""
+    h = hashlib.sha256()
+    for f in ("lk_decode.cu", "lk_append.cuh", "lk_device.cuh", "lk_internal.h"):
+        h.update(open(os.path.join(ROOT, "decode_attention_pruned_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 class ClockSampler:
@@ -238,11 +242,16 @@ def run_gpu(args, rank, local_rank, world):
     # one step: the new token into every layer (one launch), then decode
     # attention of every layer (one launch; for one layer these are the plain
     # per-layer calls)
+    fused = args.step == "fused" and kvf == lkb.KV_BF16
+
     def enqueue_step(i):
         c = caches[i % copies]
         s = i % bank
-        c.append_layers(0, gk[s], gv[s], gid[s], stream=stream)
-        c.decode_layers(0, gq[s], outs[i % copies], stream=stream)
+        if args.step == "fused":
+            c.step_layers(0, gq[s], gk[s], gv[s], gid[s], outs[i % copies], stream=stream)
+        else:
+            c.append_layers(0, gk[s], gv[s], gid[s], stream=stream)
+            c.decode_layers(0, gq[s], outs[i % copies], stream=stream)
 
     # graphs of whole rotations (copies steps) plus one of the remainder
     def capture(n_steps, start):
@@ -366,11 +375,23 @@ def run_gpu(args, rank, local_rank, world):
     for c in caches:
         c.check(stream)
 
-    # algorithmic bytes of one decode launch (every layer of copy 0 at its length)
+    # algorithmic bytes of one decode launch (every layer of copy 0 at its
+    # length): resident K/V, q in, o out; a fused launch also reads the new
+    # token's K, V and writes them into the window (1 KiB per layer, sequence
+    # and kv head; the evicted row's move into the middle is not counted)
     alg_bytes = resident_step + L * B * w.num_q_heads * 128 * (2 + 4)
+    if fused:
+        alg_bytes += L * B * w.num_kv_heads * 1024
+        kernel_s = elapsed / K                 # one launch per step
+        kernel_timing = "the timed step graph: one fused append + decode launch per step, events around it"
+        kernel_name = "decode_kernel (fused append)"
+    else:
+        kernel_s = kdur
+        kernel_timing = "graph of back-to-back decode launches over the rotating copies, events around it"
+        kernel_name = "decode_kernel"
     peak, peak_kind = _peaks()
-    achieved = alg_bytes / kdur / 1e9
-    traffic = NCU_TRAFFIC.get(f"{_decode_source_hash()}:{w.name}:{args.kv}")
+    achieved = alg_bytes / kernel_s / 1e9
+    traffic = NCU_TRAFFIC.get(f"{_decode_source_hash()}:{w.name}:{args.kv}:{'fused' if fused else 'decode'}")
 
     line = {
         "metric": METRIC,
@@ -388,22 +409,24 @@ def run_gpu(args, rank, local_rank, world):
         "config": {
             **workload_config(w, args), "context_growth_max": growth,
             "resident_bytes_per_call": resident_step // L, "effective_GBps": resident_step * K * world / elapsed / 1e9,
-            "launches_per_step": "append (all layers) + decode (all layers)",
+            "launches_per_step": "one fused append + decode (all layers)" if fused
+            else "append (all layers) + decode (all layers)",
             "cache_copies": copies, "l2_policy": "inputs larger than L2 (rotating cache copies)",
             "cuda_graph": True, "pdl": True, "parallelism": f"replicas x{world}",
             "decode_ctas": args.decode_ctas or "library default",
         },
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": traffic, "peak_source": peak_kind, "kernel": "decode_kernel",
-            "kernel_ms": kdur * 1e3, "alg_bytes_per_launch": alg_bytes, "timed_launches": reps * n_kg,
-            "kernel_timing": "graph of back-to-back decode launches over the rotating copies, events around it",
-            "kernel_ms_isolated": kdur_isolated * 1e3,
+            "traffic": traffic, "peak_source": peak_kind, "kernel": kernel_name,
+            "kernel_ms": kernel_s * 1e3, "alg_bytes_per_launch": alg_bytes,
+            "timed_launches": K if fused else reps * n_kg, "kernel_timing": kernel_timing,
+            "decode_only_kernel_ms": kdur * 1e3,
+            "decode_only_kernel_ms_isolated": kdur_isolated * 1e3,
         },
         "e2e": None if e2e_value is None else {
             "value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": e2e_steps},
-        "gpu_launches": 2 * K,
+        "gpu_launches": K if fused else 2 * K,
     }
     cs = clocks.summary()
     if cs is not None:
@@ -490,6 +513,8 @@ def main(argv=None):
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"])
     ap.add_argument("--decode-ctas", type=int, default=0, help="CTAs of a decode launch (0: the library's choice)")
+    ap.add_argument("--step", default="fused", choices=["fused", "split"],
+                    help="fused: lk_step_layers (one launch per step with a bf16 middle); split: append + decode")
     ap.add_argument("--e2e-steps", type=int, default=4000)
     ap.add_argument("--kernel-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=10.0)

@@ -73,6 +73,8 @@ SIGNATURES = {
     "lk_append_layers": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp]),
     "lk_decode_attn": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "lk_decode_attn_layers": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "lk_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "lk_step_layers": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lk_decode_attn_static": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp]),
     "lk_step_host": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lk_step_host_packed": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
@@ -376,6 +378,41 @@ class Cache:
         _need(o, torch.float32, (B, Hq, 128), "o")
         _check(_lib.lk_decode_attn(self._h, layer, q.data_ptr(), o.data_ptr(), self.workspace.data_ptr(),
                                    self.workspace.numel(), _stream(stream)))
+        return o
+
+    def step(self, layer, q, k, v, ids=None, o=None, stream=None):
+        """lk_step: append k, v (ids) to `layer`, then attend with q, in one
+        launch for a bf16 middle.  q [B, Hq, 128] bf16 -> o fp32."""
+        import torch
+        B, Hq, H = self.batch, self.plan.num_q_heads, self.plan.num_kv_heads
+        _need(q, torch.bfloat16, (B, Hq, 128), "q")
+        _need(k, torch.bfloat16, (B, H, 128), "k")
+        _need(v, torch.bfloat16, (B, H, 128), "v")
+        if ids is not None:
+            _need(ids, torch.int32, (B,), "ids")
+        if o is None:
+            o = torch.empty((B, Hq, 128), dtype=torch.float32, device=q.device)
+        _need(o, torch.float32, (B, Hq, 128), "o")
+        _check(_lib.lk_step(self._h, layer, q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(ids), o.data_ptr(),
+                            self.workspace.data_ptr(), self.workspace.numel(), _stream(stream)))
+        return o
+
+    def step_layers(self, layer0, q, k, v, ids=None, o=None, stream=None):
+        """lk_step_layers: q [nlayers, B, Hq, 128], k, v [nlayers, B, Hkv, 128]."""
+        import torch
+        nl = q.shape[0]
+        B, Hq, H = self.batch, self.plan.num_q_heads, self.plan.num_kv_heads
+        _need(q, torch.bfloat16, (nl, B, Hq, 128), "q")
+        _need(k, torch.bfloat16, (nl, B, H, 128), "k")
+        _need(v, torch.bfloat16, (nl, B, H, 128), "v")
+        if ids is not None:
+            _need(ids, torch.int32, (B,), "ids")
+        if o is None:
+            o = torch.empty((nl, B, Hq, 128), dtype=torch.float32, device=q.device)
+        _need(o, torch.float32, (nl, B, Hq, 128), "o")
+        _check(_lib.lk_step_layers(self._h, layer0, nl, q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(ids),
+                                   o.data_ptr(), self.workspace.data_ptr(), self.workspace.numel(),
+                                   _stream(stream)))
         return o
 
     def decode_static(self, layer, q, o, stream=None):

@@ -228,8 +228,8 @@ WsLayout ws_layout(const lk_plan_desc& d, int B) {
   const size_t G = (size_t)(d.num_q_heads / d.num_kv_heads);
   const size_t slots = (size_t)kMaxCtas + E;
   size_t off = 0;
-  w.off_counters = off;
-  off = align_up(off + E * 4, 256);
+  w.off_counters = off;                      // per entry, then one for the whole grid
+  off = align_up(off + (E + 1) * 4, 256);
   w.off_ml = off;
   off = align_up(off + slots * G * 8, 256);
   w.off_part = off;
@@ -762,62 +762,59 @@ lk_status lk_cache_pages(lk_cache cache, int32_t width, int64_t* total, int64_t*
   return LK_OK;
 }
 
-lk_status lk_append_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* k, const void* v,
-                           const int32_t* ids, void* stream) {
-  if (!cache) return fail(LK_ERR_ARG, "lk_append: null cache");
+}  // extern "C"
+
+namespace {
+
+// Host side of an append over layers [layer0, layer0 + nlayers): argument
+// and capacity checks, and the pages the appends will pop (taken from the
+// host count into need; the caller returns them if its launch fails).
+lk_status append_prepare(lk_cache cache, int32_t layer0, int32_t nlayers, const void* k, const void* v,
+                         const int32_t* ids, const char* what, int64_t need[kNumPools]) {
+  if (!cache) return fail(LK_ERR_ARG, "%s: null cache", what);
   if (nlayers < 1 || layer0 < 0 || layer0 + nlayers > cache->cv.L)
-    return fail(LK_ERR_ARG, "lk_append: layers [%d, %d) out of range", layer0, layer0 + nlayers);
-  if (!k || !v) return fail(LK_ERR_ARG, "lk_append: null k or v");
-  if (!aligned(k, 16) || !aligned(v, 16)) return fail(LK_ERR_ALIGN, "lk_append: k and v must be 16-byte aligned");
-  if (ids && !aligned(ids, 4)) return fail(LK_ERR_ALIGN, "lk_append: ids must be 4-byte aligned");
+    return fail(LK_ERR_ARG, "%s: layers [%d, %d) out of range", what, layer0, layer0 + nlayers);
+  if (!k || !v) return fail(LK_ERR_ARG, "%s: null k or v", what);
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(LK_ERR_ALIGN, "%s: k and v must be 16-byte aligned", what);
+  if (ids && !aligned(ids, 4)) return fail(LK_ERR_ALIGN, "%s: ids must be 4-byte aligned", what);
   const int B = cache->B;
-  int64_t need[kNumPools] = {0, 0, 0, 0, 0};
+  for (int pl = 0; pl < kNumPools; ++pl) need[pl] = 0;
   for (int l = layer0; l < layer0 + nlayers; ++l)
     for (int b = 0; b < B; ++b) {
       if (!cache->active[b]) continue;
       const int n = cache->host_len[(size_t)l * B + b];
       if (n >= cache->cap)
-        return fail(LK_ERR_CAPACITY, "lk_append: sequence %d of layer %d is full (%d tokens)", b, l, cache->cap);
+        return fail(LK_ERR_CAPACITY, "%s: sequence %d of layer %d is full (%d tokens)", what, b, l, cache->cap);
       cache->pages_needed(l, n, n + 1, need);
     }
-  lk_status st = cache->take_pages(need, "lk_append");
-  if (st != LK_OK) return st;
-  AppendArgs a;
-  a.cv = cache->cv;
-  a.layer = layer0;
-  a.nlayers = nlayers;
-  a.k = static_cast<const uint16_t*>(k);
-  a.v = static_cast<const uint16_t*>(v);
-  a.ids = ids;
-  cudaError_t err = launch_append(a, static_cast<cudaStream_t>(stream));
-  if (err != cudaSuccess) {
-    for (int pl = 0; pl < kNumPools; ++pl) cache->host_free[pl] += need[pl];
-    return cuda_fail(err, "lk_append launch");
-  }
+  return cache->take_pages(need, what);
+}
+
+void append_commit(lk_cache cache, int32_t layer0, int32_t nlayers) {
+  const int B = cache->B;
   for (int l = layer0; l < layer0 + nlayers; ++l)
     for (int b = 0; b < B; ++b)
       if (cache->active[b]) cache->host_len[(size_t)l * B + b] += 1;
-  return LK_OK;
 }
 
-lk_status lk_append(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
-                    void* stream) {
-  return lk_append_layers(cache, layer, 1, k, v, ids, stream);
+void return_pages(lk_cache cache, const int64_t need[kNumPools]) {
+  for (int pl = 0; pl < kNumPools; ++pl) cache->host_free[pl] += need[pl];
 }
 
-lk_status lk_decode_attn_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, float* o,
-                                void* workspace, size_t ws_bytes, void* stream) {
-  if (!cache) return fail(LK_ERR_ARG, "lk_decode_attn: null cache");
+// Host side of a decode launch: checks, and the kernel arguments (no fused
+// append) and CTA count.
+lk_status decode_prepare(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, float* o, void* workspace,
+                         size_t ws_bytes, const char* what, DecodeArgs& a, int& ctas) {
+  if (!cache) return fail(LK_ERR_ARG, "%s: null cache", what);
   if (nlayers < 1 || layer0 < 0 || layer0 + nlayers > cache->cv.L)
-    return fail(LK_ERR_ARG, "lk_decode_attn: layers [%d, %d) out of range", layer0, layer0 + nlayers);
-  if (!q || !o || !workspace) return fail(LK_ERR_ARG, "lk_decode_attn: null q, o or workspace");
-  if (!aligned(q, 16) || !aligned(o, 16)) return fail(LK_ERR_ALIGN, "lk_decode_attn: q and o must be 16-byte aligned");
-  if (!aligned(workspace, 256)) return fail(LK_ERR_ALIGN, "lk_decode_attn: workspace must be 256-byte aligned");
+    return fail(LK_ERR_ARG, "%s: layers [%d, %d) out of range", what, layer0, layer0 + nlayers);
+  if (!q || !o || !workspace) return fail(LK_ERR_ARG, "%s: null q, o or workspace", what);
+  if (!aligned(q, 16) || !aligned(o, 16)) return fail(LK_ERR_ALIGN, "%s: q and o must be 16-byte aligned", what);
+  if (!aligned(workspace, 256)) return fail(LK_ERR_ALIGN, "%s: workspace must be 256-byte aligned", what);
   const WsLayout w = ws_layout(cache->plan.d, cache->B);
-  if (ws_bytes < w.total)
-    return fail(LK_ERR_CAPACITY, "lk_decode_attn: workspace has %zu bytes; %zu needed", ws_bytes, w.total);
+  if (ws_bytes < w.total) return fail(LK_ERR_CAPACITY, "%s: workspace has %zu bytes; %zu needed", what, ws_bytes, w.total);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  DecodeArgs a;
+  a = DecodeArgs{};
   a.cv = cache->cv;
   a.layer = layer0;
   a.nlayers = nlayers;
@@ -828,8 +825,49 @@ lk_status lk_decode_attn_layers(lk_cache cache, int32_t layer0, int32_t nlayers,
   a.counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
   a.wait_limit_ns = kWaitLimitNs;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
-  int ctas = cache->decode_ctas > 0 ? cache->decode_ctas : default_decode_ctas(cache, nlayers);
+  a.k_new = a.v_new = nullptr;
+  a.ids = nullptr;
+  ctas = cache->decode_ctas > 0 ? cache->decode_ctas : default_decode_ctas(cache, nlayers);
   ctas = std::max(1, std::min(ctas, kMaxCtas));
+  return LK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lk_status lk_append_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* k, const void* v,
+                           const int32_t* ids, void* stream) {
+  int64_t need[kNumPools];
+  lk_status st = append_prepare(cache, layer0, nlayers, k, v, ids, "lk_append", need);
+  if (st != LK_OK) return st;
+  AppendArgs a;
+  a.cv = cache->cv;
+  a.layer = layer0;
+  a.nlayers = nlayers;
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.ids = ids;
+  cudaError_t err = launch_append(a, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) {
+    return_pages(cache, need);
+    return cuda_fail(err, "lk_append launch");
+  }
+  append_commit(cache, layer0, nlayers);
+  return LK_OK;
+}
+
+lk_status lk_append(lk_cache cache, int32_t layer, const void* k, const void* v, const int32_t* ids,
+                    void* stream) {
+  return lk_append_layers(cache, layer, 1, k, v, ids, stream);
+}
+
+lk_status lk_decode_attn_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, float* o,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  DecodeArgs a;
+  int ctas = 0;
+  lk_status st = decode_prepare(cache, layer0, nlayers, q, o, workspace, ws_bytes, "lk_decode_attn", a, ctas);
+  if (st != LK_OK) return st;
   cudaError_t err = launch_decode(cache->maps, a, ctas, static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn launch");
   return LK_OK;
@@ -840,16 +878,48 @@ lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
   return lk_decode_attn_layers(cache, layer, 1, q, o, workspace, ws_bytes, stream);
 }
 
+lk_status lk_step_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, const void* k,
+                         const void* v, const int32_t* ids, float* o, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  DecodeArgs a;
+  int ctas = 0;
+  lk_status st = decode_prepare(cache, layer0, nlayers, q, o, workspace, ws_bytes, "lk_step", a, ctas);
+  if (st != LK_OK) return st;
+  if (cache->cv.kv_format == kKvInt8) {
+    // an append may seal a block (the values decode reads change): two launches
+    st = lk_append_layers(cache, layer0, nlayers, k, v, ids, stream);
+    if (st != LK_OK) return st;
+    return lk_decode_attn_layers(cache, layer0, nlayers, q, o, workspace, ws_bytes, stream);
+  }
+  int64_t need[kNumPools];
+  st = append_prepare(cache, layer0, nlayers, k, v, ids, "lk_step", need);
+  if (st != LK_OK) return st;
+  a.k_new = static_cast<const uint16_t*>(k);
+  a.v_new = static_cast<const uint16_t*>(v);
+  a.ids = ids;
+  cudaError_t err = launch_decode(cache->maps, a, ctas, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) {
+    return_pages(cache, need);
+    return cuda_fail(err, "lk_step launch");
+  }
+  append_commit(cache, layer0, nlayers);
+  return LK_OK;
+}
+
+lk_status lk_step(lk_cache cache, int32_t layer, const void* q, const void* k, const void* v, const int32_t* ids,
+                  float* o, void* workspace, size_t ws_bytes, void* stream) {
+  return lk_step_layers(cache, layer, 1, q, k, v, ids, o, workspace, ws_bytes, stream);
+}
+
 // Append + decode from the inputs staged in the workspace, then copy o back.
 static lk_status step_from_staging(lk_cache cache, int32_t layer, bool has_ids, float* o_host, void* workspace,
                             size_t ws_bytes, void* stream) {
   const WsLayout w = ws_layout(cache->plan.d, cache->B);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  lk_status st = lk_append(cache, layer, ws + w.off_k, ws + w.off_v,
-                           has_ids ? reinterpret_cast<const int32_t*>(ws + w.off_ids) : nullptr, stream);
-  if (st != LK_OK) return st;
   float* o_dev = reinterpret_cast<float*>(ws + w.off_o);
-  st = lk_decode_attn(cache, layer, ws + w.off_q, o_dev, workspace, ws_bytes, stream);
+  lk_status st = lk_step(cache, layer, ws + w.off_q, ws + w.off_k, ws + w.off_v,
+                         has_ids ? reinterpret_cast<const int32_t*>(ws + w.off_ids) : nullptr, o_dev, workspace,
+                         ws_bytes, stream);
   if (st != LK_OK) return st;
   const size_t ob = (size_t)cache->B * cache->plan.d.num_q_heads * kHeadDim * 4;
   cudaError_t err = cudaMemcpyAsync(o_host, o_dev, ob, cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream));
@@ -1097,6 +1167,8 @@ lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, fl
   a.counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
   a.wait_limit_ns = kWaitLimitNs;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
+  a.k_new = a.v_new = nullptr;
+  a.ids = nullptr;
   int ctas = cache->decode_ctas > 0 ? cache->decode_ctas : default_decode_ctas(cache, 1);
   ctas = std::max(1, std::min(ctas, kMaxCtas));
   err = launch_decode(cache->maps, a, ctas, s);

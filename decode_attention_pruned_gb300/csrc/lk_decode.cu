@@ -30,10 +30,19 @@
 //   * Segment end: warps merge through shared memory; a CTA that owns the
 //     whole entry writes o, otherwise it writes (o, m, l) to its partial slot
 //     and the last of the entry's CTAs (atomic counter) merges them.
+//   * Fused append (lk_step, bf16 middle): the launch also appends one token
+//     per sequence, as an append kernel followed by this decode would.  The
+//     window slot the token replaces is left out of the scores; the CTA whose
+//     range holds that slot (else full-width row 0) loads the token, the row
+//     it evicts and the kept-channel list as one more stage, folds the token
+//     (all channels) and the evicted row (kept channels) into its softmax,
+//     and writes both into the cache after it has read the slot.  The last
+//     CTA to finish advances the lengths, which every CTA read in its split.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include "lk_append.cuh"
 #include "lk_device.cuh"
 #include "lk_internal.h"
 #include "lk_kernels.h"
@@ -67,7 +76,14 @@ struct StageDesc {
   int32_t first_cta;   // CTAs first..last hold partials of the entry
   int32_t last_cta;
   uint32_t koff;       // ring offset of the K tile; the V tile follows it
+  int32_t mrow;        // tile row left out (fused append: the window slot being replaced), or -1
+  int32_t n, cnt;      // region 3: the entry's length and special count before the append
 };
+// region-3 descriptors: mrow holds these flags, width the kept channels of
+// the evicted window row (0: none)
+constexpr int kTokAlways = 1;        // FULL / LOCAL head: the token always enters
+constexpr int kTokSpecialHead = 2;   // SPECIAL head: the token enters if its id is special ...
+constexpr int kTokRoom = 4;          // ... and the head has a free row
 
 struct SmemLayout {
   static constexpr int kRingOff = 0;
@@ -81,13 +97,20 @@ struct SmemLayout {
   static constexpr int kCBarOff = kBarOff + 2 * kSlots * 8;                  // consumer barrier
   static constexpr int kScanOff = kCBarOff + 8;
   static constexpr int kMiscOff = kScanOff + (kThreads / 32) * 8;
-  static constexpr int kBytes = kMiscOff + 64;
+  static constexpr int kBytes = kMiscOff + 96;
 };
 constexpr int kSmemBytes = SmemLayout::kBytes + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
 
+// Region 3 (fused append): the new token's K, V rows, then -- when it evicts
+// a window row into the middle -- that row's K, V and the kept-channel list.
+constexpr uint32_t kTokenBytes = 2 * kHeadDim * 2;
+constexpr uint32_t kTokenEvictBytes = 2 * kTokenBytes + kHeadDim * 2;
+
 __device__ __forceinline__ uint32_t stage_bytes(int region, int width) {
-  return region == 2 ? (uint32_t)qblock_bytes(width) : (uint32_t)kTileRows * (2 * width + 256);
+  return region == 3   ? (width != 0 ? kTokenEvictBytes : kTokenBytes)
+         : region == 2 ? (uint32_t)qblock_bytes(width)
+                       : (uint32_t)kTileRows * (2 * width + 256);
 }
 // ring footprint of a stage: 1024-byte granules (swizzled TMA boxes need
 // 1024-byte aligned destinations)
@@ -95,10 +118,22 @@ __device__ __forceinline__ uint32_t ring_bytes(int region, int width) {
   return (stage_bytes(region, width) + 1023u) & ~1023u;
 }
 
+// Lengths and special counts are read through L2 (they are written by the
+// preceding append kernel).  The loads are split from the arithmetic so the
+// producer can issue the next entry's loads one entry ahead.
+struct EntryLen {
+  int n;      // tokens of the sequence in this layer
+  int cnt;    // special rows (SPECIAL heads), else 0
+  int act;    // fused launches: the sequence takes the appended token
+};
+
 // Rows of an entry in line order: n_a full width, n_q in sealed INT8 blocks,
-// n_b bf16 kept-channel rows (INT8 caches: the open tail block).
+// n_b bf16 kept-channel rows (INT8 caches: the open tail block).  mrow: the
+// full-width row a fused append replaces (left out of the scores), or -1;
+// len: what the geometry was computed from.
 struct Entry {
-  int n_a, n_q, n_b, kb;
+  int n_a, n_q, n_b, kb, mrow;
+  EntryLen len;
 };
 
 // Entry e of a launch = (layer offset lr, sequence b, kv head h), layers
@@ -118,13 +153,6 @@ __device__ __forceinline__ EntryId entry_id(const DecodeArgs& a, int e) {
   return r;
 }
 
-// Lengths and special counts are read through L2 (they are written by the
-// preceding append kernel).  The loads are split from the arithmetic so the
-// producer can issue the next entry's loads one entry ahead.
-struct EntryLen {
-  int n;      // tokens of the sequence in this layer
-  int cnt;    // special rows (SPECIAL heads), else 0
-};
 __device__ __forceinline__ EntryLen entry_len(const DecodeArgs& a, int e) {
   const CacheView& cv = a.cv;
   const EntryId id = entry_id(a, e);
@@ -132,7 +160,16 @@ __device__ __forceinline__ EntryLen entry_len(const DecodeArgs& a, int e) {
   EntryLen r;
   r.n = __ldcg(&cv.len[id.l * cv.B + id.b]);
   r.cnt = hd.policy == kSpecial ? __ldcg(&cv.cnt[id.l * cv.B + id.b]) : 0;
+  r.act = a.k_new != nullptr && __ldcg(&cv.active[id.b]) != 0 && r.n < cv.capacity;
   return r;
+}
+
+// Whether the token a fused launch appends for sequence b is special (its
+// id in [0, vocab) and flagged).
+__device__ __forceinline__ bool token_special(const DecodeArgs& a, int b) {
+  if (a.ids == nullptr) return false;
+  const int id = a.ids[b];
+  return id >= 0 && id < a.cv.vocab && a.cv.is_special[id] != 0;
 }
 
 __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen len) {
@@ -140,9 +177,11 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
   const EntryId id = entry_id(a, e);
   const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
   const int N = len.n;
-  Entry r{0, 0, 0, 0};
+  Entry r{0, 0, 0, 0, -1, len};
   if (hd.policy == kFull) {
     r.n_a = min(N, cv.S + cv.W);
+    // a fused append into a full window replaces the slot of token N - W
+    if (len.act && N >= cv.S + cv.W) r.mrow = cv.S + (N - cv.S) % cv.W;
     if (hd.n_kept > 0) {
       const int m = max(0, N - cv.S - cv.W);
       if (cv.kv_format == kKvInt8) {
@@ -156,6 +195,7 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
     }
   } else if (hd.policy == kLocal) {
     r.n_a = min(N, cv.W_loc);
+    if (len.act && N >= cv.W_loc) r.mrow = N % cv.W_loc;
   } else {
     r.n_a = min(len.cnt, hd.cap_a);
   }
@@ -262,6 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[1] = 0;       // its line offset
     misc[2] = 0;       // last-CTA flag of a segment
     misc[3] = misc[4] = misc[5] = misc[6] = 0;   // geometry of the first entry
+    misc[7] = -1;
+    misc[8] = misc[9] = misc[10] = 0;
   }
   if (warp == kConsumerWarps && lane == 0) {
     tma_prefetch_map(&tm_k128);
@@ -308,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
   // the first two entries of the chunk keep their geometry for the second
   // pass (a whole single-layer launch fits that)
-  Entry g0{0, 0, 0, 0}, g1{0, 0, 0, 0};
+  Entry g0{0, 0, 0, 0, -1, {0, 0, 0}}, g1{0, 0, 0, 0, -1, {0, 0, 0}};
   if (e_lo < e_hi) g0 = entry_geometry(a, e_lo);
   if (e_lo + 1 < e_hi) g1 = entry_geometry(a, e_lo + 1);
   uint64_t local = entry_cost(g0) + entry_cost(g1);
@@ -337,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // geometry go to the producer through shared memory
     uint64_t acc = excl;
     int found = -1;
-    Entry fg{0, 0, 0, 0};
+    Entry fg{0, 0, 0, 0, -1, {0, 0, 0}};
     for (int e = e_lo; found < 0 && e < e_hi; ++e) {
       const Entry g = e == e_lo ? g0 : e == e_lo + 1 ? g1 : entry_geometry(a, e);
       const uint64_t c = entry_cost(g);
@@ -354,6 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[4] = fg.n_b;
     misc[5] = fg.kb;
     misc[6] = fg.n_q;
+    misc[7] = fg.mrow;
+    misc[8] = fg.len.n;
+    misc[9] = fg.len.cnt;
+    misc[10] = fg.len.act;
   }
   __syncthreads();
 
@@ -411,13 +457,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         head = at + bytes;
         return true;
       };
+      const bool fused_launch = !kQ8 && a.k_new != nullptr;
       const int e0 = (int)misc[0];
       int e = e0;
       uint64_t off = (uint64_t)misc[1];
       // entry geometry: the first from the scan, later ones from lengths
       // loaded one entry ahead
-      Entry g{(int)misc[3], (int)misc[6], (int)misc[4], (int)misc[5]};
-      EntryLen ahead{0, 0};
+      Entry g{(int)misc[3], (int)misc[6], (int)misc[4], (int)misc[5], (int)misc[7],
+              {(int)misc[8], (int)misc[9], (int)misc[10]}};
+      EntryLen ahead{0, 0, 0};
       if (e + 1 < E) ahead = entry_len(a, e + 1);
       for (; ok && e < E && off < end; ++e) {
         if (e != e0) {
@@ -459,6 +507,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             fc = range_owner(off, C, P);
             lc = range_owner(last_row_off, C, P);
           }
+          // Fused append: the CTA holding the entry's anchor row -- the window
+          // slot the new token replaces, else full-width row 0 -- loads the
+          // token (and the row it evicts into the middle) as a region-3 stage
+          // right after that row's tile, so the slot is overwritten only
+          // after this CTA has read it; no other CTA reads it.
+          const int anc = g.mrow >= 0 ? g.mrow : 0;
+          const int xj = fused_launch && g.len.act && g.n_a > 0 && anc >= a0 && anc < a1 ? (anc - a0) / kTileRows
+                                                                                         : -1;
           int32_t page_ahead = 0;
           for (int j = 0; j < nt; ++j) {
             const int region = j < nta ? 0 : j < nta + ntq ? 2 : 1;
@@ -506,10 +562,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             d.rlo = rlo;
             d.nrows = rend - r;
             d.width = width;
-            d.flags = (j == 0 ? kFirst : 0) | (j + 1 == nt ? kLast : 0);
+            d.flags = (j == 0 ? kFirst : 0) | (j + 1 == nt && j != xj ? kLast : 0);
             d.first_cta = fc;
             d.last_cta = lc;
             d.koff = at;
+            d.mrow = region == 0 && g.mrow >= r && g.mrow < rend ? g.mrow - r : -1;
+            d.n = d.cnt = 0;
             desc[stage] = d;
             const uint32_t fb = bar_full + 8 * stage;
             mbar_arrive_expect_tx(fb, bytes);
@@ -537,6 +595,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (fc < 0) {
               fc = range_owner(off, C, P);
               lc = range_owner(last_row_off, C, P);
+            }
+            if (j == xj) {
+              const bool evict = hd.policy == kFull && g.kb > 0 && g.mrow >= 0;
+              const uint32_t xbytes = stage_bytes(3, evict ? g.kb : 0);
+              if (!reserve(ring_bytes(3, evict ? g.kb : 0), at)) {
+                ok = false;
+                break;
+              }
+              const uint32_t xs = issued & (kSlots - 1);
+              StageDesc x;
+              x.e = e;
+              x.region = 3;
+              x.rlo = x.nrows = 0;
+              x.width = evict ? g.kb : 0;
+              x.flags = j + 1 == nt ? kLast : 0;
+              x.first_cta = fc;
+              x.last_cta = lc;
+              x.koff = at;
+              x.mrow = hd.policy != kSpecial ? kTokAlways
+                                             : kTokSpecialHead | (g.len.cnt < hd.cap_a ? kTokRoom : 0);
+              x.n = g.len.n;
+              x.cnt = g.len.cnt;
+              desc[xs] = x;
+              const uint32_t xb = bar_full + 8 * xs;
+              mbar_arrive_expect_tx(xb, xbytes);
+              const uint32_t dst = base + SmemLayout::kRingOff + at;
+              const size_t src = (((size_t)id.lr * cv.B + b) * cv.Hkv + id.h) * kHeadDim;
+              bulk_load(dst, a.k_new + src, kHeadDim * 2, xb, policy);
+              bulk_load(dst + kHeadDim * 2, a.v_new + src, kHeadDim * 2, xb, policy);
+              if (evict) {
+                const int64_t srow = hd.row_a + (int64_t)b * hd.cap_a + g.mrow;
+                bulk_load(dst + 2 * kHeadDim * 2, cv.pool[kPoolK128] + srow * kHeadDim, kHeadDim * 2, xb, policy);
+                bulk_load(dst + 3 * kHeadDim * 2, cv.pool[kPoolV] + srow * kHeadDim, kHeadDim * 2, xb, policy);
+                bulk_load(dst + 4 * kHeadDim * 2, cv.kept + ((size_t)id.l * cv.Hkv + id.h) * kHeadDim, kHeadDim * 2,
+                          xb, policy);
+              }
+              ++issued;
             }
           }
         }
@@ -581,12 +676,102 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t qa_lane = base + SmemLayout::kQOff + (uint32_t)((lane & 7) * kQStride + 8 * (lane >> 3)) * 2;
   const uint32_t qb_lane = base + SmemLayout::kQKOff + (uint32_t)((lane & 7) * kQStride + 8 * (lane >> 3)) * 2;
 
-  // entries with no resident token: o = 0, written by CTA (e mod grid)
+  // ---- fused append (bf16 caches, a.k_new set).  Entries with resident rows
+  // take the token through a region-3 stage (below); entries without any
+  // take it here, through global memory.  The last CTA of the grid advances
+  // the lengths.  Scratch `ex` lives in the q staging area, free before the
+  // first entry's q is staged.
+  const bool fused = !kQ8 && a.k_new != nullptr;
+  float* ex = reinterpret_cast<float*>(sm + SmemLayout::kQOff);
+  constexpr int kExS = 0, kExE = kMaxGroup, kExVn = 2 * kMaxGroup, kExVe = kExVn + kHeadDim;
+  static_assert(kExVe + kHeadDim <= kMaxGroup * kQStride / 2, "fused scratch fits the q area");
+  // The tokens the append adds to entry e: the new token (all channels;
+  // SPECIAL heads take it only if its id is special) and, when a FULL window
+  // with kept channels is full, the token n - W leaving it for the middle
+  // (kept channels, read from its window row before the edit replaces it).
+  // Scores in log2 units (-inf: absent) and V rows as fp32 into ex.  All
+  // consumer threads; callers sync before reading ex.
+  auto fused_extras = [&](int e) {
+    const EntryId id = entry_id(a, e);
+    const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+    const EntryLen len = entry_len(a, e);
+    const bool add_new = len.act && (hd.policy != kSpecial || (token_special(a, id.b) && len.cnt < hd.cap_a));
+    const bool add_ev = len.act && hd.policy == kFull && hd.n_kept > 0 && len.n >= cv.S + cv.W;
+    const int64_t slot = hd.row_a + (int64_t)id.b * hd.cap_a + (add_ev ? cv.S + (len.n - cv.S) % cv.W : 0);
+    const size_t src = (((size_t)id.lr * cv.B + id.b) * cv.Hkv + id.h) * kHeadDim;
+    if (warp < G) {
+      const uint16_t* qg = a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G + warp) * kHeadDim;
+      float sn = 0.f, se = 0.f;
+      if (add_new) {
+        const uint2 qw = reinterpret_cast<const uint2*>(qg)[lane];
+        const uint2 kw = reinterpret_cast<const uint2*>(a.k_new + src)[lane];
+        sn = bf16_lo(qw.x) * bf16_lo(kw.x) + bf16_hi(qw.x) * bf16_hi(kw.x) + bf16_lo(qw.y) * bf16_lo(kw.y) +
+             bf16_hi(qw.y) * bf16_hi(kw.y);
+      }
+      if (add_ev) {
+        const int16_t* kept = cv.kept + ((size_t)id.l * cv.Hkv + id.h) * kHeadDim;
+        const uint16_t* k_old = cv.pool[kPoolK128] + slot * kHeadDim;
+        for (int c = lane; c < hd.n_kept; c += 32) {
+          const int ch = kept[c];
+          se += bf16_to_f32(qg[ch]) * bf16_to_f32(k_old[ch]);
+        }
+      }
+#pragma unroll
+      for (int sh = 16; sh > 0; sh >>= 1) {
+        sn += __shfl_xor_sync(0xffffffffu, sn, sh);
+        se += __shfl_xor_sync(0xffffffffu, se, sh);
+      }
+      if (lane == 0) {
+        ex[kExS + warp] = add_new ? sn * a.scale_log2 : NEG_INF;
+        ex[kExE + warp] = add_ev ? se * a.scale_log2 : NEG_INF;
+      }
+    }
+    if (ct < 64) {
+      const int c4 = ct & 31;
+      const bool on = ct < 32 ? add_new : add_ev;
+      const uint2 w = !on ? make_uint2(0u, 0u)
+                      : ct < 32 ? reinterpret_cast<const uint2*>(a.v_new + src)[c4]
+                                : row8(cv.pool[kPoolV], slot)[c4];
+      *reinterpret_cast<float4*>(&ex[(ct < 32 ? kExVn : kExVe) + 4 * c4]) =
+          make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+    }
+  };
+  // The cache edit of entry e (one warp): the append of the token, after
+  // fused_extras and a consumer barrier.
+  auto fused_edit = [&](int e) {
+    const EntryId id = entry_id(a, e);
+    const EntryLen len = entry_len(a, e);
+    if (!len.act) return;
+    const size_t src = (((size_t)id.lr * cv.B + id.b) * cv.Hkv + id.h) * kHeadDim;
+    append_head<false>(cv, id.l, id.b, id.h, len.n, len.cnt, token_special(a, id.b), a.k_new + src,
+                       a.v_new + src, lane);
+  };
+
+  // entries with no resident token, by CTA (e mod grid): o = 0, or with a
+  // fused append the new token alone
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
     if (entry_cost(entry_geometry(a, e)) != 0) continue;
     const EntryId id = entry_id(a, e);
     float* dst = a.o + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
-    for (int i = ct; i < G * kHeadDim; i += kConsumerWarps * 32) dst[i] = 0.f;
+    if (fused) {
+      fused_extras(e);
+      consumer_sync(cbar, cphase, a);
+      for (int i = ct; i < G * kHeadDim; i += kConsumerWarps * 32) {
+        const int g = i >> 7, c = i & (kHeadDim - 1);
+        const float sn = ex[kExS + g], se = ex[kExE + g];
+        const float M = fmaxf(sn, se);
+        float out = 0.f;
+        if (M != NEG_INF) {
+          const float fn = sn == NEG_INF ? 0.f : exp2f(sn - M), fe = se == NEG_INF ? 0.f : exp2f(se - M);
+          out = (fn * ex[kExVn + c] + fe * ex[kExVe + c]) / (fn + fe);
+        }
+        dst[i] = out;
+      }
+      if (warp == kConsumerWarps - 1) fused_edit(e);
+      consumer_sync(cbar, cphase, a);
+    } else {
+      for (int i = ct; i < G * kHeadDim; i += kConsumerWarps * 32) dst[i] = 0.f;
+    }
   }
 
   float o[8][4];
@@ -657,10 +842,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // valid rows rlo .. rhi - 1 of the tile (sealed blocks may be shared with
-    // another CTA)
+    // another CTA) except mrow; the warp works if one of its 16 rows is valid
+    // (a block of masked rows would leave the running max at -inf)
     const int rlo = d.rlo, rhi = d.rlo + d.nrows;
     const uint32_t kbase = base + SmemLayout::kRingOff + d.koff;
-    if (r0 < rhi && r0 + 16 > rlo) {
+    const int wlo = max(r0, rlo), whi = min(r0 + 16, rhi);
+    if (whi - wlo - (d.mrow >= wlo && d.mrow < whi ? 1 : 0) > 0) {
       // two independent accumulators halve the mma dependency chain
       float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
       if (kQ8 && d.region == 2) {
@@ -728,7 +915,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) sc[i] += sd[i];
       const int t0 = r0 + gid;
-      const bool v0 = t0 >= rlo && t0 < rhi, v1 = t0 + 8 >= rlo && t0 + 8 < rhi;
+      const bool v0 = t0 >= rlo && t0 < rhi && t0 != d.mrow;
+      const bool v1 = t0 + 8 >= rlo && t0 + 8 < rhi && t0 + 8 != d.mrow;
       const float x0 = v0 ? sc[0] * a.scale_log2 : NEG_INF;
       const float x1 = v0 ? sc[1] * a.scale_log2 : NEG_INF;
       const float x2 = v1 ? sc[2] * a.scale_log2 : NEG_INF;
@@ -816,6 +1004,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (!kQ8 && d.region == 3) {
+      // ---- fused append: the new token (and the window row it evicts into
+      // the middle, scored on the kept channels) join warp 0's running
+      // softmax of this segment; the last warp writes them into the cache
+      // from the staged copies.  The descriptor carries what decides this
+      // (mrow: kTok* flags; width: kept channels of an
+      // evicted row, else 0), so warp 0 reads nothing but shared memory
+      // unless the head is SPECIAL.
+      const uint16_t* kn = reinterpret_cast<const uint16_t*>(sm + SmemLayout::kRingOff + d.koff);
+      const uint16_t* vn = kn + kHeadDim;
+      const uint16_t* ko = kn + 2 * kHeadDim;
+      const uint16_t* vo = kn + 3 * kHeadDim;
+      const int16_t* kl = reinterpret_cast<const int16_t*>(kn + 4 * kHeadDim);
+      const EntryId id = entry_id(a, d.e);
+      const bool special = (d.mrow & kTokSpecialHead) != 0 && token_special(a, id.b);
+      const bool add_new = (d.mrow & kTokAlways) != 0 || (special && (d.mrow & kTokRoom) != 0);
+      const int kk = d.width;
+      const bool add_ev = kk != 0;
+      if (warp == 0 && (add_new || add_ev)) {
+        // the evicted row's kept channels as a 128-bit mask
+        uint32_t km[4] = {0u, 0u, 0u, 0u};
+        if (add_ev) {
+          for (int c = lane; c < kk; c += 32) {
+            const int ch = kl[c];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) km[w] |= (ch >> 5) == w ? 1u << (ch & 31) : 0u;
+          }
+#pragma unroll
+          for (int w = 0; w < 4; ++w) km[w] = __reduce_or_sync(0xffffffffu, km[w]);
+        }
+        // lane = 4 g + part: head g on channels 32 part .. 32 part + 31
+        const int gq = lane >> 2, part = lane & 3;
+        const uint32_t kmask = part == 0 ? km[0] : part == 1 ? km[1] : part == 2 ? km[2] : km[3];
+        const uint16_t* qr = qa_s + gq * kQStride + 32 * part;
+        float sn = 0.f, se = 0.f;
+#pragma unroll 1
+        for (int j = 0; j < 32; j += 8) {
+          const uint4 qv = *reinterpret_cast<const uint4*>(qr + j);
+          const uint4 nv = *reinterpret_cast<const uint4*>(kn + 32 * part + j);
+          const uint4 ov = *reinterpret_cast<const uint4*>(ko + 32 * part + j);
+          const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, nw[4] = {nv.x, nv.y, nv.z, nv.w};
+          const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const float q0 = bf16_lo(qw[t]), q1 = bf16_hi(qw[t]);
+            sn += q0 * bf16_lo(nw[t]) + q1 * bf16_hi(nw[t]);
+            const uint32_t bits = kmask >> (j + 2 * t);
+            se += ((bits & 1u) ? q0 * bf16_lo(ow[t]) : 0.f) + ((bits & 2u) ? q1 * bf16_hi(ow[t]) : 0.f);
+          }
+        }
+        sn += __shfl_xor_sync(0xffffffffu, sn, 1);
+        se += __shfl_xor_sync(0xffffffffu, se, 1);
+        sn += __shfl_xor_sync(0xffffffffu, sn, 2);
+        se += __shfl_xor_sync(0xffffffffu, se, 2);
+        // this lane's head columns 2 tig, 2 tig + 1 sit in lanes 8 tig, 8 tig + 4
+        float xn0 = __shfl_sync(0xffffffffu, sn, 8 * tig), xn1 = __shfl_sync(0xffffffffu, sn, 8 * tig + 4);
+        float xe0 = __shfl_sync(0xffffffffu, se, 8 * tig), xe1 = __shfl_sync(0xffffffffu, se, 8 * tig + 4);
+        xn0 = add_new ? xn0 * a.scale_log2 : NEG_INF;
+        xn1 = add_new ? xn1 * a.scale_log2 : NEG_INF;
+        xe0 = add_ev ? xe0 * a.scale_log2 : NEG_INF;
+        xe1 = add_ev ? xe1 * a.scale_log2 : NEG_INF;
+        const float mn0 = fmaxf(m0, fmaxf(xn0, xe0)), mn1 = fmaxf(m1, fmaxf(xn1, xe1));
+        const float al0 = mn0 > m0 ? (m0 == NEG_INF ? 0.f : exp2f(m0 - mn0)) : 1.f;
+        const float al1 = mn1 > m1 ? (m1 == NEG_INF ? 0.f : exp2f(m1 - mn1)) : 1.f;
+        m0 = mn0;
+        m1 = mn1;
+        const float pn0 = xn0 == NEG_INF ? 0.f : exp2f(xn0 - m0), pe0 = xe0 == NEG_INF ? 0.f : exp2f(xe0 - m0);
+        const float pn1 = xn1 == NEG_INF ? 0.f : exp2f(xn1 - m1), pe1 = xe1 == NEG_INF ? 0.f : exp2f(xe1 - m1);
+        // l is summed over the gid lanes at the segment end: count p once
+        l0 = l0 * al0 + (gid == 0 ? pn0 + pe0 : 0.f);
+        l1 = l1 * al1 + (gid == 0 ? pn1 + pe1 : 0.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float vna = bf16_to_f32(vn[16 * i + gid]), vnb = bf16_to_f32(vn[16 * i + gid + 8]);
+          const float voa = add_ev ? bf16_to_f32(vo[16 * i + gid]) : 0.f;
+          const float vob = add_ev ? bf16_to_f32(vo[16 * i + gid + 8]) : 0.f;
+          o[i][0] = o[i][0] * al0 + pn0 * vna + pe0 * voa;
+          o[i][1] = o[i][1] * al1 + pn1 * vna + pe1 * voa;
+          o[i][2] = o[i][2] * al0 + pn0 * vnb + pe0 * vob;
+          o[i][3] = o[i][3] * al1 + pn1 * vnb + pe1 * vob;
+        }
+      }
+      if (warp == kConsumerWarps - 1)
+        append_head<false>(cv, id.l, id.b, id.h, d.n, d.cnt, special, kn, vn, lane, add_ev ? ko : nullptr,
+                           add_ev ? vo : nullptr, add_ev ? kl : nullptr);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
 
@@ -902,10 +1176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       l0 = l1 = c0 = c1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      const bool single = d.first_cta == d.last_cta;
       consumer_sync(cbar, cphase, a);
       const EntryId id = entry_id(a, d.e);
       float* dst = a.o + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
-      const bool single = d.first_cta == d.last_cta;
       const size_t slot = (size_t)blockIdx.x + d.e;
       // CTA-level merge, 4 channels per thread
       for (int q4 = ct; q4 < G * 32; q4 += kConsumerWarps * 32) {
@@ -1015,6 +1289,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (++stage == kSlots) {
       stage = 0;
       phase ^= 1u;
+    }
+  }
+
+  if (fused) {
+    // Lengths move only when every CTA is done (each read them in its work
+    // split): the last CTA to finish advances them, as the append kernel
+    // does per sequence.  Every CTA loads the new values of its threads'
+    // first (layer, sequence) before the count, which nothing can change
+    // before the last CTA stores them.
+    const int nlb = a.nlayers * cv.B;
+    auto next_len = [&](int i, int& lb, int& n1, int& c1) {
+      const int b = i % cv.B;
+      lb = (a.layer + i / cv.B) * cv.B + b;
+      // independent loads first: one round trip (two with token ids)
+      const int act = __ldcg(&cv.active[b]);
+      const int n = __ldcg(&cv.len[lb]);
+      const int c = __ldcg(&cv.cnt[lb]);
+      const bool sp = token_special(a, b);
+      n1 = act != 0 && n < cv.capacity ? n + 1 : -1;
+      c1 = n1 > 0 && sp && c < cv.spec_cap ? c + 1 : -1;
+    };
+    // (Every length this CTA reads was read before its consumers left the
+    // loop: the producer's last loads precede its final arrive.  The count
+    // orders nothing else -- the cache writes are for the next kernel.)
+    int lb0 = 0, n0 = -1, cn0 = -1;
+    if (ct < nlb) next_len(ct, lb0, n0, cn0);
+    if (ct == 0) misc[2] = atomicAdd(&a.counters[E], 1) == (int)gridDim.x - 1 ? 1 : 0;
+    consumer_sync(cbar, cphase, a);
+    if (misc[2]) {
+      for (int i = ct; i < nlb; i += kConsumerWarps * 32) {
+        int lb = lb0, n1 = n0, c1 = cn0;
+        if (i != ct) next_len(i, lb, n1, c1);
+        if (n1 > 0) cv.len[lb] = n1;
+        if (c1 > 0) cv.cnt[lb] = c1;
+        const int b = i % cv.B;
+        if (a.ids != nullptr && __ldcg(&cv.active[b]) != 0 && (a.ids[b] < 0 || a.ids[b] >= cv.vocab))
+          set_status(cv, kStatusBadId);
+      }
+      if (ct == 0) a.counters[E] = 0;
     }
   }
 }

@@ -15,9 +15,16 @@ struct DecodeArgs {
   float* o;                 // fp32 [nlayers][B][Hq][128]
   float* part;              // fp32 [slots][G][128] split partials (unnormalised o)
   float2* part_ml;          // [slots][G] (running max in log2 units, sum of p)
-  int32_t* counters;        // [nlayers*B*Hkv] CTAs done per entry; self-resetting
+  int32_t* counters;        // [nlayers*B*Hkv] CTAs done per entry, then CTAs done in all;
+                            // self-resetting
   uint64_t wait_limit_ns;   // bound of every mbarrier wait
   float scale_log2;         // log2(e) / sqrt(128)
+  // Fused append (bf16 caches): null for a plain decode.  Otherwise the
+  // launch appends one token per active sequence and layer and attends to
+  // it, as an append followed by a decode would.
+  const uint16_t* k_new;    // bf16 [nlayers][B][Hkv][128]
+  const uint16_t* v_new;
+  const int32_t* ids;       // [B] or null
 };
 
 struct AppendArgs {

@@ -314,9 +314,31 @@ lk_status lk_append_layers(lk_cache cache, int32_t layer0, int32_t nlayers, cons
 lk_status lk_decode_attn_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, float* o,
                                 void* workspace, size_t ws_bytes, void* stream);
 
+/* One decode step of a layer: the append of the new token followed by
+ * attention with the new query (FastGen 2.1: append K_t, V_t, then attend
+ * with Q_t), in one launch.  Same arguments, results and errors as
+ *   lk_append(cache, layer, k, v, ids, stream);
+ *   lk_decode_attn(cache, layer, q, o, workspace, ws_bytes, stream);
+ * and the cache is left as they leave it (byte for byte, except that a
+ * paged cache may hand out its free pages in another order).  With a bf16
+ * middle one kernel does both: the CTA that combines a head's split
+ * partials adds the new token (and the token leaving a full window for the
+ * middle) to the softmax from the inputs, then writes them into the cache;
+ * the window slot being replaced is left out of the scores.  INT8 caches
+ * (where an append may seal a block, changing the values decode reads) run
+ * the two launches.  Nothing is launched on an error. */
+lk_status lk_step(lk_cache cache, int32_t layer, const void* q, const void* k, const void* v,
+                  const int32_t* ids, float* o, void* workspace, size_t ws_bytes, void* stream);
+
+/* lk_step over layers layer0 .. layer0+nlayers-1 in one launch: q, o as for
+ * lk_decode_attn_layers, k, v, ids as for lk_append_layers. */
+lk_status lk_step_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, const void* k,
+                         const void* v, const int32_t* ids, float* o, void* workspace, size_t ws_bytes,
+                         void* stream);
+
 /* One decode step end to end from host memory: copies q [B][Hq][128] bf16,
  * k, v [B][Hkv][128] bf16 and ids [B] int32 (NULL allowed) from host to the
- * workspace, runs lk_append then lk_decode_attn, and copies o [B][Hq][128]
+ * workspace, runs lk_step, and copies o [B][Hq][128]
  * fp32 back to host.  Host buffers should be pinned for the copies to be
  * asynchronous; read o only after synchronising `stream`. */
 lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const void* k_host,

@@ -174,14 +174,17 @@ def test_step_host_matches_device_path(cuda):
     b.prefill(0, 600)
     k, v = a.history(0)
     q = a.q(0, 601)
-    a.append(0, 600)
-    o_dev = a.cache.decode(0, q)
+    # the host entry point runs lk_step on the staged copies: the same launch
+    # as the device call on the same values
+    o_dev = a.cache.step(0, q, k[:, 600].contiguous(), v[:, 600].contiguous())
     pin = lambda t: t.cpu().pin_memory()
     o_host = torch.empty(o_dev.shape, dtype=torch.float32).pin_memory()
     b.cache.step_host(0, pin(q), pin(k[:, 600].contiguous()), pin(v[:, 600].contiguous()), None, o_host)
     torch.cuda.synchronize()
     b.cache.check()
     assert torch.equal(o_host, o_dev.cpu())
+    assert float(np.abs(o_host.double().numpy() - a.expected(0, q, 601)).max()) <= DECODE_TOL
+    assert torch.equal(a.cache.buffer, b.cache.buffer)
 
 
 def test_capacity_is_enforced(cuda):

@@ -1,0 +1,233 @@
+"""The fused decode step (lk_step): the append of token t and attention with
+the query of step t in one launch, against the fp64 oracle over tokens
+0..t and against the split path (lk_append, then lk_decode_attn).
+
+The order is the method's: the new K, V enter the cache, then the query
+attends to everything resident (FastGen article, mhpn.cn, section 2.1; the
+LeanK article, framerc.cn, section 3.1 for the split cache the token goes
+into).  The fused launch scores the new token from its inputs, leaves out
+the window slot it replaces, scores the token that slot sends to the middle
+on the kept channels, and only then writes the cache; so its output must
+match the oracle, and the cache it leaves must equal the split path's byte
+for byte (contiguous caches) or row for row through the page table (paged
+caches, whose free pages may be handed out in another order)."""
+import numpy as np
+import pytest
+import torch
+
+from decode_attention_pruned_gb300 import binding as lkb
+from decode_attention_pruned_gb300 import synth as S
+from helpers import DECODE_TOL, Case
+
+pytestmark = pytest.mark.gpu
+
+TINY = S.WORKLOADS[0]
+LLAMA = S.WORKLOADS[1]
+SERVING = S.WORKLOADS[2]
+FASTGEN = S.WORKLOADS[4]
+
+
+def _max_err(o, ref):
+    return float(np.abs(o.double().cpu().numpy() - ref).max())
+
+
+def _token(case, layer, pos):
+    """k, v [B, Hkv, 128] and ids [B] of the token at position pos[b] of each
+    sequence (pos an int or one position per sequence)."""
+    k, v = case.history(layer)
+    B = case.w.batch
+    p = torch.as_tensor(np.broadcast_to(np.asarray(pos, dtype=np.int64), (B,)).copy(), device=k.device)
+    bi = torch.arange(B, device=k.device)
+    ids = case.ids[bi, p].contiguous() if len(case.is_special) else None
+    return k[bi, p].contiguous(), v[bi, p].contiguous(), ids
+
+
+def _twins(w, total, **kw):
+    return Case(w, total=total, **kw), Case(w, total=total, **kw)
+
+
+def _step_both(fused, split, layer, pos, q):
+    """One step on both caches: fused on one, append + decode on the other."""
+    k, v, ids = _token(fused, layer, pos)
+    of = fused.cache.step(layer, q, k, v, ids)
+    split.cache.append(layer, k, v, ids)
+    os_ = split.cache.decode(layer, q)
+    return of, os_
+
+
+@pytest.mark.parametrize("counts", [(0, 64), (64, 64), None], ids=["k0-64", "k64-64", "seeded"])
+def test_tiny_steps_from_an_empty_cache(cuda, counts):
+    # S = 4, W = 64: the steps fill the sinks (entries without resident
+    # tokens at t = 0), the window, and wrap the ring into the middle
+    masks = None if counts is None else S.masks_with_counts(TINY, counts)
+    fused, split = _twins(TINY, 200, masks=masks)
+    for t in range(200):
+        q = fused.q(0, t + 1, step=t)
+        of, os_ = _step_both(fused, split, 0, t, q)
+        if t % 9 == 0 or t in (3, 4, 67, 68, 69, 131, 132, 199):
+            fused.cache.check()
+            assert _max_err(of, fused.expected(0, q, t + 1)) <= DECODE_TOL, t
+            assert float((of - os_).abs().max()) <= 1e-4, t
+    fused.cache.check()
+    split.cache.check()
+    assert list(fused.cache.lengths(0)) == [200]
+    torch.cuda.synchronize()
+    assert torch.equal(fused.cache.buffer, split.cache.buffer)
+    fused.check_layout(0, 200)
+
+
+@pytest.mark.parametrize("paged", [False, True], ids=["contiguous", "paged"])
+@pytest.mark.parametrize("ctas", [1, 7, 0])
+def test_llama_layer_all_widths(cuda, paged, ctas):
+    w = LLAMA.scaled(context=3000, batch=2)
+    masks = S.masks_with_counts(w, [0, 32, 64, 96, 128, 32, 0, 64])
+    mt = 2 * 3010 if paged else None
+    fused, split = _twins(w, 3010, masks=masks, middle_tokens=mt)
+    # S + W = 1040: the middle starts a new page at 1040 + 1920 = 2960 + 128k
+    fused.prefill(0, 2985)
+    split.prefill(0, 2985)
+    fused.cache.set_decode_ctas(ctas)
+    split.cache.set_decode_ctas(ctas)
+    for t in range(2985, 3010):
+        q = fused.q(0, t + 1, step=t)
+        of, os_ = _step_both(fused, split, 0, t, q)
+        if t % 6 == 0 or t == 3009:
+            fused.cache.check()
+            assert _max_err(of, fused.expected(0, q, t + 1)) <= DECODE_TOL, t
+            assert float((of - os_).abs().max()) <= 1e-4, t
+    fused.cache.check()
+    split.cache.check()
+    torch.cuda.synchronize()
+    if paged:
+        assert {c: fused.cache.pages(c) for c in (32, 64, 96, 128)} == \
+            {c: split.cache.pages(c) for c in (32, 64, 96, 128)}
+    else:
+        assert torch.equal(fused.cache.buffer, split.cache.buffer)
+    fused.check_layout(0, 3010)
+
+
+def test_fastgen_policies_two_layers_in_one_launch(cuda):
+    # LOCAL heads wrap their W_loc = 256 ring; SPECIAL heads take a token only
+    # when its id is special; FULL heads evict into the middle
+    w = FASTGEN.scaled(num_layers=2, batch=3, context=600, policy_counts=(6, 4, 6))
+    fused, split = _twins(w, 640)
+    L = w.num_layers
+    for layer in range(L):
+        fused.prefill(layer, 600)
+        split.prefill(layer, 600)
+    for t in range(600, 640):
+        qs = torch.stack([fused.q(l, t + 1, step=t) for l in range(L)]).contiguous()
+        ks = torch.stack([_token(fused, l, t)[0] for l in range(L)]).contiguous()
+        vs = torch.stack([_token(fused, l, t)[1] for l in range(L)]).contiguous()
+        ids = _token(fused, 0, t)[2]
+        of = fused.cache.step_layers(0, qs, ks, vs, ids)
+        split.cache.append_layers(0, ks, vs, ids)
+        os_ = split.cache.decode_layers(0, qs)
+        if t % 8 == 0 or t == 639:
+            fused.cache.check()
+            for layer in range(L):
+                assert _max_err(of[layer], fused.expected(layer, qs[layer], t + 1)) <= DECODE_TOL, (t, layer)
+            assert float((of - os_).abs().max()) <= 1e-4, t
+    fused.cache.check()
+    torch.cuda.synchronize()
+    assert torch.equal(fused.cache.buffer, split.cache.buffer)
+    for layer in range(L):
+        fused.check_layout(layer, 640)
+
+
+def test_fastgen_from_empty_special_rows(cuda):
+    # SPECIAL heads start with no rows: entries with nothing resident take
+    # the new token alone when it is special and give o = 0 otherwise
+    w = FASTGEN.scaled(num_layers=1, batch=4, context=64, policy_counts=(2, 4, 2))
+    fused, split = _twins(w, 64)
+    assert fused.flags[:, :40].any()
+    for t in range(40):
+        q = fused.q(0, t + 1, step=t)
+        of, os_ = _step_both(fused, split, 0, t, q)
+        fused.cache.check()
+        assert _max_err(of, fused.expected(0, q, t + 1)) <= DECODE_TOL, t
+        assert float((of - os_).abs().max()) <= 1e-4, t
+    torch.cuda.synchronize()
+    assert torch.equal(fused.cache.buffer, split.cache.buffer)
+    fused.check_layout(0, 40)
+
+
+def test_ragged_released_and_refilled_slots(cuda):
+    w = SERVING.scaled(num_layers=1, batch=3, context=1400)
+    fused, split = _twins(w, 1500, middle_tokens=3 * 1500)
+    lens = np.array([1400, 1100, 700], dtype=np.int32)
+    for c in (fused, split):
+        k, v = c.history(0)
+        c.cache.prefill_ragged(0, k[:, :1400].contiguous(), v[:, :1400].contiguous(), lens)
+        c.cache.release(1)
+    lens[1] = 0
+    for step in range(12):
+        q = fused.q(0, int(lens.max()) + 1, step=step)
+        of, os_ = _step_both(fused, split, 0, lens, q)
+        lens = lens + np.array([1, 0, 1], dtype=np.int32)
+        assert list(fused.cache.lengths(0)) == list(lens)
+        fused.cache.check()
+        assert torch.all(of[1] == 0)
+        assert _max_err(of, fused.expected(0, q, lens)) <= DECODE_TOL, step
+        assert float((of - os_).abs().max()) <= 1e-4
+    # slot 1 takes a new sequence and decodes on
+    for c in (fused, split):
+        k, v = c.history(0)
+        c.cache.prefill_sequence(0, 1, k[1, :1290].contiguous(), v[1, :1290].contiguous())
+    lens[1] = 1290
+    for step in range(12):
+        q = fused.q(0, int(lens.max()) + 1, step=100 + step)
+        of, os_ = _step_both(fused, split, 0, lens, q)
+        lens = lens + 1
+        fused.cache.check()
+        assert _max_err(of, fused.expected(0, q, lens)) <= DECODE_TOL, step
+    split.cache.check()
+    assert list(fused.cache.lengths(0)) == list(split.cache.lengths(0)) == list(lens)
+    fused.check_layout(0, lens)
+    split.check_layout(0, lens)
+
+
+def test_int8_middle_runs_append_then_decode(cuda):
+    # an append may seal a block, which changes the values decode reads: the
+    # step is the two launches, so both paths agree exactly
+    fused, split = _twins(TINY, 600, masks=S.masks_with_counts(TINY, (64, 32)), kv_format=lkb.KV_INT8)
+    fused.prefill(0, 570)
+    split.prefill(0, 570)
+    for t in range(570, 590):                  # seals a block at 580 tokens
+        q = fused.q(0, t + 1, step=t)
+        of, os_ = _step_both(fused, split, 0, t, q)
+        assert torch.equal(of, os_), t
+    fused.cache.check()
+    assert _max_err(of, fused.expected(0, q, 590)) <= DECODE_TOL
+    torch.cuda.synchronize()
+    assert torch.equal(fused.cache.buffer, split.cache.buffer)
+
+
+def test_full_sequence_is_refused_before_launch(cuda):
+    w = SERVING.scaled(num_layers=1, batch=2, context=600)
+    case = Case(w, total=601, capacity=600)
+    case.prefill(0, 600)
+    q = case.q(0, 601)
+    k, v, ids = _token(case, 0, 600)
+    with pytest.raises(lkb.LeankError) as e:
+        case.cache.step(0, q, k, v, ids)
+    assert e.value.status == lkb.LK_ERR_CAPACITY
+    assert list(case.cache.lengths(0)) == [600, 600]
+    case.cache.check()
+    o = case.cache.decode(0, q)
+    assert _max_err(o, case.expected(0, q, 600)) <= DECODE_TOL
+
+
+def test_out_of_range_id_is_reported(cuda):
+    w = FASTGEN.scaled(num_layers=1, batch=2, context=300, policy_counts=(2, 2, 4))
+    case = Case(w, total=302)
+    case.prefill(0, 300)
+    k, v, ids = _token(case, 0, 300)
+    bad = ids.clone()
+    bad[1] = w.vocab + 5
+    case.cache.step(0, case.q(0, 301), k, v, bad)
+    with pytest.raises(lkb.LeankError) as e:
+        case.cache.check()
+    assert e.value.status == lkb.LK_ERR_ARG
+    # the token still entered (as not special), as lk_append does
+    assert list(case.cache.lengths(0)) == [301, 301]
