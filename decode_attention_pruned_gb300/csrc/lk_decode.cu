@@ -63,6 +63,7 @@ constexpr int kQStride = kHeadDim + 8;                  // padded q row (bf16): 
 constexpr int kSlots = 16;                              // barrier pairs = stages in flight at most (power of 2)
 constexpr int kRingBytes = 204 * 1024;
 constexpr int kUnitsA = 2 * kHeadDim * 2;               // line cost of a full-width row: its bytes
+constexpr uint64_t kMinCtaBytes = 64 * 1024;            // line bytes a CTA takes at least (one full-width tile)
 constexpr int kFirst = 1, kLast = 2;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;      // bound of the producer's final wait for its copies
 
@@ -369,8 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     C += scan[w];
   }
   const uint64_t excl = warp_base + incl - local;
-  // every CTA range must hold at least one row start (a row costs <= 16)
-  const int P = (int)max((uint64_t)1, min((uint64_t)gridDim.x, C / kUnitsA));
+  // every CTA range holds at least kMinCtaBytes of rows (so at least one row
+  // start): a small launch runs on fewer CTAs, with fewer partials to merge
+  const int P = (int)max((uint64_t)1, min((uint64_t)gridDim.x, C / kMinCtaBytes));
   const int cta = blockIdx.x;
   const uint64_t start = cta < P ? ((uint64_t)cta * C) / P : C;
   const uint64_t end = cta < P ? ((uint64_t)(cta + 1) * C) / P : C;

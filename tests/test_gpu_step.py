@@ -231,3 +231,24 @@ def test_out_of_range_id_is_reported(cuda):
     assert e.value.status == lkb.LK_ERR_ARG
     # the token still entered (as not special), as lk_append does
     assert list(case.cache.lengths(0)) == [301, 301]
+
+
+@pytest.mark.parametrize("fused_step", [True, False], ids=["fused", "split"])
+def test_one_long_head_over_many_ctas(cuda, fused_step):
+    # one full-width head holds most of the bytes, so its entry spans ~100
+    # CTAs and the in-launch combine merges its partials in several rounds
+    w = LLAMA.scaled(context=20000)
+    masks = S.masks_with_counts(w, [128, 0, 0, 0, 0, 0, 0, 0])
+    case = Case(w, total=20004, masks=masks)
+    case.prefill(0, 20000)
+    for t in range(20000, 20004):
+        q = case.q(0, t + 1, step=t)
+        k, v, ids = _token(case, 0, t)
+        if fused_step:
+            o = case.cache.step(0, q, k, v, ids)
+        else:
+            case.cache.append(0, k, v, ids)
+            o = case.cache.decode(0, q)
+        case.cache.check()
+        assert _max_err(o, case.expected(0, q, t + 1)) <= DECODE_TOL, t
+    case.check_layout(0, 20004)
