@@ -64,6 +64,7 @@ constexpr int kSlots = 16;                              // barrier pairs = stage
 constexpr int kRingBytes = 204 * 1024;
 constexpr int kUnitsA = 2 * kHeadDim * 2;               // line cost of a full-width row: its bytes
 constexpr uint64_t kMinCtaBytes = 64 * 1024;            // line bytes a CTA takes at least (one full-width tile)
+constexpr uint64_t kTokenUnits = 48 * 1024;             // line charge of a fused token stage (~1 us of streaming)
 constexpr int kFirst = 1, kLast = 2;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;      // bound of the producer's final wait for its copies
 
@@ -98,7 +99,7 @@ struct SmemLayout {
   static constexpr int kCBarOff = kBarOff + 2 * kSlots * 8;                  // consumer barrier
   static constexpr int kScanOff = kCBarOff + 8;
   static constexpr int kMiscOff = kScanOff + (kThreads / 32) * 8;
-  static constexpr int kBytes = kMiscOff + 96;
+  static constexpr int kBytes = kMiscOff + 12 * 8;
 };
 constexpr int kSmemBytes = SmemLayout::kBytes + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
@@ -135,6 +136,7 @@ struct EntryLen {
 struct Entry {
   int n_a, n_q, n_b, kb, mrow;
   EntryLen len;
+  int anc;    // fused launches: the full-width row the token stage follows, or -1
 };
 
 // Entry e of a launch = (layer offset lr, sequence b, kv head h), layers
@@ -178,7 +180,7 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
   const EntryId id = entry_id(a, e);
   const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
   const int N = len.n;
-  Entry r{0, 0, 0, 0, -1, len};
+  Entry r{0, 0, 0, 0, -1, len, -1};
   if (hd.policy == kFull) {
     r.n_a = min(N, cv.S + cv.W);
     // a fused append into a full window replaces the slot of token N - W
@@ -202,6 +204,7 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
   }
   r.n_a = min(r.n_a, hd.cap_a);
   r.n_b = min(r.n_b, hd.cap_b);
+  r.anc = len.act && r.n_a > 0 ? (r.mrow >= 0 ? r.mrow : 0) : -1;
   return r;
 }
 
@@ -211,8 +214,13 @@ __device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) { re
 __device__ __forceinline__ uint64_t row_cost_b(int kb) { return (uint64_t)(2 * kb + 256); }
 __device__ __forceinline__ uint64_t row_cost_q(int kb) { return (uint64_t)(qblock_bytes(kb) / kQBlockRows); }
 
+// The token stage of a fused launch is charged kTokenUnits of line right
+// after its anchor row, so the CTA that folds and writes the token streams
+// correspondingly fewer rows.
+__device__ __forceinline__ uint64_t token_units(const Entry& g) { return g.anc >= 0 ? kTokenUnits : 0; }
+
 __device__ __forceinline__ uint64_t entry_cost(const Entry& g) {
-  return (uint64_t)kUnitsA * g.n_a + row_cost_q(g.kb) * g.n_q + row_cost_b(g.kb) * g.n_b;
+  return (uint64_t)kUnitsA * g.n_a + token_units(g) + row_cost_q(g.kb) * g.n_q + row_cost_b(g.kb) * g.n_b;
 }
 
 // a / b for 64-bit a with a 32-bit path when it fits
@@ -305,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[3] = misc[4] = misc[5] = misc[6] = 0;   // geometry of the first entry
     misc[7] = -1;
     misc[8] = misc[9] = misc[10] = 0;
+    misc[11] = -1;
   }
   if (warp == kConsumerWarps && lane == 0) {
     tma_prefetch_map(&tm_k128);
@@ -351,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
   // the first two entries of the chunk keep their geometry for the second
   // pass (a whole single-layer launch fits that)
-  Entry g0{0, 0, 0, 0, -1, {0, 0, 0}}, g1{0, 0, 0, 0, -1, {0, 0, 0}};
+  Entry g0{0, 0, 0, 0, -1, {0, 0, 0}, -1}, g1{0, 0, 0, 0, -1, {0, 0, 0}, -1};
   if (e_lo < e_hi) g0 = entry_geometry(a, e_lo);
   if (e_lo + 1 < e_hi) g1 = entry_geometry(a, e_lo + 1);
   uint64_t local = entry_cost(g0) + entry_cost(g1);
@@ -381,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // geometry go to the producer through shared memory
     uint64_t acc = excl;
     int found = -1;
-    Entry fg{0, 0, 0, 0, -1, {0, 0, 0}};
+    Entry fg{0, 0, 0, 0, -1, {0, 0, 0}, -1};
     for (int e = e_lo; found < 0 && e < e_hi; ++e) {
       const Entry g = e == e_lo ? g0 : e == e_lo + 1 ? g1 : entry_geometry(a, e);
       const uint64_t c = entry_cost(g);
@@ -402,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[8] = fg.len.n;
     misc[9] = fg.len.cnt;
     misc[10] = fg.len.act;
+    misc[11] = fg.anc;
   }
   __syncthreads();
 
@@ -466,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // entry geometry: the first from the scan, later ones from lengths
       // loaded one entry ahead
       Entry g{(int)misc[3], (int)misc[6], (int)misc[4], (int)misc[5], (int)misc[7],
-              {(int)misc[8], (int)misc[9], (int)misc[10]}};
+              {(int)misc[8], (int)misc[9], (int)misc[10]}, (int)misc[11]};
       EntryLen ahead{0, 0, 0};
       if (e + 1 < E) ahead = entry_len(a, e + 1);
       for (; ok && e < E && off < end; ++e) {
@@ -476,10 +486,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint64_t cost = entry_cost(g);
         const uint64_t cq = row_cost_q(g.kb), cb = row_cost_b(g.kb);
-        const uint64_t off_q = off + (uint64_t)kUnitsA * g.n_a;
+        const uint64_t xu = token_units(g);
+        const uint64_t off_q = off + (uint64_t)kUnitsA * g.n_a + xu;
         const uint64_t off_b = off_q + cq * g.n_q;
         int a0, a1, q0, q1, b0, b1;
-        rows_in_range(off, kUnitsA, g.n_a, start, end, a0, a1);
+        if (xu == 0) {
+          rows_in_range(off, kUnitsA, g.n_a, start, end, a0, a1);
+        } else {
+          // full-width rows 0 .. anc, the token's charge, rows anc+1 .. n_a-1
+          const int n1 = g.anc + 1;
+          int p0, p1, s0, s1;
+          rows_in_range(off, kUnitsA, n1, start, end, p0, p1);
+          rows_in_range(off + (uint64_t)kUnitsA * n1 + xu, kUnitsA, g.n_a - n1, start, end, s0, s1);
+          if (p1 > p0) {
+            a0 = p0;
+            a1 = s1 > s0 ? n1 + s1 : p1;
+          } else if (s1 > s0) {
+            a0 = n1 + s0;
+            a1 = n1 + s1;
+          } else {
+            a0 = a1 = 0;
+          }
+        }
         rows_in_range(off_q, cq, g.n_q, start, end, q0, q1);
         rows_in_range(off_b, cb, g.n_b, start, end, b0, b1);
         // paged bf16 region B: tiles end at page boundaries (the box may read
@@ -501,7 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               cv.page_table + (((int64_t)id.l * cv.B + b) * cv.Hkv + id.h) * cv.max_pages;
           const uint64_t last_row_off = g.n_b > 0   ? off_b + cb * (g.n_b - 1)
                                         : g.n_q > 0 ? off_q + cq * (g.n_q - 1)
-                                                    : off + (uint64_t)kUnitsA * (g.n_a - 1);
+                                                    : off + (uint64_t)kUnitsA * (g.n_a - 1) +
+                                                          (g.n_a - 1 > g.anc ? xu : 0);
           // the entry's first / last owning CTA is read only from the segment's
           // last descriptor: work it out after the first load is in flight
           int fc = -1, lc = -1;
@@ -514,9 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // token (and the row it evicts into the middle) as a region-3 stage
           // right after that row's tile, so the slot is overwritten only
           // after this CTA has read it; no other CTA reads it.
-          const int anc = g.mrow >= 0 ? g.mrow : 0;
-          const int xj = fused_launch && g.len.act && g.n_a > 0 && anc >= a0 && anc < a1 ? (anc - a0) / kTileRows
-                                                                                         : -1;
+          const int anc = g.anc;
+          const int xj = fused_launch && anc >= 0 && anc >= a0 && anc < a1 ? (anc - a0) / kTileRows : -1;
           int32_t page_ahead = 0;
           for (int j = 0; j < nt; ++j) {
             const int region = j < nta ? 0 : j < nta + ntq ? 2 : 1;
