@@ -2,9 +2,10 @@
 
 One step = one pass of the whole hot path for one decode token of the
 workload: for each layer, the append (new K/V into the window ring, eviction
-into K_prun) then the split-K decode with its in-launch combine.  With a bf16
-middle both run in one launch per step (lk_step_layers); --step split (and
-every INT8 cache) runs lk_append_layers then lk_decode_attn_layers.
+into K_prun) then the split-K decode with its in-launch combine, through
+lk_step_layers.  --step auto (default) lets the library choose between one
+fused launch and the append + decode launches (it fuses launches over few,
+long entries with a bf16 middle); --step fused / split force one.
 Default workload: the Llama-3.1-8B-shaped layer (32 q / 8 kv heads, d 128,
 batch 1, context 32768, sink 16, window 1024, 70 % channel pruning rounded
 down to multiples of 32, K with 4 channel pairs x8).
@@ -242,16 +243,15 @@ def run_gpu(args, rank, local_rank, world):
     # one step: the new token into every layer (one launch), then decode
     # attention of every layer (one launch; for one layer these are the plain
     # per-layer calls)
-    fused = args.step == "fused" and kvf == lkb.KV_BF16
+    mode = {"auto": lkb.STEP_AUTO, "fused": lkb.STEP_FUSED, "split": lkb.STEP_SPLIT}[args.step]
+    for c in caches:
+        c.set_step_mode(mode)
+    fused = caches[0].step_is_fused(0, L)
 
     def enqueue_step(i):
         c = caches[i % copies]
         s = i % bank
-        if args.step == "fused":
-            c.step_layers(0, gq[s], gk[s], gv[s], gid[s], outs[i % copies], stream=stream)
-        else:
-            c.append_layers(0, gk[s], gv[s], gid[s], stream=stream)
-            c.decode_layers(0, gq[s], outs[i % copies], stream=stream)
+        c.step_layers(0, gq[s], gk[s], gv[s], gid[s], outs[i % copies], stream=stream)
 
     # graphs of whole rotations (copies steps) plus one of the remainder
     def capture(n_steps, start):
@@ -409,6 +409,7 @@ def run_gpu(args, rank, local_rank, world):
         "config": {
             **workload_config(w, args), "context_growth_max": growth,
             "resident_bytes_per_call": resident_step // L, "effective_GBps": resident_step * K * world / elapsed / 1e9,
+            "step_mode": args.step,
             "launches_per_step": "one fused append + decode (all layers)" if fused
             else "append (all layers) + decode (all layers)",
             "cache_copies": copies, "l2_policy": "inputs larger than L2 (rotating cache copies)",
@@ -513,8 +514,8 @@ def main(argv=None):
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"])
     ap.add_argument("--decode-ctas", type=int, default=0, help="CTAs of a decode launch (0: the library's choice)")
-    ap.add_argument("--step", default="fused", choices=["fused", "split"],
-                    help="fused: lk_step_layers (one launch per step with a bf16 middle); split: append + decode")
+    ap.add_argument("--step", default="auto", choices=["auto", "fused", "split"],
+                    help="lk_step_layers mode: the library's choice, one fused launch, or append + decode")
     ap.add_argument("--e2e-steps", type=int, default=4000)
     ap.add_argument("--kernel-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=10.0)

@@ -42,6 +42,7 @@ class RegionInfo(ctypes.Structure):
 
 
 KV_BF16, KV_INT8 = 0, 1
+STEP_AUTO, STEP_FUSED, STEP_SPLIT = 0, 1, 2
 
 
 class CacheOptions(ctypes.Structure):
@@ -74,6 +75,8 @@ SIGNATURES = {
     "lk_decode_attn": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "lk_decode_attn_layers": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "lk_step": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "lk_set_step_mode": (ctypes.c_int, [_vp, _i32]),
+    "lk_step_is_fused": (ctypes.c_int, [_vp, _i32, _i32, ctypes.POINTER(_i32)]),
     "lk_step_layers": (ctypes.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lk_decode_attn_static": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp]),
     "lk_step_host": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -379,6 +382,15 @@ class Cache:
         _check(_lib.lk_decode_attn(self._h, layer, q.data_ptr(), o.data_ptr(), self.workspace.data_ptr(),
                                    self.workspace.numel(), _stream(stream)))
         return o
+
+    def set_step_mode(self, mode):
+        """lk_set_step_mode: STEP_AUTO, STEP_FUSED or STEP_SPLIT."""
+        _check(_lib.lk_set_step_mode(self._h, mode))
+
+    def step_is_fused(self, layer0=0, nlayers=1):
+        f = _i32(0)
+        _check(_lib.lk_step_is_fused(self._h, layer0, nlayers, ctypes.byref(f)))
+        return bool(f.value)
 
     def step(self, layer, q, k, v, ids=None, o=None, stream=None):
         """lk_step: append k, v (ids) to `layer`, then attend with q, in one

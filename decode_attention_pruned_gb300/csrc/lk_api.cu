@@ -335,7 +335,7 @@ struct lk_cache_s {
     return LK_OK;
   }
   CUtensorMap maps[kNumPools];
-  int device = 0, num_sms = 0, decode_ctas = 0;
+  int device = 0, num_sms = 0, decode_ctas = 0, step_mode = LK_STEP_AUTO;
   std::vector<uint8_t> upload;     // host image of the tables (kept alive for the async copy)
 };
 
@@ -350,6 +350,51 @@ int default_decode_ctas(const lk_cache_s* cache, int nlayers) {
   const int64_t entries = (int64_t)nlayers * cache->B * cache->cv.Hkv;
   if (cache->lay.kv_format == kKvBf16 && entries <= 64) return std::max(1, cache->num_sms * 27 / 32);
   return cache->num_sms;
+}
+
+// Resident K+V bytes of one (layer, head) entry at N tokens and `cnt`
+// special rows: what a decode call streams for it.
+uint64_t entry_bytes(const lk_cache_s* cache, const HeadDesc& hd, int N, int cnt) {
+  const int S = cache->cv.S, W = cache->cv.W;
+  uint64_t na = 0, nb = 0;
+  if (hd.policy == kFull) {
+    na = std::min(N, S + W);
+    if (hd.n_kept > 0) nb = std::max(0, N - S - W);
+  } else if (hd.policy == kLocal) {
+    na = std::min(N, cache->cv.W_loc);
+  } else {
+    na = std::min(cnt, hd.cap_a);
+  }
+  if (cache->lay.kv_format == kKvInt8 && nb > 0) {
+    const uint64_t sealed = nb / kQBlockRows, tail = nb % kQBlockRows;
+    return na * (2 * kHeadDim * 2) + sealed * (uint64_t)qblock_bytes(hd.n_kept) +
+           tail * (uint64_t)(hd.n_kept + kHeadDim) * 2;
+  }
+  return na * (2 * kHeadDim * 2) + nb * (uint64_t)(hd.n_kept + kHeadDim) * 2;
+}
+
+// Whether lk_step fuses the append into the decode launch.  Fusion removes a
+// kernel boundary (~3.5 us) but puts the append's latency -- the token
+// stage's copy, its fold into the softmax, the cache write -- on one CTA per
+// entry: it pays off when there are few entries and each CTA streams long
+// (the 32K-token layer: 27.0 -> 25.3 us per step; the 128K-token 4-sequence
+// layer: 89.8 -> 88.8 us) and loses when CTAs stream little (the 0.24 MB
+// layer: 15.0 -> 17.4 us) or carry many entries (the 64-sequence 32-layer
+// step: 3.09 -> 3.14 ms).  Lengths are the host's; SPECIAL rows count as 0.
+bool fuse_step(const lk_cache_s* cache, int layer0, int nlayers) {
+  if (cache->lay.kv_format != kKvBf16 || cache->step_mode == LK_STEP_SPLIT) return false;
+  if (cache->step_mode == LK_STEP_FUSED) return true;
+  const int B = cache->B, H = cache->cv.Hkv;
+  if ((int64_t)nlayers * B * H > 64) return false;
+  uint64_t bytes = 0;
+  for (int l = layer0; l < layer0 + nlayers; ++l)
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h)
+        bytes += entry_bytes(cache, cache->lay.heads[(size_t)l * H + h], cache->host_len[(size_t)l * B + b], 0);
+  const int ctas = cache->decode_ctas > 0 ? cache->decode_ctas : default_decode_ctas(cache, nlayers);
+  // the kernel gives every CTA at least 64 KB of the work
+  const uint64_t p = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)ctas, bytes / (64u << 10)));
+  return bytes / p >= (256u << 10);
 }
 }  // namespace
 
@@ -885,8 +930,9 @@ lk_status lk_step_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const 
   int ctas = 0;
   lk_status st = decode_prepare(cache, layer0, nlayers, q, o, workspace, ws_bytes, "lk_step", a, ctas);
   if (st != LK_OK) return st;
-  if (cache->cv.kv_format == kKvInt8) {
-    // an append may seal a block (the values decode reads change): two launches
+  if (!fuse_step(cache, layer0, nlayers)) {
+    // INT8 middles always: an append may seal a block, which changes the
+    // values the decode reads
     st = lk_append_layers(cache, layer0, nlayers, k, v, ids, stream);
     if (st != LK_OK) return st;
     return lk_decode_attn_layers(cache, layer0, nlayers, q, o, workspace, ws_bytes, stream);
@@ -1078,31 +1124,26 @@ lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_
   if (err == cudaSuccess)
     err = cudaMemcpy(cnt.data(), cache->cv.cnt + (size_t)layer * B, B * 4, cudaMemcpyDeviceToHost);
   if (err != cudaSuccess) return cuda_fail(err, "lk_resident_bytes");
-  const int S = cache->cv.S, W = cache->cv.W;
   uint64_t total = 0;
-  for (int b = 0; b < B; ++b) {
-    const int N = len[b];
-    for (int h = 0; h < H; ++h) {
-      const HeadDesc& hd = cache->lay.heads[(size_t)layer * H + h];
-      uint64_t na = 0, nb = 0;
-      if (hd.policy == kFull) {
-        na = std::min(N, S + W);
-        if (hd.n_kept > 0) nb = std::max(0, N - S - W);
-      } else if (hd.policy == kLocal) {
-        na = std::min(N, cache->cv.W_loc);
-      } else {
-        na = std::min(cnt[b], hd.cap_a);
-      }
-      if (cache->lay.kv_format == kKvInt8 && nb > 0) {
-        const uint64_t sealed = nb / kQBlockRows, tail = nb % kQBlockRows;
-        total += na * (2 * kHeadDim * 2) + sealed * (uint64_t)qblock_bytes(hd.n_kept) +
-                 tail * (uint64_t)(hd.n_kept + kHeadDim) * 2;
-      } else {
-        total += na * (2 * kHeadDim * 2) + nb * (uint64_t)(hd.n_kept + kHeadDim) * 2;
-      }
-    }
-  }
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h) total += entry_bytes(cache, cache->lay.heads[(size_t)layer * H + h], len[b], cnt[b]);
   *bytes = total;
+  return LK_OK;
+}
+
+lk_status lk_set_step_mode(lk_cache cache, int32_t mode) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_set_step_mode: null cache");
+  if (mode != LK_STEP_AUTO && mode != LK_STEP_FUSED && mode != LK_STEP_SPLIT)
+    return fail(LK_ERR_ARG, "lk_set_step_mode: mode %d is not LK_STEP_AUTO, LK_STEP_FUSED or LK_STEP_SPLIT", mode);
+  cache->step_mode = mode;
+  return LK_OK;
+}
+
+lk_status lk_step_is_fused(lk_cache cache, int32_t layer0, int32_t nlayers, int32_t* fused) {
+  if (!cache || !fused) return fail(LK_ERR_ARG, "lk_step_is_fused: null argument");
+  if (nlayers < 1 || layer0 < 0 || layer0 + nlayers > cache->cv.L)
+    return fail(LK_ERR_ARG, "lk_step_is_fused: layers [%d, %d) out of range", layer0, layer0 + nlayers);
+  *fused = fuse_step(cache, layer0, nlayers) ? 1 : 0;
   return LK_OK;
 }
 

@@ -366,6 +366,23 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
  * (synchronises `stream` to read the special-token counts). */
 lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_t* bytes);
 
+/* How lk_step / lk_step_layers run a step on a bf16 middle:
+ *   LK_STEP_AUTO   the library's choice (default): one fused launch for
+ *                  launches over at most 64 (sequence, kv head) entries
+ *                  whose CTAs each stream at least 256 KB (e.g. a 32K-token
+ *                  layer: 27.0 -> 25.3 us per step), else the append and
+ *                  decode launches (a 0.24 MB layer, or a 32-layer,
+ *                  64-sequence step, are faster that way);
+ *   LK_STEP_FUSED  always one launch;   LK_STEP_SPLIT  always two.
+ * Results and cache contents do not depend on the mode.  INT8 middles
+ * always run two launches. */
+typedef enum { LK_STEP_AUTO = 0, LK_STEP_FUSED = 1, LK_STEP_SPLIT = 2 } lk_step_mode;
+lk_status lk_set_step_mode(lk_cache cache, int32_t mode);
+
+/* Whether lk_step_layers(cache, layer0, nlayers, ...) would run as one fused
+ * launch now (at the host's current lengths): *fused = 1 or 0. */
+lk_status lk_step_is_fused(lk_cache cache, int32_t layer0, int32_t nlayers, int32_t* fused);
+
 /* Override the number of CTAs of lk_decode_attn (0 = the library's choice:
  * one per SM, or 27/32 of the SMs for a bf16 launch over at most 64
  * (sequence, kv head) entries, where fewer, longer streams reach a higher

@@ -42,8 +42,14 @@ def _token(case, layer, pos):
     return k[bi, p].contiguous(), v[bi, p].contiguous(), ids
 
 
+def _fused(case):
+    """The case's cache runs lk_step as one launch whatever its size."""
+    case.cache.set_step_mode(lkb.STEP_FUSED)
+    return case
+
+
 def _twins(w, total, **kw):
-    return Case(w, total=total, **kw), Case(w, total=total, **kw)
+    return _fused(Case(w, total=total, **kw)), Case(w, total=total, **kw)
 
 
 def _step_both(fused, split, layer, pos, q):
@@ -205,7 +211,7 @@ def test_int8_middle_runs_append_then_decode(cuda):
 
 def test_full_sequence_is_refused_before_launch(cuda):
     w = SERVING.scaled(num_layers=1, batch=2, context=600)
-    case = Case(w, total=601, capacity=600)
+    case = _fused(Case(w, total=601, capacity=600))
     case.prefill(0, 600)
     q = case.q(0, 601)
     k, v, ids = _token(case, 0, 600)
@@ -220,7 +226,7 @@ def test_full_sequence_is_refused_before_launch(cuda):
 
 def test_out_of_range_id_is_reported(cuda):
     w = FASTGEN.scaled(num_layers=1, batch=2, context=300, policy_counts=(2, 2, 4))
-    case = Case(w, total=302)
+    case = _fused(Case(w, total=302))
     case.prefill(0, 300)
     k, v, ids = _token(case, 0, 300)
     bad = ids.clone()
@@ -239,7 +245,7 @@ def test_one_long_head_over_many_ctas(cuda, fused_step):
     # CTAs and the in-launch combine merges its partials in several rounds
     w = LLAMA.scaled(context=20000)
     masks = S.masks_with_counts(w, [128, 0, 0, 0, 0, 0, 0, 0])
-    case = Case(w, total=20004, masks=masks)
+    case = _fused(Case(w, total=20004, masks=masks))
     case.prefill(0, 20000)
     for t in range(20000, 20004):
         q = case.q(0, t + 1, step=t)
@@ -252,3 +258,29 @@ def test_one_long_head_over_many_ctas(cuda, fused_step):
         case.cache.check()
         assert _max_err(o, case.expected(0, q, t + 1)) <= DECODE_TOL, t
     case.check_layout(0, 20004)
+
+
+def test_automatic_mode_fuses_long_few_entry_layers_only(cuda):
+    # one launch for the 32K-token layer (8 entries, ~660 KB per CTA); two
+    # for the 0.24 MB tiny layer, for 32 layers at once, and for INT8
+    big = Case(LLAMA, total=LLAMA.context + 2)
+    big.prefill(0, LLAMA.context)
+    assert big.cache.step_is_fused(0, 1)
+    small = Case(TINY, total=TINY.context + 2)
+    small.prefill(0, TINY.context)
+    assert not small.cache.step_is_fused(0, 1)
+    small.cache.set_step_mode(lkb.STEP_FUSED)
+    assert small.cache.step_is_fused(0, 1)
+    big.cache.set_step_mode(lkb.STEP_SPLIT)
+    assert not big.cache.step_is_fused(0, 1)
+    many = Case(SERVING.scaled(num_layers=4, batch=4, context=4000), total=4002)
+    assert not many.cache.step_is_fused(0, 4)
+    q8 = Case(TINY, total=TINY.context + 2, kv_format=lkb.KV_INT8)
+    q8.cache.set_step_mode(lkb.STEP_FUSED)
+    assert not q8.cache.step_is_fused(0, 1)
+    # either way the step gives the oracle's output
+    q = big.q(0, LLAMA.context + 1)
+    k, v, ids = _token(big, 0, LLAMA.context)
+    o = big.cache.step(0, q, k, v, ids)
+    big.cache.check()
+    assert _max_err(o, big.expected(0, q, LLAMA.context + 1)) <= DECODE_TOL
