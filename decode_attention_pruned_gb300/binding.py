@@ -439,7 +439,9 @@ class Cache:
         return o
 
     def step_host(self, layer, q, k, v, ids, o, stream=None):
-        """q/k/v/ids/o are pinned host tensors; o is valid after the stream syncs."""
+        """q/k/v/ids/o are host tensors (pinned ones are read and written in
+        place by the kernels, others are copied); o is valid after the stream
+        syncs."""
         import torch
         B, Hq, H = self.batch, self.plan.num_q_heads, self.plan.num_kv_heads
         _need(q, torch.bfloat16, (B, Hq, 128), "q", "cpu")

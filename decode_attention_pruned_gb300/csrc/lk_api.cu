@@ -957,6 +957,30 @@ lk_status lk_step(lk_cache cache, int32_t layer, const void* q, const void* k, c
   return lk_step_layers(cache, layer, 1, q, k, v, ids, o, workspace, ws_bytes, stream);
 }
 
+// Device address of a page-locked host buffer mapped into the device's
+// address space (cudaHostAlloc, or cudaHostRegister with mapping -- torch's
+// pin_memory), else null.
+static const void* mapped_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+// A host-driven step whose buffers the device can address: the kernels read
+// q, k, v, ids from host memory and write o there over the host link (on
+// Grace, NVLink-C2C), with no staging copies.  Always the append and decode
+// launches: the fused kernel loads the new token with bulk copies, which
+// this path keeps away from host memory.
+static lk_status step_in_place(lk_cache cache, int32_t layer, const void* q, const void* k, const void* v,
+                               const int32_t* ids, float* o, void* workspace, size_t ws_bytes, void* stream) {
+  lk_status st = lk_append_layers(cache, layer, 1, k, v, ids, stream);
+  if (st != LK_OK) return st;
+  return lk_decode_attn_layers(cache, layer, 1, q, o, workspace, ws_bytes, stream);
+}
+
 // Append + decode from the inputs staged in the workspace, then copy o back.
 static lk_status step_from_staging(lk_cache cache, int32_t layer, bool has_ids, float* o_host, void* workspace,
                             size_t ws_bytes, void* stream) {
@@ -983,6 +1007,16 @@ lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const 
   if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_step_host: layer %d out of range", layer);
   if (cache->max_len(layer) >= cache->cap)
     return fail(LK_ERR_CAPACITY, "lk_step_host: a sequence of layer %d is full (%d tokens)", layer, cache->cap);
+  {
+    const void* qd = mapped_host(q_host);
+    const void* kd = mapped_host(k_host);
+    const void* vd = mapped_host(v_host);
+    const void* idd = ids_host ? mapped_host(ids_host) : nullptr;
+    float* od = static_cast<float*>(const_cast<void*>(mapped_host(o_host)));
+    if (qd && kd && vd && od && (!ids_host || idd))
+      return step_in_place(cache, layer, qd, kd, vd, static_cast<const int32_t*>(idd), od, workspace, ws_bytes,
+                           stream);
+  }
   const lk_plan_desc& d = cache->plan.d;
   const size_t B = cache->B;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1011,6 +1045,14 @@ lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in
   const size_t B = cache->B;
   const size_t qb = B * d.num_q_heads * kHeadDim * 2, kvb = B * d.num_kv_heads * kHeadDim * 2;
   const size_t bytes = qb + 2 * kvb + (has_ids ? B * 4 : 0);
+  {
+    const uint8_t* in = static_cast<const uint8_t*>(mapped_host(host_in));
+    float* od = static_cast<float*>(const_cast<void*>(mapped_host(o_host)));
+    if (in && od)
+      return step_in_place(cache, layer, in, in + qb, in + qb + kvb,
+                           has_ids ? reinterpret_cast<const int32_t*>(in + qb + 2 * kvb) : nullptr, od, workspace,
+                           ws_bytes, stream);
+  }
   // the staging areas q | k | v | ids are adjacent in the workspace
   if (w.off_k != w.off_q + qb || w.off_v != w.off_k + kvb || w.off_ids != w.off_v + kvb)
     return fail(LK_ERR_UNSUPPORTED, "lk_step_host_packed: staging areas are not adjacent");

@@ -336,19 +336,25 @@ lk_status lk_step_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const 
                          const void* v, const int32_t* ids, float* o, void* workspace, size_t ws_bytes,
                          void* stream);
 
-/* One decode step end to end from host memory: copies q [B][Hq][128] bf16,
- * k, v [B][Hkv][128] bf16 and ids [B] int32 (NULL allowed) from host to the
- * workspace, runs lk_step, and copies o [B][Hq][128]
- * fp32 back to host.  Host buffers should be pinned for the copies to be
- * asynchronous; read o only after synchronising `stream`. */
+/* One decode step end to end from host memory: q [B][Hq][128] bf16, k, v
+ * [B][Hkv][128] bf16 and ids [B] int32 (NULL allowed) in, o [B][Hq][128]
+ * fp32 out.  When every buffer is page-locked and mapped into the device's
+ * address space (cudaHostAlloc / cudaMallocHost, cudaHostRegister with
+ * mapping; torch's pin_memory), the append and decode kernels read the
+ * inputs from host memory and write o there directly over the host link
+ * (NVLink-C2C on Grace) -- no staging copies.  Otherwise the inputs are
+ * copied into the workspace, lk_step runs, and o is copied back (pinned
+ * buffers keep those copies asynchronous).  Read o only after synchronising
+ * `stream`. */
 lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const void* k_host,
                        const void* v_host, const int32_t* ids_host, float* o_host,
                        void* workspace, size_t ws_bytes, void* stream);
 
-/* lk_step_host with the step's inputs in one host block, moved by a single
- * copy: host_in = q bf16 [B][Hq][128] | k bf16 [B][Hkv][128] | v bf16
- * [B][Hkv][128] | ids int32 [B] (present iff has_ids != 0), back to back.
- * The block should be one pinned allocation. */
+/* lk_step_host with the step's inputs in one host block: host_in = q bf16
+ * [B][Hq][128] | k bf16 [B][Hkv][128] | v bf16 [B][Hkv][128] | ids int32 [B]
+ * (present iff has_ids != 0), back to back.  Read in place when the block
+ * and o are mapped page-locked memory, else moved by a single copy each
+ * way. */
 lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in, int32_t has_ids,
                               float* o_host, void* workspace, size_t ws_bytes, void* stream);
 

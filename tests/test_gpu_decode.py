@@ -187,6 +187,25 @@ def test_step_host_matches_device_path(cuda):
     assert torch.equal(a.cache.buffer, b.cache.buffer)
 
 
+def test_step_host_pageable_buffers_are_copied(cuda):
+    # pageable host memory cannot be read by the kernels: the step stages
+    # the inputs through the workspace and copies o back, with the same result
+    w = SERVING.scaled(num_layers=1, batch=2, context=600)
+    a = Case(w, total=601)
+    b = Case(w, total=601)
+    a.prefill(0, 600)
+    b.prefill(0, 600)
+    k, v = a.history(0)
+    q = a.q(0, 601)
+    o_dev = a.cache.step(0, q, k[:, 600].contiguous(), v[:, 600].contiguous())
+    o_host = torch.empty(o_dev.shape, dtype=torch.float32)
+    b.cache.step_host(0, q.cpu(), k[:, 600].contiguous().cpu(), v[:, 600].contiguous().cpu(), None, o_host)
+    torch.cuda.synchronize()
+    b.cache.check()
+    assert torch.equal(o_host, o_dev.cpu())
+    assert torch.equal(a.cache.buffer, b.cache.buffer)
+
+
 def test_capacity_is_enforced(cuda):
     w = TINY
     case = Case(w, total=10, capacity=10)
