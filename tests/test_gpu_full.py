@@ -1,7 +1,10 @@
 """Parity at the workloads' full sizes, in the launch configuration bench.py
-times (one CTA per SM, append then decode).  The oracle recomputes sampled
-(sequence, kv head) outputs one by one from the same seeded history; the
-layout check reads sampled heads' cache rows byte for byte."""
+times: lk_step / lk_step_layers in the library's automatic mode (one fused
+launch for the single-layer 32K and 128K-token workloads, append + decode
+launches over all 32 layers at once for the serving and FastGen steps),
+after a prefill of N-1 tokens.  The oracle recomputes sampled (sequence, kv
+head) outputs one by one from the same seeded history; the layout check
+reads sampled heads' cache rows byte for byte."""
 import numpy as np
 import pytest
 import torch
@@ -17,12 +20,13 @@ def _sample_pairs(w, layer, k, rng):
     return sorted(set(pairs))
 
 
-def _check_layer(case, layer, N, pairs, layout_pairs):
-    case.prefill(layer, N - 1)
-    case.append(layer, N - 1)
-    q = case.q(layer, N)
-    o = case.cache.decode(layer, q)
-    case.cache.check()
+def _token(case, layer, t):
+    k, v = case.history(layer)
+    ids = case.ids[:, t].contiguous() if len(case.is_special) else None
+    return k[:, t].contiguous(), v[:, t].contiguous(), ids
+
+
+def _check(case, layer, N, o, q, pairs, layout_pairs):
     ref = case.expected(layer, q, N, heads=pairs)
     G = case.w.group
     worst = 0.0
@@ -31,38 +35,79 @@ def _check_layer(case, layer, N, pairs, layout_pairs):
         worst = max(worst, err)
         assert err <= DECODE_TOL, (layer, b, h, err)
     case.check_layout(layer, N, heads=layout_pairs)
+    return worst
+
+
+def _check_layer(case, layer, N, pairs, layout_pairs, fused=None):
+    """One layer: prefill N-1 tokens, then one lk_step with token N-1."""
+    case.prefill(layer, N - 1)
+    if fused is not None:
+        assert case.cache.step_is_fused(layer, 1) == fused
+    q = case.q(layer, N)
+    k, v, ids = _token(case, layer, N - 1)
+    o = case.cache.step(layer, q, k, v, ids)
+    case.cache.check()
+    worst = _check(case, layer, N, o, q, pairs, layout_pairs)
     case.drop_history(layer)
     return worst
+
+
+def _check_all_layers(case, N, pick):
+    """Every layer prefilled to N-1 tokens, then one lk_step_layers over all
+    of them (the bench's step); pick(layer) -> (pairs, layout_pairs)."""
+    w = case.w
+    L = w.num_layers
+    ks, vs = [], []
+    for layer in range(L):
+        case.prefill(layer, N - 1)
+        k, v, _ = _token(case, layer, N - 1)
+        ks.append(k)
+        vs.append(v)
+        case.drop_history(layer)
+    assert not case.cache.step_is_fused(0, L)
+    ids = case.ids[:, N - 1].contiguous() if len(case.is_special) else None
+    qs = torch.stack([case.q(layer, N) for layer in range(L)]).contiguous()
+    o = case.cache.step_layers(0, qs, torch.stack(ks).contiguous(), torch.stack(vs).contiguous(), ids)
+    case.cache.check()
+    del ks, vs
+    for layer in range(L):
+        pairs, layout_pairs = pick(layer)
+        _check(case, layer, N, o[layer], qs[layer], pairs, layout_pairs)
+        case.drop_history(layer)
 
 
 def test_full_llama31_8b_layer(cuda):
     w = S.WORKLOADS[1]
     case = Case(w, total=w.context, gen_device=cuda)
     pairs = [(0, h) for h in range(w.num_kv_heads)]
-    _check_layer(case, 0, w.context, pairs, pairs)
+    _check_layer(case, 0, w.context, pairs, pairs, fused=True)
 
 
 def test_full_qwen25_7b_long(cuda):
     w = S.WORKLOADS[3]
     case = Case(w, total=w.context, gen_device=cuda)
     pairs = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
-    _check_layer(case, 0, w.context, pairs, [(0, h) for h in range(w.num_kv_heads)])
+    _check_layer(case, 0, w.context, pairs, [(0, h) for h in range(w.num_kv_heads)], fused=True)
 
 
 def test_full_serving_b64_all_layers(cuda):
     w = S.WORKLOADS[2]
     case = Case(w, total=w.context, gen_device=cuda)
     rng = np.random.default_rng(7)
-    for layer in range(w.num_layers):
+
+    def pick(layer):
         pairs = _sample_pairs(w, layer, 4, rng)
-        _check_layer(case, layer, w.context, pairs, pairs[:1])
+        return pairs, pairs[:1]
+
+    _check_all_layers(case, w.context, pick)
 
 
 def test_full_fastgen_mix_all_layers(cuda):
     w = S.WORKLOADS[4]
     case = Case(w, total=w.context, gen_device=cuda)
     rng = np.random.default_rng(11)
-    for layer in range(w.num_layers):
+
+    def pick(layer):
         # one head of each policy present in the layer, plus a random one
         pairs = set(_sample_pairs(w, layer, 1, rng))
         for pol in (S.POLICY_FULL, S.POLICY_LOCAL, S.POLICY_SPECIAL):
@@ -70,7 +115,9 @@ def test_full_fastgen_mix_all_layers(cuda):
             if len(hs):
                 pairs.add((int(rng.integers(w.batch)), int(hs[0])))
         pairs = sorted(pairs)
-        _check_layer(case, layer, w.context, pairs, pairs[:2])
+        return pairs, pairs[:2]
+
+    _check_all_layers(case, w.context, pick)
 
 
 def test_full_qwen25_7b_long_int8(cuda):
