@@ -383,8 +383,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // start): a small launch runs on fewer CTAs, with fewer partials to merge
   const int P = (int)max((uint64_t)1, min((uint64_t)gridDim.x, C / kMinCtaBytes));
   const int cta = blockIdx.x;
-  const uint64_t start = cta < P ? ((uint64_t)cta * C) / P : C;
-  const uint64_t end = cta < P ? ((uint64_t)(cta + 1) * C) / P : C;
+  // floor(iC/P) = i*(C/P) + floor(i*(C mod P)/P): one division of C by P,
+  // then 32-bit arithmetic (i, C mod P < P <= 256)
+  const uint64_t cq = udiv(C, (uint64_t)P);
+  const uint32_t cr = (uint32_t)(C - cq * (uint64_t)P);
+  const uint64_t start = cta < P ? (uint64_t)cta * cq + ((uint32_t)cta * cr) / (uint32_t)P : C;
+  const uint64_t end = cta < P ? (uint64_t)(cta + 1) * cq + ((uint32_t)(cta + 1) * cr) / (uint32_t)P : C;
   if (local > 0 && excl <= start && start < excl + local) {
     // this chunk holds the CTA's first row: its entry, line offset and
     // geometry go to the producer through shared memory
@@ -1184,7 +1188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         m0 = mn0;
         m1 = mn1;
       }
-      consumer_sync(cbar, cphase, a);
+      // warp w < 4 overwrites only slot w, which only it read: a warp-level
+      // barrier separates its lanes' reads from the writes
+      __syncwarp();
       if (warp < kMergeSlots) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
