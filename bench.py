@@ -59,9 +59,9 @@ COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 # "<sha256[:16] of the decode kernel sources>:<workload>:<kv format>:<fused |
 # decode>" (the bench reports null when the kernel changed since the capture).
 NCU_TRAFFIC = {
-    "edb70aaa3ce730a9:llama31_8b_layer:bf16:fused": 86373120 + 2529792,
-    "edb70aaa3ce730a9:qwen25_7b_long:bf16:fused": 514358784 + 3164672,
-    "edb70aaa3ce730a9:qwen25_7b_long:int8:decode": 276291328 + 3414528,
+    "3d83c02683750c44:llama31_8b_layer:bf16:fused": 86299648 + 2440960,
+    "3d83c02683750c44:qwen25_7b_long:bf16:fused": 514351360 + 3139328,
+    "3d83c02683750c44:qwen25_7b_long:int8:decode": 276279296 + 3110656,
 }
 
 
