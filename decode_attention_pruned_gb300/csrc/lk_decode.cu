@@ -229,12 +229,29 @@ __device__ __forceinline__ uint64_t udiv(uint64_t a, uint64_t b) {
   return a / b;
 }
 
+// x / c for a row cost c of the line: every cost the line uses is one of
+// these constants, so the division compiles to a multiply (the producer
+// divides before its first copy of every entry)
+__device__ __forceinline__ uint64_t div_cost(uint64_t x, uint64_t c) {
+  switch (c) {
+    case 512: return x >> 9;       // full-width rows; kept-channel rows of k = 128
+    case 320: return x / 320u;     // kept-channel rows, k = 32 / 64 / 96
+    case 384: return x / 384u;
+    case 448: return x / 448u;
+    case 165: return x / 165u;     // sealed INT8 rows, k = 32 / 64 / 96 / 128
+    case 198: return x / 198u;
+    case 231: return x / 231u;
+    case 264: return x / 264u;
+    default: return udiv(x, c);
+  }
+}
+
 // Rows r in [0, n) of a region whose row r sits at line offset o0 + c*r and
 // starts inside [start, end): r in [r0, r1).
 __device__ __forceinline__ void rows_in_range(uint64_t o0, uint64_t c, int n, uint64_t start, uint64_t end,
                                               int& r0, int& r1) {
-  r0 = start > o0 ? (int)min((uint64_t)n, udiv(start - o0 + c - 1, c)) : 0;
-  r1 = end > o0 ? (int)min((uint64_t)n, udiv(end - o0 + c - 1, c)) : 0;
+  r0 = start > o0 ? (int)min((uint64_t)n, div_cost(start - o0 + c - 1, c)) : 0;
+  r1 = end > o0 ? (int)min((uint64_t)n, div_cost(end - o0 + c - 1, c)) : 0;
 }
 
 // The CTA whose range [floor(iC/P), floor((i+1)C/P)) holds offset x < C:
@@ -351,73 +368,118 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(&cv.len[id0.l * cv.B + id0.b]));
     }
   }
+  // barrier inits and misc visible to every thread (before the dependency
+  // wait, so it overlaps the preceding kernel)
+  __syncthreads();
   const uint64_t policy = l2_policy_evict_first();
   grid_dependency_wait();
   grid_launch_dependents();
 
-  // ---- the line: per-thread chunks of entries, block exclusive scan
-  const int per = (E + kThreads - 1) / kThreads;
-  const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
-  // the first two entries of the chunk keep their geometry for the second
-  // pass (a whole single-layer launch fits that)
-  Entry g0{0, 0, 0, 0, -1, {0, 0, 0}, -1}, g1{0, 0, 0, 0, -1, {0, 0, 0}, -1};
-  if (e_lo < e_hi) g0 = entry_geometry(a, e_lo);
-  if (e_lo + 1 < e_hi) g1 = entry_geometry(a, e_lo + 1);
-  uint64_t local = entry_cost(g0) + entry_cost(g1);
-  for (int e = e_lo + 2; e < e_hi; ++e) local += entry_cost(entry_geometry(a, e));
-  uint64_t incl = local;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint64_t v = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += v;
-  }
-  if (lane == 31) scan[warp] = incl;
-  __syncthreads();
-  uint64_t warp_base = 0, C = 0;
-  for (int w = 0; w < kThreads / 32; ++w) {
-    if (w < warp) warp_base += scan[w];
-    C += scan[w];
-  }
-  const uint64_t excl = warp_base + incl - local;
-  // every CTA range holds at least kMinCtaBytes of rows (so at least one row
-  // start): a small launch runs on fewer CTAs, with fewer partials to merge
-  const int P = (int)max((uint64_t)1, min((uint64_t)gridDim.x, C / kMinCtaBytes));
+  // ---- the line: the total cost C, this CTA's range [start, end), and the
+  // entry, line offset and geometry of its first row
+  uint64_t C = 0, start = 0, end = 0;
+  int P = 1;
+  int first_e = E;
+  uint64_t first_off = 0;
+  Entry fg{0, 0, 0, 0, -1, {0, 0, 0}, -1};
   const int cta = blockIdx.x;
+  // every CTA range holds at least kMinCtaBytes of rows (so at least one row
+  // start): a small launch runs on fewer CTAs, with fewer partials to merge.
   // floor(iC/P) = i*(C/P) + floor(i*(C mod P)/P): one division of C by P,
   // then 32-bit arithmetic (i, C mod P < P <= 256)
-  const uint64_t cq = udiv(C, (uint64_t)P);
-  const uint32_t cr = (uint32_t)(C - cq * (uint64_t)P);
-  const uint64_t start = cta < P ? (uint64_t)cta * cq + ((uint32_t)cta * cr) / (uint32_t)P : C;
-  const uint64_t end = cta < P ? (uint64_t)(cta + 1) * cq + ((uint32_t)(cta + 1) * cr) / (uint32_t)P : C;
-  if (local > 0 && excl <= start && start < excl + local) {
-    // this chunk holds the CTA's first row: its entry, line offset and
-    // geometry go to the producer through shared memory
-    uint64_t acc = excl;
-    int found = -1;
-    Entry fg{0, 0, 0, 0, -1, {0, 0, 0}, -1};
-    for (int e = e_lo; found < 0 && e < e_hi; ++e) {
-      const Entry g = e == e_lo ? g0 : e == e_lo + 1 ? g1 : entry_geometry(a, e);
-      const uint64_t c = entry_cost(g);
-      if (acc + c > start) {
-        found = e;
-        fg = g;
-      } else {
-        acc += c;
-      }
+  auto split_line = [&]() {
+    P = (int)max((uint64_t)1, min((uint64_t)gridDim.x, C / kMinCtaBytes));
+    const uint64_t cq = udiv(C, (uint64_t)P);
+    const uint32_t cr = (uint32_t)(C - cq * (uint64_t)P);
+    start = cta < P ? (uint64_t)cta * cq + ((uint32_t)cta * cr) / (uint32_t)P : C;
+    end = cta < P ? (uint64_t)(cta + 1) * cq + ((uint32_t)(cta + 1) * cr) / (uint32_t)P : C;
+  };
+  if (E <= 32) {
+    // few entries: every warp scans them all itself (lane = entry), so no
+    // block barrier stands between the length loads and the first copy
+    const Entry g = lane < E ? entry_geometry(a, lane) : Entry{0, 0, 0, 0, -1, {0, 0, 0}, -1};
+    const uint64_t cost = entry_cost(g);
+    uint64_t incl = cost;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
     }
-    misc[0] = found;
-    misc[1] = (int64_t)acc;
-    misc[3] = fg.n_a;
-    misc[4] = fg.n_b;
-    misc[5] = fg.kb;
-    misc[6] = fg.n_q;
-    misc[7] = fg.mrow;
-    misc[8] = fg.len.n;
-    misc[9] = fg.len.cnt;
-    misc[10] = fg.len.act;
-    misc[11] = fg.anc;
+    C = __shfl_sync(0xffffffffu, incl, 31);
+    split_line();
+    const unsigned hit = __ballot_sync(0xffffffffu, cost > 0 && incl - cost <= start && start < incl);
+    const int src = hit ? __ffs(hit) - 1 : 0;
+    if (hit) first_e = src;
+    first_off = __shfl_sync(0xffffffffu, incl - cost, src);
+    fg.n_a = __shfl_sync(0xffffffffu, g.n_a, src);
+    fg.n_q = __shfl_sync(0xffffffffu, g.n_q, src);
+    fg.n_b = __shfl_sync(0xffffffffu, g.n_b, src);
+    fg.kb = __shfl_sync(0xffffffffu, g.kb, src);
+    fg.mrow = __shfl_sync(0xffffffffu, g.mrow, src);
+    fg.len.n = __shfl_sync(0xffffffffu, g.len.n, src);
+    fg.len.cnt = __shfl_sync(0xffffffffu, g.len.cnt, src);
+    fg.len.act = __shfl_sync(0xffffffffu, g.len.act, src);
+    fg.anc = __shfl_sync(0xffffffffu, g.anc, src);
+  } else {
+    // per-thread chunks of entries, block exclusive scan
+    const int per = (E + kThreads - 1) / kThreads;
+    const int e_lo = min(E, tid * per), e_hi = min(E, e_lo + per);
+    // the first two entries of the chunk keep their geometry for the second
+    // pass
+    Entry g0{0, 0, 0, 0, -1, {0, 0, 0}, -1}, g1{0, 0, 0, 0, -1, {0, 0, 0}, -1};
+    if (e_lo < e_hi) g0 = entry_geometry(a, e_lo);
+    if (e_lo + 1 < e_hi) g1 = entry_geometry(a, e_lo + 1);
+    uint64_t local = entry_cost(g0) + entry_cost(g1);
+    for (int e = e_lo + 2; e < e_hi; ++e) local += entry_cost(entry_geometry(a, e));
+    uint64_t incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    uint64_t warp_base = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) warp_base += scan[w];
+      C += scan[w];
+    }
+    const uint64_t excl = warp_base + incl - local;
+    split_line();
+    if (local > 0 && excl <= start && start < excl + local) {
+      // this chunk holds the CTA's first row: its entry, line offset and
+      // geometry go to every warp through shared memory
+      uint64_t acc = excl;
+      int found = -1;
+      Entry f{0, 0, 0, 0, -1, {0, 0, 0}, -1};
+      for (int e = e_lo; found < 0 && e < e_hi; ++e) {
+        const Entry g = e == e_lo ? g0 : e == e_lo + 1 ? g1 : entry_geometry(a, e);
+        const uint64_t c = entry_cost(g);
+        if (acc + c > start) {
+          found = e;
+          f = g;
+        } else {
+          acc += c;
+        }
+      }
+      misc[0] = found;
+      misc[1] = (int64_t)acc;
+      misc[3] = f.n_a;
+      misc[4] = f.n_b;
+      misc[5] = f.kb;
+      misc[6] = f.n_q;
+      misc[7] = f.mrow;
+      misc[8] = f.len.n;
+      misc[9] = f.len.cnt;
+      misc[10] = f.len.act;
+      misc[11] = f.anc;
+    }
+    __syncthreads();
+    first_e = (int)misc[0];
+    first_off = (uint64_t)misc[1];
+    fg = Entry{(int)misc[3], (int)misc[6], (int)misc[4], (int)misc[5], (int)misc[7],
+               {(int)misc[8], (int)misc[9], (int)misc[10]}, (int)misc[11]};
   }
-  __syncthreads();
 
   if (warp == kConsumerWarps) {
     // ================================================================ producer
@@ -474,13 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       const bool fused_launch = !kQ8 && a.k_new != nullptr;
-      const int e0 = (int)misc[0];
+      const int e0 = first_e;
       int e = e0;
-      uint64_t off = (uint64_t)misc[1];
+      uint64_t off = first_off;
       // entry geometry: the first from the scan, later ones from lengths
       // loaded one entry ahead
-      Entry g{(int)misc[3], (int)misc[6], (int)misc[4], (int)misc[5], (int)misc[7],
-              {(int)misc[8], (int)misc[9], (int)misc[10]}, (int)misc[11]};
+      Entry g = fg;
       EntryLen ahead{0, 0, 0};
       if (e + 1 < E) ahead = entry_len(a, e + 1);
       for (; ok && e < E && off < end; ++e) {
@@ -848,7 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   // the first entry's q loads while the first tile is in flight
-  int q_entry = (int)misc[0];
+  int q_entry = first_e;
   if (q_entry < E) stage_q(q_entry);
 
   // this warp's 16 rows of every tile
