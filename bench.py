@@ -59,9 +59,9 @@ COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 # "<sha256[:16] of the decode kernel sources>:<workload>:<kv format>:<fused |
 # decode>" (the bench reports null when the kernel changed since the capture).
 NCU_TRAFFIC = {
-    "3d83c02683750c44:llama31_8b_layer:bf16:fused": 86299648 + 2440960,
-    "3d83c02683750c44:qwen25_7b_long:bf16:fused": 514351360 + 3139328,
-    "3d83c02683750c44:qwen25_7b_long:int8:decode": 276279296 + 3110656,
+    "bc051b3b8ee73c52:llama31_8b_layer:bf16:fused": 86314496 + 2442496,
+    "bc051b3b8ee73c52:qwen25_7b_long:bf16:fused": 514349056 + 3090688,
+    "bc051b3b8ee73c52:qwen25_7b_long:int8:decode": 276290560 + 2989056,
 }
 
 
