@@ -376,16 +376,18 @@ uint64_t entry_bytes(const lk_cache_s* cache, const HeadDesc& hd, int N, int cnt
 // Whether lk_step fuses the append into the decode launch.  Fusion removes a
 // kernel boundary (~3.5 us) but puts the append's latency -- the token
 // stage's copy, its fold into the softmax, the cache write -- on one CTA per
-// entry: it pays off when there are few entries and each CTA streams long
-// (the 32K-token layer: 27.0 -> 25.3 us per step; the 128K-token 4-sequence
-// layer: 89.8 -> 88.8 us) and loses when CTAs stream little (the 0.24 MB
-// layer: 15.0 -> 17.4 us) or carry many entries (the 64-sequence 32-layer
-// step: 3.09 -> 3.14 ms).  Lengths are the host's; SPECIAL rows count as 0.
+// entry: it pays off when each CTA streams long and meets few entries (the
+// 32K-token layer: 26.6 -> 25.1 us per step; the 128K-token 4-sequence
+// layer: 89.8 -> 88.8 us; the 16-sequence 32-layer FastGen step, 27 entries
+// per CTA: 1.54 -> 1.51 ms) and loses when CTAs stream little (the 0.24 MB
+// layer: 15.0 -> 17.4 us) or meet many entries (the 64-sequence 32-layer
+// step, 108 per CTA: 3.09 -> 3.14 ms).  Lengths are the host's; SPECIAL
+// rows count as 0.
 bool fuse_step(const lk_cache_s* cache, int layer0, int nlayers) {
   if (cache->lay.kv_format != kKvBf16 || cache->step_mode == LK_STEP_SPLIT) return false;
   if (cache->step_mode == LK_STEP_FUSED) return true;
   const int B = cache->B, H = cache->cv.Hkv;
-  if ((int64_t)nlayers * B * H > 64) return false;
+  const int64_t entries = (int64_t)nlayers * B * H;
   uint64_t bytes = 0;
   for (int l = layer0; l < layer0 + nlayers; ++l)
     for (int b = 0; b < B; ++b)
@@ -394,7 +396,7 @@ bool fuse_step(const lk_cache_s* cache, int layer0, int nlayers) {
   const int ctas = cache->decode_ctas > 0 ? cache->decode_ctas : default_decode_ctas(cache, nlayers);
   // the kernel gives every CTA at least 64 KB of the work
   const uint64_t p = std::max<uint64_t>(1, std::min<uint64_t>((uint64_t)ctas, bytes / (64u << 10)));
-  return bytes / p >= (256u << 10);
+  return bytes / p >= (256u << 10) && entries <= 32 * (int64_t)p;
 }
 }  // namespace
 

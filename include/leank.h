@@ -373,12 +373,12 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
 lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_t* bytes);
 
 /* How lk_step / lk_step_layers run a step on a bf16 middle:
- *   LK_STEP_AUTO   the library's choice (default): one fused launch for
- *                  launches over at most 64 (sequence, kv head) entries
- *                  whose CTAs each stream at least 256 KB (e.g. a 32K-token
- *                  layer: 27.0 -> 25.3 us per step), else the append and
- *                  decode launches (a 0.24 MB layer, or a 32-layer,
- *                  64-sequence step, are faster that way);
+ *   LK_STEP_AUTO   the library's choice (default): one fused launch when
+ *                  the decode's CTAs each stream at least 256 KB and meet
+ *                  at most 32 (layer, sequence, kv head) entries (e.g. a
+ *                  32K-token layer: 26.6 -> 25.1 us per step), else the
+ *                  append and decode launches (a 0.24 MB layer, or a
+ *                  32-layer, 64-sequence step, are faster that way);
  *   LK_STEP_FUSED  always one launch;   LK_STEP_SPLIT  always two.
  * Results and cache contents do not depend on the mode.  INT8 middles
  * always run two launches. */

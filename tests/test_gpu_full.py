@@ -1,7 +1,8 @@
 """Parity at the workloads' full sizes, in the launch configuration bench.py
 times: lk_step / lk_step_layers in the library's automatic mode (one fused
-launch for the single-layer 32K and 128K-token workloads, append + decode
-launches over all 32 layers at once for the serving and FastGen steps),
+launch for the single-layer 32K and 128K-token workloads and for the
+32-layer FastGen step, append + decode launches over all 32 layers for the
+64-sequence serving step),
 after a prefill of N-1 tokens.  The oracle recomputes sampled (sequence, kv
 head) outputs one by one from the same seeded history; the layout check
 reads sampled heads' cache rows byte for byte."""
@@ -52,7 +53,7 @@ def _check_layer(case, layer, N, pairs, layout_pairs, fused=None):
     return worst
 
 
-def _check_all_layers(case, N, pick):
+def _check_all_layers(case, N, pick, fused):
     """Every layer prefilled to N-1 tokens, then one lk_step_layers over all
     of them (the bench's step); pick(layer) -> (pairs, layout_pairs)."""
     w = case.w
@@ -64,7 +65,7 @@ def _check_all_layers(case, N, pick):
         ks.append(k)
         vs.append(v)
         case.drop_history(layer)
-    assert not case.cache.step_is_fused(0, L)
+    assert case.cache.step_is_fused(0, L) == fused
     ids = case.ids[:, N - 1].contiguous() if len(case.is_special) else None
     qs = torch.stack([case.q(layer, N) for layer in range(L)]).contiguous()
     o = case.cache.step_layers(0, qs, torch.stack(ks).contiguous(), torch.stack(vs).contiguous(), ids)
@@ -99,7 +100,7 @@ def test_full_serving_b64_all_layers(cuda):
         pairs = _sample_pairs(w, layer, 4, rng)
         return pairs, pairs[:1]
 
-    _check_all_layers(case, w.context, pick)
+    _check_all_layers(case, w.context, pick, fused=False)
 
 
 def test_full_fastgen_mix_all_layers(cuda):
@@ -117,7 +118,7 @@ def test_full_fastgen_mix_all_layers(cuda):
         pairs = sorted(pairs)
         return pairs, pairs[:2]
 
-    _check_all_layers(case, w.context, pick)
+    _check_all_layers(case, w.context, pick, fused=True)
 
 
 def test_full_qwen25_7b_long_int8(cuda):

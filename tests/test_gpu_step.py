@@ -262,7 +262,7 @@ def test_one_long_head_over_many_ctas(cuda, fused_step):
 
 def test_automatic_mode_fuses_long_few_entry_layers_only(cuda):
     # one launch for the 32K-token layer (8 entries, ~660 KB per CTA); two
-    # for the 0.24 MB tiny layer, for 32 layers at once, and for INT8
+    # for the 0.24 MB tiny layer, for many entries per CTA, and for INT8
     big = Case(LLAMA, total=LLAMA.context + 2)
     big.prefill(0, LLAMA.context)
     assert big.cache.step_is_fused(0, 1)
@@ -273,8 +273,12 @@ def test_automatic_mode_fuses_long_few_entry_layers_only(cuda):
     assert small.cache.step_is_fused(0, 1)
     big.cache.set_step_mode(lkb.STEP_SPLIT)
     assert not big.cache.step_is_fused(0, 1)
-    many = Case(SERVING.scaled(num_layers=4, batch=4, context=4000), total=4002)
-    assert not many.cache.step_is_fused(0, 4)
+    # 32 layers x 64 sequences x 8 heads: 108 entries per CTA
+    many = Case(SERVING.scaled(context=600), total=602, gen_device=cuda)
+    for layer in range(many.w.num_layers):
+        many.prefill(layer, 600)
+        many.drop_history(layer)
+    assert not many.cache.step_is_fused(0, many.w.num_layers)
     q8 = Case(TINY, total=TINY.context + 2, kv_format=lkb.KV_INT8)
     q8.cache.set_step_mode(lkb.STEP_FUSED)
     assert not q8.cache.step_is_fused(0, 1)
