@@ -85,19 +85,20 @@ def test_tiny_steps_from_an_empty_cache(cuda, counts):
 @pytest.mark.parametrize("paged", [False, True], ids=["contiguous", "paged"])
 @pytest.mark.parametrize("ctas", [1, 7, 0])
 def test_llama_layer_all_widths(cuda, paged, ctas):
-    w = LLAMA.scaled(context=3000, batch=2)
+    w = LLAMA.scaled(context=3100, batch=2)
     masks = S.masks_with_counts(w, [0, 32, 64, 96, 128, 32, 0, 64])
-    mt = 2 * 3010 if paged else None
-    fused, split = _twins(w, 3010, masks=masks, middle_tokens=mt)
-    # S + W = 1040: the middle starts a new page at 1040 + 1920 = 2960 + 128k
-    fused.prefill(0, 2985)
-    split.prefill(0, 2985)
+    mt = 2 * 3100 if paged else None
+    fused, split = _twins(w, 3100, masks=masks, middle_tokens=mt)
+    # S + W = 1040: the token appended at n = 3088 evicts middle row 2048,
+    # the first row of page 16
+    fused.prefill(0, 3075)
+    split.prefill(0, 3075)
     fused.cache.set_decode_ctas(ctas)
     split.cache.set_decode_ctas(ctas)
-    for t in range(2985, 3010):
+    for t in range(3075, 3100):
         q = fused.q(0, t + 1, step=t)
         of, os_ = _step_both(fused, split, 0, t, q)
-        if t % 6 == 0 or t == 3009:
+        if t % 6 == 0 or t in (3087, 3088, 3089, 3099):
             fused.cache.check()
             assert _max_err(of, fused.expected(0, q, t + 1)) <= DECODE_TOL, t
             assert float((of - os_).abs().max()) <= 1e-4, t
@@ -109,7 +110,7 @@ def test_llama_layer_all_widths(cuda, paged, ctas):
             {c: split.cache.pages(c) for c in (32, 64, 96, 128)}
     else:
         assert torch.equal(fused.cache.buffer, split.cache.buffer)
-    fused.check_layout(0, 3010)
+    fused.check_layout(0, 3100)
 
 
 def test_fastgen_policies_two_layers_in_one_launch(cuda):
