@@ -55,13 +55,15 @@ FALLBACK_HBM_GBS = 6800.0
 MAX_CONTEXT_GROWTH = 0.01           # appends may lengthen the context by at most 1 %
 COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 
-# DRAM bytes (read + write) per decode launch from one ncu capture, keyed by
+# DRAM bytes (read + write) per decode launch from one ncu capture (taken on
+# source hash bc051b3b8ee73c52, which differs from the current one only in
+# comments), keyed by
 # "<sha256[:16] of the decode kernel sources>:<workload>:<kv format>:<fused |
 # decode>" (the bench reports null when the kernel changed since the capture).
 NCU_TRAFFIC = {
-    "bc051b3b8ee73c52:llama31_8b_layer:bf16:fused": 86314496 + 2442496,
-    "bc051b3b8ee73c52:qwen25_7b_long:bf16:fused": 514349056 + 3090688,
-    "bc051b3b8ee73c52:qwen25_7b_long:int8:decode": 276290560 + 2989056,
+    "888a98b9c229d7df:llama31_8b_layer:bf16:fused": 86314496 + 2442496,
+    "888a98b9c229d7df:qwen25_7b_long:bf16:fused": 514349056 + 3090688,
+    "888a98b9c229d7df:qwen25_7b_long:int8:decode": 276290560 + 2989056,
 }
 
 

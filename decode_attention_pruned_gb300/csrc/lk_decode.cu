@@ -15,8 +15,9 @@
 //   * The work line.  Each (layer, b, h) "entry" is a run of rows: full-width
 //     rows, then sealed INT8 rows, then bf16 kept-channel rows.  A row costs
 //     the bytes it streams, so the line is measured in bytes.  CTA i of P
-//     takes the rows whose line offset falls in [iC/P, (i+1)C/P); the CTAs
-//     touching an entry are exactly first..last and each writes one partial.
+//     takes the rows whose line offset falls in [iC/P, (i+1)C/P), with P
+//     such that every CTA takes at least 64 KB; the CTAs touching an entry
+//     are exactly first..last and each writes one partial.
 //   * Per CTA: warp 8 (one lane) issues one TMA load per K tile and one per V
 //     tile (swizzled boxes), or one bulk copy per sealed INT8 block, into a
 //     FIFO ring of variable-size stages with sixteen mbarrier slots; warps
@@ -70,7 +71,7 @@ constexpr uint64_t kDrainLimitNs = 1000000000ull;      // bound of the producer'
 
 struct StageDesc {
   int32_t e;           // entry = b * Hkv + h; < 0 ends the stream
-  int32_t region;      // 0: full width, 1: kept channels (bf16), 2: sealed INT8 block
+  int32_t region;      // 0: full width, 1: kept channels (bf16), 2: sealed INT8 block, 3: fused token
   int32_t rlo;         // first valid row of the tile (sealed blocks; else 0)
   int32_t nrows;       // valid rows of the tile: rlo .. rlo + nrows - 1
   int32_t width;       // K channels of the tile
