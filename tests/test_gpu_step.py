@@ -289,3 +289,22 @@ def test_automatic_mode_fuses_long_few_entry_layers_only(cuda):
     o = big.cache.step(0, q, k, v, ids)
     big.cache.check()
     assert _max_err(o, big.expected(0, q, LLAMA.context + 1)) <= DECODE_TOL
+
+
+@pytest.mark.parametrize("hq,hkv", [(4, 4), (32, 4), (12, 4)], ids=["G1", "G8", "G3"])
+def test_fused_query_group_sizes(cuda, hq, hkv):
+    # the token fold splits warp 0 as 8 heads x 4 channel quarters: G = 1,
+    # the full G = 8 and an odd G = 3, on every width class (with evictions)
+    w = LLAMA.scaled(num_q_heads=hq, num_kv_heads=hkv, context=1700, batch=2)
+    masks = S.masks_with_counts(w, [32, 0, 96, 128])
+    fused, split = _twins(w, 1706, masks=masks)
+    fused.prefill(0, 1700)
+    split.prefill(0, 1700)
+    for t in range(1700, 1706):
+        q = fused.q(0, t + 1, step=t)
+        of, os_ = _step_both(fused, split, 0, t, q)
+        fused.cache.check()
+        assert _max_err(of, fused.expected(0, q, t + 1)) <= DECODE_TOL, t
+        assert float((of - os_).abs().max()) <= 1e-4, t
+    torch.cuda.synchronize()
+    assert torch.equal(fused.cache.buffer, split.cache.buffer)
