@@ -177,6 +177,13 @@ def run_gpu(args, rank, local_rank, world):
     pol = S.make_policies(w)
     masks = S.make_masks(w, pol)
     spec = S.make_special_table(w)
+    if args.layers:
+        # a smaller case for profiling: the workload's first layers, with the
+        # masks and policies they have in the whole workload
+        if not 0 < args.layers <= w.num_layers:
+            raise SystemExit(f"--layers must be in 1..{w.num_layers}")
+        w = w.scaled(num_layers=args.layers)
+        pol, masks = pol[: w.num_layers].copy(), masks[: w.num_layers].copy()
     plan = lkb.Plan.for_workload(w, masks, pol, spec if len(spec) else None)
     L, B = w.num_layers, w.batch
     W, K = args.warmup, args.steps
@@ -396,7 +403,8 @@ def run_gpu(args, rank, local_rank, world):
         kernel_name = "decode_kernel"
     peak, peak_kind = _peaks()
     achieved = alg_bytes / kernel_s / 1e9
-    traffic = NCU_TRAFFIC.get(f"{_decode_source_hash()}:{w.name}:{args.kv}:{'fused' if fused else 'decode'}")
+    wkey = w.name if w.num_layers == S.WORKLOAD_BY_NAME[w.name].num_layers else f"{w.name}/{w.num_layers}L"
+    traffic = NCU_TRAFFIC.get(f"{_decode_source_hash()}:{wkey}:{args.kv}:{'fused' if fused else 'decode'}")
 
     line = {
         "metric": METRIC,
@@ -475,7 +483,8 @@ def oracle_sample(w_name, budget_s, max_units=None, kv="bf16"):
         el = time.perf_counter() - t0
         if el >= budget_s or (max_units is not None and units >= max_units):
             break
-    units_per_call = w.batch * w.num_kv_heads * w.num_layers
+    # one call is the decode attention of one layer: every (sequence, kv head)
+    units_per_call = w.batch * w.num_kv_heads
     return units / el / units_per_call, units, el
 
 
@@ -497,7 +506,7 @@ def run_reference(args):
     oracle_sample(args.workload, 0.0, max_units=max(1, min(W, 3)), kv=args.kv)
     value, units, el = oracle_sample(args.workload, args.reference_budget, max_units=K, kv=args.kv)
     sample = (f"fp64 numpy oracle, one (sequence, kv head) of layer 0 per step; {units} steps in {el:.1f} s "
-              f"(capped at {args.reference_budget:.0f} s); calls/s = steps/s / (batch x kv heads x layers)")
+              f"(capped at {args.reference_budget:.0f} s); calls/s = steps/s / (batch x kv heads)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": units,
         "warmup": W, "ms_per_step": el / units * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -521,6 +530,8 @@ def main(argv=None):
     ap.add_argument("--decode-ctas", type=int, default=0, help="CTAs of a decode launch (0: the library's choice)")
     ap.add_argument("--step", default="auto", choices=["auto", "fused", "split"],
                     help="lk_step_layers mode: the library's choice, one fused launch, or append + decode")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: run the workload's first LAYERS layers (0: all)")
     ap.add_argument("--e2e-steps", type=int, default=4000)
     ap.add_argument("--kernel-steps", type=int, default=2000)
     ap.add_argument("--cpu-budget", type=float, default=10.0)

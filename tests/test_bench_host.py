@@ -61,3 +61,15 @@ def test_reference_arm_nonzero_rank_is_silent(monkeypatch):
     with contextlib.redirect_stdout(buf):
         rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--workload", "tiny"])
     assert rc == 0 and buf.getvalue() == ""
+
+
+def test_oracle_rate_counts_layer_calls():
+    """A call is one layer's decode attention (every sequence and kv head),
+    as in the GPU arm's value (steps x layers / s): a 32-layer workload's
+    oracle rate is not divided by its layers."""
+    from decode_attention_pruned_gb300 import synth as S
+    w = S.WORKLOAD_BY_NAME["serving_b64"]
+    value, units, el = bench.oracle_sample("serving_b64", 0.0, max_units=1)
+    assert units == 1
+    assert value == pytest.approx(units / el / (w.batch * w.num_kv_heads))
+    assert bench.job_throughput(10, w.num_layers, 1, 2.0) == pytest.approx(10 * w.num_layers / 2.0)
