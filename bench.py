@@ -55,15 +55,24 @@ FALLBACK_HBM_GBS = 6800.0
 MAX_CONTEXT_GROWTH = 0.01           # appends may lengthen the context by at most 1 %
 COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 
-# DRAM bytes (read + write) per decode launch from one ncu capture (taken on
-# source hash bc051b3b8ee73c52, which differs from the current one only in
-# comments), keyed by
-# "<sha256[:16] of the decode kernel sources>:<workload>:<kv format>:<fused |
-# decode>" (the bench reports null when the kernel changed since the capture).
+# DRAM bytes (read + write) per decode launch from one ncu capture, keyed by
+# "<sha256[:16] of the decode kernel sources>:<workload>[/<layers>L]:<kv
+# format>:<fused | decode>" (the bench reports null when the kernel changed
+# since the capture).  The 32-layer launches are too large to capture with
+# the multi-pass sections; their entries scale the 4-layer capture's
+# traffic per algorithmic byte to the full launch's algorithmic bytes (the
+# 2- and 4-layer captures give 1.0108 and 1.0059 of the algorithmic bytes
+# for serving_b64, 1.0200 and 1.0148 for fastgen_mix).
 NCU_TRAFFIC = {
-    "888a98b9c229d7df:llama31_8b_layer:bf16:fused": 86314496 + 2442496,
-    "888a98b9c229d7df:qwen25_7b_long:bf16:fused": 514349056 + 3090688,
-    "888a98b9c229d7df:qwen25_7b_long:int8:decode": 276290560 + 2989056,
+    "69f4f2651982a365:llama31_8b_layer:bf16:fused": 86260992 + 2471424,
+    "69f4f2651982a365:qwen25_7b_long:bf16:fused": 513990656 + 3203840,
+    "69f4f2651982a365:qwen25_7b_long:int8:decode": 275990784 + 3170048,
+    "69f4f2651982a365:serving_b64/2L:bf16:decode": 943220736 + 4510976,
+    "69f4f2651982a365:serving_b64/4L:bf16:decode": 2175133440 + 5291264,
+    "69f4f2651982a365:fastgen_mix/2L:bf16:fused": 441189120 + 3350272,
+    "69f4f2651982a365:fastgen_mix/4L:bf16:fused": 864369920 + 3672064,
+    "69f4f2651982a365:serving_b64:bf16:decode": 19795624561,
+    "69f4f2651982a365:fastgen_mix:bf16:fused": 10545616751,
 }
 
 

@@ -71,6 +71,12 @@ struct Layout {
   int32_t max_pages = 0;                 // 0: contiguous region B
   int32_t num_pages[kNumPools] = {};     // paged: pages of each width class
   int32_t free_off[kNumPools] = {};
+  // decode TMA views: first row, rows per block and blocks of region A of
+  // each policy class (pools K128 and V) and of region B of each pool
+  int64_t a_base[3] = {}, a_blocks[3] = {};
+  int32_t a_rows[3] = {};
+  int64_t b_base[kNumPools] = {}, b_blocks[kNumPools] = {};
+  int32_t b_rows = 0;
   std::vector<HeadDesc> heads;
 };
 
@@ -114,17 +120,30 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_toke
   int64_t rows[kNumPools] = {0, 0, 0, 0, 0};
   int64_t ra = 0;
   int64_t class_heads[kNumPools] = {0, 0, 0, 0, 0};
-  for (int i = 0; i < L * H; ++i) {
-    HeadDesc& hd = lay->heads[i];
-    hd.policy = p.policy[i];
-    hd.n_kept = hd.policy == kFull ? p.n_kept[i] : 0;
-    hd.cap_a = hd.policy == kFull    ? std::min(cap, d.sink + d.local)
-               : hd.policy == kLocal ? std::min(cap, d.local_only_window)
-                                     : lay->spec_cap;
-    hd.row_a = ra;
-    ra += (int64_t)B * hd.cap_a;
-    hd.pool_kb = kPoolK128;
-    if (hd.policy == kFull && hd.n_kept > 0) class_heads[pool_for_width(hd.n_kept)] += 1;
+  // region A, one policy class after another: a class's rows are equal
+  // blocks of cap_a rows, one per (head, sequence)
+  for (int cls = kFull; cls <= kSpecial; ++cls) {
+    const int32_t cap_a = cls == kFull    ? std::min(cap, d.sink + d.local)
+                          : cls == kLocal ? std::min(cap, d.local_only_window)
+                                          : lay->spec_cap;
+    lay->a_base[cls] = ra;
+    lay->a_rows[cls] = cap_a;
+    int64_t blocks = 0;
+    for (int i = 0; i < L * H; ++i) {
+      if (p.policy[i] != cls) continue;
+      HeadDesc& hd = lay->heads[i];
+      hd.policy = cls;
+      hd.n_kept = cls == kFull ? p.n_kept[i] : 0;
+      hd.cap_a = cap_a;
+      hd.row_a = ra;
+      hd.blk_a = (int32_t)blocks;
+      blocks += B;
+      ra += (int64_t)B * cap_a;
+      hd.pool_kb = kPoolK128;
+      if (cls == kFull && hd.n_kept > 0) class_heads[pool_for_width(hd.n_kept)] += 1;
+    }
+    if (blocks > INT32_MAX) return fail(LK_ERR_CAPACITY, "%lld region-A blocks in one policy class", (long long)blocks);
+    lay->a_blocks[cls] = blocks;
   }
   rows[kPoolK128] = ra;
   rows[kPoolV] = ra;
@@ -198,6 +217,27 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_toke
         hd.vrow_b = rows[kPoolV];
         rows[kPoolV] += (int64_t)B * hd.cap_b;
       }
+    }
+  }
+  // region-B views: blocks of one sequence's rows (INT8: its bf16 tail), or
+  // of one page, from the first region-B row of each pool
+  {
+    const int64_t rows_b = paged && !q8 ? kPageRows : q8 ? std::min<int64_t>(mid_cap, kQBlockRows) : mid_cap;
+    lay->b_rows = (int32_t)std::max<int64_t>(1, rows_b);
+    for (int pl = 0; pl < kNumPools; ++pl) {
+      lay->b_base[pl] = pl == kPoolK128 || pl == kPoolV ? ra : 0;
+      lay->b_blocks[pl] = std::max<int64_t>(1, (rows[pl] - lay->b_base[pl]) / lay->b_rows);
+      if (lay->b_blocks[pl] > INT32_MAX)
+        return fail(LK_ERR_CAPACITY, "pool %d needs %lld region-B blocks", pl, (long long)lay->b_blocks[pl]);
+    }
+    for (int i = 0; i < L * H; ++i) {
+      HeadDesc& hd = lay->heads[i];
+      if (hd.policy != kFull || hd.n_kept == 0 || rows_b == 0) continue;
+      const int64_t kr = hd.krow_b - lay->b_base[hd.pool_kb], vr = hd.vrow_b - lay->b_base[kPoolV];
+      if (kr % rows_b != 0 || vr % rows_b != 0)
+        return fail(LK_ERR_STATE, "internal: region-B rows of head %d are not block aligned", i);
+      hd.kblk_b = (int32_t)(kr / rows_b);
+      hd.vblk_b = (int32_t)(vr / rows_b);
     }
   }
   for (int pl = 0; pl < kNumPools; ++pl) {
@@ -334,7 +374,7 @@ struct lk_cache_s {
     for (int pl = 0; pl < kNumPools; ++pl) host_free[pl] -= need[pl];
     return LK_OK;
   }
-  CUtensorMap maps[kNumPools];
+  DecodeMaps maps;
   int device = 0, num_sms = 0, decode_ctas = 0, step_mode = LK_STEP_AUTO;
   std::vector<uint8_t> upload;     // host image of the tables (kept alive for the async copy)
 };
@@ -650,25 +690,62 @@ static lk_status cache_init_impl(lk_plan plan, void* dev_buf, size_t bytes, int3
   // One TMA operation per tile and operand (bandwidth grows with the size of
   // each operation): 128-byte-row pools load as 64-channel halves with
   // 128-byte swizzle, 64-byte-row pools as 32-channel stripes with 64-byte
-  // swizzle; 3-D maps fold the halves / stripes of a row into one box.
-  for (int pl = 0; pl < kNumPools; ++pl) {
+  // swizzle; the halves / stripes of a row fold into one box.  Flat maps are
+  // {channels, rows, parts}; block views {channels, rows per block, blocks,
+  // parts}, so that a box stops at the end of its (head, sequence) block or
+  // page.
+  std::memset(&c->maps, 0, sizeof(c->maps));
+  auto encode_view = [&](int map, int pl, int64_t first_row, int64_t rows, int64_t blocks) -> CUresult {
     const int width = pool_width(pl);
     const bool fam128 = (width % 64) == 0;
     const int inner = fam128 ? 64 : 32;              // channels per half / stripe
     const int parts = width / inner;
     const cuuint64_t row_bytes = (cuuint64_t)width * 2;
-    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)lay.pool_rows[pl], (cuuint64_t)parts};
-    cuuint64_t strides[2] = {row_bytes, (cuuint64_t)inner * 2};
-    cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)kTmaBoxRows, (cuuint32_t)parts};
-    const cuuint32_t estride[3] = {1, 1, 1};
-    const cuuint32_t rank = parts > 1 ? 3 : 2;
-    CUresult r = encode(&c->maps[pl], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, cv.pool[pl], dims, strides, box,
-                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        fam128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const bool blocked = blocks > 0;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    cuuint32_t rank = 0;
+    dims[rank] = (cuuint64_t)inner;
+    box[rank++] = (cuuint32_t)inner;
+    dims[rank] = (cuuint64_t)rows;
+    strides[rank - 1] = row_bytes;
+    box[rank++] = (cuuint32_t)kTmaBoxRows;
+    if (blocked) {
+      dims[rank] = (cuuint64_t)blocks;
+      strides[rank - 1] = (cuuint64_t)rows * row_bytes;
+      box[rank++] = 1;
+    }
+    if (parts > 1) {
+      dims[rank] = (cuuint64_t)parts;
+      strides[rank - 1] = (cuuint64_t)inner * 2;
+      box[rank++] = (cuuint32_t)parts;
+    }
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    return encode(&c->maps.m[map], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, cv.pool[pl] + first_row * width, dims,
+                  strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  fam128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  };
+  for (int map = 0; map < kNumMaps; ++map) {
+    CUresult r;
+    if (map < kMapAK) {
+      r = encode_view(map, map - kMapFlat, 0, lay.pool_rows[map - kMapFlat], 0);
+    } else {
+      // block views shorter than a box are never used: encode them over one
+      // box of the pool so that every map is valid
+      const bool a = map < kMapB;
+      const int cls = (map - kMapAK) % 3;
+      const int pl = a ? (map < kMapAV ? kPoolK128 : kPoolV) : map - kMapB;
+      const int64_t first = a ? lay.a_base[cls] : lay.b_base[pl];
+      const int64_t rows = a ? lay.a_rows[cls] : lay.b_rows;
+      const int64_t blocks = a ? lay.a_blocks[cls] : lay.b_blocks[pl];
+      const bool usable = rows >= kTmaBoxRows && blocks > 0;
+      c->maps.block_rows[map] = usable ? (int32_t)rows : 0;
+      r = usable ? encode_view(map, pl, first, rows, blocks) : encode_view(map, pl, 0, kTmaBoxRows, 1);
+    }
     if (r != CUDA_SUCCESS) {
       delete c;
-      return fail(LK_ERR_CUDA, "cuTensorMapEncodeTiled failed for pool %d (CUresult %d)", pl, (int)r);
+      return fail(LK_ERR_CUDA, "cuTensorMapEncodeTiled failed for map %d (CUresult %d)", map, (int)r);
     }
   }
   *out = c;

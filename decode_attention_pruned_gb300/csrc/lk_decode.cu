@@ -294,9 +294,7 @@ __device__ __forceinline__ uint32_t tile_addr64(uint32_t base, int r, int c) {
 // instantiation carries no INT8 code.
 template <bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_k32, const __grid_constant__ CUtensorMap tm_k64,
-                  const __grid_constant__ CUtensorMap tm_k96, const DecodeArgs a) {
+    decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -333,12 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     misc[8] = misc[9] = misc[10] = 0;
     misc[11] = -1;
   }
+  // the flat maps; the block views (few boxes use them) load on first use
+  if (warp == kConsumerWarps && lane < kMapAK) tma_prefetch_map(&maps.m[lane]);
   if (warp == kConsumerWarps && lane == 0) {
-    tma_prefetch_map(&tm_k128);
-    tma_prefetch_map(&tm_v);
-    tma_prefetch_map(&tm_k32);
-    tma_prefetch_map(&tm_k64);
-    tma_prefetch_map(&tm_k96);
     // read every launch parameter the producer uses once, so their constant
     // cache lines arrive while the preceding kernel finishes
     uint64_t touch = (uint64_t)cv.hdr ^ (uint64_t)cv.len ^ (uint64_t)cv.cnt ^ (uint64_t)cv.page_table ^
@@ -576,9 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         rows_in_range(off_q, cq, g.n_q, start, end, q0, q1);
         rows_in_range(off_b, cb, g.n_b, start, end, b0, b1);
-        // paged bf16 region B: tiles end at page boundaries (the box may read
-        // past a page end; those rows are beyond nrows and ignored).  Sealed
-        // INT8 blocks: one tile per block, whole block loaded, rows masked.
+        // paged bf16 region B: tiles end at page boundaries (a box that starts
+        // inside a page is clipped at its end: the page is a block of the
+        // view).  Sealed INT8 blocks: one tile per block, whole block loaded,
+        // rows masked.
         const bool paged = cv.max_pages > 0;
         const bool bpaged = paged && cv.kv_format == kKvBf16;
         const int nta = (a1 - a0 + kTileRows - 1) / kTileRows;
@@ -670,22 +666,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t kdst = base + SmemLayout::kRingOff + at;
             const uint32_t vdst = kdst + (uint32_t)kTileRows * 2 * width;
             if (region == 0) {
-              const int32_t row = (int32_t)(hd.row_a + (int64_t)b * hd.cap_a + r);
-              tma_load_3d(kdst, &tm_k128, 0, row, 0, fb, policy);
-              tma_load_3d(vdst, &tm_v, 0, row, 0, fb, policy);
+              // a box past the end of the (head, sequence) block takes the
+              // class's block view
+              const int cls = hd.policy;
+              if (r + kTileRows > hd.cap_a && maps.block_rows[kMapAK + cls] != 0) {
+                tma_load_4d(kdst, &maps.m[kMapAK + cls], 0, r, hd.blk_a + b, 0, fb, policy);
+                tma_load_4d(vdst, &maps.m[kMapAV + cls], 0, r, hd.blk_a + b, 0, fb, policy);
+              } else {
+                const int32_t row = (int32_t)(hd.row_a + (int64_t)b * hd.cap_a + r);
+                tma_load_3d(kdst, &maps.m[kMapFlat + kPoolK128], 0, row, 0, fb, policy);
+                tma_load_3d(vdst, &maps.m[kMapFlat + kPoolV], 0, row, 0, fb, policy);
+              }
             } else if (region == 2) {
               bulk_load(kdst, cv.qpool + hd.qoff + (int64_t)page * bytes, bytes, fb, policy);
             } else {
-              const int64_t rb = bpaged ? (int64_t)page * kPageRows + r % kPageRows : (int64_t)b * hd.cap_b + r;
-              const int32_t krow = (int32_t)(hd.krow_b + rb);
-              const int32_t vrow = (int32_t)(hd.vrow_b + rb);
-              switch (hd.pool_kb) {
-                case kPoolK32: tma_load_2d(kdst, &tm_k32, 0, krow, fb, policy); break;
-                case kPoolK64: tma_load_2d(kdst, &tm_k64, 0, krow, fb, policy); break;
-                case kPoolK96: tma_load_3d(kdst, &tm_k96, 0, krow, 0, fb, policy); break;
-                default: tma_load_3d(kdst, &tm_k128, 0, krow, 0, fb, policy); break;
+              // block: the sequence's region-B rows, or the page
+              const int32_t blk = bpaged ? page : b;
+              const int rr = bpaged ? r % kPageRows : r;
+              const int pk = hd.pool_kb;
+              const bool narrow = pk == kPoolK32 || pk == kPoolK64;     // one part per row
+              const int32_t brows = maps.block_rows[kMapB + pk];
+              if (brows != 0 && rr + kTileRows > brows) {
+                const int32_t kz = hd.kblk_b + blk, vz = hd.vblk_b + blk;
+                if (narrow)
+                  tma_load_3d(kdst, &maps.m[kMapB + pk], 0, rr, kz, fb, policy);
+                else
+                  tma_load_4d(kdst, &maps.m[kMapB + pk], 0, rr, kz, 0, fb, policy);
+                tma_load_4d(vdst, &maps.m[kMapB + kPoolV], 0, rr, vz, 0, fb, policy);
+              } else {
+                const int64_t rb = bpaged ? (int64_t)page * kPageRows + rr : (int64_t)b * hd.cap_b + r;
+                const int32_t krow = (int32_t)(hd.krow_b + rb);
+                const int32_t vrow = (int32_t)(hd.vrow_b + rb);
+                if (narrow)
+                  tma_load_2d(kdst, &maps.m[kMapFlat + pk], 0, krow, fb, policy);
+                else
+                  tma_load_3d(kdst, &maps.m[kMapFlat + pk], 0, krow, 0, fb, policy);
+                tma_load_3d(vdst, &maps.m[kMapFlat + kPoolV], 0, vrow, 0, fb, policy);
               }
-              tma_load_3d(vdst, &tm_v, 0, vrow, 0, fb, policy);
             }
             ++issued;
             if (fc < 0) {
@@ -1434,7 +1451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t decode_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int ctas, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ctas, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t err = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -1453,11 +1470,8 @@ cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (args.cv.kv_format == kKvInt8)
-    return cudaLaunchKernelEx(&cfg, decode_kernel<true>, maps[kPoolK128], maps[kPoolV], maps[kPoolK32],
-                              maps[kPoolK64], maps[kPoolK96], args);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<false>, maps[kPoolK128], maps[kPoolV], maps[kPoolK32],
-                            maps[kPoolK64], maps[kPoolK96], args);
+  if (args.cv.kv_format == kKvInt8) return cudaLaunchKernelEx(&cfg, decode_kernel<true>, maps, args);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<false>, maps, args);
 }
 
 }  // namespace lk

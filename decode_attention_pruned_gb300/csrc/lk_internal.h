@@ -5,10 +5,11 @@
 //   | HeadDesc[L][Hkv] | kept[L][Hkv][128] i16 | is_special[vocab] u8
 //   | pool K128 | pool V | pool K32 | pool K64 | pool K96
 //
-// Pools are 2-D row arrays (rows x width bf16) so that one TMA tensor map
-// covers each; heads of equal kept width share a pool (the head grouping of
-// LeanK section 3.1).  Region A (full width: sinks + window ring, LOCAL ring,
-// SPECIAL rows) of every head sits at the same row index in pools K128 and V.
+// Pools are 2-D row arrays (rows x width bf16); heads of equal kept width
+// share a pool (the head grouping of LeanK section 3.1).  Region A (full
+// width: sinks + window ring, LOCAL ring, SPECIAL rows) of every head sits at
+// the same row index in pools K128 and V, grouped by policy class so that a
+// class's rows are equal blocks of cap_a rows per (head, sequence).
 // Region B (middle tokens of FULL heads with k > 0) has its K rows in the
 // pool of width k and its V rows after all region-A rows of pool V: either
 // contiguous per (layer, sequence, head), or in 128-row pages drawn from a
@@ -78,9 +79,14 @@ struct HeadDesc {                 // one (layer, kv head)
   int64_t qoff;                   // INT8: byte offset in the Q pool of sequence 0's blocks
                                   //       (paged: of the class's page area)
   int32_t qblocks;                // INT8, contiguous: sealed blocks per sequence
-  int32_t pad;
+  // decode TMA views (a pool's rows seen as equal blocks, one per sequence or
+  // page): the block of sequence 0's region A in its policy class's view,
+  // and of sequence 0's region-B K and V rows (paged: of the class's page 0)
+  int32_t blk_a;
+  int32_t kblk_b;
+  int32_t vblk_b;
 };
-static_assert(sizeof(HeadDesc) == 64, "HeadDesc layout");
+static_assert(sizeof(HeadDesc) == 72, "HeadDesc layout");
 
 struct DevHeader {
   uint32_t status;

@@ -7,6 +7,25 @@
 
 namespace lk {
 
+// TMA tensor maps of the decode kernel.  Flat maps: one per pool, over all
+// its rows (a 128-row box that starts near the end of a (head, sequence)
+// block reads rows of the next block).  Block views: one pool's rows seen as
+// [blocks][rows per block][channels], a block being one (head, sequence) of
+// region A of a policy class, or one sequence's region B of a head (paged:
+// one page), so a box that runs past the block's end is clipped there (zero
+// fill, no DRAM read).  Higher-rank boxes stream slightly slower, so only a
+// box that would cross its block's end takes the block view.
+constexpr int kMapFlat = 0;         // + pool: every row of the pool
+constexpr int kMapAK = kNumPools;   // + policy class: region-A K rows (pool K128)
+constexpr int kMapAV = kMapAK + 3;  // + policy class: region-A V rows (pool V)
+constexpr int kMapB = kMapAV + 3;   // + pool: region-B rows of that pool (kPoolV: V rows)
+constexpr int kNumMaps = kMapB + kNumPools;
+struct DecodeMaps {
+  CUtensorMap m[kNumMaps];
+  // rows per block of each block view; below one box the view is not used
+  int32_t block_rows[kNumMaps];
+};
+
 struct DecodeArgs {
   CacheView cv;
   int32_t layer;            // first layer
@@ -47,7 +66,7 @@ struct PrefillArgs {
 };
 
 size_t decode_smem_bytes();
-cudaError_t launch_decode(const CUtensorMap* maps, const DecodeArgs& args, int ctas, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ctas, cudaStream_t stream);
 cudaError_t launch_append(const AppendArgs& args, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& args, bool has_special, int num_sms, cudaStream_t stream);
 cudaError_t launch_release(const CacheView& cv, int b, cudaStream_t stream);
