@@ -6,7 +6,7 @@ LeanK article (framerc.cn) §2.2 stage 2 ("hardware-friendly mask"): a global
 threshold keeps the most important channels over all (layer, head) pairs,
 each head's kept count is brought to a multiple of the alignment, and each
 head keeps its most important channels.  Readings (the printed routine is
-garbled; these follow the survey of the pages):
+garbled; these are the plainest readings the rest of the section supports):
 
 * ``prune_pct`` = s is the share of channels pruned: the threshold is the
   s-th percentile of the eligible alphas, and a channel stays when
