@@ -20,8 +20,9 @@ dependent launch between consecutive kernels).
 Printed: one JSON line (rank 0).  `value` = decode-attention calls/s of all
 ranks; `roofline` = the step's decode kernel (the fused one when the step is one
 launch): algorithmic bytes / event-timed launch duration, against the HBM
-peak; `e2e` = the same metric through
-lk_step_host_packed from pinned host memory (copies inside the timed region);
+peak; `e2e` = the same metric through lk_step_host_packed (one layer) or
+lk_step_layers_host_packed (several) from pinned host memory, the host
+traffic inside the timed region;
 `cpu_baseline` = the fp64 oracle on a bounded sample on the host cores.
 
 --impl reference times the oracle (the only reference this method has) on
@@ -361,34 +362,33 @@ def run_gpu(args, rank, local_rank, world):
     stream.synchronize()
     kdur_isolated = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
 
-    # end to end through lk_step_host_packed: each step's inputs sit in one
-    # pinned host block (q | k | v | ids) moved by one copy
-    def packed_inputs(s, l):
-        parts = [gq[s][l].view(torch.uint8).reshape(-1), gk[s][l].view(torch.uint8).reshape(-1),
-                 gv[s][l].view(torch.uint8).reshape(-1)]
+    # end to end from pinned host memory: each step's inputs sit in one host
+    # block, read in place by the kernels (lk_step_host_packed: q | k | v |
+    # ids of one layer; over several layers lk_step_layers_host_packed: q of
+    # every layer | k | v | ids), and o lands in a pinned host buffer
+    def packed_inputs(s):
+        if L == 1:
+            parts = [gq[s][0], gk[s][0], gv[s][0]]
+        else:
+            parts = [gq[s], gk[s], gv[s]]
+        parts = [p.contiguous().view(torch.uint8).reshape(-1) for p in parts]
         if gid[s] is not None:
             parts.append(gid[s].view(torch.uint8).reshape(-1))
-        blk = torch.cat([p.cpu() for p in parts]).pin_memory()
-        sizes = [p.numel() for p in parts]
-        offs = [sum(sizes[:i]) for i in range(len(sizes))]
-        view = lambda i, dt, shape: blk[offs[i]:offs[i] + sizes[i]].view(dt).view(shape)
-        q_h = view(0, torch.bfloat16, (B, w.num_q_heads, 128))
-        k_h = view(1, torch.bfloat16, (B, w.num_kv_heads, 128))
-        v_h = view(2, torch.bfloat16, (B, w.num_kv_heads, 128))
-        i_h = view(3, torch.int32, (B,)) if gid[s] is not None else None
-        return blk, q_h, k_h, v_h, i_h
-    packed = [[packed_inputs(s, l) for l in range(L)] for s in range(bank)]
+        return torch.cat([p.cpu() for p in parts]).pin_memory()
+    packed = [packed_inputs(s) for s in range(bank)]
     with_ids = gid[0] is not None
-    ho = torch.empty((B, w.num_q_heads, 128), dtype=torch.float32).pin_memory()
-    h2d = packed[0][0][0].numel() * L
-    d2h = ho.numel() * 4 * L
+    ho = torch.empty((L, B, w.num_q_heads, 128), dtype=torch.float32).pin_memory()
+    h2d = packed[0].numel()
+    d2h = ho.numel() * 4
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(e2e_steps):
         c = caches[i % copies]
-        for l in range(L):
-            c.step_host_packed(l, packed[i % bank][l][0], with_ids, ho, stream=stream)
+        if L == 1:
+            c.step_host_packed(0, packed[i % bank], with_ids, ho[0], stream=stream)
+        else:
+            c.step_layers_host_packed(0, L, packed[i % bank], with_ids, ho, stream=stream)
     e1.record(stream)
     e1.synchronize()
     e2e_elapsed = e0.elapsed_time(e1) / 1e3

@@ -81,6 +81,7 @@ SIGNATURES = {
     "lk_decode_attn_static": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp]),
     "lk_step_host": (ctypes.c_int, [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lk_step_host_packed": (ctypes.c_int, [_vp, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
+    "lk_step_layers_host_packed": (ctypes.c_int, [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _sz, _vp]),
     "lk_cache_length": (ctypes.c_int, [_vp, _i32, ctypes.POINTER(_i32)]),
     "lk_cache_lengths": (ctypes.c_int, [_vp, _i32, _vp]),
     "lk_cache_region": (ctypes.c_int, [_vp, _i32, _i32, _i32, ctypes.POINTER(RegionInfo)]),
@@ -465,6 +466,20 @@ class Cache:
         _need(o, torch.float32, (self.batch, self.plan.num_q_heads, 128), "o", "cpu")
         _check(_lib.lk_step_host_packed(self._h, layer, host_in.data_ptr(), 1 if with_ids else 0, o.data_ptr(),
                                         self.workspace.data_ptr(), self.workspace.numel(), _stream(stream)))
+
+    def layers_packed_input_bytes(self, nlayers, with_ids):
+        B, Hq, H = self.batch, self.plan.num_q_heads, self.plan.num_kv_heads
+        return nlayers * B * (Hq + 2 * H) * 256 + (B * 4 if with_ids else 0)
+
+    def step_layers_host_packed(self, layer0, nlayers, host_in, with_ids, o, stream=None):
+        """lk_step_layers_host_packed: host_in is one pinned uint8 block
+        q (all layers) | k | v | ids; o pinned fp32 [nlayers, B, Hq, 128]."""
+        import torch
+        _need(host_in, torch.uint8, (self.layers_packed_input_bytes(nlayers, with_ids),), "host_in", "cpu")
+        _need(o, torch.float32, (nlayers, self.batch, self.plan.num_q_heads, 128), "o", "cpu")
+        _check(_lib.lk_step_layers_host_packed(self._h, layer0, nlayers, host_in.data_ptr(), 1 if with_ids else 0,
+                                               o.data_ptr(), self.workspace.data_ptr(), self.workspace.numel(),
+                                               _stream(stream)))
 
     # -- queries
     def length(self, layer):

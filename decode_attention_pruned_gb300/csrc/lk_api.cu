@@ -1141,6 +1141,26 @@ lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in
   return step_from_staging(cache, layer, has_ids != 0, o_host, workspace, ws_bytes, stream);
 }
 
+lk_status lk_step_layers_host_packed(lk_cache cache, int32_t layer0, int32_t nlayers, const void* host_in,
+                                     int32_t has_ids, float* o_host, void* workspace, size_t ws_bytes,
+                                     void* stream) {
+  if (!cache || !host_in || !o_host || !workspace)
+    return fail(LK_ERR_ARG, "lk_step_layers_host_packed: null argument");
+  if (nlayers < 1 || layer0 < 0 || layer0 + nlayers > cache->cv.L)
+    return fail(LK_ERR_ARG, "lk_step_layers_host_packed: layers %d .. %d out of range", layer0, layer0 + nlayers - 1);
+  const uint8_t* in = static_cast<const uint8_t*>(mapped_host(host_in));
+  float* od = static_cast<float*>(const_cast<void*>(mapped_host(o_host)));
+  if (!in || !od)
+    return fail(LK_ERR_ARG, "lk_step_layers_host_packed: host buffers must be page-locked and mapped");
+  const lk_plan_desc& d = cache->plan.d;
+  const size_t rows = (size_t)nlayers * cache->B;
+  const size_t qb = rows * d.num_q_heads * kHeadDim * 2, kvb = rows * d.num_kv_heads * kHeadDim * 2;
+  const int32_t* ids = has_ids ? reinterpret_cast<const int32_t*>(in + qb + 2 * kvb) : nullptr;
+  lk_status st = lk_append_layers(cache, layer0, nlayers, in + qb, in + qb + kvb, ids, stream);
+  if (st != LK_OK) return st;
+  return lk_decode_attn_layers(cache, layer0, nlayers, in, od, workspace, ws_bytes, stream);
+}
+
 lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n) {
   if (!cache || !n) return fail(LK_ERR_ARG, "lk_cache_length: null argument");
   if (layer < 0 || layer >= cache->cv.L) return fail(LK_ERR_ARG, "lk_cache_length: layer %d out of range", layer);

@@ -358,6 +358,21 @@ lk_status lk_step_host(lk_cache cache, int32_t layer, const void* q_host, const 
 lk_status lk_step_host_packed(lk_cache cache, int32_t layer, const void* host_in, int32_t has_ids,
                               float* o_host, void* workspace, size_t ws_bytes, void* stream);
 
+/* A step of layers layer0 .. layer0+nlayers-1 from host memory, as
+ * lk_append_layers + lk_decode_attn_layers: host_in = q bf16
+ * [nlayers][B][Hq][128] | k bf16 [nlayers][B][Hkv][128] | v (as k) | ids
+ * int32 [B] (present iff has_ids != 0; the same token for every layer),
+ * back to back; o_host fp32 [nlayers][B][Hq][128] out.  Both must be
+ * page-locked and mapped into the device's address space (the kernels read
+ * and write them in place over the host link); otherwise LK_ERR_ARG and
+ * nothing is launched.  Two launches whatever the step mode (the fused
+ * kernel stages the new token with bulk copies, which are kept away from
+ * host memory).  Errors as for lk_append_layers and lk_decode_attn_layers.
+ * Read o only after synchronising `stream`. */
+lk_status lk_step_layers_host_packed(lk_cache cache, int32_t layer0, int32_t nlayers, const void* host_in,
+                                     int32_t has_ids, float* o_host, void* workspace, size_t ws_bytes,
+                                     void* stream);
+
 /* Host-tracked token count of a layer: the longest sequence's length. */
 lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n);
 

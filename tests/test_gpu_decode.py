@@ -324,3 +324,36 @@ def test_query_group_sizes(cuda, hq, hkv, kv):
     o = case.cache.decode(0, q)
     case.cache.check()
     assert _max_err(o, case.expected(0, q, 1701)) <= DECODE_TOL
+
+
+def test_step_layers_host_packed_matches_device_path(cuda):
+    # every layer's step from one mapped pinned block (q of all layers | k |
+    # v | ids): the append and decode launches of the device path, read and
+    # written in place, so outputs and cache bytes are identical
+    w = FASTGEN.scaled(num_layers=3, batch=2, context=500, policy_counts=(6, 4, 14))
+    a = Case(w, total=502)
+    b = Case(w, total=502)
+    a.cache.set_step_mode(lkb.STEP_SPLIT)
+    L, N = w.num_layers, 500
+    for case in (a, b):
+        for layer in range(L):
+            case.prefill(layer, N)
+    qs = torch.stack([a.q(layer, N + 1) for layer in range(L)]).contiguous()
+    ks = torch.stack([a.history(layer)[0][:, N] for layer in range(L)]).contiguous()
+    vs = torch.stack([a.history(layer)[1][:, N] for layer in range(L)]).contiguous()
+    ids = a.ids[:, N].contiguous()
+    o_dev = a.cache.step_layers(0, qs, ks, vs, ids)
+    blk = torch.cat([t.cpu().contiguous().view(torch.uint8).reshape(-1) for t in (qs, ks, vs, ids)]).pin_memory()
+    o_host = torch.empty(o_dev.shape, dtype=torch.float32).pin_memory()
+    b.cache.step_layers_host_packed(0, L, blk, True, o_host)
+    torch.cuda.synchronize()
+    b.cache.check()
+    assert torch.equal(o_host, o_dev.cpu())
+    for layer in range(L):
+        assert float(np.abs(o_host[layer].double().numpy() - a.expected(layer, qs[layer], N + 1)).max()) <= DECODE_TOL
+    assert torch.equal(a.cache.buffer, b.cache.buffer)
+    # pageable buffers are refused before anything is launched
+    with pytest.raises(lkb.LeankError) as e:
+        b.cache.step_layers_host_packed(0, L, blk.clone(), True, torch.empty_like(o_host))
+    assert e.value.status == lkb.LK_ERR_ARG
+    assert list(b.cache.lengths(0)) == [N + 1, N + 1]
