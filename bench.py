@@ -63,7 +63,8 @@ COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 # the multi-pass sections; their entries scale the 4-layer capture's
 # traffic per algorithmic byte to the full launch's algorithmic bytes (the
 # 2- and 4-layer captures give 1.0108 and 1.0059 of the algorithmic bytes
-# for serving_b64, 1.0200 and 1.0148 for fastgen_mix).
+# for serving_b64, 1.0200 and 1.0148 for fastgen_mix; with INT8 middles
+# 1.0145 and 1.0086, 1.0378 and 1.0234).
 NCU_TRAFFIC = {
     "69f4f2651982a365:llama31_8b_layer:bf16:fused": 86260992 + 2471424,
     "69f4f2651982a365:qwen25_7b_long:bf16:fused": 513990656 + 3203840,
@@ -74,6 +75,13 @@ NCU_TRAFFIC = {
     "69f4f2651982a365:fastgen_mix/4L:bf16:fused": 864369920 + 3672064,
     "69f4f2651982a365:serving_b64:bf16:decode": 19795624561,
     "69f4f2651982a365:fastgen_mix:bf16:fused": 10545616751,
+    "69f4f2651982a365:llama31_8b_layer:int8:decode": 46448384 + 1536,
+    "69f4f2651982a365:serving_b64/2L:int8:decode": 634033664 + 4177664,
+    "69f4f2651982a365:serving_b64/4L:int8:decode": 1420505344 + 4938240,
+    "69f4f2651982a365:fastgen_mix/2L:int8:decode": 262525696 + 3104768,
+    "69f4f2651982a365:fastgen_mix/4L:int8:decode": 511828480 + 3425280,
+    "69f4f2651982a365:serving_b64:int8:decode": 12655465598,
+    "69f4f2651982a365:fastgen_mix:int8:decode": 6019713306,
 }
 
 
