@@ -83,6 +83,8 @@ NCU_TRAFFIC = {
     "69f4f2651982a365:serving_b64:int8:decode": 12655465598,
     "69f4f2651982a365:fastgen_mix:int8:decode": 6019713306,
 }
+# entries scaled from a smaller capture of the same workload (see above)
+NCU_TRAFFIC_SCALED = {"serving_b64", "fastgen_mix"}
 
 
 def _rank_env():
@@ -448,7 +450,10 @@ def run_gpu(args, rank, local_rank, world):
         },
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": traffic, "peak_source": peak_kind, "kernel": kernel_name,
+            "traffic": traffic,
+            "traffic_source": None if traffic is None else
+            ("4-layer ncu capture scaled by algorithmic bytes" if wkey in NCU_TRAFFIC_SCALED else "ncu capture"),
+            "peak_source": peak_kind, "kernel": kernel_name,
             "kernel_ms": kernel_s * 1e3, "alg_bytes_per_launch": alg_bytes,
             "timed_launches": K if fused else reps * n_kg, "kernel_timing": kernel_timing,
             "decode_only_kernel_ms": kdur * 1e3,
