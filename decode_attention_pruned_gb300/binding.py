@@ -87,6 +87,7 @@ SIGNATURES = {
     "lk_cache_region": (ctypes.c_int, [_vp, _i32, _i32, _i32, ctypes.POINTER(RegionInfo)]),
     "lk_resident_bytes": (ctypes.c_int, [_vp, _i32, _vp, ctypes.POINTER(_u64)]),
     "lk_set_decode_ctas": (ctypes.c_int, [_vp, _i32]),
+    "lk_set_wait_limit": (ctypes.c_int, [_vp, _u64]),
     "lk_check": (ctypes.c_int, [_vp, _vp]),
     "lk_last_error": (ctypes.c_char_p, []),
 }
@@ -499,6 +500,14 @@ class Cache:
 
     def set_decode_ctas(self, ctas):
         _check(_lib.lk_set_decode_ctas(self._h, ctas))
+
+    def workspace_init(self, stream=None):
+        """lk_workspace_init: zero this cache's workspace (after LK_ERR_TIMEOUT)."""
+        _check(_lib.lk_workspace_init(self._h, self.workspace.data_ptr(), self.workspace.numel(), _stream(stream)))
+
+    def set_wait_limit(self, ns):
+        """lk_set_wait_limit: bound of the decode kernel's waits (ns)."""
+        _check(_lib.lk_set_wait_limit(self._h, int(ns)))
 
     def check(self, stream=None):
         _check(_lib.lk_check(self._h, _stream(stream)))

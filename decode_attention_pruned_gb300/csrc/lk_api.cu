@@ -13,7 +13,6 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
-#include <mutex>
 #include <vector>
 
 #include "../../include/leank.h"
@@ -44,7 +43,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s bound on device waits
+constexpr uint64_t kWaitLimitNs = 1000000000ull;      // 1 s bound on device waits
+constexpr uint64_t kMaxWaitLimitNs = 10000000000ull;  // lk_set_wait_limit: at most 10 s
 constexpr int64_t kMaxPoolRows = (1ll << 31) - 2 * kTmaBoxRows;
 
 }  // namespace
@@ -312,30 +312,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // until the process exits; all calls share it.
 namespace {
 constexpr size_t kStaticScratchBytes = 8u << 20;
-constexpr int kStaticMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
-std::mutex g_scratch_mutex;
-void* g_scratch_addr[kStaticMaxDevices] = {};
 
-// Device address of g_decode_scratch on the current device, looked up (and
-// zeroed) once per device.  Host code must not use the symbol itself: on the
-// host it names a stand-in, not device memory.
+// Device address of g_decode_scratch in the current device's context.  Host
+// code must not use the symbol itself: on the host it names a stand-in, not
+// device memory.  The lookup allocates nothing and is repeated on every call,
+// so a context that was torn down and created again (cudaDeviceReset) never
+// leaves a stale address behind.  Nothing is cleared here: each call zeroes
+// its counters on its own stream, and every partial is written before it is
+// read.
 lk_status static_scratch(void** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static: cudaGetDevice");
-  if (dev < 0 || dev >= kStaticMaxDevices)
-    return fail(LK_ERR_UNSUPPORTED, "lk_decode_attn_static: device %d >= %d", dev, kStaticMaxDevices);
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
-    void* ptr = nullptr;
-    err = cudaGetSymbolAddress(&ptr, g_decode_scratch);
-    if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static: cudaGetSymbolAddress");
-    err = cudaMemset(ptr, 0, kStaticScratchBytes);
-    if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static: scratch clear");
-    g_scratch_addr[dev] = ptr;
-  }
-  *out = g_scratch_addr[dev];
+  void* ptr = nullptr;
+  cudaError_t err = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+  if (err != cudaSuccess) return cuda_fail(err, "lk_decode_attn_static: cudaGetSymbolAddress");
+  *out = ptr;
   return LK_OK;
 }
 }  // namespace
@@ -376,6 +366,7 @@ struct lk_cache_s {
   }
   DecodeMaps maps;
   int device = 0, num_sms = 0, decode_ctas = 0, step_mode = LK_STEP_AUTO;
+  uint64_t wait_limit_ns = kWaitLimitNs;   // decode ring and segment waits
   std::vector<uint8_t> upload;     // host image of the tables (kept alive for the async copy)
 };
 
@@ -947,7 +938,7 @@ lk_status decode_prepare(lk_cache cache, int32_t layer0, int32_t nlayers, const 
   a.part = reinterpret_cast<float*>(ws + w.off_part);
   a.part_ml = reinterpret_cast<float2*>(ws + w.off_ml);
   a.counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
-  a.wait_limit_ns = kWaitLimitNs;
+  a.wait_limit_ns = cache->wait_limit_ns;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
   a.k_new = a.v_new = nullptr;
   a.ids = nullptr;
@@ -1052,12 +1043,19 @@ static const void* mapped_host(const void* p) {
 // q, k, v, ids from host memory and write o there over the host link (on
 // Grace, NVLink-C2C), with no staging copies.  Always the append and decode
 // launches: the fused kernel loads the new token with bulk copies, which
-// this path keeps away from host memory.
+// this path keeps away from host memory.  The decode launch is checked
+// before the append commits the token.
 static lk_status step_in_place(lk_cache cache, int32_t layer, const void* q, const void* k, const void* v,
                                const int32_t* ids, float* o, void* workspace, size_t ws_bytes, void* stream) {
-  lk_status st = lk_append_layers(cache, layer, 1, k, v, ids, stream);
+  DecodeArgs a;
+  int ctas = 0;
+  lk_status st = decode_prepare(cache, layer, 1, q, o, workspace, ws_bytes, "lk_step_host", a, ctas);
   if (st != LK_OK) return st;
-  return lk_decode_attn_layers(cache, layer, 1, q, o, workspace, ws_bytes, stream);
+  st = lk_append_layers(cache, layer, 1, k, v, ids, stream);
+  if (st != LK_OK) return st;
+  cudaError_t err = launch_decode(cache->maps, a, ctas, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_step_host decode launch");
+  return LK_OK;
 }
 
 // Append + decode from the inputs staged in the workspace, then copy o back.
@@ -1156,9 +1154,18 @@ lk_status lk_step_layers_host_packed(lk_cache cache, int32_t layer0, int32_t nla
   const size_t rows = (size_t)nlayers * cache->B;
   const size_t qb = rows * d.num_q_heads * kHeadDim * 2, kvb = rows * d.num_kv_heads * kHeadDim * 2;
   const int32_t* ids = has_ids ? reinterpret_cast<const int32_t*>(in + qb + 2 * kvb) : nullptr;
-  lk_status st = lk_append_layers(cache, layer0, nlayers, in + qb, in + qb + kvb, ids, stream);
+  // every check of the decode launch (workspace size and alignment, q and o
+  // alignment) before the append, which commits the token
+  DecodeArgs a;
+  int ctas = 0;
+  lk_status st = decode_prepare(cache, layer0, nlayers, in, od, workspace, ws_bytes, "lk_step_layers_host_packed",
+                                a, ctas);
   if (st != LK_OK) return st;
-  return lk_decode_attn_layers(cache, layer0, nlayers, in, od, workspace, ws_bytes, stream);
+  st = lk_append_layers(cache, layer0, nlayers, in + qb, in + qb + kvb, ids, stream);
+  if (st != LK_OK) return st;
+  cudaError_t err = launch_decode(cache->maps, a, ctas, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "lk_step_layers_host_packed decode launch");
+  return LK_OK;
 }
 
 lk_status lk_cache_length(lk_cache cache, int32_t layer, int32_t* n) {
@@ -1288,6 +1295,15 @@ lk_status lk_step_is_fused(lk_cache cache, int32_t layer0, int32_t nlayers, int3
   return LK_OK;
 }
 
+lk_status lk_set_wait_limit(lk_cache cache, uint64_t ns) {
+  if (!cache) return fail(LK_ERR_ARG, "lk_set_wait_limit: null cache");
+  if (ns > kMaxWaitLimitNs)
+    return fail(LK_ERR_ARG, "lk_set_wait_limit: %llu ns exceeds %llu ns", (unsigned long long)ns,
+                (unsigned long long)kMaxWaitLimitNs);
+  cache->wait_limit_ns = ns;
+  return LK_OK;
+}
+
 lk_status lk_set_decode_ctas(lk_cache cache, int32_t ctas) {
   if (!cache) return fail(LK_ERR_ARG, "lk_set_decode_ctas: null cache");
   if (ctas < 0 || ctas > kMaxCtas) return fail(LK_ERR_ARG, "lk_set_decode_ctas: %d out of [0, %d]", ctas, kMaxCtas);
@@ -1347,7 +1363,7 @@ lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, fl
   a.part = reinterpret_cast<float*>(ws + w.off_part);
   a.part_ml = reinterpret_cast<float2*>(ws + w.off_ml);
   a.counters = reinterpret_cast<int32_t*>(ws + w.off_counters);
-  a.wait_limit_ns = kWaitLimitNs;
+  a.wait_limit_ns = cache->wait_limit_ns;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
   a.k_new = a.v_new = nullptr;
   a.ids = nullptr;

@@ -38,6 +38,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -45,8 +58,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Wait for the phase of `parity` to complete, giving up after `limit_ns`.
-// Returns false on time-out (the caller records it and leaves).
+// Returns false on time-out (the caller records it and leaves).  A limit of
+// 0 does not wait at all: one non-blocking test (the failure path's tests
+// use it to make a wait run out for certain).
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns == 0) return mbar_test_wait(bar, parity);
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {

@@ -293,12 +293,14 @@ lk_status lk_decode_attn(lk_cache cache, int32_t layer, const void* q, float* o,
  *   q, o  as for lk_decode_attn.
  * Limit: the split scratch of the cache (about (256 + B*Hkv) * G * 520
  * bytes) must fit in 8 MiB, else LK_ERR_CAPACITY and nothing is enqueued.
- * The first call on a device looks up the array's device address and zeroes
- * it (synchronously); make that first call before any stream capture.  Each
- * call then clears the split counters on `stream` before its launch.  All
- * calls share the one array and it keeps the last call's contents: calls
- * that overlap on the GPU (other streams, other threads) race and give wrong
- * results. */
+ * Every call looks up the array's device address in the current context
+ * (cudaGetSymbolAddress, which allocates nothing); on the first call on a
+ * device that lookup may load the library's device code into the context,
+ * so make that first call before any stream capture.  Each call clears the
+ * split counters on `stream` before its launch; the partials need no
+ * clearing (each is written before it is read).  All calls share the one
+ * array and it keeps the last call's contents: calls that overlap on the GPU
+ * (other streams, other threads) race and give wrong results. */
 lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, float* o, void* stream);
 
 /* lk_append over layers layer0 .. layer0+nlayers-1 in one launch:
@@ -409,6 +411,15 @@ lk_status lk_step_is_fused(lk_cache cache, int32_t layer0, int32_t nlayers, int3
  * (sequence, kv head) entries, where fewer, longer streams reach a higher
  * HBM rate); for tuning and split-invariance tests.  Must be <= 256. */
 lk_status lk_set_decode_ctas(lk_cache cache, int32_t ctas);
+
+/* Bound of the decode kernel's waits on its stage ring and on its warps'
+ * segment barriers, in ns (default 1 s; at most 10 s).  A wait that runs out
+ * records LK_ERR_TIMEOUT for lk_check and the launch's outputs are garbage;
+ * after it, call lk_workspace_init before the next decode.  0 makes every
+ * wait that is not already complete run out at once: a way to exercise that
+ * failure path without a fault.  The kernel's final wait for its own copies
+ * to land keeps its 1 s bound whatever this is.  Errors: LK_ERR_ARG. */
+lk_status lk_set_wait_limit(lk_cache cache, uint64_t ns);
 
 /* Synchronise `stream`, read and clear the device status word.  Returns
  * LK_ERR_TIMEOUT, LK_ERR_CAPACITY or LK_ERR_ARG (bad token id) for a set

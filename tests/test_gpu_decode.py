@@ -8,6 +8,7 @@ import torch
 from decode_attention_pruned_gb300 import binding as lkb
 from decode_attention_pruned_gb300 import synth as S
 from helpers import DECODE_TOL, Case
+from oracle import masks as OM
 
 pytestmark = pytest.mark.gpu
 
@@ -282,8 +283,8 @@ def test_alignment_64_masks(cuda):
     # per-head kept counts rounded to multiples of 64 (the H100 setting of the
     # LeanK article's troubleshooting notes): widths 0, 64 and 128 only
     w = SERVING.scaled(num_layers=2, batch=2, context=900, tau=0.5)
-    alpha = S.draw_alpha(w)
-    masks = S.aligned_prune_masks(alpha, 60.0, align=64, budget="exact")
+    alpha = S.draw_alpha(w).astype(np.float32)
+    masks = OM.top_s_prune(alpha, 60.0, align=64, budget="exact")
     counts = masks.sum(-1)
     assert set(np.unique(counts)) <= {0, 64, 128} and len(set(np.unique(counts))) >= 2
     case = Case(w, total=901, masks=masks)
@@ -357,3 +358,67 @@ def test_step_layers_host_packed_matches_device_path(cuda):
         b.cache.step_layers_host_packed(0, L, blk.clone(), True, torch.empty_like(o_host))
     assert e.value.status == lkb.LK_ERR_ARG
     assert list(b.cache.lengths(0)) == [N + 1, N + 1]
+
+
+def test_bounded_wait_runs_out_and_the_cache_recovers(cuda):
+    # Failure path of the decode kernel, with no fault: a wait limit of 0
+    # makes every ring and segment wait that is not already complete run out
+    # (a CTA of 4 streams ~40 tiles through a ring of 3 to 5 stages, so the
+    # producer's first slot wait finds its oldest stage still in use).  The
+    # launch records LK_ERR_TIMEOUT; the producer still waits (bounded) for
+    # its own copies to land before its CTA exits.  With the limit back and
+    # the workspace zeroed, the next decode matches the oracle.
+    w = LLAMA.scaled(context=3000, batch=2)
+    masks = S.masks_with_counts(w, [32, 64, 0, 96, 128, 32, 32, 64])
+    case = Case(w, total=3000, masks=masks)
+    case.prefill(0, 3000)
+    case.cache.set_decode_ctas(4)
+    q = case.q(0, 3000)
+    case.cache.set_wait_limit(0)
+    case.cache.decode(0, q)
+    with pytest.raises(lkb.LeankError) as e:
+        case.cache.check()
+    assert e.value.status == lkb.LK_ERR_TIMEOUT
+    case.cache.check()                        # the status word was cleared
+    case.cache.set_wait_limit(10 ** 9)
+    case.cache.workspace_init()
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    assert _max_err(o, case.expected(0, q, 3000)) <= DECODE_TOL
+    with pytest.raises(lkb.LeankError) as e:
+        case.cache.set_wait_limit(11 * 10 ** 9)
+    assert e.value.status == lkb.LK_ERR_ARG
+
+
+def test_host_step_is_refused_before_the_append(cuda):
+    # a workspace too small for the decode is refused before the append, so
+    # no token is committed (lengths and cache bytes unchanged)
+    import ctypes
+    w = FASTGEN.scaled(num_layers=2, batch=2, context=300, policy_counts=(1, 1, 14))
+    case = Case(w, total=301)
+    L, N = w.num_layers, 300
+    for layer in range(L):
+        case.prefill(layer, N)
+    qs = torch.stack([case.q(layer, N + 1) for layer in range(L)]).contiguous()
+    ks = torch.stack([case.history(layer)[0][:, N] for layer in range(L)]).contiguous()
+    vs = torch.stack([case.history(layer)[1][:, N] for layer in range(L)]).contiguous()
+    ids = case.ids[:, N].contiguous()
+    blk = torch.cat([t.cpu().contiguous().view(torch.uint8).reshape(-1) for t in (qs, ks, vs, ids)]).pin_memory()
+    o_host = torch.empty((L, w.batch, w.num_q_heads, 128), dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    before = case.cache.buffer.clone()
+    lib = lkb.load()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = lib.lk_step_layers_host_packed(case.cache._h, 0, L, blk.data_ptr(), 1, o_host.data_ptr(),
+                                        case.cache.workspace.data_ptr(), 256, s)
+    assert st == lkb.LK_ERR_CAPACITY
+    # one layer from mapped host buffers, with a misaligned o
+    o1 = torch.empty(w.batch * w.num_q_heads * 128 + 4, dtype=torch.float32).pin_memory()
+    st = lib.lk_step_host_packed(case.cache._h, 0, blk.data_ptr(), 0, o1.data_ptr() + 4,
+                                 case.cache.workspace.data_ptr(), case.cache.workspace.numel(), s)
+    assert st == lkb.LK_ERR_ALIGN
+    torch.cuda.synchronize()
+    case.cache.check()
+    for layer in range(L):
+        assert list(case.cache.lengths(layer)) == [N] * w.batch
+    assert torch.equal(case.cache.buffer, before)

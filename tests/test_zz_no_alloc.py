@@ -20,6 +20,35 @@ from helpers import DECODE_TOL, Case
 pytestmark = pytest.mark.gpu
 
 
+def test_static_scratch_first_call_on_a_side_stream_and_a_later_layer(cuda):
+    # Kept first in this file, so that in a run of the whole suite (and in a
+    # fresh process) it makes the process's first call of this entry point:
+    # on a non-blocking stream (nothing orders it after work on the legacy
+    # default stream) and on layer 1 of a two-layer cache (entries and split
+    # slots of a launch count from its first layer).  Two calls in a row.
+    w = S.WORKLOADS[2].scaled(num_layers=2, batch=3, context=900)
+    case = Case(w, total=902)
+    for layer in range(2):
+        case.prefill(layer, 900)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    for t in (900, 901):
+        for layer in range(2):
+            case.append(layer, t)
+        q = case.q(1, t + 1, step=t)
+        o_ws = case.cache.decode(1, q)
+        torch.cuda.synchronize()
+        o_st = torch.full_like(o_ws, float("nan"))
+        with torch.cuda.stream(side):
+            case.cache.decode_static(1, q, o_st, stream=side)
+        side.synchronize()
+        case.cache.check(stream=side)
+        err = float((o_st.double() - o_ws.double()).abs().max())
+        assert err <= DECODE_TOL, err
+        ref = case.expected(1, q, t + 1)
+        assert float(np.abs(o_st.double().cpu().numpy() - ref).max()) <= DECODE_TOL
+
+
 def test_static_scratch_matches_workspace_path_twice(cuda):
     w = S.WORKLOADS[1].scaled(context=2600, batch=2)
     masks = S.masks_with_counts(w, [0, 32, 64, 96, 128, 32, 0, 64])
