@@ -1,9 +1,10 @@
 """Seeded synthetic inputs for decode attention over a LeanK-pruned KV cache.
 
-This module only draws inputs: workload shapes, channel masks, per-head
-policies, token ids, and the bf16 Q/K/V tensors.  It computes no attention,
-no cache layout and no byte count; the CUDA path and the fp64 oracle both
-consume what it returns and nothing else is shared between them.
+This module only draws inputs: workload shapes, channel importances (the
+input of LeanK's mask construction) or drawn kept counts, per-head policies,
+token ids, and the bf16 Q/K/V tensors.  It computes no mask threshold, no
+attention, no cache layout and no byte count; the CUDA path and the fp64
+oracle both consume what it returns and nothing else is shared between them.
 
 Sources of the workload shapes (page titles as cited throughout the repo):
   * "LeanK pruning technique analysis" (framerc.cn), §1: Llama-3.1-8B serving
@@ -66,8 +67,9 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads.  Index 0 is the tiny case; index 1 is the
-# Llama-3.1-8B-shaped layer that throughput is quoted on.
+# The five workloads.  Index 0 is the tiny case; index 2, the 32-layer
+# batch-64 serving step, is the largest one and the default of the throughput
+# measurement.
 WORKLOADS = [
     Workload("tiny", num_layers=1, batch=1, num_q_heads=4, num_kv_heads=2, context=512,
              sink=4, local=64, seed=1001, budget="choice64"),
@@ -105,59 +107,6 @@ def draw_alpha(w: Workload) -> np.ndarray:
     return np.exp(z + w.tau * u)
 
 
-def aligned_prune_masks(alpha: np.ndarray, prune_pct: float, align: int = 32,
-                        budget: str = "round_down",
-                        eligible: Optional[np.ndarray] = None) -> np.ndarray:
-    """Binary mask beta[l,h,c] from importance alpha (LeanK §2.2, stage 2).
-
-    A global threshold keeps the channels whose alpha is at or above the
-    ``prune_pct`` percentile of all eligible alphas.  Each head's kept count is
-    then brought to a multiple of ``align``: rounded down (``round_down``), or
-    rounded down and topped up by ``align`` on the heads with the largest
-    remainders until the total equals the aligned global budget (``exact``).
-    A head keeps its ``n_keep`` channels of largest alpha; equal alphas go to
-    the lower channel index.  Heads not ``eligible`` get an all-ones row (their
-    mask is unused by the cache).
-    """
-    L, H, D = alpha.shape
-    if eligible is None:
-        eligible = np.ones((L, H), dtype=bool)
-    vals = alpha[eligible]
-    thr = np.percentile(vals.reshape(-1), prune_pct)
-    above = (alpha >= thr).sum(axis=-1)
-    n_keep = (above // align) * align
-    if budget == "exact":
-        n_heads = int(eligible.sum())
-        target = align * int(round((1.0 - prune_pct / 100.0) * n_heads * D / align))
-        deficit = target - int(n_keep[eligible].sum())
-        rem = np.where(eligible, above - n_keep, -1)
-        flat_order = np.argsort(-rem.reshape(-1), kind="stable")
-        while deficit > 0:
-            progressed = False
-            for idx in flat_order:
-                l, h = divmod(int(idx), H)
-                if not eligible[l, h] or n_keep[l, h] + align > D:
-                    continue
-                n_keep[l, h] += align
-                deficit -= align
-                progressed = True
-                if deficit <= 0:
-                    break
-            if not progressed:
-                break
-    elif budget != "round_down":
-        raise ValueError(budget)
-    mask = np.zeros((L, H, D), dtype=np.uint8)
-    for l in range(L):
-        for h in range(H):
-            if not eligible[l, h]:
-                mask[l, h, :] = 1
-                continue
-            order = np.argsort(-alpha[l, h], kind="stable")
-            mask[l, h, order[: int(n_keep[l, h])]] = 1
-    return mask
-
-
 def make_policies(w: Workload) -> np.ndarray:
     """Per (layer, kv head) policy ids; exact counts by a seeded permutation."""
     L, H = w.num_layers, w.num_kv_heads
@@ -171,25 +120,27 @@ def make_policies(w: Workload) -> np.ndarray:
     return flat[perm].reshape(L, H)
 
 
-def make_masks(w: Workload, policies: Optional[np.ndarray] = None) -> np.ndarray:
-    """uint8 [L, Hkv, 128] kept-channel masks for the workload."""
+def stage2_inputs(w: Workload, policies: Optional[np.ndarray] = None):
+    """What LeanK's stage 2 builds a pruned workload's mask from: the
+    importances alpha [L, Hkv, 128] (float32) and the heads that take a mask
+    (FULL policy), bool [L, Hkv].  With ``w.prune_pct``, ``w.align`` and
+    ``w.budget`` these fully determine the mask; this module does not build
+    it (the library's mask builder does, and so does the oracle)."""
     if policies is None:
         policies = make_policies(w)
-    alpha = draw_alpha(w)
+    return draw_alpha(w).astype(np.float32), np.asarray(policies) == POLICY_FULL
+
+
+def drawn_counts(w: Workload) -> np.ndarray:
+    """Kept-channel counts [L, Hkv] of a workload whose counts are drawn
+    rather than derived from a prune ratio: the tiny case draws 0 or 64 per
+    head (seeded); a workload without a prune ratio keeps all 128."""
     if w.budget == "choice64":
-        # tiny case: each head keeps 0 or 64 channels (seeded), the top-64 by alpha
         r = rng(w.seed, 0, STREAM_POLICY + 100)
-        ks = r.choice([0, 64], size=(w.num_layers, w.num_kv_heads))
-        mask = np.zeros(alpha.shape, dtype=np.uint8)
-        for l in range(w.num_layers):
-            for h in range(w.num_kv_heads):
-                order = np.argsort(-alpha[l, h], kind="stable")
-                mask[l, h, order[: int(ks[l, h])]] = 1
-        return mask
+        return r.choice([0, 64], size=(w.num_layers, w.num_kv_heads))
     if w.prune_pct is None:
-        return np.ones(alpha.shape, dtype=np.uint8)
-    return aligned_prune_masks(alpha, w.prune_pct, w.align, w.budget,
-                               eligible=(policies == POLICY_FULL))
+        return np.full((w.num_layers, w.num_kv_heads), w.head_dim)
+    raise ValueError(f"{w.name}: counts follow from the prune ratio (stage 2), not from a draw")
 
 
 def masks_with_counts(w: Workload, counts) -> np.ndarray:

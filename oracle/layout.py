@@ -55,8 +55,3 @@ def region_b(policy: int, n_kept: int, N: int, S: int, W: int):
         return np.arange(0, dtype=np.int64), np.arange(0, dtype=np.int64)
     toks = np.arange(S, max(S, N - W))
     return (toks - S).astype(np.int64), toks.astype(np.int64)
-
-
-def special_count(special_flags, N: int) -> int:
-    """Number of special tokens among the first N (FastGen §3.2)."""
-    return int(np.asarray(special_flags[:N], dtype=bool).sum())

@@ -26,6 +26,7 @@ from __future__ import annotations
 import numpy as np
 
 from .attention import decode_head
+from .footprint import resident_bytes as _resident_bytes_bf16
 
 BLOCK_ROWS = 128
 QMAX = 127
@@ -114,3 +115,19 @@ def decode_head_quantized(q, K, V, policy: int, kept, N: int, S: int, W: int, W_
     """``attention.decode_head`` over the quantised cache's values."""
     Kq, Vq = quantized_history(K, V, kept, policy, N, S, W)
     return decode_head(q, Kq, Vq, policy, kept, N, S, W, W_loc, special_flags)
+
+
+def resident_bytes_quantized(policy: int, n_kept: int, N: int, S: int, W: int, W_loc: int,
+                             n_special: int = 0, head_dim: int = 128) -> int:
+    """Bytes one decode step reads for one (b, kv head) of a cache whose
+    complete middle blocks are quantised: the bf16 bytes of every row that is
+    not in a sealed block (sinks, window, LOCAL / SPECIAL rows, the open
+    middle block) plus, per sealed block, its int8 codes (128 x k for K,
+    128 x d for V, one byte each) and fp32 scales (k for K, 128 for V)."""
+    bf16 = _resident_bytes_bf16(policy, n_kept, N, S, W, W_loc, n_special, head_dim)
+    nb = sealed_blocks(n_kept, N, S, W) if policy == 0 and 0 < n_kept else 0
+    if nb == 0:
+        return bf16
+    mid_row_bf16 = (n_kept + head_dim) * 2
+    block = BLOCK_ROWS * (n_kept + head_dim) + 4 * (n_kept + BLOCK_ROWS)
+    return bf16 - nb * BLOCK_ROWS * mid_row_bf16 + nb * block

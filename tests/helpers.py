@@ -9,11 +9,22 @@ from decode_attention_pruned_gb300 import binding as lkb
 from decode_attention_pruned_gb300 import synth as S
 from oracle import attention as OA
 from oracle import layout as OL
+from oracle import masks as OM
 from oracle import quant as OQ
 
 # max |err| bound of the decode output against the fp64 oracle (bf16 inputs,
 # fp32 accumulation), as stated for this method's GPU path
 DECODE_TOL = 2e-3
+
+
+def workload_masks(w: S.Workload, policies=None) -> np.ndarray:
+    """The workload's kept-channel masks [L, Hkv, 128]: LeanK stage 2 (the
+    oracle's construction) on the seeded importances for a pruned workload,
+    else the drawn per-head counts (top channels by importance)."""
+    if w.prune_pct is None or w.budget == "choice64":
+        return S.masks_with_counts(w, S.drawn_counts(w))
+    alpha, elig = S.stage2_inputs(w, policies)
+    return OM.top_s_prune(alpha, w.prune_pct, w.align, w.budget, elig)
 
 
 def f64(t: torch.Tensor) -> np.ndarray:
@@ -33,7 +44,7 @@ class Case:
         self.w = w
         self.total = total
         self.policies = S.make_policies(w) if policies is None else np.asarray(policies, np.int32)
-        self.masks = S.make_masks(w, self.policies) if masks is None else np.asarray(masks, np.uint8)
+        self.masks = workload_masks(w, self.policies) if masks is None else np.asarray(masks, np.uint8)
         self.is_special = S.make_special_table(w)
         self.plan = lkb.Plan.for_workload(w, self.masks, self.policies, self.is_special,
                                           special_capacity=special_capacity)

@@ -9,6 +9,7 @@ import pytest
 
 from decode_attention_pruned_gb300 import binding as lkb
 from decode_attention_pruned_gb300 import synth as S
+from helpers import workload_masks
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -83,7 +84,7 @@ def test_plan_rejects_unsupported_shapes(lib):
 def test_plan_groups_heads_and_orders_kept_channels(lib):
     w = S.WORKLOADS[2]
     pol = S.make_policies(w)
-    masks = S.make_masks(w, pol)
+    masks = workload_masks(w, pol)
     plan = lkb.Plan.for_workload(w, masks, pol)
     for l, h in [(0, 0), (3, 5), (31, 7)]:
         p, k, kept = plan.head(l, h)
@@ -117,7 +118,7 @@ def test_cache_bytes_grow_with_capacity_and_width(lib):
 
 def test_workspace_bytes(lib):
     w = S.WORKLOADS[3]
-    plan = lkb.Plan.for_workload(w, S.make_masks(w), S.make_policies(w))
+    plan = lkb.Plan.for_workload(w, workload_masks(w), S.make_policies(w))
     n = plan.workspace_bytes(w.batch)
     E, G = w.batch * w.num_kv_heads, w.group
     assert n >= (256 + E) * G * 128 * 4
@@ -128,7 +129,7 @@ def test_cache_init_without_gpu_fails_cleanly(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     w = S.WORKLOADS[0]
-    plan = lkb.Plan.for_workload(w, S.make_masks(w), S.make_policies(w))
+    plan = lkb.Plan.for_workload(w, workload_masks(w), S.make_policies(w))
     buf = np.zeros(plan.cache_bytes(1, 64) + 256, dtype=np.uint8)
     addr = (buf.ctypes.data + 255) // 256 * 256
     h = ctypes.c_void_p()

@@ -114,3 +114,33 @@ def test_on_grid_history_decodes_exactly_like_plain_attention():
     d_o = np.abs(Q.decode_head_quantized(q, Kf, Vf, 0, kept, N, S, W, 0)
                  - OA.decode_head(q, Kf, Vf, 0, kept, N, S, W, 0)).max()
     assert 1e-6 < d_o < 0.05
+
+
+def test_quantized_resident_bytes_are_the_arrays_sizes():
+    # the closed form against the sizes of the representation itself: bf16
+    # rows outside sealed blocks plus, per sealed block, the int8 code arrays
+    # and fp32 scale arrays that middle_blocks builds
+    from oracle import footprint as F
+    rs = _rng(9)
+    S, W, d = 4, 16, 128
+    for k in (0, 32, 64, 96, 128):
+        for N in (1, S + W, S + W + 127, S + W + 128, S + W + 300, S + W + 512):
+            K = rs.standard_normal((N, d)).astype(np.float32)
+            V = rs.standard_normal((N, d)).astype(np.float32)
+            kept = np.arange(k)
+            blocks = Q.middle_blocks(K, V, kept, N, S, W)
+            sealed_rows = 128 * len(blocks)
+            n_full, n_mid = F.resident_tokens(0, k, N, S, W, 0)
+            if k == 128:                                  # dense head: no middle region of its own
+                n_full, n_mid = min(N, S + W), max(0, N - S - W)
+            arrays = sum(a.nbytes for blk in blocks for a in blk)
+            want = n_full * 2 * d * 2 + (n_mid - sealed_rows) * (k + d) * 2 + arrays
+            if k == 0:
+                want = n_full * 2 * d * 2
+            assert Q.resident_bytes_quantized(0, k, N, S, W, 0) == want, (k, N)
+    # a whole k = 128 block takes 132 / 256 of its bf16 bytes
+    assert Q.resident_bytes_quantized(0, 128, S + W + 128, S, W, 0) == \
+        (S + W) * 512 + 128 * 256 + 4 * 256
+    # other policies are untouched by quantisation
+    assert Q.resident_bytes_quantized(1, 0, 1000, S, W, 64) == F.resident_bytes(1, 0, 1000, S, W, 64)
+    assert Q.resident_bytes_quantized(2, 0, 1000, S, W, 64, n_special=9) == 9 * 512

@@ -4,35 +4,49 @@ import pytest
 import torch
 
 from decode_attention_pruned_gb300 import synth as S
+from helpers import workload_masks
 
 
 @pytest.mark.parametrize("w", S.WORKLOADS, ids=[w.name for w in S.WORKLOADS])
-def test_masks_are_aligned_and_deterministic(w):
+def test_workload_masks_are_aligned_and_deterministic(w):
+    # the masks every test and the bench use: stage 2 on the drawn
+    # importances (pruned workloads) or the drawn counts (the tiny case)
     pol = S.make_policies(w)
-    m1 = S.make_masks(w, pol)
-    m2 = S.make_masks(w, pol)
+    m1 = workload_masks(w, pol)
+    m2 = workload_masks(w, pol)
     assert m1.shape == (w.num_layers, w.num_kv_heads, w.head_dim)
     assert np.array_equal(m1, m2)
     counts = m1.sum(-1)
     assert np.all(counts % 32 == 0)
     assert set(np.unique(m1)) <= {0, 1}
+    if w.prune_pct is not None:
+        alpha, elig = S.stage2_inputs(w, pol)
+        assert alpha.dtype == np.float32 and np.array_equal(elig, pol == S.POLICY_FULL)
+
+
+def test_drawn_counts_of_the_tiny_case():
+    w = S.WORKLOADS[0]
+    c = S.drawn_counts(w)
+    assert c.shape == (1, 2) and set(np.unique(c)) <= {0, 64}
+    with pytest.raises(ValueError):
+        S.drawn_counts(S.WORKLOADS[1])
 
 
 def test_exact_budget_hits_the_aligned_target():
     for w in (S.WORKLOAD_BY_NAME["qwen25_7b_long"], S.WORKLOAD_BY_NAME["fastgen_mix"]):
         pol = S.make_policies(w)
-        m = S.make_masks(w, pol)
+        m = workload_masks(w, pol)
         full = pol == S.POLICY_FULL
-        target = 32 * round((1 - w.prune_pct / 100) * full.sum() * 128 / 32)
+        target = 32 * int(np.floor((1 - w.prune_pct / 100) * full.sum() * 128 / 32 + 0.5))
         assert m.sum(-1)[full].sum() == target
 
 
 def test_round_down_never_exceeds_threshold_count():
     w = S.WORKLOAD_BY_NAME["serving_b64"]
-    alpha = S.draw_alpha(w)
-    thr = np.percentile(alpha.reshape(-1), w.prune_pct)
+    alpha, _ = S.stage2_inputs(w)
+    thr = np.percentile(alpha.astype(np.float64).reshape(-1), w.prune_pct)
     above = (alpha >= thr).sum(-1)
-    m = S.make_masks(w)
+    m = workload_masks(w)
     assert np.all(m.sum(-1) == (above // 32) * 32)
     # kept channels are the head's largest alphas
     for l, h in [(0, 0), (5, 3), (31, 7)]:
@@ -82,6 +96,6 @@ def test_kv_shapes_outliers_and_rope():
 def test_mask_stats_report():
     w = S.WORKLOAD_BY_NAME["serving_b64"]
     pol = S.make_policies(w)
-    st = S.mask_stats(w, S.make_masks(w, pol), pol)
+    st = S.mask_stats(w, workload_masks(w, pol), pol)
     assert 0.7 <= st["prune_ratio"] <= 0.85
     assert 0.05 <= st["zero_head_fraction"] <= 0.35
