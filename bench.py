@@ -6,27 +6,34 @@ into K_prun) then the split-K decode with its in-launch combine, through
 lk_step_layers.  --step auto (default) lets the library choose between one
 fused launch and the append + decode launches (it fuses launches over few,
 long entries with a bf16 middle); --step fused / split force one.
-Default workload: the Llama-3.1-8B-shaped layer (32 q / 8 kv heads, d 128,
-batch 1, context 32768, sink 16, window 1024, 70 % channel pruning rounded
-down to multiples of 32, K with 4 channel pairs x8).
+Default workload: the batch-serving step (32 layers x 32 q / 8 kv heads,
+d 128, batch 64, context 4096, sink 16, window 512, 70 % channel pruning
+rounded down to multiples of 32), the largest single-GPU workload; the
+channel masks come from the library's mask builder (lk_build_masks) on the
+seeded importances.
 
-Timing rules: W untimed warm-up steps; exactly K timed steps bracketed by a
-barrier + synchronize; CUDA events on the launching stream; max over ranks.
-Inputs are larger than L2: the steps rotate over C copies of the cache whose
-resident bytes together exceed 4x L2, and C also bounds the context growth
-of the appends.  The step loop is captured in CUDA graphs (programmatic
-dependent launch between consecutive kernels).
+Timing rules: W untimed warm-up steps (at least one use of every cache copy
+and one replay of every captured graph, whatever W is); exactly K timed steps
+bracketed by a barrier + synchronize; CUDA events on the launching stream;
+max over ranks.  Inputs are larger than L2: the steps rotate over C copies of
+the cache whose resident bytes together exceed 4x L2, and C also bounds the
+context growth of the appends.  The step loop is captured in CUDA graphs
+(programmatic dependent launch between consecutive kernels).  Clocks are
+sampled over the loaded window: untimed decode-only replays that bring the
+GPU to its load clocks, then the timed steps.
 
 Printed: one JSON line (rank 0).  `value` = decode-attention calls/s of all
-ranks; `roofline` = the step's decode kernel (the fused one when the step is one
+ranks (a call = one layer's decode over every sequence and kv head);
+`roofline` = the step's decode kernel (the fused one when the step is one
 launch): algorithmic bytes / event-timed launch duration, against the HBM
 peak; `e2e` = the same metric through lk_step_host_packed (one layer) or
 lk_step_layers_host_packed (several) from pinned host memory, the host
-traffic inside the timed region;
-`cpu_baseline` = the fp64 oracle on a bounded sample on the host cores.
+traffic inside the timed region; `cpu_baseline` = the fp64 oracle on a
+bounded sample on all host cores (worker processes) and on one core.
 
 --impl reference times the oracle (the only reference this method has) on
-the host cores, on the same workload, one (sequence, kv head) per step.
+the host's cores, on the same workload: each step is one (sequence, kv head)
+unit per worker process.
 """
 from __future__ import annotations
 
@@ -55,6 +62,8 @@ UNIT = "calls/s"
 FALLBACK_HBM_GBS = 6800.0
 MAX_CONTEXT_GROWTH = 0.01           # appends may lengthen the context by at most 1 %
 COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
+MAX_COPIES = 256                    # rotating cache copies at most
+LOAD_SECONDS = 0.4                  # untimed decode replays before the timed steps
 
 # DRAM bytes (read + write) per decode launch from one ncu capture, keyed by
 # "<sha256[:16] of the decode kernel sources>:<workload>[/<layers>L]:<kv
@@ -184,6 +193,23 @@ def job_throughput(steps: int, layers: int, world: int, seconds: float) -> float
 # the GPU arm
 # ---------------------------------------------------------------------------
 
+def device_masks(w, pol, dev):
+    """The workload's kept-channel masks [L, Hkv, 128] (host uint8): LeanK
+    stage 2 by the library's mask builder on the seeded importances, or the
+    drawn counts of a workload without a prune ratio."""
+    import torch
+    from decode_attention_pruned_gb300 import binding as lkb
+    from decode_attention_pruned_gb300 import synth as S
+    if w.prune_pct is None or w.budget == "choice64":
+        return S.masks_with_counts(w, S.drawn_counts(w))
+    alpha, elig = S.stage2_inputs(w, pol)
+    a = torch.from_numpy(alpha).to(dev)
+    e = None if elig.all() else torch.from_numpy(elig.astype(np.uint8)).to(dev)
+    m = lkb.build_masks(a, w.prune_pct, align=w.align, exact=w.budget == "exact", eligible=e)
+    torch.cuda.synchronize(dev)
+    return m.cpu().numpy()
+
+
 def run_gpu(args, rank, local_rank, world):
     import torch
     from decode_attention_pruned_gb300 import binding as lkb
@@ -195,7 +221,7 @@ def run_gpu(args, rank, local_rank, world):
     w = S.WORKLOAD_BY_NAME[args.workload]
     N = w.context
     pol = S.make_policies(w)
-    masks = S.make_masks(w, pol)
+    masks = device_masks(w, pol, dev)
     spec = S.make_special_table(w)
     if args.layers:
         # a smaller case for profiling: the workload's first layers, with the
@@ -209,6 +235,9 @@ def run_gpu(args, rank, local_rank, world):
     W, K = args.warmup, args.steps
     e2e_steps = min(K, args.e2e_steps)
     kt_steps = min(K, args.kernel_steps)
+    # appends over all copies: the warm-up, the timed steps, the end-to-end
+    # steps, slack; every copy also takes up to 3 in the warm-up's first
+    # rotations (eager step, graph replay, remainder graph)
     appends = W + K + 2 * e2e_steps + 8
 
     # one copy first, to size the rest
@@ -236,9 +265,9 @@ def run_gpu(args, rank, local_rank, world):
     torch.cuda.synchronize()
     resident = [first.resident_bytes(l) for l in range(L)]
     resident_step = sum(resident)
-    copies = max(1, math.ceil(4 * l2 / max(1, resident_step)), math.ceil(appends / max_growth))
-    copies = int(min(copies, max(1, COPY_BUDGET_BYTES // copy_bytes)))
-    growth = math.ceil(appends / copies) + 2
+    copies = max(1, math.ceil(4 * l2 / max(1, resident_step)), math.ceil(appends / max(1, max_growth - 3)))
+    copies = int(min(copies, MAX_COPIES, max(1, COPY_BUDGET_BYTES // copy_bytes)))
+    growth = math.ceil(appends / copies) + 6
     capacity = N + growth
     del first
     torch.cuda.empty_cache()
@@ -293,28 +322,53 @@ def run_gpu(args, rank, local_rank, world):
                 enqueue_step(start + j)
         return g
 
-    # warm-up: eager steps (also the first use of every cache copy), then graphs
+    # warm-up: one eager step on every cache copy (its first use), then one
+    # replay of every captured graph (their uploads), then the rest of W
     with torch.cuda.stream(stream):
-        for i in range(min(W, copies)):
+        for i in range(copies):
             enqueue_step(i)
     stream.synchronize()
     for c in caches:
         c.check(stream)
-    done = min(W, copies)
-    full_graph = capture(copies, 0) if K >= copies or W > copies else None
+    full_graph = capture(copies, 0)
     rem = K % copies
     rem_graph = capture(rem, 0) if rem else None
-    # graph capture records the steps; the host lengths advanced by the capture
-    # are not device lengths -- re-sync by reading them back is unnecessary as
-    # the device-side counts drive the kernels.
-    warm_left = W - done
+    # (capture only records the steps: the kernels read the device lengths,
+    # which only executed steps advance)
     with torch.cuda.stream(stream):
-        while warm_left >= copies and full_graph is not None:
+        full_graph.replay()
+        if rem_graph is not None:
+            rem_graph.replay()
+        warm_done = 2 * copies + rem
+        while warm_done < W:
             full_graph.replay()
-            warm_left -= copies
-        for i in range(warm_left):
-            enqueue_step(done + i)
+            warm_done += copies
     stream.synchronize()
+    for c in caches:
+        c.check(stream)
+
+    # decode-only graph: back-to-back decode launches over the rotating
+    # copies (no append between; the lengths stay put).  Its replays load
+    # the GPU before the timed steps (so the clock samples show it under
+    # load) and, after them, time the decode kernel alone.
+    n_kg = min(max(kt_steps, 1), max(copies, 8))
+    kgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(kgraph, stream=stream):
+        for i in range(n_kg):
+            caches[i % copies].decode_layers(0, gq[i % bank], outs[i % copies], stream=stream)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        kgraph.replay()                        # upload
+        k0.record(stream)
+        kgraph.replay()
+        k1.record(stream)
+    k1.synchronize()
+    t_kg = max(1e-6, k0.elapsed_time(k1) / 1e3)
+    load_reps = int(min(20000, max(1, math.ceil(LOAD_SECONDS / t_kg))))
+    # resident bytes of the timed steps: every copy holds the same lengths
+    # (the steps rotate over them), which grow by at most one token per copy
+    # and rotation; the launches' mean is the mean of the two ends
+    res_before = sum(caches[0].resident_bytes(l, stream=stream) for l in range(L))
 
     dist = None
     if world > 1:
@@ -324,6 +378,9 @@ def run_gpu(args, rank, local_rank, world):
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            for _ in range(load_reps):
+                kgraph.replay()
         ev0.record(stream)
         with torch.cuda.stream(stream):
             for _ in range(K // copies):
@@ -338,22 +395,14 @@ def run_gpu(args, rank, local_rank, world):
         elapsed = max_over_ranks(elapsed, dist, dev)
     for c in caches:
         c.check(stream)
+    res_after = sum(caches[K % copies].resident_bytes(l, stream=stream) for l in range(L))
+    resident_step = (res_before + res_after) / 2
 
-    # decode kernel duration: a graph of back-to-back decode launches over the
-    # rotating copies (no append between; the lengths stay put), CUDA events
-    # around its replays on the launching stream, divided by the launches.
-    # Event pairs around single launches are also reported: they add each
-    # launch's front-end latency, so they understate the kernel's rate.
-    n_kg = min(kt_steps, max(copies, 8))
-    kgraph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(kgraph, stream=stream):
-        for i in range(n_kg):
-            caches[i % copies].decode_layers(0, gq[i % bank], outs[i % copies], stream=stream)
+    # the decode kernel alone: kgraph replays, CUDA events around them on the
+    # launching stream, divided by the launches.  Event pairs around single
+    # launches are also reported: they add each launch's front-end latency,
+    # so they understate the kernel's rate.
     reps = max(3, kt_steps // n_kg)
-    with torch.cuda.stream(stream):
-        kgraph.replay()
-    stream.synchronize()
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     k0.record(stream)
     with torch.cuda.stream(stream):
         for _ in range(reps):
@@ -361,6 +410,7 @@ def run_gpu(args, rank, local_rank, world):
     k1.record(stream)
     k1.synchronize()
     kdur = k0.elapsed_time(k1) / 1e3 / (reps * n_kg)
+    res_kernel = sum(caches[0].resident_bytes(l, stream=stream) for l in range(L))
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(kt_steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(kt_steps)]
     with torch.cuda.stream(stream):
@@ -370,7 +420,7 @@ def run_gpu(args, rank, local_rank, world):
             c.decode_layers(0, gq[i % bank], outs[i % copies], stream=stream)
             ends[i].record(stream)
     stream.synchronize()
-    kdur_isolated = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3
+    kdur_isolated = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)) / 1e3 if kt_steps else kdur
 
     # end to end from pinned host memory: each step's inputs sit in one host
     # block, read in place by the kernels (lk_step_host_packed: q | k | v |
@@ -406,17 +456,19 @@ def run_gpu(args, rank, local_rank, world):
     for c in caches:
         c.check(stream)
 
-    # algorithmic bytes of one decode launch (every layer of copy 0 at its
-    # length): resident K/V, q in, o out; a fused launch also reads the new
-    # token's K, V and writes them into the window (1 KiB per layer, sequence
-    # and kv head; the evicted row's move into the middle is not counted)
-    alg_bytes = resident_step + L * B * w.num_q_heads * 128 * (2 + 4)
+    # algorithmic bytes of one decode launch (every layer at the timed
+    # launches' lengths): resident K/V, q in, o out; a fused launch also reads
+    # the new token's K, V and writes them into the window (1 KiB per layer,
+    # sequence and kv head; the evicted row's move into the middle is not
+    # counted)
+    qo_bytes = L * B * w.num_q_heads * 128 * (2 + 4)
     if fused:
-        alg_bytes += L * B * w.num_kv_heads * 1024
+        alg_bytes = resident_step + qo_bytes + L * B * w.num_kv_heads * 1024
         kernel_s = elapsed / K                 # one launch per step
         kernel_timing = "the timed step graph: one fused append + decode launch per step, events around it"
         kernel_name = "decode_kernel (fused append)"
     else:
+        alg_bytes = res_kernel + qo_bytes
         kernel_s = kdur
         kernel_timing = "graph of back-to-back decode launches over the rotating copies, events around it"
         kernel_name = "decode_kernel"
@@ -437,15 +489,19 @@ def run_gpu(args, rank, local_rank, world):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16" if kvf == lkb.KV_BF16 else "bf16 + int8 (middle blocks)",
-        "data": "synthetic (seeded; random K/V/q, seeded LeanK masks)",
+        "data": "synthetic (seeded K/V/q; LeanK masks from the library's mask builder on seeded importances)",
         "config": {
             **workload_config(w, args), "context_growth_max": growth,
-            "resident_bytes_per_call": resident_step // L, "effective_GBps": resident_step * K * world / elapsed / 1e9,
+            "resident_bytes_per_call": int(resident_step // L),
+            "effective_GBps": resident_step * K * world / elapsed / 1e9,
+            "warmup_steps_run": warm_done,
             "step_mode": args.step,
             "launches_per_step": "one fused append + decode (all layers)" if fused
             else "append (all layers) + decode (all layers)",
             "cache_copies": copies, "l2_policy": "inputs larger than L2 (rotating cache copies)",
             "cuda_graph": True, "pdl": True, "parallelism": f"replicas x{world}",
+            "clock_window": f"{load_reps} untimed decode-only graph replays ({load_reps * n_kg} launches), "
+                            "then the timed steps",
             "decode_ctas": args.decode_ctas or "library default",
         },
         "roofline": {
@@ -474,40 +530,138 @@ def run_gpu(args, rank, local_rank, world):
 # the oracle (CPU)
 # ---------------------------------------------------------------------------
 
+class _OracleUnits:
+    """The inputs of one workload's oracle units: one sequence of layer 0
+    (its dense history, q, special flags) and its kv heads.  A unit is the
+    decode of one (sequence, kv head); a call (the metric's unit) is
+    batch x kv heads units."""
+
+    def __init__(self, w_name, kv):
+        from decode_attention_pruned_gb300 import synth as S
+        from oracle import attention as OA
+        from oracle import masks as OM
+        from oracle import quant as OQ
+        self.head_fn = OQ.decode_head_quantized if kv == "int8" else OA.decode_head
+        w = S.WORKLOAD_BY_NAME[w_name]
+        self.w = w
+        self.N = w.context
+        self.pol = S.make_policies(w)
+        if w.prune_pct is None or w.budget == "choice64":
+            masks = S.masks_with_counts(w, S.drawn_counts(w))
+        else:
+            alpha, elig = S.stage2_inputs(w, self.pol)
+            masks = OM.top_s_prune(alpha, w.prune_pct, w.align, w.budget, elig)
+        self.kept = [np.nonzero(masks[0, h])[0] for h in range(w.num_kv_heads)]
+        spec = S.make_special_table(w)
+        k, v = S.make_kv(w.scaled(batch=1), 0, self.N)           # one sequence of layer 0
+        q = S.make_q(w.scaled(batch=1), 0, self.N - 1)
+        self.K = k[0].float().numpy()
+        self.V = v[0].float().numpy()
+        self.Q = q[0].float().numpy()
+        self.flags = spec[S.make_token_ids(w.scaled(batch=1), self.N)[0]].astype(bool) if len(spec) else None
+        self.units_per_call = w.batch * w.num_kv_heads
+
+    def run(self, u):
+        w, G = self.w, self.w.group
+        h = u % w.num_kv_heads
+        self.head_fn(self.Q[h * G:(h + 1) * G], self.K[:, h], self.V[:, h], int(self.pol[0, h]), self.kept[h],
+                     self.N, w.sink, w.local, w.local_only_window, self.flags)
+
+
 def oracle_sample(w_name, budget_s, max_units=None, kv="bf16"):
-    """Time the fp64 oracle on (sequence, kv head) units of the workload's
-    decode call until `budget_s` or `max_units`; returns (calls/s, units, s).
-    kv="int8": the oracle over the quantised middle (quantisation included)."""
-    import torch
-    from decode_attention_pruned_gb300 import synth as S
-    from oracle import attention as OA
-    from oracle import quant as OQ
-    head_fn = OQ.decode_head_quantized if kv == "int8" else OA.decode_head
-    w = S.WORKLOAD_BY_NAME[w_name]
-    N = w.context
-    pol = S.make_policies(w)
-    masks = S.make_masks(w, pol)
-    spec = S.make_special_table(w)
-    k, v = S.make_kv(w.scaled(batch=1), 0, N)           # one sequence of layer 0
-    q = S.make_q(w.scaled(batch=1), 0, N - 1)
-    K = k[0].float().numpy()
-    V = v[0].float().numpy()
-    Q = q[0].float().numpy()
-    flags = spec[S.make_token_ids(w.scaled(batch=1), N)[0]].astype(bool) if len(spec) else None
-    G = w.group
+    """Time the fp64 oracle on one core on (sequence, kv head) units of the
+    workload's decode call until `budget_s` or `max_units`; returns (calls/s,
+    units, s).  kv="int8": the oracle over the quantised middle (quantisation
+    included)."""
+    ou = _OracleUnits(w_name, kv)
     units, t0 = 0, time.perf_counter()
     while True:
-        h = units % w.num_kv_heads
-        kept = np.nonzero(masks[0, h])[0]
-        head_fn(Q[h * G:(h + 1) * G], K[:, h], V[:, h], int(pol[0, h]), kept, N, w.sink, w.local,
-                w.local_only_window, flags)
+        ou.run(units)
         units += 1
         el = time.perf_counter() - t0
         if el >= budget_s or (max_units is not None and units >= max_units):
             break
-    # one call is the decode attention of one layer: every (sequence, kv head)
-    units_per_call = w.batch * w.num_kv_heads
-    return units / el / units_per_call, units, el
+    return units / el / ou.units_per_call, units, el
+
+
+def _oracle_worker(w_name, kv, budget_s, max_units, start, ready, out):
+    ou = _OracleUnits(w_name, kv)
+    ou.run(0)                                      # first-touch warm-up
+    ready.put(1)
+    start.wait()
+    units, t0 = 0, time.perf_counter()
+    while True:
+        ou.run(units)
+        units += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_units is not None and units >= max_units):
+            break
+    out.put((units, el))
+
+
+def oracle_sample_parallel(w_name, budget_s, workers, max_units=None, kv="bf16"):
+    """The fp64 oracle on `workers` processes (one core each: one BLAS thread
+    per process), all timed over the same window after their inputs are
+    built; returns (calls/s of all workers, units, seconds).  Processes are
+    spawned, never forked, so a CUDA context in the parent is not copied."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    start, ready, out = ctx.Event(), ctx.Queue(), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(w_name, kv, budget_s, max_units, start, ready, out))
+             for _ in range(workers)]
+    for p in procs:
+        p.start()
+    for _ in procs:
+        ready.get(timeout=600)
+    start.set()
+    res = [out.get(timeout=600 + 4 * budget_s) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+    from decode_attention_pruned_gb300 import synth as S
+    w = S.WORKLOAD_BY_NAME[w_name]
+    units = sum(u for u, _ in res)
+    el = max(e for _, e in res)
+    rate = sum(u / e for u, e in res) / (w.batch * w.num_kv_heads)
+    return rate, units, el
+
+
+def host_cpu():
+    """(CPU model, logical cores available to this process)."""
+    model = None
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    import platform
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    return model or platform.processor() or platform.machine(), cores
+
+
+def cpu_baseline(w_name, budget_s, kv):
+    """The oracle on every host core (the reported value) and on one core."""
+    model, cores = host_cpu()
+    v1, u1, e1 = oracle_sample(w_name, budget_s / 2, kv=kv)
+    vn, un, en = oracle_sample_parallel(w_name, budget_s / 2, cores, kv=kv)
+    return {
+        "value": vn, "unit": UNIT, "cores": cores, "kind": "oracle",
+        "sample": f"fp64 numpy oracle, (sequence, kv head) units of layer 0: {un} units on {cores} worker "
+                  f"processes (one core each) in {en:.1f} s; calls/s = units/s / (batch x kv heads)",
+        "cpu_model": model,
+        "single_core": {"value": v1, "unit": UNIT, "cores": 1,
+                        "sample": f"{u1} units on one core in {e1:.1f} s"},
+    }
 
 
 def workload_config(w, args):
@@ -525,28 +679,48 @@ def workload_config(w, args):
 def run_reference(args):
     from decode_attention_pruned_gb300 import synth as S
     W, K = args.warmup, args.steps
-    oracle_sample(args.workload, 0.0, max_units=max(1, min(W, 3)), kv=args.kv)
-    value, units, el = oracle_sample(args.workload, args.reference_budget, max_units=K, kv=args.kv)
-    sample = (f"fp64 numpy oracle, one (sequence, kv head) of layer 0 per step; {units} steps in {el:.1f} s "
-              f"(capped at {args.reference_budget:.0f} s); calls/s = steps/s / (batch x kv heads)")
+    model, cores = host_cpu()
+    workers = cores if args.reference_cores == 0 else args.reference_cores
+    # a step is one (sequence, kv head) unit per worker process; the steps
+    # stop at K or at the time budget, whichever comes first
+    value, units, el = oracle_sample_parallel(args.workload, args.reference_budget, workers,
+                                              max_units=max(1, K), kv=args.kv)
+    steps = max(1, units // workers)
+    sample = (f"fp64 numpy oracle on {workers} worker processes (one core each), one (sequence, kv head) unit of "
+              f"layer 0 per worker and step: {units} units in {el:.1f} s (at most {K} steps, capped at "
+              f"{args.reference_budget:.0f} s; the workers' inputs built and warmed before); calls/s = units/s / "
+              f"(batch x kv heads)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": units,
-        "warmup": W, "ms_per_step": el / units * 1e3, "higher_is_better": True, "scaling": "weak",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": steps,
+        "warmup": W, "ms_per_step": el / steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": workload_config(S.WORKLOAD_BY_NAME[args.workload], args),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": workers, "kind": "oracle", "sample": sample,
+                         "cpu_model": model},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
 
 
+# defaults per workload: (timed steps, warm-up steps, end-to-end steps); the
+# timed region stays within a few seconds and the appends grow the context
+# by about 1 % (the rotating copies of the 20 GB serving step are few)
+DEFAULT_STEPS = {
+    "tiny": (60000, 2000, 4000),
+    "llama31_8b_layer": (60000, 2000, 4000),
+    "serving_b64": (150, 10, 30),
+    "qwen25_7b_long": (20000, 500, 2000),
+    "fastgen_mix": (1000, 20, 200),
+}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: per workload)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default: per workload)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama31_8b_layer")
+    ap.add_argument("--workload", default="serving_b64", choices=sorted(DEFAULT_STEPS))
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"])
     ap.add_argument("--decode-ctas", type=int, default=0, help="CTAs of a decode launch (0: the library's choice)")
@@ -554,13 +728,21 @@ def main(argv=None):
                     help="lk_step_layers mode: the library's choice, one fused launch, or append + decode")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run the workload's first LAYERS layers (0: all)")
-    ap.add_argument("--e2e-steps", type=int, default=4000)
+    ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--kernel-steps", type=int, default=2000)
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-budget", type=float, default=16.0,
+                    help="seconds of oracle timing for cpu_baseline (half on one core, half on all)")
     ap.add_argument("--reference-budget", type=float, default=60.0)
+    ap.add_argument("--reference-cores", type=int, default=0, help="oracle worker processes (0: every core)")
     args = ap.parse_args(argv)
+    d_steps, d_warm, d_e2e = DEFAULT_STEPS[args.workload]
+    args.steps = d_steps if args.steps is None else args.steps
+    args.warmup = d_warm if args.warmup is None else args.warmup
+    args.e2e_steps = d_e2e if args.e2e_steps is None else args.e2e_steps
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     rank, local_rank, world = _rank_env()
 
     if args.impl == "reference":
@@ -575,11 +757,8 @@ def main(argv=None):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = run_gpu(args, rank, local_rank, world)
     if rank == 0:
-        value, units, el = oracle_sample(args.workload, args.cpu_budget, kv=args.kv)
-        line["cpu_baseline"] = {
-            "value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"fp64 numpy oracle on {units} (sequence, kv head) units of layer 0 in {el:.1f} s, "
-                      f"scaled to calls/s"}
+        if world == 1:
+            line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget, args.kv)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

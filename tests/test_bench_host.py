@@ -45,13 +45,25 @@ def test_reference_arm_prints_contract_line(monkeypatch):
     buf = io.StringIO()
     with contextlib.redirect_stdout(buf):
         rc = bench.main(["--impl", "reference", "--steps", "4", "--warmup", "3", "--workload", "tiny",
-                         "--reference-budget", "2"])
+                         "--reference-budget", "2", "--reference-cores", "2"])
     assert rc == 0
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "calls/s"
     assert line["value"] > 0 and line["higher_is_better"] is True
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 2
+    assert line["cpu_baseline"]["cpu_model"]
+    assert line["steps"] == 4
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+
+
+def test_default_workload_is_the_largest_single_gpu_one():
+    from decode_attention_pruned_gb300 import synth as S
+    sizes = {w.name: w.num_layers * w.batch * w.num_kv_heads * w.context for w in S.WORKLOADS}
+    assert sizes["serving_b64"] == max(sizes.values())
+    ap_default = bench.DEFAULT_STEPS["serving_b64"]
+    assert ap_default[1] >= 3
+    model, cores = bench.host_cpu()
+    assert model and cores >= 1
 
 
 def test_reference_arm_nonzero_rank_is_silent(monkeypatch):
