@@ -144,3 +144,95 @@ def test_quantized_resident_bytes_are_the_arrays_sizes():
     # other policies are untouched by quantisation
     assert Q.resident_bytes_quantized(1, 0, 1000, S, W, 64) == F.resident_bytes(1, 0, 1000, S, W, 64)
     assert Q.resident_bytes_quantized(2, 0, 1000, S, W, 64, n_special=9) == 9 * 512
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3): the encoder against the format's definition and a library cast
+# ---------------------------------------------------------------------------
+
+def test_e4m3_values_of_the_format():
+    # fields S.EEEE.MMM with bias 7: the largest finite value, the smallest
+    # subnormal and normal, one, a negative, and the NaN pattern
+    v = Q.e4m3_value(np.arange(256))
+    assert v[0x7E] == 448.0 and v[0x01] == 2.0 ** -9 and v[0x08] == 2.0 ** -6 and v[0x07] == 7 * 2.0 ** -9
+    assert v[0x38] == 1.0 and v[0x39] == 1.125 and v[0x77] == 240.0 and v[0xC0] == -2.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    assert v[0x00] == 0.0 and np.signbit(v[0x80])
+    finite = v[:0x7F]
+    assert np.all(np.diff(finite) > 0)               # codes 0..126 ascend
+    assert len(np.unique(np.abs(v[np.isfinite(v)]))) == 127
+
+
+def test_e4m3_encoder_round_trip_ties_and_saturation():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = Q.e4m3_value(codes).astype(np.float32)
+    assert np.array_equal(Q.encode_e4m3(vals), codes)
+    pos = Q.e4m3_value(np.arange(0x7F))
+    mid = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)      # exact in fp32
+    got = Q.encode_e4m3(mid).astype(np.int64)
+    lo = np.arange(0x7E)
+    assert np.array_equal(got, np.where(lo % 2 == 0, lo, lo + 1))          # ties to the even code
+    up = np.nextafter(mid, np.float32(np.inf))
+    dn = np.nextafter(mid, np.float32(-np.inf))
+    assert np.array_equal(Q.encode_e4m3(up).astype(np.int64), lo + 1)
+    assert np.array_equal(Q.encode_e4m3(dn).astype(np.int64), lo)
+    assert list(Q.encode_e4m3(np.float32([448.0, 449.0, 464.0, 1e6, -1e6]))) == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
+
+
+def test_e4m3_encoder_matches_a_library_cast():
+    # torch's float8_e4m3fn cast rounds to nearest even; inside the finite
+    # range it must give the same codes, subnormals and ties included
+    import torch
+    rs = _rng(11)
+    x = np.concatenate([rs.standard_normal(20000) * s for s in (1e-3, 0.05, 1.0, 30.0, 150.0)])
+    x = np.concatenate([x, Q.e4m3_value(np.arange(0x7F)) * 1.0625, [0.0, 2.0 ** -10, 3 * 2.0 ** -10]])
+    x = np.clip(x, -448.0, 448.0).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(Q.encode_e4m3(x), ref)
+
+
+def test_fp8_quantisation_bounds_and_axes():
+    x = _rng(12).standard_normal((128, 64)).astype(np.float32) * 3
+    codes, s = Q.quantize_per_channel(x, "fp8")
+    assert codes.dtype == np.uint8 and s.shape == (64,)
+    assert np.all(s == np.abs(x).max(axis=0) / np.float32(448))
+    deq = Q.dequantize_per_channel(codes, s, "fp8")
+    # 3 mantissa bits: within half a step, 2^-4 relative, or half the
+    # smallest subnormal step (2^-10 of the scale)
+    assert np.all(np.abs(deq - x) <= np.maximum(np.abs(x) * 2.0 ** -4, s[None, :] * 2.0 ** -10) * (1 + 1e-6))
+    i = np.abs(x).argmax(axis=0)
+    assert np.all((codes[i, np.arange(64)] & 0x7F) == 0x7E)          # the absmax lands on +-448
+    assert np.all(np.abs(deq[i, np.arange(64)]) == 448.0 * s.astype(np.float64))
+    v = np.ones((128, 128), np.float32)
+    v[7, 9] = -50.0
+    c, sv = Q.quantize_per_token(v, "fp8")
+    assert sv[7] == np.float32(50.0) / np.float32(448) and c[7, 9] == 0xFE
+    assert np.all(np.delete(sv, 7) == np.float32(1) / np.float32(448))
+    z, zs = Q.quantize_per_channel(np.zeros((128, 32), np.float32), "fp8")
+    assert not z.any() and not zs.any()
+
+
+def test_fp8_on_grid_history_decodes_exactly_like_plain_attention():
+    # K, V drawn from the e4m3 values with every block / channel / token
+    # reaching 448: scale 1, quantisation is the identity
+    S, W, N, G, d = 4, 16, 4 + 16 + 256 + 50, 2, 128
+    rng = _rng(13)
+    grid = Q.e4m3_value(np.arange(0x7F))
+    K = (rng.choice(grid, size=(N, d)) * rng.choice([-1.0, 1.0], size=(N, d))).astype(np.float32)
+    V = (rng.choice(grid, size=(N, d)) * rng.choice([-1.0, 1.0], size=(N, d))).astype(np.float32)
+    V[:, 0] = 448.0
+    kept = np.arange(32)
+    for blk in range(2):
+        K[S + 128 * blk, kept] = 448.0
+    q = rng.standard_normal((G, d)) * 1e-4
+    o_q = Q.decode_head_quantized(q, K, V, 0, kept, N, S, W, 0, fmt="fp8")
+    o = OA.decode_head(q, K, V, 0, kept, N, S, W, 0)
+    assert np.array_equal(o_q, o)
+    Kf = rng.standard_normal((N, d)).astype(np.float32)
+    Vf = rng.standard_normal((N, d)).astype(np.float32)
+    q = rng.standard_normal((G, d))
+    d8 = np.abs(Q.decode_head_quantized(q, Kf, Vf, 0, kept, N, S, W, 0, fmt="fp8")
+                - OA.decode_head(q, Kf, Vf, 0, kept, N, S, W, 0)).max()
+    d_i8 = np.abs(Q.decode_head_quantized(q, Kf, Vf, 0, kept, N, S, W, 0)
+                  - OA.decode_head(q, Kf, Vf, 0, kept, N, S, W, 0)).max()
+    assert 1e-6 < d8 < 0.2 and d8 > d_i8          # 3 mantissa bits lose more than 7-bit codes
