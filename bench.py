@@ -246,7 +246,7 @@ def run_gpu(args, rank, local_rank, world):
     max_growth = max(1, int(MAX_CONTEXT_GROWTH * N))
     cap_probe = N + 64
     paged = args.layout == "paged"
-    kvf = lkb.KV_INT8 if args.kv == "int8" else lkb.KV_BF16
+    kvf = {"bf16": lkb.KV_BF16, "int8": lkb.KV_INT8, "fp8": lkb.KV_FP8}[args.kv]
     # paged: page pools sized for every sequence's middle at the capacity
     middle = (lambda cap: B * max(0, cap - w.sink - w.local)) if paged else (lambda cap: None)
     copy_bytes = plan.cache_bytes(B, cap_probe, middle(cap_probe), kvf) + plan.workspace_bytes(B)
@@ -488,7 +488,7 @@ def run_gpu(args, rank, local_rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if kvf == lkb.KV_BF16 else "bf16 + int8 (middle blocks)",
+        "dtype": "bf16" if kvf == lkb.KV_BF16 else f"bf16 + {args.kv} (middle blocks)",
         "data": "synthetic (seeded K/V/q; LeanK masks from the library's mask builder on seeded importances)",
         "config": {
             **workload_config(w, args), "context_growth_max": growth,
@@ -541,7 +541,10 @@ class _OracleUnits:
         from oracle import attention as OA
         from oracle import masks as OM
         from oracle import quant as OQ
-        self.head_fn = OQ.decode_head_quantized if kv == "int8" else OA.decode_head
+        if kv == "bf16":
+            self.head_fn = OA.decode_head
+        else:
+            self.head_fn = lambda *a: OQ.decode_head_quantized(*a, fmt=kv)
         w = S.WORKLOAD_BY_NAME[w_name]
         self.w = w
         self.N = w.context
@@ -571,7 +574,7 @@ class _OracleUnits:
 def oracle_sample(w_name, budget_s, max_units=None, kv="bf16"):
     """Time the fp64 oracle on one core on (sequence, kv head) units of the
     workload's decode call until `budget_s` or `max_units`; returns (calls/s,
-    units, s).  kv="int8": the oracle over the quantised middle (quantisation
+    units, s).  kv="int8" / "fp8": the oracle over the quantised middle (quantisation
     included)."""
     ou = _OracleUnits(w_name, kv)
     units, t0 = 0, time.perf_counter()
@@ -671,8 +674,8 @@ def workload_config(w, args):
         "kv_heads": w.num_kv_heads, "head_dim": 128, "context": w.context, "sink": w.sink, "local": w.local,
         "prune_pct": w.prune_pct, "mask_budget": w.budget,
         "cache_layout": "paged (128-row pages per width class)" if args.layout == "paged" else "contiguous",
-        "middle_format": "int8 (complete 128-row blocks; per-channel K / per-token V scales)"
-        if args.kv == "int8" else "bf16",
+        "middle_format": f"{args.kv} (complete 128-row blocks; per-channel K / per-token V scales)"
+        if args.kv != "bf16" else "bf16",
     }
 
 
@@ -722,7 +725,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="serving_b64", choices=sorted(DEFAULT_STEPS))
     ap.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"])
-    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8", "fp8"])
     ap.add_argument("--decode-ctas", type=int, default=0, help="CTAs of a decode launch (0: the library's choice)")
     ap.add_argument("--step", default="auto", choices=["auto", "fused", "split"],
                     help="lk_step_layers mode: the library's choice, one fused launch, or append + decode")

@@ -41,7 +41,8 @@ class RegionInfo(ctypes.Structure):
                 ("sealed_blocks", ctypes.c_int32)]
 
 
-KV_BF16, KV_INT8 = 0, 1
+KV_BF16, KV_INT8, KV_FP8 = 0, 1, 2
+KV_FORMAT_NAMES = {KV_BF16: "bf16", KV_INT8: "int8", KV_FP8: "fp8"}
 STEP_AUTO, STEP_FUSED, STEP_SPLIT = 0, 1, 2
 
 
@@ -232,7 +233,8 @@ class Cache:
     With ``middle_tokens`` the cache is paged (lk_cache_init_paged): the
     middle rows of all sequences share page pools sized for that many middle
     tokens in total.  ``kv_format=KV_INT8`` quantises complete 128-row
-    blocks of the middle (lk_cache_init_ex)."""
+    blocks of the middle (lk_cache_init_ex); ``KV_FP8`` stores them as e4m3
+    codes."""
 
     def __init__(self, plan: Plan, batch: int, capacity: int, device=None, stream=None, middle_tokens=None,
                  kv_format=KV_BF16):
@@ -326,7 +328,8 @@ class Cache:
 
     def block(self, layer, b, kv_head, j, stream=None):
         """lk_cache_block: (k_codes [128, k], k_scales [k], v_codes [128, 128],
-        v_scales [128]) of sealed block j, logical order."""
+        v_scales [128]) of sealed block j, logical order; codes int8 (INT8)
+        or uint8 e4m3 bit patterns (FP8)."""
         k = self.plan.head(layer, kv_head)[1]
         kc = np.zeros((128, k), np.int8)
         ks = np.zeros(k, np.float32)
@@ -334,6 +337,8 @@ class Cache:
         vs = np.zeros(128, np.float32)
         _check(_lib.lk_cache_block(self._h, layer, b, kv_head, j, kc.ctypes.data, ks.ctypes.data, vc.ctypes.data,
                                    vs.ctypes.data, _stream(stream)))
+        if self.kv_format == KV_FP8:
+            kc, vc = kc.view(np.uint8), vc.view(np.uint8)
         return kc, ks, vc, vs
 
     def lengths(self, layer):

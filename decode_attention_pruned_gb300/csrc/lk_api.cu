@@ -87,7 +87,7 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // is the head's bf16 tail).
 inline int32_t pages_at(int n, int S, int W, int fmt) {
   const int m = std::max(0, n - S - W);
-  return fmt == kKvInt8 ? m / kQBlockRows : (int32_t)ceil_div(m, kPageRows);
+  return kv_quantized(fmt) ? m / kQBlockRows : (int32_t)ceil_div(m, kPageRows);
 }
 
 // middle_tokens < 0: region B contiguous per (layer, sequence, head), sized
@@ -98,7 +98,7 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_toke
   const lk_plan_desc& d = p.d;
   const int L = d.num_layers, H = d.num_kv_heads;
   const bool paged = middle_tokens >= 0;
-  const bool q8 = fmt == kKvInt8;
+  const bool q8 = kv_quantized(fmt);
   lay->kv_format = fmt;
   lay->max_pages = paged ? std::max<int32_t>(1, pages_at(cap, d.sink, d.local, fmt)) : 0;
   int64_t pages_per_head = 0;
@@ -396,7 +396,7 @@ uint64_t entry_bytes(const lk_cache_s* cache, const HeadDesc& hd, int N, int cnt
   } else {
     na = std::min(cnt, hd.cap_a);
   }
-  if (cache->lay.kv_format == kKvInt8 && nb > 0) {
+  if (kv_quantized(cache->lay.kv_format) && nb > 0) {
     const uint64_t sealed = nb / kQBlockRows, tail = nb % kQBlockRows;
     return na * (2 * kHeadDim * 2) + sealed * (uint64_t)qblock_bytes(hd.n_kept) +
            tail * (uint64_t)(hd.n_kept + kHeadDim) * 2;
@@ -552,7 +552,8 @@ static lk_status cache_bytes_impl(lk_plan plan, int32_t batch, int32_t capacity_
     return fail(LK_ERR_ARG, "batch %d out of range", batch);
   if (capacity_tokens < 1 || capacity_tokens > (1 << 30))
     return fail(LK_ERR_ARG, "capacity_tokens %d out of [1, 2^30]", capacity_tokens);
-  if (fmt != kKvBf16 && fmt != kKvInt8) return fail(LK_ERR_ARG, "kv_format %d is not LK_KV_BF16 or LK_KV_INT8", fmt);
+  if (fmt != kKvBf16 && fmt != kKvInt8 && fmt != kKvFp8)
+    return fail(LK_ERR_ARG, "kv_format %d is not LK_KV_BF16, LK_KV_INT8 or LK_KV_FP8", fmt);
   Layout lay;
   lk_status st = compute_layout(*plan, batch, capacity_tokens, middle_tokens, fmt, &lay);
   if (st != LK_OK) return st;
@@ -1200,9 +1201,10 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
   out->page_table_offset = 0;
   out->kv_format = lay.kv_format;
   out->sealed_blocks = 0;
-  const bool q8 = lay.kv_format == kKvInt8;
+  const bool q8 = kv_quantized(lay.kv_format);
   if (q8 && hd.cap_b > 0)
-    out->sealed_blocks = pages_at(cache->host_len[(size_t)layer * cache->B + b], cache->cv.S, cache->cv.W, kKvInt8);
+    out->sealed_blocks =
+        pages_at(cache->host_len[(size_t)layer * cache->B + b], cache->cv.S, cache->cv.W, lay.kv_format);
   if (hd.cap_b > 0 && cache->paged() && !q8) {
     out->rows_b = (int32_t)std::min<int64_t>((int64_t)lay.num_pages[hd.pool_kb] * kPageRows, INT32_MAX);
     out->k_b_offset = lay.off_pool[hd.pool_kb] + (uint64_t)hd.krow_b * hd.n_kept * 2;
@@ -1223,12 +1225,13 @@ lk_status lk_cache_region(lk_cache cache, int32_t layer, int32_t b, int32_t kv_h
 lk_status lk_cache_block(lk_cache cache, int32_t layer, int32_t b, int32_t kv_head, int32_t block, int8_t* k_codes,
                          float* k_scales, int8_t* v_codes, float* v_scales, void* stream) {
   if (!cache) return fail(LK_ERR_ARG, "lk_cache_block: null cache");
-  if (cache->lay.kv_format != kKvInt8) return fail(LK_ERR_STATE, "lk_cache_block: the cache is not INT8");
+  if (!kv_quantized(cache->lay.kv_format))
+    return fail(LK_ERR_STATE, "lk_cache_block: the cache is not INT8 or FP8");
   if (layer < 0 || layer >= cache->cv.L || b < 0 || b >= cache->B || kv_head < 0 || kv_head >= cache->cv.Hkv)
     return fail(LK_ERR_ARG, "lk_cache_block: (layer %d, b %d, kv_head %d) out of range", layer, b, kv_head);
   const HeadDesc& hd = cache->lay.heads[(size_t)layer * cache->cv.Hkv + kv_head];
   const int sealed = hd.cap_b > 0 ? pages_at(cache->host_len[(size_t)layer * cache->B + b], cache->cv.S,
-                                             cache->cv.W, kKvInt8)
+                                             cache->cv.W, cache->lay.kv_format)
                                   : 0;
   if (block < 0 || block >= sealed)
     return fail(LK_ERR_ARG, "lk_cache_block: block %d not in [0, %d) sealed blocks", block, sealed);
@@ -1253,8 +1256,11 @@ lk_status lk_cache_block(lk_cache cache, int32_t layer, int32_t b, int32_t kv_he
     if (k_codes)
       for (int c = 0; c < k; ++c) k_codes[r * k + c] = (int8_t)img[(size_t)r * k + qbyte(k, r, c)];
     if (v_codes)
-      for (int c = 0; c < kHeadDim; ++c)
-        v_codes[r * kHeadDim + c] = (int8_t)((int)img[qblock_voff(k) + (size_t)r * kHeadDim + qbyte(kHeadDim, r, c)] - 128);
+      for (int c = 0; c < kHeadDim; ++c) {
+        const int byte = img[qblock_voff(k) + (size_t)r * kHeadDim + qbyte(kHeadDim, r, c)];
+        // INT8 V codes are stored offset binary; FP8 codes as they are
+        v_codes[r * kHeadDim + c] = (int8_t)(uint8_t)(cache->lay.kv_format == kKvInt8 ? byte - 128 : byte);
+      }
   }
   if (k_scales) std::memcpy(k_scales, img.data() + qblock_ksoff(k), (size_t)k * 4);
   if (v_scales) std::memcpy(v_scales, img.data() + qblock_vsoff(k), (size_t)kQBlockRows * 4);

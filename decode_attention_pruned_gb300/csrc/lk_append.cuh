@@ -1,5 +1,5 @@
 // Cache editing shared by the append kernel and the fused append + decode
-// kernel: the per-head append of one token, with the paged and INT8 paths
+// kernel: the per-head append of one token, with the paged and INT8 / FP8 paths
 // (LeanK article, framerc.cn, sections 3.1-3.2; FastGen article, mhpn.cn,
 // section 3.2 stage 2; KIVI-style sealing after the pruning, LeanK section
 // 4.2 and the pruning white paper's section 5.2.1).  Every helper is
@@ -57,7 +57,7 @@ __device__ void pop_pages(const CacheView& cv, const HeadDesc& hd, int k, int32_
 // no free page).
 __device__ __forceinline__ bool middle_rows(const CacheView& cv, const HeadDesc& hd, int b, int mid, int32_t page,
                                             int64_t& krow, int64_t& vrow) {
-  if (cv.kv_format == kKvInt8) {           // the open block: bf16 tail row mid mod 128
+  if (kv_quantized(cv.kv_format)) {        // the open block: bf16 tail row mid mod 128
     krow = hd.krow_b + (int64_t)b * hd.cap_b + mid % kQBlockRows;
     vrow = hd.vrow_b + (int64_t)b * hd.cap_b + mid % kQBlockRows;
     return true;
@@ -75,10 +75,10 @@ __device__ __forceinline__ bool middle_rows(const CacheView& cv, const HeadDesc&
 }
 
 // Region-B pages a (FULL, k > 0) head holds at n tokens: started pages
-// (bf16) or sealed blocks (INT8).
+// (bf16) or sealed blocks (INT8 / FP8).
 __device__ __forceinline__ int pages_at(const CacheView& cv, int n) {
   const int m = max(0, n - cv.S - cv.W);
-  return cv.kv_format == kKvInt8 ? m / kQBlockRows : (m + kPageRows - 1) / kPageRows;
+  return kv_quantized(cv.kv_format) ? m / kQBlockRows : (m + kPageRows - 1) / kPageRows;
 }
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
@@ -91,6 +91,20 @@ __device__ __forceinline__ int8_t quant8(float x, float s) {
   return (int8_t)max(-127, min(127, q));
 }
 
+// e4m3 code of x for scale s (s = max|x| / 448 in fp32): x / s in fp32,
+// rounded to the nearest e4m3 value (ties to the even code) and saturated at
+// +-448 by the conversion instruction; a zero code keeps the sign of x;
+// s = 0 gives 0.
+__device__ __forceinline__ uint8_t quant_e4m3(float x, float s) {
+  if (!(s > 0.f)) return 0;
+  const float y = __fdiv_rn(x, s);
+  uint16_t pair;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.f), "f"(y));
+  uint8_t c = (uint8_t)(pair & 0xFFu);
+  if ((c & 0x7Fu) == 0) c = signbit(y) ? 0x80 : 0x00;
+  return c;
+}
+
 // Device address of sealed block j of (layer, b, h); null if its page is
 // missing.
 __device__ __forceinline__ uint8_t* qblock_addr(const CacheView& cv, const HeadDesc& hd, int layer, int b, int h,
@@ -101,20 +115,26 @@ __device__ __forceinline__ uint8_t* qblock_addr(const CacheView& cv, const HeadD
   return page < 0 ? nullptr : cv.qpool + hd.qoff + (int64_t)page * qb;
 }
 
-// One warp seals a 128-row block: kv(r, c) / vv(r, c) give the bf16 bits of
-// K row r at kept channel c (c < k) and of V row r at channel c.  K: one
-// scale per channel (lane per channel); V: one scale per row (lane per four
-// channels, warp max).  Codes go to their swizzled byte (qbyte).
+// One warp seals a 128-row block in format fmt (INT8 or FP8): kv(r, c) /
+// vv(r, c) give the bf16 bits of K row r at kept channel c (c < k) and of V
+// row r at channel c.  K: one scale per channel (lane per channel); V: one
+// scale per row (lane per four channels, warp max).  Codes go to their
+// swizzled byte (qbyte).
 template <class KF, class VF>
-__device__ void seal_block(uint8_t* dst, int k, KF kv, VF vv, int lane) {
+__device__ void seal_block(uint8_t* dst, int k, int fmt, KF kv, VF vv, int lane) {
   float* ks = reinterpret_cast<float*>(dst + qblock_ksoff(k));
   float* vs = reinterpret_cast<float*>(dst + qblock_vsoff(k));
+  const bool fp8 = fmt == kKvFp8;
+  const float qmax = fp8 ? 448.f : 127.f;
   for (int c = lane; c < k; c += 32) {
     float m = 0.f;
     for (int r = 0; r < kQBlockRows; ++r) m = fmaxf(m, fabsf(bf16_to_f32(kv(r, c))));
-    const float sc = __fdiv_rn(m, 127.f);
+    const float sc = __fdiv_rn(m, qmax);
     ks[c] = sc;
-    for (int r = 0; r < kQBlockRows; ++r) dst[r * k + qbyte(k, r, c)] = (uint8_t)quant8(bf16_to_f32(kv(r, c)), sc);
+    for (int r = 0; r < kQBlockRows; ++r) {
+      const float x = bf16_to_f32(kv(r, c));
+      dst[r * k + qbyte(k, r, c)] = fp8 ? quant_e4m3(x, sc) : (uint8_t)quant8(x, sc);
+    }
   }
   uint8_t* vc = dst + qblock_voff(k);
   for (int r = 0; r < kQBlockRows; ++r) {
@@ -127,11 +147,12 @@ __device__ void seal_block(uint8_t* dst, int k, KF kv, VF vv, int lane) {
     }
 #pragma unroll
     for (int sh = 16; sh > 0; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
-    const float sc = __fdiv_rn(m, 127.f);
+    const float sc = __fdiv_rn(m, qmax);
     if (lane == 0) vs[r] = sc;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      vc[r * kHeadDim + qbyte(kHeadDim, r, 4 * lane + i)] = (uint8_t)(quant8(x[i], sc) + 128);   // offset binary
+      vc[r * kHeadDim + qbyte(kHeadDim, r, 4 * lane + i)] =
+          fp8 ? quant_e4m3(x[i], sc) : (uint8_t)(quant8(x[i], sc) + 128);   // INT8: offset binary
   }
 }
 
@@ -139,13 +160,13 @@ __device__ void seal_block(uint8_t* dst, int k, KF kv, VF vv, int lane) {
 // v_src are its bf16 rows [128]; cnt / special are the layer's special-row
 // count and whether the token's id is special.  FULL: sink row n, or ring
 // row S + (n-S) mod W after moving the token n-W it replaces into the middle
-// (K gathered to the kept channels; INT8 caches write the bf16 tail and seal
-// it into a block when it fills).  LOCAL: ring row n mod W_loc.  SPECIAL:
-// row cnt if the token is special.  The caller updates len / cnt afterwards.
-// kWithQ8 = false compiles the INT8 paths out (callers that never see an
-// INT8 cache).  k_old / v_old / kept, when given, are copies of the evicted
-// window row and of the head's kept-channel list (e.g. in shared memory) to
-// read instead of the cache.
+// (K gathered to the kept channels; INT8 / FP8 caches write the bf16 tail and
+// seal it into a block when it fills).  LOCAL: ring row n mod W_loc.
+// SPECIAL: row cnt if the token is special.  The caller updates len / cnt
+// afterwards.  kWithQ8 = false compiles the quantised paths out (callers that
+// never see a quantised cache).  k_old / v_old / kept, when given, are copies
+// of the evicted window row and of the head's kept-channel list (e.g. in
+// shared memory) to read instead of the cache.
 template <bool kWithQ8>
 __device__ void append_head(const CacheView& cv, int layer, int b, int h, int n, int cnt, bool special,
                             const uint16_t* k_src, const uint16_t* v_src, int lane,
@@ -165,7 +186,7 @@ __device__ void append_head(const CacheView& cv, int layer, int b, int h, int n,
       if (n - cv.S >= cv.W && hd.n_kept > 0) {
         const int mid = n - cv.W - cv.S;               // K_prun row of token n - W
         int32_t page = -1;
-        if (cv.max_pages > 0 && !(kWithQ8 && cv.kv_format == kKvInt8)) {
+        if (cv.max_pages > 0 && !(kWithQ8 && kv_quantized(cv.kv_format))) {
           int32_t* pt = page_row(cv, layer, b, h) + mid / kPageRows;
           if (mid % kPageRows == 0) {         // first row of a new page
             if (lane == 0) {
@@ -186,7 +207,7 @@ __device__ void append_head(const CacheView& cv, int layer, int b, int h, int n,
           write_middle(cv, hd, kept, krow, vrow, k_old, v_old, lane);
         }
         __syncwarp();
-        if (kWithQ8 && cv.kv_format == kKvInt8 && mid % kQBlockRows == kQBlockRows - 1) {
+        if (kWithQ8 && kv_quantized(cv.kv_format) && mid % kQBlockRows == kQBlockRows - 1) {
           // the tail block is complete: seal it into block mid / 128
           const int j = mid / kQBlockRows;
           uint8_t* dst;
@@ -206,7 +227,7 @@ __device__ void append_head(const CacheView& cv, int layer, int b, int h, int n,
             const uint16_t* kt = cv.pool[hd.pool_kb] + (hd.krow_b + (int64_t)b * hd.cap_b) * k;
             const uint16_t* vt = va_pool + (hd.vrow_b + (int64_t)b * hd.cap_b) * kHeadDim;
             seal_block(
-                dst, k, [&](int r, int c) { return kt[(size_t)r * k + c]; },
+                dst, k, cv.kv_format, [&](int r, int c) { return kt[(size_t)r * k + c]; },
                 [&](int r, int c) { return vt[(size_t)r * kHeadDim + c]; }, lane);
             __syncwarp();
             // the open block restarts empty (zeros), as a prefill leaves it

@@ -188,7 +188,7 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
     if (len.act && N >= cv.S + cv.W) r.mrow = cv.S + (N - cv.S) % cv.W;
     if (hd.n_kept > 0) {
       const int m = max(0, N - cv.S - cv.W);
-      if (cv.kv_format == kKvInt8) {
+      if (kv_quantized(cv.kv_format)) {
         const int nblk = min(m / kQBlockRows, cv.max_pages > 0 ? cv.max_pages : hd.qblocks);
         r.n_q = nblk * kQBlockRows;
         r.n_b = m - m / kQBlockRows * kQBlockRows;
@@ -277,6 +277,21 @@ __device__ __forceinline__ void consumer_sync(uint32_t cbar, uint32_t& phase, co
   phase ^= 1u;
 }
 
+// Codes of a sealed block as exact f16 pairs, from one 32-bit word of an
+// ldmatrix fragment (bytes 0..3): (byte 0, byte 2) and (byte 1, byte 3).
+// K codes: INT8 two's complement or e4m3.  V codes: INT8 offset binary,
+// given as 1152 + code (the caller removes the bias), or e4m3.
+template <int kFmt>
+__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& even, uint32_t& odd) {
+  if (kFmt == kKvFp8) e4m3x4_to_f16x2(w, even, odd);
+  else i8x4_to_f16x2(w, even, odd);
+}
+template <int kFmt>
+__device__ __forceinline__ void vcodes_to_f16x2(uint32_t w, uint32_t& even, uint32_t& odd) {
+  if (kFmt == kKvFp8) e4m3x4_to_f16x2(w, even, odd);
+  else u8x4_to_f16x2_biased(w, even, odd);
+}
+
 // Shared-memory address of 16-byte chunk `c` (channels 8c..8c+7) of tile row
 // `r`.  128-byte family (K128, V, K64): 64-channel halves of T rows x 128 B,
 // 128-byte swizzle (chunk ^= row mod 8).  64-byte family (K32, K96):
@@ -290,11 +305,12 @@ __device__ __forceinline__ uint32_t tile_addr64(uint32_t base, int r, int c) {
          ((uint32_t)((c & 3) ^ ((r >> 1) & 3)) << 4);
 }
 
-// kQ8: the cache's middle is INT8 (sealed blocks may occur); the bf16
-// instantiation carries no INT8 code.
-template <bool kQ8>
+// kFmt: the cache's middle format (KvFormat).  The quantised instantiations
+// (INT8, FP8) handle sealed blocks; the bf16 one carries no code for them.
+template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
+  constexpr bool kQ8 = kFmt != kKvBf16;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -991,12 +1007,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t w0, w1, w2, w3;
             ldsm_x4(kbase + (uint32_t)(row * kb + 16 * (grp ^ qswz(kb, row))), w0, w1, w2, w3);
             uint32_t f0, f1, f2, f3;
-            i8x4_to_f16x2(w0, f0, f2);       // rows gid: k 2tig.. / 2tig+8..
-            i8x4_to_f16x2(w1, f1, f3);       // rows gid + 8
+            codes_to_f16x2<kFmt>(w0, f0, f2);       // rows gid: k 2tig.. / 2tig+8..
+            codes_to_f16x2<kFmt>(w1, f1, f3);       // rows gid + 8
             mma_f16_16816(sc, f0, f1, f2, f3, bh[0][0], bh[0][1]);
             mma_f16_16816(sd, f0, f1, f2, f3, bl[0][0], bl[0][1]);
-            i8x4_to_f16x2(w2, f0, f2);
-            i8x4_to_f16x2(w3, f1, f3);
+            codes_to_f16x2<kFmt>(w2, f0, f2);
+            codes_to_f16x2<kFmt>(w3, f1, f3);
             mma_f16_16816(sc, f0, f1, f2, f3, bh[1][0], bh[1][1]);
             mma_f16_16816(sd, f0, f1, f2, f3, bl[1][0], bl[1][1]);
           }
@@ -1075,8 +1091,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + d.koff + qblock_vsoff(d.width));
         const float sv0 = vsc[r0 + gid], sv1 = vsc[r0 + gid + 8];
         const float q0 = p0 * sv0, q1 = p1 * sv0, q2 = p2 * sv1, q3 = p3 * sv1;
-        c0 += q0 + q2;
-        c1 += q1 + q3;
+        if (kFmt == kKvInt8) {
+          c0 += q0 + q2;
+          c1 += q1 + q3;
+        }
         const uint32_t h01 = pack_f16x2(q0, q1), h23 = pack_f16x2(q2, q3);
         const uint32_t r01 = pack_f16x2(q0 - f16_lo(h01), q1 - f16_hi(h01));
         const uint32_t r23 = pack_f16x2(q2 - f16_lo(h23), q3 - f16_hi(h23));
@@ -1089,12 +1107,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t w0, w1, w2, w3;
           ldsm_x4_trans(vbase + (uint32_t)(row * kHeadDim + 16 * (grp ^ (row & 7))), w0, w1, w2, w3);
           uint32_t f0, f1, f2, f3;
-          u8x4_to_f16x2_biased(w0, f0, f1);  // tokens 2tig.. of rows 0-7: channels gid / gid + 8
-          u8x4_to_f16x2_biased(w1, f2, f3);  // tokens 2tig + 8..
+          vcodes_to_f16x2<kFmt>(w0, f0, f1);  // tokens 2tig.. of rows 0-7: channels gid / gid + 8
+          vcodes_to_f16x2<kFmt>(w1, f2, f3);  // tokens 2tig + 8..
           mma_f16_16816(o[2 * i2], f0, f1, f2, f3, ph0, ph1);
           mma_f16_16816(o[2 * i2], f0, f1, f2, f3, pr0, pr1);
-          u8x4_to_f16x2_biased(w2, f0, f1);
-          u8x4_to_f16x2_biased(w3, f2, f3);
+          vcodes_to_f16x2<kFmt>(w2, f0, f1);
+          vcodes_to_f16x2<kFmt>(w3, f2, f3);
           mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, ph0, ph1);
           mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, pr0, pr1);
         }
@@ -1207,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(bar_empty + 8 * stage);
 
     if (d.flags & kLast) {
-      if (kQ8) {
+      if (kFmt == kKvInt8) {
         // remove the 1152 bias of the INT8 V codes: o -= 1152 * sum(P')
         float s0 = c0, s1 = c1;
 #pragma unroll
@@ -1454,9 +1472,12 @@ size_t decode_smem_bytes() { return kSmemBytes; }
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ctas, cudaStream_t stream) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t err =
+        cudaFuncSetAttribute(decode_kernel<kKvBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      err = cudaFuncSetAttribute(decode_kernel<kKvInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(decode_kernel<kKvFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_done = true;
   }
@@ -1470,8 +1491,9 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ct
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (args.cv.kv_format == kKvInt8) return cudaLaunchKernelEx(&cfg, decode_kernel<true>, maps, args);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<false>, maps, args);
+  if (args.cv.kv_format == kKvInt8) return cudaLaunchKernelEx(&cfg, decode_kernel<kKvInt8>, maps, args);
+  if (args.cv.kv_format == kKvFp8) return cudaLaunchKernelEx(&cfg, decode_kernel<kKvFp8>, maps, args);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kKvBf16>, maps, args);
 }
 
 }  // namespace lk

@@ -205,6 +205,17 @@ __device__ __forceinline__ void u8x4_to_f16x2_biased(uint32_t w, uint32_t& even,
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(odd) : "r"(w), "r"(0x64646464u), "r"(0x4341u));
 }
 
+// Four e4m3 codes (bytes 0..3 of w) as exact f16 pairs: (byte 0, byte 2) and
+// (byte 1, byte 3).  Every e4m3 value, subnormals included, is an f16 value.
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& even, uint32_t& odd) {
+  uint32_t p;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(p) : "r"(w), "r"(0u), "r"(0x3120u));     // bytes (0, 2, 1, 3)
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(even), "=r"(odd)
+      : "r"(p));
+}
+
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;

@@ -18,16 +18,17 @@
 // [L][B][Hkv][max_pages].  Free pages of each class sit on a device stack, so
 // appends allocate pages inside the kernel (graph replays included).
 //
-// INT8 caches (KIVI-style quantisation after pruning): region B keeps only
-// its last, incomplete 128-row block in bf16 (the "tail", 128 rows per
+// INT8 / FP8 caches (KIVI-style quantisation after pruning): region B keeps
+// only its last, incomplete 128-row block in bf16 (the "tail", 128 rows per
 // (layer, sequence, head) in pools K_k and V); every complete block is sealed
 // into a byte block of the Q pool (contiguous per head and sequence, or a
 // page of its width class):
 //   [K codes 128 x k][V codes 128 x 128][K scales k x f32][V scales 128 x f32]
 // Codes are row-major; within each 16-channel group a row stores channels
 // (0, 8, 1, 9, ..., 7, 15) and its 16-byte groups are XOR-swizzled by row
-// (qswz), so ldmatrix reads mma fragments without bank conflicts.  K codes
-// are two's complement, V codes offset binary (code + 128).
+// (qswz), so ldmatrix reads mma fragments without bank conflicts.  INT8: K
+// codes are two's complement, V codes offset binary (code + 128).  FP8: K and
+// V codes are e4m3 bytes.
 #pragma once
 #include <stdint.h>
 
@@ -38,11 +39,14 @@ constexpr int kMaxGroup = 8;        // query heads per kv head handled by one mm
 constexpr int kMaxCtas = 256;       // decode grid cap (partial workspace; combine staging np*G <= 2048)
 constexpr int kTmaBoxRows = 128;    // token rows per TMA box = decode tile rows
 constexpr int kPageRows = 128;      // middle rows per page (paged caches)
-constexpr int kQBlockRows = 128;    // rows per sealed INT8 block (= one page, one tile)
+constexpr int kQBlockRows = 128;    // rows per sealed INT8 / FP8 block (= one page, one tile)
 
-enum KvFormat : int32_t { kKvBf16 = 0, kKvInt8 = 1 };
+enum KvFormat : int32_t { kKvBf16 = 0, kKvInt8 = 1, kKvFp8 = 2 };
+// complete middle blocks are sealed into one-byte codes + fp32 scales
+__host__ __device__ constexpr bool kv_quantized(int fmt) { return fmt != kKvBf16; }
 
-// Bytes of a sealed INT8 block of width k and the offsets of its parts.
+// Bytes of a sealed block (INT8 or FP8: one byte per code) of width k and the
+// offsets of its parts.
 __host__ __device__ constexpr int qblock_bytes(int k) { return 132 * (k + 128); }
 __host__ __device__ constexpr int qblock_voff(int k) { return 128 * k; }
 __host__ __device__ constexpr int qblock_ksoff(int k) { return 128 * k + 128 * 128; }

@@ -1,6 +1,6 @@
 // Cache editing: append one token per sequence, and prefill a layer from a
 // dense history.  Pure data movement (every bf16 copy is bit-exact) plus the
-// INT8 sealing of complete middle blocks.
+// INT8 / FP8 sealing of complete middle blocks.
 //
 // Rules (LeanK article, framerc.cn, section 3.1 "cache partition" and 3.2;
 // StreamingLLM sinks + sliding window as in the "intelligent pruning white
@@ -22,11 +22,13 @@
 // host checks that enough pages are free before it launches, so a pop that
 // finds the stack empty only records kStatusCapacity.
 //
-// INT8 caches (KIVI-style quantisation after the pruning; LeanK article
+// INT8 / FP8 caches (KIVI-style quantisation after the pruning; LeanK article
 // sections 4.2 and 5.2, the white paper's section 5.2.1): middle rows go to a
 // 128-row bf16 tail; the append that fills its last row seals it into a byte
 // block of the Q pool (per-channel K and per-token V scales, absmax / 127 in
-// fp32, codes x / scale rounded half to even) and clears the tail.  Prefill
+// fp32 and codes x / scale rounded half to even for INT8; absmax / 448 and
+// codes x / scale rounded to the nearest e4m3 value for FP8) and clears the
+// tail.  Prefill
 // seals complete blocks straight from its inputs, so both give the same
 // bytes; with paging the sealed blocks are the pages.
 #include <cuda_runtime.h>
@@ -120,9 +122,9 @@ __global__ void __launch_bounds__(256) prefill_kernel(const PrefillArgs a) {
       row8(ka_pool, abase + arow)[lane] = reinterpret_cast<const uint2*>(k_src)[lane];
       row8(va_pool, abase + arow)[lane] = reinterpret_cast<const uint2*>(v_src)[lane];
     } else if (mid >= 0) {
-      // INT8: rows of complete blocks are sealed from the inputs by
+      // INT8 / FP8: rows of complete blocks are sealed from the inputs by
       // prefill_seal_kernel; only the open block's rows go to the bf16 tail
-      if (cv.kv_format == kKvInt8 && mid < (n - cv.S - cv.W) / kQBlockRows * kQBlockRows) continue;
+      if (kv_quantized(cv.kv_format) && mid < (n - cv.S - cv.W) / kQBlockRows * kQBlockRows) continue;
       const int32_t page = cv.max_pages > 0 && cv.kv_format == kKvBf16
                                ? __ldcg(&page_row(cv, a.layer, b, h)[mid / kPageRows])
                                : -1;
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(256) prefill_pages_kernel(const PrefillArgs a)
   pop_pages(cv, hd, min(pages_at(cv, n), cv.max_pages), page_row(cv, a.layer, b, h));
 }
 
-// INT8 caches: a warp per (sequence, head, complete block) quantises the
+// INT8 / FP8 caches: a warp per (sequence, head, complete block) quantises the
 // block straight from the prefill inputs (K gathered to the kept channels),
 // exactly as appends seal it from the bf16 tail.
 __global__ void __launch_bounds__(256) prefill_seal_kernel(const PrefillArgs a, int max_blocks) {
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(256) prefill_seal_kernel(const PrefillArgs a, 
   const uint16_t* vin = a.v + (((size_t)i * a.n + t0) * cv.Hkv + h) * kHeadDim;
   const size_t rs = (size_t)cv.Hkv * kHeadDim;
   seal_block(
-      dst, hd.n_kept, [&](int r, int c) { return kin[r * rs + kept[c]]; },
+      dst, hd.n_kept, cv.kv_format, [&](int r, int c) { return kin[r * rs + kept[c]]; },
       [&](int r, int c) { return vin[r * rs + c]; }, lane);
 }
 
@@ -297,7 +299,7 @@ cudaError_t launch_prefill(const PrefillArgs& args, bool has_special, int num_sm
   prefill_kernel<<<(unsigned)blocks, 256, 0, stream>>>(args);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  if (args.cv.kv_format == kKvInt8) {
+  if (kv_quantized(args.cv.kv_format)) {
     const int max_blocks = max(0, args.n - args.cv.S - args.cv.W) / kQBlockRows;
     const int64_t warps = (int64_t)args.nb * args.cv.Hkv * max_blocks;
     if (warps > 0) {

@@ -111,15 +111,20 @@ typedef struct lk_region_info {
  *               INT8 codes with one fp32 scale per kept K channel and one per
  *               V token, scale = max|x| / 127 (fp32), code = x / scale
  *               rounded half to even, clipped to +-127; the last,
- *               incomplete block stays bf16. */
-typedef enum { LK_KV_BF16 = 0, LK_KV_INT8 = 1 } lk_kv_format;
+ *               incomplete block stays bf16.
+ *   LK_KV_FP8   as LK_KV_INT8 with FP8 codes (one of the low-precision
+ *               formats of the white paper's 5.2.1): OCP e4m3 (largest
+ *               finite value 448), scale = max|x| / 448 (fp32), code = x /
+ *               scale rounded to the nearest e4m3 value, ties to the even
+ *               code, saturated at +-448; a zero code keeps the sign. */
+typedef enum { LK_KV_BF16 = 0, LK_KV_INT8 = 1, LK_KV_FP8 = 2 } lk_kv_format;
 
 /* Cache options for lk_cache_bytes_ex / lk_cache_init_ex. */
 typedef struct lk_cache_options {
   int64_t middle_tokens;      /* < 0: contiguous region B; >= 0: paged, pools
-                                 sized as in lk_cache_bytes_paged (INT8: sealed
-                                 blocks are the pages, floor(middle_tokens/128)
-                                 per head of a class) */
+                                 sized as in lk_cache_bytes_paged (INT8 / FP8:
+                                 sealed blocks are the pages,
+                                 floor(middle_tokens/128) per head of a class) */
   int32_t kv_format;          /* lk_kv_format */
   int32_t reserved;           /* 0 */
 } lk_cache_options;
@@ -197,11 +202,12 @@ lk_status lk_cache_init_ex(lk_plan plan, void* dev_buf, size_t bytes, int32_t ba
                            int32_t capacity_tokens, const lk_cache_options* opt, void* stream,
                            lk_cache* out);
 
-/* Host copy of sealed block `block` of an INT8 cache's (layer, b, kv_head),
- * in logical order: k_codes [128][n_kept] (kept channels ascending), k_scales
- * [n_kept], v_codes [128][128], v_scales [128]; any pointer may be NULL.
- * Synchronises `stream`.  Errors: LK_ERR_STATE (not an INT8 cache),
- * LK_ERR_ARG (no such sealed block). */
+/* Host copy of sealed block `block` of an INT8 or FP8 cache's (layer, b,
+ * kv_head), in logical order: k_codes [128][n_kept] (kept channels
+ * ascending), k_scales [n_kept], v_codes [128][128], v_scales [128]; any
+ * pointer may be NULL.  Codes are one byte each: INT8 values, or e4m3 bit
+ * patterns for FP8.  Synchronises `stream`.  Errors: LK_ERR_STATE (not a
+ * quantised cache), LK_ERR_ARG (no such sealed block). */
 lk_status lk_cache_block(lk_cache cache, int32_t layer, int32_t b, int32_t kv_head, int32_t block,
                          int8_t* k_codes, float* k_scales, int8_t* v_codes, float* v_scales, void* stream);
 

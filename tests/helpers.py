@@ -88,7 +88,8 @@ class Case:
         k, v = self.history(layer)
         w = self.w
         ragged = not np.isscalar(N)
-        quant = self.kv_format == lkb.KV_INT8
+        quant = self.kv_format != lkb.KV_BF16
+        fmt = lkb.KV_FORMAT_NAMES[self.kv_format]
         if heads is None and not ragged and not quant:
             K, V = f64(k[:, :N]), f64(v[:, :N])
             return OA.decode_layer(f64(q), K, V, self.masks[layer], self.policies[layer], N, w.sink,
@@ -100,9 +101,9 @@ class Case:
             Nb = int(N[b]) if ragged else N
             K, V = f64(k[b, :Nb, h]), f64(v[b, :Nb, h])
             kept = np.nonzero(self.masks[layer, h])[0]
-            head = OQ.decode_head_quantized if quant else OA.decode_head
-            out[(b, h)] = head(f64(q[b, h * G:(h + 1) * G]), K, V, int(self.policies[layer, h]),
-                               kept, Nb, w.sink, w.local, w.local_only_window, self.flags[b])
+            args = (f64(q[b, h * G:(h + 1) * G]), K, V, int(self.policies[layer, h]), kept, Nb, w.sink, w.local,
+                    w.local_only_window, self.flags[b])
+            out[(b, h)] = OQ.decode_head_quantized(*args, fmt=fmt) if quant else OA.decode_head(*args)
         if heads is None:
             full = np.zeros((w.batch, w.num_q_heads, 128))
             for (b, h), r in out.items():
@@ -131,11 +132,11 @@ class Case:
                 assert torch.equal(ka[ri], k[b, ti, h]), (layer, b, h, "K region A")
                 assert torch.equal(va[ri], v[b, ti, h]), (layer, b, h, "V region A")
             rows, toks = OL.region_b(pol, len(kept), Nb, w.sink, w.local)
-            if len(rows) and self.kv_format == lkb.KV_INT8:
+            if len(rows) and self.kv_format != lkb.KV_BF16:
                 # complete blocks: codes and scales exactly as the oracle
                 # quantises them; the open block: bf16 tail rows
                 blocks = OQ.middle_blocks(f64(k[b, :, h]).astype(np.float32), f64(v[b, :, h]).astype(np.float32),
-                                          kept, Nb, w.sink, w.local)
+                                          kept, Nb, w.sink, w.local, fmt=lkb.KV_FORMAT_NAMES[self.kv_format])
                 assert r.sealed_blocks == len(blocks), (layer, b, h, r.sealed_blocks, len(blocks))
                 for j, (kc, ks, vc, vs) in enumerate(blocks):
                     gk, gks, gv, gvs = self.cache.block(layer, b, h, j)

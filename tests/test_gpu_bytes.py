@@ -1,15 +1,15 @@
 """lk_resident_bytes -- the numerator of every GB/s and roofline figure the
 bench reports -- against the oracle's byte counts, at the five workloads'
-full sizes: contiguous and paged bf16 caches and INT8 middles.
+full sizes: contiguous and paged bf16 caches, INT8 and paged FP8 middles.
 
 The oracle counts per (sequence, kv head) from the method's rules alone
 (LeanK article, framerc.cn, sections 3.1-3.2: sinks and window at full
 width, middle tokens on the kept channels plus their V row, nothing in the
 middle for a head with no kept channel; FastGen article, mhpn.cn, section
 3.2: the last W_loc tokens of a LOCAL head, the special tokens of a SPECIAL
-head up to its row capacity; INT8: complete 128-row middle blocks as int8
-codes plus fp32 scales).  The cache contents do not matter for the count, so
-the histories are zeros; the token ids are the workload's."""
+head up to its row capacity; INT8 / FP8: complete 128-row middle blocks as
+one-byte codes plus fp32 scales).  The cache contents do not matter for the
+count, so the histories are zeros; the token ids are the workload's."""
 import numpy as np
 import pytest
 import torch
@@ -25,7 +25,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 def _oracle_bytes(w, masks, pol, N, flags, spec_cap, kv):
     per_layer = []
-    fn = OQ.resident_bytes_quantized if kv == lkb.KV_INT8 else F.resident_bytes
+    fn = OQ.resident_bytes_quantized if kv != lkb.KV_BF16 else F.resident_bytes
     n_special = np.minimum(flags[:, :N].sum(axis=1), spec_cap) if flags is not None else np.zeros(w.batch, int)
     for l in range(w.num_layers):
         tot = 0
@@ -38,7 +38,8 @@ def _oracle_bytes(w, masks, pol, N, flags, spec_cap, kv):
 
 
 @pytest.mark.parametrize("layout,kv", [("contiguous", lkb.KV_BF16), ("paged", lkb.KV_BF16),
-                                       ("contiguous", lkb.KV_INT8)], ids=["bf16", "bf16-paged", "int8"])
+                                       ("contiguous", lkb.KV_INT8), ("paged", lkb.KV_FP8)],
+                         ids=["bf16", "bf16-paged", "int8", "fp8-paged"])
 @pytest.mark.parametrize("w", S.WORKLOADS, ids=[w.name for w in S.WORKLOADS])
 def test_resident_bytes_match_the_oracle(cuda, w, layout, kv):
     N = w.context

@@ -312,7 +312,7 @@ def test_device_status_bits_reach_the_host(cuda):
 
 
 @pytest.mark.parametrize("hq,hkv", [(4, 4), (32, 4), (12, 4)], ids=["G1", "G8", "G3"])
-@pytest.mark.parametrize("kv", [lkb.KV_BF16, lkb.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv", [lkb.KV_BF16, lkb.KV_INT8, lkb.KV_FP8], ids=["bf16", "int8", "fp8"])
 def test_query_group_sizes(cuda, hq, hkv, kv):
     # G = 1 (one query head per kv head), G = 8 (the largest group, all of the
     # mma's N) and an odd G = 3

@@ -129,6 +129,27 @@ def test_full_qwen25_7b_long_int8(cuda):
     _check_layer(case, 0, w.context, pairs, [(1, h) for h in range(w.num_kv_heads)])
 
 
+def test_full_qwen25_7b_long_fp8(cuda):
+    from decode_attention_pruned_gb300 import binding as lkb
+    w = S.WORKLOADS[3]
+    case = Case(w, total=w.context, gen_device=cuda, kv_format=lkb.KV_FP8)
+    pairs = [(b, h) for b in range(w.batch) for h in range(w.num_kv_heads)]
+    _check_layer(case, 0, w.context, pairs, [(2, h) for h in range(w.num_kv_heads)])
+
+
+def test_full_serving_b64_fp8_all_layers(cuda):
+    from decode_attention_pruned_gb300 import binding as lkb
+    w = S.WORKLOADS[2]
+    case = Case(w, total=w.context, gen_device=cuda, kv_format=lkb.KV_FP8)
+    rng = np.random.default_rng(17)
+
+    def pick(layer):
+        pairs = _sample_pairs(w, layer, 3, rng)
+        return pairs, pairs[:1]
+
+    _check_all_layers(case, w.context, pick, fused=False)
+
+
 def test_full_llama31_8b_layer_int8_paged(cuda):
     from decode_attention_pruned_gb300 import binding as lkb
     w = S.WORKLOADS[1]

@@ -1,12 +1,13 @@
-"""INT8 middle region (KIVI-style quantisation after LeanK pruning) vs the
-fp64 oracle over the dequantised cache.
+"""Quantised middle region (KIVI-style quantisation after LeanK pruning),
+INT8 and FP8 (e4m3), vs the fp64 oracle over the dequantised cache.
 
-Complete 128-row blocks of each head's middle are stored as INT8 codes with
-per-channel K scales and per-token V scales (LeanK article §4.2 and §5.2
-problem 3; the pruning white paper §5.2.1); the open block stays bf16.  The
-codes and scales of every sealed block must equal the oracle's byte for
+Complete 128-row blocks of each head's middle are stored as one-byte codes
+with per-channel K scales and per-token V scales (LeanK article §4.2 and
+§5.2 problem 3; the pruning white paper §5.2.1); the open block stays bf16.
+The codes and scales of every sealed block must equal the oracle's byte for
 byte, the tail rows must equal the inputs, and decode must match the oracle
-evaluated on the dequantised values element by element."""
+evaluated on the dequantised values element by element.  Every test runs
+for both formats."""
 import numpy as np
 import pytest
 import torch
@@ -21,7 +22,11 @@ TINY = S.WORKLOADS[0]
 LLAMA = S.WORKLOADS[1]
 SERVING = S.WORKLOADS[2]
 FASTGEN = S.WORKLOADS[4]
-Q8 = lkb.KV_INT8
+
+
+@pytest.fixture(params=[lkb.KV_INT8, lkb.KV_FP8], ids=["int8", "fp8"])
+def Q8(request):
+    return request.param
 
 
 def _max_err(o, ref):
@@ -29,7 +34,7 @@ def _max_err(o, ref):
 
 
 @pytest.mark.parametrize("counts", [(0, 64), (64, 64), None], ids=["k0-64", "k64-64", "seeded"])
-def test_tiny_seal_during_appends(cuda, counts):
+def test_tiny_seal_during_appends(cuda, Q8, counts):
     # S + W = 68: prefill 560 leaves 3 sealed blocks + 108 tail rows; the
     # appends seal a fourth block at 580 tokens
     masks = None if counts is None else S.masks_with_counts(TINY, counts)
@@ -47,7 +52,7 @@ def test_tiny_seal_during_appends(cuda, counts):
             case.check_layout(0, N)
 
 
-def test_llama_layer_all_widths(cuda):
+def test_llama_layer_all_widths(cuda, Q8):
     w = LLAMA.scaled(context=3000, batch=2)
     masks = S.masks_with_counts(w, [0, 32, 64, 96, 128, 32, 0, 64])
     case = Case(w, total=3003, masks=masks, kv_format=Q8)
@@ -67,7 +72,7 @@ def test_llama_layer_all_widths(cuda):
 
 
 @pytest.mark.parametrize("ctas", [1, 7, 0])
-def test_split_invariance(cuda, ctas):
+def test_split_invariance(cuda, Q8, ctas):
     w = LLAMA.scaled(context=2300, batch=2)
     masks = S.masks_with_counts(w, [32, 64, 0, 96, 128, 32, 32, 64])
     case = Case(w, total=2300, masks=masks, kv_format=Q8)
@@ -79,7 +84,7 @@ def test_split_invariance(cuda, ctas):
     assert _max_err(o, case.expected(0, q, 2300)) <= DECODE_TOL
 
 
-def test_prefill_equals_appends_byte_for_byte(cuda):
+def test_prefill_equals_appends_byte_for_byte(cuda, Q8):
     w = FASTGEN.scaled(num_layers=1, batch=2, context=900, policy_counts=(2, 2, 4))
     a = Case(w, total=930, kv_format=Q8)
     b = Case(w, total=930, kv_format=Q8)
@@ -94,7 +99,7 @@ def test_prefill_equals_appends_byte_for_byte(cuda):
     a.check_layout(0, 930)
 
 
-def test_fastgen_policy_mix_two_layers(cuda):
+def test_fastgen_policy_mix_two_layers(cuda, Q8):
     w = FASTGEN.scaled(num_layers=2, batch=3, context=1200, policy_counts=(6, 4, 6))
     case = Case(w, total=1203, kv_format=Q8)
     for layer in range(2):
@@ -108,7 +113,7 @@ def test_fastgen_policy_mix_two_layers(cuda):
         case.check_layout(layer, 1203)
 
 
-def test_paged_int8_release_and_refill(cuda):
+def test_paged_release_and_refill(cuda, Q8):
     w = SERVING.scaled(num_layers=1, batch=3, context=1400)
     case = Case(w, total=1500, kv_format=Q8, middle_tokens=3 * 1000)
     k, v = case.history(0)
@@ -141,7 +146,7 @@ def test_paged_int8_release_and_refill(cuda):
     case.check_layout(0, lens)
 
 
-def test_all_layers_in_one_launch(cuda):
+def test_all_layers_in_one_launch(cuda, Q8):
     w = FASTGEN.scaled(num_layers=3, batch=2, context=800, policy_counts=(2, 2, 20))
     case = Case(w, total=802, kv_format=Q8)
     L = w.num_layers

@@ -10,7 +10,7 @@ reach either case, so these tests build K, V and q to reach them:
 * climbing scores: a per-128-token offset of the scores (a random walk in
   log2 units with steps in [-6, 14]) makes later tiles beat the running max
   by more and by less than 2^8, across the full-width and middle regions and
-  across CTA splits (1, 7 and the library's count), for bf16 and INT8
+  across CTA splits (1, 7 and the library's count), for bf16, INT8 and FP8
   middles and for fused and two-launch steps;
 * peaky P: three dominant tokens (a sink, a middle and a window token) with
   near-equal scores and V rows of magnitude 6-8, beside a head with no kept
@@ -114,7 +114,7 @@ CLIMB_COUNTS = [64, 0, 32, 128]
 
 
 @pytest.mark.parametrize("ctas", [1, 7, 0], ids=["ctas1", "ctas7", "default"])
-@pytest.mark.parametrize("kv", [lkb.KV_BF16, lkb.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv", [lkb.KV_BF16, lkb.KV_INT8, lkb.KV_FP8], ids=["bf16", "int8", "fp8"])
 def test_climbing_scores_decode(cuda, kv, ctas):
     N = CLIMB_W.context
     case, q = _planted_case(CLIMB_W, CLIMB_COUNTS, N, kv, _climb(CLIMB_W, N, 5))
@@ -177,7 +177,7 @@ def _peaky(w, counts, kv, seed):
     return _planted_case(w, counts, N, kv, target, vrow, seed=seed, exact=order)
 
 
-@pytest.mark.parametrize("kv", [lkb.KV_BF16, lkb.KV_INT8], ids=["bf16", "int8"])
+@pytest.mark.parametrize("kv", [lkb.KV_BF16, lkb.KV_INT8, lkb.KV_FP8], ids=["bf16", "int8", "fp8"])
 @pytest.mark.parametrize("ctas", [1, 0], ids=["ctas1", "default"])
 def test_peaky_p_near_equal_dominant_tokens(cuda, kv, ctas):
     # o is a weighted mix of three V rows of size 6-8 with weights of equal
