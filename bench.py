@@ -63,7 +63,6 @@ FALLBACK_HBM_GBS = 6800.0
 MAX_CONTEXT_GROWTH = 0.01           # appends may lengthen the context by at most 1 %
 COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 MAX_COPIES = 256                    # rotating cache copies at most
-LOAD_SECONDS = 0.4                  # untimed decode replays before the timed steps
 
 # DRAM bytes (read + write) per decode launch from one ncu capture, keyed by
 # "<sha256[:16] of the decode kernel sources>:<workload>[/<layers>L]:<kv
@@ -364,7 +363,7 @@ def run_gpu(args, rank, local_rank, world):
         k1.record(stream)
     k1.synchronize()
     t_kg = max(1e-6, k0.elapsed_time(k1) / 1e3)
-    load_reps = int(min(20000, max(1, math.ceil(LOAD_SECONDS / t_kg))))
+    load_reps = int(min(20000, math.ceil(args.load_seconds / t_kg))) if args.load_seconds > 0 else 0
     # resident bytes of the timed steps: every copy holds the same lengths
     # (the steps rotate over them), which grow by at most one token per copy
     # and rotation; the launches' mean is the mean of the two ends
@@ -737,6 +736,8 @@ def main(argv=None):
                     help="seconds of oracle timing for cpu_baseline (half on one core, half on all)")
     ap.add_argument("--reference-budget", type=float, default=60.0)
     ap.add_argument("--reference-cores", type=int, default=0, help="oracle worker processes (0: every core)")
+    ap.add_argument("--load-seconds", type=float, default=0.4,
+                    help="untimed decode-only replays that load the GPU before the timed steps (0: none)")
     args = ap.parse_args(argv)
     d_steps, d_warm, d_e2e = DEFAULT_STEPS[args.workload]
     args.steps = d_steps if args.steps is None else args.steps
@@ -761,7 +762,8 @@ def main(argv=None):
     line = run_gpu(args, rank, local_rank, world)
     if rank == 0:
         if world == 1:
-            line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget, args.kv)
+            line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_budget, args.kv) if args.cpu_budget > 0 \
+                else None
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -917,6 +917,20 @@ void return_pages(lk_cache cache, const int64_t need[kNumPools]) {
   for (int pl = 0; pl < kNumPools; ++pl) cache->host_free[pl] += need[pl];
 }
 
+// The decode kernel's launch-fixed divisors.
+void set_divisors(const lk_cache_s* cache, DecodeArgs& a) {
+  const CacheView& cv = cache->cv;
+  a.div_bh = make_fastdiv((uint32_t)(cv.B * cv.Hkv));
+  a.div_h = make_fastdiv((uint32_t)cv.Hkv);
+  a.div_w = make_fastdiv((uint32_t)std::max(1, cv.W));
+  a.div_wloc = make_fastdiv((uint32_t)std::max(1, cv.W_loc));
+  for (int i = 0; i < 5; ++i) {
+    const int k = 32 * i;
+    a.div_cost_b[i] = make_fastdiv((uint32_t)(2 * k + 256));
+    a.div_cost_q[i] = make_fastdiv((uint32_t)(qblock_bytes(k) / kQBlockRows));
+  }
+}
+
 // Host side of a decode launch: checks, and the kernel arguments (no fused
 // append) and CTA count.
 lk_status decode_prepare(lk_cache cache, int32_t layer0, int32_t nlayers, const void* q, float* o, void* workspace,
@@ -943,6 +957,7 @@ lk_status decode_prepare(lk_cache cache, int32_t layer0, int32_t nlayers, const 
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
   a.k_new = a.v_new = nullptr;
   a.ids = nullptr;
+  set_divisors(cache, a);
   ctas = cache->decode_ctas > 0 ? cache->decode_ctas : default_decode_ctas(cache, nlayers);
   ctas = std::max(1, std::min(ctas, kMaxCtas));
   return LK_OK;
@@ -1373,6 +1388,7 @@ lk_status lk_decode_attn_static(lk_cache cache, int32_t layer, const void* q, fl
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kHeadDim));
   a.k_new = a.v_new = nullptr;
   a.ids = nullptr;
+  set_divisors(cache, a);
   int ctas = cache->decode_ctas > 0 ? cache->decode_ctas : default_decode_ctas(cache, 1);
   ctas = std::max(1, std::min(ctas, kMaxCtas));
   err = launch_decode(cache->maps, a, ctas, s);

@@ -62,8 +62,13 @@ constexpr int kQStride = kHeadDim + 8;                  // padded q row (bf16): 
 // stages in flight where full-width ones (64 KB) keep three; sealed INT8
 // blocks (21-33 KB) keep up to nine.
 constexpr int kSlots = 16;                              // barrier pairs = stages in flight at most (power of 2)
-constexpr int kRingBytes = 204 * 1024;
+constexpr int kRingBytes = 200 * 1024;
+// A launch over at most this many (layer, kv head) pairs keeps their head
+// descriptors in shared memory, copied before the dependency wait: after it
+// the work split and the producer read them there instead of through L2.
+constexpr int kMaxSmemHeads = 56;
 constexpr int kUnitsA = 2 * kHeadDim * 2;               // line cost of a full-width row: its bytes
+static_assert(kUnitsA == 2 * kHeadDim + 256, "a full-width row costs what a k = 128 middle row costs");
 constexpr uint64_t kMinCtaBytes = 64 * 1024;            // line bytes a CTA takes at least (one full-width tile)
 constexpr uint64_t kTokenUnits = 48 * 1024;             // line charge of a fused token stage (~1 us of streaming)
 constexpr int kFirst = 1, kLast = 2;
@@ -100,7 +105,8 @@ struct SmemLayout {
   static constexpr int kCBarOff = kBarOff + 2 * kSlots * 8;                  // consumer barrier
   static constexpr int kScanOff = kCBarOff + 8;
   static constexpr int kMiscOff = kScanOff + (kThreads / 32) * 8;
-  static constexpr int kBytes = kMiscOff + 12 * 8;
+  static constexpr int kHeadsOff = kMiscOff + 12 * 8;                        // head descriptors of the launch
+  static constexpr int kBytes = kHeadsOff + kMaxSmemHeads * (int)sizeof(HeadDesc);
 };
 constexpr int kSmemBytes = SmemLayout::kBytes + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
@@ -145,22 +151,30 @@ struct Entry {
 struct EntryId {
   int lr, l, b, h;
 };
+// x / d and x mod d by a launch-fixed divisor (see FastDiv), 32-bit x
+__device__ __forceinline__ uint32_t fdiv(uint32_t x, const FastDiv& f) {
+  return f.m == 0 ? x : (uint32_t)__umul64hi((uint64_t)x, f.m);
+}
+__device__ __forceinline__ uint32_t fmod(uint32_t x, const FastDiv& f) { return x - fdiv(x, f) * f.d; }
+
 __device__ __forceinline__ EntryId entry_id(const DecodeArgs& a, int e) {
   const CacheView& cv = a.cv;
   const int per_layer = cv.B * cv.Hkv;
   EntryId r;
-  r.lr = e / per_layer;
+  r.lr = (int)fdiv((uint32_t)e, a.div_bh);
   const int rem = e - r.lr * per_layer;
-  r.b = rem / cv.Hkv;
+  r.b = (int)fdiv((uint32_t)rem, a.div_h);
   r.h = rem - r.b * cv.Hkv;
   r.l = a.layer + r.lr;
   return r;
 }
 
-__device__ __forceinline__ EntryLen entry_len(const DecodeArgs& a, int e) {
+// hb: the head descriptors of the launch's layers, [nlayers][Hkv] (in
+// shared memory, or the cache's table from the launch's first layer on).
+__device__ __forceinline__ EntryLen entry_len(const DecodeArgs& a, const HeadDesc* hb, int e) {
   const CacheView& cv = a.cv;
   const EntryId id = entry_id(a, e);
-  const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+  const HeadDesc& hd = hb[id.lr * cv.Hkv + id.h];
   EntryLen r;
   r.n = __ldcg(&cv.len[id.l * cv.B + id.b]);
   r.cnt = hd.policy == kSpecial ? __ldcg(&cv.cnt[id.l * cv.B + id.b]) : 0;
@@ -176,16 +190,16 @@ __device__ __forceinline__ bool token_special(const DecodeArgs& a, int b) {
   return id >= 0 && id < a.cv.vocab && a.cv.is_special[id] != 0;
 }
 
-__device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen len) {
+__device__ __forceinline__ Entry entry_from(const DecodeArgs& a, const HeadDesc* hb, int e, EntryLen len) {
   const CacheView& cv = a.cv;
   const EntryId id = entry_id(a, e);
-  const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+  const HeadDesc& hd = hb[id.lr * cv.Hkv + id.h];
   const int N = len.n;
   Entry r{0, 0, 0, 0, -1, len, -1};
   if (hd.policy == kFull) {
     r.n_a = min(N, cv.S + cv.W);
     // a fused append into a full window replaces the slot of token N - W
-    if (len.act && N >= cv.S + cv.W) r.mrow = cv.S + (N - cv.S) % cv.W;
+    if (len.act && N >= cv.S + cv.W) r.mrow = cv.S + (int)fmod((uint32_t)(N - cv.S), a.div_w);
     if (hd.n_kept > 0) {
       const int m = max(0, N - cv.S - cv.W);
       if (kv_quantized(cv.kv_format)) {
@@ -199,7 +213,7 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
     }
   } else if (hd.policy == kLocal) {
     r.n_a = min(N, cv.W_loc);
-    if (len.act && N >= cv.W_loc) r.mrow = N % cv.W_loc;
+    if (len.act && N >= cv.W_loc) r.mrow = (int)fmod((uint32_t)N, a.div_wloc);
   } else {
     r.n_a = min(len.cnt, hd.cap_a);
   }
@@ -209,7 +223,9 @@ __device__ __forceinline__ Entry entry_from(const DecodeArgs& a, int e, EntryLen
   return r;
 }
 
-__device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, int e) { return entry_from(a, e, entry_len(a, e)); }
+__device__ __forceinline__ Entry entry_geometry(const DecodeArgs& a, const HeadDesc* hb, int e) {
+  return entry_from(a, hb, e, entry_len(a, hb, e));
+}
 
 // line costs per row = bytes streamed per row
 __device__ __forceinline__ uint64_t row_cost_b(int kb) { return (uint64_t)(2 * kb + 256); }
@@ -230,29 +246,24 @@ __device__ __forceinline__ uint64_t udiv(uint64_t a, uint64_t b) {
   return a / b;
 }
 
-// x / c for a row cost c of the line: every cost the line uses is one of
-// these constants, so the division compiles to a multiply (the producer
-// divides before its first copy of every entry)
-__device__ __forceinline__ uint64_t div_cost(uint64_t x, uint64_t c) {
-  switch (c) {
-    case 512: return x >> 9;       // full-width rows; kept-channel rows of k = 128
-    case 320: return x / 320u;     // kept-channel rows, k = 32 / 64 / 96
-    case 384: return x / 384u;
-    case 448: return x / 448u;
-    case 165: return x / 165u;     // sealed INT8 rows, k = 32 / 64 / 96 / 128
-    case 198: return x / 198u;
-    case 231: return x / 231u;
-    case 264: return x / 264u;
-    default: return udiv(x, c);
-  }
+// x / c for a row cost c of the line, given c's FastDiv f: one multiply
+// while x (an offset inside one entry) fits 32 bits.  The producer divides
+// before its first copy of every entry.
+__device__ __forceinline__ uint64_t div_cost(uint64_t x, const FastDiv& f) {
+  return (x >> 32) == 0 ? fdiv((uint32_t)x, f) : udiv(x, f.d);
 }
 
 // Rows r in [0, n) of a region whose row r sits at line offset o0 + c*r and
-// starts inside [start, end): r in [r0, r1).
-__device__ __forceinline__ void rows_in_range(uint64_t o0, uint64_t c, int n, uint64_t start, uint64_t end,
+// starts inside [start, end): r in [r0, r1).  f: the FastDiv of c.
+__device__ __forceinline__ void rows_in_range(uint64_t o0, const FastDiv& f, int n, uint64_t start, uint64_t end,
                                               int& r0, int& r1) {
-  r0 = start > o0 ? (int)min((uint64_t)n, div_cost(start - o0 + c - 1, c)) : 0;
-  r1 = end > o0 ? (int)min((uint64_t)n, div_cost(end - o0 + c - 1, c)) : 0;
+  const uint64_t c = f.d;
+  if (n == 0) {
+    r0 = r1 = 0;
+    return;
+  }
+  r0 = start > o0 ? (int)min((uint64_t)n, div_cost(start - o0 + c - 1, f)) : 0;
+  r1 = end > o0 ? (int)min((uint64_t)n, div_cost(end - o0 + c - 1, f)) : 0;
 }
 
 // The CTA whose range [floor(iC/P), floor((i+1)C/P)) holds offset x < C:
@@ -357,16 +368,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (uint64_t)a.part ^ (uint64_t)a.part_ml ^ (uint64_t)a.counters ^ a.wait_limit_ns;
     touch ^= (uint64_t)(cv.B ^ cv.Hkv ^ cv.S ^ cv.W ^ cv.W_loc ^ cv.max_pages ^ cv.kv_format ^ a.layer ^ a.nlayers ^
                         cv.G ^ cv.Hq);
+#pragma unroll
+    for (int i = 0; i < kNumMaps; ++i) touch ^= (uint64_t)maps.block_rows[i];
     asm volatile("" ::"l"(touch));
   }
-  // the head table is static (written once at cache init): load it while
-  // the preceding kernel finishes, which also walks the page table for the
-  // cache header (a prefetch may be dropped on a TLB miss; a load is not).
-  // Lengths and special counts are written by that kernel, so they are read
-  // only after the dependency wait.
-  {
+  // The head table is static (written once at cache init): read it while
+  // the preceding kernel finishes -- into shared memory when the launch has
+  // few heads (the work split and the producer then read it there), else
+  // touched, which also walks the page table for the cache header (a
+  // prefetch may be dropped on a TLB miss; a load is not).  Lengths and
+  // special counts are written by that kernel, so they are read only after
+  // the dependency wait.
+  const int nheads = a.nlayers * cv.Hkv;
+  const bool heads_in_smem = nheads <= kMaxSmemHeads;
+  HeadDesc* sheads = reinterpret_cast<HeadDesc*>(sm + SmemLayout::kHeadsOff);
+  const HeadDesc* hb = heads_in_smem ? sheads : cv.heads + (size_t)a.layer * cv.Hkv;
+  if (heads_in_smem) {
+    static_assert(sizeof(HeadDesc) % 8 == 0, "head descriptors copy as 8-byte words");
+    constexpr int kWords = (int)sizeof(HeadDesc) / 8;
+    const uint64_t* src = reinterpret_cast<const uint64_t*>(cv.heads + (size_t)a.layer * cv.Hkv);
+    uint64_t* dst = reinterpret_cast<uint64_t*>(sheads);
+    for (int i = tid; i < nheads * kWords; i += kThreads) dst[i] = src[i];
+  } else {
     int64_t touch = 0;
-    for (int h = tid; h < a.nlayers * cv.Hkv; h += kThreads) touch += cv.heads[a.layer * cv.Hkv + h].row_a;
+    for (int h = tid; h < nheads; h += kThreads) touch += cv.heads[a.layer * cv.Hkv + h].row_a;
     asm volatile("" ::"l"(touch));
   }
   {
@@ -409,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (E <= 32) {
     // few entries: every warp scans them all itself (lane = entry), so no
     // block barrier stands between the length loads and the first copy
-    const Entry g = lane < E ? entry_geometry(a, lane) : Entry{0, 0, 0, 0, -1, {0, 0, 0}, -1};
+    const Entry g = lane < E ? entry_geometry(a, hb, lane) : Entry{0, 0, 0, 0, -1, {0, 0, 0}, -1};
     const uint64_t cost = entry_cost(g);
     uint64_t incl = cost;
 #pragma unroll
@@ -439,10 +464,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the first two entries of the chunk keep their geometry for the second
     // pass
     Entry g0{0, 0, 0, 0, -1, {0, 0, 0}, -1}, g1{0, 0, 0, 0, -1, {0, 0, 0}, -1};
-    if (e_lo < e_hi) g0 = entry_geometry(a, e_lo);
-    if (e_lo + 1 < e_hi) g1 = entry_geometry(a, e_lo + 1);
+    if (e_lo < e_hi) g0 = entry_geometry(a, hb, e_lo);
+    if (e_lo + 1 < e_hi) g1 = entry_geometry(a, hb, e_lo + 1);
     uint64_t local = entry_cost(g0) + entry_cost(g1);
-    for (int e = e_lo + 2; e < e_hi; ++e) local += entry_cost(entry_geometry(a, e));
+    for (int e = e_lo + 2; e < e_hi; ++e) local += entry_cost(entry_geometry(a, hb, e));
     uint64_t incl = local;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -465,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int found = -1;
       Entry f{0, 0, 0, 0, -1, {0, 0, 0}, -1};
       for (int e = e_lo; found < 0 && e < e_hi; ++e) {
-        const Entry g = e == e_lo ? g0 : e == e_lo + 1 ? g1 : entry_geometry(a, e);
+        const Entry g = e == e_lo ? g0 : e == e_lo + 1 ? g1 : entry_geometry(a, hb, e);
         const uint64_t c = entry_cost(g);
         if (acc + c > start) {
           found = e;
@@ -555,26 +580,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       // loaded one entry ahead
       Entry g = fg;
       EntryLen ahead{0, 0, 0};
-      if (e + 1 < E) ahead = entry_len(a, e + 1);
+      if (e + 1 < E) ahead = entry_len(a, hb, e + 1);
       for (; ok && e < E && off < end; ++e) {
         if (e != e0) {
-          g = entry_from(a, e, ahead);
-          if (e + 1 < E) ahead = entry_len(a, e + 1);
+          g = entry_from(a, hb, e, ahead);
+          if (e + 1 < E) ahead = entry_len(a, hb, e + 1);
         }
         const uint64_t cost = entry_cost(g);
         const uint64_t cq = row_cost_q(g.kb), cb = row_cost_b(g.kb);
+        const FastDiv& dq = a.div_cost_q[g.kb >> 5];
+        const FastDiv& dbr = a.div_cost_b[g.kb >> 5];
+        const FastDiv& da = a.div_cost_b[kHeadDim >> 5];     // a full-width row costs what a k = 128 row does
         const uint64_t xu = token_units(g);
         const uint64_t off_q = off + (uint64_t)kUnitsA * g.n_a + xu;
         const uint64_t off_b = off_q + cq * g.n_q;
         int a0, a1, q0, q1, b0, b1;
         if (xu == 0) {
-          rows_in_range(off, kUnitsA, g.n_a, start, end, a0, a1);
+          rows_in_range(off, da, g.n_a, start, end, a0, a1);
         } else {
           // full-width rows 0 .. anc, the token's charge, rows anc+1 .. n_a-1
           const int n1 = g.anc + 1;
           int p0, p1, s0, s1;
-          rows_in_range(off, kUnitsA, n1, start, end, p0, p1);
-          rows_in_range(off + (uint64_t)kUnitsA * n1 + xu, kUnitsA, g.n_a - n1, start, end, s0, s1);
+          rows_in_range(off, da, n1, start, end, p0, p1);
+          rows_in_range(off + (uint64_t)kUnitsA * n1 + xu, da, g.n_a - n1, start, end, s0, s1);
           if (p1 > p0) {
             a0 = p0;
             a1 = s1 > s0 ? n1 + s1 : p1;
@@ -585,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             a0 = a1 = 0;
           }
         }
-        rows_in_range(off_q, cq, g.n_q, start, end, q0, q1);
-        rows_in_range(off_b, cb, g.n_b, start, end, b0, b1);
+        rows_in_range(off_q, dq, g.n_q, start, end, q0, q1);
+        rows_in_range(off_b, dbr, g.n_b, start, end, b0, b1);
         // paged bf16 region B: tiles end at page boundaries (a box that starts
         // inside a page is clipped at its end: the page is a block of the
         // view).  Sealed INT8 blocks: one tile per block, whole block loaded,
@@ -602,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nt > 0) {
           const EntryId id = entry_id(a, e);
           const int b = id.b;
-          const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+          const HeadDesc& hd = hb[id.lr * cv.Hkv + id.h];
           const int32_t* pt =
               cv.page_table + (((int64_t)id.l * cv.B + b) * cv.Hkv + id.h) * cv.max_pages;
           const uint64_t last_row_off = g.n_b > 0   ? off_b + cb * (g.n_b - 1)
@@ -822,11 +850,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // consumer threads; callers sync before reading ex.
   auto fused_extras = [&](int e) {
     const EntryId id = entry_id(a, e);
-    const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
-    const EntryLen len = entry_len(a, e);
+    const HeadDesc& hd = hb[id.lr * cv.Hkv + id.h];
+    const EntryLen len = entry_len(a, hb, e);
     const bool add_new = len.act && (hd.policy != kSpecial || (token_special(a, id.b) && len.cnt < hd.cap_a));
     const bool add_ev = len.act && hd.policy == kFull && hd.n_kept > 0 && len.n >= cv.S + cv.W;
-    const int64_t slot = hd.row_a + (int64_t)id.b * hd.cap_a + (add_ev ? cv.S + (len.n - cv.S) % cv.W : 0);
+    const int64_t slot =
+        hd.row_a + (int64_t)id.b * hd.cap_a + (add_ev ? cv.S + (int)fmod((uint32_t)(len.n - cv.S), a.div_w) : 0);
     const size_t src = (((size_t)id.lr * cv.B + id.b) * cv.Hkv + id.h) * kHeadDim;
     if (warp < G) {
       const uint16_t* qg = a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G + warp) * kHeadDim;
@@ -869,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // fused_extras and a consumer barrier.
   auto fused_edit = [&](int e) {
     const EntryId id = entry_id(a, e);
-    const EntryLen len = entry_len(a, e);
+    const EntryLen len = entry_len(a, hb, e);
     if (!len.act) return;
     const size_t src = (((size_t)id.lr * cv.B + id.b) * cv.Hkv + id.h) * kHeadDim;
     append_head<false>(cv, id.l, id.b, id.h, len.n, len.cnt, token_special(a, id.b), a.k_new + src,
@@ -879,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // entries with no resident token, by CTA (e mod grid): o = 0, or with a
   // fused append the new token alone
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
-    if (entry_cost(entry_geometry(a, e)) != 0) continue;
+    if (entry_cost(entry_geometry(a, hb, e)) != 0) continue;
     const EntryId id = entry_id(a, e);
     float* dst = a.o + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
     if (fused) {
@@ -917,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the previous q with a consumer barrier.
   auto stage_q = [&](int e) {
     const EntryId id = entry_id(a, e);
-    const HeadDesc& hd = cv.heads[id.l * cv.Hkv + id.h];
+    const HeadDesc& hd = hb[id.lr * cv.Hkv + id.h];
     const int16_t* kept = cv.kept + ((size_t)id.l * cv.Hkv + id.h) * kHeadDim;
     const int kk = hd.policy == kFull ? hd.n_kept : 0;
     const uint16_t* qg = a.q + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
@@ -1343,11 +1372,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!single) {
-        __threadfence();
+        // The barrier orders every thread's partial stores before thread 0's
+        // fence, which releases them all (fences are cumulative) ahead of the
+        // counter; the entry's last CTA acquires the other partials the same
+        // way before its barrier hands them to its threads.
         consumer_sync(cbar, cphase, a);
         if (ct == 0) {
+          __threadfence();
           const int prev = atomicAdd(&a.counters[d.e], 1);
-          misc[2] = (prev == d.last_cta - d.first_cta) ? 1 : 0;
+          const bool last = prev == d.last_cta - d.first_cta;
+          if (last) __threadfence();
+          misc[2] = last ? 1 : 0;
         }
         consumer_sync(cbar, cphase, a);
         if (misc[2]) {
@@ -1357,7 +1392,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // while the (m, l) pairs are staged into shared memory, so a chunk
           // costs one round trip; a warp per query head turns the pairs into
           // weights w_c = 2^(m_c - M) / L.
-          __threadfence();
           const int np = d.last_cta - d.first_cta + 1;
           const size_t slot0 = (size_t)d.first_cta + d.e;
           const float4* src = reinterpret_cast<const float4*>(a.part) + slot0 * G * 32;

@@ -26,6 +26,19 @@ struct DecodeMaps {
   int32_t block_rows[kNumMaps];
 };
 
+// x / d for a 32-bit x and a divisor fixed for a launch: m = ceil(2^64 / d)
+// for d >= 2 (m = 0 stands for d = 1), q = high 64 bits of x * m.  Exact for
+// every 32-bit x: x * m / 2^64 = x / d + x * eps / 2^64 with eps < 1, and
+// x * eps / 2^64 < 1 / d because x * d < 2^64.
+struct FastDiv {
+  uint64_t m;
+  uint32_t d;
+  uint32_t pad;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  return FastDiv{d <= 1 ? 0ull : ~0ull / d + 1, d, 0u};
+}
+
 struct DecodeArgs {
   CacheView cv;
   int32_t layer;            // first layer
@@ -44,6 +57,12 @@ struct DecodeArgs {
   const uint16_t* k_new;    // bf16 [nlayers][B][Hkv][128]
   const uint16_t* v_new;
   const int32_t* ids;       // [B] or null
+  // divisions of the work split and the producer, by divisors fixed for the
+  // launch: sequences x kv heads, kv heads, window, LOCAL window; and the
+  // line cost of a middle row per kept width (index k / 32): bf16 rows
+  // 2k + 256 bytes, sealed INT8 / FP8 rows 132 (k + 128) / 128 bytes
+  FastDiv div_bh, div_h, div_w, div_wloc;
+  FastDiv div_cost_b[5], div_cost_q[5];
 };
 
 struct AppendArgs {
