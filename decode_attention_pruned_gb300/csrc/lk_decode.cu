@@ -19,9 +19,9 @@
 //     such that every CTA takes at least 64 KB; the CTAs touching an entry
 //     are exactly first..last and each writes one partial.
 //   * Per CTA: warp 8 (one lane) issues one TMA load per K tile and one per V
-//     tile (swizzled boxes), or one bulk copy per sealed INT8 block, into a
-//     FIFO ring of variable-size stages with sixteen mbarrier slots; warps
-//     0-7 each take 16 rows of every 128-row tile.
+//     tile (swizzled boxes), or one bulk copy per two or three consecutive
+//     sealed blocks, into a FIFO ring of variable-size stages with sixteen
+//     mbarrier slots; warps 0-7 each take 16 rows of every 128-row tile.
 //   * Tensor cores (mma.sync m16n8k16, fp32 accumulate) with tokens on M:
 //     S^T[16 tok x 8] = K[16 x w] Q^T[w x 8] and O^T[128 x 8] += V^T P^T, so
 //     the G <= 8 query heads only pad N.  P goes from the S^T accumulator to
@@ -67,6 +67,11 @@ constexpr int kRingBytes = 200 * 1024;
 // descriptors in shared memory, copied before the dependency wait: after it
 // the work split and the producer read them there instead of through L2.
 constexpr int kMaxSmemHeads = 56;
+// Sealed blocks per stage: three of k = 32 (62 KB), else two (up to 66 KB).
+constexpr int kQPerStageNarrow = 3;
+constexpr int kQPerStage = 2;
+static_assert(kQPerStageNarrow * 132 * (32 + 128) <= 66 * 1024 && kQPerStage * 132 * (128 + 128) <= 66 * 1024,
+              "three stages of sealed blocks fit the ring");
 constexpr int kUnitsA = 2 * kHeadDim * 2;               // line cost of a full-width row: its bytes
 static_assert(kUnitsA == 2 * kHeadDim + 256, "a full-width row costs what a k = 128 middle row costs");
 constexpr uint64_t kMinCtaBytes = 64 * 1024;            // line bytes a CTA takes at least (one full-width tile)
@@ -85,7 +90,8 @@ struct StageDesc {
   int32_t last_cta;
   uint32_t koff;       // ring offset of the K tile; the V tile follows it
   int32_t mrow;        // tile row left out (fused append: the window slot being replaced), or -1
-  int32_t n, cnt;      // region 3: the entry's length and special count before the append
+  int32_t n, cnt;      // region 3: the entry's length and special count before the append;
+                       // region 2: n = sealed blocks in the stage
 };
 // region-3 descriptors: mrow holds these flags, width the kept channels of
 // the evicted window row (0: none)
@@ -617,12 +623,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         rows_in_range(off_b, dbr, g.n_b, start, end, b0, b1);
         // paged bf16 region B: tiles end at page boundaries (a box that starts
         // inside a page is clipped at its end: the page is a block of the
-        // view).  Sealed INT8 blocks: one tile per block, whole block loaded,
-        // rows masked.
+        // view).  Sealed blocks: whole blocks loaded, rows outside the range
+        // masked; a stage takes up to qper consecutive blocks (one bulk copy,
+        // or one per page), so the producer's and the consumers' per-stage
+        // work is paid once per 42-66 KB.
         const bool paged = cv.max_pages > 0;
         const bool bpaged = paged && cv.kv_format == kKvBf16;
         const int nta = (a1 - a0 + kTileRows - 1) / kTileRows;
-        const int ntq = q1 <= q0 ? 0 : (q1 - 1) / kQBlockRows - q0 / kQBlockRows + 1;
+        const int qfirst = q0 / kQBlockRows;
+        const int nqb = q1 <= q0 ? 0 : (q1 - 1) / kQBlockRows - qfirst + 1;   // sealed blocks in range
+        const int qper = g.kb == 32 ? kQPerStageNarrow : kQPerStage;
+        const int ntq = (nqb + qper - 1) / qper;
         const int ntb = b1 <= b0   ? 0
                         : bpaged ? (b1 - 1) / kPageRows - b0 / kPageRows + 1
                                  : (b1 - b0 + kTileRows - 1) / kTileRows;
@@ -652,23 +663,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int anc = g.anc;
           const int xj = fused_launch && anc >= 0 && anc >= a0 && anc < a1 ? (anc - a0) / kTileRows : -1;
           int32_t page_ahead = 0;
+          int32_t qpg_ahead[kQPerStageNarrow] = {0, 0, 0};
           for (int j = 0; j < nt; ++j) {
             const int region = j < nta ? 0 : j < nta + ntq ? 2 : 1;
             const int width = region == 0 ? kHeadDim : g.kb;
-            int r, rend, rlo = 0;
+            int r, rend, rlo = 0, nq = 0;
             int32_t page = 0;
+            int32_t qpg[kQPerStageNarrow] = {0, 0, 0};
             if (region == 0) {
               r = a0 + j * kTileRows;
               rend = min(a1, r + kTileRows);
             } else if (region == 2) {
-              const int blk = q0 / kQBlockRows + (j - nta);
+              const int blk = qfirst + (j - nta) * qper;
+              nq = min(qper, qfirst + nqb - blk);
               r = max(q0, blk * kQBlockRows);
-              rend = min(q1, (blk + 1) * kQBlockRows);
+              rend = min(q1, (blk + nq) * kQBlockRows);
               rlo = r - blk * kQBlockRows;
               if (paged) {
-                page = j == nta ? __ldcg(pt + blk) : page_ahead;
-                if (j + 1 < nta + ntq) page_ahead = __ldcg(pt + blk + 1);
-                page = max(0, page);
+                // page ids load one stage ahead (and before the slot wait); a
+                // missing page (status already recorded) reads page 0
+#pragma unroll
+                for (int i = 0; i < kQPerStageNarrow; ++i) {
+                  if (j == nta && i < nq) qpg_ahead[i] = __ldcg(pt + blk + i);
+                  qpg[i] = max(0, qpg_ahead[i]);
+                }
+                if (j + 1 < nta + ntq) {
+                  const int nb = blk + qper, nq2 = min(qper, qfirst + nqb - nb);
+#pragma unroll
+                  for (int i = 0; i < kQPerStageNarrow; ++i)
+                    if (i < nq2) qpg_ahead[i] = __ldcg(pt + nb + i);
+                }
               } else {
                 page = b * hd.qblocks + blk;
               }
@@ -685,9 +709,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               r = b0 + (j - nta - ntq) * kTileRows;
               rend = min(b1, r + kTileRows);
             }
-            const uint32_t bytes = stage_bytes(region, width);
+            const uint32_t bytes = region == 2 ? (uint32_t)(nq * qblock_bytes(width)) : stage_bytes(region, width);
             uint32_t at = 0;
-            if (!reserve(ring_bytes(region, width), at)) {
+            if (!reserve(region == 2 ? (bytes + 1023u) & ~1023u : ring_bytes(region, width), at)) {
               ok = false;
               break;
             }
@@ -703,7 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             d.last_cta = lc;
             d.koff = at;
             d.mrow = region == 0 && g.mrow >= r && g.mrow < rend ? g.mrow - r : -1;
-            d.n = d.cnt = 0;
+            d.n = nq;         // region 2: sealed blocks in the stage
+            d.cnt = 0;
             desc[stage] = d;
             const uint32_t fb = bar_full + 8 * stage;
             mbar_arrive_expect_tx(fb, bytes);
@@ -722,7 +747,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(vdst, &maps.m[kMapFlat + kPoolV], 0, row, 0, fb, policy);
               }
             } else if (region == 2) {
-              bulk_load(kdst, cv.qpool + hd.qoff + (int64_t)page * bytes, bytes, fb, policy);
+              const uint32_t qb = (uint32_t)qblock_bytes(width);
+              if (!paged) {
+                // a sequence's blocks are consecutive: one copy for the stage
+                bulk_load(kdst, cv.qpool + hd.qoff + (int64_t)page * qb, bytes, fb, policy);
+              } else {
+#pragma unroll
+                for (int i = 0; i < kQPerStageNarrow; ++i)
+                  if (i < nq) bulk_load(kdst + i * qb, cv.qpool + hd.qoff + (int64_t)qpg[i] * qb, qb, fb, policy);
+              }
             } else {
               // block: the sequence's region-B rows, or the page
               const int32_t blk = bpaged ? page : b;
@@ -999,11 +1032,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
 
+    // A stage of sealed blocks holds d.n consecutive blocks of the entry (one
+    // softmax runs through them in order); any other stage is one tile.
+    const int nsub = kQ8 && d.region == 2 ? d.n : 1;
+    const uint32_t sub_bytes = kQ8 && d.region == 2 ? (uint32_t)qblock_bytes(d.width) : 0u;
+#pragma unroll 1
+    for (int sb = 0; sb < nsub; ++sb) {
     // valid rows rlo .. rhi - 1 of the tile (sealed blocks may be shared with
     // another CTA) except mrow; the warp works if one of its 16 rows is valid
     // (a block of masked rows would leave the running max at -inf)
-    const int rlo = d.rlo, rhi = d.rlo + d.nrows;
-    const uint32_t kbase = base + SmemLayout::kRingOff + d.koff;
+    const int rlo = max(0, d.rlo - sb * kQBlockRows), rhi = min(kTileRows, d.rlo + d.nrows - sb * kQBlockRows);
+    const uint32_t koff = d.koff + (uint32_t)sb * sub_bytes;
+    const uint32_t kbase = base + SmemLayout::kRingOff + koff;
     const int wlo = max(r0, rlo), whi = min(r0 + 16, rhi);
     if (whi - wlo - (d.mrow >= wlo && d.mrow < whi ? 1 : 0) > 0) {
       // two independent accumulators halve the mma dependency chain
@@ -1012,7 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- sealed INT8 block: S^T = K_codes (f16, exact) . Q'^T with
         // Q' = q[kept] * (K scale of the channel), split into f16 hi + lo
         const int kb = d.width;
-        const float* ksc = reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + d.koff + qblock_ksoff(kb));
+        const float* ksc = reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + koff + qblock_ksoff(kb));
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
           if (2 * kp < (kb >> 4)) {
@@ -1117,7 +1157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the token), split into f16 hi + lo
         const uint32_t vbase = kbase + (uint32_t)qblock_voff(d.width);
         const float* vsc =
-            reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + d.koff + qblock_vsoff(d.width));
+            reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + koff + qblock_vsoff(d.width));
         const float sv0 = vsc[r0 + gid], sv1 = vsc[r0 + gid + 8];
         const float q0 = p0 * sv0, q1 = p1 * sv0, q2 = p2 * sv1, q3 = p3 * sv1;
         if (kFmt == kKvInt8) {
@@ -1164,6 +1204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    }   // sub-blocks of the stage
     if (!kQ8 && d.region == 3) {
       // ---- fused append: the new token (and the window row it evicts into
       // the middle, scored on the kept channels) join warp 0's running
