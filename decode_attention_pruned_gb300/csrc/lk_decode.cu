@@ -376,6 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         cv.G ^ cv.Hq);
 #pragma unroll
     for (int i = 0; i < kNumMaps; ++i) touch ^= (uint64_t)maps.block_rows[i];
+    touch ^= a.div_bh.m ^ a.div_h.m ^ a.div_w.m ^ a.div_wloc.m ^ (uint64_t)a.scale_log2 ^ (uint64_t)a.k_new ^
+             (uint64_t)a.v_new ^ (uint64_t)a.ids;
+#pragma unroll
+    for (int i = 0; i < 5; ++i) touch ^= a.div_cost_b[i].m ^ a.div_cost_q[i].m ^ a.div_cost_b[i].d ^ a.div_cost_q[i].d;
     asm volatile("" ::"l"(touch));
   }
   // The head table is static (written once at cache init): read it while
@@ -583,14 +587,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int e = e0;
       uint64_t off = first_off;
       // entry geometry: the first from the scan, later ones from lengths
-      // loaded one entry ahead
+      // loaded one entry ahead -- after the entry's first copy is issued, so
+      // that no copy waits behind those loads
       Entry g = fg;
       EntryLen ahead{0, 0, 0};
-      if (e + 1 < E) ahead = entry_len(a, hb, e + 1);
+      bool have_ahead = false;
       for (; ok && e < E && off < end; ++e) {
         if (e != e0) {
-          g = entry_from(a, hb, e, ahead);
-          if (e + 1 < E) ahead = entry_len(a, hb, e + 1);
+          g = entry_from(a, hb, e, have_ahead ? ahead : entry_len(a, hb, e));
+          have_ahead = false;
         }
         const uint64_t cost = entry_cost(g);
         const uint64_t cq = row_cost_q(g.kb), cb = row_cost_b(g.kb);
@@ -782,6 +787,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             ++issued;
+            if (j == 0 && e + 1 < E) {
+              ahead = entry_len(a, hb, e + 1);
+              have_ahead = true;
+            }
             if (fc < 0) {
               fc = range_owner(off, C, P);
               lc = range_owner(last_row_off, C, P);
