@@ -68,31 +68,44 @@ MAX_COPIES = 256                    # rotating cache copies at most
 # "<sha256[:16] of the decode kernel sources>:<workload>[/<layers>L]:<kv
 # format>:<fused | decode>" (the bench reports null when the kernel changed
 # since the capture).  The 32-layer launches are too large to capture with
-# the multi-pass sections; their entries scale the 4-layer capture's
-# traffic per algorithmic byte to the full launch's algorithmic bytes (the
-# 2- and 4-layer captures give 1.0108 and 1.0059 of the algorithmic bytes
-# for serving_b64, 1.0200 and 1.0148 for fastgen_mix; with INT8 middles
-# 1.0145 and 1.0086, 1.0378 and 1.0234).
+# multi-pass metrics; their entries are the traffic per algorithmic byte of
+# the same workload's 4-layer capture (the 2-layer one is listed beside it:
+# the ratio falls as the launch grows, since the excess is mostly per CTA --
+# split partials, each CTA's last box past its range end), applied to the
+# full launch's algorithmic bytes.
 NCU_TRAFFIC = {
-    "69f4f2651982a365:llama31_8b_layer:bf16:fused": 86260992 + 2471424,
-    "69f4f2651982a365:qwen25_7b_long:bf16:fused": 513990656 + 3203840,
-    "69f4f2651982a365:qwen25_7b_long:int8:decode": 275990784 + 3170048,
-    "69f4f2651982a365:serving_b64/2L:bf16:decode": 943220736 + 4510976,
-    "69f4f2651982a365:serving_b64/4L:bf16:decode": 2175133440 + 5291264,
-    "69f4f2651982a365:fastgen_mix/2L:bf16:fused": 441189120 + 3350272,
-    "69f4f2651982a365:fastgen_mix/4L:bf16:fused": 864369920 + 3672064,
-    "69f4f2651982a365:serving_b64:bf16:decode": 19795624561,
-    "69f4f2651982a365:fastgen_mix:bf16:fused": 10545616751,
-    "69f4f2651982a365:llama31_8b_layer:int8:decode": 46448384 + 1536,
-    "69f4f2651982a365:serving_b64/2L:int8:decode": 634033664 + 4177664,
-    "69f4f2651982a365:serving_b64/4L:int8:decode": 1420505344 + 4938240,
-    "69f4f2651982a365:fastgen_mix/2L:int8:decode": 262525696 + 3104768,
-    "69f4f2651982a365:fastgen_mix/4L:int8:decode": 511828480 + 3425280,
-    "69f4f2651982a365:serving_b64:int8:decode": 12655465598,
-    "69f4f2651982a365:fastgen_mix:int8:decode": 6019713306,
+    "5e7aea585db78f34:tiny:bf16:decode": 525568,
+    "5e7aea585db78f34:llama31_8b_layer:bf16:fused": 88086784,
+    "5e7aea585db78f34:llama31_8b_layer:bf16:decode": 88168960,
+    "5e7aea585db78f34:llama31_8b_layer:int8:decode": 46443520,
+    "5e7aea585db78f34:llama31_8b_layer:fp8:decode": 46442752,
+    "5e7aea585db78f34:qwen25_7b_long:bf16:fused": 517348864,
+    "5e7aea585db78f34:qwen25_7b_long:int8:decode": 278787328,
+    "5e7aea585db78f34:qwen25_7b_long:fp8:decode": 278737664,
+    "5e7aea585db78f34:serving_b64/2L:bf16:decode": 947137536,
+    "5e7aea585db78f34:serving_b64/4L:bf16:decode": 2180094208,
+    "5e7aea585db78f34:serving_b64/2L:bf16:fused": 946799104,
+    "5e7aea585db78f34:serving_b64/4L:bf16:fused": 2180032000,
+    "5e7aea585db78f34:serving_b64/2L:int8:decode": 637889792,
+    "5e7aea585db78f34:serving_b64/4L:int8:decode": 1425141504,
+    "5e7aea585db78f34:serving_b64/2L:fp8:decode": 637803008,
+    "5e7aea585db78f34:serving_b64/4L:fp8:decode": 1425130752,
+    "5e7aea585db78f34:fastgen_mix/2L:bf16:fused": 445602048,
+    "5e7aea585db78f34:fastgen_mix/4L:bf16:fused": 867552000,
+    "5e7aea585db78f34:fastgen_mix/2L:int8:decode": 265468160,
+    "5e7aea585db78f34:fastgen_mix/4L:int8:decode": 514942464,
+    "5e7aea585db78f34:fastgen_mix/2L:fp8:decode": 265115392,
+    "5e7aea585db78f34:fastgen_mix/4L:fp8:decode": 514908672,
 }
-# entries scaled from a smaller capture of the same workload (see above)
-NCU_TRAFFIC_SCALED = {"serving_b64", "fastgen_mix"}
+# 32-layer launches: DRAM bytes per algorithmic byte of the 4-layer capture
+NCU_TRAFFIC_RATIO = {
+    "5e7aea585db78f34:serving_b64:bf16:decode": 2180094208 / 2178351104,
+    "5e7aea585db78f34:serving_b64:int8:decode": 1425141504 / 1396178944,
+    "5e7aea585db78f34:serving_b64:fp8:decode": 1425130752 / 1396178944,
+    "5e7aea585db78f34:fastgen_mix:bf16:fused": 867552000 / 856061952,
+    "5e7aea585db78f34:fastgen_mix:int8:decode": 514942464 / 504039424,
+    "5e7aea585db78f34:fastgen_mix:fp8:decode": 514908672 / 504039424,
+}
 
 
 def _rank_env():
@@ -474,7 +487,11 @@ def run_gpu(args, rank, local_rank, world):
     peak, peak_kind = _peaks()
     achieved = alg_bytes / kernel_s / 1e9
     wkey = w.name if w.num_layers == S.WORKLOAD_BY_NAME[w.name].num_layers else f"{w.name}/{w.num_layers}L"
-    traffic = NCU_TRAFFIC.get(f"{_decode_source_hash()}:{wkey}:{args.kv}:{'fused' if fused else 'decode'}")
+    tkey = f"{_decode_source_hash()}:{wkey}:{args.kv}:{'fused' if fused else 'decode'}"
+    traffic = NCU_TRAFFIC.get(tkey)
+    traffic_scaled = traffic is None and tkey in NCU_TRAFFIC_RATIO
+    if traffic_scaled:
+        traffic = int(round(NCU_TRAFFIC_RATIO[tkey] * alg_bytes))
 
     line = {
         "metric": METRIC,
@@ -507,7 +524,8 @@ def run_gpu(args, rank, local_rank, world):
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic,
             "traffic_source": None if traffic is None else
-            ("4-layer ncu capture scaled by algorithmic bytes" if wkey in NCU_TRAFFIC_SCALED else "ncu capture"),
+            ("the 4-layer ncu capture's DRAM bytes per algorithmic byte x this launch's algorithmic bytes"
+             if traffic_scaled else "ncu capture"),
             "peak_source": peak_kind, "kernel": kernel_name,
             "kernel_ms": kernel_s * 1e3, "alg_bytes_per_launch": alg_bytes,
             "timed_launches": K if fused else reps * n_kg, "kernel_timing": kernel_timing,
