@@ -160,3 +160,53 @@ def test_all_layers_in_one_launch(cuda, Q8):
     case.cache.check()
     for layer in range(L):
         assert _max_err(o[layer], case.expected(layer, qs[layer], 801)) <= DECODE_TOL, layer
+
+
+def test_sealing_edge_values_match_the_oracle_bit_for_bit(cuda, Q8):
+    # Values planted on the quantiser's decision edges, in units of a scale
+    # that is a power of two (so x / scale is exact in fp32): exact ties
+    # (INT8 .5 steps; FP8 midpoints between neighbouring e4m3 values),
+    # values one fp32 ulp either side of a tie, tiny negatives that round to
+    # a zero code, zeros of both signs, and the absmax itself.  Every sealed
+    # byte and scale must equal the oracle's (the same fp32 decisions).
+    from oracle import quant as OQ
+    w = TINY.scaled(num_q_heads=2, num_kv_heads=1, context=4 + 64 + 256)
+    masks = S.masks_with_counts(w, [32])
+    N = w.context
+    case = Case(w, total=N, masks=masks, kv_format=Q8)
+    kept = np.nonzero(masks[0, 0])[0]
+    rs = np.random.default_rng(5)
+    if Q8 == lkb.KV_FP8:
+        qmax, scale = 448.0, 2.0 ** -6
+        grid = OQ.e4m3_value(np.arange(0x7F))
+        mids = (grid[:-1] + grid[1:]) / 2
+        ties = np.concatenate([mids, -mids])
+    else:
+        qmax, scale = 127.0, 2.0 ** -4
+        ties = np.concatenate([np.arange(126) + 0.5, -(np.arange(126) + 0.5)])
+    edge = np.concatenate([ties, np.nextafter(ties, np.inf), np.nextafter(ties, -np.inf),
+                           [0.0, -0.0, -2.0 ** -12, 2.0 ** -12, -1e-7, qmax, -qmax]])
+    vals = (edge * scale).astype(np.float32)
+    # bf16 holds only 8 significant bits: keep the values bf16 represents
+    # exactly, so the cache's inputs are these very numbers
+    vals = vals[torch.from_numpy(vals).to(torch.bfloat16).float().numpy() == vals]
+    k = torch.randn((1, N, 1, 128), dtype=torch.float64, generator=torch.Generator().manual_seed(3))
+    v = torch.randn((1, N, 1, 128), dtype=torch.float64, generator=torch.Generator().manual_seed(4))
+    mid = slice(w.sink, w.sink + 256)           # the first two middle blocks (sealed)
+    kb = rs.choice(vals, size=(256, len(kept)))
+    vb = rs.choice(vals, size=(256, 128))
+    kb[0, :] = qmax * scale                      # every K channel of block 0 reaches the absmax
+    kb[128, :] = -qmax * scale
+    vb[:, 0] = qmax * scale                      # every V token reaches it
+    kk = k[0, mid, 0].numpy().copy()
+    kk[:, kept] = kb
+    k[0, mid, 0] = torch.from_numpy(kk)
+    v[0, mid, 0] = torch.from_numpy(vb)
+    case.hist[0] = (k.to(torch.bfloat16).to(cuda), v.to(torch.bfloat16).to(cuda))
+    case.prefill(0, N)
+    case.cache.check()
+    case.check_layout(0, N)                      # codes and scales byte for byte
+    q = case.q(0, N)
+    o = case.cache.decode(0, q)
+    case.cache.check()
+    assert _max_err(o, case.expected(0, q, N)) <= DECODE_TOL
