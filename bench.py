@@ -508,6 +508,7 @@ def run_gpu(args, rank, local_rank, world):
         "data": "synthetic (seeded K/V/q; LeanK masks from the library's mask builder on seeded importances)",
         "config": {
             **workload_config(w, args), "context_growth_max": growth,
+            "steps_per_s": K * world / elapsed,
             "resident_bytes_per_call": int(resident_step // L),
             "effective_GBps": resident_step * K * world / elapsed / 1e9,
             "warmup_steps_run": warm_done,
