@@ -65,7 +65,7 @@ COPY_BUDGET_BYTES = 120 << 30       # device memory the rotating copies may take
 MAX_COPIES = 256                    # rotating cache copies at most
 
 # DRAM bytes (read + write) per decode launch from one ncu capture, keyed by
-# "<sha256[:16] of the decode kernel sources>:<workload>[/<layers>L]:<kv
+# "<sha256[:16] of the decode kernel sources>:<workload>[/<layers>L][/paged]:<kv
 # format>:<fused | decode>" (the bench reports null when the kernel changed
 # since the capture).  The 32-layer launches are too large to capture with
 # multi-pass metrics; their entries are the traffic per algorithmic byte of
@@ -487,7 +487,9 @@ def run_gpu(args, rank, local_rank, world):
     peak, peak_kind = _peaks()
     achieved = alg_bytes / kernel_s / 1e9
     wkey = w.name if w.num_layers == S.WORKLOAD_BY_NAME[w.name].num_layers else f"{w.name}/{w.num_layers}L"
-    tkey = f"{_decode_source_hash()}:{wkey}:{args.kv}:{'fused' if fused else 'decode'}"
+    # the captures are of contiguous caches: a paged launch has no entry
+    layout_key = "/paged" if paged else ""
+    tkey = f"{_decode_source_hash()}:{wkey}{layout_key}:{args.kv}:{'fused' if fused else 'decode'}"
     traffic = NCU_TRAFFIC.get(tkey)
     traffic_scaled = traffic is None and tkey in NCU_TRAFFIC_RATIO
     if traffic_scaled:
