@@ -74,37 +74,37 @@ MAX_COPIES = 256                    # rotating cache copies at most
 # split partials, each CTA's last box past its range end), applied to the
 # full launch's algorithmic bytes.
 NCU_TRAFFIC = {
-    "5e7aea585db78f34:tiny:bf16:decode": 525568,
-    "5e7aea585db78f34:llama31_8b_layer:bf16:fused": 88086784,
-    "5e7aea585db78f34:llama31_8b_layer:bf16:decode": 88168960,
-    "5e7aea585db78f34:llama31_8b_layer:int8:decode": 46443520,
-    "5e7aea585db78f34:llama31_8b_layer:fp8:decode": 46442752,
-    "5e7aea585db78f34:qwen25_7b_long:bf16:fused": 517348864,
-    "5e7aea585db78f34:qwen25_7b_long:int8:decode": 278787328,
-    "5e7aea585db78f34:qwen25_7b_long:fp8:decode": 278737664,
-    "5e7aea585db78f34:serving_b64/2L:bf16:decode": 947137536,
-    "5e7aea585db78f34:serving_b64/4L:bf16:decode": 2180094208,
-    "5e7aea585db78f34:serving_b64/2L:bf16:fused": 946799104,
-    "5e7aea585db78f34:serving_b64/4L:bf16:fused": 2180032000,
-    "5e7aea585db78f34:serving_b64/2L:int8:decode": 637889792,
-    "5e7aea585db78f34:serving_b64/4L:int8:decode": 1425141504,
-    "5e7aea585db78f34:serving_b64/2L:fp8:decode": 637803008,
-    "5e7aea585db78f34:serving_b64/4L:fp8:decode": 1425130752,
-    "5e7aea585db78f34:fastgen_mix/2L:bf16:fused": 445602048,
-    "5e7aea585db78f34:fastgen_mix/4L:bf16:fused": 867552000,
-    "5e7aea585db78f34:fastgen_mix/2L:int8:decode": 265468160,
-    "5e7aea585db78f34:fastgen_mix/4L:int8:decode": 514942464,
-    "5e7aea585db78f34:fastgen_mix/2L:fp8:decode": 265115392,
-    "5e7aea585db78f34:fastgen_mix/4L:fp8:decode": 514908672,
+    "b87f1e1dbaefc81b:tiny:bf16:decode": 525568,
+    "b87f1e1dbaefc81b:llama31_8b_layer:bf16:fused": 88086784,
+    "b87f1e1dbaefc81b:llama31_8b_layer:bf16:decode": 88168960,
+    "b87f1e1dbaefc81b:llama31_8b_layer:int8:decode": 46443520,
+    "b87f1e1dbaefc81b:llama31_8b_layer:fp8:decode": 46442752,
+    "b87f1e1dbaefc81b:qwen25_7b_long:bf16:fused": 517348864,
+    "b87f1e1dbaefc81b:qwen25_7b_long:int8:decode": 278787328,
+    "b87f1e1dbaefc81b:qwen25_7b_long:fp8:decode": 278737664,
+    "b87f1e1dbaefc81b:serving_b64/2L:bf16:decode": 947137536,
+    "b87f1e1dbaefc81b:serving_b64/4L:bf16:decode": 2180094208,
+    "b87f1e1dbaefc81b:serving_b64/2L:bf16:fused": 946799104,
+    "b87f1e1dbaefc81b:serving_b64/4L:bf16:fused": 2180032000,
+    "b87f1e1dbaefc81b:serving_b64/2L:int8:decode": 637889792,
+    "b87f1e1dbaefc81b:serving_b64/4L:int8:decode": 1425141504,
+    "b87f1e1dbaefc81b:serving_b64/2L:fp8:decode": 637803008,
+    "b87f1e1dbaefc81b:serving_b64/4L:fp8:decode": 1425130752,
+    "b87f1e1dbaefc81b:fastgen_mix/2L:bf16:fused": 445602048,
+    "b87f1e1dbaefc81b:fastgen_mix/4L:bf16:fused": 867552000,
+    "b87f1e1dbaefc81b:fastgen_mix/2L:int8:decode": 265468160,
+    "b87f1e1dbaefc81b:fastgen_mix/4L:int8:decode": 514942464,
+    "b87f1e1dbaefc81b:fastgen_mix/2L:fp8:decode": 265115392,
+    "b87f1e1dbaefc81b:fastgen_mix/4L:fp8:decode": 514908672,
 }
 # 32-layer launches: DRAM bytes per algorithmic byte of the 4-layer capture
 NCU_TRAFFIC_RATIO = {
-    "5e7aea585db78f34:serving_b64:bf16:decode": 2180094208 / 2178351104,
-    "5e7aea585db78f34:serving_b64:int8:decode": 1425141504 / 1396178944,
-    "5e7aea585db78f34:serving_b64:fp8:decode": 1425130752 / 1396178944,
-    "5e7aea585db78f34:fastgen_mix:bf16:fused": 867552000 / 856061952,
-    "5e7aea585db78f34:fastgen_mix:int8:decode": 514942464 / 504039424,
-    "5e7aea585db78f34:fastgen_mix:fp8:decode": 514908672 / 504039424,
+    "b87f1e1dbaefc81b:serving_b64:bf16:decode": 2180094208 / 2178351104,
+    "b87f1e1dbaefc81b:serving_b64:int8:decode": 1425141504 / 1396178944,
+    "b87f1e1dbaefc81b:serving_b64:fp8:decode": 1425130752 / 1396178944,
+    "b87f1e1dbaefc81b:fastgen_mix:bf16:fused": 867552000 / 856061952,
+    "b87f1e1dbaefc81b:fastgen_mix:int8:decode": 514942464 / 504039424,
+    "b87f1e1dbaefc81b:fastgen_mix:fp8:decode": 514908672 / 504039424,
 }
 
 

@@ -62,7 +62,7 @@ namespace {
 
 struct Layout {
   size_t off_len, off_cnt, off_active, off_pt, off_free, off_heads, off_kept, off_spec, off_q;
-  size_t q_bytes = 0;                    // INT8: Q pool bytes
+  size_t q_bytes = 0;                    // INT8 / FP8: Q pool bytes
   int32_t kv_format = kKvBf16;
   size_t off_pool[kNumPools];
   int64_t pool_rows[kNumPools];
@@ -83,7 +83,7 @@ struct Layout {
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Region-B pages one (FULL, k > 0) head holds for a sequence of n tokens:
-// every started page (bf16), or the sealed blocks only (INT8; the open block
+// every started page (bf16), or the sealed blocks only (INT8 / FP8; the open block
 // is the head's bf16 tail).
 inline int32_t pages_at(int n, int S, int W, int fmt) {
   const int m = std::max(0, n - S - W);
@@ -219,7 +219,7 @@ lk_status compute_layout(const lk_plan_s& p, int B, int cap, int64_t middle_toke
       }
     }
   }
-  // region-B views: blocks of one sequence's rows (INT8: its bf16 tail), or
+  // region-B views: blocks of one sequence's rows (INT8 / FP8: its bf16 tail), or
   // of one page, from the first region-B row of each pool
   {
     const int64_t rows_b = paged && !q8 ? kPageRows : q8 ? std::min<int64_t>(mid_cap, kQBlockRows) : mid_cap;
@@ -376,7 +376,7 @@ namespace {
 // a higher aggregate HBM rate than all of them (on 152 SMs: 128 CTAs take
 // 86.5 us where 152 take 91.2 us on the 4-sequence 128K-token layer, and the
 // 32K-token layer is flat).  Launches over many entries (the 32-layer
-// steps) and INT8 middles (bound by the tile math) use every SM.
+// steps) and quantised middles (bound by the tile math) use every SM.
 int default_decode_ctas(const lk_cache_s* cache, int nlayers) {
   const int64_t entries = (int64_t)nlayers * cache->B * cache->cv.Hkv;
   if (cache->lay.kv_format == kKvBf16 && entries <= 64) return std::max(1, cache->num_sms * 27 / 32);
@@ -1017,7 +1017,7 @@ lk_status lk_step_layers(lk_cache cache, int32_t layer0, int32_t nlayers, const 
   lk_status st = decode_prepare(cache, layer0, nlayers, q, o, workspace, ws_bytes, "lk_step", a, ctas);
   if (st != LK_OK) return st;
   if (!fuse_step(cache, layer0, nlayers)) {
-    // INT8 middles always: an append may seal a block, which changes the
+    // quantised middles always: an append may seal a block, which changes the
     // values the decode reads
     st = lk_append_layers(cache, layer0, nlayers, k, v, ids, stream);
     if (st != LK_OK) return st;

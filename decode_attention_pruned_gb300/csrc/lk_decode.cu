@@ -7,13 +7,13 @@
 // (sinks + window ring, LOCAL ring or SPECIAL rows) on all 128 channels and the
 // middle rows of K_prun on the head's kept channels (q gathered to the kept
 // channel list), s = q.k / sqrt(128); one online softmax runs over both
-// regions and o = sum p V.  INT8 caches hold complete 128-row middle blocks
+// regions and o = sum p V.  INT8 / FP8 caches hold complete 128-row middle blocks
 // as codes with per-channel K / per-token V scales (KIVI-style, after the
 // pruning); those blocks are scored on the dequantised values.
 //
 // How:
 //   * The work line.  Each (layer, b, h) "entry" is a run of rows: full-width
-//     rows, then sealed INT8 rows, then bf16 kept-channel rows.  A row costs
+//     rows, then sealed INT8 / FP8 rows, then bf16 kept-channel rows.  A row costs
 //     the bytes it streams, so the line is measured in bytes.  CTA i of P
 //     takes the rows whose line offset falls in [iC/P, (i+1)C/P), with P
 //     such that every CTA takes at least 64 KB; the CTAs touching an entry
@@ -26,7 +26,7 @@
 //     S^T[16 tok x 8] = K[16 x w] Q^T[w x 8] and O^T[128 x 8] += V^T P^T, so
 //     the G <= 8 query heads only pad N.  P goes from the S^T accumulator to
 //     the B operand of P.V with one movmatrix transpose per 8x8 block; it is
-//     split into hi + lo halves (two mmas) so P.V keeps ~16 bits of P.  INT8
+//     split into hi + lo halves (two mmas) so P.V keeps ~16 bits of P.  INT8 / FP8
 //     codes enter the f16 mmas exactly; the scales fold into q and p.
 //   * Segment end: warps merge through shared memory; a CTA that owns the
 //     whole entry writes o, otherwise it writes (o, m, l) to its partial slot
@@ -59,8 +59,8 @@ constexpr int kMergeSlots = 4;                          // (o, m, l) slots of th
 constexpr int kQStride = kHeadDim + 8;                  // padded q row (bf16): conflict-free ldmatrix
 // Stages live in a byte ring: a stage holds a K tile (128 rows x width) and a
 // V tile (128 rows x 128), so narrow-K tiles (40 KB at k = 32) keep five
-// stages in flight where full-width ones (64 KB) keep three; sealed INT8
-// blocks (21-33 KB) keep up to nine.
+// stages in flight where full-width ones (64 KB) keep three; stages of two
+// or three sealed blocks (42-66 KB) keep three.
 constexpr int kSlots = 16;                              // barrier pairs = stages in flight at most (power of 2)
 constexpr int kRingBytes = 200 * 1024;
 // A launch over at most this many (layer, kv head) pairs keeps their head
@@ -81,7 +81,7 @@ constexpr uint64_t kDrainLimitNs = 1000000000ull;      // bound of the producer'
 
 struct StageDesc {
   int32_t e;           // entry = b * Hkv + h; < 0 ends the stream
-  int32_t region;      // 0: full width, 1: kept channels (bf16), 2: sealed INT8 block, 3: fused token
+  int32_t region;      // 0: full width, 1: kept channels (bf16), 2: sealed INT8 / FP8 blocks, 3: fused token
   int32_t rlo;         // first valid row of the tile (sealed blocks; else 0)
   int32_t nrows;       // valid rows of the tile: rlo .. rlo + nrows - 1
   int32_t width;       // K channels of the tile
@@ -142,8 +142,8 @@ struct EntryLen {
   int act;    // fused launches: the sequence takes the appended token
 };
 
-// Rows of an entry in line order: n_a full width, n_q in sealed INT8 blocks,
-// n_b bf16 kept-channel rows (INT8 caches: the open tail block).  mrow: the
+// Rows of an entry in line order: n_a full width, n_q in sealed blocks,
+// n_b bf16 kept-channel rows (quantised caches: the open tail block).  mrow: the
 // full-width row a fused append replaces (left out of the scores), or -1;
 // len: what the geometry was computed from.
 struct Entry {
@@ -1058,7 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // two independent accumulators halve the mma dependency chain
       float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
       if (kQ8 && d.region == 2) {
-        // ---- sealed INT8 block: S^T = K_codes (f16, exact) . Q'^T with
+        // ---- sealed INT8 / FP8 block: S^T = K_codes (f16, exact) . Q'^T with
         // Q' = q[kept] * (K scale of the channel), split into f16 hi + lo
         const int kb = d.width;
         const float* ksc = reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + koff + qblock_ksoff(kb));

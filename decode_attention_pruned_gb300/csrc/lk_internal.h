@@ -80,9 +80,9 @@ struct HeadDesc {                 // one (layer, kv head)
   int64_t row_a;                  // first region-A row (sequence 0) in K128 and V
   int64_t krow_b;                 // first region-B row (sequence 0) in pool_kb; paged: page area
   int64_t vrow_b;                 // first region-B row (sequence 0) in V; paged: page area
-  int64_t qoff;                   // INT8: byte offset in the Q pool of sequence 0's blocks
+  int64_t qoff;                   // INT8 / FP8: byte offset in the Q pool of sequence 0's blocks
                                   //       (paged: of the class's page area)
-  int32_t qblocks;                // INT8, contiguous: sealed blocks per sequence
+  int32_t qblocks;                // INT8 / FP8, contiguous: sealed blocks per sequence
   // decode TMA views (a pool's rows seen as equal blocks, one per sequence or
   // page): the block of sequence 0's region A in its policy class's view,
   // and of sequence 0's region-B K and V rows (paged: of the class's page 0)
@@ -111,7 +111,7 @@ struct CacheView {
   const int16_t* kept;            // [L][Hkv][128] kept channels ascending
   const uint8_t* is_special;      // [vocab]
   uint16_t* pool[kNumPools];      // bf16 rows
-  uint8_t* qpool;                 // INT8: sealed blocks
+  uint8_t* qpool;                 // INT8 / FP8: sealed blocks
   int64_t pool_rows[kNumPools];
   int32_t L, B, Hq, Hkv, G, S, W, W_loc, vocab, capacity;
   int32_t spec_cap;               // rows of a SPECIAL head per sequence

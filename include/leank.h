@@ -96,7 +96,7 @@ typedef struct lk_region_info {
   int32_t max_pages;          /* entries of the head's page-table row */
   uint64_t page_table_offset; /* int32 [max_pages] */
   int32_t kv_format;          /* lk_kv_format of region B */
-  int32_t sealed_blocks;      /* INT8: complete 128-row blocks (read them with
+  int32_t sealed_blocks;      /* INT8 / FP8: complete 128-row blocks (read them with
                                  lk_cache_block); region B's offsets then give
                                  the bf16 tail: middle row m >= 128 * sealed_blocks
                                  is tail row m - 128 * sealed_blocks */
@@ -332,7 +332,7 @@ lk_status lk_decode_attn_layers(lk_cache cache, int32_t layer0, int32_t nlayers,
  * middle one kernel does both: the CTA that combines a head's split
  * partials adds the new token (and the token leaving a full window for the
  * middle) to the softmax from the inputs, then writes them into the cache;
- * the window slot being replaced is left out of the scores.  INT8 caches
+ * the window slot being replaced is left out of the scores.  INT8 / FP8 caches
  * (where an append may seal a block, changing the values decode reads) run
  * the two launches.  Nothing is launched on an error. */
 lk_status lk_step(lk_cache cache, int32_t layer, const void* q, const void* k, const void* v,
@@ -403,7 +403,7 @@ lk_status lk_resident_bytes(lk_cache cache, int32_t layer, void* stream, uint64_
  *                  append and decode launches (a 0.24 MB layer, or a
  *                  32-layer, 64-sequence step, are faster that way);
  *   LK_STEP_FUSED  always one launch;   LK_STEP_SPLIT  always two.
- * Results and cache contents do not depend on the mode.  INT8 middles
+ * Results and cache contents do not depend on the mode.  INT8 / FP8 middles
  * always run two launches. */
 typedef enum { LK_STEP_AUTO = 0, LK_STEP_FUSED = 1, LK_STEP_SPLIT = 2 } lk_step_mode;
 lk_status lk_set_step_mode(lk_cache cache, int32_t mode);
