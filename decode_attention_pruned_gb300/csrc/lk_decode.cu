@@ -43,6 +43,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "lk_append.cuh"
 #include "lk_device.cuh"
 #include "lk_internal.h"
@@ -307,6 +309,58 @@ template <int kFmt>
 __device__ __forceinline__ void vcodes_to_f16x2(uint32_t w, uint32_t& even, uint32_t& odd) {
   if (kFmt == kKvFp8) e4m3x4_to_f16x2(w, even, odd);
   else u8x4_to_f16x2_biased(w, even, odd);
+}
+
+// One online-softmax step of a warp over NB groups of its 16 tile rows: x
+// holds scaled scores (log2 units, -inf for masked rows) in the S^T
+// accumulator layout (x[j][0], x[j][2]: head column 2tig; x[j][1], x[j][3]:
+// column 2tig + 1), p receives 2^(x - m).  Lazy rescaling: the running max m
+// of a column moves only when some score exceeds it by more than
+// kRescaleGap (log2 units); otherwise p <= 2^kRescaleGap, exact in the fp32
+// accumulators and in the hi/lo splits of P.  One warp vote replaces the
+// column-max shuffles in the common case.  When m moves, l, o and the INT8
+// bias sums c are rescaled with it.
+template <int NB>
+__device__ __forceinline__ void online_softmax(const float (&x)[NB][4], float (&p)[NB][4], float& m0, float& m1,
+                                               float& l0, float& l1, float& c0, float& c1, float (&o)[8][4]) {
+  float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+  for (int j = 1; j < NB; ++j) {
+    mx0 = fmaxf(mx0, fmaxf(x[j][0], x[j][2]));
+    mx1 = fmaxf(mx1, fmaxf(x[j][1], x[j][3]));
+  }
+  constexpr float kRescaleGap = 8.f;
+  if (__any_sync(0xffffffffu, mx0 > m0 + kRescaleGap || mx1 > m1 + kRescaleGap)) {
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    l0 *= al0;
+    l1 *= al1;
+    c0 *= al0;
+    c1 *= al1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o[i][0] *= al0;
+      o[i][1] *= al1;
+      o[i][2] *= al0;
+      o[i][3] *= al1;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NB; ++j) {
+    p[j][0] = exp2f(x[j][0] - m0);     // token gid
+    p[j][1] = exp2f(x[j][1] - m1);
+    p[j][2] = exp2f(x[j][2] - m0);     // token gid + 8
+    p[j][3] = exp2f(x[j][3] - m1);
+    l0 += p[j][0] + p[j][2];
+    l1 += p[j][1] + p[j][3];
+  }
 }
 
 // Shared-memory address of 16-byte chunk `c` (channels 8c..8c+7) of tile row
@@ -668,13 +722,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int anc = g.anc;
           const int xj = fused_launch && anc >= 0 && anc >= a0 && anc < a1 ? (anc - a0) / kTileRows : -1;
           int32_t page_ahead = 0;
-          int32_t qpg_ahead[kQPerStageNarrow] = {0, 0, 0};
+          int32_t qpg_ahead[kQPerStageNarrow] = {};
           for (int j = 0; j < nt; ++j) {
             const int region = j < nta ? 0 : j < nta + ntq ? 2 : 1;
             const int width = region == 0 ? kHeadDim : g.kb;
             int r, rend, rlo = 0, nq = 0;
             int32_t page = 0;
-            int32_t qpg[kQPerStageNarrow] = {0, 0, 0};
+            int32_t qpg[kQPerStageNarrow] = {};
             if (region == 0) {
               r = a0 + j * kTileRows;
               rend = min(a1, r + kTileRows);
@@ -1019,6 +1073,124 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // this warp's 16 rows of every tile
   const int r0 = 16 * warp;
+
+  // A stage of NB sealed INT8 / FP8 blocks (valid rows d.rlo .. d.rlo +
+  // d.nrows - 1 counted from the first block's row 0: blocks at a segment's
+  // ends are shared with another CTA).  The warp takes its 16 rows of every
+  // block at once: the blocks' score and P.V chains are independent until
+  // one softmax step joins them, so the warp keeps NB mma chains in flight.
+  //   S^T = K_codes (f16, exact) . Q'^T, Q' = q[kept] * (K scale of the
+  //   channel in the block), split into f16 hi + lo;
+  //   O^T += V_codes^T (f16, exact) . P'^T, P' = p * (V scale of the token),
+  //   split into f16 hi + lo.
+  auto qstage = [&](auto nbc, const StageDesc& d) {
+    constexpr int NB = decltype(nbc)::value;
+    const int kb = d.width;
+    const uint32_t qbytes = (uint32_t)qblock_bytes(kb);
+    const uint32_t sbase = base + SmemLayout::kRingOff + d.koff;
+    const uint8_t* sptr = sm + SmemLayout::kRingOff + d.koff;
+    const int t0 = r0 + gid;
+    bool va[NB], vb[NB];
+    bool any = false;     // warp-uniform: one of the warp's rows is valid
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int rlo = d.rlo - j * kQBlockRows, rhi = d.rlo + d.nrows - j * kQBlockRows;
+      va[j] = t0 >= rlo && t0 < rhi;
+      vb[j] = t0 + 8 >= rlo && t0 + 8 < rhi;
+      any = any || max(r0, rlo) < min(r0 + 16, rhi);
+    }
+    if (!any) return;
+    // two independent accumulators per block halve the mma dependency chain
+    float sc[NB][4], sd[NB][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[j][i] = sd[j][i] = 0.f;
+    const int krow = r0 + rk;
+#pragma unroll
+    for (int kp = 0; kp < 4; ++kp) {
+      if (2 * kp < (kb >> 4)) {
+        uint32_t qv[4];
+        ldsm_x4(qb_lane + 64u * kp, qv[0], qv[1], qv[2], qv[3]);
+        const uint32_t krow_off = (uint32_t)(krow * kb + 16 * ((2 * kp + ck) ^ qswz(kb, krow)));
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const float* ksc = reinterpret_cast<const float*>(sptr + j * qbytes + qblock_ksoff(kb));
+          uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = 16 * (2 * kp + u) + 2 * tig;
+            const float2 s01 = *reinterpret_cast<const float2*>(&ksc[c]);
+            const float2 s89 = *reinterpret_cast<const float2*>(&ksc[c + 8]);
+            const float q0 = bf16_lo(qv[2 * u]) * s01.x, q1 = bf16_hi(qv[2 * u]) * s01.y;
+            const float q8 = bf16_lo(qv[2 * u + 1]) * s89.x, q9 = bf16_hi(qv[2 * u + 1]) * s89.y;
+            bh[u][0] = pack_f16x2(q0, q1);
+            bh[u][1] = pack_f16x2(q8, q9);
+            bl[u][0] = pack_f16x2(q0 - f16_lo(bh[u][0]), q1 - f16_hi(bh[u][0]));
+            bl[u][1] = pack_f16x2(q8 - f16_lo(bh[u][1]), q9 - f16_hi(bh[u][1]));
+          }
+          uint32_t w0, w1, w2, w3;
+          ldsm_x4(sbase + j * qbytes + krow_off, w0, w1, w2, w3);
+          uint32_t f0, f1, f2, f3;
+          codes_to_f16x2<kFmt>(w0, f0, f2);       // rows gid: k 2tig.. / 2tig+8..
+          codes_to_f16x2<kFmt>(w1, f1, f3);       // rows gid + 8
+          mma_f16_16816(sc[j], f0, f1, f2, f3, bh[0][0], bh[0][1]);
+          mma_f16_16816(sd[j], f0, f1, f2, f3, bl[0][0], bl[0][1]);
+          codes_to_f16x2<kFmt>(w2, f0, f2);
+          codes_to_f16x2<kFmt>(w3, f1, f3);
+          mma_f16_16816(sc[j], f0, f1, f2, f3, bh[1][0], bh[1][1]);
+          mma_f16_16816(sd[j], f0, f1, f2, f3, bl[1][0], bl[1][1]);
+        }
+      }
+    }
+    float x[NB][4], p[NB][4];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      x[j][0] = va[j] ? (sc[j][0] + sd[j][0]) * a.scale_log2 : NEG_INF;
+      x[j][1] = va[j] ? (sc[j][1] + sd[j][1]) * a.scale_log2 : NEG_INF;
+      x[j][2] = vb[j] ? (sc[j][2] + sd[j][2]) * a.scale_log2 : NEG_INF;
+      x[j][3] = vb[j] ? (sc[j][3] + sd[j][3]) * a.scale_log2 : NEG_INF;
+    }
+    online_softmax<NB>(x, p, m0, m1, l0, l1, c0, c1, o);
+    uint32_t ph[NB][2], pr[NB][2];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const float* vsc = reinterpret_cast<const float*>(sptr + j * qbytes + qblock_vsoff(kb));
+      const float sv0 = vsc[t0], sv1 = vsc[t0 + 8];
+      const float q0 = p[j][0] * sv0, q1 = p[j][1] * sv0, q2 = p[j][2] * sv1, q3 = p[j][3] * sv1;
+      if (kFmt == kKvInt8) {
+        c0 += q0 + q2;
+        c1 += q1 + q3;
+      }
+      const uint32_t h01 = pack_f16x2(q0, q1), h23 = pack_f16x2(q2, q3);
+      const uint32_t r01 = pack_f16x2(q0 - f16_lo(h01), q1 - f16_hi(h01));
+      const uint32_t r23 = pack_f16x2(q2 - f16_lo(h23), q3 - f16_hi(h23));
+      ph[j][0] = movmatrix_trans(h01);
+      ph[j][1] = movmatrix_trans(h23);
+      pr[j][0] = movmatrix_trans(r01);
+      pr[j][1] = movmatrix_trans(r23);
+    }
+#pragma unroll
+    for (int i2 = 0; i2 < 4; ++i2) {
+      const uint32_t vrow_off =
+          (uint32_t)(qblock_voff(kb) + krow * kHeadDim + 16 * ((2 * i2 + ck) ^ (krow & 7)));
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        uint32_t w0, w1, w2, w3;
+        ldsm_x4_trans(sbase + j * qbytes + vrow_off, w0, w1, w2, w3);
+        uint32_t f0, f1, f2, f3;
+        vcodes_to_f16x2<kFmt>(w0, f0, f1);  // tokens 2tig.. of rows 0-7: channels gid / gid + 8
+        vcodes_to_f16x2<kFmt>(w1, f2, f3);  // tokens 2tig + 8..
+        mma_f16_16816(o[2 * i2], f0, f1, f2, f3, ph[j][0], ph[j][1]);
+        mma_f16_16816(o[2 * i2], f0, f1, f2, f3, pr[j][0], pr[j][1]);
+        vcodes_to_f16x2<kFmt>(w2, f0, f1);
+        vcodes_to_f16x2<kFmt>(w3, f2, f3);
+        mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, ph[j][0], ph[j][1]);
+        mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, pr[j][0], pr[j][1]);
+      }
+    }
+  };
+
   int stage = 0;
   uint32_t phase = 0;
   while (true) {
@@ -1041,179 +1213,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
 
-    // A stage of sealed blocks holds d.n consecutive blocks of the entry (one
-    // softmax runs through them in order); any other stage is one tile.
-    const int nsub = kQ8 && d.region == 2 ? d.n : 1;
-    const uint32_t sub_bytes = kQ8 && d.region == 2 ? (uint32_t)qblock_bytes(d.width) : 0u;
-#pragma unroll 1
-    for (int sb = 0; sb < nsub; ++sb) {
-    // valid rows rlo .. rhi - 1 of the tile (sealed blocks may be shared with
-    // another CTA) except mrow; the warp works if one of its 16 rows is valid
-    // (a block of masked rows would leave the running max at -inf)
-    const int rlo = max(0, d.rlo - sb * kQBlockRows), rhi = min(kTileRows, d.rlo + d.nrows - sb * kQBlockRows);
-    const uint32_t koff = d.koff + (uint32_t)sb * sub_bytes;
-    const uint32_t kbase = base + SmemLayout::kRingOff + koff;
+    // A stage of sealed blocks holds d.n (1-3) consecutive blocks of the
+    // entry; any other stage is one tile.
+    if (kQ8 && d.region == 2) {
+      if (d.n == 3)
+        qstage(std::integral_constant<int, 3>(), d);
+      else if (d.n == 2)
+        qstage(std::integral_constant<int, 2>(), d);
+      else
+        qstage(std::integral_constant<int, 1>(), d);
+    } else {
+    // valid rows rlo .. rhi - 1 of the tile except mrow; the warp works if
+    // one of its 16 rows is valid (a block of masked rows would leave the
+    // running max at -inf)
+    const int rlo = max(0, d.rlo), rhi = min(kTileRows, d.rlo + d.nrows);
+    const uint32_t kbase = base + SmemLayout::kRingOff + d.koff;
     const int wlo = max(r0, rlo), whi = min(r0 + 16, rhi);
     if (whi - wlo - (d.mrow >= wlo && d.mrow < whi ? 1 : 0) > 0) {
       // two independent accumulators halve the mma dependency chain
       float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
-      if (kQ8 && d.region == 2) {
-        // ---- sealed INT8 / FP8 block: S^T = K_codes (f16, exact) . Q'^T with
-        // Q' = q[kept] * (K scale of the channel), split into f16 hi + lo
-        const int kb = d.width;
-        const float* ksc = reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + koff + qblock_ksoff(kb));
+      const bool fam128 = (d.width & 63) == 0;          // widths 64 / 128 use 128-byte rows
+      const int nks = d.width >> 4;
+      const uint32_t q_lane = d.region == 0 ? qa_lane : qb_lane;
+      const int row = r0 + rk;
 #pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-          if (2 * kp < (kb >> 4)) {
-            uint32_t qv[4];
-            ldsm_x4(qb_lane + 64u * kp, qv[0], qv[1], qv[2], qv[3]);
-            uint32_t bh[2][2], bl[2][2];
+      for (int kp = 0; kp < 4; ++kp) {
+        if (2 * kp < nks) {
+          uint32_t qv[4];
+          ldsm_x4(q_lane + 64u * kp, qv[0], qv[1], qv[2], qv[3]);
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int c = 16 * (2 * kp + u) + 2 * tig;
-              const float2 s01 = *reinterpret_cast<const float2*>(&ksc[c]);
-              const float2 s89 = *reinterpret_cast<const float2*>(&ksc[c + 8]);
-              const float q0 = bf16_lo(qv[2 * u]) * s01.x, q1 = bf16_hi(qv[2 * u]) * s01.y;
-              const float q8 = bf16_lo(qv[2 * u + 1]) * s89.x, q9 = bf16_hi(qv[2 * u + 1]) * s89.y;
-              bh[u][0] = pack_f16x2(q0, q1);
-              bh[u][1] = pack_f16x2(q8, q9);
-              bl[u][0] = pack_f16x2(q0 - f16_lo(bh[u][0]), q1 - f16_hi(bh[u][0]));
-              bl[u][1] = pack_f16x2(q8 - f16_lo(bh[u][1]), q9 - f16_hi(bh[u][1]));
-            }
-            const int row = r0 + rk;
-            const int grp = 2 * kp + ck;
-            uint32_t w0, w1, w2, w3;
-            ldsm_x4(kbase + (uint32_t)(row * kb + 16 * (grp ^ qswz(kb, row))), w0, w1, w2, w3);
-            uint32_t f0, f1, f2, f3;
-            codes_to_f16x2<kFmt>(w0, f0, f2);       // rows gid: k 2tig.. / 2tig+8..
-            codes_to_f16x2<kFmt>(w1, f1, f3);       // rows gid + 8
-            mma_f16_16816(sc, f0, f1, f2, f3, bh[0][0], bh[0][1]);
-            mma_f16_16816(sd, f0, f1, f2, f3, bl[0][0], bl[0][1]);
-            codes_to_f16x2<kFmt>(w2, f0, f2);
-            codes_to_f16x2<kFmt>(w3, f1, f3);
-            mma_f16_16816(sc, f0, f1, f2, f3, bh[1][0], bh[1][1]);
-            mma_f16_16816(sd, f0, f1, f2, f3, bl[1][0], bl[1][1]);
-          }
-        }
-      } else {
-        const bool fam128 = (d.width & 63) == 0;          // widths 64 / 128 use 128-byte rows
-        const int nks = d.width >> 4;
-        const uint32_t q_lane = d.region == 0 ? qa_lane : qb_lane;
-        const int row = r0 + rk;
-#pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-          if (2 * kp < nks) {
-            uint32_t qv[4];
-            ldsm_x4(q_lane + 64u * kp, qv[0], qv[1], qv[2], qv[3]);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int c = 2 * (2 * kp + u) + ck;
-              const uint32_t addr = fam128 ? tile_addr128(kbase, row, c) : tile_addr64(kbase, row, c);
-              uint32_t a0, a1, a2, a3;
-              ldsm_x4(addr, a0, a1, a2, a3);
-              if (u == 0)
-                mma_bf16_16816(sc, a0, a1, a2, a3, qv[0], qv[1]);
-              else
-                mma_bf16_16816(sd, a0, a1, a2, a3, qv[2], qv[3]);
-            }
+          for (int u = 0; u < 2; ++u) {
+            const int c = 2 * (2 * kp + u) + ck;
+            const uint32_t addr = fam128 ? tile_addr128(kbase, row, c) : tile_addr64(kbase, row, c);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(addr, a0, a1, a2, a3);
+            if (u == 0)
+              mma_bf16_16816(sc, a0, a1, a2, a3, qv[0], qv[1]);
+            else
+              mma_bf16_16816(sd, a0, a1, a2, a3, qv[2], qv[3]);
           }
         }
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sc[i] += sd[i];
       const int t0 = r0 + gid;
       const bool v0 = t0 >= rlo && t0 < rhi && t0 != d.mrow;
       const bool v1 = t0 + 8 >= rlo && t0 + 8 < rhi && t0 + 8 != d.mrow;
-      const float x0 = v0 ? sc[0] * a.scale_log2 : NEG_INF;
-      const float x1 = v0 ? sc[1] * a.scale_log2 : NEG_INF;
-      const float x2 = v1 ? sc[2] * a.scale_log2 : NEG_INF;
-      const float x3 = v1 ? sc[3] * a.scale_log2 : NEG_INF;
-      // Lazy rescaling: the running max m of a column moves only when some
-      // score of the tile exceeds it by more than kRescaleGap (log2 units);
-      // otherwise p = 2^(s - m) <= 2^kRescaleGap, exact in the fp32
-      // accumulators and in the hi/lo splits of P.  One warp vote replaces
-      // the column-max shuffles in the common case.
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-      constexpr float kRescaleGap = 8.f;
-      if (__any_sync(0xffffffffu, mx0 > m0 + kRescaleGap || mx1 > m1 + kRescaleGap)) {
+      const float x[1][4] = {{v0 ? (sc[0] + sd[0]) * a.scale_log2 : NEG_INF,
+                              v0 ? (sc[1] + sd[1]) * a.scale_log2 : NEG_INF,
+                              v1 ? (sc[2] + sd[2]) * a.scale_log2 : NEG_INF,
+                              v1 ? (sc[3] + sd[3]) * a.scale_log2 : NEG_INF}};
+      float p[1][4];
+      online_softmax<1>(x, p, m0, m1, l0, l1, c0, c1, o);
+      // P as a bf16 pair hi + lo (two mmas): P.V keeps ~16 mantissa bits
+      const uint32_t vbase = kbase + (uint32_t)kTileRows * 2 * d.width;
+      const uint32_t h01 = pack_bf16x2(p[0][0], p[0][1]), h23 = pack_bf16x2(p[0][2], p[0][3]);
+      const uint32_t r01 = pack_bf16x2(p[0][0] - bf16_lo(h01), p[0][1] - bf16_hi(h01));
+      const uint32_t r23 = pack_bf16x2(p[0][2] - bf16_lo(h23), p[0][3] - bf16_hi(h23));
+      // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
+      const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
+      const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
+      const int vrow = r0 + rv;
 #pragma unroll
-        for (int sh = 4; sh < 32; sh <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        l0 *= al0;
-        l1 *= al1;
-        c0 *= al0;
-        c1 *= al1;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[i][0] *= al0;
-          o[i][1] *= al1;
-          o[i][2] *= al0;
-          o[i][3] *= al1;
-        }
-      }
-      const float p0 = exp2f(x0 - m0), p1 = exp2f(x1 - m1);   // token gid
-      const float p2 = exp2f(x2 - m0), p3 = exp2f(x3 - m1);   // token gid + 8
-      l0 += p0 + p2;
-      l1 += p1 + p3;
-      if (kQ8 && d.region == 2) {
-        // ---- O^T += V_codes^T (f16, exact) . P'^T, P' = p * (V scale of
-        // the token), split into f16 hi + lo
-        const uint32_t vbase = kbase + (uint32_t)qblock_voff(d.width);
-        const float* vsc =
-            reinterpret_cast<const float*>(sm + SmemLayout::kRingOff + koff + qblock_vsoff(d.width));
-        const float sv0 = vsc[r0 + gid], sv1 = vsc[r0 + gid + 8];
-        const float q0 = p0 * sv0, q1 = p1 * sv0, q2 = p2 * sv1, q3 = p3 * sv1;
-        if (kFmt == kKvInt8) {
-          c0 += q0 + q2;
-          c1 += q1 + q3;
-        }
-        const uint32_t h01 = pack_f16x2(q0, q1), h23 = pack_f16x2(q2, q3);
-        const uint32_t r01 = pack_f16x2(q0 - f16_lo(h01), q1 - f16_hi(h01));
-        const uint32_t r23 = pack_f16x2(q2 - f16_lo(h23), q3 - f16_hi(h23));
-        const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
-        const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
-        const int row = r0 + rk;
-#pragma unroll
-        for (int i2 = 0; i2 < 4; ++i2) {
-          const int grp = 2 * i2 + ck;
-          uint32_t w0, w1, w2, w3;
-          ldsm_x4_trans(vbase + (uint32_t)(row * kHeadDim + 16 * (grp ^ (row & 7))), w0, w1, w2, w3);
-          uint32_t f0, f1, f2, f3;
-          vcodes_to_f16x2<kFmt>(w0, f0, f1);  // tokens 2tig.. of rows 0-7: channels gid / gid + 8
-          vcodes_to_f16x2<kFmt>(w1, f2, f3);  // tokens 2tig + 8..
-          mma_f16_16816(o[2 * i2], f0, f1, f2, f3, ph0, ph1);
-          mma_f16_16816(o[2 * i2], f0, f1, f2, f3, pr0, pr1);
-          vcodes_to_f16x2<kFmt>(w2, f0, f1);
-          vcodes_to_f16x2<kFmt>(w3, f2, f3);
-          mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, ph0, ph1);
-          mma_f16_16816(o[2 * i2 + 1], f0, f1, f2, f3, pr0, pr1);
-        }
-      } else {
-        // P as a bf16 pair hi + lo (two mmas): P.V keeps ~16 mantissa bits
-        const uint32_t vbase = kbase + (uint32_t)kTileRows * 2 * d.width;
-        const uint32_t h01 = pack_bf16x2(p0, p1), h23 = pack_bf16x2(p2, p3);
-        const uint32_t r01 = pack_bf16x2(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-        const uint32_t r23 = pack_bf16x2(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-        // S^T accumulator rows (tokens) -> B operand rows (k = tokens) of P^T
-        const uint32_t ph0 = movmatrix_trans(h01), ph1 = movmatrix_trans(h23);
-        const uint32_t pr0 = movmatrix_trans(r01), pr1 = movmatrix_trans(r23);
-        const int row = r0 + rv;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(tile_addr128(vbase, row, 2 * i + cvh), a0, a1, a2, a3);
-          mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
-          mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
-        }
+      for (int i = 0; i < 8; ++i) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(tile_addr128(vbase, vrow, 2 * i + cvh), a0, a1, a2, a3);
+        mma_bf16_16816(o[i], a0, a1, a2, a3, ph0, ph1);
+        mma_bf16_16816(o[i], a0, a1, a2, a3, pr0, pr1);
       }
     }
-    }   // sub-blocks of the stage
+    }   // tile stage
     if (!kQ8 && d.region == 3) {
       // ---- fused append: the new token (and the window row it evicts into
       // the middle, scored on the kept channels) join warp 0's running
@@ -1423,80 +1490,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!single) {
         // The barrier orders every thread's partial stores before thread 0's
-        // fence, which releases them all (fences are cumulative) ahead of the
-        // counter; the entry's last CTA acquires the other partials the same
-        // way before its barrier hands them to its threads.
+        // acquire-release add on the counter, which releases them all
+        // (release is cumulative); the entry's last CTA acquires the other
+        // partials by the same add before its barrier hands them to its
+        // threads.
         consumer_sync(cbar, cphase, a);
         if (ct == 0) {
-          __threadfence();
-          const int prev = atomicAdd(&a.counters[d.e], 1);
-          const bool last = prev == d.last_cta - d.first_cta;
-          if (last) __threadfence();
-          misc[2] = last ? 1 : 0;
+          const int prev = atom_add_acq_rel_gpu(&a.counters[d.e], 1);
+          misc[2] = prev == d.last_cta - d.first_cta ? 1 : 0;
         }
         consumer_sync(cbar, cphase, a);
         if (misc[2]) {
           // last CTA of the entry: LSE-merge the partials of CTAs first..last
-          // (slots first+e .. last+e, consecutive).  Each thread owns 4 output
-          // channels: it issues the o loads of its first chunk of partials
-          // while the (m, l) pairs are staged into shared memory, so a chunk
-          // costs one round trip; a warp per query head turns the pairs into
-          // weights w_c = 2^(m_c - M) / L.
+          // (slots first+e .. last+e, consecutive).  Each thread owns 4
+          // output channels of one query head and merges on its own: per
+          // chunk of partials it issues every o and (m, l) load at once (one
+          // round trip), then folds the chunk into a running (M, L, acc)
+          // with weights 2^(m_c - M).
           const int np = d.last_cta - d.first_cta + 1;
           const size_t slot0 = (size_t)d.first_cta + d.e;
-          const float4* src = reinterpret_cast<const float4*>(a.part) + slot0 * G * 32;
-          float2* mlb = reinterpret_cast<float2*>(merge_o);      // [np][G], np * G <= 2048
-          constexpr int kChunk = 20;
-          const int q4a = ct, q4b = ct + kConsumerWarps * 32;  // G * 32 <= 256 outputs
-          float4 v[kChunk];
-#pragma unroll
-          for (int u = 0; u < kChunk; ++u) {
-            const int c = min(u, np - 1);
-            v[u] = q4a < G * 32 ? __ldcg(src + (size_t)c * G * 32 + q4a) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          for (int i = ct; i < np * G; i += kConsumerWarps * 32) mlb[i] = __ldcg(&a.part_ml[slot0 * G + i]);
-          consumer_sync(cbar, cphase, a);
-          for (int g = warp; g < G; g += kConsumerWarps) {
-            float M = NEG_INF;
-            for (int c = lane; c < np; c += 32) M = fmaxf(M, mlb[c * G + g].x);
-#pragma unroll
-            for (int sh = 16; sh > 0; sh >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, sh));
-            float L = 0.f;
-            for (int c = lane; c < np; c += 32) {
-              const float2 ml = mlb[c * G + g];
-              L += ml.x == NEG_INF ? 0.f : exp2f(ml.x - M) * ml.y;
-            }
-#pragma unroll
-            for (int sh = 16; sh > 0; sh >>= 1) L += __shfl_xor_sync(0xffffffffu, L, sh);
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            __syncwarp();
-            for (int c = lane; c < np; c += 32) {
-              const float mc = mlb[c * G + g].x;
-              mlb[c * G + g].x = mc == NEG_INF ? 0.f : exp2f(mc - M) * inv;
-            }
-          }
-          consumer_sync(cbar, cphase, a);
-          for (int pass = 0; pass < 2; ++pass) {
-            const int q4 = pass == 0 ? q4a : q4b;
-            if (q4 >= G * 32) continue;
+          const int q4 = ct;                                   // G * 32 <= 256 outputs
+          if (q4 < G * 32) {
             const int g = q4 >> 5;
+            const float4* src = reinterpret_cast<const float4*>(a.part) + slot0 * G * 32 + q4;
+            const float2* mls = a.part_ml + slot0 * G + g;
+            constexpr int kChunk = 16;
+            float M = NEG_INF, L = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int c0 = 0; c0 < np; c0 += kChunk) {
-              if (pass == 1 || c0 > 0) {
-#pragma unroll
-                for (int u = 0; u < kChunk; ++u)
-                  v[u] = __ldcg(src + (size_t)min(c0 + u, np - 1) * G * 32 + q4);
-              }
+              float4 v[kChunk];
+              float2 ml[kChunk];
 #pragma unroll
               for (int u = 0; u < kChunk; ++u) {
-                const float wgt = c0 + u < np ? mlb[(c0 + u) * G + g].x : 0.f;
-                acc.x += wgt * v[u].x;
-                acc.y += wgt * v[u].y;
-                acc.z += wgt * v[u].z;
-                acc.w += wgt * v[u].w;
+                const int c = min(c0 + u, np - 1);        // past np: the last partial again
+                v[u] = __ldcg(src + (size_t)c * G * 32);
+                ml[u] = __ldcg(mls + (size_t)c * G);
+              }
+              float Mc = M;
+#pragma unroll
+              for (int u = 0; u < kChunk; ++u) Mc = fmaxf(Mc, ml[u].x);
+              if (Mc != NEG_INF) {
+                const float f = M == NEG_INF ? 0.f : exp2f(M - Mc);
+                acc.x *= f;
+                acc.y *= f;
+                acc.z *= f;
+                acc.w *= f;
+                L *= f;
+#pragma unroll
+                for (int u = 0; u < kChunk; ++u) {
+                  const float w = c0 + u < np && ml[u].x != NEG_INF ? exp2f(ml[u].x - Mc) : 0.f;
+                  acc.x += w * v[u].x;
+                  acc.y += w * v[u].y;
+                  acc.z += w * v[u].z;
+                  acc.w += w * v[u].w;
+                  L += w * ml[u].y;
+                }
+                M = Mc;
               }
             }
-            *reinterpret_cast<float4*>(&dst[q4 * 4]) = acc;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            *reinterpret_cast<float4*>(&dst[q4 * 4]) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
           }
           if (ct == 0) a.counters[d.e] = 0;
         }
