@@ -103,6 +103,33 @@ def test_full_serving_b64_all_layers(cuda):
     _check_all_layers(case, w.context, pick, fused=False)
 
 
+def test_full_serving_b64_three_ctas(cuda):
+    """The 32-layer serving cache (19.7 GB) decoded on three CTAs: each CTA's
+    range of the line is ~6.5 GB, so the row ranges and the owners of the
+    split entries are computed from offsets past 2^32 bytes.  Every output
+    agrees with the default grid's (a different split, so within rounding of
+    the partial merges), and sampled heads agree with the oracle."""
+    w = S.WORKLOADS[2]
+    N = w.context
+    L = w.num_layers
+    case = Case(w, total=N, gen_device=cuda)
+    for layer in range(L):
+        case.prefill(layer, N)
+        case.drop_history(layer)
+    assert sum(case.cache.resident_bytes(layer) for layer in range(L)) > 3 * (1 << 32)
+    qs = torch.stack([case.q(layer, N) for layer in range(L)]).contiguous()
+    o_def = case.cache.decode_layers(0, qs)
+    case.cache.set_decode_ctas(3)
+    o_3 = case.cache.decode_layers(0, qs)
+    case.cache.check()
+    case.cache.set_decode_ctas(0)
+    assert float((o_3 - o_def).abs().max()) <= 2e-4
+    rng = np.random.default_rng(5)
+    for layer in (0, L // 2, L - 1):
+        _check(case, layer, N, o_3[layer], qs[layer], _sample_pairs(w, layer, 3, rng), [])
+        case.drop_history(layer)
+
+
 def test_full_fastgen_mix_all_layers(cuda):
     w = S.WORKLOADS[4]
     case = Case(w, total=w.context, gen_device=cuda)
