@@ -311,6 +311,30 @@ __device__ __forceinline__ void vcodes_to_f16x2(uint32_t w, uint32_t& even, uint
   else u8x4_to_f16x2_biased(w, even, odd);
 }
 
+// LSE merge of NS shared-memory slots of HS head rows (o: [NS*HS][128],
+// m, l: [NS*HS]) for head g, channels dd .. dd+3: acc = sum_w 2^(m_w - M) o_w,
+// L = sum_w 2^(m_w - M) l_w, M = max_w m_w.
+template <int NS, int HS>
+__device__ __forceinline__ void merge_slots(const float* merge_o, const float* merge_m, const float* merge_l, int g,
+                                            int dd, float4& acc, float& M, float& L) {
+  M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NS; ++w) M = fmaxf(M, merge_m[w * HS + g]);
+  acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  L = 0.f;
+#pragma unroll
+  for (int w = 0; w < NS; ++w) {
+    const float mw = merge_m[w * HS + g];
+    const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
+    const float4 v = *reinterpret_cast<const float4*>(&merge_o[(w * HS + g) * kHeadDim + dd]);
+    acc.x += f * v.x;
+    acc.y += f * v.y;
+    acc.z += f * v.z;
+    acc.w += f * v.w;
+    L += f * merge_l[w * HS + g];
+  }
+}
+
 // One online-softmax step of a warp over NB groups of its 16 tile rows: x
 // holds scaled scores (log2 units, -inf for masked rows) in the S^T
 // accumulator layout (x[j][0], x[j][2]: head column 2tig; x[j][1], x[j][3]:
@@ -1387,67 +1411,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           o[i][3] = fmaf(-1152.f, s1, o[i][3]);
         }
       }
-      // ---- merge the warps' (o, m, l) of this segment: warps 4..7 hand
-      // theirs to warps 0..3 through the merge slots, then 0..3 publish
+      // ---- merge the warps' (o, m, l) of this segment through shared
+      // memory slots of hs head rows.  bf16 middles with G <= 4: every warp
+      // publishes its own slot (eight slots of four heads) and one barrier
+      // precedes the CTA merge.  Otherwise warps 4..7 hand theirs to warps
+      // 0..3 first (four slots of eight heads), which merge and publish.
       float lr0 = l0, lr1 = l1;
 #pragma unroll
       for (int sh = 4; sh < 32; sh <<= 1) {
         lr0 += __shfl_xor_sync(0xffffffffu, lr0, sh);
         lr1 += __shfl_xor_sync(0xffffffffu, lr1, sh);
       }
-      const int slotw = warp & (kMergeSlots - 1);
-      float* ob = merge_o + slotw * kMaxGroup * kHeadDim;
-      if (warp >= kMergeSlots) {
+      const bool one_pass = !kQ8 && G <= 4;
+      const int hs = one_pass ? 4 : kMaxGroup;
+      auto publish = [&](int slotw) {
+        if (2 * tig < hs) {       // this lane's head columns 2tig, 2tig+1 exist in the slot
+          float* ob = merge_o + slotw * hs * kHeadDim;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          ob[(2 * tig) * kHeadDim + 16 * i + gid] = o[i][0];
-          ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] = o[i][1];
-          ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] = o[i][2];
-          ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] = o[i][3];
+          for (int i = 0; i < 8; ++i) {
+            ob[(2 * tig) * kHeadDim + 16 * i + gid] = o[i][0];
+            ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] = o[i][1];
+            ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] = o[i][2];
+            ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] = o[i][3];
+          }
+          if (gid == 0) {
+            merge_m[slotw * hs + 2 * tig] = m0;
+            merge_m[slotw * hs + 2 * tig + 1] = m1;
+            merge_l[slotw * hs + 2 * tig] = lr0;
+            merge_l[slotw * hs + 2 * tig + 1] = lr1;
+          }
         }
-        if (gid == 0) {
-          merge_m[slotw * kMaxGroup + 2 * tig] = m0;
-          merge_m[slotw * kMaxGroup + 2 * tig + 1] = m1;
-          merge_l[slotw * kMaxGroup + 2 * tig] = lr0;
-          merge_l[slotw * kMaxGroup + 2 * tig + 1] = lr1;
-        }
-      }
-      consumer_sync(cbar, cphase, a);
-      if (warp < kMergeSlots) {
-        const float mo0 = merge_m[slotw * kMaxGroup + 2 * tig], mo1 = merge_m[slotw * kMaxGroup + 2 * tig + 1];
-        const float lo0 = merge_l[slotw * kMaxGroup + 2 * tig], lo1 = merge_l[slotw * kMaxGroup + 2 * tig + 1];
-        const float mn0 = fmaxf(m0, mo0), mn1 = fmaxf(m1, mo1);
-        const float fa0 = m0 == NEG_INF ? 0.f : exp2f(m0 - mn0), fb0 = mo0 == NEG_INF ? 0.f : exp2f(mo0 - mn0);
-        const float fa1 = m1 == NEG_INF ? 0.f : exp2f(m1 - mn1), fb1 = mo1 == NEG_INF ? 0.f : exp2f(mo1 - mn1);
+      };
+      if (one_pass) {
+        publish(warp);
+      } else {
+        const int slotw = warp & (kMergeSlots - 1);
+        const float* ob = merge_o + slotw * kMaxGroup * kHeadDim;
+        if (warp >= kMergeSlots) publish(slotw);
+        consumer_sync(cbar, cphase, a);
+        if (warp < kMergeSlots) {
+          const float mo0 = merge_m[slotw * kMaxGroup + 2 * tig], mo1 = merge_m[slotw * kMaxGroup + 2 * tig + 1];
+          const float lo0 = merge_l[slotw * kMaxGroup + 2 * tig], lo1 = merge_l[slotw * kMaxGroup + 2 * tig + 1];
+          const float mn0 = fmaxf(m0, mo0), mn1 = fmaxf(m1, mo1);
+          const float fa0 = m0 == NEG_INF ? 0.f : exp2f(m0 - mn0), fb0 = mo0 == NEG_INF ? 0.f : exp2f(mo0 - mn0);
+          const float fa1 = m1 == NEG_INF ? 0.f : exp2f(m1 - mn1), fb1 = mo1 == NEG_INF ? 0.f : exp2f(mo1 - mn1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          o[i][0] = o[i][0] * fa0 + ob[(2 * tig) * kHeadDim + 16 * i + gid] * fb0;
-          o[i][1] = o[i][1] * fa1 + ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] * fb1;
-          o[i][2] = o[i][2] * fa0 + ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] * fb0;
-          o[i][3] = o[i][3] * fa1 + ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] * fb1;
+          for (int i = 0; i < 8; ++i) {
+            o[i][0] = o[i][0] * fa0 + ob[(2 * tig) * kHeadDim + 16 * i + gid] * fb0;
+            o[i][1] = o[i][1] * fa1 + ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] * fb1;
+            o[i][2] = o[i][2] * fa0 + ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] * fb0;
+            o[i][3] = o[i][3] * fa1 + ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] * fb1;
+          }
+          lr0 = lr0 * fa0 + lo0 * fb0;
+          lr1 = lr1 * fa1 + lo1 * fb1;
+          m0 = mn0;
+          m1 = mn1;
         }
-        lr0 = lr0 * fa0 + lo0 * fb0;
-        lr1 = lr1 * fa1 + lo1 * fb1;
-        m0 = mn0;
-        m1 = mn1;
-      }
-      // warp w < 4 overwrites only slot w, which only it read: a warp-level
-      // barrier separates its lanes' reads from the writes
-      __syncwarp();
-      if (warp < kMergeSlots) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          ob[(2 * tig) * kHeadDim + 16 * i + gid] = o[i][0];
-          ob[(2 * tig + 1) * kHeadDim + 16 * i + gid] = o[i][1];
-          ob[(2 * tig) * kHeadDim + 16 * i + gid + 8] = o[i][2];
-          ob[(2 * tig + 1) * kHeadDim + 16 * i + gid + 8] = o[i][3];
-        }
-        if (gid == 0) {
-          merge_m[slotw * kMaxGroup + 2 * tig] = m0;
-          merge_m[slotw * kMaxGroup + 2 * tig + 1] = m1;
-          merge_l[slotw * kMaxGroup + 2 * tig] = lr0;
-          merge_l[slotw * kMaxGroup + 2 * tig + 1] = lr1;
-        }
+        // warp w < 4 overwrites only slot w, which only it read: a warp-level
+        // barrier separates its lanes' reads from the writes
+        __syncwarp();
+        if (warp < kMergeSlots) publish(slotw);
       }
       // the segment's state now lives in the merge slots (the next tile
       // starts a segment); free its registers for the combine below
@@ -1463,22 +1486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // CTA-level merge, 4 channels per thread
       for (int q4 = ct; q4 < G * 32; q4 += kConsumerWarps * 32) {
         const int g = q4 >> 5, dd = (q4 & 31) * 4;
-        float M = NEG_INF;
-#pragma unroll
-        for (int w = 0; w < kMergeSlots; ++w) M = fmaxf(M, merge_m[w * kMaxGroup + g]);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float L = 0.f;
-#pragma unroll
-        for (int w = 0; w < kMergeSlots; ++w) {
-          const float mw = merge_m[w * kMaxGroup + g];
-          const float f = mw == NEG_INF ? 0.f : exp2f(mw - M);
-          const float4 v = *reinterpret_cast<const float4*>(&merge_o[(w * kMaxGroup + g) * kHeadDim + dd]);
-          acc.x += f * v.x;
-          acc.y += f * v.y;
-          acc.z += f * v.z;
-          acc.w += f * v.w;
-          L += f * merge_l[w * kMaxGroup + g];
-        }
+        float4 acc;
+        float M, L;
+        if (one_pass)
+          merge_slots<kConsumerWarps, 4>(merge_o, merge_m, merge_l, g, dd, acc, M, L);
+        else
+          merge_slots<kMergeSlots, kMaxGroup>(merge_o, merge_m, merge_l, g, dd, acc, M, L);
         if (single) {
           const float inv = L > 0.f ? 1.f / L : 0.f;
           *reinterpret_cast<float4*>(&dst[g * kHeadDim + dd]) =
@@ -1569,33 +1582,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first (layer, sequence) before the count, which nothing can change
     // before the last CTA stores them.
     const int nlb = a.nlayers * cv.B;
-    auto next_len = [&](int i, int& lb, int& n1, int& c1) {
+    // next lengths of (layer, sequence) i, and whether its active sequence's
+    // token id is outside [0, vocab) (then it counts as not special)
+    auto next_len = [&](int i, int& lb, int& n1, int& c1, bool& bad) {
       const int b = i % cv.B;
       lb = (a.layer + i / cv.B) * cv.B + b;
       // independent loads first: one round trip (two with token ids)
       const int act = __ldcg(&cv.active[b]);
       const int n = __ldcg(&cv.len[lb]);
       const int c = __ldcg(&cv.cnt[lb]);
-      const bool sp = token_special(a, b);
+      const int id = a.ids != nullptr ? a.ids[b] : 0;
+      const bool in_vocab = id >= 0 && id < cv.vocab;
+      const bool sp = a.ids != nullptr && in_vocab && cv.is_special[id] != 0;
       n1 = act != 0 && n < cv.capacity ? n + 1 : -1;
       c1 = n1 > 0 && sp && c < cv.spec_cap ? c + 1 : -1;
+      bad = a.ids != nullptr && act != 0 && !in_vocab;
     };
     // (Every length this CTA reads was read before its consumers left the
     // loop: the producer's last loads precede its final arrive.  The count
     // orders nothing else -- the cache writes are for the next kernel.)
     int lb0 = 0, n0 = -1, cn0 = -1;
-    if (ct < nlb) next_len(ct, lb0, n0, cn0);
+    bool bad0 = false;
+    if (ct < nlb) next_len(ct, lb0, n0, cn0, bad0);
     if (ct == 0) misc[2] = atomicAdd(&a.counters[E], 1) == (int)gridDim.x - 1 ? 1 : 0;
     consumer_sync(cbar, cphase, a);
     if (misc[2]) {
       for (int i = ct; i < nlb; i += kConsumerWarps * 32) {
         int lb = lb0, n1 = n0, c1 = cn0;
-        if (i != ct) next_len(i, lb, n1, c1);
+        bool bad = bad0;
+        if (i != ct) next_len(i, lb, n1, c1, bad);
         if (n1 > 0) cv.len[lb] = n1;
         if (c1 > 0) cv.cnt[lb] = c1;
-        const int b = i % cv.B;
-        if (a.ids != nullptr && __ldcg(&cv.active[b]) != 0 && (a.ids[b] < 0 || a.ids[b] >= cv.vocab))
-          set_status(cv, kStatusBadId);
+        if (bad) set_status(cv, kStatusBadId);
       }
       if (ct == 0) a.counters[E] = 0;
     }

@@ -225,13 +225,14 @@ def test_full_sequence_is_refused_before_launch(cuda):
     assert _max_err(o, case.expected(0, q, 600)) <= DECODE_TOL
 
 
-def test_out_of_range_id_is_reported(cuda):
+@pytest.mark.parametrize("offset", [5, -1], ids=["past_vocab", "negative"])
+def test_out_of_range_id_is_reported(cuda, offset):
     w = FASTGEN.scaled(num_layers=1, batch=2, context=300, policy_counts=(2, 2, 4))
     case = _fused(Case(w, total=302))
     case.prefill(0, 300)
     k, v, ids = _token(case, 0, 300)
     bad = ids.clone()
-    bad[1] = w.vocab + 5
+    bad[1] = w.vocab + offset if offset > 0 else offset
     case.cache.step(0, case.q(0, 301), k, v, bad)
     with pytest.raises(lkb.LeankError) as e:
         case.cache.check()
