@@ -402,7 +402,10 @@ __device__ __forceinline__ uint32_t tile_addr64(uint32_t base, int r, int c) {
 
 // kFmt: the cache's middle format (KvFormat).  The quantised instantiations
 // (INT8, FP8) handle sealed blocks; the bf16 one carries no code for them.
-template <int kFmt>
+// kPaged: the middle rows live in pages (cv.max_pages > 0).  The layouts'
+// producers differ per tile (page ids, tiles cut at page ends), so each is
+// compiled on its own and a contiguous cache runs no paged code.
+template <int kFmt, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
   constexpr bool kQ8 = kFmt != kKvBf16;
@@ -710,8 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // masked; a stage takes up to qper consecutive blocks (one bulk copy,
         // or one per page), so the producer's and the consumers' per-stage
         // work is paid once per 42-66 KB.
-        const bool paged = cv.max_pages > 0;
-        const bool bpaged = paged && cv.kv_format == kKvBf16;
+        constexpr bool paged = kPaged;
+        constexpr bool bpaged = kPaged && kFmt == kKvBf16;
         const int nta = (a1 - a0 + kTileRows - 1) / kTileRows;
         const int qfirst = q0 / kQBlockRows;
         const int nqb = q1 <= q0 ? 0 : (q1 - 1) / kQBlockRows - qfirst + 1;   // sealed blocks in range
@@ -745,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // after this CTA has read it; no other CTA reads it.
           const int anc = g.anc;
           const int xj = fused_launch && anc >= 0 && anc >= a0 && anc < a1 ? (anc - a0) / kTileRows : -1;
-          int32_t page_ahead = 0;
+          int32_t pq0 = 0, pq1 = 0, pq2 = 0, pq3 = 0;     // page ids of the next middle-row tiles
           int32_t qpg_ahead[kQPerStageNarrow] = {};
           for (int j = 0; j < nt; ++j) {
             const int region = j < nta ? 0 : j < nta + ntq ? 2 : 1;
@@ -780,14 +783,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 page = b * hd.qblocks + blk;
               }
             } else if (bpaged) {
-              const int pg = b0 / kPageRows + (j - nta - ntq);
+              const int jb = j - nta - ntq;           // middle-row tile = page of the range
+              const int pg = b0 / kPageRows + jb;
               r = max(b0, pg * kPageRows);
               rend = min(b1, (pg + 1) * kPageRows);
-              // page ids load one tile ahead (and before the slot wait); a
-              // missing page (status already recorded) reads page 0
-              page = j == nta + ntq ? __ldcg(pt + pg) : page_ahead;
-              if (j + 1 < nt) page_ahead = __ldcg(pt + pg + 1);
-              page = max(0, page);
+              // page ids load four tiles ahead (a one-tile lead leaves the
+              // id's L2 round trip exposed whenever a ring slot is free at
+              // once); a missing page (status already recorded) reads page 0
+              if (jb == 0) {
+                pq0 = __ldcg(pt + pg);
+                pq1 = 1 < ntb ? __ldcg(pt + pg + 1) : 0;
+                pq2 = 2 < ntb ? __ldcg(pt + pg + 2) : 0;
+                pq3 = 3 < ntb ? __ldcg(pt + pg + 3) : 0;
+              }
+              page = max(0, pq0);
+              pq0 = pq1;
+              pq1 = pq2;
+              pq2 = pq3;
+              pq3 = jb + 4 < ntb ? __ldcg(pt + pg + 4) : 0;
             } else {
               r = b0 + (j - nta - ntq) * kTileRows;
               rend = min(b1, r + kTileRows);
@@ -868,6 +881,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j == 0 && e + 1 < E) {
               ahead = entry_len(a, hb, e + 1);
               have_ahead = true;
+              if (paged) {
+                // the next entry's page ids into L2
+                const EntryId nid = entry_id(a, e + 1);
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(
+                    cv.page_table + (((int64_t)nid.l * cv.B + nid.b) * cv.Hkv + nid.h) * cv.max_pages));
+              }
             }
             if (fc < 0) {
               fc = range_owner(off, C, P);
@@ -1624,18 +1643,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t decode_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ctas, cudaStream_t stream) {
+// One instantiation: its shared-memory limit raised on first use, then the
+// launch.
+template <int kFmt, bool kPaged>
+static cudaError_t launch_one(const cudaLaunchConfig_t& cfg, const DecodeMaps& maps, const DecodeArgs& args) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t err =
-        cudaFuncSetAttribute(decode_kernel<kKvBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(decode_kernel<kKvInt8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(decode_kernel<kKvFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const cudaError_t err =
+        cudaFuncSetAttribute(decode_kernel<kFmt, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_done = true;
   }
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kFmt, kPaged>, maps, args);
+}
+
+cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ctas, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas);
   cfg.blockDim = dim3(kThreads);
@@ -1646,9 +1668,12 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ct
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (args.cv.kv_format == kKvInt8) return cudaLaunchKernelEx(&cfg, decode_kernel<kKvInt8>, maps, args);
-  if (args.cv.kv_format == kKvFp8) return cudaLaunchKernelEx(&cfg, decode_kernel<kKvFp8>, maps, args);
-  return cudaLaunchKernelEx(&cfg, decode_kernel<kKvBf16>, maps, args);
+  const bool paged = args.cv.max_pages > 0;
+  if (args.cv.kv_format == kKvInt8)
+    return paged ? launch_one<kKvInt8, true>(cfg, maps, args) : launch_one<kKvInt8, false>(cfg, maps, args);
+  if (args.cv.kv_format == kKvFp8)
+    return paged ? launch_one<kKvFp8, true>(cfg, maps, args) : launch_one<kKvFp8, false>(cfg, maps, args);
+  return paged ? launch_one<kKvBf16, true>(cfg, maps, args) : launch_one<kKvBf16, false>(cfg, maps, args);
 }
 
 }  // namespace lk
