@@ -74,37 +74,46 @@ MAX_COPIES = 256                    # rotating cache copies at most
 # split partials, each CTA's last box past its range end), applied to the
 # full launch's algorithmic bytes.
 NCU_TRAFFIC = {
-    "b87f1e1dbaefc81b:tiny:bf16:decode": 525568,
-    "b87f1e1dbaefc81b:llama31_8b_layer:bf16:fused": 88086784,
-    "b87f1e1dbaefc81b:llama31_8b_layer:bf16:decode": 88168960,
-    "b87f1e1dbaefc81b:llama31_8b_layer:int8:decode": 46443520,
-    "b87f1e1dbaefc81b:llama31_8b_layer:fp8:decode": 46442752,
-    "b87f1e1dbaefc81b:qwen25_7b_long:bf16:fused": 517348864,
-    "b87f1e1dbaefc81b:qwen25_7b_long:int8:decode": 278787328,
-    "b87f1e1dbaefc81b:qwen25_7b_long:fp8:decode": 278737664,
-    "b87f1e1dbaefc81b:serving_b64/2L:bf16:decode": 947137536,
-    "b87f1e1dbaefc81b:serving_b64/4L:bf16:decode": 2180094208,
-    "b87f1e1dbaefc81b:serving_b64/2L:bf16:fused": 946799104,
-    "b87f1e1dbaefc81b:serving_b64/4L:bf16:fused": 2180032000,
-    "b87f1e1dbaefc81b:serving_b64/2L:int8:decode": 637889792,
-    "b87f1e1dbaefc81b:serving_b64/4L:int8:decode": 1425141504,
-    "b87f1e1dbaefc81b:serving_b64/2L:fp8:decode": 637803008,
-    "b87f1e1dbaefc81b:serving_b64/4L:fp8:decode": 1425130752,
-    "b87f1e1dbaefc81b:fastgen_mix/2L:bf16:fused": 445602048,
-    "b87f1e1dbaefc81b:fastgen_mix/4L:bf16:fused": 867552000,
-    "b87f1e1dbaefc81b:fastgen_mix/2L:int8:decode": 265468160,
-    "b87f1e1dbaefc81b:fastgen_mix/4L:int8:decode": 514942464,
-    "b87f1e1dbaefc81b:fastgen_mix/2L:fp8:decode": 265115392,
-    "b87f1e1dbaefc81b:fastgen_mix/4L:fp8:decode": 514908672,
+    "a658a922510db767:fastgen_mix/2L:bf16:fused": 445635328,
+    "a658a922510db767:fastgen_mix/2L:fp8:decode": 265385728,
+    "a658a922510db767:fastgen_mix/2L:int8:decode": 265501952,
+    "a658a922510db767:fastgen_mix/4L:bf16:fused": 867274240,
+    "a658a922510db767:fastgen_mix/4L:fp8:decode": 514929152,
+    "a658a922510db767:fastgen_mix/4L:int8:decode": 515043840,
+    "a658a922510db767:llama31_8b_layer:bf16:decode": 88065792,
+    "a658a922510db767:llama31_8b_layer:bf16:fused": 88070656,
+    "a658a922510db767:llama31_8b_layer:fp8:decode": 46447616,
+    "a658a922510db767:llama31_8b_layer:int8:decode": 46448128,
+    "a658a922510db767:llama31_8b_layer/paged:bf16:fused": 87910400,
+    "a658a922510db767:qwen25_7b_long:bf16:fused": 517307136,
+    "a658a922510db767:qwen25_7b_long:fp8:decode": 278884608,
+    "a658a922510db767:qwen25_7b_long:int8:decode": 278860800,
+    "a658a922510db767:serving_b64/2L:bf16:decode": 947173632,
+    "a658a922510db767:serving_b64/2L:bf16:fused": 947049216,
+    "a658a922510db767:serving_b64/2L:fp8:decode": 638276352,
+    "a658a922510db767:serving_b64/2L:int8:decode": 637889024,
+    "a658a922510db767:serving_b64/2L/paged:bf16:decode": 946441984,
+    "a658a922510db767:serving_b64/2L/paged:bf16:fused": 946357504,
+    "a658a922510db767:serving_b64/2L/paged:int8:decode": 638337280,
+    "a658a922510db767:serving_b64/4L:bf16:decode": 2179853824,
+    "a658a922510db767:serving_b64/4L:bf16:fused": 2179924736,
+    "a658a922510db767:serving_b64/4L:fp8:decode": 1425155328,
+    "a658a922510db767:serving_b64/4L:int8:decode": 1425082368,
+    "a658a922510db767:serving_b64/4L/paged:bf16:decode": 2178627072,
+    "a658a922510db767:serving_b64/4L/paged:bf16:fused": 2178602752,
+    "a658a922510db767:serving_b64/4L/paged:int8:decode": 1425574400,
+    "a658a922510db767:tiny:bf16:decode": 516608,
 }
 # 32-layer launches: DRAM bytes per algorithmic byte of the 4-layer capture
 NCU_TRAFFIC_RATIO = {
-    "b87f1e1dbaefc81b:serving_b64:bf16:decode": 2180094208 / 2178351104,
-    "b87f1e1dbaefc81b:serving_b64:int8:decode": 1425141504 / 1396178944,
-    "b87f1e1dbaefc81b:serving_b64:fp8:decode": 1425130752 / 1396178944,
-    "b87f1e1dbaefc81b:fastgen_mix:bf16:fused": 867552000 / 856061952,
-    "b87f1e1dbaefc81b:fastgen_mix:int8:decode": 514942464 / 504039424,
-    "b87f1e1dbaefc81b:fastgen_mix:fp8:decode": 514908672 / 504039424,
+    "a658a922510db767:serving_b64:bf16:decode": 2179853824 / 2178351104,
+    "a658a922510db767:serving_b64:int8:decode": 1425082368 / 1396178944,
+    "a658a922510db767:serving_b64:fp8:decode": 1425155328 / 1396178944,
+    "a658a922510db767:serving_b64/paged:bf16:decode": 2178627072 / 2178351104,
+    "a658a922510db767:serving_b64/paged:int8:decode": 1425574400 / 1396178944,
+    "a658a922510db767:fastgen_mix:bf16:fused": 867274240 / 856061952,
+    "a658a922510db767:fastgen_mix:int8:decode": 515043840 / 504039424,
+    "a658a922510db767:fastgen_mix:fp8:decode": 514929152 / 504039424,
 }
 
 
@@ -487,7 +496,7 @@ def run_gpu(args, rank, local_rank, world):
     peak, peak_kind = _peaks()
     achieved = alg_bytes / kernel_s / 1e9
     wkey = w.name if w.num_layers == S.WORKLOAD_BY_NAME[w.name].num_layers else f"{w.name}/{w.num_layers}L"
-    # the captures are of contiguous caches: a paged launch has no entry
+    # paged caches have entries of their own (their producer differs per tile)
     layout_key = "/paged" if paged else ""
     tkey = f"{_decode_source_hash()}:{wkey}{layout_key}:{args.kv}:{'fused' if fused else 'decode'}"
     traffic = NCU_TRAFFIC.get(tkey)
