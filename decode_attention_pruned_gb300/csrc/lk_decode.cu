@@ -114,8 +114,11 @@ struct SmemLayout {
   static constexpr int kScanOff = kCBarOff + 8;
   static constexpr int kMiscOff = kScanOff + (kThreads / 32) * 8;
   static constexpr int kHeadsOff = kMiscOff + 12 * 8;                        // head descriptors of the launch
-  static constexpr int kBytes = kHeadsOff + kMaxSmemHeads * (int)sizeof(HeadDesc);
+  static constexpr int kLensOff = kHeadsOff + kMaxSmemHeads * (int)sizeof(HeadDesc);   // lengths of <= 32 entries
+  static constexpr int kSBarOff = kLensOff + 32 * 12;                        // split-done barrier
+  static constexpr int kBytes = kSBarOff + 8;
 };
+static_assert(SmemLayout::kSBarOff % 8 == 0, "mbarrier alignment");
 constexpr int kSmemBytes = SmemLayout::kBytes + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per block");
 
@@ -143,6 +146,7 @@ struct EntryLen {
   int cnt;    // special rows (SPECIAL heads), else 0
   int act;    // fused launches: the sequence takes the appended token
 };
+static_assert(sizeof(EntryLen) == 12, "shared-memory length table");
 
 // Rows of an entry in line order: n_a full width, n_q in sealed blocks,
 // n_b bf16 kept-channel rows (quantised caches: the open tail block).  mrow: the
@@ -405,7 +409,11 @@ __device__ __forceinline__ uint32_t tile_addr64(uint32_t base, int r, int c) {
 // kPaged: the middle rows live in pages (cv.max_pages > 0).  The layouts'
 // producers differ per tile (page ids, tiles cut at page ends), so each is
 // compiled on its own and a contiguous cache runs no paged code.
-template <int kFmt, bool kPaged>
+// kSmallE: the launch has at most 32 (layer, sequence, kv head) entries
+// (the host picks it): one warp holds every entry's lengths, which the
+// kernel then keeps in shared memory; larger launches carry none of that
+// code.
+template <int kFmt, bool kPaged, bool kSmallE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ DecodeMaps maps, const DecodeArgs a) {
   constexpr bool kQ8 = kFmt != kKvBf16;
@@ -426,6 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const CacheView& cv = a.cv;
   const int E = a.nlayers * cv.B * cv.Hkv;
   const int G = cv.G;
+  // Launches of at most 32 entries keep the lengths each warp's split read
+  // in shared memory and read them there from then on; a fused one then
+  // advances the lengths as soon as every CTA has finished its split,
+  // instead of at its end (see the early advance below).
+  EntryLen* slens = reinterpret_cast<EntryLen*>(sm + SmemLayout::kLensOff);
+  const uint32_t sbar = base + SmemLayout::kSBarOff;
+  const bool early_len = !kQ8 && kSmallE && a.k_new != nullptr;
 
   static_assert(kSlots < 32, "one barrier pair per lane of warp 0, plus the consumer barrier");
   if (tid < kSlots) {
@@ -434,6 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   } else if (tid == kSlots) {
     mbar_init(base + SmemLayout::kCBarOff, kConsumerWarps);
+    fence_barrier_init();
+  } else if (tid == kSlots + 1) {
+    mbar_init(base + SmemLayout::kSBarOff, kThreads / 32);
     fence_barrier_init();
   }
   if (tid == 0) {
@@ -522,10 +540,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     start = cta < P ? (uint64_t)cta * cq + ((uint32_t)cta * cr) / (uint32_t)P : C;
     end = cta < P ? (uint64_t)(cta + 1) * cq + ((uint32_t)(cta + 1) * cr) / (uint32_t)P : C;
   };
-  if (E <= 32) {
+  if constexpr (kSmallE) {
     // few entries: every warp scans them all itself (lane = entry), so no
     // block barrier stands between the length loads and the first copy
     const Entry g = lane < E ? entry_geometry(a, hb, lane) : Entry{0, 0, 0, 0, -1, {0, 0, 0}, -1};
+    // every warp writes the same values; each reads back its own writes
+    if (lane < E) slens[lane] = g.len;
+    __syncwarp();
     const uint64_t cost = entry_cost(g);
     uint64_t incl = cost;
 #pragma unroll
@@ -548,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fg.len.cnt = __shfl_sync(0xffffffffu, g.len.cnt, src);
     fg.len.act = __shfl_sync(0xffffffffu, g.len.act, src);
     fg.anc = __shfl_sync(0xffffffffu, g.anc, src);
+    // this warp's length loads are done (their values are in use)
+    if (early_len && lane == 0) mbar_arrive(sbar);
   } else {
     // per-thread chunks of entries, block exclusive scan
     const int per = (E + kThreads - 1) / kThreads;
@@ -675,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool have_ahead = false;
       for (; ok && e < E && off < end; ++e) {
         if (e != e0) {
-          g = entry_from(a, hb, e, have_ahead ? ahead : entry_len(a, hb, e));
+          g = entry_from(a, hb, e, have_ahead ? ahead : kSmallE ? slens[e] : entry_len(a, hb, e));
           have_ahead = false;
         }
         const uint64_t cost = entry_cost(g);
@@ -879,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++issued;
             if (j == 0 && e + 1 < E) {
-              ahead = entry_len(a, hb, e + 1);
+              ahead = kSmallE ? slens[e + 1] : entry_len(a, hb, e + 1);
               have_ahead = true;
               if (paged) {
                 // the next entry's page ids into L2
@@ -990,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto fused_extras = [&](int e) {
     const EntryId id = entry_id(a, e);
     const HeadDesc& hd = hb[id.lr * cv.Hkv + id.h];
-    const EntryLen len = entry_len(a, hb, e);
+    const EntryLen len = kSmallE ? slens[e] : entry_len(a, hb, e);
     const bool add_new = len.act && (hd.policy != kSpecial || (token_special(a, id.b) && len.cnt < hd.cap_a));
     const bool add_ev = len.act && hd.policy == kFull && hd.n_kept > 0 && len.n >= cv.S + cv.W;
     const int64_t slot =
@@ -1037,17 +1060,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   // fused_extras and a consumer barrier.
   auto fused_edit = [&](int e) {
     const EntryId id = entry_id(a, e);
-    const EntryLen len = entry_len(a, hb, e);
+    const EntryLen len = kSmallE ? slens[e] : entry_len(a, hb, e);
     if (!len.act) return;
     const size_t src = (((size_t)id.lr * cv.B + id.b) * cv.Hkv + id.h) * kHeadDim;
     append_head<false>(cv, id.l, id.b, id.h, len.n, len.cnt, token_special(a, id.b), a.k_new + src,
                        a.v_new + src, lane);
   };
 
+  const int nlb = a.nlayers * cv.B;
+  // next lengths of (layer, sequence) i, and whether its active sequence's
+  // token id is outside [0, vocab) (then it counts as not special)
+  auto next_len = [&](int i, int& lb, int& n1, int& c1, bool& bad) {
+    const int b = i % cv.B;
+    lb = (a.layer + i / cv.B) * cv.B + b;
+    // independent loads first: one round trip (two with token ids)
+    const int act = __ldcg(&cv.active[b]);
+    const int n = __ldcg(&cv.len[lb]);
+    const int c = __ldcg(&cv.cnt[lb]);
+    const int id = a.ids != nullptr ? a.ids[b] : 0;
+    const bool in_vocab = id >= 0 && id < cv.vocab;
+    const bool sp = a.ids != nullptr && in_vocab && cv.is_special[id] != 0;
+    n1 = act != 0 && n < cv.capacity ? n + 1 : -1;
+    c1 = n1 > 0 && sp && c < cv.spec_cap ? c + 1 : -1;
+    bad = a.ids != nullptr && act != 0 && !in_vocab;
+  };
+
   // entries with no resident token, by CTA (e mod grid): o = 0, or with a
   // fused append the new token alone
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
-    if (entry_cost(entry_geometry(a, hb, e)) != 0) continue;
+    if (entry_cost(entry_from(a, hb, e, kSmallE ? slens[e] : entry_len(a, hb, e))) != 0) continue;
     const EntryId id = entry_id(a, e);
     float* dst = a.o + (((size_t)id.lr * cv.B + id.b) * cv.Hq + (size_t)id.h * G) * kHeadDim;
     if (fused) {
@@ -1068,6 +1109,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       consumer_sync(cbar, cphase, a);
     } else {
       for (int i = ct; i < G * kHeadDim; i += kConsumerWarps * 32) dst[i] = 0.f;
+    }
+  }
+
+  // Early length advance (fused launches of at most 32 entries): once every
+  // warp of this CTA is past its split (the split-done barrier), nothing in
+  // the CTA reads the lengths from memory again, so the CTA is counted; the
+  // CTA that completes the count advances them, as the append kernel does
+  // per sequence.  The last consumer warp does it while the first tiles are
+  // in flight.  The barrier waits its fixed bound whatever the configured
+  // limit: on time-out the status is set and the lengths stay.
+  if (early_len && warp == kConsumerWarps - 1) {
+    if (!mbar_wait_bounded(sbar, 0u, kDrainLimitNs)) {
+      if (lane == 0) record_status(a, kStatusTimeout);
+    } else {
+      int last = 0;
+      if (lane == 0) last = atomicAdd(&a.counters[E], 1) == (int)gridDim.x - 1 ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, last, 0)) {
+        for (int i = lane; i < nlb; i += 32) {
+          int lb, n1, c1;
+          bool bad;
+          next_len(i, lb, n1, c1, bad);
+          if (n1 > 0) cv.len[lb] = n1;
+          if (c1 > 0) cv.cnt[lb] = c1;
+          if (bad) set_status(cv, kStatusBadId);
+        }
+        __syncwarp();
+        if (lane == 0) a.counters[E] = 0;
+      }
     }
   }
 
@@ -1594,29 +1663,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (fused) {
+  if (fused && !early_len) {
     // Lengths move only when every CTA is done (each read them in its work
     // split): the last CTA to finish advances them, as the append kernel
     // does per sequence.  Every CTA loads the new values of its threads'
     // first (layer, sequence) before the count, which nothing can change
     // before the last CTA stores them.
-    const int nlb = a.nlayers * cv.B;
-    // next lengths of (layer, sequence) i, and whether its active sequence's
-    // token id is outside [0, vocab) (then it counts as not special)
-    auto next_len = [&](int i, int& lb, int& n1, int& c1, bool& bad) {
-      const int b = i % cv.B;
-      lb = (a.layer + i / cv.B) * cv.B + b;
-      // independent loads first: one round trip (two with token ids)
-      const int act = __ldcg(&cv.active[b]);
-      const int n = __ldcg(&cv.len[lb]);
-      const int c = __ldcg(&cv.cnt[lb]);
-      const int id = a.ids != nullptr ? a.ids[b] : 0;
-      const bool in_vocab = id >= 0 && id < cv.vocab;
-      const bool sp = a.ids != nullptr && in_vocab && cv.is_special[id] != 0;
-      n1 = act != 0 && n < cv.capacity ? n + 1 : -1;
-      c1 = n1 > 0 && sp && c < cv.spec_cap ? c + 1 : -1;
-      bad = a.ids != nullptr && act != 0 && !in_vocab;
-    };
     // (Every length this CTA reads was read before its consumers left the
     // loop: the producer's last loads precede its final arrive.  The count
     // orders nothing else -- the cache writes are for the next kernel.)
@@ -1645,16 +1697,27 @@ size_t decode_smem_bytes() { return kSmemBytes; }
 
 // One instantiation: its shared-memory limit raised on first use, then the
 // launch.
-template <int kFmt, bool kPaged>
+template <int kFmt, bool kPaged, bool kSmallE>
 static cudaError_t launch_one(const cudaLaunchConfig_t& cfg, const DecodeMaps& maps, const DecodeArgs& args) {
   static bool attr_done = false;
   if (!attr_done) {
-    const cudaError_t err =
-        cudaFuncSetAttribute(decode_kernel<kFmt, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const cudaError_t err = cudaFuncSetAttribute(decode_kernel<kFmt, kPaged, kSmallE>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (err != cudaSuccess) return err;
     attr_done = true;
   }
-  return cudaLaunchKernelEx(&cfg, decode_kernel<kFmt, kPaged>, maps, args);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kFmt, kPaged, kSmallE>, maps, args);
+}
+
+// The instantiation of a format for the cache's layout and the launch's
+// entry count.
+template <int kFmt>
+static cudaError_t launch_fmt(const cudaLaunchConfig_t& cfg, const DecodeMaps& maps, const DecodeArgs& args) {
+  const bool paged = args.cv.max_pages > 0;
+  const bool small = (int64_t)args.nlayers * args.cv.B * args.cv.Hkv <= 32;
+  if (paged)
+    return small ? launch_one<kFmt, true, true>(cfg, maps, args) : launch_one<kFmt, true, false>(cfg, maps, args);
+  return small ? launch_one<kFmt, false, true>(cfg, maps, args) : launch_one<kFmt, false, false>(cfg, maps, args);
 }
 
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ctas, cudaStream_t stream) {
@@ -1668,12 +1731,9 @@ cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ct
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const bool paged = args.cv.max_pages > 0;
-  if (args.cv.kv_format == kKvInt8)
-    return paged ? launch_one<kKvInt8, true>(cfg, maps, args) : launch_one<kKvInt8, false>(cfg, maps, args);
-  if (args.cv.kv_format == kKvFp8)
-    return paged ? launch_one<kKvFp8, true>(cfg, maps, args) : launch_one<kKvFp8, false>(cfg, maps, args);
-  return paged ? launch_one<kKvBf16, true>(cfg, maps, args) : launch_one<kKvBf16, false>(cfg, maps, args);
+  if (args.cv.kv_format == kKvInt8) return launch_fmt<kKvInt8>(cfg, maps, args);
+  if (args.cv.kv_format == kKvFp8) return launch_fmt<kKvFp8>(cfg, maps, args);
+  return launch_fmt<kKvBf16>(cfg, maps, args);
 }
 
 }  // namespace lk

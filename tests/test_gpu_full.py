@@ -183,3 +183,27 @@ def test_full_llama31_8b_layer_int8_paged(cuda):
     case = Case(w, total=w.context, gen_device=cuda, kv_format=lkb.KV_INT8, middle_tokens=w.context)
     pairs = [(0, h) for h in range(w.num_kv_heads)]
     _check_layer(case, 0, w.context, pairs, pairs)
+
+
+def test_full_llama31_8b_layer_paged(cuda):
+    # bf16 middle rows in 128-row pages: each entry's ~248 pages are split
+    # over 16 CTAs, most of which start inside a page (a short first tile,
+    # then page ids loaded four tiles ahead)
+    w = S.WORKLOADS[1]
+    case = Case(w, total=w.context, gen_device=cuda, middle_tokens=w.context)
+    pairs = [(0, h) for h in range(w.num_kv_heads)]
+    _check_layer(case, 0, w.context, pairs, pairs, fused=True)
+
+
+def test_full_serving_b64_paged_all_layers(cuda):
+    # the 32-layer serving step on a paged cache (24 pages per entry, every
+    # CTA range crossing entries), as the bench's --layout paged runs it
+    w = S.WORKLOADS[2]
+    case = Case(w, total=w.context, gen_device=cuda, middle_tokens=w.batch * w.context)
+    rng = np.random.default_rng(13)
+
+    def pick(layer):
+        pairs = _sample_pairs(w, layer, 3, rng)
+        return pairs, pairs[:1]
+
+    _check_all_layers(case, w.context, pick, fused=False)
