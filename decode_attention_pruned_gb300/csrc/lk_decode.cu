@@ -61,19 +61,18 @@ constexpr int kMergeSlots = 4;                          // (o, m, l) slots of th
 constexpr int kQStride = kHeadDim + 8;                  // padded q row (bf16): conflict-free ldmatrix
 // Stages live in a byte ring: a stage holds a K tile (128 rows x width) and a
 // V tile (128 rows x 128), so narrow-K tiles (40 KB at k = 32) keep five
-// stages in flight where full-width ones (64 KB) keep three; stages of two
-// or three sealed blocks (42-66 KB) keep three.
+// stages in flight where full-width ones (64 KB) keep three; stages of
+// three sealed blocks (62-99 KB) keep two or three.
 constexpr int kSlots = 16;                              // barrier pairs = stages in flight at most (power of 2)
 constexpr int kRingBytes = 200 * 1024;
 // A launch over at most this many (layer, kv head) pairs keeps their head
 // descriptors in shared memory, copied before the dependency wait: after it
 // the work split and the producer read them there instead of through L2.
 constexpr int kMaxSmemHeads = 56;
-// Sealed blocks per stage: three of k = 32 (62 KB), else two (up to 66 KB).
-constexpr int kQPerStageNarrow = 3;
-constexpr int kQPerStage = 2;
-static_assert(kQPerStageNarrow * 132 * (32 + 128) <= 66 * 1024 && kQPerStage * 132 * (128 + 128) <= 66 * 1024,
-              "three stages of sealed blocks fit the ring");
+// Sealed blocks per stage: three (62 KB at k = 32 .. 99 KB at k = 128);
+// at least two stages fit the ring.
+constexpr int kQPerStage = 3;
+static_assert(2 * kQPerStage * 132 * (128 + 128) <= kRingBytes, "stages of sealed blocks fit the ring");
 constexpr int kUnitsA = 2 * kHeadDim * 2;               // line cost of a full-width row: its bytes
 static_assert(kUnitsA == 2 * kHeadDim + 256, "a full-width row costs what a k = 128 middle row costs");
 constexpr uint64_t kMinCtaBytes = 64 * 1024;            // line bytes a CTA takes at least (one full-width tile)
@@ -735,13 +734,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // view).  Sealed blocks: whole blocks loaded, rows outside the range
         // masked; a stage takes up to qper consecutive blocks (one bulk copy,
         // or one per page), so the producer's and the consumers' per-stage
-        // work is paid once per 42-66 KB.
+        // work is paid once per 62-99 KB.
         constexpr bool paged = kPaged;
         constexpr bool bpaged = kPaged && kFmt == kKvBf16;
         const int nta = (a1 - a0 + kTileRows - 1) / kTileRows;
         const int qfirst = q0 / kQBlockRows;
         const int nqb = q1 <= q0 ? 0 : (q1 - 1) / kQBlockRows - qfirst + 1;   // sealed blocks in range
-        const int qper = g.kb == 32 ? kQPerStageNarrow : kQPerStage;
+        const int qper = kQPerStage;
         const int ntq = (nqb + qper - 1) / qper;
         const int ntb = b1 <= b0   ? 0
                         : bpaged ? (b1 - 1) / kPageRows - b0 / kPageRows + 1
@@ -772,13 +771,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int anc = g.anc;
           const int xj = fused_launch && anc >= 0 && anc >= a0 && anc < a1 ? (anc - a0) / kTileRows : -1;
           int32_t pq0 = 0, pq1 = 0, pq2 = 0, pq3 = 0;     // page ids of the next middle-row tiles
-          int32_t qpg_ahead[kQPerStageNarrow] = {};
+          int32_t qpg_ahead[kQPerStage] = {};
           for (int j = 0; j < nt; ++j) {
             const int region = j < nta ? 0 : j < nta + ntq ? 2 : 1;
             const int width = region == 0 ? kHeadDim : g.kb;
             int r, rend, rlo = 0, nq = 0;
             int32_t page = 0;
-            int32_t qpg[kQPerStageNarrow] = {};
+            int32_t qpg[kQPerStage] = {};
             if (region == 0) {
               r = a0 + j * kTileRows;
               rend = min(a1, r + kTileRows);
@@ -792,14 +791,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // page ids load one stage ahead (and before the slot wait); a
                 // missing page (status already recorded) reads page 0
 #pragma unroll
-                for (int i = 0; i < kQPerStageNarrow; ++i) {
+                for (int i = 0; i < kQPerStage; ++i) {
                   if (j == nta && i < nq) qpg_ahead[i] = __ldcg(pt + blk + i);
                   qpg[i] = max(0, qpg_ahead[i]);
                 }
                 if (j + 1 < nta + ntq) {
                   const int nb = blk + qper, nq2 = min(qper, qfirst + nqb - nb);
 #pragma unroll
-                  for (int i = 0; i < kQPerStageNarrow; ++i)
+                  for (int i = 0; i < kQPerStage; ++i)
                     if (i < nq2) qpg_ahead[i] = __ldcg(pt + nb + i);
                 }
               } else {
@@ -872,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_load(kdst, cv.qpool + hd.qoff + (int64_t)page * qb, bytes, fb, policy);
               } else {
 #pragma unroll
-                for (int i = 0; i < kQPerStageNarrow; ++i)
+                for (int i = 0; i < kQPerStage; ++i)
                   if (i < nq) bulk_load(kdst + i * qb, cv.qpool + hd.qoff + (int64_t)qpg[i] * qb, qb, fb, policy);
               }
             } else {
