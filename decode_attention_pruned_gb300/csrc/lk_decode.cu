@@ -19,9 +19,10 @@
 //     such that every CTA takes at least 64 KB; the CTAs touching an entry
 //     are exactly first..last and each writes one partial.
 //   * Per CTA: warp 8 (one lane) issues one TMA load per K tile and one per V
-//     tile (swizzled boxes), or one bulk copy per two or three consecutive
-//     sealed blocks, into a FIFO ring of variable-size stages with sixteen
-//     mbarrier slots; warps 0-7 each take 16 rows of every 128-row tile.
+//     tile (swizzled boxes), or one bulk copy per three consecutive sealed
+//     blocks, into a FIFO ring of variable-size stages with sixteen
+//     mbarrier slots; warps 0-7 each take 16 rows of every 128-row tile (of
+//     every block of a stage at once).
 //   * Tensor cores (mma.sync m16n8k16, fp32 accumulate) with tokens on M:
 //     S^T[16 tok x 8] = K[16 x w] Q^T[w x 8] and O^T[128 x 8] += V^T P^T, so
 //     the G <= 8 query heads only pad N.  P goes from the S^T accumulator to
@@ -30,15 +31,22 @@
 //     codes enter the f16 mmas exactly; the scales fold into q and p.
 //   * Segment end: warps merge through shared memory; a CTA that owns the
 //     whole entry writes o, otherwise it writes (o, m, l) to its partial slot
-//     and the last of the entry's CTAs (atomic counter) merges them.
+//     and the last of the entry's CTAs (acquire-release counter add) merges
+//     them.
+//   * Instantiations: one per middle format, cache layout (contiguous or
+//     paged) and launch size (at most 32 entries or more), picked on the
+//     host.
 //   * Fused append (lk_step, bf16 middle): the launch also appends one token
 //     per sequence, as an append kernel followed by this decode would.  The
 //     window slot the token replaces is left out of the scores; the CTA whose
 //     range holds that slot (else full-width row 0) loads the token, the row
 //     it evicts and the kept-channel list as one more stage, folds the token
 //     (all channels) and the evicted row (kept channels) into its softmax,
-//     and writes both into the cache after it has read the slot.  The last
-//     CTA to finish advances the lengths, which every CTA read in its split.
+//     and writes both into the cache after it has read the slot.  The
+//     lengths advance once no CTA reads them again: right after every CTA's
+//     work split when the launch has at most 32 entries (the split's copy in
+//     shared memory serves the rest of the launch), else when the last CTA
+//     finishes.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
