@@ -309,3 +309,42 @@ def test_fused_query_group_sizes(cuda, hq, hkv):
         assert float((of - os_).abs().max()) <= 1e-4, t
     torch.cuda.synchronize()
     assert torch.equal(fused.cache.buffer, split.cache.buffer)
+
+
+@pytest.mark.parametrize("layers,batch,hkv", [(1, 4, 8), (1, 3, 11), (4, 2, 4), (3, 11, 1)],
+                         ids=["E32-1layer", "E33-1layer", "E32-4layers", "E33-3layers"])
+def test_fused_steps_either_side_of_32_entries(cuda, layers, batch, hkv):
+    # Launches of at most 32 (layer, sequence, kv head) entries keep the
+    # lengths their split read in shared memory and advance them right after
+    # every CTA's split; larger ones advance them at the end.  Both sides of
+    # the boundary, one layer and several, with LOCAL / SPECIAL / FULL heads:
+    # outputs against the oracle and the two-launch path, lengths after every
+    # step, and the cache byte for byte.
+    n = layers * hkv
+    counts = (n // 3, n // 3, n - 2 * (n // 3))
+    w = FASTGEN.scaled(num_layers=layers, batch=batch, num_q_heads=4 * hkv, num_kv_heads=hkv, context=600,
+                       policy_counts=counts)
+    fused, split = _twins(w, 612)
+    L = w.num_layers
+    for layer in range(L):
+        fused.prefill(layer, 600)
+        split.prefill(layer, 600)
+    for t in range(600, 612):
+        qs = torch.stack([fused.q(l, t + 1, step=t) for l in range(L)]).contiguous()
+        ks = torch.stack([_token(fused, l, t)[0] for l in range(L)]).contiguous()
+        vs = torch.stack([_token(fused, l, t)[1] for l in range(L)]).contiguous()
+        ids = _token(fused, 0, t)[2]
+        of = fused.cache.step_layers(0, qs, ks, vs, ids)
+        split.cache.append_layers(0, ks, vs, ids)
+        os_ = split.cache.decode_layers(0, qs)
+        fused.cache.check()
+        for layer in range(L):
+            assert list(fused.cache.lengths(layer)) == [t + 1] * batch, (t, layer)
+        assert float((of - os_).abs().max()) <= 1e-4, t
+        if t % 4 == 3:
+            for layer in range(L):
+                assert _max_err(of[layer], fused.expected(layer, qs[layer], t + 1)) <= DECODE_TOL, (t, layer)
+    torch.cuda.synchronize()
+    assert torch.equal(fused.cache.buffer, split.cache.buffer)
+    for layer in range(L):
+        fused.check_layout(layer, 612)
