@@ -74,46 +74,46 @@ MAX_COPIES = 256                    # rotating cache copies at most
 # split partials, each CTA's last box past its range end), applied to the
 # full launch's algorithmic bytes.
 NCU_TRAFFIC = {
-    "58386bebce908855:fastgen_mix/2L:bf16:fused": 445553920,
-    "58386bebce908855:fastgen_mix/2L:fp8:decode": 265454848,
-    "58386bebce908855:fastgen_mix/2L:int8:decode": 265398784,
-    "58386bebce908855:fastgen_mix/4L:bf16:fused": 867623168,
-    "58386bebce908855:fastgen_mix/4L:fp8:decode": 514760960,
-    "58386bebce908855:fastgen_mix/4L:int8:decode": 515117824,
-    "58386bebce908855:llama31_8b_layer:bf16:decode": 87901696,
-    "58386bebce908855:llama31_8b_layer:bf16:fused": 88002560,
-    "58386bebce908855:llama31_8b_layer:fp8:decode": 46434816,
-    "58386bebce908855:llama31_8b_layer:int8:decode": 46437120,
-    "58386bebce908855:llama31_8b_layer/paged:bf16:fused": 87954688,
-    "58386bebce908855:qwen25_7b_long:bf16:fused": 517366272,
-    "58386bebce908855:qwen25_7b_long:fp8:decode": 278887936,
-    "58386bebce908855:qwen25_7b_long:int8:decode": 278878976,
-    "58386bebce908855:serving_b64/2L:bf16:decode": 947132160,
-    "58386bebce908855:serving_b64/2L:bf16:fused": 946755840,
-    "58386bebce908855:serving_b64/2L:fp8:decode": 637858560,
-    "58386bebce908855:serving_b64/2L:int8:decode": 637961472,
-    "58386bebce908855:serving_b64/2L/paged:bf16:decode": 946527744,
-    "58386bebce908855:serving_b64/2L/paged:bf16:fused": 946539520,
-    "58386bebce908855:serving_b64/2L/paged:int8:decode": 637942272,
-    "58386bebce908855:serving_b64/4L:bf16:decode": 2179910912,
-    "58386bebce908855:serving_b64/4L:bf16:fused": 2179837184,
-    "58386bebce908855:serving_b64/4L:fp8:decode": 1424805632,
-    "58386bebce908855:serving_b64/4L:int8:decode": 1425400064,
-    "58386bebce908855:serving_b64/4L/paged:bf16:decode": 2178608896,
-    "58386bebce908855:serving_b64/4L/paged:bf16:fused": 2178280448,
-    "58386bebce908855:serving_b64/4L/paged:int8:decode": 1425447936,
-    "58386bebce908855:tiny:bf16:decode": 516096,
+    "aa19380664917386:fastgen_mix/2L:bf16:fused": 445553920,
+    "aa19380664917386:fastgen_mix/2L:fp8:decode": 265454848,
+    "aa19380664917386:fastgen_mix/2L:int8:decode": 265398784,
+    "aa19380664917386:fastgen_mix/4L:bf16:fused": 867623168,
+    "aa19380664917386:fastgen_mix/4L:fp8:decode": 514760960,
+    "aa19380664917386:fastgen_mix/4L:int8:decode": 515117824,
+    "aa19380664917386:llama31_8b_layer:bf16:decode": 87901696,
+    "aa19380664917386:llama31_8b_layer:bf16:fused": 88002560,
+    "aa19380664917386:llama31_8b_layer:fp8:decode": 46434816,
+    "aa19380664917386:llama31_8b_layer:int8:decode": 46437120,
+    "aa19380664917386:llama31_8b_layer/paged:bf16:fused": 87954688,
+    "aa19380664917386:qwen25_7b_long:bf16:fused": 517366272,
+    "aa19380664917386:qwen25_7b_long:fp8:decode": 278887936,
+    "aa19380664917386:qwen25_7b_long:int8:decode": 278878976,
+    "aa19380664917386:serving_b64/2L:bf16:decode": 947132160,
+    "aa19380664917386:serving_b64/2L:bf16:fused": 946755840,
+    "aa19380664917386:serving_b64/2L:fp8:decode": 637858560,
+    "aa19380664917386:serving_b64/2L:int8:decode": 637961472,
+    "aa19380664917386:serving_b64/2L/paged:bf16:decode": 946527744,
+    "aa19380664917386:serving_b64/2L/paged:bf16:fused": 946539520,
+    "aa19380664917386:serving_b64/2L/paged:int8:decode": 637942272,
+    "aa19380664917386:serving_b64/4L:bf16:decode": 2179910912,
+    "aa19380664917386:serving_b64/4L:bf16:fused": 2179837184,
+    "aa19380664917386:serving_b64/4L:fp8:decode": 1424805632,
+    "aa19380664917386:serving_b64/4L:int8:decode": 1425400064,
+    "aa19380664917386:serving_b64/4L/paged:bf16:decode": 2178608896,
+    "aa19380664917386:serving_b64/4L/paged:bf16:fused": 2178280448,
+    "aa19380664917386:serving_b64/4L/paged:int8:decode": 1425447936,
+    "aa19380664917386:tiny:bf16:decode": 516096,
 }
 # 32-layer launches: DRAM bytes per algorithmic byte of the 4-layer capture
 NCU_TRAFFIC_RATIO = {
-    "58386bebce908855:serving_b64:bf16:decode": 2179910912 / 2178351104,
-    "58386bebce908855:serving_b64:int8:decode": 1425400064 / 1396178944,
-    "58386bebce908855:serving_b64:fp8:decode": 1424805632 / 1396178944,
-    "58386bebce908855:serving_b64/paged:bf16:decode": 2178608896 / 2178351104,
-    "58386bebce908855:serving_b64/paged:int8:decode": 1425447936 / 1396178944,
-    "58386bebce908855:fastgen_mix:bf16:fused": 867623168 / 856061952,
-    "58386bebce908855:fastgen_mix:int8:decode": 515117824 / 504039424,
-    "58386bebce908855:fastgen_mix:fp8:decode": 514760960 / 504039424,
+    "aa19380664917386:serving_b64:bf16:decode": 2179910912 / 2178351104,
+    "aa19380664917386:serving_b64:int8:decode": 1425400064 / 1396178944,
+    "aa19380664917386:serving_b64:fp8:decode": 1424805632 / 1396178944,
+    "aa19380664917386:serving_b64/paged:bf16:decode": 2178608896 / 2178351104,
+    "aa19380664917386:serving_b64/paged:int8:decode": 1425447936 / 1396178944,
+    "aa19380664917386:fastgen_mix:bf16:fused": 867623168 / 856061952,
+    "aa19380664917386:fastgen_mix:int8:decode": 515117824 / 504039424,
+    "aa19380664917386:fastgen_mix:fp8:decode": 514760960 / 504039424,
 }
 
 

@@ -1702,17 +1702,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t decode_smem_bytes() { return kSmemBytes; }
 
-// One instantiation: its shared-memory limit raised on first use, then the
-// launch.
+// One instantiation: its shared-memory limit raised on first use on the
+// device, then the launch.
 template <int kFmt, bool kPaged, bool kSmallE>
 static cudaError_t launch_one(const cudaLaunchConfig_t& cfg, const DecodeMaps& maps, const DecodeArgs& args) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    const cudaError_t err = cudaFuncSetAttribute(decode_kernel<kFmt, kPaged, kSmallE>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (err != cudaSuccess) return err;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t err = set_smem_limit_once(decode_kernel<kFmt, kPaged, kSmallE>, kSmemBytes, attr_done);
+  if (err != cudaSuccess) return err;
   return cudaLaunchKernelEx(&cfg, decode_kernel<kFmt, kPaged, kSmallE>, maps, args);
 }
 

@@ -3,6 +3,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "lk_internal.h"
 
 namespace lk {
@@ -83,6 +85,22 @@ struct PrefillArgs {
   const int32_t* ids;       // [nb][n] or null
   int32_t n;                // tokens per sequence in k / v / ids (the longest length)
 };
+
+// Raise kernel `fn`'s dynamic shared-memory limit to `bytes` on the current
+// device the first time it launches there: the attribute is per device, so
+// `done` keeps one bit per device ordinal (ordinals past 63 set it every
+// time).  Concurrent first launches may both set it, which is harmless.
+template <typename F>
+inline cudaError_t set_smem_limit_once(F* fn, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const uint64_t bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return err;
+}
 
 size_t decode_smem_bytes();
 cudaError_t launch_decode(const DecodeMaps& maps, const DecodeArgs& args, int ctas, cudaStream_t stream);

@@ -210,12 +210,9 @@ constexpr int kMaskSmem = 256 * 4 + 8192 * 4 + 8192 * 2;
 
 cudaError_t launch_build_masks(const float* alpha, const uint8_t* eligible, int nh, double pct, int align,
                                int exact, uint8_t* masks, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(build_masks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaskSmem);
-    if (err != cudaSuccess) return err;
-    attr_done = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const cudaError_t err = set_smem_limit_once(build_masks_kernel, kMaskSmem, attr_done);
+  if (err != cudaSuccess) return err;
   MaskArgs a{alpha, eligible, masks, nh, pct, align, exact};
   build_masks_kernel<<<1, kThreadsM, kMaskSmem, stream>>>(a);
   return cudaGetLastError();
