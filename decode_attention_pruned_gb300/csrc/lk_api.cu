@@ -407,18 +407,20 @@ uint64_t entry_bytes(const lk_cache_s* cache, const HeadDesc& hd, int N, int cnt
 // Whether lk_step fuses the append into the decode launch.  Fusion removes a
 // kernel boundary (~3.5 us) but puts the append's latency -- the token
 // stage's copy, its fold into the softmax, the cache write -- on one CTA per
-// entry: it pays off when each CTA streams long and meets few entries (the
-// 32K-token layer: 26.6 -> 25.1 us per step; the 128K-token 4-sequence
-// layer: 89.8 -> 88.8 us; the 16-sequence 32-layer FastGen step, 27 entries
-// per CTA: 1.54 -> 1.51 ms) and loses when CTAs stream little (the 0.24 MB
-// layer: 15.0 -> 17.4 us) or meet many entries (the 64-sequence 32-layer
-// step, 108 per CTA: 3.09 -> 3.14 ms).  Lengths are the host's; SPECIAL
-// rows count as 0.
+// entry.  A launch of at most 32 entries advances the lengths right after
+// its work split, so fusing it costs nothing at the end and always pays
+// (the 0.24 MB tiny layer: 12.2 -> 10.0 us per step).  A larger launch
+// counts its CTAs at the end: fusion pays when each CTA streams long and
+// meets few entries (the 16-sequence 32-layer FastGen step, 27 entries per
+// CTA: 1.534 -> 1.524 ms) and loses when CTAs meet many entries (the
+// 64-sequence 32-layer step, 108 per CTA: 2.926 -> 2.993 ms).  Lengths are
+// the host's; SPECIAL rows count as 0.
 bool fuse_step(const lk_cache_s* cache, int layer0, int nlayers) {
   if (cache->lay.kv_format != kKvBf16 || cache->step_mode == LK_STEP_SPLIT) return false;
   if (cache->step_mode == LK_STEP_FUSED) return true;
   const int B = cache->B, H = cache->cv.Hkv;
   const int64_t entries = (int64_t)nlayers * B * H;
+  if (entries <= 32) return true;
   uint64_t bytes = 0;
   for (int l = layer0; l < layer0 + nlayers; ++l)
     for (int b = 0; b < B; ++b)

@@ -175,8 +175,11 @@ def test_step_host_matches_device_path(cuda):
     b.prefill(0, 600)
     k, v = a.history(0)
     q = a.q(0, 601)
-    # the host entry point runs lk_step on the staged copies: the same launch
-    # as the device call on the same values
+    # pinned buffers: the host entry point reads them in place with the append
+    # and decode launches (no bulk copies from host memory), so the device
+    # call runs as those two launches too -- the same launches on the same
+    # values
+    a.cache.set_step_mode(lkb.STEP_SPLIT)
     o_dev = a.cache.step(0, q, k[:, 600].contiguous(), v[:, 600].contiguous())
     pin = lambda t: t.cpu().pin_memory()
     o_host = torch.empty(o_dev.shape, dtype=torch.float32).pin_memory()

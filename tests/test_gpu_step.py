@@ -262,19 +262,26 @@ def test_one_long_head_over_many_ctas(cuda, fused_step):
     case.check_layout(0, 20004)
 
 
-def test_automatic_mode_fuses_long_few_entry_layers_only(cuda):
-    # one launch for the 32K-token layer (8 entries, ~660 KB per CTA); two
-    # for the 0.24 MB tiny layer, for many entries per CTA, and for INT8
+def test_automatic_mode_fuses_small_or_long_few_entry_launches(cuda):
+    # one launch for launches of at most 32 entries (the 32K-token layer, the
+    # 0.24 MB tiny layer) and for larger ones whose CTAs stream long and meet
+    # few entries; two for short CTAs over more than 32 entries, for many
+    # entries per CTA, and for INT8
     big = Case(LLAMA, total=LLAMA.context + 2)
     big.prefill(0, LLAMA.context)
     assert big.cache.step_is_fused(0, 1)
     small = Case(TINY, total=TINY.context + 2)
     small.prefill(0, TINY.context)
-    assert not small.cache.step_is_fused(0, 1)
-    small.cache.set_step_mode(lkb.STEP_FUSED)
     assert small.cache.step_is_fused(0, 1)
+    small.cache.set_step_mode(lkb.STEP_SPLIT)
+    assert not small.cache.step_is_fused(0, 1)
     big.cache.set_step_mode(lkb.STEP_SPLIT)
     assert not big.cache.step_is_fused(0, 1)
+    # 2 layers x 3 sequences x 8 heads = 48 entries, ~64 KB per CTA
+    short = Case(FASTGEN.scaled(num_layers=2, batch=3, context=600, policy_counts=(6, 4, 6)), total=602)
+    for layer in range(2):
+        short.prefill(layer, 600)
+    assert not short.cache.step_is_fused(0, 2)
     # 32 layers x 64 sequences x 8 heads: 108 entries per CTA
     many = Case(SERVING.scaled(context=600), total=602, gen_device=cuda)
     for layer in range(many.w.num_layers):
