@@ -1507,17 +1507,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // ---- merge the warps' (o, m, l) of this segment through shared
-      // memory slots of hs head rows.  bf16 middles with G <= 4: every warp
-      // publishes its own slot (eight slots of four heads) and one barrier
-      // precedes the CTA merge.  Otherwise warps 4..7 hand theirs to warps
-      // 0..3 first (four slots of eight heads), which merge and publish.
+      // memory slots of hs head rows.  G <= 4: every warp publishes its own
+      // slot (eight slots of four heads) and one barrier precedes the CTA
+      // merge.  Otherwise warps 4..7 hand theirs to warps 0..3 first (four
+      // slots of eight heads), which merge and publish.
       float lr0 = l0, lr1 = l1;
 #pragma unroll
       for (int sh = 4; sh < 32; sh <<= 1) {
         lr0 += __shfl_xor_sync(0xffffffffu, lr0, sh);
         lr1 += __shfl_xor_sync(0xffffffffu, lr1, sh);
       }
-      const bool one_pass = !kQ8 && G <= 4;
+      const bool one_pass = G <= 4;
       const int hs = one_pass ? 4 : kMaxGroup;
       auto publish = [&](int slotw) {
         if (2 * tig < hs) {       // this lane's head columns 2tig, 2tig+1 exist in the slot
