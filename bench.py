@@ -74,46 +74,46 @@ MAX_COPIES = 256                    # rotating cache copies at most
 # split partials, each CTA's last box past its range end), applied to the
 # full launch's algorithmic bytes.
 NCU_TRAFFIC = {
-    "aa19380664917386:fastgen_mix/2L:bf16:fused": 445553920,
-    "aa19380664917386:fastgen_mix/2L:fp8:decode": 265454848,
-    "aa19380664917386:fastgen_mix/2L:int8:decode": 265398784,
-    "aa19380664917386:fastgen_mix/4L:bf16:fused": 867623168,
-    "aa19380664917386:fastgen_mix/4L:fp8:decode": 514760960,
-    "aa19380664917386:fastgen_mix/4L:int8:decode": 515117824,
-    "aa19380664917386:llama31_8b_layer:bf16:decode": 87901696,
-    "aa19380664917386:llama31_8b_layer:bf16:fused": 88002560,
-    "aa19380664917386:llama31_8b_layer:fp8:decode": 46434816,
-    "aa19380664917386:llama31_8b_layer:int8:decode": 46437120,
-    "aa19380664917386:llama31_8b_layer/paged:bf16:fused": 87954688,
-    "aa19380664917386:qwen25_7b_long:bf16:fused": 517366272,
-    "aa19380664917386:qwen25_7b_long:fp8:decode": 278887936,
-    "aa19380664917386:qwen25_7b_long:int8:decode": 278878976,
-    "aa19380664917386:serving_b64/2L:bf16:decode": 947132160,
-    "aa19380664917386:serving_b64/2L:bf16:fused": 946755840,
-    "aa19380664917386:serving_b64/2L:fp8:decode": 637858560,
-    "aa19380664917386:serving_b64/2L:int8:decode": 637961472,
-    "aa19380664917386:serving_b64/2L/paged:bf16:decode": 946527744,
-    "aa19380664917386:serving_b64/2L/paged:bf16:fused": 946539520,
-    "aa19380664917386:serving_b64/2L/paged:int8:decode": 637942272,
-    "aa19380664917386:serving_b64/4L:bf16:decode": 2179910912,
-    "aa19380664917386:serving_b64/4L:bf16:fused": 2179837184,
-    "aa19380664917386:serving_b64/4L:fp8:decode": 1424805632,
-    "aa19380664917386:serving_b64/4L:int8:decode": 1425400064,
-    "aa19380664917386:serving_b64/4L/paged:bf16:decode": 2178608896,
-    "aa19380664917386:serving_b64/4L/paged:bf16:fused": 2178280448,
-    "aa19380664917386:serving_b64/4L/paged:int8:decode": 1425447936,
-    "aa19380664917386:tiny:bf16:decode": 516096,
+    "0197f9dad46f17ec:fastgen_mix/2L:bf16:fused": 445716480,
+    "0197f9dad46f17ec:fastgen_mix/2L:fp8:decode": 265465088,
+    "0197f9dad46f17ec:fastgen_mix/2L:int8:decode": 265490688,
+    "0197f9dad46f17ec:fastgen_mix/4L:bf16:fused": 867568128,
+    "0197f9dad46f17ec:fastgen_mix/4L:fp8:decode": 514968832,
+    "0197f9dad46f17ec:fastgen_mix/4L:int8:decode": 515119872,
+    "0197f9dad46f17ec:llama31_8b_layer:bf16:decode": 88016128,
+    "0197f9dad46f17ec:llama31_8b_layer:bf16:fused": 88024320,
+    "0197f9dad46f17ec:llama31_8b_layer:fp8:decode": 46433792,
+    "0197f9dad46f17ec:llama31_8b_layer:int8:decode": 46436864,
+    "0197f9dad46f17ec:llama31_8b_layer/paged:bf16:fused": 87989504,
+    "0197f9dad46f17ec:qwen25_7b_long:bf16:fused": 517321216,
+    "0197f9dad46f17ec:qwen25_7b_long:fp8:decode": 278952960,
+    "0197f9dad46f17ec:qwen25_7b_long:int8:decode": 278957056,
+    "0197f9dad46f17ec:serving_b64/2L:bf16:decode": 947085056,
+    "0197f9dad46f17ec:serving_b64/2L:bf16:fused": 947103232,
+    "0197f9dad46f17ec:serving_b64/2L:fp8:decode": 637853952,
+    "0197f9dad46f17ec:serving_b64/2L:int8:decode": 637905408,
+    "0197f9dad46f17ec:serving_b64/2L/paged:bf16:decode": 946146048,
+    "0197f9dad46f17ec:serving_b64/2L/paged:bf16:fused": 946523904,
+    "0197f9dad46f17ec:serving_b64/2L/paged:int8:decode": 637677056,
+    "0197f9dad46f17ec:serving_b64/4L:bf16:decode": 2179566080,
+    "0197f9dad46f17ec:serving_b64/4L:bf16:fused": 2179599872,
+    "0197f9dad46f17ec:serving_b64/4L:fp8:decode": 1425171200,
+    "0197f9dad46f17ec:serving_b64/4L:int8:decode": 1425136640,
+    "0197f9dad46f17ec:serving_b64/4L/paged:bf16:decode": 2178592000,
+    "0197f9dad46f17ec:serving_b64/4L/paged:bf16:fused": 2178788608,
+    "0197f9dad46f17ec:serving_b64/4L/paged:int8:decode": 1425398528,
+    "0197f9dad46f17ec:tiny:bf16:fused": 529920,
 }
 # 32-layer launches: DRAM bytes per algorithmic byte of the 4-layer capture
 NCU_TRAFFIC_RATIO = {
-    "aa19380664917386:serving_b64:bf16:decode": 2179910912 / 2178351104,
-    "aa19380664917386:serving_b64:int8:decode": 1425400064 / 1396178944,
-    "aa19380664917386:serving_b64:fp8:decode": 1424805632 / 1396178944,
-    "aa19380664917386:serving_b64/paged:bf16:decode": 2178608896 / 2178351104,
-    "aa19380664917386:serving_b64/paged:int8:decode": 1425447936 / 1396178944,
-    "aa19380664917386:fastgen_mix:bf16:fused": 867623168 / 856061952,
-    "aa19380664917386:fastgen_mix:int8:decode": 515117824 / 504039424,
-    "aa19380664917386:fastgen_mix:fp8:decode": 514760960 / 504039424,
+    "0197f9dad46f17ec:serving_b64:bf16:decode": 2179566080 / 2178351104,
+    "0197f9dad46f17ec:serving_b64:int8:decode": 1425136640 / 1396178944,
+    "0197f9dad46f17ec:serving_b64:fp8:decode": 1425171200 / 1396178944,
+    "0197f9dad46f17ec:serving_b64/paged:bf16:decode": 2178592000 / 2178351104,
+    "0197f9dad46f17ec:serving_b64/paged:int8:decode": 1425398528 / 1396178944,
+    "0197f9dad46f17ec:fastgen_mix:bf16:fused": 867568128 / 856061952,
+    "0197f9dad46f17ec:fastgen_mix:int8:decode": 515119872 / 504039424,
+    "0197f9dad46f17ec:fastgen_mix:fp8:decode": 514968832 / 504039424,
 }
 
 
