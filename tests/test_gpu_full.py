@@ -148,6 +148,38 @@ def test_full_fastgen_mix_all_layers(cuda):
     _check_all_layers(case, w.context, pick, fused=True)
 
 
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_full_fastgen_mix_quantized_all_layers(cuda, fmt):
+    """The 32-layer FastGen step with INT8 / FP8 middles (append + decode
+    launches, as the bench runs it).  Its FULL heads keep 32 or 64
+    channels (stages of three 21 or 25 KB sealed blocks): each layer checks
+    one FULL head of every width it has, one LOCAL and one SPECIAL head
+    against the oracle."""
+    from decode_attention_pruned_gb300 import binding as lkb
+    w = S.WORKLOADS[4]
+    case = Case(w, total=w.context, gen_device=cuda, kv_format=lkb.KV_INT8 if fmt == "int8" else lkb.KV_FP8)
+    rng = np.random.default_rng(19)
+    widths_seen = set()
+
+    def pick(layer):
+        pairs = set()
+        by_width = {}
+        for h in np.nonzero(case.policies[layer] == S.POLICY_FULL)[0]:
+            by_width.setdefault(int(case.masks[layer, h].sum()), int(h))
+        widths_seen.update(by_width)
+        for h in by_width.values():
+            pairs.add((int(rng.integers(w.batch)), h))
+        for pol in (S.POLICY_LOCAL, S.POLICY_SPECIAL):
+            hs = np.nonzero(case.policies[layer] == pol)[0]
+            if len(hs):
+                pairs.add((int(rng.integers(w.batch)), int(hs[0])))
+        pairs = sorted(pairs)
+        return pairs, pairs[:2]
+
+    _check_all_layers(case, w.context, pick, fused=False)
+    assert widths_seen == {32, 64}
+
+
 def test_full_qwen25_7b_long_int8(cuda):
     from decode_attention_pruned_gb300 import binding as lkb
     w = S.WORKLOADS[3]
