@@ -85,3 +85,27 @@ def test_oracle_rate_counts_layer_calls():
     assert units == 1
     assert value == pytest.approx(units / el / (w.batch * w.num_kv_heads))
     assert bench.job_throughput(10, w.num_layers, 1, 2.0) == pytest.approx(10 * w.num_layers / 2.0)
+
+
+def test_traffic_table_is_current_and_self_consistent():
+    """The DRAM traffic the bench reports comes from captures of the kernel
+    sources as they stand (every key carries their hash), and each 32-layer
+    ratio is the matching 4-layer capture's traffic over a whole number of
+    algorithmic bytes, just above one."""
+    from decode_attention_pruned_gb300 import synth as S
+    h = bench._decode_source_hash()
+    keys = list(bench.NCU_TRAFFIC) + list(bench.NCU_TRAFFIC_RATIO)
+    assert keys and all(k.split(":")[0] == h for k in keys), "kernel sources changed since the captures"
+    for k in keys:
+        _, wl, kv, mode = k.split(":")
+        assert wl.split("/")[0] in S.WORKLOAD_BY_NAME
+        assert kv in ("bf16", "int8", "fp8") and mode in ("fused", "decode")
+    for k, ratio in bench.NCU_TRAFFIC_RATIO.items():
+        _, wl, kv, mode = k.split(":")
+        name, *rest = wl.split("/")
+        assert S.WORKLOAD_BY_NAME[name].num_layers > 4
+        cut = ":".join([h, "/".join([name, "4L", *rest]), kv, mode])
+        assert cut in bench.NCU_TRAFFIC, cut
+        alg4 = bench.NCU_TRAFFIC[cut] / ratio
+        assert abs(alg4 - round(alg4)) < 1e-3
+        assert 1.0 <= ratio < 1.05
