@@ -1344,7 +1344,11 @@ lk_status lk_check(lk_cache cache, void* stream) {
   err = cudaMemcpy(&status, &cache->cv.hdr->status, 4, cudaMemcpyDeviceToHost);
   if (err != cudaSuccess) return cuda_fail(err, "lk_check: status read");
   if (status == 0) return LK_OK;
-  err = cudaMemset(&cache->cv.hdr->status, 0, 4);
+  // clear on the caller's stream and wait for it: a plain cudaMemset would
+  // run on the legacy stream, which non-blocking streams do not wait for, so
+  // a bit set by the caller's next launch could be cleared after the fact
+  err = cudaMemsetAsync(&cache->cv.hdr->status, 0, 4, static_cast<cudaStream_t>(stream));
+  if (err == cudaSuccess) err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "lk_check: status clear");
   if (status & kStatusTimeout) return fail(LK_ERR_TIMEOUT, "a device-side wait ran out (status 0x%x)", status);
   if (status & kStatusCapacity)

@@ -427,7 +427,9 @@ lk_status lk_set_decode_ctas(lk_cache cache, int32_t ctas);
  * to land keeps its 1 s bound whatever this is.  Errors: LK_ERR_ARG. */
 lk_status lk_set_wait_limit(lk_cache cache, uint64_t ns);
 
-/* Synchronise `stream`, read and clear the device status word.  Returns
+/* Synchronise `stream`, read the device status word and, when a bit is set,
+ * clear it on `stream` and synchronise again (the clear has landed when the
+ * call returns).  Returns
  * LK_ERR_TIMEOUT, LK_ERR_CAPACITY or LK_ERR_ARG (bad token id) for a set
  * bit, LK_ERR_CUDA for a pending CUDA error, else LK_OK. */
 lk_status lk_check(lk_cache cache, void* stream);
