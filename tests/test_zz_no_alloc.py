@@ -78,3 +78,23 @@ def test_static_scratch_rejects_caches_beyond_its_size(cuda):
     with pytest.raises(lkb.LeankError) as e:
         case.cache.decode_static(0, q, o)
     assert e.value.status == lkb.LK_ERR_CAPACITY
+
+
+@pytest.mark.parametrize("kv,paged", [(lkb.KV_BF16, True), (lkb.KV_INT8, False), (lkb.KV_FP8, True)],
+                         ids=["bf16-paged", "int8", "fp8-paged"])
+def test_static_scratch_on_paged_and_quantized_caches(cuda, kv, paged):
+    # the same launch as lk_decode_attn over the other cache layouts: region B
+    # through the page table, and sealed INT8 / FP8 blocks beside a bf16 tail
+    w = S.WORKLOADS[1].scaled(context=1500, batch=2)
+    masks = S.masks_with_counts(w, [32, 0, 64, 128, 96, 32, 64, 0])
+    case = Case(w, total=1501, masks=masks, kv_format=kv, middle_tokens=2 * 1501 if paged else None)
+    case.prefill(0, 1500)
+    case.append(0, 1500)
+    q = case.q(0, 1501, step=1500)
+    o_ws = case.cache.decode(0, q)
+    o_st = torch.full_like(o_ws, float("nan"))
+    case.cache.decode_static(0, q, o_st)
+    case.cache.check()
+    assert torch.equal(o_st, o_ws)
+    ref = case.expected(0, q, 1501)
+    assert float(np.abs(o_st.double().cpu().numpy() - ref).max()) <= DECODE_TOL
