@@ -210,6 +210,30 @@ def test_step_host_pageable_buffers_are_copied(cuda):
     assert torch.equal(a.cache.buffer, b.cache.buffer)
 
 
+def test_step_host_packed_matches_device_path(cuda):
+    # one pinned block q | k | v, read in place by the append and decode
+    # launches (o written into the mapped host buffer): the device call run
+    # as those two launches gives identical o and cache bytes
+    w = SERVING.scaled(num_layers=1, batch=2, context=600)
+    a = Case(w, total=601)
+    b = Case(w, total=601)
+    for case in (a, b):
+        case.prefill(0, 600)
+    a.cache.set_step_mode(lkb.STEP_SPLIT)
+    k, v = a.history(0)
+    q = a.q(0, 601)
+    kn, vn = k[:, 600].contiguous(), v[:, 600].contiguous()
+    o_dev = a.cache.step(0, q, kn, vn)
+    blk = torch.cat([t.cpu().contiguous().view(torch.uint8).reshape(-1) for t in (q, kn, vn)]).pin_memory()
+    o_host = torch.full(o_dev.shape, float("nan"), dtype=torch.float32).pin_memory()
+    b.cache.step_host_packed(0, blk, False, o_host)
+    torch.cuda.synchronize()
+    b.cache.check()
+    assert torch.equal(o_host, o_dev.cpu())
+    assert float(np.abs(o_host.double().numpy() - a.expected(0, q, 601)).max()) <= DECODE_TOL
+    assert torch.equal(a.cache.buffer, b.cache.buffer)
+
+
 def test_capacity_is_enforced(cuda):
     w = TINY
     case = Case(w, total=10, capacity=10)
