@@ -176,3 +176,70 @@ def test_int8_cache_bytes(lib):
     with pytest.raises(lkb.LeankError) as e:
         plan.cache_bytes(B, cap, kv_format=7)
     assert e.value.status == lkb.LK_ERR_ARG
+
+
+_LAYOUT_PROBE = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "leank.h"
+#define SIZE(T) printf(#T " %zu\n", sizeof(T));
+#define OFF(T, m) printf(#T "." #m " %zu\n", offsetof(T, m));
+#define VAL(e) printf(#e " %d\n", (int)(e));
+int main(void) {
+  SIZE(lk_plan_desc) SIZE(lk_region_info) SIZE(lk_cache_options)
+  OFF(lk_plan_desc, num_layers) OFF(lk_plan_desc, num_q_heads) OFF(lk_plan_desc, num_kv_heads)
+  OFF(lk_plan_desc, head_dim) OFF(lk_plan_desc, sink) OFF(lk_plan_desc, local)
+  OFF(lk_plan_desc, local_only_window) OFF(lk_plan_desc, vocab) OFF(lk_plan_desc, special_capacity)
+  OFF(lk_region_info, policy) OFF(lk_region_info, n_kept) OFF(lk_region_info, rows_a)
+  OFF(lk_region_info, rows_b) OFF(lk_region_info, k_a_offset) OFF(lk_region_info, v_a_offset)
+  OFF(lk_region_info, k_b_offset) OFF(lk_region_info, v_b_offset) OFF(lk_region_info, page_rows)
+  OFF(lk_region_info, max_pages) OFF(lk_region_info, page_table_offset) OFF(lk_region_info, kv_format)
+  OFF(lk_region_info, sealed_blocks)
+  OFF(lk_cache_options, middle_tokens) OFF(lk_cache_options, kv_format) OFF(lk_cache_options, reserved)
+  VAL(LK_OK) VAL(LK_ERR_ARG) VAL(LK_ERR_ALIGN) VAL(LK_ERR_CAPACITY) VAL(LK_ERR_STATE) VAL(LK_ERR_CUDA)
+  VAL(LK_ERR_TIMEOUT) VAL(LK_ERR_UNSUPPORTED)
+  VAL(LK_POLICY_FULL) VAL(LK_POLICY_LOCAL) VAL(LK_POLICY_SPECIAL)
+  VAL(LK_KV_BF16) VAL(LK_KV_INT8) VAL(LK_KV_FP8)
+  VAL(LK_STEP_AUTO) VAL(LK_STEP_FUSED) VAL(LK_STEP_SPLIT)
+  return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_cxx_and_matches_the_binding(tmp_path):
+    """The public header stands alone in C99 and C++17 with every warning an
+    error, and the binding's structures and constants have the header's
+    sizes, field offsets and values (a mismatch would pass garbage through
+    ctypes without an error)."""
+    import shutil
+    import subprocess
+    gcc, gxx = shutil.which("gcc"), shutil.which("g++")
+    if gcc is None or gxx is None:
+        pytest.skip("no host C / C++ compiler")
+    inc = os.path.join(ROOT, "include")
+    src = tmp_path / "layout.c"
+    src.write_text(_LAYOUT_PROBE)
+    exe = tmp_path / "layout"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src), "-o", str(exe)],
+                   check=True)
+    cxx = tmp_path / "header.cc"
+    cxx.write_text('#include "leank.h"\nint main() { return LK_OK; }\n')
+    subprocess.run([gxx, "-std=c++17", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only", "-I", inc,
+                    str(cxx)], check=True)
+    got = dict(line.rsplit(" ", 1) for line in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                              text=True).stdout.splitlines())
+    got = {k: int(v) for k, v in got.items()}
+    structs = {"lk_plan_desc": lkb.PlanDesc, "lk_region_info": lkb.RegionInfo,
+               "lk_cache_options": lkb.CacheOptions}
+    for cname, ct in structs.items():
+        assert ctypes.sizeof(ct) == got[cname], cname
+        for field, _ in ct._fields_:
+            assert getattr(ct, field).offset == got[f"{cname}.{field}"], (cname, field)
+    assert len([k for k in got if "." in k]) == sum(len(ct._fields_) for ct in structs.values())
+    for i, name in enumerate(lkb.STATUS_NAMES):
+        assert got[name] == i
+    assert (got["LK_POLICY_FULL"], got["LK_POLICY_LOCAL"], got["LK_POLICY_SPECIAL"]) == \
+        (lkb.POLICY_FULL, lkb.POLICY_LOCAL, lkb.POLICY_SPECIAL)
+    assert (got["LK_KV_BF16"], got["LK_KV_INT8"], got["LK_KV_FP8"]) == (lkb.KV_BF16, lkb.KV_INT8, lkb.KV_FP8)
+    assert (got["LK_STEP_AUTO"], got["LK_STEP_FUSED"], got["LK_STEP_SPLIT"]) == \
+        (lkb.STEP_AUTO, lkb.STEP_FUSED, lkb.STEP_SPLIT)
